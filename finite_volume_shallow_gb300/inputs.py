@@ -1,0 +1,203 @@
+"""Seeded synthetic inputs for the shallow-water workloads.
+
+This module only draws and lays out initial data (bathymetry ``H``, depth
+``h``, discharge ``qx, qy`` and pollutant mass ``hC``); it holds none of the
+numerical scheme's arithmetic, so the CUDA path and the CPU oracle can both be
+fed from it without sharing any code of the method.
+
+Conventions (An MPI-CUDA implementation of an improved Roe method for
+two-layer shallow water systems, Sec. 2.1, eq. (1)): ``H`` is the depth of the
+bottom measured downward from a fixed reference level, so the bottom elevation
+is ``z_b = -H`` and the free surface is ``h - H``.  Cell ``(i, j)`` of an
+``nx x ny`` grid is stored at flat index ``j * nx + i`` with its centre at
+``((i + 1/2) dx, (j + 1/2) dy)``.
+
+Workloads (the pages give no datasets; these stand in for their "internal dam
+break" and "realistic pollutant problem"):
+
+* ``dam128``   128 x 128, dx = 1 m, flat bottom, circular dam break of radius
+  20 m about (64, 64): h = 2 inside, 1 outside, q = 0, C = 1 inside, 0 outside.
+* ``hills2048`` 2048 x 2048, dx = 10 m, 8 Gaussian hills under a 5 m surface,
+  3 surface bumps of 0.5 m, q = 0, C uniform per 16 x 16 block.
+* ``pulses8192`` 8192 x 8192, dx = 10 m, 128 hills (8 per 2048^2 of area),
+  16 surface pulses of 0.5 m, random velocities |u| <= 0.1 m/s, C per block.
+
+Every random draw comes from ``numpy.random.Generator(PCG64(seed))`` in the
+order documented in each function, so a workload is a pure function of its
+name, size and seed.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+G_DEFAULT = 9.81
+CFL_DEFAULT = 0.9
+
+# workload name -> (nx, ny, dx, default steps, seed, default precision)
+WORKLOADS = {
+    "dam128": dict(nx=128, ny=128, dx=1.0, steps=100, seed=1001, precision=64),
+    "hills2048": dict(nx=2048, ny=2048, dx=10.0, steps=1000, seed=1002, precision=32),
+    "pulses8192": dict(nx=8192, ny=8192, dx=10.0, steps=200, seed=1003, precision=32),
+}
+
+
+def _gaussian_sum(nx, ny, dx, dy, amp, sigma, cx, cy, cutoff=8.0):
+    """Sum of isotropic Gaussians ``amp * exp(-r^2 / (2 sigma^2))`` sampled at
+    cell centres.  Each Gaussian is evaluated on the window within
+    ``cutoff * sigma`` of its centre (exp(-32) ~ 1e-14 relative is dropped)
+    as an outer product of its separable x and y factors."""
+    out = np.zeros((ny, nx), dtype=np.float64)
+    xc = (np.arange(nx) + 0.5) * dx
+    yc = (np.arange(ny) + 0.5) * dy
+    for a, s, x0, y0 in zip(amp, sigma, cx, cy):
+        i0 = max(int(np.floor((x0 - cutoff * s) / dx)), 0)
+        i1 = min(int(np.ceil((x0 + cutoff * s) / dx)) + 1, nx)
+        j0 = max(int(np.floor((y0 - cutoff * s) / dy)), 0)
+        j1 = min(int(np.ceil((y0 + cutoff * s) / dy)) + 1, ny)
+        if i0 >= i1 or j0 >= j1:
+            continue
+        gx = np.exp(-((xc[i0:i1] - x0) ** 2) / (2.0 * s * s))
+        gy = np.exp(-((yc[j0:j1] - y0) ** 2) / (2.0 * s * s))
+        out[j0:j1, i0:i1] += a * np.outer(gy, gx)
+    return out
+
+
+def _hills(rng, n, lx, ly, amp_lo, amp_hi):
+    """Draw ``n`` Gaussian features: amplitudes U[amp_lo, amp_hi], widths
+    sigma U[50, 300] m, centres U[0, lx] x U[0, ly]; drawn in that order."""
+    amp = rng.uniform(amp_lo, amp_hi, n)
+    sigma = rng.uniform(50.0, 300.0, n)
+    cx = rng.uniform(0.0, lx, n)
+    cy = rng.uniform(0.0, ly, n)
+    return amp, sigma, cx, cy
+
+
+def _block_concentration(rng, nx, ny, block=16):
+    """C ~ U[0, 1], constant on each ``block x block`` tile of cells."""
+    bx = (nx + block - 1) // block
+    by = (ny + block - 1) // block
+    cb = rng.uniform(0.0, 1.0, (by, bx))
+    return np.repeat(np.repeat(cb, block, axis=0), block, axis=1)[:ny, :nx]
+
+
+def _as_fields(H, h, qx, qy, hC, **meta):
+    d = dict(meta)
+    d["H"] = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    d["h"] = np.ascontiguousarray(h, dtype=np.float64).reshape(-1)
+    d["qx"] = np.ascontiguousarray(qx, dtype=np.float64).reshape(-1)
+    d["qy"] = np.ascontiguousarray(qy, dtype=np.float64).reshape(-1)
+    d["hC"] = np.ascontiguousarray(hC, dtype=np.float64).reshape(-1)
+    return d
+
+
+def circular_dam(nx=128, ny=128, dx=1.0, dy=None, radius=20.0, centre=None,
+                 h_in=2.0, h_out=1.0, c_in=1.0, c_out=0.0):
+    """Circular dam break on a flat bottom (H = 0), water at rest."""
+    dy = dx if dy is None else dy
+    if centre is None:
+        centre = (0.5 * nx * dx, 0.5 * ny * dy)
+    x = (np.arange(nx) + 0.5) * dx
+    y = (np.arange(ny) + 0.5) * dy
+    X, Y = np.meshgrid(x, y)
+    inside = (X - centre[0]) ** 2 + (Y - centre[1]) ** 2 < radius * radius
+    h = np.where(inside, h_in, h_out)
+    C = np.where(inside, c_in, c_out)
+    z = np.zeros_like(h)
+    return _as_fields(z, h, z, z, h * C, nx=nx, ny=ny, dx=dx, dy=dy)
+
+
+def hills(nx, ny, dx=10.0, dy=None, seed=1002, n_hills=8, n_bumps=3,
+          eta0=5.0, bump_amp=0.5, umax=0.0, lake_at_rest=False):
+    """Gaussian-hill bathymetry under a flat surface ``eta0`` plus Gaussian
+    surface bumps; pollutant concentration uniform per 16 x 16 block.
+
+    Draw order: hills (amp U[0.2, 0.8], sigma, cx, cy), bumps (amp fixed at
+    ``bump_amp``; sigma, cx, cy drawn with amplitudes drawn and discarded so the
+    stream layout matches the hills), block concentrations, then (only when
+    ``umax > 0``) per-cell speed U[0, umax] and direction U[0, 2 pi) as two
+    full arrays.  ``lake_at_rest`` drops the bumps and velocities (surface
+    exactly ``eta0``) while keeping the same draws.
+    """
+    dy = dx if dy is None else dy
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lx, ly = nx * dx, ny * dy
+    a, s, cx, cy = _hills(rng, n_hills, lx, ly, 0.2, 0.8)
+    zb = _gaussian_sum(nx, ny, dx, dy, a, s, cx, cy)
+    _, bs, bx, by = _hills(rng, n_bumps, lx, ly, 0.0, 1.0)
+    bumps = _gaussian_sum(nx, ny, dx, dy, np.full(n_bumps, bump_amp), bs, bx, by)
+    C = _block_concentration(rng, nx, ny)
+    if umax > 0.0:
+        speed = rng.uniform(0.0, umax, (ny, nx))
+        theta = rng.uniform(0.0, 2.0 * np.pi, (ny, nx))
+    H = -zb
+    if lake_at_rest:
+        h = eta0 + H
+        qx = np.zeros_like(h)
+        qy = np.zeros_like(h)
+    else:
+        h = eta0 + bumps + H
+        if umax > 0.0:
+            qx = h * speed * np.cos(theta)
+            qy = h * speed * np.sin(theta)
+        else:
+            qx = np.zeros_like(h)
+            qy = np.zeros_like(h)
+    if np.min(h) < 0.5:
+        raise ValueError("generator produced a depth below 0.5 m")
+    return _as_fields(H, h, qx, qy, h * C, nx=nx, ny=ny, dx=dx, dy=dy)
+
+
+def dam_break_1d(nx, ny=4, length=2000.0, x_dam=1000.0, h_left=2.0, h_right=1.0):
+    """Wet-bed dam break along x on a flat bottom: h = h_left for x < x_dam,
+    h_right beyond, water at rest, C = 1 on the left and 0 on the right;
+    square cells (dy = dx)."""
+    dx = length / nx
+    x = (np.arange(nx) + 0.5) * dx
+    h1 = np.where(x < x_dam, h_left, h_right)
+    h = np.tile(h1, (ny, 1))
+    C = np.tile(np.where(x < x_dam, 1.0, 0.0), (ny, 1))
+    z = np.zeros_like(h)
+    return _as_fields(z, h, z, z, h * C, nx=nx, ny=ny, dx=dx, dy=dx)
+
+
+def make_workload(name, nx=None, ny=None, lake_at_rest=False):
+    """Initial data of a named workload, optionally at a reduced size.
+
+    Returns a dict with ``nx, ny, dx, dy, g, cfl, steps, precision`` and the
+    fp64 flat arrays ``H, h, qx, qy, hC`` (length ``nx * ny``).  Reduced sizes
+    keep the recipe and the grid spacing; the hill count of ``pulses8192``
+    scales with the domain area (8 per 2048 x 2048 cells, at least 8).
+    """
+    if name not in WORKLOADS:
+        raise KeyError(f"unknown workload {name!r}; known: {sorted(WORKLOADS)}")
+    w = WORKLOADS[name]
+    nx = w["nx"] if nx is None else int(nx)
+    ny = w["ny"] if ny is None else int(ny)
+    dx = w["dx"]
+    if name == "dam128":
+        d = circular_dam(nx, ny, dx, radius=20.0 * min(nx, ny) / 128.0)
+    elif name == "hills2048":
+        d = hills(nx, ny, dx, seed=w["seed"], n_hills=8, n_bumps=3,
+                  lake_at_rest=lake_at_rest)
+    else:
+        n_h = max(8, int(round(8 * nx * ny / (2048 * 2048))))
+        d = hills(nx, ny, dx, seed=w["seed"], n_hills=n_h, n_bumps=16,
+                  umax=0.1, lake_at_rest=lake_at_rest)
+    d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"],
+             precision=w["precision"], name=name)
+    return d
+
+
+def fields_of(d, dtype=np.float64):
+    """The four conserved fields (h, qx, qy, hC) of a workload dict, cast."""
+    return [np.ascontiguousarray(d[k], dtype=dtype) for k in ("h", "qx", "qy", "hC")]
+
+
+def rounded(d, dtype):
+    """A copy of a workload whose fields and bathymetry are rounded to
+    ``dtype`` and widened back to fp64, so a reduced-precision run and an fp64
+    run start from the same values."""
+    out = dict(d)
+    for k in ("H", "h", "qx", "qy", "hC"):
+        out[k] = d[k].astype(dtype).astype(np.float64)
+    return out

@@ -1,0 +1,95 @@
+/*
+ * swe_oracle.h -- plain fp64 CPU oracle of the IR-Roe finite-volume step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this code; only the tests, the package smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, header or constant with the CUDA
+ * path.
+ *
+ * What it computes: An MPI-CUDA implementation of an improved Roe method for
+ * two-layer shallow water systems (de la Asuncion, Mantas, Castro,
+ * Fernandez-Nieto), Sec. 2.2: the update of eq. (4) with the numerical flux
+ * of steps 1-4 and the time step of the CFL condition eq. (5), restricted to
+ * one layer, plus a passive pollutant transported as in A multi-GPU
+ * shallow-water simulation with transport of contaminants (Vinas et al.),
+ * abstract.  The mesh is a generic polygon mesh: every cell lists its edges
+ * (neighbour, outward unit normal, length); a neighbour of -1 is a reflective
+ * wall.  Everything is fp64 and single threaded.
+ */
+#ifndef SWE_ORACLE_H
+#define SWE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Polygon mesh in compressed per-cell edge lists.  Cell i owns the edge
+ * entries e in [edge_start[i], edge_start[i+1]); nbr[e] is the neighbour
+ * cell j (or -1 for a wall), (eta_x[e], eta_y[e]) the unit normal of the
+ * common edge pointing from i towards j, and len[e] its length |Gamma_ij|.
+ * area[i] is |V_i|.  An interior edge appears twice, once from each side. */
+typedef struct {
+  int64_t n_cells;
+  const double *area;
+  const int64_t *edge_start;
+  const int64_t *nbr;
+  const double *eta_x;
+  const double *eta_y;
+  const double *len;
+} om_mesh;
+
+/* status codes */
+#define OM_OK 0
+#define OM_ERR_DEPTH (-4)     /* a depth h <= 0 appeared */
+#define OM_ERR_NONFINITE (-5) /* a non-finite value appeared */
+#define OM_ERR_ARG (-1)
+
+/* Number of edge entries of the nx x ny Cartesian grid as a polygon mesh. */
+int64_t om_grid_edges(int64_t nx, int64_t ny);
+
+/* Fill the polygon-mesh arrays of the nx x ny Cartesian grid with spacing
+ * (dx, dy).  Cell (i, j) is index j*nx + i; its edges are listed East,
+ * North, West, South. */
+void om_grid_mesh(int64_t nx, int64_t ny, double dx, double dy, double *area,
+                  int64_t *edge_start, int64_t *nbr, double *eta_x,
+                  double *eta_y, double *len);
+
+/* Numerical flux F_ij^- of eq. (4) (one layer + pollutant) for the state
+ * Wi = (h, qx, qy, hC) of cell i, Wj of cell j, bathymetry Hi, Hj and unit
+ * normal (ex, ey) from i to j.  Writes the Cartesian flux F[4] and the
+ * spectral radius ||D_ij||_inf of the Roe matrix. */
+void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
+              double ex, double ey, double g, double *F, double *Dinf);
+
+/* Mirror ghost state of a reflective wall with outward normal (ex, ey). */
+void om_wall_ghost1(const double *Wi, double ex, double ey, double *Wg);
+
+/* Time step of eq. (5): min_i 2 cfl |V_i| / sum_j |Gamma_ij| ||D_ij||_inf.
+ * W holds the four fields h, qx, qy, hC as separate arrays (W[0..3]). */
+double om_dt1(const om_mesh *m, const double *const *W, const double *H,
+              double g, double cfl);
+
+/* One explicit step of eq. (4) with the given dt, in place.  work must hold
+ * 4 * n_cells doubles.  Returns OM_OK or an error code. */
+int om_update1(const om_mesh *m, double *const *W, const double *H, double g,
+               double dt, double *work);
+
+/* The updated state after one step of size dt, at the listed cells only
+ * (out[k*n_sel + s] is field k of cell cells[s]); W is left unchanged. */
+void om_update1_at(const om_mesh *m, const double *const *W, const double *H,
+                   double g, double dt, const int64_t *cells, int64_t n_sel,
+                   double *out);
+
+/* nsteps steps: dt from eq. (5) on the current state, then eq. (4).  The dt
+ * of each step is written to dts (may be NULL).  Returns OM_OK or the error
+ * of the first failing step; *steps_done counts completed steps. */
+int om_run1(const om_mesh *m, double *const *W, const double *H, double g,
+            double cfl, int64_t nsteps, double *dts, double *work,
+            int64_t *steps_done);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,78 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU,
+in a temporary directory), compiles it, and runs the pin suite against that
+copy; the suite must fail.  The committed oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(ROOT, "oracle", "swe_oracle.c")
+HDR = os.path.join(ROOT, "oracle", "swe_oracle.h")
+
+MUTANTS = {
+    # bathymetry source with the wrong sign
+    "source_sign": ("- g * hbar * (Hj - Hi)", "+ g * hbar * (Hj - Hi)"),
+    # source term dropped
+    "source_dropped": ("- g * hbar * (Hj - Hi)", "- 0.0 * (Hj - Hi)"),
+    # arithmetic instead of sqrt(h)-weighted velocity average
+    "plain_average": ("double ux = (si * uxi + sj * uxj) / (si + sj);",
+                      "double ux = 0.5 * (uxi + uxj);"),
+    # P^+ instead of P^-
+    "p_plus": ("0.5 * (1.0 - sgn(lam[0])), 0.5 * (1.0 - sgn(lam[1]))",
+               "0.5 * (1.0 + sgn(lam[0])), 0.5 * (1.0 + sgn(lam[1]))"),
+    # tangential velocity upwinded from the wrong side
+    "tangential_downwind": ("double ut = (phi[0] > 0.0) ? qti / hi : qtj / hj;",
+                            "double ut = (phi[0] > 0.0) ? qtj / hj : qti / hi;"),
+    # pollutant upwinded from the wrong side
+    "pollutant_downwind": ("double Cs = (phi[0] > 0.0) ? Wi[3] / hi : Wj[3] / hj;",
+                           "double Cs = (phi[0] > 0.0) ? Wj[3] / hj : Wi[3] / hi;"),
+    # back-rotation with a transposed operator
+    "back_rotation": ("F[1] = phi[1] * ex - phit * ey;", "F[1] = phi[1] * ex + phit * ey;"),
+    # hydrostatic pressure without its factor 1/2
+    "pressure_half": ("qn * qn / h + 0.5 * g * h * h", "qn * qn / h + g * h * h"),
+    # CFL without the factor 2 of eq. (5)
+    "cfl_factor": ("double dti = 2.0 * cfl * m->area[i] / s;",
+                   "double dti = cfl * m->area[i] / s;"),
+    # edge lengths of the two directions swapped
+    "edge_length": ("len[e] = (k == 0 || k == 2) ? dy : dx;",
+                    "len[e] = (k == 0 || k == 2) ? dx : dy;"),
+    # wrong neighbour index (North points South)
+    "neighbour_index": ("static const int dj[4] = {0, 1, 0, -1};",
+                        "static const int dj[4] = {0, -1, 0, -1};"),
+    # update with the wrong sign
+    "update_sign": ("work[c * N + i] = W[c][i] - dt / m->area[i]",
+                    "work[c * N + i] = W[c][i] + dt / m->area[i]"),
+    # wall ghost that does not reflect the normal discharge
+    "wall_no_reflect": ("Wg[1] = Wi[1] - 2.0 * qn * ex;", "Wg[1] = Wi[1];"),
+}
+
+
+@pytest.fixture(scope="module")
+def workdir(tmp_path_factory):
+    return tmp_path_factory.mktemp("mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, workdir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site of {name} not found exactly once"
+    d = workdir / name
+    d.mkdir()
+    (d / "swe_oracle.c").write_text(src.replace(old, new))
+    shutil.copy(HDR, d / "swe_oracle.h")
+    so = d / "liboracle.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), str(d / "swe_oracle.c"), "-lm"], check=True)
+    env = dict(os.environ, SWE_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -79,6 +79,13 @@ def lib():
         _lib.om_run1.restype = C.c_int
         _lib.om_run1.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, i64, vp, vp,
                                  C.POINTER(C.c_int64)]
+        _lib.om_grid_dt1.restype = d
+        _lib.om_grid_dt1.argtypes = [i64, i64, d, d, vp, vp, d, d]
+        _lib.om_grid_update1.restype = C.c_int
+        _lib.om_grid_update1.argtypes = [i64, i64, d, d, vp, vp, d, d, vp]
+        _lib.om_grid_run1.restype = C.c_int
+        _lib.om_grid_run1.argtypes = [i64, i64, d, d, vp, vp, d, d, i64, vp, vp,
+                                      C.POINTER(C.c_int64)]
     return _lib
 
 
@@ -198,6 +205,38 @@ def run1(mesh: Mesh, H, W, g, cfl, nsteps):
     st = lib().om_run1(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(cfl),
                        int(nsteps), _ptr(dts), _ptr(work), C.byref(done))
     return Wf, dts[: done.value], int(st), int(done.value)
+
+
+def grid_dt1(nx, ny, dx, dy, H, W, g, cfl) -> float:
+    """eq. (5) on the implicit nx x ny grid (no mesh arrays)."""
+    Wf = [np.ascontiguousarray(w, dtype=np.float64).reshape(-1) for w in W]
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    return float(lib().om_grid_dt1(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf),
+                                   _ptr(Hf), float(g), float(cfl)))
+
+
+def grid_update1(nx, ny, dx, dy, H, W, g, dt):
+    """eq. (4) with a given dt on the implicit grid; returns (fields, status)."""
+    Wf = _fields(W, int(nx) * int(ny))
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(4 * int(nx) * int(ny))
+    st = lib().om_grid_update1(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf),
+                               _ptr(Hf), float(g), float(dt), _ptr(work))
+    return Wf, int(st)
+
+
+def grid_run1(nx, ny, dx, dy, H, W, g, cfl, nsteps):
+    """``nsteps`` steps on the implicit grid; returns (fields, dts, status)."""
+    n = int(nx) * int(ny)
+    Wf = _fields(W, n)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(4 * n)
+    dts = np.zeros(max(int(nsteps), 1))
+    done = C.c_int64(0)
+    st = lib().om_grid_run1(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf), _ptr(Hf),
+                            float(g), float(cfl), int(nsteps), _ptr(dts), _ptr(work),
+                            C.byref(done))
+    return Wf, dts[: done.value], int(st)
 
 
 def run_grid(d, nsteps=None, cfl=None):

@@ -36,30 +36,32 @@
 
 int64_t om_grid_edges(int64_t nx, int64_t ny) { return 4 * nx * ny; }
 
+/* The four edges of cell c of the nx x ny grid: East, North, West, South. */
+static void grid_cell_edges(int64_t nx, int64_t ny, double dx, double dy, int64_t c,
+                            int64_t nbr[4], double ex[4], double ey[4], double len[4]) {
+  static const int di[4] = {1, 0, -1, 0};
+  static const int dj[4] = {0, 1, 0, -1};
+  int64_t i = c % nx, j = c / nx;
+  for (int k = 0; k < 4; ++k) {
+    int64_t ii = i + di[k], jj = j + dj[k];
+    int inside = ii >= 0 && ii < nx && jj >= 0 && jj < ny;
+    nbr[k] = inside ? jj * nx + ii : -1;
+    ex[k] = (double)di[k];
+    ey[k] = (double)dj[k];
+    len[k] = (k == 0 || k == 2) ? dy : dx;
+  }
+}
+
 void om_grid_mesh(int64_t nx, int64_t ny, double dx, double dy, double *area,
                   int64_t *edge_start, int64_t *nbr, double *eta_x,
                   double *eta_y, double *len) {
-  /* East, North, West, South */
-  static const int di[4] = {1, 0, -1, 0};
-  static const int dj[4] = {0, 1, 0, -1};
-  int64_t e = 0;
-  for (int64_t j = 0; j < ny; ++j) {
-    for (int64_t i = 0; i < nx; ++i) {
-      int64_t c = j * nx + i;
-      area[c] = dx * dy;
-      edge_start[c] = e;
-      for (int k = 0; k < 4; ++k) {
-        int64_t ii = i + di[k], jj = j + dj[k];
-        int inside = ii >= 0 && ii < nx && jj >= 0 && jj < ny;
-        nbr[e] = inside ? jj * nx + ii : -1;
-        eta_x[e] = (double)di[k];
-        eta_y[e] = (double)dj[k];
-        len[e] = (k == 0 || k == 2) ? dy : dx;
-        ++e;
-      }
-    }
+  for (int64_t c = 0; c < nx * ny; ++c) {
+    area[c] = dx * dy;
+    edge_start[c] = 4 * c;
+    grid_cell_edges(nx, ny, dx, dy, c, nbr + 4 * c, eta_x + 4 * c, eta_y + 4 * c,
+                    len + 4 * c);
   }
-  edge_start[nx * ny] = e;
+  edge_start[nx * ny] = 4 * nx * ny;
 }
 
 static double sgn(double x) { return (x > 0.0) ? 1.0 : ((x < 0.0) ? -1.0 : 0.0); }
@@ -149,21 +151,51 @@ static void cell_state(const double *const *W, int64_t i, double out[4]) {
   for (int k = 0; k < 4; ++k) out[k] = W[k][i];
 }
 
+/* A cell-edge source: an explicit polygon mesh, or the implicit Cartesian
+ * grid (the same edges as om_grid_mesh, generated per cell). */
+typedef struct {
+  const om_mesh *m;
+  int64_t nx, ny;
+  double dx, dy;
+} view;
+
+static int64_t view_cells(const view *v) { return v->m ? v->m->n_cells : v->nx * v->ny; }
+static double view_area(const view *v, int64_t i) { return v->m ? v->m->area[i] : v->dx * v->dy; }
+
+static int view_edges(const view *v, int64_t i, int64_t nbr[OM_MAX_EDGES],
+                      double ex[OM_MAX_EDGES], double ey[OM_MAX_EDGES],
+                      double len[OM_MAX_EDGES]) {
+  if (!v->m) {
+    grid_cell_edges(v->nx, v->ny, v->dx, v->dy, i, nbr, ex, ey, len);
+    return 4;
+  }
+  int64_t e0 = v->m->edge_start[i], e1 = v->m->edge_start[i + 1];
+  int n = (int)(e1 - e0);
+  if (n > OM_MAX_EDGES) n = OM_MAX_EDGES; /* meshes are checked by the caller */
+  for (int k = 0; k < n; ++k) {
+    nbr[k] = v->m->nbr[e0 + k];
+    ex[k] = v->m->eta_x[e0 + k];
+    ey[k] = v->m->eta_y[e0 + k];
+    len[k] = v->m->len[e0 + k];
+  }
+  return n;
+}
+
 /* All edge terms of cell i: L_e F_e (4 components) and L_e ||D_e||. */
-static int cell_terms(const om_mesh *m, const double *const *W, const double *H,
+static int cell_terms(const view *v, const double *const *W, const double *H,
                       double g, int64_t i, double Fl[4][OM_MAX_EDGES],
                       double Dl[OM_MAX_EDGES]) {
-  int64_t e0 = m->edge_start[i], e1 = m->edge_start[i + 1];
-  int n = (int)(e1 - e0);
+  int64_t nbr[OM_MAX_EDGES];
+  double exs[OM_MAX_EDGES], eys[OM_MAX_EDGES], lens[OM_MAX_EDGES];
+  int n = view_edges(v, i, nbr, exs, eys, lens);
   double Wi[4], Wj[4];
   cell_state(W, i, Wi);
   for (int k = 0; k < n; ++k) {
-    int64_t e = e0 + k;
-    double ex = m->eta_x[e], ey = m->eta_y[e], L = m->len[e];
+    double ex = exs[k], ey = eys[k], L = lens[k];
     double Hj;
-    if (m->nbr[e] >= 0) {
-      cell_state(W, m->nbr[e], Wj);
-      Hj = H[m->nbr[e]];
+    if (nbr[k] >= 0) {
+      cell_state(W, nbr[k], Wj);
+      Hj = H[nbr[k]];
     } else {
       om_wall_ghost1(Wi, ex, ey, Wj);
       Hj = H[i];
@@ -176,14 +208,15 @@ static int cell_terms(const om_mesh *m, const double *const *W, const double *H,
   return n;
 }
 
-double om_dt1(const om_mesh *m, const double *const *W, const double *H,
-              double g, double cfl) {
+static double dt_view(const view *v, const double *const *W, const double *H,
+                      double g, double cfl) {
   double dt = INFINITY;
   double Fl[4][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
-  for (int64_t i = 0; i < m->n_cells; ++i) {
-    int n = cell_terms(m, W, H, g, i, Fl, Dl);
+  int64_t N = view_cells(v);
+  for (int64_t i = 0; i < N; ++i) {
+    int n = cell_terms(v, W, H, g, i, Fl, Dl);
     double s = psum(Dl, n);
-    double dti = 2.0 * cfl * m->area[i] / s;
+    double dti = 2.0 * cfl * view_area(v, i) / s;
     if (isnan(dti)) return dti;
     if (dti < dt) dt = dti;
   }
@@ -197,15 +230,15 @@ static int check_state(const double w[4]) {
   return OM_OK;
 }
 
-int om_update1(const om_mesh *m, double *const *W, const double *H, double g,
-               double dt, double *work) {
+static int update_view(const view *v, double *const *W, const double *H, double g,
+                       double dt, double *work) {
   const double *const *Wc = (const double *const *)W;
   double Fl[4][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
-  int64_t N = m->n_cells;
+  int64_t N = view_cells(v);
   for (int64_t i = 0; i < N; ++i) {
-    int n = cell_terms(m, Wc, H, g, i, Fl, Dl);
+    int n = cell_terms(v, Wc, H, g, i, Fl, Dl);
     for (int c = 0; c < 4; ++c)
-      work[c * N + i] = W[c][i] - dt / m->area[i] * psum(Fl[c], n);
+      work[c * N + i] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
   }
   int status = OM_OK;
   for (int64_t i = 0; i < N; ++i) {
@@ -220,34 +253,88 @@ int om_update1(const om_mesh *m, double *const *W, const double *H, double g,
   return status;
 }
 
-void om_update1_at(const om_mesh *m, const double *const *W, const double *H,
-                   double g, double dt, const int64_t *cells, int64_t n_sel,
-                   double *out) {
+static void update_at_view(const view *v, const double *const *W, const double *H,
+                           double g, double dt, const int64_t *cells, int64_t n_sel,
+                           double *out) {
   double Fl[4][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
   for (int64_t s = 0; s < n_sel; ++s) {
     int64_t i = cells[s];
-    int n = cell_terms(m, W, H, g, i, Fl, Dl);
+    int n = cell_terms(v, W, H, g, i, Fl, Dl);
     for (int c = 0; c < 4; ++c)
-      out[c * n_sel + s] = W[c][i] - dt / m->area[i] * psum(Fl[c], n);
+      out[c * n_sel + s] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
   }
 }
 
-int om_run1(const om_mesh *m, double *const *W, const double *H, double g,
-            double cfl, int64_t nsteps, double *dts, double *work,
-            int64_t *steps_done) {
+static int run_view(const view *v, double *const *W, const double *H, double g,
+                    double cfl, int64_t nsteps, double *dts, double *work,
+                    int64_t *steps_done) {
   int64_t done = 0;
   int status = OM_OK;
   for (int64_t n = 0; n < nsteps; ++n) {
-    double dt = om_dt1(m, (const double *const *)W, H, g, cfl);
+    double dt = dt_view(v, (const double *const *)W, H, g, cfl);
     if (dts) dts[n] = dt;
     if (!isfinite(dt) || !(dt > 0.0)) {
       status = OM_ERR_NONFINITE;
       break;
     }
-    status = om_update1(m, W, H, g, dt, work);
+    status = update_view(v, W, H, g, dt, work);
     ++done;
     if (status != OM_OK) break;
   }
   if (steps_done) *steps_done = done;
   return status;
+}
+
+static view mesh_view(const om_mesh *m) {
+  view v = {m, 0, 0, 0.0, 0.0};
+  return v;
+}
+static view grid_view(int64_t nx, int64_t ny, double dx, double dy) {
+  view v = {0, nx, ny, dx, dy};
+  return v;
+}
+
+double om_dt1(const om_mesh *m, const double *const *W, const double *H,
+              double g, double cfl) {
+  view v = mesh_view(m);
+  return dt_view(&v, W, H, g, cfl);
+}
+
+int om_update1(const om_mesh *m, double *const *W, const double *H, double g,
+               double dt, double *work) {
+  view v = mesh_view(m);
+  return update_view(&v, W, H, g, dt, work);
+}
+
+void om_update1_at(const om_mesh *m, const double *const *W, const double *H,
+                   double g, double dt, const int64_t *cells, int64_t n_sel,
+                   double *out) {
+  view v = mesh_view(m);
+  update_at_view(&v, W, H, g, dt, cells, n_sel, out);
+}
+
+int om_run1(const om_mesh *m, double *const *W, const double *H, double g,
+            double cfl, int64_t nsteps, double *dts, double *work,
+            int64_t *steps_done) {
+  view v = mesh_view(m);
+  return run_view(&v, W, H, g, cfl, nsteps, dts, work, steps_done);
+}
+
+double om_grid_dt1(int64_t nx, int64_t ny, double dx, double dy,
+                   const double *const *W, const double *H, double g, double cfl) {
+  view v = grid_view(nx, ny, dx, dy);
+  return dt_view(&v, W, H, g, cfl);
+}
+
+int om_grid_update1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                    const double *H, double g, double dt, double *work) {
+  view v = grid_view(nx, ny, dx, dy);
+  return update_view(&v, W, H, g, dt, work);
+}
+
+int om_grid_run1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                 const double *H, double g, double cfl, int64_t nsteps, double *dts,
+                 double *work, int64_t *steps_done) {
+  view v = grid_view(nx, ny, dx, dy);
+  return run_view(&v, W, H, g, cfl, nsteps, dts, work, steps_done);
 }

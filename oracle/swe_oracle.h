@@ -89,6 +89,18 @@ int om_run1(const om_mesh *m, double *const *W, const double *H, double g,
             double cfl, int64_t nsteps, double *dts, double *work,
             int64_t *steps_done);
 
+/* The same three operations on the nx x ny Cartesian grid (cell (i, j) is
+ * index j*nx + i, edges East, North, West, South) without storing a mesh:
+ * each cell's edges are generated on the fly exactly as om_grid_mesh lists
+ * them.  For grids too large to hold as explicit meshes. */
+double om_grid_dt1(int64_t nx, int64_t ny, double dx, double dy,
+                   const double *const *W, const double *H, double g, double cfl);
+int om_grid_update1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                    const double *H, double g, double dt, double *work);
+int om_grid_run1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                 const double *H, double g, double cfl, int64_t nsteps, double *dts,
+                 double *work, int64_t *steps_done);
+
 #ifdef __cplusplus
 }
 #endif

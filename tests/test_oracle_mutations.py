@@ -38,17 +38,17 @@ MUTANTS = {
     # hydrostatic pressure without its factor 1/2
     "pressure_half": ("qn * qn / h + 0.5 * g * h * h", "qn * qn / h + g * h * h"),
     # CFL without the factor 2 of eq. (5)
-    "cfl_factor": ("double dti = 2.0 * cfl * m->area[i] / s;",
-                   "double dti = cfl * m->area[i] / s;"),
+    "cfl_factor": ("double dti = 2.0 * cfl * view_area(v, i) / s;",
+                   "double dti = cfl * view_area(v, i) / s;"),
     # edge lengths of the two directions swapped
-    "edge_length": ("len[e] = (k == 0 || k == 2) ? dy : dx;",
-                    "len[e] = (k == 0 || k == 2) ? dx : dy;"),
+    "edge_length": ("len[k] = (k == 0 || k == 2) ? dy : dx;",
+                    "len[k] = (k == 0 || k == 2) ? dx : dy;"),
     # wrong neighbour index (North points South)
     "neighbour_index": ("static const int dj[4] = {0, 1, 0, -1};",
                         "static const int dj[4] = {0, -1, 0, -1};"),
     # update with the wrong sign
-    "update_sign": ("work[c * N + i] = W[c][i] - dt / m->area[i]",
-                    "work[c * N + i] = W[c][i] + dt / m->area[i]"),
+    "update_sign": ("work[c * N + i] = W[c][i] - dt / view_area(v, i)",
+                    "work[c * N + i] = W[c][i] + dt / view_area(v, i)"),
     # wall ghost that does not reflect the normal discharge
     "wall_no_reflect": ("Wg[1] = Wi[1] - 2.0 * qn * ex;", "Wg[1] = Wi[1];"),
 }

@@ -331,3 +331,17 @@ def test_depth_error_reported():
     W0 = [np.array([1.0, 1e-3]), np.array([0.0, -5.0]), np.zeros(2), np.zeros(2)]
     _, _, st, done = O.run1(m, np.zeros(2), W0, G, 0.9, 5)
     assert st in (O.OM_ERR_DEPTH, O.OM_ERR_NONFINITE)
+
+
+def test_implicit_grid_equals_explicit_mesh():
+    # the mesh-free Cartesian entry points list the same edges in the same
+    # order as the explicit mesh, so they agree bit for bit
+    d = I.make_workload("pulses8192", nx=37, ny=29)
+    m = O.grid_mesh(37, 29, d["dx"], d["dy"])
+    W0 = [d[k] for k in ("h", "qx", "qy", "hC")]
+    Wa, dta, sa, _ = O.run1(m, d["H"], W0, G, 0.9, 20)
+    Wb, dtb, sb = O.grid_run1(37, 29, d["dx"], d["dy"], d["H"], W0, G, 0.9, 20)
+    assert sa == sb == O.OM_OK and np.array_equal(dta, dtb)
+    for a, b in zip(Wa, Wb):
+        assert np.array_equal(a, b)
+    assert O.grid_dt1(37, 29, d["dx"], d["dy"], d["H"], W0, G, 0.9) == dta[0]

@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Throughput of the Roe finite-volume shallow-water step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload pulses8192|hills2048|dam128] [--precision 32|64]
+
+One "step" is one explicit time step of the one-layer + pollutant IR-Roe
+scheme over the whole grid: edge fluxes with the bathymetry source, per-cell
+accumulation, the global CFL dt reduced on the device, and the update of h,
+q and hC (one fused kernel launch).  The default workload is the 8192 x 8192
+fp32 grid of seeded Gaussian hills and surface pulses with small random
+velocities (2.4 GB of state per step, far beyond the 129 MB L2).
+
+Prints one JSON line on rank 0.  ``value`` is cell-updates per second over all
+ranks (Mcell-updates/s), timed with CUDA events on the stream the kernels run
+on, inputs resident in HBM.  ``e2e`` is the same metric through the C ABI with
+host buffers (pinned): every step uploads the state, steps once and reads the
+state back.  ``roofline`` compares the step kernel's algorithmic bytes (5
+fields read + 4 written per cell) per launch with the measured HBM copy
+bandwidth.  ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of
+the same workload on one host core.
+
+Several GPUs run independent replicas (the step has no exchange that would
+shard across GPUs here): weak scaling, max time over ranks.
+``--impl reference`` times the oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "cell-updates/s (Mcell-steps/s) of the Roe FV step; achieved HBM GB/s vs peak"
+UNIT = "Mcell-updates/s"
+BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC written
+DTYPE_NAME = {32: "f32", 64: "f64"}
+KERNEL = "cart1_step_kernel"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cart1_step_traffic.txt")
+STEP_SOURCE = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc", "swe_cart1.cu")
+
+DESCR = {
+    "pulses8192": "8192x8192 Cartesian, dx=10 m, 128 seeded Gaussian hills, 16 surface pulses, "
+                  "|u|<=0.1 m/s, pollutant per 16x16 block, reflective walls",
+    "hills2048": "2048x2048 Cartesian, dx=10 m, 8 seeded Gaussian hills, 3 surface bumps, "
+                 "q=0, pollutant per 16x16 block, reflective walls",
+    "dam128": "128x128 Cartesian, dx=1 m, circular dam break, flat bottom, reflective walls",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="pulses8192", choices=sorted(DESCR))
+    p.add_argument("--precision", type=int, choices=[32, 64], default=None)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    a = p.parse_args()
+    if a.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if a.steps < 1:
+        p.error("--steps must be at least 1")
+    return a
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_per_launch(precision, workload):
+    """DRAM bytes per launch of the step kernel from the committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    try:
+        src_hash = hashlib.sha256(open(STEP_SOURCE, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in open(TRAFFIC_FILE):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("source_sha256_16") != src_hash:
+            return None
+        key = f"bytes_per_launch_{workload}_f{precision}"
+        return float(vals[key]) if key in vals else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="swe_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t_marks):
+        # rows carry no timestamps; all samples lie in the busy window that
+        # brackets the timed steps
+        if not rows or isinstance(rows, dict):
+            return rows if isinstance(rows, dict) else {"sm_mhz": None, "sm_max_mhz": None,
+                                                        "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_median": statistics.median(pw) if pw else None}
+
+
+def physical_gpu(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def cpu_baseline(d, budget_s=12.0):
+    """The oracle (fp64, one thread) on a band of the workload's first rows."""
+    import numpy as np
+
+    import oracle as O
+    from finite_volume_shallow_gb300 import inputs as I
+
+    nx = d["nx"]
+    rows = min(d["ny"], 64)
+    def window(r):
+        sl = slice(0, r * nx)
+        return d["H"][sl], [f[sl] for f in I.fields_of(d)]
+    H, W = window(rows)
+    t0 = time.perf_counter()
+    O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], 1)
+    per_cell = (time.perf_counter() - t0) / (nx * rows)
+    rows = int(max(8, min(d["ny"], budget_s / 4 / (per_cell * nx))))
+    steps = max(1, int(budget_s / (per_cell * nx * rows)))
+    H, W = window(rows)
+    t0 = time.perf_counter()
+    _, dts, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], steps)
+    el = time.perf_counter() - t0
+    return {"value": nx * rows * steps / el / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {d['nx']}x{d['ny']} initial state as a "
+                      f"walled {nx}x{rows} grid, {steps} steps, fp64, single thread, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle, timed on the host cores, on a
+    bounded sample of the workload per step."""
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle as O
+    from finite_volume_shallow_gb300 import inputs as I
+
+    d = I.make_workload(args.workload)
+    precision = args.precision or d["precision"]
+    nx = d["nx"]
+    cal_rows = min(d["ny"], 16)
+    sl = slice(0, cal_rows * nx)
+    t0 = time.perf_counter()
+    O.grid_run1(nx, cal_rows, d["dx"], d["dy"], d["H"][sl], [f[sl] for f in I.fields_of(d)],
+                d["g"], d["cfl"], 1)
+    per_cell = (time.perf_counter() - t0) / (nx * cal_rows)
+    budget = 150.0
+    rows = int(max(4, min(d["ny"], budget / ((args.steps + args.warmup) * per_cell * nx))))
+    sl = slice(0, rows * nx)
+    H = d["H"][sl]
+    W = [f[sl] for f in I.fields_of(d)]
+    W, _, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], args.warmup)
+    t0 = time.perf_counter()
+    W, _, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], args.steps)
+    el = time.perf_counter() - t0
+    value = nx * rows * args.steps / el / 1e6
+    sample = (f"each step: one oracle step over rows 0..{rows - 1} of the {d['nx']}x{d['ny']} "
+              f"workload as a walled {nx}x{rows} grid (fp64, single thread)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}",
+                   "cells": d["nx"] * d["ny"], "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "status": st,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+
+    from finite_volume_shallow_gb300 import inputs as I
+    from finite_volume_shallow_gb300 import swe as S
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    S.load()
+    d = I.make_workload(args.workload)
+    precision = args.precision or d["precision"]
+    npdt = np.float32 if precision == 32 else np.float64
+    tdt = torch.float32 if precision == 32 else torch.float64
+    n = d["nx"] * d["ny"]
+    fields = [f.astype(npdt) for f in I.fields_of(d)]
+    stream = torch.cuda.Stream()
+    st = S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(npdt), fields,
+                           precision=precision, g=d["g"], cfl=d["cfl"],
+                           stream=stream.cuda_stream)
+    info = S.swe_get_info(st)
+
+    # warm-up (also gives a step-time estimate for the busy window below)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    S.swe_run(st, args.warmup)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - w0) / args.warmup
+
+    # timed region, inside a busy window sampled by nvidia-smi: about 0.5 s of
+    # the same steps runs untimed right before it so the clock record covers
+    # the kernel even when the timed region is shorter than the sampling period
+    sampler = ClockSampler(physical_gpu(local))
+    sampler.start()
+    pre = int(min(5000, 0.5 / max(est, 1e-6)))
+    if pre:
+        S.swe_run(st, pre)
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    S.swe_run(st, args.steps)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    rows = sampler.stop()
+    clocks = ClockSampler.summarise(rows, None)
+
+    t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    value = world * n * args.steps / (ms_max / 1e3) / 1e6
+
+    # end to end through the C ABI with pinned host buffers
+    ke = max(3, min(args.e2e_steps, args.steps))
+    host = [torch.from_numpy(f).pin_memory() for f in S.swe_get_state(st)[0]]
+    S.swe_set_state(st, host, 0.0)
+    S.swe_step(st, d["cfl"])
+    S.swe_get_state(st, out=host)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        S.swe_set_state(st, host, 0.0)
+        S.swe_step(st, d["cfl"])
+        S.swe_get_state(st, out=host)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_s = float(te.item())
+    esz = 4 if precision == 32 else 8
+    e2e = {"value": world * n * ke / e2e_s / 1e6, "unit": UNIT, "steps": ke,
+           "h2d_bytes_per_step": 4 * n * esz + 8, "d2h_bytes_per_step": 4 * n * esz + 8 + 8 + 4,
+           "api": "swe_set_state + swe_step + swe_get_state, pinned host buffers"}
+    S.swe_destroy(st)
+
+    peak, peak_kind = load_peaks()
+    achieved = BYTES_PER_CELL[precision] * n / (ms_per_step / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_kind,
+            "traffic": traffic_per_launch(precision, args.workload),
+            "kernel": KERNEL, "algorithmic_bytes_per_launch": BYTES_PER_CELL[precision] * n}
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(d)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_NAME[precision], "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}",
+                       "cells": n, "nx": d["nx"], "ny": d["ny"], "parallelism": "replicas",
+                       "l2": "inputs larger than L2" if n * BYTES_PER_CELL[precision] > 129e6
+                             else "inputs fit in L2 (no flush)",
+                       "launch": {"bands": info["bands"], "segments": info["segments"],
+                                  "warps_per_block": info["warps_per_block"]}},
+            "e2e": e2e, "roofline": roof, "cpu_baseline": base, "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

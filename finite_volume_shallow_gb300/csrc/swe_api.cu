@@ -1,0 +1,400 @@
+// swe_api.cu -- host side of the libswe C ABI (include/swe.h): argument
+// checking, device memory, launch orchestration and the dt bookkeeping of
+// the time loop of An MPI-CUDA implementation of an improved Roe method for
+// two-layer shallow water systems, Sec. 3 and Algorithm 1 (edges, per-volume
+// dt, global minimum, volume update, t += dt), on one GPU.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/swe.h"
+#include "swe_internal.h"
+
+using namespace swe;
+
+struct swe_state {
+  int nx = 0, ny = 0;
+  double dx = 0, dy = 0;
+  swe_params p{};
+  int prec = 0;
+  size_t esz = 0;
+  int pitch = 0;
+  int64_t field_stride = 0;  // elements between field bases in the allocation
+  void* dev = nullptr;
+  size_t dev_bytes = 0;
+  void* w[2][4] = {{nullptr}};
+  void* H = nullptr;
+  void* slots = nullptr;      // 3 wave-speed maxima (8 bytes each)
+  double* dt_hist = nullptr;
+  double* t_dev = nullptr;
+  unsigned* err = nullptr;
+  int cur = 0;
+  int64_t step = 0;
+  cudaStream_t stream = nullptr;
+  int nbands = 0, nsegs = 0, blocks = 0;
+  double* h_dt = nullptr;     // pinned readback
+  unsigned* h_err = nullptr;
+  double* h_t = nullptr;
+  unsigned sticky = 0;
+};
+
+namespace {
+
+swe_status status_of_bits(unsigned bits) {
+  if (bits & kErrTimeout) return SWE_ERR_TIMEOUT;
+  if (bits & kErrNonfinite) return SWE_ERR_NONFINITE;
+  if (bits & kErrDepth) return SWE_ERR_DEPTH;
+  return SWE_OK;
+}
+
+swe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SWE_OK;
+  (void)cudaGetLastError();  // clear a non-sticky error
+  return e == cudaErrorMemoryAllocation ? SWE_ERR_OOM : SWE_ERR_CUDA;
+}
+
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_status(e_); \
+  } while (0)
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Launch shape: one warp per (column band, row segment); enough segments to
+// give every resident warp slot one unit, but no segment shorter than
+// kMinSegRows rows (each segment re-reads four halo rows).
+constexpr int kMinSegRows = 32;
+
+template <typename T>
+swe_status plan_launch(swe_state* s) {
+  int bpsm = 0;
+  size_t smem = 0;
+  CK(step_occupancy<T>(&bpsm, &smem));
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (bpsm < 1) return SWE_ERR_CUDA;
+  const int64_t slots = (int64_t)sms * bpsm * kWarpsPerBlock;
+  const int own = band_owned<T>();
+  s->nbands = (s->nx + own - 1) / own;
+  int64_t nsegs = slots / s->nbands;
+  int64_t max_segs = s->ny / kMinSegRows;
+  if (nsegs > max_segs) nsegs = max_segs;
+  if (nsegs < 1) nsegs = 1;
+  if (nsegs > s->ny) nsegs = s->ny;
+  s->nsegs = (int)nsegs;
+  const int64_t units = (int64_t)s->nbands * s->nsegs;
+  s->blocks = (int)((units + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  return SWE_OK;
+}
+
+template <typename T>
+swe_status enqueue_dt0(swe_state* s) {
+  // all three wave-speed slots to zero, then slot (step % 3) <- max of W^n
+  CK(cudaMemsetAsync(s->slots, 0, 3 * sizeof(uint64_t), s->stream));
+  const T* w[4] = {(const T*)s->w[s->cur][0], (const T*)s->w[s->cur][1],
+                   (const T*)s->w[s->cur][2], (const T*)s->w[s->cur][3]};
+  void* slot = (char*)s->slots + (s->step % 3) * sizeof(uint64_t);
+  CK(launch_dt0<T>(w, (const T*)s->H, s->nx, s->ny, s->pitch, (T)(0.5 * s->p.g),
+                   (T)(s->dx / s->dy), slot, s->err, s->stream));
+  return SWE_OK;
+}
+
+template <typename T>
+swe_status enqueue_step(swe_state* s, double cfl) {
+  StepArgs<T> a;
+  for (int f = 0; f < 4; ++f) {
+    a.win[f] = (const T*)s->w[s->cur][f];
+    a.wout[f] = (T*)s->w[s->cur ^ 1][f];
+  }
+  a.H = (const T*)s->H;
+  a.nx = s->nx;
+  a.ny = s->ny;
+  a.pitch = s->pitch;
+  a.nbands = s->nbands;
+  a.nsegs = s->nsegs;
+  a.ghalf = (T)(0.5 * s->p.g);
+  a.rho = (T)(s->dx / s->dy);
+  a.two_cfl = 2.0 * cfl;
+  a.dx = s->dx;
+  char* sl = (char*)s->slots;
+  a.tmax_in = sl + (s->step % 3) * sizeof(uint64_t);
+  a.tmax_out = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
+  a.tmax_clear = sl + ((s->step + 2) % 3) * sizeof(uint64_t);
+  a.dt_hist = s->dt_hist;
+  a.t_dev = s->t_dev;
+  a.step = s->step;
+  a.err = s->err;
+  CK(launch_step<T>(a, s->blocks, s->stream));
+  s->cur ^= 1;
+  s->step += 1;
+  return SWE_OK;
+}
+
+swe_status enqueue_dt0_any(swe_state* s) {
+  return s->prec == 32 ? enqueue_dt0<float>(s) : enqueue_dt0<double>(s);
+}
+swe_status enqueue_step_any(swe_state* s, double cfl) {
+  return s->prec == 32 ? enqueue_step<float>(s, cfl) : enqueue_step<double>(s, cfl);
+}
+
+// Copy 4 host fields (or H when n == 1) into the padded layout of `dst`.
+swe_status upload(swe_state* s, void* const* dst, const void* const* src, int n) {
+  const size_t row = (size_t)s->nx * s->esz;
+  const size_t dpitch = (size_t)s->pitch * s->esz;
+  const size_t off = ((size_t)kPadY * s->pitch + kPadX) * s->esz;
+  for (int f = 0; f < n; ++f)
+    CK(cudaMemcpy2DAsync((char*)dst[f] + off, dpitch, src[f], row, row, (size_t)s->ny,
+                         cudaMemcpyHostToDevice, s->stream));
+  return SWE_OK;
+}
+
+swe_status read_err(swe_state* s) {
+  CK(cudaMemcpyAsync(s->h_err, s->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s->stream));
+  CK(cudaStreamSynchronize(s->stream));
+  s->sticky |= *s->h_err;
+  return SWE_OK;
+}
+
+bool finite_pos(double v) { return isfinite(v) && v > 0.0; }
+
+template <typename T>
+swe_status fill_pads(swe_state* s) {
+  // whole padded arrays: h = 1, everything else 0; interiors are then copied
+  const int64_t n = s->field_stride;
+  for (int b = 0; b < 2; ++b)
+    for (int f = 0; f < 4; ++f) CK(launch_fill<T>((T*)s->w[b][f], n, f == 0 ? T(1) : T(0), s->stream));
+  CK(launch_fill<T>((T*)s->H, n, T(0), s->stream));
+  return SWE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* swe_status_str(swe_status st) {
+  switch (st) {
+    case SWE_OK: return "ok";
+    case SWE_ERR_ARG: return "invalid argument";
+    case SWE_ERR_CUDA: return "CUDA runtime error";
+    case SWE_ERR_OOM: return "out of device memory";
+    case SWE_ERR_DEPTH: return "a depth h <= 0 appeared";
+    case SWE_ERR_NONFINITE: return "a non-finite value appeared";
+    case SWE_ERR_HYPERBOLIC: return "loss of hyperbolicity";
+    case SWE_ERR_UNSUPPORTED: return "not supported by this build";
+    case SWE_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+void swe_destroy(swe_state* s) {
+  if (!s) return;
+  if (s->stream || s->dev) cudaStreamSynchronize(s->stream);
+  if (s->dev) cudaFree(s->dev);
+  if (s->h_dt) cudaFreeHost(s->h_dt);
+  delete s;
+}
+
+swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* const* W0,
+                           const swe_params* params, swe_state** out) {
+  if (!out) return SWE_ERR_ARG;
+  *out = nullptr;
+  if (!grid || !H || !W0 || !params) return SWE_ERR_ARG;
+  for (int f = 0; f < 4; ++f)
+    if (!W0[f]) return SWE_ERR_ARG;
+  if (grid->nx < 1 || grid->ny < 1) return SWE_ERR_ARG;
+  if (!finite_pos(grid->dx) || !finite_pos(grid->dy)) return SWE_ERR_ARG;
+  if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
+  if (!finite_pos(params->g)) return SWE_ERR_ARG;
+  if (!(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
+  if (params->n_layers == 2) return SWE_ERR_UNSUPPORTED;
+  if (params->n_layers != 1) return SWE_ERR_ARG;
+  if (params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  // index arithmetic inside the kernels is 32-bit per row and column
+  if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
+
+  swe_state* s = new (std::nothrow) swe_state();
+  if (!s) return SWE_ERR_OOM;
+  s->nx = grid->nx;
+  s->ny = grid->ny;
+  s->dx = grid->dx;
+  s->dy = grid->dy;
+  s->p = *params;
+  s->prec = params->precision;
+  s->esz = s->prec == 32 ? 4 : 8;
+  s->stream = (cudaStream_t)params->stream;
+  s->pitch = (int)(s->prec == 32 ? grid_pitch<float>(s->nx) : grid_pitch<double>(s->nx));
+
+  swe_status st = SWE_OK;
+  auto fail = [&](swe_status e) {
+    swe_destroy(s);
+    return e;
+  };
+  const int64_t felems = (int64_t)(s->ny + 2 * kPadY) * s->pitch;
+  const int64_t fbytes = round_up(felems * (int64_t)s->esz, 256);
+  s->field_stride = fbytes / (int64_t)s->esz;
+  const int64_t aux = 256 + round_up((int64_t)kHistCap * 8, 256) + 256 + 256;
+  s->dev_bytes = (size_t)(9 * fbytes + aux);
+  cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
+  if (e != cudaSuccess) {
+    s->dev = nullptr;
+    return fail(cuda_status(e));
+  }
+  char* p = (char*)s->dev;
+  for (int b = 0; b < 2; ++b)
+    for (int f = 0; f < 4; ++f) {
+      s->w[b][f] = p;
+      p += fbytes;
+    }
+  s->H = p;
+  p += fbytes;
+  s->slots = p;
+  p += 256;
+  s->dt_hist = (double*)p;
+  p += round_up((int64_t)kHistCap * 8, 256);
+  s->t_dev = (double*)p;
+  p += 256;
+  s->err = (unsigned*)p;
+  e = cudaMallocHost(&s->h_dt, 64);
+  if (e != cudaSuccess) {
+    s->h_dt = nullptr;
+    return fail(cuda_status(e));
+  }
+  s->h_err = (unsigned*)(s->h_dt + 1);
+  s->h_t = s->h_dt + 2;
+
+  st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
+  if (st != SWE_OK) return fail(st);
+  st = s->prec == 32 ? fill_pads<float>(s) : fill_pads<double>(s);
+  if (st != SWE_OK) return fail(st);
+  void* hdst[1] = {s->H};
+  const void* hsrc[1] = {H};
+  if ((st = upload(s, hdst, hsrc, 1)) != SWE_OK) return fail(st);
+  if ((st = upload(s, s->w[0], W0, 4)) != SWE_OK) return fail(st);
+  if ((e = cudaMemsetAsync(s->t_dev, 0, 256 + 256, s->stream)) != cudaSuccess)
+    return fail(cuda_status(e));
+  s->cur = 0;
+  s->step = 0;
+  if ((st = enqueue_dt0_any(s)) != SWE_OK) return fail(st);
+  if ((st = read_err(s)) != SWE_OK) return fail(st);
+  if (s->sticky) return fail(SWE_ERR_ARG);
+  *out = s;
+  return SWE_OK;
+}
+
+swe_status swe_set_state(swe_state* s, const void* const* fields, double t) {
+  if (!s || !fields) return SWE_ERR_ARG;
+  for (int f = 0; f < 4; ++f)
+    if (!fields[f]) return SWE_ERR_ARG;
+  if (!isfinite(t)) return SWE_ERR_ARG;
+  swe_status st;
+  if ((st = upload(s, s->w[s->cur], fields, 4)) != SWE_OK) return st;
+  *s->h_t = t;
+  CK(cudaMemcpyAsync(s->t_dev, s->h_t, sizeof(double), cudaMemcpyHostToDevice, s->stream));
+  CK(cudaMemsetAsync(s->err, 0, sizeof(unsigned), s->stream));
+  s->step = 0;
+  s->sticky = 0;
+  if ((st = enqueue_dt0_any(s)) != SWE_OK) return st;
+  if ((st = read_err(s)) != SWE_OK) return st;
+  if (s->sticky) {
+    // keep the state usable for another set_state, but refuse to step it
+    return SWE_ERR_ARG;
+  }
+  return SWE_OK;
+}
+
+swe_status swe_step(swe_state* s, double cfl, double* dt_out) {
+  if (!s) return SWE_ERR_ARG;
+  if (!(cfl > 0.0 && cfl <= 1.0)) return SWE_ERR_ARG;
+  if (s->sticky) return status_of_bits(s->sticky);
+  swe_status st = enqueue_step_any(s, cfl);
+  if (st != SWE_OK) return st;
+  CK(cudaMemcpyAsync(s->h_dt, s->dt_hist + ((s->step - 1) % kHistCap), sizeof(double),
+                     cudaMemcpyDeviceToHost, s->stream));
+  if ((st = read_err(s)) != SWE_OK) return st;
+  if (dt_out) *dt_out = *s->h_dt;
+  return status_of_bits(s->sticky);
+}
+
+swe_status swe_run(swe_state* s, int64_t nsteps) {
+  if (!s || nsteps < 0) return SWE_ERR_ARG;
+  if (s->sticky) return status_of_bits(s->sticky);
+  for (int64_t n = 0; n < nsteps; ++n) {
+    swe_status st = enqueue_step_any(s, s->p.cfl);
+    if (st != SWE_OK) return st;
+  }
+  swe_status st = read_err(s);
+  if (st != SWE_OK) return st;
+  return status_of_bits(s->sticky);
+}
+
+swe_status swe_get_state(const swe_state* cs, void* const* fields_out, double* t_out) {
+  swe_state* s = const_cast<swe_state*>(cs);
+  if (!s || !fields_out) return SWE_ERR_ARG;
+  for (int f = 0; f < 4; ++f)
+    if (!fields_out[f]) return SWE_ERR_ARG;
+  const size_t row = (size_t)s->nx * s->esz;
+  const size_t spitch = (size_t)s->pitch * s->esz;
+  const size_t off = ((size_t)kPadY * s->pitch + kPadX) * s->esz;
+  for (int f = 0; f < 4; ++f)
+    CK(cudaMemcpy2DAsync(fields_out[f], row, (const char*)s->w[s->cur][f] + off, spitch, row,
+                         (size_t)s->ny, cudaMemcpyDeviceToHost, s->stream));
+  CK(cudaMemcpyAsync(s->h_t, s->t_dev, sizeof(double), cudaMemcpyDeviceToHost, s->stream));
+  CK(cudaStreamSynchronize(s->stream));
+  if (t_out) *t_out = *s->h_t;
+  return SWE_OK;
+}
+
+swe_status swe_get_dt_history(const swe_state* cs, double* dts, int64_t max, int64_t* n) {
+  swe_state* s = const_cast<swe_state*>(cs);
+  if (!s || !n || max < 0 || (max > 0 && !dts)) return SWE_ERR_ARG;
+  int64_t have = s->step < kHistCap ? s->step : kHistCap;
+  int64_t cnt = have < max ? have : max;
+  // the cnt most recent entries, oldest first
+  int64_t first = s->step - cnt;
+  int64_t done = 0;
+  while (done < cnt) {
+    int64_t idx = (first + done) % kHistCap;
+    int64_t run = kHistCap - idx;
+    if (run > cnt - done) run = cnt - done;
+    CK(cudaMemcpyAsync(dts + done, s->dt_hist + idx, (size_t)run * sizeof(double),
+                       cudaMemcpyDeviceToHost, s->stream));
+    done += run;
+  }
+  CK(cudaStreamSynchronize(s->stream));
+  *n = cnt;
+  return SWE_OK;
+}
+
+swe_status swe_get_info(const swe_state* s, swe_info* info) {
+  if (!s || !info) return SWE_ERR_ARG;
+  swe_state* m = const_cast<swe_state*>(s);
+  CK(cudaMemcpyAsync(m->h_t, m->t_dev, sizeof(double), cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  info->steps = s->step;
+  info->t = *m->h_t;
+  info->nx = s->nx;
+  info->ny = s->ny;
+  info->precision = s->prec;
+  info->pitch = s->pitch;
+  info->field_offset = (int64_t)kPadY * s->pitch + kPadX;
+  info->device_bytes = (int64_t)s->dev_bytes;
+  info->bands = s->nbands;
+  info->segments = s->nsegs;
+  info->warps_per_block = kWarpsPerBlock;
+  return SWE_OK;
+}
+
+swe_status swe_device_fields(swe_state* s, void** ptrs) {
+  if (!s || !ptrs) return SWE_ERR_ARG;
+  for (int f = 0; f < 4; ++f) ptrs[f] = s->w[s->cur][f];
+  ptrs[4] = s->H;
+  return SWE_OK;
+}
+
+}  // extern "C"

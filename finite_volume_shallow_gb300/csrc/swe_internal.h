@@ -1,0 +1,81 @@
+// swe_internal.h -- shared between the host side of libswe and its kernels.
+//
+// Device layout of a Cartesian state (one allocation per handle):
+//   every field is a padded 2D array of (ny + 2*kPadY) rows of `pitch`
+//   elements; logical cell (x, y) sits at element (y + kPadY) * pitch +
+//   (x + kPadX).  The padding is never updated after creation: it only
+//   keeps the fixed-width row windows the step kernel loads inside the
+//   allocation.  Wall (mirror) states are formed in registers.
+//   Column windows: the grid is cut into vertical bands of kOwn<T> owned
+//   columns; band b loads the 32*kCpt<T> physical columns starting at
+//   b*kOwn<T>, i.e. its owned columns plus two halo columns on each side.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace swe {
+
+constexpr int kPadX = 2;
+constexpr int kPadY = 2;
+constexpr int kHistCap = 65536;   // dt history ring length
+
+// error bits written by the kernels into the sticky error word
+constexpr unsigned kErrDepth = 1u;
+constexpr unsigned kErrNonfinite = 2u;
+constexpr unsigned kErrTimeout = 4u;
+
+template <typename T> struct Cpt;
+template <> struct Cpt<float> { static constexpr int v = 4; };
+template <> struct Cpt<double> { static constexpr int v = 2; };
+
+template <typename T> constexpr int cells_per_lane() { return Cpt<T>::v; }
+template <typename T> constexpr int band_window() { return 32 * Cpt<T>::v; }
+template <typename T> constexpr int band_owned() { return 32 * Cpt<T>::v - 4; }
+
+// Pipeline depth (rows in flight per warp) and warps per block of the step.
+constexpr int kStages = 4;
+constexpr int kWarpsPerBlock = 4;
+
+// Row pitch (elements) for an nx-wide grid of element type T.
+template <typename T>
+inline int64_t grid_pitch(int nx) {
+  int64_t own = band_owned<T>();
+  int64_t nb = (nx + own - 1) / own;
+  int64_t need = own * (nb - 1) + band_window<T>();
+  return (need + 31) / 32 * 32;
+}
+
+template <typename T>
+struct StepArgs {
+  const T* win[4];      // W^n: h, qx, qy, hC (field bases, padded layout)
+  T* wout[4];           // W^{n+1}
+  const T* H;           // bottom depth (padded layout)
+  int nx, ny, pitch;
+  int nbands, nsegs;
+  T ghalf;              // g / 2
+  T rho;                // dx / dy (y-edge weight relative to x-edges)
+  double two_cfl;       // 2 * cfl of this step
+  double dx;
+  const void* tmax_in;  // max over cells of sum D (this step), raw bits
+  void* tmax_out;       // accumulated for the next step (must start at 0)
+  void* tmax_clear;     // slot zeroed for the step after next
+  double* dt_hist;      // dt ring
+  double* t_dev;        // simulated time
+  int64_t step;         // index of this step (selects the history slot)
+  unsigned* err;        // sticky error bits
+};
+
+// host-side launchers (swe_cart1.cu)
+template <typename T>
+cudaError_t launch_step(const StepArgs<T>& a, int blocks, cudaStream_t st);
+template <typename T>
+cudaError_t launch_dt0(const T* const* w, const T* H, int nx, int ny, int pitch,
+                       T ghalf, T rho, void* tmax_out, unsigned* err,
+                       cudaStream_t st);
+template <typename T>
+cudaError_t launch_fill(T* base, int64_t count, T value, cudaStream_t st);
+template <typename T>
+cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes);
+
+}  // namespace swe

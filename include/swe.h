@@ -1,0 +1,168 @@
+/*
+ * swe.h -- C ABI of the GB300 shallow-water finite-volume library (libswe).
+ *
+ * The library advances the 2D shallow-water equations with the first-order,
+ * path-conservative Roe-type ("IR-Roe") finite-volume scheme of
+ *
+ *   [P1] de la Asuncion, Mantas, Castro, Fernandez-Nieto, "An MPI-CUDA
+ *        implementation of an improved Roe method for two-layer shallow
+ *        water systems": Sec. 2.1 (model, eq. (1); rotation invariance,
+ *        eq. (2)-(3)), Sec. 2.2 (update eq. (4), numerical flux steps 1-4,
+ *        CFL condition eq. (5)), Sec. 3 and Algorithm 1 (time loop: edge
+ *        fluxes, per-volume dt, global minimum, volume update);
+ *   [P2] Vinas et al., "A multi-GPU shallow-water simulation with transport
+ *        of contaminants": abstract (one layer + a pollutant carried by a
+ *        transport equation) and Figure 4 (each edge's flux computed once per
+ *        tile and shared between its two cells).
+ *
+ * One explicit step, for every cell V_i with neighbours j:
+ *     W_i^{n+1} = W_i^n - dt_n / |V_i| * sum_j |Gamma_ij| F_ij^-      (eq. (4))
+ *     dt_n = min_i 2 cfl |V_i| / sum_j |Gamma_ij| ||D_ij||_inf          (eq. (5))
+ * with W = (h, qx, qy, hC): depth, discharge and pollutant mass per area.
+ * H is the depth of the bottom below a fixed reference level (positive
+ * downward, [P1] Sec. 2.1), so the free surface is h - H.  Domain boundaries
+ * are reflective walls (mirror ghost: same h, hC, H; normal discharge
+ * negated).  dt_n is reduced on the device from the state W^n; the host never
+ * sits between two steps unless it asks for dt.
+ *
+ * Conventions of every call:
+ *  - Every function returns a swe_status; nothing aborts or prints.
+ *  - Host arrays are in the caller's memory, owned by the caller, and copied
+ *    during the call.  Their element type is the state's precision: float
+ *    when swe_params.precision == 32, double when it is 64.
+ *  - Grid fields are nx*ny values, cell (i, j) at index j*nx + i (row-major,
+ *    x fastest), centre ((i+1/2) dx, (j+1/2) dy).
+ *  - Field order: h, qx, qy, hC.
+ *  - A handle is not thread-safe; it may be used from any one thread at a
+ *    time.  All device work of a handle is ordered on swe_params.stream.
+ *  - Device-detected errors (SWE_ERR_DEPTH, SWE_ERR_NONFINITE,
+ *    SWE_ERR_TIMEOUT) are sticky: every later swe_step / swe_run returns them
+ *    until swe_set_state installs a new state.  The handle stays valid and
+ *    destroyable after any error.
+ */
+#ifndef SWE_H
+#define SWE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SWE_OK = 0,
+  SWE_ERR_ARG = -1,         /* invalid argument (NULL, size, parameter)     */
+  SWE_ERR_CUDA = -2,        /* a CUDA runtime call failed                   */
+  SWE_ERR_OOM = -3,         /* device memory exhausted                      */
+  SWE_ERR_DEPTH = -4,       /* a depth h <= 0 appeared (dry cells are out   */
+                            /* of scope of the scheme as implemented)       */
+  SWE_ERR_NONFINITE = -5,   /* a non-finite value appeared in the state     */
+  SWE_ERR_HYPERBOLIC = -6,  /* reserved: loss of hyperbolicity (two layers) */
+  SWE_ERR_UNSUPPORTED = -7, /* valid request this build does not implement  */
+  SWE_ERR_TIMEOUT = -8      /* a bounded device wait gave up                */
+} swe_status;
+
+/* Cartesian grid of nx x ny rectangular cells of size dx x dy, walls on all
+ * four sides ([P1] Sec. 2.2 volumes V_i with |V_i| = dx dy; edges of length
+ * dy (normal (1, 0)) and dx (normal (0, 1))). */
+typedef struct {
+  int32_t nx, ny;
+  double dx, dy;
+} swe_grid;
+
+/* Model and run parameters.
+ *  n_layers   1 (the two-layer system of [P1] eq. (1) is not in this build:
+ *             SWE_ERR_UNSUPPORTED)
+ *  precision  32 or 64: arithmetic and storage type of the state
+ *  pollutant  must be 1: the state carries hC ([P2] transport equation)
+ *  g          gravity (> 0)
+ *  r          density ratio rho1/rho2 of two-layer runs; ignored for 1 layer
+ *  cfl        gamma of eq. (5), 0 < cfl <= 1, used by swe_run
+ *  stream     cudaStream_t the handle orders its work on; NULL = legacy
+ *             default stream */
+typedef struct {
+  int32_t n_layers;
+  int32_t precision;
+  int32_t pollutant;
+  double g;
+  double r;
+  double cfl;
+  void *stream;
+} swe_params;
+
+typedef struct swe_state swe_state;
+
+/* Create a simulation on a Cartesian grid ([P1] Algorithm 1, before the time
+ * loop: mesh construction and initial state).
+ *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite
+ *  H       host, nx*ny values: bottom depth below the reference level
+ *  W0      host, array of 4 pointers (h, qx, qy, hC), nx*ny values each;
+ *          h > 0 everywhere
+ *  params  see swe_params
+ *  out     receives the handle (NULL on failure)
+ * Allocates the device state (about 9 padded fields of the chosen precision),
+ * copies H and W0 to the device and computes dt_0 there.
+ * Errors: SWE_ERR_ARG (bad argument, h <= 0 or non-finite input),
+ * SWE_ERR_UNSUPPORTED, SWE_ERR_OOM, SWE_ERR_CUDA. */
+swe_status swe_create_grid(const swe_grid *grid, const void *H,
+                           const void *const *W0, const swe_params *params,
+                           swe_state **out);
+
+/* Advance one step of eq. (4) with dt_n from eq. (5) evaluated on the
+ * current state with CFL number cfl (0 < cfl <= 1).  Waits for the step to
+ * finish; *dt_out (if not NULL) receives dt_n.  Returns the sticky device
+ * error, if any, after the step. */
+swe_status swe_step(swe_state *s, double cfl, double *dt_out);
+
+/* Advance nsteps >= 0 steps with params.cfl.  Enqueues all steps on the
+ * handle's stream without host synchronisation, then waits once and reports
+ * the sticky device error. */
+swe_status swe_run(swe_state *s, int64_t nsteps);
+
+/* Copy the current state to the host.  fields_out: array of 4 host pointers
+ * (h, qx, qy, hC) of nx*ny elements of the state's precision; t_out (may be
+ * NULL) receives the simulated time (sum of the dt of all steps since the
+ * last swe_create_grid / swe_set_state, plus the t given there). */
+swe_status swe_get_state(const swe_state *s, void *const *fields_out,
+                         double *t_out);
+
+/* Replace the state (a restart), set the simulated time to t, clear the
+ * sticky error and recompute dt on the device.  Same layout as
+ * swe_get_state.  Errors: SWE_ERR_ARG for h <= 0 or non-finite input. */
+swe_status swe_set_state(swe_state *s, const void *const *fields, double t);
+
+/* dt of the most recent steps, oldest first: up to max values are written
+ * to dts (host) and *n receives the count written.  The library keeps the
+ * last 65536 steps. */
+swe_status swe_get_dt_history(const swe_state *s, double *dts, int64_t max,
+                              int64_t *n);
+
+/* Information about a handle. */
+typedef struct {
+  int64_t steps;        /* steps taken since create / set_state            */
+  double t;             /* simulated time                                  */
+  int32_t nx, ny;
+  int32_t precision;
+  int32_t pitch;        /* elements between rows of a device field         */
+  int64_t field_offset; /* elements from a field's base to cell (0, 0)     */
+  int64_t device_bytes; /* device memory held by the handle                */
+  int32_t bands, segments, warps_per_block; /* launch shape of the step    */
+} swe_info;
+swe_status swe_get_info(const swe_state *s, swe_info *info);
+
+/* Device pointers of the current state's fields (h, qx, qy, hC, H), for
+ * zero-copy inspection on the device.  Cell (i, j) of field k is at
+ * ptrs[k] + field_offset + j*pitch + i (see swe_info).  The pointers stay
+ * owned by the handle and change after every step (double buffering). */
+swe_status swe_device_fields(swe_state *s, void **ptrs);
+
+/* Release every resource of the handle.  NULL is accepted. */
+void swe_destroy(swe_state *s);
+
+/* Static English description of a status code. */
+const char *swe_status_str(swe_status st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWE_H */

@@ -1,0 +1,68 @@
+"""Helpers shared by the GPU tests: run a workload through the C ABI and
+through the oracle on the same seeded inputs, and compare."""
+import numpy as np
+
+import oracle as O
+from finite_volume_shallow_gb300 import inputs as I
+from finite_volume_shallow_gb300 import swe as S
+
+# tolerances: max |gpu - oracle| / max |oracle| per field, and relative dt
+TOL = {
+    64: {"h": 1e-10, "qx": 1e-10, "qy": 1e-10, "hC": 1e-10, "dt": 1e-12},
+    32: {"h": 1e-4, "qx": 1e-3, "qy": 1e-3, "hC": 1e-3, "dt": 1e-6},
+}
+
+
+def np_dtype(precision):
+    return np.float32 if precision == 32 else np.float64
+
+
+def gpu_create(d, precision, cfl=None, stream=None):
+    dt = np_dtype(precision)
+    return S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(dt),
+                             [f.astype(dt) for f in I.fields_of(d)], precision=precision,
+                             g=d["g"], cfl=d["cfl"] if cfl is None else cfl, stream=stream)
+
+
+def gpu_run(d, precision, nsteps, use_run=False):
+    """(fields as fp64, dts, t) after nsteps GPU steps."""
+    st = gpu_create(d, precision)
+    if use_run:
+        S.swe_run(st, nsteps)
+        dts = S.swe_get_dt_history(st, nsteps)
+    else:
+        dts = np.array([S.swe_step(st, d["cfl"]) for _ in range(nsteps)])
+    W, t = S.swe_get_state(st)
+    S.swe_destroy(st)
+    return [w.astype(np.float64) for w in W], np.asarray(dts), t
+
+
+def oracle_run(d, precision, nsteps):
+    """The oracle on the same inputs (rounded to the GPU's precision)."""
+    dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
+    W, dts, st = O.grid_run1(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields_of(dr),
+                             d["g"], d["cfl"], nsteps)
+    assert st == O.OM_OK, st
+    return W, dts
+
+
+def rel_errors(W_gpu, W_ref):
+    out = {}
+    for k, a, b in zip(("h", "qx", "qy", "hC"), W_gpu, W_ref):
+        scale = max(np.abs(b).max(), 1e-30)
+        out[k] = float(np.abs(a - b).max() / scale)
+    return out
+
+
+def assert_parity(d, precision, nsteps, use_run=False):
+    Wg, dtg, tg = gpu_run(d, precision, nsteps, use_run=use_run)
+    Wo, dto = oracle_run(d, precision, nsteps)
+    tol = TOL[precision]
+    errs = rel_errors(Wg, Wo)
+    for k in ("h", "qx", "qy", "hC"):
+        assert errs[k] <= tol[k], (k, errs)
+    assert len(dtg) == len(dto) == nsteps
+    dte = float(np.abs(dtg / dto - 1.0).max())
+    assert dte <= tol["dt"], dte
+    assert abs(tg - dto.sum()) <= tol["dt"] * dto.sum()
+    return errs, dte

@@ -1,0 +1,121 @@
+"""libswe loads and exports every function that include/swe.h declares, and
+rejects bad arguments before it touches the GPU (no compute calls here)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from finite_volume_shallow_gb300 import build as B
+from finite_volume_shallow_gb300 import swe as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swe_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return S.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("swe_create_grid", "swe_step", "swe_run", "swe_get_state", "swe_set_state",
+                 "swe_get_dt_history", "swe_get_info", "swe_device_fields", "swe_destroy",
+                 "swe_status_str"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    handle = C.CDLL(B.LIB)
+    for name in declared_functions():
+        assert hasattr(handle, name), name
+
+
+def test_library_is_for_sm103a():
+    out = open(B.LIB, "rb").read()
+    assert b"sm_103a" in out or b"sm_103" in out
+
+
+def test_status_strings(lib):
+    for code in range(-8, 1):
+        s = S.swe_status_str(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert S.swe_status_str(-99) == "unknown status"
+
+
+def _grid(nx=4, ny=3, dx=1.0, dy=1.0):
+    return S._Grid(nx, ny, dx, dy)
+
+
+def _params(**kw):
+    p = dict(n_layers=1, precision=64, pollutant=1, g=9.81, r=0.0, cfl=0.9, stream=None)
+    p.update(kw)
+    return S._Params(p["n_layers"], p["precision"], p["pollutant"], p["g"], p["r"], p["cfl"],
+                     p["stream"])
+
+
+def _create(lib, grid, params, n=12, with_fields=True):
+    H = np.zeros(n)
+    W = [np.ones(n), np.zeros(n), np.zeros(n), np.zeros(n)]
+    Wp = (C.c_void_p * 4)(*[w.ctypes.data for w in W]) if with_fields else None
+    out = C.c_void_p(123)
+    st = lib.swe_create_grid(C.byref(grid) if grid is not None else None,
+                             C.c_void_p(H.ctypes.data), Wp,
+                             C.byref(params) if params is not None else None, C.byref(out))
+    return st, out.value
+
+
+@pytest.mark.parametrize("grid,params,expect", [
+    (None, _params(), S.SWE_ERR_ARG),
+    (_grid(), None, S.SWE_ERR_ARG),
+    (_grid(nx=0), _params(), S.SWE_ERR_ARG),
+    (_grid(ny=-3), _params(), S.SWE_ERR_ARG),
+    (_grid(dx=0.0), _params(), S.SWE_ERR_ARG),
+    (_grid(dy=float("nan")), _params(), S.SWE_ERR_ARG),
+    (_grid(), _params(precision=16), S.SWE_ERR_ARG),
+    (_grid(), _params(g=-1.0), S.SWE_ERR_ARG),
+    (_grid(), _params(cfl=0.0), S.SWE_ERR_ARG),
+    (_grid(), _params(cfl=1.5), S.SWE_ERR_ARG),
+    (_grid(), _params(n_layers=3), S.SWE_ERR_ARG),
+    (_grid(), _params(n_layers=2), S.SWE_ERR_UNSUPPORTED),
+    (_grid(), _params(pollutant=0), S.SWE_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_arguments(lib, grid, params, expect):
+    st, out = _create(lib, grid, params)
+    assert st == expect
+    assert out is None   # *out is cleared on failure
+
+
+def test_create_rejects_missing_fields(lib):
+    st, out = _create(lib, _grid(), _params(), with_fields=False)
+    assert st == S.SWE_ERR_ARG and out is None
+
+
+def test_null_handles(lib):
+    lib.swe_destroy(None)
+    assert lib.swe_step(None, C.c_double(0.9), None) == S.SWE_ERR_ARG
+    assert lib.swe_run(None, 1) == S.SWE_ERR_ARG
+    assert lib.swe_get_state(None, None, None) == S.SWE_ERR_ARG
+    assert lib.swe_set_state(None, None, C.c_double(0.0)) == S.SWE_ERR_ARG
+    n = C.c_int64()
+    assert lib.swe_get_dt_history(None, None, 0, C.byref(n)) == S.SWE_ERR_ARG
+    assert lib.swe_get_info(None, None) == S.SWE_ERR_ARG
+    assert lib.swe_device_fields(None, None) == S.SWE_ERR_ARG
+
+
+def test_binding_checks_host_arrays(lib):
+    with pytest.raises(ValueError):
+        S._host_ptr(np.zeros(5, dtype=np.float32), np.float64, 5)
+    with pytest.raises(ValueError):
+        S._host_ptr(np.zeros(6), np.float64, 5)
+    with pytest.raises(ValueError):
+        S._host_ptr(np.zeros((4, 4))[:, 0], np.float64, 4)

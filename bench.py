@@ -66,6 +66,10 @@ def parse():
     p.add_argument("--precision", type=int, choices=[32, 64], default=None)
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--nx", type=int, default=None, help="reduced grid (same recipe)")
+    p.add_argument("--ny", type=int, default=None)
+    p.add_argument("--no-clocks", action="store_true",
+                   help="skip the nvidia-smi clock window (profiling runs)")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -215,7 +219,7 @@ def run_reference(args, rank, world):
     import oracle as O
     from finite_volume_shallow_gb300 import inputs as I
 
-    d = I.make_workload(args.workload)
+    d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
     precision = args.precision or d["precision"]
     nx = d["nx"]
     cal_rows = min(d["ny"], 16)
@@ -274,7 +278,7 @@ def main():
             torch.distributed.barrier()
 
     S.load()
-    d = I.make_workload(args.workload)
+    d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
     precision = args.precision or d["precision"]
     npdt = np.float32 if precision == 32 else np.float64
     tdt = torch.float32 if precision == 32 else torch.float64
@@ -297,9 +301,9 @@ def main():
     # the same steps runs untimed right before it so the clock record covers
     # the kernel even when the timed region is shorter than the sampling period
     sampler = ClockSampler(physical_gpu(local))
-    sampler.start()
-    pre = int(min(5000, 0.5 / max(est, 1e-6)))
-    if pre:
+    if not args.no_clocks:
+        sampler.start()
+        pre = int(min(5000, 0.5 / max(est, 1e-6)))
         S.swe_run(st, pre)
     barrier()
     torch.cuda.synchronize()
@@ -311,8 +315,10 @@ def main():
     torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
-    rows = sampler.stop()
-    clocks = ClockSampler.summarise(rows, None)
+    if args.no_clocks:
+        clocks = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled (--no-clocks)"]}
+    else:
+        clocks = ClockSampler.summarise(sampler.stop(), None)
 
     t = torch.tensor([ms], device="cuda", dtype=torch.float64)
     if world > 1:
@@ -363,7 +369,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_NAME[precision], "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}"
+                                   + (f", reduced to {d['nx']}x{d['ny']}" if args.nx or args.ny
+                                      else ""),
                        "cells": n, "nx": d["nx"], "ny": d["ny"], "parallelism": "replicas",
                        "l2": "inputs larger than L2" if n * BYTES_PER_CELL[precision] > 129e6
                              else "inputs fit in L2 (no flush)",

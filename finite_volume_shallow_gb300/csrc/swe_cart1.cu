@@ -47,13 +47,31 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 template <typename T> struct Fm;
+// fp32: the MUFU approximations (relative error of a few ulp; the fp32
+// tolerances of the method are orders of magnitude looser).
 template <> struct Fm<float> {
-  __device__ static __forceinline__ float rsq(float x) { return rsqrtf(x); }
-  __device__ static __forceinline__ float rcp(float x) { return __frcp_rn(x); }
+  __device__ static __forceinline__ float rsq(float x) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+  }
+  __device__ static __forceinline__ float rcp(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+  }
 };
 template <> struct Fm<double> {
   __device__ static __forceinline__ double rsq(double x) { return rsqrt(x); }
   __device__ static __forceinline__ double rcp(double x) { return __drcp_rn(x); }
+};
+
+template <typename T> struct Lim;
+template <> struct Lim<float> {
+  __device__ static __forceinline__ float max() { return 3.402823466e38f; }
+};
+template <> struct Lim<double> {
+  __device__ static __forceinline__ double max() { return 1.7976931348623157e308; }
 };
 
 // ---------------------------------------------------------------------------
@@ -110,104 +128,167 @@ __device__ __forceinline__ void fence_proxy_async() {
 constexpr long long kWaitCycles = 4000000000LL;
 
 // ---------------------------------------------------------------------------
-// vector moves of one lane's cells
-template <typename T, int N>
-__device__ __forceinline__ void lds_cells(const unsigned char* p, T (&a)[N]) {
-  if constexpr (std::is_same<T, float>::value) {
-    static_assert(N == 4, "four floats per lane");
-    float4 v = *reinterpret_cast<const float4*>(p);
-    a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-  } else {
-    static_assert(N == 2, "two doubles per lane");
-    double2 v = *reinterpret_cast<const double2*>(p);
-    a[0] = v.x; a[1] = v.y;
-  }
+// Scalar operations with explicit rounding (never contracted into FMAs), so
+// the host-loaded dt pass reproduces the fused kernel's wave speeds exactly.
+__device__ __forceinline__ float sadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ double sadd(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ float smul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double smul(double a, double b) { return __dmul_rn(a, b); }
+__device__ __forceinline__ float sfma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+__device__ __forceinline__ double sfma(double a, double b, double c) { return __fma_rn(a, b, c); }
+
+// ---------------------------------------------------------------------------
+// Pairs: the two cells of a lane.  fp32 pairs use the packed FP32x2 pipe
+// (one FADD2/FMUL2/FFMA2 per operation on both cells); fp64 pairs are two
+// scalar operations.
+template <typename T> struct PairOf;
+template <> struct PairOf<float> { using type = float2; };
+template <> struct PairOf<double> { using type = double2; };
+template <typename T> using Pr = typename PairOf<T>::type;
+
+__device__ __forceinline__ float2 pr(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ double2 pr(double a, double b) { return make_double2(a, b); }
+template <typename T> __device__ __forceinline__ Pr<T> psplat(T v) { return pr(v, v); }
+
+__device__ __forceinline__ float2 padd(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 pmul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 psub(float2 a, float2 b) {
+  return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
 }
-template <typename T, int N>
-__device__ __forceinline__ void stg_cells(T* p, const T (&a)[N]) {
-  if constexpr (std::is_same<T, float>::value) {
-    *reinterpret_cast<float4*>(p) = make_float4(a[0], a[1], a[2], a[3]);
-  } else {
-    *reinterpret_cast<double2*>(p) = make_double2(a[0], a[1]);
-  }
+__device__ __forceinline__ double2 padd(double2 a, double2 b) {
+  return pr(__dadd_rn(a.x, b.x), __dadd_rn(a.y, b.y));
+}
+__device__ __forceinline__ double2 pmul(double2 a, double2 b) {
+  return pr(__dmul_rn(a.x, b.x), __dmul_rn(a.y, b.y));
+}
+__device__ __forceinline__ double2 pfma(double2 a, double2 b, double2 c) {
+  return pr(__fma_rn(a.x, b.x, c.x), __fma_rn(a.y, b.y, c.y));
+}
+__device__ __forceinline__ double2 psub(double2 a, double2 b) {
+  return pr(__dsub_rn(a.x, b.x), __dsub_rn(a.y, b.y));
+}
+template <typename P> __device__ __forceinline__ P pneg(P a) { return pr(-a.x, -a.y); }
+template <typename P> __device__ __forceinline__ P pabs(P a) { return pr(fabs(a.x), fabs(a.y)); }
+template <typename T> __device__ __forceinline__ Pr<T> prsq(Pr<T> a) {
+  return pr(Fm<T>::rsq(a.x), Fm<T>::rsq(a.y));
+}
+template <typename T> __device__ __forceinline__ Pr<T> prcp(Pr<T> a) {
+  return pr(Fm<T>::rcp(a.x), Fm<T>::rcp(a.y));
+}
+template <typename P> __device__ __forceinline__ P pshup(P a) {  // (left lane's y, own x)
+  return pr(__shfl_up_sync(kFull, a.y, 1), a.x);
 }
 
 template <typename T>
 __device__ __forceinline__ T shdn(T v) { return __shfl_down_sync(kFull, v, 1); }
+
 template <typename T>
-__device__ __forceinline__ T shup(T v) { return __shfl_up_sync(kFull, v, 1); }
+__device__ __forceinline__ Pr<T> lds_pair(const unsigned char* p) {
+  return *reinterpret_cast<const Pr<T>*>(p);
+}
 
 // ---------------------------------------------------------------------------
-// One side of an edge in the frame of the edge normal eta:
+// Two edges (one per component) seen in the frame of their normals eta:
 // depth h, s = sqrt(h), v = q_eta / sqrt(h), normal discharge q_eta,
 // qu = q_eta^2 / h, tangential velocity ut, concentration C, bottom H.
 template <typename T>
-struct Side {
-  T h, s, v, qn, qu, ut, C, H;
+struct SideP {
+  Pr<T> h, s, v, qn, qu, ut, C, H;
 };
-// Reflective wall: the ghost has the normal discharge negated.
+// Reflective wall: the ghost is the cell with its normal discharge negated.
 template <typename T>
-__device__ __forceinline__ Side<T> mirror(const Side<T>& a) {
-  Side<T> m = a;
-  m.v = -a.v;
-  m.qn = -a.qn;
+__device__ __forceinline__ SideP<T> mirror(const SideP<T>& a) {
+  SideP<T> m = a;
+  m.v = pneg(a.v);
+  m.qn = pneg(a.qn);
   return m;
 }
-
-// Contributions of one edge (left/lower cell a, right/upper cell b):
-//   m   mass flux Phi^-[1] (to a: +m, to b: -m)
-//   pm  (P^- d)[2]: normal-momentum fluctuation of a
-//   dm  d[2] - (P^- d)[2]: normal-momentum fluctuation of b
-//   t   tangential momentum flux m * u_t^* (to a: +t, to b: -t)
-//   c   pollutant flux m * C^* (to a: +c, to b: -c)
+// the same, for one component only (k = 0: .x, 1: .y)
 template <typename T>
-struct EdgeF {
-  T m, pm, dm, t, c;
+__device__ __forceinline__ void mirror_into(SideP<T>& dst, const SideP<T>& src, int k) {
+  if (k == 0) {
+    dst.h.x = src.h.x; dst.s.x = src.s.x; dst.v.x = -src.v.x; dst.qn.x = -src.qn.x;
+    dst.qu.x = src.qu.x; dst.ut.x = src.ut.x; dst.C.x = src.C.x; dst.H.x = src.H.x;
+  } else {
+    dst.h.y = src.h.y; dst.s.y = src.s.y; dst.v.y = -src.v.y; dst.qn.y = -src.qn.y;
+    dst.qu.y = src.qu.y; dst.ut.y = src.ut.y; dst.C.y = src.C.y; dst.H.y = src.H.y;
+  }
+}
+
+// Contributions of a pair of edges (left/lower cell a, right/upper cell b):
+//   m     mass flux Phi^-[1]                 a: +m   b: -m
+//   pm    (P^- d)[2], normal momentum        a: +pm
+//   dsum  (P^- d)[2] - d[2]                  b: -dsum  (= (P^+ d)[2])
+//   t     tangential momentum m u_t^*        a: +t   b: -t
+//   c     pollutant m C^*                    a: +c   b: -c
+template <typename T>
+struct FluxP {
+  Pr<T> m, pm, dsum, t, c;
 };
 
 template <typename T>
-__device__ __forceinline__ EdgeF<T> roe_edge(const Side<T>& a, const Side<T>& b, T gh) {
+__device__ __forceinline__ T sgn_weight(T l) {  // (1 - sgn l) / 2, sgn 0 = 0
+  return (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
+}
+
+template <typename T>
+__device__ __forceinline__ FluxP<T> roe_pair(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
+  using P = Pr<T>;
   // Roe averages: sqrt(h)-weighted normal velocity, arithmetic depth;
-  // eigenvalues u -+ c of A_ij, c^2 = g hbar.
-  const T un = (a.v + b.v) * Fm<T>::rcp(a.s + b.s);
-  const T c2 = gh * (a.h + b.h);
-  const T rc = Fm<T>::rsq(c2);
-  const T c = c2 * rc;
-  const T i2c = T(0.5) * rc;
-  const T l1 = un - c;
-  const T l2 = un + c;
+  // eigenvalues l1,2 = u -+ c of A_ij with c^2 = g hbar.
+  const P un = pmul(padd(a.v, b.v), prcp<T>(padd(a.s, b.s)));
+  const P c2 = pmul(gh, padd(a.h, b.h));
+  const P rc = prsq<T>(c2);
+  const P c = pmul(c2, rc);
+  const P i2c = pmul(psplat<T>(T(0.5)), rc);
+  const P l1 = psub(un, c);
+  const P l2 = padd(un, c);
   // d = F_1(W_j) - F_1(W_i) - S_ij (H_j - H_i); the pressure difference
-  // g/2 (h_j^2 - h_i^2) is written g hbar (h_j - h_i).
-  const T dH = b.H - a.H;
-  const T d0 = b.qn - a.qn;
-  const T d1 = (b.qu - a.qu) + c2 * ((b.h - a.h) - dH);
-  // alpha = K^-1 d with K = [[1, 1], [l1, l2]]; P^- d = sum_k w_k alpha_k K_k,
-  // w_k = (1 - sgn l_k) / 2 with sgn 0 = 0.
-  const T a1 = (l2 * d0 - d1) * i2c;
-  const T a2 = (d1 - l1 * d0) * i2c;
-  const T w1 = (l1 < T(0)) ? T(1) : ((l1 > T(0)) ? T(0) : T(0.5));
-  const T w2 = (l2 < T(0)) ? T(1) : ((l2 > T(0)) ? T(0) : T(0.5));
-  const T b1 = w1 * a1;
-  const T b2 = w2 * a2;
-  EdgeF<T> f;
-  f.m = (a.qn + b1) + b2;
-  f.pm = b1 * l1 + b2 * l2;
-  f.dm = d1 - f.pm;
-  const bool up = f.m > T(0);
-  f.t = f.m * (up ? a.ut : b.ut);
-  f.c = f.m * (up ? a.C : b.C);
+  // g/2 (h_j^2 - h_i^2) is written g hbar (h_j - h_i).  d1n = -d[2].
+  const P d0 = psub(b.qn, a.qn);
+  const P d1n = pfma(c2, psub(psub(b.H, a.H), psub(b.h, a.h)), psub(a.qu, b.qu));
+  // alpha = K^-1 d with K = [[1, 1], [l1, l2]]
+  const P a1 = pmul(pfma(l2, d0, d1n), i2c);
+  FluxP<T> f;
+  const bool subcritical = (l1.x < T(0)) & (l1.y < T(0)) & (l2.x > T(0)) & (l2.y > T(0));
+  if (__all_sync(kFull, subcritical)) {
+    // P^- d = alpha_1 K_1: the general branch below with w = (1, 0),
+    // bit for bit
+    f.m = padd(a.qn, a1);
+    f.pm = pmul(a1, l1);
+  } else {
+    const P a2n = pmul(pfma(l1, d0, d1n), i2c);  // -alpha_2
+    const P b1 = pmul(pr(sgn_weight(l1.x), sgn_weight(l1.y)), a1);
+    const P b2n = pmul(pr(sgn_weight(l2.x), sgn_weight(l2.y)), a2n);
+    f.m = psub(padd(a.qn, b1), b2n);
+    f.pm = psub(pmul(b1, l1), pmul(b2n, l2));
+  }
+  f.dsum = padd(d1n, f.pm);
+  // passive upwinding of the tangential velocity and the concentration
+  const P ut = pr(f.m.x > T(0) ? a.ut.x : b.ut.x, f.m.y > T(0) ? a.ut.y : b.ut.y);
+  const P cc = pr(f.m.x > T(0) ? a.C.x : b.C.x, f.m.y > T(0) ? a.C.y : b.C.y);
+  f.t = pmul(f.m, ut);
+  f.c = pmul(f.m, cc);
   return f;
 }
 
-// ||D_ij||_inf = |u_eta| + c of the Roe matrix of an edge (eq. (5)).
+// ||D_ij||_inf = |u_eta| + c of the Roe matrix of an edge (eq. (5)); the
+// pair form and the scalar form round identically.
 template <typename T>
-__device__ __forceinline__ T roe_speed(T ha, T sa, T va, T hb, T sb, T vb, T gh) {
-  const T un = (va + vb) * Fm<T>::rcp(sa + sb);
-  const T c2 = gh * (ha + hb);
-  return fabs(un) + c2 * Fm<T>::rsq(c2);
+__device__ __forceinline__ Pr<T> speed_pair(Pr<T> ha, Pr<T> sa, Pr<T> va, Pr<T> hb, Pr<T> sb,
+                                            Pr<T> vb, Pr<T> gh) {
+  const Pr<T> un = pmul(padd(va, vb), prcp<T>(padd(sa, sb)));
+  const Pr<T> c2 = pmul(gh, padd(ha, hb));
+  return pfma(c2, prsq<T>(c2), pabs(un));
+}
+template <typename T>
+__device__ __forceinline__ T speed_scalar(T ha, T sa, T va, T hb, T sb, T vb, T gh) {
+  const T un = smul(sadd(va, vb), Fm<T>::rcp(sadd(sa, sb)));
+  const T c2 = smul(gh, sadd(ha, hb));
+  return sfma(c2, Fm<T>::rsq(c2), fabs(un));
 }
 
-// max that keeps a NaN once it has appeared
 template <typename T>
 __device__ __forceinline__ T nanmax(T acc, T x) {
   return (x > acc || x != x) ? x : acc;
@@ -229,274 +310,364 @@ template <typename T>
 __device__ __forceinline__ void warp_max_publish(T v, void* slot) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = nanmax(v, __shfl_xor_sync(kFull, v, o));
-  if ((threadIdx.x & 31) == 0 && v > T(0)) atomic_max_pos<T>(slot, v);
-  else if ((threadIdx.x & 31) == 0 && v != v) atomic_max_pos<T>(slot, v);
+  if ((threadIdx.x & 31) == 0 && (v > T(0) || v != v)) atomic_max_pos<T>(slot, v);
 }
 
 // ---------------------------------------------------------------------------
 // The fused step.  See the file comment.
+
+// W^n of one row of a lane (two cells) with the quantities its edges need,
+// and the residual the row accumulates (R.x, R.y: x and y momentum).
+template <typename T>
+struct RowN {
+  Pr<T> h, qx, qy, hC, H;
+  Pr<T> s, vx, vy, ux, uy, C, qux, quy;
+  Pr<T> Rm, Rx, Ry, Rc;
+};
+// W^{n+1} of one row: what the y-edge wave speeds need, and the row's
+// partial wave-speed sum.
+template <typename T>
+struct RowW {
+  Pr<T> h, s, vy, D;
+};
+
+template <typename T>
+__device__ __forceinline__ SideP<T> side_x(const RowN<T>& q) {
+  return SideP<T>{q.h, q.s, q.vx, q.qx, q.qux, q.uy, q.C, q.H};
+}
+template <typename T>
+__device__ __forceinline__ SideP<T> side_y(const RowN<T>& q) {
+  return SideP<T>{q.h, q.s, q.vy, q.qy, q.quy, q.ux, q.C, q.H};
+}
+
+// Everything a warp keeps while it marches.
+template <typename T>
+struct Ctx {
+  const StepArgs<T>* A;
+  unsigned char* wsm;
+  uint64_t* mbar;
+  int y0, y1, nrows, xb, lane;
+  int64_t col0;
+  unsigned own;  // bit 0 / 1: cell 0 / 1 of this lane is owned by this warp
+  Pr<T> gh, rho, nkdt;
+  T tmax;
+  unsigned flags;
+};
+
+template <typename T> constexpr uint32_t row_bytes() { return 64 * sizeof(T); }
+template <typename T> constexpr uint32_t stage_bytes() { return 2 * 5 * row_bytes<T>(); }
+
+// Stage s holds rows 2s and 2s+1 of the march: 5 fields each, copied by up
+// to ten lanes at once, completion on the stage's mbarrier.
+template <typename T>
+__device__ __forceinline__ void issue_stage(const Ctx<T>& c, int s) {
+  const int nr = min(2, c.nrows - 2 * s);
+  const int st = s % kStages;
+  const uint32_t bar = smem_u32(&c.mbar[st]);
+  if (c.lane == 0) mbar_expect_tx(bar, (uint32_t)nr * 5u * row_bytes<T>());
+  __syncwarp();
+  if (c.lane < 5 * nr) {
+    const StepArgs<T>& A = *c.A;
+    const int j = c.lane >= 5 ? 1 : 0;
+    const int f = c.lane - 5 * j;
+    const int r = c.y0 - 2 + 2 * s + j;
+    const T* src = f == 0 ? A.win[0] : f == 1 ? A.win[1] : f == 2 ? A.win[2]
+                 : f == 3 ? A.win[3] : A.H;
+    const int64_t off = (int64_t)(r + kPadY) * A.pitch + c.col0;
+    bulk_g2s(smem_u32(c.wsm + st * stage_bytes<T>() + (j * 5 + f) * row_bytes<T>()), src + off,
+             row_bytes<T>(), bar);
+  }
+}
+
+// x-edges of a row: edge pair (cell0|cell1, cell1|next lane's cell0).
+template <typename T, bool WALLX, bool INIT>
+__device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
+  SideP<T> a = side_x(q);
+  SideP<T> b;
+  b.h = pr(q.h.y, shdn(q.h.x));
+  b.s = pr(q.s.y, shdn(q.s.x));
+  b.v = pr(q.vx.y, shdn(q.vx.x));
+  b.qn = pr(q.qx.y, shdn(q.qx.x));
+  b.qu = pr(q.qux.y, shdn(q.qux.x));
+  b.ut = pr(q.uy.y, shdn(q.uy.x));
+  b.C = pr(q.C.y, shdn(q.C.x));
+  b.H = pr(q.H.y, shdn(q.H.x));
+  bool w0 = false, w1 = false;
+  if (WALLX) {
+    const int nx = c.A->nx;
+    if (c.xb == -1) { mirror_into(a, b, 0); w0 = true; }
+    else if (c.xb == nx - 1) { mirror_into(b, a, 0); w0 = true; }
+    if (c.xb + 1 == -1) { mirror_into(a, b, 1); w1 = true; }
+    else if (c.xb + 1 == nx - 1) { mirror_into(b, a, 1); w1 = true; }
+  }
+  FluxP<T> f = roe_pair<T>(a, b, c.gh);
+  if (WALLX) {
+    if (w0) { f.m.x = T(0); f.t.x = T(0); f.c.x = T(0); }
+    if (w1) { f.m.y = T(0); f.t.y = T(0); f.c.y = T(0); }
+  }
+  if (INIT) {
+    q.Rm = f.m; q.Rx = f.pm; q.Ry = f.t; q.Rc = f.c;
+  } else {
+    q.Rm = padd(q.Rm, f.m); q.Rx = padd(q.Rx, f.pm); q.Ry = padd(q.Ry, f.t); q.Rc = padd(q.Rc, f.c);
+  }
+  q.Rm = psub(q.Rm, pshup(f.m));
+  q.Rx = psub(q.Rx, pshup(f.dsum));
+  q.Ry = psub(q.Ry, pshup(f.t));
+  q.Rc = psub(q.Rc, pshup(f.c));
+}
+
+// y-edges between row p (below) and row q (above).  WALL: a horizontal
+// wall, `lower_is_ghost` telling which side is the real cell.
+template <typename T, bool ANISO, bool WALL>
+__device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q,
+                                           bool lower_is_ghost) {
+  SideP<T> a = side_y(p);
+  SideP<T> b = side_y(q);
+  if (WALL) {
+    if (lower_is_ghost) a = mirror(b);
+    else b = mirror(a);
+  }
+  FluxP<T> f = roe_pair<T>(a, b, c.gh);
+  if (WALL) {
+    f.m = psplat<T>(T(0)); f.t = f.m; f.c = f.m;
+  }
+  if (ANISO) {
+    f.m = pmul(f.m, c.rho); f.pm = pmul(f.pm, c.rho); f.dsum = pmul(f.dsum, c.rho);
+    f.t = pmul(f.t, c.rho); f.c = pmul(f.c, c.rho);
+  }
+  p.Rm = padd(p.Rm, f.m); p.Ry = padd(p.Ry, f.pm); p.Rx = padd(p.Rx, f.t); p.Rc = padd(p.Rc, f.c);
+  q.Rm = psub(q.Rm, f.m); q.Ry = psub(q.Ry, f.dsum); q.Rx = psub(q.Rx, f.t); q.Rc = psub(q.Rc, f.c);
+}
+
+// wave speeds of the y-edges between new rows u (below) and w (above)
+template <typename T, bool ANISO, bool WALL>
+__device__ __forceinline__ void row_yspeeds(const Ctx<T>& c, RowW<T>& u, RowW<T>& w,
+                                            bool lower_is_ghost) {
+  Pr<T> ha = u.h, sa = u.s, va = u.vy, hb = w.h, sb = w.s, vb = w.vy;
+  if (WALL) {
+    if (lower_is_ghost) { ha = hb; sa = sb; va = pneg(vb); }
+    else { hb = ha; sb = sa; vb = pneg(va); }
+  }
+  Pr<T> D = speed_pair<T>(ha, sa, va, hb, sb, vb, c.gh);
+  if (ANISO) D = pmul(D, c.rho);
+  u.D = padd(u.D, D);
+  w.D = padd(w.D, D);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T* p, Pr<T> v, unsigned own) {
+  if (own == 3u) *reinterpret_cast<Pr<T>*>(p) = v;
+  else if (own == 1u) p[0] = v.x;
+  else if (own == 2u) p[1] = v.y;
+}
+
+// One row of the march.  Row r = y0 - 2 + k arrives into q (p holds row
+// r-1); row r-1 is updated into w (u holds the new row r-2).
+//   STEADY  r in [y0+2, y1-1]: every part runs, no horizontal wall
+//   PAR     0 / 1: k even / odd; 2: decided at run time
+// Returns false if a bounded wait gave up.
+template <typename T, bool ANISO, bool WALLX, bool STEADY, int PAR>
+__device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>& q, RowW<T>& u,
+                                          RowW<T>& w) {
+  const StepArgs<T>& A = *c.A;
+  const int r = c.y0 - 2 + k;
+  const bool odd = PAR == 2 ? (k & 1) != 0 : PAR == 1;
+  const int s = k >> 1;
+  const int st = s % kStages;
+  // ---- a1: the row from shared memory ------------------------------------
+  if (!odd) {
+    const bool ok = mbar_wait_bounded(smem_u32(&c.mbar[st]), (uint32_t)((s / kStages) & 1),
+                                      kWaitCycles);
+    if (!__all_sync(kFull, ok)) return false;
+  }
+  {
+    const unsigned char* rowp = c.wsm + st * stage_bytes<T>() + (odd ? 5 : 0) * row_bytes<T>() +
+                                c.lane * 2 * sizeof(T);
+    q.h = lds_pair<T>(rowp + 0 * row_bytes<T>());
+    q.qx = lds_pair<T>(rowp + 1 * row_bytes<T>());
+    q.qy = lds_pair<T>(rowp + 2 * row_bytes<T>());
+    q.hC = lds_pair<T>(rowp + 3 * row_bytes<T>());
+    q.H = lds_pair<T>(rowp + 4 * row_bytes<T>());
+  }
+  if (odd || (!STEADY && k == c.nrows - 1)) {  // stage consumed: refill it
+    fence_proxy_async();
+    __syncwarp();
+    if (2 * (s + kStages) < c.nrows) issue_stage(c, s + kStages);
+  }
+  {
+    const Pr<T> rs = prsq<T>(q.h);
+    const Pr<T> ih = pmul(rs, rs);
+    q.s = pmul(q.h, rs);
+    q.vx = pmul(q.qx, rs);
+    q.vy = pmul(q.qy, rs);
+    q.ux = pmul(q.qx, ih);
+    q.uy = pmul(q.qy, ih);
+    q.C = pmul(q.hC, ih);
+    q.qux = pmul(q.qx, q.ux);
+    q.quy = pmul(q.qy, q.uy);
+  }
+  // ---- a2/a3: x-edges of row r, y-edges between rows r-1 and r ----------
+  if (STEADY) {
+    row_xedges<T, WALLX, true>(c, q);
+    row_yedges<T, ANISO, false>(c, p, q, false);
+  } else {
+    if (r >= c.y0 - 1 && r <= c.y1) {
+      row_xedges<T, WALLX, true>(c, q);
+    } else {
+      q.Rm = q.Rx = q.Ry = q.Rc = psplat<T>(T(0));
+    }
+    if (r >= c.y0 - 1) {
+      if (r == 0 || r == A.ny) row_yedges<T, ANISO, true>(c, p, q, r == 0);
+      else row_yedges<T, ANISO, false>(c, p, q, false);
+    }
+    if (r < c.y0) return true;
+  }
+  // ---- a5: update row r-1 (its residual is complete) ---------------------
+  const int rr = r - 1;
+  w.h = pfma(c.nkdt, p.Rm, p.h);
+  const Pr<T> nqx = pfma(c.nkdt, p.Rx, p.qx);
+  const Pr<T> nqy = pfma(c.nkdt, p.Ry, p.qy);
+  const Pr<T> nhC = pfma(c.nkdt, p.Rc, p.hC);
+  const bool owned_row = STEADY || (rr >= c.y0 && rr < c.y1);
+  if (owned_row) {
+    const Pr<T> sum = padd(padd(w.h, nqx), padd(nqy, nhC));
+    if (c.own & 1u) {
+      if (!(fabs(sum.x) <= Lim<T>::max())) c.flags |= kErrNonfinite;
+      if (!(w.h.x > T(0))) c.flags |= kErrDepth;
+    }
+    if (c.own & 2u) {
+      if (!(fabs(sum.y) <= Lim<T>::max())) c.flags |= kErrNonfinite;
+      if (!(w.h.y > T(0))) c.flags |= kErrDepth;
+    }
+    const int64_t off = (int64_t)(rr + kPadY) * A.pitch + c.col0 + 2 * c.lane;
+    store_pair<T>(A.wout[0] + off, w.h, c.own);
+    store_pair<T>(A.wout[1] + off, nqx, c.own);
+    store_pair<T>(A.wout[2] + off, nqy, c.own);
+    store_pair<T>(A.wout[3] + off, nhC, c.own);
+  }
+  // ---- a4: wave speeds of the new state ----------------------------------
+  Pr<T> nvx;
+  {
+    const Pr<T> rs = prsq<T>(w.h);
+    w.s = pmul(w.h, rs);
+    nvx = pmul(nqx, rs);
+    w.vy = pmul(nqy, rs);
+  }
+  if (owned_row) {  // x-edges of the new row
+    Pr<T> ha = w.h, sa = w.s, va = nvx;
+    Pr<T> hb = pr(w.h.y, shdn(w.h.x)), sb = pr(w.s.y, shdn(w.s.x)), vb = pr(nvx.y, shdn(nvx.x));
+    if (WALLX) {
+      const int nx = A.nx;
+      if (c.xb == -1) { ha.x = hb.x; sa.x = sb.x; va.x = -vb.x; }
+      else if (c.xb == nx - 1) { hb.x = ha.x; sb.x = sa.x; vb.x = -va.x; }
+      if (c.xb + 1 == -1) { ha.y = hb.y; sa.y = sb.y; va.y = -vb.y; }
+      else if (c.xb + 1 == nx - 1) { hb.y = ha.y; sb.y = sa.y; vb.y = -va.y; }
+    }
+    const Pr<T> D = speed_pair<T>(ha, sa, va, hb, sb, vb, c.gh);
+    w.D = padd(D, pshup(D));
+  } else {
+    w.D = psplat<T>(T(0));
+  }
+  if (STEADY || r >= c.y0 + 1) {  // y-edges between the new rows rr-1 and rr
+    if (!STEADY && (rr == 0 || rr == A.ny)) row_yspeeds<T, ANISO, true>(c, u, w, rr == 0);
+    else row_yspeeds<T, ANISO, false>(c, u, w, false);
+    if (STEADY || (rr - 1 >= c.y0 && rr - 1 < c.y1)) {
+      if (c.own & 1u) c.tmax = fmax(c.tmax, u.D.x);
+      if (c.own & 2u) c.tmax = fmax(c.tmax, u.D.y);
+    }
+  }
+  return true;
+}
+
+template <typename T, bool ANISO, bool WALLX>
+__device__ __forceinline__ bool general_row(Ctx<T>& c, int k, RowN<T>& P, RowN<T>& Q,
+                                            RowW<T>& U, RowW<T>& V) {
+  if (k & 1) return march_row<T, ANISO, WALLX, false, 2>(c, k, Q, P, V, U);
+  return march_row<T, ANISO, WALLX, false, 2>(c, k, P, Q, U, V);
+}
+
 template <typename T, bool ANISO, bool WALLX>
 __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, uint64_t* mbar,
                                       int band, int y0, int y1, T kdt) {
-  constexpr int CPT = Cpt<T>::v;
-  constexpr int WIN = 32 * CPT;
-  constexpr int OWN = WIN - 4;
-  constexpr uint32_t ROWB = WIN * sizeof(T);
-  constexpr uint32_t STAGEB = 5 * ROWB;
-  const int lane = threadIdx.x & 31;
-  const int nx = A.nx, ny = A.ny;
-  const T gh = A.ghalf;
-  const int xb = band * OWN - 2 + lane * CPT;  // logical column of cell 0
-  const int nrows = y1 - y0 + 4;               // rows y0-2 .. y1+1
-  const int64_t col0 = (int64_t)band * OWN;    // physical column of the window
-
-  unsigned own = 0;  // bit k: cell k of this lane is owned by this warp
+  constexpr int OWN = 64 - 4;
+  Ctx<T> c;
+  c.A = &A;
+  c.wsm = wsm;
+  c.mbar = mbar;
+  c.y0 = y0;
+  c.y1 = y1;
+  c.nrows = y1 - y0 + 4;  // rows y0-2 .. y1+1
+  c.lane = threadIdx.x & 31;
+  c.xb = band * OWN - 2 + 2 * c.lane;  // logical column of the lane's cell 0
+  c.col0 = (int64_t)band * OWN;        // physical column of the window
+  c.own = 0;
 #pragma unroll
-  for (int k = 0; k < CPT; ++k) {
-    const int x = xb + k;
-    if (x >= band * OWN && x < band * OWN + OWN && x < nx) own |= 1u << k;
+  for (int i = 0; i < 2; ++i) {
+    const int x = c.xb + i;
+    if (x >= band * OWN && x < band * OWN + OWN && x < A.nx) c.own |= 1u << i;
   }
-  const bool own_all = own == (1u << CPT) - 1u;
+  c.gh = psplat<T>(A.ghalf);
+  c.rho = psplat<T>(A.rho);
+  c.nkdt = psplat<T>(-kdt);
+  c.tmax = T(0);
+  c.flags = 0;
 
-  const T* src[5] = {A.win[0], A.win[1], A.win[2], A.win[3], A.H};
-  auto issue = [&](int k) {
-    const int st = k % kStages;
-    const int r = y0 - 2 + k;
-    const int64_t off = (int64_t)(r + kPadY) * A.pitch + col0;
-    const uint32_t bar = smem_u32(&mbar[st]);
-    mbar_expect_tx(bar, STAGEB);
-#pragma unroll
-    for (int f = 0; f < 5; ++f)
-      bulk_g2s(smem_u32(wsm + st * STAGEB + f * ROWB), src[f] + off, ROWB, bar);
-  };
-
-  if (lane == 0) {
+  const int nstages = (c.nrows + 1) / 2;
+  if (c.lane == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&mbar[st]), 1);
     mbar_init_fence();
-    for (int k = 0; k < kStages && k < nrows; ++k) issue(k);
   }
   __syncwarp();
+  for (int s = 0; s < kStages && s < nstages; ++s) issue_stage(c, s);
 
-  // W^n of the row below (r-1): what its y-edge with row r and its update need
-  T ph[CPT], ps[CPT], pvy[CPT], pqy[CPT], pquy[CPT], pux[CPT], pC[CPT], pH[CPT];
-  T pqx[CPT], phC[CPT];
-  // residuals of rows r-1 (R1) and r (R0)
-  T R1m[CPT], R1x[CPT], R1y[CPT], R1c[CPT];
-  // new state of row r-2 and its partial wave-speed sum
-  T n1h[CPT], n1s[CPT], n1vy[CPT], T1[CPT];
-  T tmax = T(0);
-#pragma unroll
-  for (int k = 0; k < CPT; ++k) {
-    ph[k] = ps[k] = pvy[k] = pqy[k] = pquy[k] = pux[k] = pC[k] = pH[k] = pqx[k] = phC[k] = T(0);
-    R1m[k] = R1x[k] = R1y[k] = R1c[k] = T(0);
-    n1h[k] = n1s[k] = n1vy[k] = T1[k] = T(0);
+  RowN<T> P, Q;
+  RowW<T> U, V;
+  P.h = P.qx = P.qy = P.hC = P.H = P.s = P.vx = P.vy = psplat<T>(T(0));
+  P.ux = P.uy = P.C = P.qux = P.quy = P.Rm = P.Rx = P.Ry = P.Rc = psplat<T>(T(0));
+  U.h = U.s = U.vy = U.D = psplat<T>(T(0));
+  // rows alternate between the two register sets: no copies between rows
+  int k = 0;
+  bool ok = true;
+  for (; k < 4 && k < c.nrows; ++k) {
+    ok = general_row<T, ANISO, WALLX>(c, k, P, Q, U, V);
+    if (!ok) break;
   }
-
-  for (int k = 0; k < nrows; ++k) {
-    const int r = y0 - 2 + k;
-    const int st = k % kStages;
-    // ---- a1: wait for the row, read it, release the stage --------------
-    bool ok = mbar_wait_bounded(smem_u32(&mbar[st]), (uint32_t)((k / kStages) & 1), kWaitCycles);
-    if (!__all_sync(kFull, ok)) {
-      // give up: report, then wait (bounded) for the copies still in flight
-      if (lane == 0) atomicOr(A.err, kErrTimeout);
-      for (int q = k; q < nrows && q < k + kStages; ++q)
-        (void)mbar_wait_bounded(smem_u32(&mbar[q % kStages]), (uint32_t)((q / kStages) & 1),
-                                kWaitCycles);
-      return;
-    }
-    T ch[CPT], cqx[CPT], cqy[CPT], chC[CPT], cH[CPT];
-    const unsigned char* rowp = wsm + st * STAGEB + lane * CPT * sizeof(T);
-    lds_cells<T, CPT>(rowp + 0 * ROWB, ch);
-    lds_cells<T, CPT>(rowp + 1 * ROWB, cqx);
-    lds_cells<T, CPT>(rowp + 2 * ROWB, cqy);
-    lds_cells<T, CPT>(rowp + 3 * ROWB, chC);
-    lds_cells<T, CPT>(rowp + 4 * ROWB, cH);
-    __syncwarp();
-    if (lane == 0 && k + kStages < nrows) {
-      fence_proxy_async();
-      issue(k + kStages);
-    }
-    // derived quantities of row r
-    T cs[CPT], cvx[CPT], cvy[CPT], cux[CPT], cuy[CPT], cC[CPT], cqux[CPT], cquy[CPT];
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      const T rs = Fm<T>::rsq(ch[i]);
-      const T ih = rs * rs;
-      cs[i] = ch[i] * rs;
-      cvx[i] = cqx[i] * rs;
-      cvy[i] = cqy[i] * rs;
-      cux[i] = cqx[i] * ih;
-      cuy[i] = cqy[i] * ih;
-      cC[i] = chC[i] * ih;
-      cqux[i] = cqx[i] * cux[i];
-      cquy[i] = cqy[i] * cuy[i];
-    }
-    T R0m[CPT], R0x[CPT], R0y[CPT], R0c[CPT];
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) R0m[i] = R0x[i] = R0y[i] = R0c[i] = T(0);
-
-    // ---- a2/a3: x-edges of row r (needed for rows y0-1 .. y1) ------------
-    if (r >= y0 - 1 && r <= y1) {
-      Side<T> nb;
-      nb.h = shdn(ch[0]); nb.s = shdn(cs[0]); nb.v = shdn(cvx[0]); nb.qn = shdn(cqx[0]);
-      nb.qu = shdn(cqux[0]); nb.ut = shdn(cuy[0]); nb.C = shdn(cC[0]); nb.H = shdn(cH[0]);
-      T cm = T(0), cx = T(0), cy = T(0), cc = T(0);
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        Side<T> a{ch[i], cs[i], cvx[i], cqx[i], cqux[i], cuy[i], cC[i], cH[i]};
-        Side<T> b;
-        if (i + 1 < CPT) b = Side<T>{ch[i + 1], cs[i + 1], cvx[i + 1], cqx[i + 1], cqux[i + 1],
-                                     cuy[i + 1], cC[i + 1], cH[i + 1]};
-        else b = nb;
-        bool wall = false;
-        if (WALLX) {
-          const int xl = xb + i;
-          if (xl == -1) { a = mirror(b); wall = true; }
-          else if (xl == nx - 1) { b = mirror(a); wall = true; }
-        }
-        EdgeF<T> f = roe_edge(a, b, gh);
-        if (WALLX && wall) { f.m = T(0); f.t = T(0); f.c = T(0); }
-        R0m[i] += f.m; R0x[i] += f.pm; R0y[i] += f.t; R0c[i] += f.c;
-        if (i + 1 < CPT) {
-          R0m[i + 1] -= f.m; R0x[i + 1] += f.dm; R0y[i + 1] -= f.t; R0c[i + 1] -= f.c;
-        } else {
-          cm = -f.m; cx = f.dm; cy = -f.t; cc = -f.c;
-        }
-      }
-      R0m[0] += shup(cm); R0x[0] += shup(cx); R0y[0] += shup(cy); R0c[0] += shup(cc);
-    }
-
-    // ---- a2/a3: y-edges between rows r-1 and r --------------------------
-    if (r >= y0 - 1) {
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        Side<T> a{ph[i], ps[i], pvy[i], pqy[i], pquy[i], pux[i], pC[i], pH[i]};
-        Side<T> b{ch[i], cs[i], cvy[i], cqy[i], cquy[i], cux[i], cC[i], cH[i]};
-        if (r == 0) a = mirror(b);
-        else if (r == ny) b = mirror(a);
-        EdgeF<T> f = roe_edge(a, b, gh);
-        if (r == 0 || r == ny) { f.m = T(0); f.t = T(0); f.c = T(0); }
-        if (ANISO) { f.m *= A.rho; f.pm *= A.rho; f.dm *= A.rho; f.t *= A.rho; f.c *= A.rho; }
-        R1m[i] += f.m; R1y[i] += f.pm; R1x[i] += f.t; R1c[i] += f.c;
-        R0m[i] -= f.m; R0y[i] += f.dm; R0x[i] -= f.t; R0c[i] -= f.c;
-      }
-    }
-
-    // ---- a5: update row r-1; a4: wave speeds of the new state ------------
-    if (r >= y0) {
-      const int rr = r - 1;
-      T nh[CPT], nqx[CPT], nqy[CPT], nhC[CPT];
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        nh[i] = ph[i] - kdt * R1m[i];
-        nqx[i] = pqx[i] - kdt * R1x[i];
-        nqy[i] = pqy[i] - kdt * R1y[i];
-        nhC[i] = phC[i] - kdt * R1c[i];
-      }
-      const bool owned_row = rr >= y0 && rr < y1;
-      if (owned_row) {
-        unsigned bad = 0;
-#pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-          if (own & (1u << i)) {
-            const bool fin = isfinite(nh[i]) && isfinite(nqx[i]) && isfinite(nqy[i]) &&
-                             isfinite(nhC[i]);
-            if (!fin) bad |= kErrNonfinite;
-            else if (!(nh[i] > T(0))) bad |= kErrDepth;
-          }
-        }
-        if (bad) atomicOr(A.err, bad);
-        const int64_t off = (int64_t)(rr + kPadY) * A.pitch + col0 + lane * CPT;
-        if (own_all) {
-          stg_cells<T, CPT>(A.wout[0] + off, nh);
-          stg_cells<T, CPT>(A.wout[1] + off, nqx);
-          stg_cells<T, CPT>(A.wout[2] + off, nqy);
-          stg_cells<T, CPT>(A.wout[3] + off, nhC);
-        } else if (own) {
-#pragma unroll
-          for (int i = 0; i < CPT; ++i) {
-            if (own & (1u << i)) {
-              A.wout[0][off + i] = nh[i];
-              A.wout[1][off + i] = nqx[i];
-              A.wout[2][off + i] = nqy[i];
-              A.wout[3][off + i] = nhC[i];
-            }
-          }
-        }
-      }
-      T ns[CPT], nvx[CPT], nvy[CPT], Tn[CPT];
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        const T rs = Fm<T>::rsq(nh[i]);
-        ns[i] = nh[i] * rs;
-        nvx[i] = nqx[i] * rs;
-        nvy[i] = nqy[i] * rs;
-        Tn[i] = T(0);
-      }
-      if (owned_row) {  // x-edges of the new row
-        const T bh = shdn(nh[0]), bs = shdn(ns[0]), bv = shdn(nvx[0]);
-        T carry = T(0);
-#pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-          T ha = nh[i], sa = ns[i], va = nvx[i];
-          T hb, sb, vb;
-          if (i + 1 < CPT) { hb = nh[i + 1]; sb = ns[i + 1]; vb = nvx[i + 1]; }
-          else { hb = bh; sb = bs; vb = bv; }
-          if (WALLX) {
-            const int xl = xb + i;
-            if (xl == -1) { ha = hb; sa = sb; va = -vb; }
-            else if (xl == nx - 1) { hb = ha; sb = sa; vb = -va; }
-          }
-          const T D = roe_speed(ha, sa, va, hb, sb, vb, gh);
-          Tn[i] += D;
-          if (i + 1 < CPT) Tn[i + 1] += D;
-          else carry = D;
-        }
-        Tn[0] += shup(carry);
-      }
-      if (r >= y0 + 1) {  // y-edges between the new rows rr-1 and rr
-#pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-          T ha = n1h[i], sa = n1s[i], va = n1vy[i];
-          T hb = nh[i], sb = ns[i], vb = nvy[i];
-          if (rr == 0) { ha = hb; sa = sb; va = -vb; }
-          else if (rr == ny) { hb = ha; sb = sa; vb = -va; }
-          T D = roe_speed(ha, sa, va, hb, sb, vb, gh);
-          if (ANISO) D *= A.rho;
-          T1[i] += D;
-          Tn[i] += D;
-        }
-        if (rr - 1 >= y0 && rr - 1 < y1) {
-#pragma unroll
-          for (int i = 0; i < CPT; ++i)
-            if (own & (1u << i)) tmax = nanmax(tmax, T1[i]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        n1h[i] = nh[i]; n1s[i] = ns[i]; n1vy[i] = nvy[i]; T1[i] = Tn[i];
-      }
-    }
-
-    // ---- shift the W^n rows ----------------------------------------------
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      ph[i] = ch[i]; ps[i] = cs[i]; pvy[i] = cvy[i]; pqy[i] = cqy[i]; pquy[i] = cquy[i];
-      pux[i] = cux[i]; pC[i] = cC[i]; pH[i] = cH[i]; pqx[i] = cqx[i]; phC[i] = chC[i];
-      R1m[i] = R0m[i]; R1x[i] = R0x[i]; R1y[i] = R0y[i]; R1c[i] = R0c[i];
-    }
+  for (; ok && k + 1 <= c.nrows - 3; k += 2) {
+    ok = march_row<T, ANISO, WALLX, true, 0>(c, k, P, Q, U, V);
+    if (!ok) break;
+    ok = march_row<T, ANISO, WALLX, true, 1>(c, k + 1, Q, P, V, U);
+    if (!ok) { ++k; break; }
   }
-  warp_max_publish<T>(tmax, A.tmax_out);
+  for (; ok && k < c.nrows; ++k) {
+    ok = general_row<T, ANISO, WALLX>(c, k, P, Q, U, V);
+    if (!ok) break;
+  }
+  if (!ok) {
+    // give up: report, then wait (bounded) for the copies still in flight
+    if (c.lane == 0) atomicOr(A.err, kErrTimeout);
+    const int s0 = k >> 1;
+    for (int s = s0; s < nstages && s < s0 + kStages; ++s)
+      (void)mbar_wait_bounded(smem_u32(&mbar[s % kStages]), (uint32_t)((s / kStages) & 1),
+                              kWaitCycles);
+    return;
+  }
+  if (c.flags) atomicOr(A.err, c.flags);
+  warp_max_publish<T>(c.tmax, A.tmax_out);
 }
 
+// Minimum resident blocks per SM the register allocation is held to: the
+// fp32 step fits 128 registers without spilling (16 warps per SM); the fp64
+// step needs about 230 and is bound by the FP64 pipe, not by latency.
+#ifndef SWE_STEP_MIN_BLOCKS_F32
+#define SWE_STEP_MIN_BLOCKS_F32 4
+#endif
+template <typename T> struct MinBlocks { static constexpr int v = 1; };
+template <> struct MinBlocks<float> { static constexpr int v = SWE_STEP_MIN_BLOCKS_F32; };
+
 template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
     cart1_step_kernel(const StepArgs<T> A) {
-  constexpr int CPT = Cpt<T>::v;
-  constexpr int WIN = 32 * CPT;
-  constexpr int OWN = WIN - 4;
-  constexpr uint32_t STAGEB = 5 * WIN * sizeof(T);
+  constexpr int OWN = 64 - 4;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
 
@@ -519,11 +690,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int seg = unit / A.nbands;
   const int y0 = (int)((int64_t)seg * A.ny / A.nsegs);
   const int y1 = (int)((int64_t)(seg + 1) * A.ny / A.nsegs);
-  unsigned char* wsm = smem + warp * (kStages * STAGEB);
+  unsigned char* wsm = smem + warp * (kStages * stage_bytes<T>());
   uint64_t* mbar =
-      reinterpret_cast<uint64_t*>(smem + kWarpsPerBlock * kStages * STAGEB) + warp * kStages;
+      reinterpret_cast<uint64_t*>(smem + kWarpsPerBlock * kStages * stage_bytes<T>()) +
+      warp * kStages;
   // bands whose window reaches a vertical wall take the checked path
-  const bool wallx = band == 0 || band * OWN + WIN - 2 > A.nx - 1;
+  const bool wallx = band == 0 || band * OWN + 64 - 2 > A.nx - 1;
   if (wallx) march<T, ANISO, true>(A, wsm, mbar, band, y0, y1, kdt);
   else march<T, ANISO, false>(A, wsm, mbar, band, y0, y1, kdt);
 }
@@ -537,9 +709,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 template <typename T>
 __device__ __forceinline__ void speed_inputs(T h, T qx, T qy, T& s, T& vx, T& vy) {
   const T rs = Fm<T>::rsq(h);
-  s = h * rs;
-  vx = qx * rs;
-  vy = qy * rs;
+  s = smul(h, rs);
+  vx = smul(qx, rs);
+  vy = smul(qy, rs);
 }
 
 template <typename T>
@@ -549,30 +721,27 @@ __global__ void cart1_dt0_kernel(const T* __restrict__ h, const T* __restrict__ 
                                  unsigned* err) {
   T tmax = T(0);
   unsigned bad = 0;
-  const int64_t n = (int64_t)nx * ny;
-  for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < n;
-       c += (int64_t)gridDim.x * blockDim.x) {
-    const int i = (int)(c % nx), j = (int)(c / nx);
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  for (int j = blockIdx.y; i < nx && j < ny; j += gridDim.y) {
     const int64_t o = (int64_t)(j + kPadY) * pitch + i + kPadX;
     const T h0 = h[o], x0 = qx[o], y0 = qy[o], c0 = hC[o];
     if (!(isfinite(h0) && isfinite(x0) && isfinite(y0) && isfinite(c0))) bad |= kErrNonfinite;
     else if (!(h0 > T(0))) bad |= kErrDepth;
-    T s0, vx0, vy0;
+    T s0, vx0, vy0, sn, vxn, vyn;
     speed_inputs(h0, x0, y0, s0, vx0, vy0);
-    T hn, sn, vxn, vyn;
     // west and east edges
     T hw = h0, sw = s0, vw = -vx0;
-    if (i > 0) { speed_inputs(h[o - 1], qx[o - 1], qy[o - 1], sn, vxn, vyn); hw = h[o - 1]; sw = sn; vw = vxn; }
+    if (i > 0) { hw = h[o - 1]; speed_inputs(hw, qx[o - 1], qy[o - 1], sn, vxn, vyn); sw = sn; vw = vxn; }
     T he = h0, se = s0, ve = -vx0;
-    if (i < nx - 1) { speed_inputs(h[o + 1], qx[o + 1], qy[o + 1], sn, vxn, vyn); he = h[o + 1]; se = sn; ve = vxn; }
+    if (i < nx - 1) { he = h[o + 1]; speed_inputs(he, qx[o + 1], qy[o + 1], sn, vxn, vyn); se = sn; ve = vxn; }
     // south and north edges
     T hs = h0, ss = s0, vs = -vy0;
-    if (j > 0) { hn = h[o - pitch]; speed_inputs(hn, qx[o - pitch], qy[o - pitch], sn, vxn, vyn); hs = hn; ss = sn; vs = vyn; }
+    if (j > 0) { hs = h[o - pitch]; speed_inputs(hs, qx[o - pitch], qy[o - pitch], sn, vxn, vyn); ss = sn; vs = vyn; }
     T hN = h0, sN = s0, vN = -vy0;
-    if (j < ny - 1) { hn = h[o + pitch]; speed_inputs(hn, qx[o + pitch], qy[o + pitch], sn, vxn, vyn); hN = hn; sN = sn; vN = vyn; }
-    T sum = roe_speed(hw, sw, vw, h0, s0, vx0, gh) + roe_speed(h0, s0, vx0, he, se, ve, gh);
-    sum += roe_speed(hs, ss, vs, h0, s0, vy0, gh) * rho;
-    sum += roe_speed(h0, s0, vy0, hN, sN, vN, gh) * rho;
+    if (j < ny - 1) { hN = h[o + pitch]; speed_inputs(hN, qx[o + pitch], qy[o + pitch], sn, vxn, vyn); sN = sn; vN = vyn; }
+    T sum = sadd(speed_scalar(h0, s0, vx0, he, se, ve, gh), speed_scalar(hw, sw, vw, h0, s0, vx0, gh));
+    sum = sadd(sum, smul(speed_scalar(hs, ss, vs, h0, s0, vy0, gh), rho));
+    sum = sadd(sum, smul(speed_scalar(h0, s0, vy0, hN, sN, vN, gh), rho));
     tmax = nanmax(tmax, sum);
   }
   if (bad) atomicOr(err, bad);
@@ -590,7 +759,7 @@ __global__ void fill_kernel(T* p, int64_t n, T v) {
 
 template <typename T>
 size_t step_smem_bytes() {
-  return (size_t)kWarpsPerBlock * kStages * 5 * band_window<T>() * sizeof(T) +
+  return (size_t)kWarpsPerBlock * kStages * stage_bytes<T>() +
          (size_t)kWarpsPerBlock * kStages * sizeof(uint64_t);
 }
 
@@ -623,11 +792,9 @@ template <typename T>
 cudaError_t launch_dt0(const T* const* w, const T* H, int nx, int ny, int pitch, T ghalf, T rho,
                        void* tmax_out, unsigned* err, cudaStream_t st) {
   (void)H;
-  const int64_t n = (int64_t)nx * ny;
-  int blocks = (int)((n + 255) / 256);
-  if (blocks > 4096) blocks = 4096;
-  cart1_dt0_kernel<T><<<blocks, 256, 0, st>>>(w[0], w[1], w[2], w[3], nx, ny, pitch, ghalf, rho,
-                                               tmax_out, err);
+  dim3 grid((unsigned)((nx + 127) / 128), (unsigned)(ny < 1024 ? ny : 1024));
+  cart1_dt0_kernel<T><<<grid, 128, 0, st>>>(w[0], w[1], w[2], w[3], nx, ny, pitch, ghalf, rho,
+                                            tmax_out, err);
   return cudaGetLastError();
 }
 

@@ -25,17 +25,22 @@ constexpr unsigned kErrDepth = 1u;
 constexpr unsigned kErrNonfinite = 2u;
 constexpr unsigned kErrTimeout = 4u;
 
-template <typename T> struct Cpt;
-template <> struct Cpt<float> { static constexpr int v = 4; };
-template <> struct Cpt<double> { static constexpr int v = 2; };
+// Every lane of the step kernel owns two adjacent cells of a row.
+template <typename T> struct Cpt { static constexpr int v = 2; };
 
 template <typename T> constexpr int cells_per_lane() { return Cpt<T>::v; }
 template <typename T> constexpr int band_window() { return 32 * Cpt<T>::v; }
 template <typename T> constexpr int band_owned() { return 32 * Cpt<T>::v - 4; }
 
 // Pipeline depth (rows in flight per warp) and warps per block of the step.
-constexpr int kStages = 4;
-constexpr int kWarpsPerBlock = 4;
+#ifndef SWE_STAGES
+#define SWE_STAGES 4
+#endif
+#ifndef SWE_WARPS_PER_BLOCK
+#define SWE_WARPS_PER_BLOCK 4
+#endif
+constexpr int kStages = SWE_STAGES;
+constexpr int kWarpsPerBlock = SWE_WARPS_PER_BLOCK;
 
 // Row pitch (elements) for an nx-wide grid of element type T.
 template <typename T>

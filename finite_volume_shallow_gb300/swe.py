@@ -77,12 +77,13 @@ def load(build_if_needed: bool = True):
     L.swe_get_dt_history.argtypes = [vp, vp, i64, C.POINTER(i64)]
     L.swe_get_info.argtypes = [vp, C.POINTER(_Info)]
     L.swe_device_fields.argtypes = [vp, vp]
+    L.swe_run_noalloc.argtypes = [C.POINTER(_Grid), C.POINTER(_Params), vp, vp, vp, i32, i64, vp]
     L.swe_destroy.argtypes = [vp]
     L.swe_destroy.restype = None
     L.swe_status_str.argtypes = [i32]
     L.swe_status_str.restype = C.c_char_p
     for name in ("swe_create_grid", "swe_step", "swe_run", "swe_get_state", "swe_set_state",
-                 "swe_get_dt_history", "swe_get_info", "swe_device_fields"):
+                 "swe_get_dt_history", "swe_get_info", "swe_device_fields", "swe_run_noalloc"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -205,6 +206,31 @@ def swe_device_fields(s: State):
     ptrs = (C.c_void_p * 5)()
     _check(load().swe_device_fields(s.ptr, ptrs), "swe_device_fields")
     return [p or 0 for p in ptrs]
+
+
+NOALLOC_MAX_STEPS = 1024
+
+
+def noalloc_pitch(nx) -> int:
+    """Smallest row pitch (elements) swe_run_noalloc accepts for nx columns."""
+    need = 60 * ((int(nx) + 59) // 60) + 4
+    return (need + 31) // 32 * 32
+
+
+def swe_run_noalloc(nx, ny, dx, dy, H, W_a, W_b, pitch, nsteps, precision=64, g=9.81,
+                    cfl=0.9, stream=None):
+    """Allocation-free run on caller-owned device buffers (see swe.h): H, W_a
+    (4) and W_b (4) are device addresses (ints) in the padded layout.
+    Returns the dt of each step."""
+    grid = _Grid(int(nx), int(ny), float(dx), float(dy))
+    params = _Params(1, int(precision), 1, float(g), 0.0, float(cfl),
+                     C.c_void_p(stream) if stream else None)
+    wa = (C.c_void_p * 4)(*[int(p) for p in W_a])
+    wb = (C.c_void_p * 4)(*[int(p) for p in W_b])
+    dts = np.zeros(max(int(nsteps), 1), dtype=np.float64)
+    _check(load().swe_run_noalloc(C.byref(grid), C.byref(params), C.c_void_p(int(H)), wa, wb,
+                                  int(pitch), int(nsteps), dts.ctypes.data), "swe_run_noalloc")
+    return dts[: int(nsteps)]
 
 
 def swe_destroy(s: State):

@@ -156,6 +156,46 @@ swe_status swe_get_info(const swe_state *s, swe_info *info);
  * owned by the handle and change after every step (double buffering). */
 swe_status swe_device_fields(swe_state *s, void **ptrs);
 
+/* Allocation-free time loop.  The papers have no counterpart of this entry
+ * point: it exists for callers that must not allocate device memory after
+ * start-up -- a framework whose memory pool already holds (nearly) all of the
+ * GPU's memory, where cudaMalloc would fail or fragment it, and real-time or
+ * embedded loops that forbid allocation because cudaMalloc can block and
+ * synchronise the device.  It runs nsteps steps of the same kernels as
+ * swe_run on buffers the caller owns, and allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *
+ *  grid, params  as for swe_create_grid (params.cfl is used for every step;
+ *                params.stream orders all work)
+ *  H             device, the bottom depth in the padded layout below
+ *  W_a           4 device pointers (h, qx, qy, hC), padded layout: the state
+ *                to advance on input, the state after nsteps steps on output
+ *  W_b           4 device pointers, padded layout: work buffers (overwritten)
+ *  pitch         elements per row of every field: a multiple of 32, at least
+ *                32 * ceil((60 * ceil(nx / 60) + 4) / 32)
+ *  nsteps        0 <= nsteps <= SWE_NOALLOC_MAX_STEPS
+ *  dts_out       host, nsteps doubles (may be NULL): dt of each step
+ * Padded layout: each field is (ny + 4) rows of `pitch` elements of the
+ * precision's type, 16-byte aligned; cell (i, j) is element
+ * (j + 2) * pitch + (i + 2).  The padding may hold anything; it is read but
+ * never affects a result and never written.
+ * The scratch (wave-speed maxima, error word, clock and the dt of at most
+ * SWE_NOALLOC_MAX_STEPS steps, about 8 KB) is one static device array per
+ * GPU, held from library load until exit.  Every call clears the parts that
+ * must start at zero; all calls share the array, so calls that overlap on the
+ * GPU (other streams, other threads) race and must be serialised.  The first
+ * call on a device also looks up the array's device address and sets the
+ * step kernel's launch attributes; make that first call before any stream
+ * capture.  The call waits for its stream before returning.
+ * Errors: SWE_ERR_ARG (bad argument, nsteps beyond SWE_NOALLOC_MAX_STEPS,
+ * pitch too small, unaligned buffer); SWE_ERR_DEPTH / SWE_ERR_NONFINITE for
+ * an invalid input state or one that appears (not sticky: nothing persists
+ * between calls); SWE_ERR_TIMEOUT, SWE_ERR_CUDA. */
+#define SWE_NOALLOC_MAX_STEPS 1024
+swe_status swe_run_noalloc(const swe_grid *grid, const swe_params *params,
+                           const void *H, void *const *W_a, void *const *W_b,
+                           int32_t pitch, int64_t nsteps, double *dts_out);
+
 /* Release every resource of the handle.  NULL is accepted. */
 void swe_destroy(swe_state *s);
 

@@ -119,3 +119,23 @@ def test_binding_checks_host_arrays(lib):
         S._host_ptr(np.zeros(6), np.float64, 5)
     with pytest.raises(ValueError):
         S._host_ptr(np.zeros((4, 4))[:, 0], np.float64, 4)
+
+
+def test_noalloc_rejects_bad_arguments_before_touching_the_gpu(lib):
+    # arguments are checked before any CUDA call (fake, aligned addresses)
+    fake = [0x10000 * (k + 1) for k in range(9)]
+    ok = dict(nx=64, ny=40, dx=1.0, dy=1.0, H=fake[0], W_a=fake[1:5], W_b=fake[5:9],
+              pitch=S.noalloc_pitch(64), nsteps=3)
+    cases = [dict(nsteps=S.NOALLOC_MAX_STEPS + 1), dict(nsteps=-1), dict(pitch=32),
+             dict(pitch=S.noalloc_pitch(64) + 8), dict(H=fake[0] + 4), dict(nx=0),
+             dict(dx=0.0)]
+    for bad in cases:
+        a = dict(ok, **bad)
+        with pytest.raises(S.SweError) as e:
+            S.swe_run_noalloc(a["nx"], a["ny"], a["dx"], a["dy"], a["H"], a["W_a"], a["W_b"],
+                              a["pitch"], a["nsteps"])
+        assert e.value.status == S.SWE_ERR_ARG, bad
+    with pytest.raises(S.SweError) as e:
+        S.swe_run_noalloc(64, 40, 1.0, 1.0, fake[0], fake[1:5], fake[5:9], S.noalloc_pitch(64), 3,
+                          precision=16)
+    assert e.value.status == S.SWE_ERR_ARG

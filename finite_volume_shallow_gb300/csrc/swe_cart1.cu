@@ -232,45 +232,76 @@ __device__ __forceinline__ T sgn_weight(T l) {  // (1 - sgn l) / 2, sgn 0 = 0
   return (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
 }
 
+// First half of the flux of a pair of edges: Roe averages (sqrt(h)-weighted
+// normal velocity, arithmetic depth), eigenvalues l1,2 = u -+ c of A_ij with
+// c^2 = g hbar, the fluctuation d = F_1(W_j) - F_1(W_i) - S_ij (H_j - H_i)
+// (the pressure difference g/2 (h_j^2 - h_i^2) written g hbar (h_j - h_i);
+// d1n = -d[2]) and alpha_1 of alpha = K^-1 d, K = [[1, 1], [l1, l2]].
 template <typename T>
-__device__ __forceinline__ FluxP<T> roe_pair(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
+struct RoeHead {
+  Pr<T> l1, l2, d0, d1n, a1, i2c;
+};
+template <typename T>
+__device__ __forceinline__ RoeHead<T> roe_head(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
   using P = Pr<T>;
-  // Roe averages: sqrt(h)-weighted normal velocity, arithmetic depth;
-  // eigenvalues l1,2 = u -+ c of A_ij with c^2 = g hbar.
+  RoeHead<T> e;
   const P un = pmul(padd(a.v, b.v), prcp<T>(padd(a.s, b.s)));
   const P c2 = pmul(gh, padd(a.h, b.h));
   const P rc = prsq<T>(c2);
   const P c = pmul(c2, rc);
-  const P i2c = pmul(psplat<T>(T(0.5)), rc);
-  const P l1 = psub(un, c);
-  const P l2 = padd(un, c);
-  // d = F_1(W_j) - F_1(W_i) - S_ij (H_j - H_i); the pressure difference
-  // g/2 (h_j^2 - h_i^2) is written g hbar (h_j - h_i).  d1n = -d[2].
-  const P d0 = psub(b.qn, a.qn);
-  const P d1n = pfma(c2, psub(psub(b.H, a.H), psub(b.h, a.h)), psub(a.qu, b.qu));
-  // alpha = K^-1 d with K = [[1, 1], [l1, l2]]
-  const P a1 = pmul(pfma(l2, d0, d1n), i2c);
+  e.i2c = pmul(psplat<T>(T(0.5)), rc);
+  e.l1 = psub(un, c);
+  e.l2 = padd(un, c);
+  e.d0 = psub(b.qn, a.qn);
+  e.d1n = pfma(c2, psub(psub(b.H, a.H), psub(b.h, a.h)), psub(a.qu, b.qu));
+  e.a1 = pmul(pfma(e.l2, e.d0, e.d1n), e.i2c);
+  return e;
+}
+template <typename T>
+__device__ __forceinline__ bool subcritical(const RoeHead<T>& e) {
+  return (e.l1.x < T(0)) & (e.l1.y < T(0)) & (e.l2.x > T(0)) & (e.l2.y > T(0));
+}
+// Second half: P^- d = sum_k w_k alpha_k K_k with w_k = (1 - sgn l_k) / 2.
+// `fast` (every edge of the warp has l1 < 0 < l2) takes w = (1, 0), which is
+// the general branch bit for bit.  Then the passive upwinding of the
+// tangential velocity and of the concentration.
+template <typename T>
+__device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>& a,
+                                             const SideP<T>& b, bool fast) {
+  using P = Pr<T>;
   FluxP<T> f;
-  const bool subcritical = (l1.x < T(0)) & (l1.y < T(0)) & (l2.x > T(0)) & (l2.y > T(0));
-  if (__all_sync(kFull, subcritical)) {
-    // P^- d = alpha_1 K_1: the general branch below with w = (1, 0),
-    // bit for bit
-    f.m = padd(a.qn, a1);
-    f.pm = pmul(a1, l1);
+  if (fast) {
+    f.m = padd(a.qn, e.a1);
+    f.pm = pmul(e.a1, e.l1);
   } else {
-    const P a2n = pmul(pfma(l1, d0, d1n), i2c);  // -alpha_2
-    const P b1 = pmul(pr(sgn_weight(l1.x), sgn_weight(l1.y)), a1);
-    const P b2n = pmul(pr(sgn_weight(l2.x), sgn_weight(l2.y)), a2n);
+    const P a2n = pmul(pfma(e.l1, e.d0, e.d1n), e.i2c);  // -alpha_2
+    const P b1 = pmul(pr(sgn_weight(e.l1.x), sgn_weight(e.l1.y)), e.a1);
+    const P b2n = pmul(pr(sgn_weight(e.l2.x), sgn_weight(e.l2.y)), a2n);
     f.m = psub(padd(a.qn, b1), b2n);
-    f.pm = psub(pmul(b1, l1), pmul(b2n, l2));
+    f.pm = psub(pmul(b1, e.l1), pmul(b2n, e.l2));
   }
-  f.dsum = padd(d1n, f.pm);
-  // passive upwinding of the tangential velocity and the concentration
+  f.dsum = padd(e.d1n, f.pm);
   const P ut = pr(f.m.x > T(0) ? a.ut.x : b.ut.x, f.m.y > T(0) ? a.ut.y : b.ut.y);
   const P cc = pr(f.m.x > T(0) ? a.C.x : b.C.x, f.m.y > T(0) ? a.C.y : b.C.y);
   f.t = pmul(f.m, ut);
   f.c = pmul(f.m, cc);
   return f;
+}
+template <typename T>
+__device__ __forceinline__ FluxP<T> roe_pair(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
+  const RoeHead<T> e = roe_head<T>(a, b, gh);
+  return roe_tail<T>(e, a, b, __all_sync(kFull, subcritical(e)));
+}
+// Two pairs at once (the x-edges and the y-edges of a row), one vote.
+template <typename T>
+__device__ __forceinline__ void roe_two(const SideP<T>& ax, const SideP<T>& bx,
+                                        const SideP<T>& ay, const SideP<T>& by, Pr<T> gh,
+                                        FluxP<T>& fx, FluxP<T>& fy) {
+  const RoeHead<T> ex = roe_head<T>(ax, bx, gh);
+  const RoeHead<T> ey = roe_head<T>(ay, by, gh);
+  const bool fast = __all_sync(kFull, subcritical(ex) & subcritical(ey));
+  fx = roe_tail<T>(ex, ax, bx, fast);
+  fy = roe_tail<T>(ey, ay, by, fast);
 }
 
 // ||D_ij||_inf = |u_eta| + c of the Roe matrix of an edge (eq. (5)); the
@@ -352,6 +383,12 @@ struct Ctx {
   Pr<T> gh, rho, nkdt;
   T tmax;
   unsigned flags;
+  Pr<T> nanacc;      // sum of (field sum * 0) over owned cells: 0 or NaN
+  T hmin;            // minimum new depth over owned cells
+  T* out[4];         // output fields at this lane's first cell of row 0
+  const T* src;      // lanes 0-9: field (lane % 5) of row (lane / 5) of stage 0
+  uint32_t dst_off;  // its offset inside a stage
+  int64_t src_step;  // elements between the same lane's rows of two stages
 };
 
 template <typename T> constexpr uint32_t row_bytes() { return 64 * sizeof(T); }
@@ -366,24 +403,17 @@ __device__ __forceinline__ void issue_stage(const Ctx<T>& c, int s) {
   const uint32_t bar = smem_u32(&c.mbar[st]);
   if (c.lane == 0) mbar_expect_tx(bar, (uint32_t)nr * 5u * row_bytes<T>());
   __syncwarp();
-  if (c.lane < 5 * nr) {
-    const StepArgs<T>& A = *c.A;
-    const int j = c.lane >= 5 ? 1 : 0;
-    const int f = c.lane - 5 * j;
-    const int r = c.y0 - 2 + 2 * s + j;
-    const T* src = f == 0 ? A.win[0] : f == 1 ? A.win[1] : f == 2 ? A.win[2]
-                 : f == 3 ? A.win[3] : A.H;
-    const int64_t off = (int64_t)(r + kPadY) * A.pitch + c.col0;
-    bulk_g2s(smem_u32(c.wsm + st * stage_bytes<T>() + (j * 5 + f) * row_bytes<T>()), src + off,
+  if (c.lane < 5 * nr)
+    bulk_g2s(smem_u32(c.wsm + st * stage_bytes<T>() + c.dst_off), c.src + s * c.src_step,
              row_bytes<T>(), bar);
-  }
 }
 
 // x-edges of a row: edge pair (cell0|cell1, cell1|next lane's cell0).
-template <typename T, bool WALLX, bool INIT>
-__device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
-  SideP<T> a = side_x(q);
-  SideP<T> b;
+// Vertical walls (WALLX bands) take the mirror state; w0/w1 mark them.
+template <typename T, bool WALLX>
+__device__ __forceinline__ void xsides(const Ctx<T>& c, const RowN<T>& q, SideP<T>& a,
+                                       SideP<T>& b, bool& w0, bool& w1) {
+  a = side_x(q);
   b.h = pr(q.h.y, shdn(q.h.x));
   b.s = pr(q.s.y, shdn(q.s.x));
   b.v = pr(q.vx.y, shdn(q.vx.x));
@@ -392,7 +422,8 @@ __device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
   b.ut = pr(q.uy.y, shdn(q.uy.x));
   b.C = pr(q.C.y, shdn(q.C.x));
   b.H = pr(q.H.y, shdn(q.H.x));
-  bool w0 = false, w1 = false;
+  w0 = false;
+  w1 = false;
   if (WALLX) {
     const int nx = c.A->nx;
     if (c.xb == -1) { mirror_into(a, b, 0); w0 = true; }
@@ -400,7 +431,9 @@ __device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
     if (c.xb + 1 == -1) { mirror_into(a, b, 1); w1 = true; }
     else if (c.xb + 1 == nx - 1) { mirror_into(b, a, 1); w1 = true; }
   }
-  FluxP<T> f = roe_pair<T>(a, b, c.gh);
+}
+template <typename T, bool WALLX, bool INIT>
+__device__ __forceinline__ void xaccum(RowN<T>& q, FluxP<T> f, bool w0, bool w1) {
   if (WALLX) {
     if (w0) { f.m.x = T(0); f.t.x = T(0); f.c.x = T(0); }
     if (w1) { f.m.y = T(0); f.t.y = T(0); f.c.y = T(0); }
@@ -415,19 +448,18 @@ __device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
   q.Ry = psub(q.Ry, pshup(f.t));
   q.Rc = psub(q.Rc, pshup(f.c));
 }
+template <typename T, bool WALLX, bool INIT>
+__device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
+  SideP<T> a, b;
+  bool w0, w1;
+  xsides<T, WALLX>(c, q, a, b, w0, w1);
+  xaccum<T, WALLX, INIT>(q, roe_pair<T>(a, b, c.gh), w0, w1);
+}
 
 // y-edges between row p (below) and row q (above).  WALL: a horizontal
 // wall, `lower_is_ghost` telling which side is the real cell.
 template <typename T, bool ANISO, bool WALL>
-__device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q,
-                                           bool lower_is_ghost) {
-  SideP<T> a = side_y(p);
-  SideP<T> b = side_y(q);
-  if (WALL) {
-    if (lower_is_ghost) a = mirror(b);
-    else b = mirror(a);
-  }
-  FluxP<T> f = roe_pair<T>(a, b, c.gh);
+__device__ __forceinline__ void yaccum(const Ctx<T>& c, RowN<T>& p, RowN<T>& q, FluxP<T> f) {
   if (WALL) {
     f.m = psplat<T>(T(0)); f.t = f.m; f.c = f.m;
   }
@@ -437,6 +469,31 @@ __device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>&
   }
   p.Rm = padd(p.Rm, f.m); p.Ry = padd(p.Ry, f.pm); p.Rx = padd(p.Rx, f.t); p.Rc = padd(p.Rc, f.c);
   q.Rm = psub(q.Rm, f.m); q.Ry = psub(q.Ry, f.dsum); q.Rx = psub(q.Rx, f.t); q.Rc = psub(q.Rc, f.c);
+}
+template <typename T, bool ANISO, bool WALL>
+__device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q,
+                                           bool lower_is_ghost) {
+  SideP<T> a = side_y(p);
+  SideP<T> b = side_y(q);
+  if (WALL) {
+    if (lower_is_ghost) a = mirror(b);
+    else b = mirror(a);
+  }
+  yaccum<T, ANISO, WALL>(c, p, q, roe_pair<T>(a, b, c.gh));
+}
+// Steady rows: the x-edges of row q and the y-edges between p and q
+// evaluated together (one vote, two independent streams of work).
+template <typename T, bool ANISO, bool WALLX>
+__device__ __forceinline__ void row_xyedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q) {
+  SideP<T> ax, bx;
+  bool w0, w1;
+  xsides<T, WALLX>(c, q, ax, bx, w0, w1);
+  const SideP<T> ay = side_y(p);
+  const SideP<T> by = side_y(q);
+  FluxP<T> fx, fy;
+  roe_two<T>(ax, bx, ay, by, c.gh, fx, fy);
+  xaccum<T, WALLX, true>(q, fx, w0, w1);
+  yaccum<T, ANISO, false>(c, p, q, fy);
 }
 
 // wave speeds of the y-edges between new rows u (below) and w (above)
@@ -452,13 +509,6 @@ __device__ __forceinline__ void row_yspeeds(const Ctx<T>& c, RowW<T>& u, RowW<T>
   if (ANISO) D = pmul(D, c.rho);
   u.D = padd(u.D, D);
   w.D = padd(w.D, D);
-}
-
-template <typename T>
-__device__ __forceinline__ void store_pair(T* p, Pr<T> v, unsigned own) {
-  if (own == 3u) *reinterpret_cast<Pr<T>*>(p) = v;
-  else if (own == 1u) p[0] = v.x;
-  else if (own == 2u) p[1] = v.y;
 }
 
 // One row of the march.  Row r = y0 - 2 + k arrives into q (p holds row
@@ -508,8 +558,7 @@ __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>&
   }
   // ---- a2/a3: x-edges of row r, y-edges between rows r-1 and r ----------
   if (STEADY) {
-    row_xedges<T, WALLX, true>(c, q);
-    row_yedges<T, ANISO, false>(c, p, q, false);
+    row_xyedges<T, ANISO, WALLX>(c, p, q);
   } else {
     if (r >= c.y0 - 1 && r <= c.y1) {
       row_xedges<T, WALLX, true>(c, q);
@@ -530,20 +579,28 @@ __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>&
   const Pr<T> nhC = pfma(c.nkdt, p.Rc, p.hC);
   const bool owned_row = STEADY || (rr >= c.y0 && rr < c.y1);
   if (owned_row) {
+    // checks: sum * 0 is 0 for finite values and NaN otherwise, so one
+    // accumulator flags any non-finite field; a running minimum of h flags a
+    // depth <= 0.  Both are read once, at the end of the march.
     const Pr<T> sum = padd(padd(w.h, nqx), padd(nqy, nhC));
-    if (c.own & 1u) {
-      if (!(fabs(sum.x) <= Lim<T>::max())) c.flags |= kErrNonfinite;
-      if (!(w.h.x > T(0))) c.flags |= kErrDepth;
+    const int64_t off = (int64_t)rr * A.pitch;
+    if (c.own == 3u) {
+      c.nanacc = pfma(sum, psplat<T>(T(0)), c.nanacc);
+      c.hmin = fmin(c.hmin, fmin(w.h.x, w.h.y));
+      *reinterpret_cast<Pr<T>*>(c.out[0] + off) = w.h;
+      *reinterpret_cast<Pr<T>*>(c.out[1] + off) = nqx;
+      *reinterpret_cast<Pr<T>*>(c.out[2] + off) = nqy;
+      *reinterpret_cast<Pr<T>*>(c.out[3] + off) = nhC;
+    } else if (c.own) {  // a lane holding the grid's last column only
+      const int i = c.own == 1u ? 0 : 1;
+      const T hs = i ? w.h.y : w.h.x;
+      c.nanacc.x = sfma(i ? sum.y : sum.x, T(0), c.nanacc.x);
+      c.hmin = fmin(c.hmin, hs);
+      c.out[0][off + i] = hs;
+      c.out[1][off + i] = i ? nqx.y : nqx.x;
+      c.out[2][off + i] = i ? nqy.y : nqy.x;
+      c.out[3][off + i] = i ? nhC.y : nhC.x;
     }
-    if (c.own & 2u) {
-      if (!(fabs(sum.y) <= Lim<T>::max())) c.flags |= kErrNonfinite;
-      if (!(w.h.y > T(0))) c.flags |= kErrDepth;
-    }
-    const int64_t off = (int64_t)(rr + kPadY) * A.pitch + c.col0 + 2 * c.lane;
-    store_pair<T>(A.wout[0] + off, w.h, c.own);
-    store_pair<T>(A.wout[1] + off, nqx, c.own);
-    store_pair<T>(A.wout[2] + off, nqy, c.own);
-    store_pair<T>(A.wout[3] + off, nhC, c.own);
   }
   // ---- a4: wave speeds of the new state ----------------------------------
   Pr<T> nvx;
@@ -611,6 +668,18 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
   c.nkdt = psplat<T>(-kdt);
   c.tmax = T(0);
   c.flags = 0;
+  c.nanacc = psplat<T>(T(0));
+  c.hmin = Lim<T>::max();
+  for (int f = 0; f < 4; ++f) c.out[f] = A.wout[f] + (int64_t)kPadY * A.pitch + c.col0 + 2 * c.lane;
+  {
+    const int j = c.lane >= 5 ? 1 : 0;
+    const int f = c.lane < 10 ? c.lane - 5 * j : 0;
+    const T* base = f == 0 ? A.win[0] : f == 1 ? A.win[1] : f == 2 ? A.win[2]
+                  : f == 3 ? A.win[3] : A.H;
+    c.src = base + (int64_t)(y0 - 2 + j + kPadY) * A.pitch + c.col0;
+    c.dst_off = (uint32_t)(j * 5 + f) * row_bytes<T>();
+    c.src_step = 2 * (int64_t)A.pitch;
+  }
 
   const int nstages = (c.nrows + 1) / 2;
   if (c.lane == 0) {
@@ -651,6 +720,8 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
                               kWaitCycles);
     return;
   }
+  if (!(c.nanacc.x == T(0) && c.nanacc.y == T(0))) c.flags |= kErrNonfinite;
+  if (!(c.hmin > T(0))) c.flags |= kErrDepth;
   if (c.flags) atomicOr(A.err, c.flags);
   warp_max_publish<T>(c.tmax, A.tmax_out);
 }

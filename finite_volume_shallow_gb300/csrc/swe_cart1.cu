@@ -120,6 +120,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Predicated forms: every lane executes the instruction, `on` selects the
+// lanes that act, so the stage refill has no divergent branch.
+__device__ __forceinline__ void mbar_expect_tx_if(bool on, uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"((uint32_t)on),
+      "r"(bar), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_if(bool on, uint32_t dst, const void* src,
+                                            uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%2], %3, [%4];"
+      "\n\t}" ::"r"((uint32_t)on),
+      "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -380,6 +398,7 @@ struct Ctx {
   int y0, y1, nrows, xb, lane;
   int64_t col0;
   unsigned own;  // bit 0 / 1: cell 0 / 1 of this lane is owned by this warp
+  bool partial;  // some lane of the warp owns one cell only (warp-uniform)
   Pr<T> gh, rho, nkdt;
   T tmax;
   unsigned flags;
@@ -401,11 +420,10 @@ __device__ __forceinline__ void issue_stage(const Ctx<T>& c, int s) {
   const int nr = min(2, c.nrows - 2 * s);
   const int st = s % kStages;
   const uint32_t bar = smem_u32(&c.mbar[st]);
-  if (c.lane == 0) mbar_expect_tx(bar, (uint32_t)nr * 5u * row_bytes<T>());
+  mbar_expect_tx_if(c.lane == 0, bar, (uint32_t)nr * 5u * row_bytes<T>());
   __syncwarp();
-  if (c.lane < 5 * nr)
-    bulk_g2s(smem_u32(c.wsm + st * stage_bytes<T>() + c.dst_off), c.src + s * c.src_step,
-             row_bytes<T>(), bar);
+  bulk_g2s_if(c.lane < 5 * nr, smem_u32(c.wsm + st * stage_bytes<T>() + c.dst_off),
+              c.src + s * c.src_step, row_bytes<T>(), bar);
 }
 
 // x-edges of a row: edge pair (cell0|cell1, cell1|next lane's cell0).
@@ -591,7 +609,8 @@ __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>&
       *reinterpret_cast<Pr<T>*>(c.out[1] + off) = nqx;
       *reinterpret_cast<Pr<T>*>(c.out[2] + off) = nqy;
       *reinterpret_cast<Pr<T>*>(c.out[3] + off) = nhC;
-    } else if (c.own) {  // a lane holding the grid's last column only
+    }
+    if (c.partial && (c.own == 1u || c.own == 2u)) {  // the grid's last column alone
       const int i = c.own == 1u ? 0 : 1;
       const T hs = i ? w.h.y : w.h.x;
       c.nanacc.x = sfma(i ? sum.y : sum.x, T(0), c.nanacc.x);
@@ -663,6 +682,7 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
     const int x = c.xb + i;
     if (x >= band * OWN && x < band * OWN + OWN && x < A.nx) c.own |= 1u << i;
   }
+  c.partial = __any_sync(kFull, c.own == 1u || c.own == 2u);
   c.gh = psplat<T>(A.ghalf);
   c.rho = psplat<T>(A.rho);
   c.nkdt = psplat<T>(-kdt);

@@ -345,3 +345,15 @@ def test_implicit_grid_equals_explicit_mesh():
     for a, b in zip(Wa, Wb):
         assert np.array_equal(a, b)
     assert O.grid_dt1(37, 29, d["dx"], d["dy"], d["H"], W0, G, 0.9) == dta[0]
+
+
+def test_update_at_selected_cells_equals_full_update():
+    d = I.make_workload("pulses8192", nx=31, ny=17)
+    m = O.grid_mesh(31, 17, d["dx"], d["dy"])
+    W0 = [d[k] for k in ("h", "qx", "qy", "hC")]
+    dt = O.dt1(m, d["H"], W0, G, 0.9)
+    Wf, st = O.update1(m, d["H"], W0, G, dt)
+    cells = np.array([0, 5, 30, 31, 263, 31 * 17 - 1])
+    sel = O.update1_at(m, d["H"], W0, G, dt, cells)
+    for k in range(4):
+        assert np.array_equal(sel[k], Wf[k][cells])

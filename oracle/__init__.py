@@ -28,6 +28,7 @@ OM_OK = 0
 OM_ERR_ARG = -1
 OM_ERR_DEPTH = -4
 OM_ERR_NONFINITE = -5
+OM_ERR_HYPERBOLIC = -6
 
 _lib = None
 
@@ -79,6 +80,26 @@ def lib():
         _lib.om_run1.restype = C.c_int
         _lib.om_run1.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, i64, vp, vp,
                                  C.POINTER(C.c_int64)]
+        _lib.om_wall_ghost2.restype = None
+        _lib.om_wall_ghost2.argtypes = [vp, d, d, vp]
+        _lib.om_roots2.restype = C.c_int
+        _lib.om_roots2.argtypes = [d, d, d, d, d, vp]
+        _lib.om_flux2.restype = C.c_int
+        _lib.om_flux2.argtypes = [vp, vp, d, d, d, d, d, d, vp, vp]
+        _lib.om_dt2.restype = d
+        _lib.om_dt2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, C.POINTER(C.c_int)]
+        _lib.om_update2.restype = C.c_int
+        _lib.om_update2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, vp]
+        _lib.om_run2.restype = C.c_int
+        _lib.om_run2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, i64, vp, vp,
+                                 C.POINTER(C.c_int64)]
+        _lib.om_grid_dt2.restype = d
+        _lib.om_grid_dt2.argtypes = [i64, i64, d, d, vp, vp, d, d, d, C.POINTER(C.c_int)]
+        _lib.om_grid_update2.restype = C.c_int
+        _lib.om_grid_update2.argtypes = [i64, i64, d, d, vp, vp, d, d, d, vp]
+        _lib.om_grid_run2.restype = C.c_int
+        _lib.om_grid_run2.argtypes = [i64, i64, d, d, vp, vp, d, d, d, i64, vp, vp,
+                                      C.POINTER(C.c_int64)]
         _lib.om_grid_dt1.restype = d
         _lib.om_grid_dt1.argtypes = [i64, i64, d, d, vp, vp, d, d]
         _lib.om_grid_update1.restype = C.c_int
@@ -138,14 +159,14 @@ def grid_mesh(nx, ny, dx, dy=None) -> Mesh:
 
 
 def _field_ptrs(W):
-    arr = (C.c_void_p * 4)(*[_ptr(w).value for w in W])
+    arr = (C.c_void_p * len(W))(*[_ptr(w).value for w in W])
     return arr
 
 
-def _fields(W, n):
+def _fields(W, n, k=4):
     out = [np.array(w, dtype=np.float64, copy=True).reshape(-1) for w in W]
-    if len(out) != 4 or any(w.size != n for w in out):
-        raise ValueError("expected four fields (h, qx, qy, hC) of n_cells values")
+    if len(out) != k or any(w.size != n for w in out):
+        raise ValueError(f"expected {k} fields of n_cells values")
     return out
 
 
@@ -247,3 +268,91 @@ def run_grid(d, nsteps=None, cfl=None):
     W = [d["h"], d["qx"], d["qy"], d["hC"]]
     Wf, dts, st, _ = run1(mesh, d["H"], W, d["g"], d["cfl"] if cfl is None else cfl, n)
     return Wf, dts, st
+
+
+# ---- two layers: W = (h1, q1x, q1y, h2, q2x, q2y) --------------------------
+
+def wall_ghost2(Wi, eta):
+    wi = np.ascontiguousarray(Wi, dtype=np.float64)
+    out = np.empty(6)
+    lib().om_wall_ghost2(_ptr(wi), float(eta[0]), float(eta[1]), _ptr(out))
+    return out
+
+
+def roots2(u1, u2, c1s, c2s, r):
+    """(status, eigenvalues ascending) of the 2-layer Roe matrix."""
+    lam = np.zeros(4)
+    st = lib().om_roots2(float(u1), float(u2), float(c1s), float(c2s), float(r), _ptr(lam))
+    return int(st), lam
+
+
+def flux2(Wi, Wj, Hi, Hj, eta, g, r):
+    """(status, F_ij^- (6 Cartesian components), ||D_ij||_inf)."""
+    wi = np.ascontiguousarray(Wi, dtype=np.float64)
+    wj = np.ascontiguousarray(Wj, dtype=np.float64)
+    F = np.zeros(6)
+    D = np.zeros(1)
+    st = lib().om_flux2(_ptr(wi), _ptr(wj), float(Hi), float(Hj), float(eta[0]), float(eta[1]),
+                        float(g), float(r), _ptr(F), _ptr(D))
+    return int(st), F, float(D[0])
+
+
+def dt2(mesh: Mesh, H, W, g, r, cfl):
+    Wf = _fields(W, mesh.n_cells, 6)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    st = C.c_int(0)
+    dt = lib().om_dt2(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(r), float(cfl),
+                      C.byref(st))
+    return float(dt), int(st.value)
+
+
+def update2(mesh: Mesh, H, W, g, r, dt):
+    Wf = _fields(W, mesh.n_cells, 6)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(6 * mesh.n_cells)
+    st = lib().om_update2(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(r), float(dt),
+                          _ptr(work))
+    return Wf, int(st)
+
+
+def run2(mesh: Mesh, H, W, g, r, cfl, nsteps):
+    Wf = _fields(W, mesh.n_cells, 6)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(6 * mesh.n_cells)
+    dts = np.zeros(max(int(nsteps), 1))
+    done = C.c_int64(0)
+    st = lib().om_run2(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(r), float(cfl),
+                       int(nsteps), _ptr(dts), _ptr(work), C.byref(done))
+    return Wf, dts[: done.value], int(st)
+
+
+def grid_dt2(nx, ny, dx, dy, H, W, g, r, cfl):
+    Wf = [np.ascontiguousarray(w, dtype=np.float64).reshape(-1) for w in W]
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    st = C.c_int(0)
+    dt = lib().om_grid_dt2(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf), _ptr(Hf),
+                           float(g), float(r), float(cfl), C.byref(st))
+    return float(dt), int(st.value)
+
+
+def grid_update2(nx, ny, dx, dy, H, W, g, r, dt):
+    n = int(nx) * int(ny)
+    Wf = _fields(W, n, 6)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(6 * n)
+    st = lib().om_grid_update2(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf),
+                               _ptr(Hf), float(g), float(r), float(dt), _ptr(work))
+    return Wf, int(st)
+
+
+def grid_run2(nx, ny, dx, dy, H, W, g, r, cfl, nsteps):
+    n = int(nx) * int(ny)
+    Wf = _fields(W, n, 6)
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    work = np.empty(6 * n)
+    dts = np.zeros(max(int(nsteps), 1))
+    done = C.c_int64(0)
+    st = lib().om_grid_run2(int(nx), int(ny), float(dx), float(dy), _field_ptrs(Wf), _ptr(Hf),
+                            float(g), float(r), float(cfl), int(nsteps), _ptr(dts), _ptr(work),
+                            C.byref(done))
+    return Wf, dts[: done.value], int(st)

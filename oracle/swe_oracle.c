@@ -338,3 +338,374 @@ int om_grid_run1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
   view v = grid_view(nx, ny, dx, dy);
   return run_view(&v, W, H, g, cfl, nsteps, dts, work, steps_done);
 }
+
+/* ======================================================================
+ * Two layers ([P1] Sec. 2.1 eq. (1), Sec. 2.2 steps 1-4 with four
+ * components in the normal frame).  W = (h1, q1x, q1y, h2, q2x, q2y).
+ * Readings: the density ratio r stripped from the garbled text is restored in
+ * the coupling of the lower layer (B: -r g h2 dh1) and in A_ij[3][0]; the
+ * wall ghost mirrors both layers.
+ * ====================================================================== */
+
+void om_wall_ghost2(const double *Wi, double ex, double ey, double *Wg) {
+  for (int k = 0; k < 2; ++k) {
+    const double *w = Wi + 3 * k;
+    double *o = Wg + 3 * k;
+    double qn = w[1] * ex + w[2] * ey;
+    o[0] = w[0];
+    o[1] = w[1] - 2.0 * qn * ex;
+    o[2] = w[2] - 2.0 * qn * ey;
+  }
+}
+
+/* p(l) = Q1(l) Q2(l) - r c1s c2s with Q_k(l) = (l - u_k)^2 - c_ks */
+typedef struct {
+  double u1, u2, c1s, c2s, r;
+} quartic;
+
+static double qk(double l, double u, double cs) { return (l - u) * (l - u) - cs; }
+static double pq(const quartic *q, double l) {
+  return qk(l, q->u1, q->c1s) * qk(l, q->u2, q->c2s) - q->r * q->c1s * q->c2s;
+}
+static double dpq(const quartic *q, double l) {
+  return 2.0 * (l - q->u1) * qk(l, q->u2, q->c2s) + 2.0 * (l - q->u2) * qk(l, q->u1, q->c1s);
+}
+
+/* bisection of f on [lo, hi] with f(lo) and f(hi) of opposite signs (or one
+ * of them zero) until the interval is a few ulp wide */
+static double bisect(const quartic *q, double (*f)(const quartic *, double), double lo,
+                     double hi) {
+  double flo = f(q, lo);
+  for (int it = 0; it < 200; ++it) {
+    double mid = 0.5 * (lo + hi);
+    if (!(mid > lo && mid < hi)) break;
+    double fm = f(q, mid);
+    if (fm == 0.0) return mid;
+    if ((fm > 0.0) == (flo > 0.0)) {
+      lo = mid;
+      flo = fm;
+    } else {
+      hi = mid;
+    }
+  }
+  return 0.5 * (lo + hi);
+}
+
+/* two Newton steps on p, kept inside [lo, hi] */
+static double polish(const quartic *q, double l, double lo, double hi) {
+  for (int it = 0; it < 2; ++it) {
+    double d = dpq(q, l);
+    if (d == 0.0) break;
+    double n = l - pq(q, l) / d;
+    if (n >= lo && n <= hi) l = n;
+  }
+  return l;
+}
+
+int om_roots2(double u1, double u2, double c1s, double c2s, double r, double *lam) {
+  quartic q = {u1, u2, c1s, c2s, r};
+  double c1 = sqrt(c1s), c2 = sqrt(c2s);
+  /* roots of Q1 Q2, sorted: p is -r c1s c2s <= 0 there */
+  double a[4] = {u1 - c1, u1 + c1, u2 - c2, u2 + c2};
+  for (int i = 1; i < 4; ++i)
+    for (int j = i; j > 0 && a[j - 1] > a[j]; --j) {
+      double t = a[j];
+      a[j] = a[j - 1];
+      a[j - 1] = t;
+    }
+  double step = c1 + c2;
+  /* p(a[k]) = -r c1s c2s <= 0; where rounding makes it non-negative (r = 0
+   * or a vanishing c_k) the root is a[k] itself */
+  /* outer roots: below a[0] and above a[3]; widen the bracket outward until
+   * p changes sign */
+  if (!(pq(&q, a[0]) < 0.0)) {
+    lam[0] = a[0];
+  } else {
+    double lo = a[0] - step;
+    while (pq(&q, lo) <= 0.0) {
+      step *= 2.0;
+      lo = a[0] - step;
+    }
+    lam[0] = polish(&q, bisect(&q, pq, lo, a[0]), lo, a[0]);
+  }
+  step = c1 + c2;
+  if (!(pq(&q, a[3]) < 0.0)) {
+    lam[3] = a[3];
+  } else {
+    double hi = a[3] + step;
+    while (pq(&q, hi) <= 0.0) {
+      step *= 2.0;
+      hi = a[3] + step;
+    }
+    lam[3] = polish(&q, bisect(&q, pq, a[3], hi), a[3], hi);
+  }
+  /* inner pair: p has its local maximum m in (a[1], a[2]) (p' > 0 at a[1],
+   * < 0 at a[2]); real roots need p(m) > 0 */
+  if (!(a[2] > a[1])) return OM_ERR_HYPERBOLIC;
+  double m = bisect(&q, dpq, a[1], a[2]);
+  if (!(pq(&q, m) > 0.0)) return OM_ERR_HYPERBOLIC;
+  lam[1] = (pq(&q, a[1]) < 0.0) ? polish(&q, bisect(&q, pq, a[1], m), a[1], m) : a[1];
+  lam[2] = (pq(&q, a[2]) < 0.0) ? polish(&q, bisect(&q, pq, m, a[2]), m, a[2]) : a[2];
+  return OM_OK;
+}
+
+/* inverse of a 4x4 matrix by Gauss-Jordan elimination with partial pivoting;
+ * returns 0 if singular */
+static int inv4(const double Min[4][4], double Inv[4][4]) {
+  double M[4][8];
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 8; ++j) M[i][j] = j < 4 ? Min[i][j] : (double)(j - 4 == i);
+  for (int col = 0; col < 4; ++col) {
+    int piv = col;
+    for (int i = col + 1; i < 4; ++i)
+      if (fabs(M[i][col]) > fabs(M[piv][col])) piv = i;
+    if (M[piv][col] == 0.0) return 0;
+    if (piv != col)
+      for (int j = 0; j < 8; ++j) {
+        double t = M[col][j];
+        M[col][j] = M[piv][j];
+        M[piv][j] = t;
+      }
+    double d = M[col][col];
+    for (int j = 0; j < 8; ++j) M[col][j] /= d;
+    for (int i = 0; i < 4; ++i) {
+      if (i == col) continue;
+      double f = M[i][col];
+      for (int j = 0; j < 8; ++j) M[i][j] -= f * M[col][j];
+    }
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) Inv[i][j] = M[i][j + 4];
+  return 1;
+}
+
+/* physical flux of one layer in the normal frame (mass, normal momentum) */
+static void flux_layer(double h, double qn, double g, double *F) {
+  F[0] = qn;
+  F[1] = qn * qn / h + 0.5 * g * h * h;
+}
+
+int om_flux2(const double *Wi, const double *Wj, double Hi, double Hj,
+             double ex, double ey, double g, double r, double *F, double *Dinf) {
+  /* step 1: W_eta = T_eta W for both layers */
+  double h[2][2], qn[2][2], qt[2][2], ux[2][2], uy[2][2];
+  const double *W[2] = {Wi, Wj};
+  for (int side = 0; side < 2; ++side)
+    for (int k = 0; k < 2; ++k) {
+      const double *w = W[side] + 3 * k;
+      h[side][k] = w[0];
+      qn[side][k] = w[1] * ex + w[2] * ey;
+      qt[side][k] = -w[1] * ey + w[2] * ex;
+      ux[side][k] = w[1] / w[0];
+      uy[side][k] = w[2] / w[0];
+    }
+  /* step 2: Roe averages per layer and the matrix A_ij */
+  double un[2], hb[2], cs[2];
+  for (int k = 0; k < 2; ++k) {
+    double si = sqrt(h[0][k]), sj = sqrt(h[1][k]);
+    double ax = (si * ux[0][k] + sj * ux[1][k]) / (si + sj);
+    double ay = (si * uy[0][k] + sj * uy[1][k]) / (si + sj);
+    un[k] = ax * ex + ay * ey;
+    hb[k] = 0.5 * (h[0][k] + h[1][k]);
+    cs[k] = g * hb[k];
+  }
+  /* A_ij = [[0, 1, 0, 0], [c1^2 - u1^2, 2 u1, c1^2, 0], [0, 0, 0, 1],
+   *         [r c2^2, 0, c2^2 - u2^2, 2 u2]] with c_k^2 = g hbar_k */
+  double lam[4];
+  int st = om_roots2(un[0], un[1], cs[0], cs[1], r, lam);
+  if (st != OM_OK) return st;
+  /* eigenvectors K_k = (1, l, Q1(l)/c1^2, l Q1(l)/c1^2) */
+  double K[4][4], Kinv[4][4];
+  for (int k = 0; k < 4; ++k) {
+    double mu = qk(lam[k], un[0], cs[0]) / cs[0];
+    K[0][k] = 1.0;
+    K[1][k] = lam[k];
+    K[2][k] = mu;
+    K[3][k] = lam[k] * mu;
+  }
+  if (!inv4(K, Kinv)) return OM_ERR_HYPERBOLIC;
+  /* P^- = 1/2 K (I - sgn D) K^-1 */
+  double w[4], P[4][4];
+  for (int k = 0; k < 4; ++k) w[k] = 0.5 * (1.0 - sgn(lam[k]));
+  for (int a = 0; a < 4; ++a)
+    for (int b = 0; b < 4; ++b) {
+      double acc = 0.0;
+      for (int k = 0; k < 4; ++k) acc += K[a][k] * w[k] * Kinv[k][b];
+      P[a][b] = acc;
+    }
+  /* d = F_1(W_j) - F_1(W_i) - B_ij (W_j - W_i) - S_ij (H_j - H_i) in the
+   * components [1, 2, 4, 5]: B couples -g h1 dh2 (upper) and -r g h2 dh1
+   * (lower); S = (0, g h1, 0, g h2) with Roe-averaged depths */
+  double Fi[4], Fj[4];
+  flux_layer(h[0][0], qn[0][0], g, Fi);
+  flux_layer(h[0][1], qn[0][1], g, Fi + 2);
+  flux_layer(h[1][0], qn[1][0], g, Fj);
+  flux_layer(h[1][1], qn[1][1], g, Fj + 2);
+  double dH = Hj - Hi;
+  double dh1 = h[1][0] - h[0][0], dh2 = h[1][1] - h[0][1];
+  double d[4];
+  d[0] = Fj[0] - Fi[0];
+  d[1] = Fj[1] - Fi[1] - (-g * hb[0] * dh2) - g * hb[0] * dH;
+  d[2] = Fj[2] - Fi[2];
+  d[3] = Fj[3] - Fi[3] - (-r * g * hb[1] * dh1) - g * hb[1] * dH;
+  /* Phi^- = P^- d + F_1(W_eta,i) */
+  double phi[4];
+  for (int a = 0; a < 4; ++a) {
+    double acc = 0.0;
+    for (int b = 0; b < 4; ++b) acc += P[a][b] * d[b];
+    phi[a] = acc + Fi[a];
+  }
+  /* step 3: tangential discharge of each layer upwinded with its mass flux */
+  double pt[2];
+  for (int k = 0; k < 2; ++k) {
+    double m = phi[2 * k];
+    double ut = (m > 0.0) ? qt[0][k] / h[0][k] : qt[1][k] / h[1][k];
+    pt[k] = m * ut;
+  }
+  /* step 4: back to Cartesian components */
+  for (int k = 0; k < 2; ++k) {
+    F[3 * k + 0] = phi[2 * k];
+    F[3 * k + 1] = phi[2 * k + 1] * ex - pt[k] * ey;
+    F[3 * k + 2] = phi[2 * k + 1] * ey + pt[k] * ex;
+  }
+  double dm = 0.0;
+  for (int k = 0; k < 4; ++k) dm = fmax(dm, fabs(lam[k]));
+  *Dinf = dm;
+  return OM_OK;
+}
+
+static int cell_terms2(const view *v, const double *const *W, const double *H, double g,
+                       double r, int64_t i, double Fl[6][OM_MAX_EDGES],
+                       double Dl[OM_MAX_EDGES], int *n_out) {
+  int64_t nbr[OM_MAX_EDGES];
+  double exs[OM_MAX_EDGES], eys[OM_MAX_EDGES], lens[OM_MAX_EDGES];
+  int n = view_edges(v, i, nbr, exs, eys, lens);
+  double Wi[6], Wj[6];
+  for (int k = 0; k < 6; ++k) Wi[k] = W[k][i];
+  for (int e = 0; e < n; ++e) {
+    double Hj;
+    if (nbr[e] >= 0) {
+      for (int k = 0; k < 6; ++k) Wj[k] = W[k][nbr[e]];
+      Hj = H[nbr[e]];
+    } else {
+      om_wall_ghost2(Wi, exs[e], eys[e], Wj);
+      Hj = H[i];
+    }
+    double F[6], D;
+    int st = om_flux2(Wi, Wj, H[i], Hj, exs[e], eys[e], g, r, F, &D);
+    if (st != OM_OK) return st;
+    for (int c = 0; c < 6; ++c) Fl[c][e] = lens[e] * F[c];
+    Dl[e] = lens[e] * D;
+  }
+  *n_out = n;
+  return OM_OK;
+}
+
+static double dt_view2(const view *v, const double *const *W, const double *H, double g,
+                       double r, double cfl, int *status) {
+  double dt = INFINITY;
+  double Fl[6][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
+  int64_t N = view_cells(v);
+  if (status) *status = OM_OK;
+  for (int64_t i = 0; i < N; ++i) {
+    int n;
+    int st = cell_terms2(v, W, H, g, r, i, Fl, Dl, &n);
+    if (st != OM_OK) {
+      if (status) *status = st;
+      return NAN;
+    }
+    double dti = 2.0 * cfl * view_area(v, i) / psum(Dl, n);
+    if (isnan(dti)) return dti;
+    if (dti < dt) dt = dti;
+  }
+  return dt;
+}
+
+static int check_state2(const double w[6]) {
+  for (int k = 0; k < 6; ++k)
+    if (!isfinite(w[k])) return OM_ERR_NONFINITE;
+  if (!(w[0] > 0.0) || !(w[3] > 0.0)) return OM_ERR_DEPTH;
+  return OM_OK;
+}
+
+static int update_view2(const view *v, double *const *W, const double *H, double g, double r,
+                        double dt, double *work) {
+  const double *const *Wc = (const double *const *)W;
+  double Fl[6][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
+  int64_t N = view_cells(v);
+  for (int64_t i = 0; i < N; ++i) {
+    int n;
+    int st = cell_terms2(v, Wc, H, g, r, i, Fl, Dl, &n);
+    if (st != OM_OK) return st;
+    for (int c = 0; c < 6; ++c)
+      work[c * N + i] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
+  }
+  int status = OM_OK;
+  for (int64_t i = 0; i < N; ++i) {
+    double w[6];
+    for (int c = 0; c < 6; ++c) {
+      w[c] = work[c * N + i];
+      W[c][i] = w[c];
+    }
+    int s = check_state2(w);
+    if (s != OM_OK && status == OM_OK) status = s;
+  }
+  return status;
+}
+
+static int run_view2(const view *v, double *const *W, const double *H, double g, double r,
+                     double cfl, int64_t nsteps, double *dts, double *work,
+                     int64_t *steps_done) {
+  int64_t done = 0;
+  int status = OM_OK;
+  for (int64_t n = 0; n < nsteps; ++n) {
+    int st = OM_OK;
+    double dt = dt_view2(v, (const double *const *)W, H, g, r, cfl, &st);
+    if (dts) dts[n] = dt;
+    if (st != OM_OK) {
+      status = st;
+      break;
+    }
+    if (!isfinite(dt) || !(dt > 0.0)) {
+      status = OM_ERR_NONFINITE;
+      break;
+    }
+    status = update_view2(v, W, H, g, r, dt, work);
+    ++done;
+    if (status != OM_OK) break;
+  }
+  if (steps_done) *steps_done = done;
+  return status;
+}
+
+double om_dt2(const om_mesh *m, const double *const *W, const double *H, double g, double r,
+              double cfl, int *status) {
+  view v = mesh_view(m);
+  return dt_view2(&v, W, H, g, r, cfl, status);
+}
+int om_update2(const om_mesh *m, double *const *W, const double *H, double g, double r,
+               double dt, double *work) {
+  view v = mesh_view(m);
+  return update_view2(&v, W, H, g, r, dt, work);
+}
+int om_run2(const om_mesh *m, double *const *W, const double *H, double g, double r,
+            double cfl, int64_t nsteps, double *dts, double *work, int64_t *steps_done) {
+  view v = mesh_view(m);
+  return run_view2(&v, W, H, g, r, cfl, nsteps, dts, work, steps_done);
+}
+double om_grid_dt2(int64_t nx, int64_t ny, double dx, double dy, const double *const *W,
+                   const double *H, double g, double r, double cfl, int *status) {
+  view v = grid_view(nx, ny, dx, dy);
+  return dt_view2(&v, W, H, g, r, cfl, status);
+}
+int om_grid_update2(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                    const double *H, double g, double r, double dt, double *work) {
+  view v = grid_view(nx, ny, dx, dy);
+  return update_view2(&v, W, H, g, r, dt, work);
+}
+int om_grid_run2(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                 const double *H, double g, double r, double cfl, int64_t nsteps,
+                 double *dts, double *work, int64_t *steps_done) {
+  view v = grid_view(nx, ny, dx, dy);
+  return run_view2(&v, W, H, g, r, cfl, nsteps, dts, work, steps_done);
+}

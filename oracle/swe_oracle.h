@@ -45,6 +45,7 @@ typedef struct {
 #define OM_ERR_DEPTH (-4)     /* a depth h <= 0 appeared */
 #define OM_ERR_NONFINITE (-5) /* a non-finite value appeared */
 #define OM_ERR_ARG (-1)
+#define OM_ERR_HYPERBOLIC (-6) /* the Roe matrix has complex eigenvalues */
 
 /* Number of edge entries of the nx x ny Cartesian grid as a polygon mesh. */
 int64_t om_grid_edges(int64_t nx, int64_t ny);
@@ -100,6 +101,42 @@ int om_grid_update1(int64_t nx, int64_t ny, double dx, double dy, double *const 
 int om_grid_run1(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
                  const double *H, double g, double cfl, int64_t nsteps, double *dts,
                  double *work, int64_t *steps_done);
+
+/* ---- two layers: W = (h1, q1x, q1y, h2, q2x, q2y), 1 = upper layer,
+ * r = rho1 / rho2 ([P1] Sec. 2.1 eq. (1)) ---------------------------------- */
+
+/* Mirror ghost of both layers at a wall with outward normal (ex, ey). */
+void om_wall_ghost2(const double *Wi, double ex, double ey, double *Wg);
+
+/* Real eigenvalues, ascending, of the 2-layer Roe matrix A_ij with averaged
+ * normal velocities u1, u2 and c1s = g hbar1, c2s = g hbar2: the roots of
+ * ((l - u1)^2 - c1s)((l - u2)^2 - c2s) - r c1s c2s.  Returns OM_OK or
+ * OM_ERR_HYPERBOLIC when the inner pair is complex. */
+int om_roots2(double u1, double u2, double c1s, double c2s, double r, double *lam);
+
+/* F_ij^- of eq. (4) for two layers (six Cartesian components) and
+ * ||D_ij||_inf.  Returns OM_OK or OM_ERR_HYPERBOLIC. */
+int om_flux2(const double *Wi, const double *Wj, double Hi, double Hj,
+             double ex, double ey, double g, double r, double *F, double *Dinf);
+
+/* eq. (5), eq. (4) and the time loop for two layers on a mesh or on the
+ * implicit nx x ny grid; W holds six field arrays.  dt2 reports a loss of
+ * hyperbolicity through *status (may be NULL). */
+double om_dt2(const om_mesh *m, const double *const *W, const double *H,
+              double g, double r, double cfl, int *status);
+int om_update2(const om_mesh *m, double *const *W, const double *H, double g,
+               double r, double dt, double *work);
+int om_run2(const om_mesh *m, double *const *W, const double *H, double g,
+            double r, double cfl, int64_t nsteps, double *dts, double *work,
+            int64_t *steps_done);
+double om_grid_dt2(int64_t nx, int64_t ny, double dx, double dy,
+                   const double *const *W, const double *H, double g, double r,
+                   double cfl, int *status);
+int om_grid_update2(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                    const double *H, double g, double r, double dt, double *work);
+int om_grid_run2(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
+                 const double *H, double g, double r, double cfl, int64_t nsteps,
+                 double *dts, double *work, int64_t *steps_done);
 
 #ifdef __cplusplus
 }

@@ -35,8 +35,9 @@ MUTANTS = {
                            "double Cs = (phi[0] > 0.0) ? Wj[3] / hj : Wi[3] / hi;"),
     # back-rotation with a transposed operator
     "back_rotation": ("F[1] = phi[1] * ex - phit * ey;", "F[1] = phi[1] * ex + phit * ey;"),
-    # hydrostatic pressure without its factor 1/2
-    "pressure_half": ("qn * qn / h + 0.5 * g * h * h", "qn * qn / h + g * h * h"),
+    # hydrostatic pressure without its factor 1/2 (one layer, two layers)
+    "pressure_half": ("qn * qn / h + 0.5 * g * h * h", "qn * qn / h + g * h * h", 0),
+    "pressure_half_2": ("qn * qn / h + 0.5 * g * h * h", "qn * qn / h + g * h * h", 1),
     # CFL without the factor 2 of eq. (5)
     "cfl_factor": ("double dti = 2.0 * cfl * view_area(v, i) / s;",
                    "double dti = cfl * view_area(v, i) / s;"),
@@ -46,11 +47,29 @@ MUTANTS = {
     # wrong neighbour index (North points South)
     "neighbour_index": ("static const int dj[4] = {0, 1, 0, -1};",
                         "static const int dj[4] = {0, -1, 0, -1};"),
-    # update with the wrong sign
+    # update with the wrong sign (one layer, then two layers)
     "update_sign": ("work[c * N + i] = W[c][i] - dt / view_area(v, i)",
-                    "work[c * N + i] = W[c][i] + dt / view_area(v, i)"),
+                    "work[c * N + i] = W[c][i] + dt / view_area(v, i)", 0),
+    "update_sign_2": ("work[c * N + i] = W[c][i] - dt / view_area(v, i)",
+                      "work[c * N + i] = W[c][i] + dt / view_area(v, i)", 1),
     # wall ghost that does not reflect the normal discharge
     "wall_no_reflect": ("Wg[1] = Wi[1] - 2.0 * qn * ex;", "Wg[1] = Wi[1];"),
+    # two layers: coupling term of the upper layer with the wrong sign
+    "coupling_sign": ("d[1] = Fj[1] - Fi[1] - (-g * hb[0] * dh2) - g * hb[0] * dH;",
+                      "d[1] = Fj[1] - Fi[1] + (-g * hb[0] * dh2) - g * hb[0] * dH;"),
+    # two layers: density ratio dropped from the lower layer's coupling
+    "coupling_no_r": ("d[3] = Fj[3] - Fi[3] - (-r * g * hb[1] * dh1) - g * hb[1] * dH;",
+                      "d[3] = Fj[3] - Fi[3] - (-g * hb[1] * dh1) - g * hb[1] * dH;"),
+    # two layers: eigenvectors built with the lower layer's Q
+    "eigvec_wrong_layer": ("double mu = qk(lam[k], un[0], cs[0]) / cs[0];",
+                           "double mu = qk(lam[k], un[1], cs[1]) / cs[0];"),
+    # two layers: P^+ instead of P^-
+    "p_plus_2": ("for (int k = 0; k < 4; ++k) w[k] = 0.5 * (1.0 - sgn(lam[k]));",
+                 "for (int k = 0; k < 4; ++k) w[k] = 0.5 * (1.0 + sgn(lam[k]));"),
+    # two layers: tangential velocity upwinded with the other layer's mass flux
+    "tangential_other_layer": ("double m = phi[2 * k];", "double m = phi[2 * (1 - k)];"),
+    # two layers: characteristic polynomial without the density ratio
+    "charpoly_no_r": ("- q->r * q->c1s * q->c2s;", "- q->c1s * q->c2s;"),
 }
 
 
@@ -61,18 +80,27 @@ def workdir(tmp_path_factory):
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_mutant(name, workdir):
-    old, new = MUTANTS[name]
+    old, new, *which = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site of {name} not found exactly once"
+    if which:   # the k-th of several identical sites
+        k = which[0]
+        pos = -1
+        for _ in range(k + 1):
+            pos = src.index(old, pos + 1)
+        mutated = src[:pos] + new + src[pos + len(old):]
+    else:
+        assert src.count(old) == 1, f"mutation site of {name} not found exactly once"
+        mutated = src.replace(old, new)
     d = workdir / name
     d.mkdir()
-    (d / "swe_oracle.c").write_text(src.replace(old, new))
+    (d / "swe_oracle.c").write_text(mutated)
     shutil.copy(HDR, d / "swe_oracle.h")
     so = d / "liboracle.so"
     subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
                     "-o", str(so), str(d / "swe_oracle.c"), "-lm"], check=True)
     env = dict(os.environ, SWE_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(HERE, "test_oracle_pins.py")],
+                        os.path.join(HERE, "test_oracle_pins.py"),
+                        os.path.join(HERE, "test_oracle_pins2.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

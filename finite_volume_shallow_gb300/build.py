@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswe.so")
-SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_noalloc.cu"]
+SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_cart2.cu", "swe_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "swe_internal.h"), os.path.join(ROOT, "include", "swe.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

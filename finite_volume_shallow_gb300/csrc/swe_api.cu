@@ -21,12 +21,16 @@ struct swe_state {
   double dx = 0, dy = 0;
   swe_params p{};
   int prec = 0;
+  int nl = 1;        // layers
+  int nf = 4;        // conserved fields: 4 (h, qx, qy, hC) or 6 (two layers)
   size_t esz = 0;
   int pitch = 0;
+  int64_t rows = 0;  // allocated rows per field
   int64_t field_stride = 0;  // elements between field bases in the allocation
   void* dev = nullptr;
   size_t dev_bytes = 0;
-  void* w[2][4] = {{nullptr}};
+  void* w[2][6] = {{nullptr}};  // one layer: two buffers of 4; two layers: w[0][0..5]
+  void* R[6] = {nullptr};        // two layers: residual scratch
   void* H = nullptr;
   void* slots = nullptr;      // 3 wave-speed maxima (8 bytes each)
   double* dt_hist = nullptr;
@@ -46,6 +50,7 @@ namespace {
 
 swe_status status_of_bits(unsigned bits) {
   if (bits & kErrTimeout) return SWE_ERR_TIMEOUT;
+  if (bits & kErrHyperbolic) return SWE_ERR_HYPERBOLIC;
   if (bits & kErrNonfinite) return SWE_ERR_NONFINITE;
   if (bits & kErrDepth) return SWE_ERR_DEPTH;
   return SWE_OK;
@@ -136,14 +141,61 @@ swe_status enqueue_step(swe_state* s, double cfl) {
   return SWE_OK;
 }
 
+// Two layers: the flux pass of step n reduces the wave-speed maximum of W^n
+// into slot n % 3 (zeroed by the update of step n - 1 or at set-up); the
+// update pass of step n reads it and zeroes slot (n + 1) % 3.
+template <typename T>
+swe_status enqueue_check2(swe_state* s) {
+  CK(cudaMemsetAsync(s->slots, 0, 3 * sizeof(uint64_t), s->stream));
+  Fields6<T> w;
+  for (int f = 0; f < 6; ++f) w.p[f] = (const T*)s->w[0][f];
+  CK(launch_check2<T>(w, s->nx, s->ny, s->pitch, s->err, s->stream));
+  return SWE_OK;
+}
+
+template <typename T>
+swe_status enqueue_step2(swe_state* s, double cfl) {
+  Step2Args<T> f;
+  Update2Args<T> u;
+  char* sl = (char*)s->slots;
+  for (int k = 0; k < 6; ++k) {
+    f.w[k] = (const T*)s->w[0][k];
+    f.R[k] = (T*)s->R[k];
+    u.w[k] = (T*)s->w[0][k];
+    u.R[k] = (const T*)s->R[k];
+  }
+  f.H = (const T*)s->H;
+  f.nx = u.nx = s->nx;
+  f.ny = u.ny = s->ny;
+  f.pitch = u.pitch = s->pitch;
+  f.g = (T)s->p.g;
+  f.r = (T)s->p.r;
+  f.rho = (T)(s->dx / s->dy);
+  f.tmax_out = sl + (s->step % 3) * sizeof(uint64_t);
+  f.err = u.err = s->err;
+  u.two_cfl = 2.0 * cfl;
+  u.dx = s->dx;
+  u.tmax_in = sl + (s->step % 3) * sizeof(uint64_t);
+  u.tmax_clear = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
+  u.dt_hist = s->dt_hist;
+  u.t_dev = s->t_dev;
+  u.step = s->step;
+  CK(launch_step2<T>(f, u, s->stream));
+  s->step += 1;
+  return SWE_OK;
+}
+
 swe_status enqueue_dt0_any(swe_state* s) {
+  if (s->nl == 2) return s->prec == 32 ? enqueue_check2<float>(s) : enqueue_check2<double>(s);
   return s->prec == 32 ? enqueue_dt0<float>(s) : enqueue_dt0<double>(s);
 }
 swe_status enqueue_step_any(swe_state* s, double cfl) {
+  if (s->nl == 2)
+    return s->prec == 32 ? enqueue_step2<float>(s, cfl) : enqueue_step2<double>(s, cfl);
   return s->prec == 32 ? enqueue_step<float>(s, cfl) : enqueue_step<double>(s, cfl);
 }
 
-// Copy 4 host fields (or H when n == 1) into the padded layout of `dst`.
+// Copy n host fields into the padded layout of `dst`.
 swe_status upload(swe_state* s, void* const* dst, const void* const* src, int n) {
   const size_t row = (size_t)s->nx * s->esz;
   const size_t dpitch = (size_t)s->pitch * s->esz;
@@ -165,10 +217,17 @@ bool finite_pos(double v) { return isfinite(v) && v > 0.0; }
 
 template <typename T>
 swe_status fill_pads(swe_state* s) {
-  // whole padded arrays: h = 1, everything else 0; interiors are then copied
+  // whole padded arrays: depths 1, everything else 0; interiors are then
+  // copied (a resting state in the padding keeps every padded edge benign)
   const int64_t n = s->field_stride;
-  for (int b = 0; b < 2; ++b)
-    for (int f = 0; f < 4; ++f) CK(launch_fill<T>((T*)s->w[b][f], n, f == 0 ? T(1) : T(0), s->stream));
+  const int nbuf = s->nl == 2 ? 1 : 2;
+  for (int b = 0; b < nbuf; ++b)
+    for (int f = 0; f < s->nf; ++f) {
+      const bool depth = f == 0 || (s->nl == 2 && f == 3);
+      CK(launch_fill<T>((T*)s->w[b][f], n, depth ? T(1) : T(0), s->stream));
+    }
+  if (s->nl == 2)
+    for (int f = 0; f < 6; ++f) CK(launch_fill<T>((T*)s->R[f], n, T(0), s->stream));
   CK(launch_fill<T>((T*)s->H, n, T(0), s->stream));
   return SWE_OK;
 }
@@ -205,16 +264,20 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   if (!out) return SWE_ERR_ARG;
   *out = nullptr;
   if (!grid || !H || !W0 || !params) return SWE_ERR_ARG;
-  for (int f = 0; f < 4; ++f)
+  const int nfields = params->n_layers == 2 ? 6 : 4;
+  for (int f = 0; f < nfields; ++f)
     if (!W0[f]) return SWE_ERR_ARG;
   if (grid->nx < 1 || grid->ny < 1) return SWE_ERR_ARG;
   if (!finite_pos(grid->dx) || !finite_pos(grid->dy)) return SWE_ERR_ARG;
   if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
   if (!finite_pos(params->g)) return SWE_ERR_ARG;
   if (!(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
-  if (params->n_layers == 2) return SWE_ERR_UNSUPPORTED;
-  if (params->n_layers != 1) return SWE_ERR_ARG;
-  if (params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->n_layers != 1 && params->n_layers != 2) return SWE_ERR_ARG;
+  if (params->n_layers == 1 && params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->n_layers == 2) {
+    if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
+    if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
+  }
   // index arithmetic inside the kernels is 32-bit per row and column
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
 
@@ -226,31 +289,51 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   s->dy = grid->dy;
   s->p = *params;
   s->prec = params->precision;
+  s->nl = params->n_layers;
+  s->nf = s->nl == 2 ? 6 : 4;
   s->esz = s->prec == 32 ? 4 : 8;
   s->stream = (cudaStream_t)params->stream;
-  s->pitch = (int)(s->prec == 32 ? grid_pitch<float>(s->nx) : grid_pitch<double>(s->nx));
+  if (s->nl == 1) {
+    s->pitch = (int)(s->prec == 32 ? grid_pitch<float>(s->nx) : grid_pitch<double>(s->nx));
+    s->rows = s->ny + 2 * kPadY;
+  } else {
+    s->pitch = (int)(s->prec == 32 ? grid_pitch2<float>(s->nx) : grid_pitch2<double>(s->nx));
+    s->rows = s->prec == 32 ? grid_rows2<float>(s->ny) : grid_rows2<double>(s->ny);
+  }
 
   swe_status st = SWE_OK;
   auto fail = [&](swe_status e) {
     swe_destroy(s);
     return e;
   };
-  const int64_t felems = (int64_t)(s->ny + 2 * kPadY) * s->pitch;
+  const int64_t felems = s->rows * s->pitch;
   const int64_t fbytes = round_up(felems * (int64_t)s->esz, 256);
   s->field_stride = fbytes / (int64_t)s->esz;
   const int64_t aux = 256 + round_up((int64_t)kHistCap * 8, 256) + 256 + 256;
-  s->dev_bytes = (size_t)(9 * fbytes + aux);
+  const int nalloc = s->nl == 2 ? 13 : 9;  // fields (+ scratch) + H
+  s->dev_bytes = (size_t)(nalloc * fbytes + aux);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
   if (e != cudaSuccess) {
     s->dev = nullptr;
     return fail(cuda_status(e));
   }
   char* p = (char*)s->dev;
-  for (int b = 0; b < 2; ++b)
-    for (int f = 0; f < 4; ++f) {
-      s->w[b][f] = p;
+  if (s->nl == 1) {
+    for (int b = 0; b < 2; ++b)
+      for (int f = 0; f < 4; ++f) {
+        s->w[b][f] = p;
+        p += fbytes;
+      }
+  } else {
+    for (int f = 0; f < 6; ++f) {
+      s->w[0][f] = p;
       p += fbytes;
     }
+    for (int f = 0; f < 6; ++f) {
+      s->R[f] = p;
+      p += fbytes;
+    }
+  }
   s->H = p;
   p += fbytes;
   s->slots = p;
@@ -268,14 +351,16 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   s->h_err = (unsigned*)(s->h_dt + 1);
   s->h_t = s->h_dt + 2;
 
-  st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
-  if (st != SWE_OK) return fail(st);
+  if (s->nl == 1) {
+    st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
+    if (st != SWE_OK) return fail(st);
+  }
   st = s->prec == 32 ? fill_pads<float>(s) : fill_pads<double>(s);
   if (st != SWE_OK) return fail(st);
   void* hdst[1] = {s->H};
   const void* hsrc[1] = {H};
   if ((st = upload(s, hdst, hsrc, 1)) != SWE_OK) return fail(st);
-  if ((st = upload(s, s->w[0], W0, 4)) != SWE_OK) return fail(st);
+  if ((st = upload(s, s->w[0], W0, s->nf)) != SWE_OK) return fail(st);
   if ((e = cudaMemsetAsync(s->t_dev, 0, 256 + 256, s->stream)) != cudaSuccess)
     return fail(cuda_status(e));
   s->cur = 0;
@@ -289,11 +374,11 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
 
 swe_status swe_set_state(swe_state* s, const void* const* fields, double t) {
   if (!s || !fields) return SWE_ERR_ARG;
-  for (int f = 0; f < 4; ++f)
+  for (int f = 0; f < s->nf; ++f)
     if (!fields[f]) return SWE_ERR_ARG;
   if (!isfinite(t)) return SWE_ERR_ARG;
   swe_status st;
-  if ((st = upload(s, s->w[s->cur], fields, 4)) != SWE_OK) return st;
+  if ((st = upload(s, s->w[s->cur], fields, s->nf)) != SWE_OK) return st;
   *s->h_t = t;
   CK(cudaMemcpyAsync(s->t_dev, s->h_t, sizeof(double), cudaMemcpyHostToDevice, s->stream));
   CK(cudaMemsetAsync(s->err, 0, sizeof(unsigned), s->stream));
@@ -336,12 +421,12 @@ swe_status swe_run(swe_state* s, int64_t nsteps) {
 swe_status swe_get_state(const swe_state* cs, void* const* fields_out, double* t_out) {
   swe_state* s = const_cast<swe_state*>(cs);
   if (!s || !fields_out) return SWE_ERR_ARG;
-  for (int f = 0; f < 4; ++f)
+  for (int f = 0; f < s->nf; ++f)
     if (!fields_out[f]) return SWE_ERR_ARG;
   const size_t row = (size_t)s->nx * s->esz;
   const size_t spitch = (size_t)s->pitch * s->esz;
   const size_t off = ((size_t)kPadY * s->pitch + kPadX) * s->esz;
-  for (int f = 0; f < 4; ++f)
+  for (int f = 0; f < s->nf; ++f)
     CK(cudaMemcpy2DAsync(fields_out[f], row, (const char*)s->w[s->cur][f] + off, spitch, row,
                          (size_t)s->ny, cudaMemcpyDeviceToHost, s->stream));
   CK(cudaMemcpyAsync(s->h_t, s->t_dev, sizeof(double), cudaMemcpyDeviceToHost, s->stream));
@@ -387,13 +472,14 @@ swe_status swe_get_info(const swe_state* s, swe_info* info) {
   info->bands = s->nbands;
   info->segments = s->nsegs;
   info->warps_per_block = kWarpsPerBlock;
+  info->n_layers = s->nl;
   return SWE_OK;
 }
 
 swe_status swe_device_fields(swe_state* s, void** ptrs) {
   if (!s || !ptrs) return SWE_ERR_ARG;
-  for (int f = 0; f < 4; ++f) ptrs[f] = s->w[s->cur][f];
-  ptrs[4] = s->H;
+  for (int f = 0; f < s->nf; ++f) ptrs[f] = s->w[s->cur][f];
+  ptrs[s->nf] = s->H;
   return SWE_OK;
 }
 

@@ -24,6 +24,7 @@ constexpr int kHistCap = 65536;   // dt history ring length
 constexpr unsigned kErrDepth = 1u;
 constexpr unsigned kErrNonfinite = 2u;
 constexpr unsigned kErrTimeout = 4u;
+constexpr unsigned kErrHyperbolic = 8u;
 
 // Every lane of the step kernel owns two adjacent cells of a row.
 template <typename T> struct Cpt { static constexpr int v = 2; };
@@ -70,6 +71,58 @@ struct StepArgs {
   int64_t step;         // index of this step (selects the history slot)
   unsigned* err;        // sticky error bits
 };
+
+// ---- two layers (swe_cart2.cu) ----------------------------------------------
+// Tiles of kTile2X x Tile2Y<T> cells; the padded layout of a two-layer state
+// covers whole tiles plus the one-cell halo: pitch2 / rows2 below.
+constexpr int kTile2X = 32;
+template <typename T> struct Tile2Y { static constexpr int v = 8; };
+template <> struct Tile2Y<double> { static constexpr int v = 4; };
+
+template <typename T>
+inline int64_t grid_pitch2(int nx) {
+  int64_t cols = (int64_t)(nx + kTile2X - 1) / kTile2X * kTile2X + 2 * kPadX;
+  return (cols + 31) / 32 * 32;
+}
+template <typename T>
+inline int64_t grid_rows2(int ny) {
+  return (int64_t)(ny + Tile2Y<T>::v - 1) / Tile2Y<T>::v * Tile2Y<T>::v + 2 * kPadY;
+}
+
+template <typename T>
+struct Fields6 {
+  const T* p[6];
+};
+
+template <typename T>
+struct Step2Args {
+  const T* w[6];   // h1, q1x, q1y, h2, q2x, q2y (padded layout)
+  const T* H;
+  T* R[6];         // residual sum_j L F / dx (scratch, padded layout)
+  int nx, ny, pitch;
+  T g, r, rho;     // gravity, density ratio, dx / dy
+  void* tmax_out;  // max over cells of sum_x D + rho sum_y D (must start at 0)
+  unsigned* err;
+};
+template <typename T>
+struct Update2Args {
+  T* w[6];
+  const T* R[6];
+  int nx, ny, pitch;
+  double two_cfl, dx;
+  const void* tmax_in;
+  void* tmax_clear;
+  double* dt_hist;
+  double* t_dev;
+  int64_t step;
+  unsigned* err;
+};
+
+template <typename T>
+cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st);
+template <typename T>
+cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsigned* err,
+                          cudaStream_t st);
 
 // host-side launchers (swe_cart1.cu)
 template <typename T>

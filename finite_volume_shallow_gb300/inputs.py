@@ -38,7 +38,9 @@ WORKLOADS = {
     "dam128": dict(nx=128, ny=128, dx=1.0, steps=100, seed=1001, precision=64),
     "hills2048": dict(nx=2048, ny=2048, dx=10.0, steps=1000, seed=1002, precision=32),
     "pulses8192": dict(nx=8192, ny=8192, dx=10.0, steps=200, seed=1003, precision=32),
+    "interface2048": dict(nx=2048, ny=2048, dx=10.0, steps=500, seed=1004, precision=64),
 }
+TWO_LAYER = ("interface2048",)
 
 
 def _gaussian_sum(nx, ny, dx, dy, amp, sigma, cx, cy, cutoff=8.0):
@@ -160,6 +162,60 @@ def dam_break_1d(nx, ny=4, length=2000.0, x_dam=1000.0, h_left=2.0, h_right=1.0)
     return _as_fields(z, h, z, z, h * C, nx=nx, ny=ny, dx=dx, dy=dx)
 
 
+def interface_dam(nx, ny, dx=10.0, depth=10.0, h_left=6.0, h_right=4.0, r=0.98):
+    """Two-layer interface dam break on a flat bottom ``depth`` deep: upper
+    layer h1 = h_left for x < L/2 and h_right beyond, lower layer
+    h2 = depth - h1, both at rest."""
+    x = (np.arange(nx) + 0.5) * dx
+    h1 = np.tile(np.where(x < 0.5 * nx * dx, h_left, h_right), (ny, 1))
+    H = np.full((ny, nx), float(depth))
+    z = np.zeros((ny, nx))
+    d = dict(nx=nx, ny=ny, dx=dx, dy=dx, r=r, n_layers=2)
+    for k, v in (("H", H), ("h1", h1), ("q1x", z), ("q1y", z), ("h2", H - h1), ("q2x", z),
+                 ("q2y", z)):
+        d[k] = np.ascontiguousarray(v, dtype=np.float64).reshape(-1)
+    return d
+
+
+def two_layer_hills(nx, ny, dx=10.0, seed=1005, interface_depth=3.0, umax=0.0,
+                    bump=0.0, r=0.95):
+    """Two layers over the Gaussian-hill bottom (pushed 10 m down): surface at
+    +5 m, flat interface ``interface_depth`` below it, an optional Gaussian
+    bump of the interface at the domain centre (amplitude ``bump``) and random
+    velocities |u| <= umax in both layers (drawn speed then direction, upper
+    layer first, after the hills)."""
+    rng = np.random.default_rng(seed)
+    lx, ly = nx * dx, ny * dx
+    a, sg, cx, cy = _hills(rng, 8, lx, ly, 0.2, 0.8)
+    H = 10.0 - _gaussian_sum(nx, ny, dx, dx, a, sg, cx, cy)
+    x = (np.arange(nx) + 0.5) * dx
+    y = (np.arange(ny) + 0.5) * dx
+    X, Y = np.meshgrid(x, y)
+    h1 = interface_depth + bump * np.exp(-((X - lx / 2) ** 2 + (Y - ly / 2) ** 2) / (0.1 * lx) ** 2)
+    h2 = H + 5.0 - h1
+    d = dict(nx=nx, ny=ny, dx=dx, dy=dx, r=r, n_layers=2)
+    q = []
+    for hk in (h1, h2):
+        if umax > 0.0:
+            sp = rng.uniform(0.0, umax, (ny, nx))
+            th = rng.uniform(0.0, 2.0 * np.pi, (ny, nx))
+            q.append((hk * sp * np.cos(th), hk * sp * np.sin(th)))
+        else:
+            q.append((np.zeros_like(hk), np.zeros_like(hk)))
+    for k, v in (("H", H), ("h1", h1), ("q1x", q[0][0]), ("q1y", q[0][1]), ("h2", h2),
+                 ("q2x", q[1][0]), ("q2y", q[1][1])):
+        d[k] = np.ascontiguousarray(v, dtype=np.float64).reshape(-1)
+    return d
+
+
+TWO_LAYER_FIELDS = ("h1", "q1x", "q1y", "h2", "q2x", "q2y")
+
+
+def fields2_of(d, dtype=np.float64):
+    """The six fields of a two-layer workload dict, cast."""
+    return [np.ascontiguousarray(d[k], dtype=dtype) for k in TWO_LAYER_FIELDS]
+
+
 def make_workload(name, nx=None, ny=None, lake_at_rest=False):
     """Initial data of a named workload, optionally at a reduced size.
 
@@ -174,6 +230,11 @@ def make_workload(name, nx=None, ny=None, lake_at_rest=False):
     nx = w["nx"] if nx is None else int(nx)
     ny = w["ny"] if ny is None else int(ny)
     dx = w["dx"]
+    if name == "interface2048":
+        d = interface_dam(nx, ny, dx)
+        d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
+                 name=name)
+        return d
     if name == "dam128":
         d = circular_dam(nx, ny, dx, radius=20.0 * min(nx, ny) / 128.0)
     elif name == "hills2048":
@@ -198,6 +259,7 @@ def rounded(d, dtype):
     ``dtype`` and widened back to fp64, so a reduced-precision run and an fp64
     run start from the same values."""
     out = dict(d)
-    for k in ("H", "h", "qx", "qy", "hC"):
-        out[k] = d[k].astype(dtype).astype(np.float64)
+    for k in ("H", "h", "qx", "qy", "hC") + TWO_LAYER_FIELDS:
+        if k in d:
+            out[k] = d[k].astype(dtype).astype(np.float64)
     return out

@@ -49,7 +49,7 @@ class _Info(C.Structure):
     _fields_ = [("steps", C.c_int64), ("t", C.c_double), ("nx", C.c_int32), ("ny", C.c_int32),
                 ("precision", C.c_int32), ("pitch", C.c_int32), ("field_offset", C.c_int64),
                 ("device_bytes", C.c_int64), ("bands", C.c_int32), ("segments", C.c_int32),
-                ("warps_per_block", C.c_int32)]
+                ("warps_per_block", C.c_int32), ("n_layers", C.c_int32)]
 
 
 _lib = None
@@ -124,10 +124,11 @@ def _host_ptr(x, dtype, n, writable=False):
 class State:
     """An open simulation handle (``swe_state*``)."""
 
-    def __init__(self, ptr, nx, ny, precision, keep=()):
+    def __init__(self, ptr, nx, ny, precision, n_layers=1):
         self.ptr = C.c_void_p(ptr)
         self.nx, self.ny, self.precision = nx, ny, precision
-        self._keep = keep
+        self.n_layers = n_layers
+        self.nfields = 6 if n_layers == 2 else 4
 
     @property
     def n(self):
@@ -143,8 +144,9 @@ class State:
 def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream=None,
                     n_layers=1, pollutant=1, r=0.0) -> State:
     """Create a simulation on an nx x ny grid (see swe_create_grid in swe.h).
-    H and the four fields of W0 (h, qx, qy, hC) are host arrays of the state's
-    precision; ``stream`` is a cudaStream_t as an int (e.g.
+    H and the fields of W0 (h, qx, qy, hC; or h1, q1x, q1y, h2, q2x, q2y with
+    n_layers=2, pollutant=0) are host arrays of the state's precision;
+    ``stream`` is a cudaStream_t as an int (e.g.
     ``torch.cuda.current_stream().cuda_stream``) or None."""
     L = load()
     dt = _dtype(precision)
@@ -153,11 +155,11 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
     params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
                      float(cfl), C.c_void_p(stream) if stream else None)
     Hp = _host_ptr(H, dt, n)
-    W = (C.c_void_p * 4)(*[_host_ptr(w, dt, n) for w in W0])
+    W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
     out = C.c_void_p()
     _check(L.swe_create_grid(C.byref(grid), C.c_void_p(Hp), W, C.byref(params), C.byref(out)),
            "swe_create_grid")
-    return State(out.value, int(nx), int(ny), int(precision))
+    return State(out.value, int(nx), int(ny), int(precision), int(n_layers))
 
 
 def swe_step(s: State, cfl) -> float:
@@ -174,8 +176,8 @@ def swe_get_state(s: State, out=None):
     """Returns (fields, t); ``out`` may supply the four host output arrays."""
     dt = _dtype(s.precision)
     if out is None:
-        out = [np.empty(s.n, dtype=dt) for _ in range(4)]
-    ptrs = (C.c_void_p * 4)(*[_host_ptr(o, dt, s.n, writable=True) for o in out])
+        out = [np.empty(s.n, dtype=dt) for _ in range(s.nfields)]
+    ptrs = (C.c_void_p * len(out))(*[_host_ptr(o, dt, s.n, writable=True) for o in out])
     t = C.c_double()
     _check(load().swe_get_state(s.ptr, ptrs, C.byref(t)), "swe_get_state")
     return out, t.value
@@ -183,7 +185,7 @@ def swe_get_state(s: State, out=None):
 
 def swe_set_state(s: State, fields, t=0.0):
     dt = _dtype(s.precision)
-    ptrs = (C.c_void_p * 4)(*[_host_ptr(f, dt, s.n) for f in fields])
+    ptrs = (C.c_void_p * len(fields))(*[_host_ptr(f, dt, s.n) for f in fields])
     _check(load().swe_set_state(s.ptr, ptrs, float(t)), "swe_set_state")
 
 
@@ -202,8 +204,8 @@ def swe_get_info(s: State) -> dict:
 
 
 def swe_device_fields(s: State):
-    """Device addresses of (h, qx, qy, hC, H) of the current state."""
-    ptrs = (C.c_void_p * 5)()
+    """Device addresses of the current state's fields followed by H."""
+    ptrs = (C.c_void_p * (s.nfields + 1))()
     _check(load().swe_device_fields(s.ptr, ptrs), "swe_device_fields")
     return [p or 0 for p in ptrs]
 

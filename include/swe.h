@@ -18,7 +18,10 @@
  * One explicit step, for every cell V_i with neighbours j:
  *     W_i^{n+1} = W_i^n - dt_n / |V_i| * sum_j |Gamma_ij| F_ij^-      (eq. (4))
  *     dt_n = min_i 2 cfl |V_i| / sum_j |Gamma_ij| ||D_ij||_inf          (eq. (5))
- * with W = (h, qx, qy, hC): depth, discharge and pollutant mass per area.
+ * with W = (h, qx, qy, hC): depth, discharge and pollutant mass per area, or,
+ * for the two-layer system of [P1] eq. (1), W = (h1, q1x, q1y, h2, q2x, q2y)
+ * (layer 1 on top, r = rho1/rho2 < 1) with the 4x4 Roe matrix of [P1]
+ * Sec. 2.2.
  * H is the depth of the bottom below a fixed reference level (positive
  * downward, [P1] Sec. 2.1), so the free surface is h - H.  Domain boundaries
  * are reflective walls (mirror ghost: same h, hC, H; normal discharge
@@ -32,7 +35,7 @@
  *    when swe_params.precision == 32, double when it is 64.
  *  - Grid fields are nx*ny values, cell (i, j) at index j*nx + i (row-major,
  *    x fastest), centre ((i+1/2) dx, (j+1/2) dy).
- *  - Field order: h, qx, qy, hC.
+ *  - Field order: h, qx, qy, hC (one layer); h1, q1x, q1y, h2, q2x, q2y (two).
  *  - A handle is not thread-safe; it may be used from any one thread at a
  *    time.  All device work of a handle is ordered on swe_params.stream.
  *  - Device-detected errors (SWE_ERR_DEPTH, SWE_ERR_NONFINITE,
@@ -57,7 +60,7 @@ typedef enum {
   SWE_ERR_DEPTH = -4,       /* a depth h <= 0 appeared (dry cells are out   */
                             /* of scope of the scheme as implemented)       */
   SWE_ERR_NONFINITE = -5,   /* a non-finite value appeared in the state     */
-  SWE_ERR_HYPERBOLIC = -6,  /* reserved: loss of hyperbolicity (two layers) */
+  SWE_ERR_HYPERBOLIC = -6,  /* the two-layer Roe matrix lost hyperbolicity  */
   SWE_ERR_UNSUPPORTED = -7, /* valid request this build does not implement  */
   SWE_ERR_TIMEOUT = -8      /* a bounded device wait gave up                */
 } swe_status;
@@ -71,12 +74,12 @@ typedef struct {
 } swe_grid;
 
 /* Model and run parameters.
- *  n_layers   1 (the two-layer system of [P1] eq. (1) is not in this build:
- *             SWE_ERR_UNSUPPORTED)
+ *  n_layers   1, or 2 for the two-layer system of [P1] eq. (1)
  *  precision  32 or 64: arithmetic and storage type of the state
- *  pollutant  must be 1: the state carries hC ([P2] transport equation)
+ *  pollutant  1 with one layer (the state carries hC, [P2] transport
+ *             equation); 0 with two layers (no pollutant there)
  *  g          gravity (> 0)
- *  r          density ratio rho1/rho2 of two-layer runs; ignored for 1 layer
+ *  r          density ratio rho1/rho2, 0 <= r < 1, two layers; ignored for 1
  *  cfl        gamma of eq. (5), 0 < cfl <= 1, used by swe_run
  *  stream     cudaStream_t the handle orders its work on; NULL = legacy
  *             default stream */
@@ -96,12 +99,13 @@ typedef struct swe_state swe_state;
  * loop: mesh construction and initial state).
  *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite
  *  H       host, nx*ny values: bottom depth below the reference level
- *  W0      host, array of 4 pointers (h, qx, qy, hC), nx*ny values each;
- *          h > 0 everywhere
+ *  W0      host, array of 4 pointers (h, qx, qy, hC), or 6 (h1, q1x, q1y,
+ *          h2, q2x, q2y) for two layers, nx*ny values each; depths > 0
  *  params  see swe_params
  *  out     receives the handle (NULL on failure)
- * Allocates the device state (about 9 padded fields of the chosen precision),
- * copies H and W0 to the device and computes dt_0 there.
+ * Allocates the device state (9 padded fields of the chosen precision for one
+ * layer, 13 for two), copies H and W0 to the device and checks the state
+ * there (one layer: also dt_0).
  * Errors: SWE_ERR_ARG (bad argument, h <= 0 or non-finite input),
  * SWE_ERR_UNSUPPORTED, SWE_ERR_OOM, SWE_ERR_CUDA. */
 swe_status swe_create_grid(const swe_grid *grid, const void *H,
@@ -111,7 +115,8 @@ swe_status swe_create_grid(const swe_grid *grid, const void *H,
 /* Advance one step of eq. (4) with dt_n from eq. (5) evaluated on the
  * current state with CFL number cfl (0 < cfl <= 1).  Waits for the step to
  * finish; *dt_out (if not NULL) receives dt_n.  Returns the sticky device
- * error, if any, after the step. */
+ * error, if any, after the step (two layers: SWE_ERR_HYPERBOLIC when an
+ * edge's Roe matrix has complex eigenvalues). */
 swe_status swe_step(swe_state *s, double cfl, double *dt_out);
 
 /* Advance nsteps >= 0 steps with params.cfl.  Enqueues all steps on the
@@ -120,7 +125,8 @@ swe_status swe_step(swe_state *s, double cfl, double *dt_out);
 swe_status swe_run(swe_state *s, int64_t nsteps);
 
 /* Copy the current state to the host.  fields_out: array of 4 host pointers
- * (h, qx, qy, hC) of nx*ny elements of the state's precision; t_out (may be
+ * (h, qx, qy, hC), or 6 for two layers, of nx*ny elements of the state's
+ * precision; t_out (may be
  * NULL) receives the simulated time (sum of the dt of all steps since the
  * last swe_create_grid / swe_set_state, plus the t given there). */
 swe_status swe_get_state(const swe_state *s, void *const *fields_out,
@@ -146,12 +152,14 @@ typedef struct {
   int32_t pitch;        /* elements between rows of a device field         */
   int64_t field_offset; /* elements from a field's base to cell (0, 0)     */
   int64_t device_bytes; /* device memory held by the handle                */
-  int32_t bands, segments, warps_per_block; /* launch shape of the step    */
+  int32_t bands, segments, warps_per_block; /* launch shape (one layer)   */
+  int32_t n_layers;
 } swe_info;
 swe_status swe_get_info(const swe_state *s, swe_info *info);
 
-/* Device pointers of the current state's fields (h, qx, qy, hC, H), for
- * zero-copy inspection on the device.  Cell (i, j) of field k is at
+/* Device pointers of the current state's fields followed by H (5 pointers
+ * for one layer: h, qx, qy, hC, H; 7 for two), for zero-copy inspection on
+ * the device; ptrs must hold that many entries.  Cell (i, j) of field k is at
  * ptrs[k] + field_offset + j*pitch + i (see swe_info).  The pointers stay
  * owned by the handle and change after every step (double buffering). */
 swe_status swe_device_fields(swe_state *s, void **ptrs);

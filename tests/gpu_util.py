@@ -71,3 +71,57 @@ def assert_parity(d, precision, nsteps, use_run=False):
     assert dte <= tol["dt"], dte
     assert abs(tg - dto.sum()) <= tol["dt"] * dto.sum()
     return errs, dte
+
+
+# ---- two layers -------------------------------------------------------------
+TOL2 = {
+    64: {"h1": 1e-10, "q1x": 1e-10, "q1y": 1e-10, "h2": 1e-10, "q2x": 1e-10, "q2y": 1e-10,
+         "dt": 1e-12},
+    32: {"h1": 1e-4, "q1x": 1e-3, "q1y": 1e-3, "h2": 1e-4, "q2x": 1e-3, "q2y": 1e-3, "dt": 1e-6},
+}
+
+
+def gpu_create2(d, precision, stream=None):
+    dt = np_dtype(precision)
+    return S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(dt),
+                             [f.astype(dt) for f in I.fields2_of(d)], precision=precision,
+                             g=d.get("g", 9.81), cfl=d.get("cfl", 0.9), stream=stream,
+                             n_layers=2, pollutant=0, r=d["r"])
+
+
+def gpu_run2(d, precision, nsteps):
+    st = gpu_create2(d, precision)
+    S.swe_run(st, nsteps)
+    dts = S.swe_get_dt_history(st, nsteps)
+    W, t = S.swe_get_state(st)
+    S.swe_destroy(st)
+    return [w.astype(np.float64) for w in W], np.asarray(dts), t
+
+
+def oracle_run2(d, precision, nsteps):
+    dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
+    W, dts, st = O.grid_run2(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields2_of(dr),
+                             d.get("g", 9.81), d["r"], d.get("cfl", 0.9), nsteps)
+    assert st == O.OM_OK, st
+    return W, dts
+
+
+def rel_errors2(W_gpu, W_ref, W_init):
+    out = {}
+    for i, k in enumerate(I.TWO_LAYER_FIELDS):
+        scale = max(np.abs(W_ref[i]).max(), np.abs(W_init[i]).max(), 1e-30)
+        out[k] = float(np.abs(W_gpu[i] - W_ref[i]).max() / scale)
+    return out
+
+
+def assert_parity2(d, precision, nsteps):
+    Wg, dtg, tg = gpu_run2(d, precision, nsteps)
+    Wo, dto = oracle_run2(d, precision, nsteps)
+    tol = TOL2[precision]
+    errs = rel_errors2(Wg, Wo, I.fields2_of(d))
+    for k in I.TWO_LAYER_FIELDS:
+        assert errs[k] <= tol[k], (k, errs)
+    assert len(dtg) == len(dto) == nsteps
+    dte = float(np.abs(dtg / dto - 1.0).max())
+    assert dte <= tol["dt"], dte
+    return errs, dte

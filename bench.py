@@ -42,6 +42,18 @@ sys.path.insert(0, ROOT)
 METRIC = "cell-updates/s (Mcell-steps/s) of the Roe FV step; achieved HBM GB/s vs peak"
 UNIT = "Mcell-updates/s"
 BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC written
+# Two layers (flux pass + update pass): 7 fields + residual 6 written, then
+# 6 state + 6 residual read and 6 written: 31 fields per cell.
+BYTES_PER_CELL_2L = {32: 124, 64: 248}
+# Floating-point operations per cell-update of the two-layer step, counted
+# from the kernel's formulas (an FMA counts 2, a division or square root 1):
+# about 2.16 edge evaluations per cell (tile halo included) of ~494 (fp32,
+# 7 + 2 Newton iterations per outer / inner root) or ~584 (fp64, 9 + 3)
+# flops, plus the residual sums and the update.
+FLOPS_PER_CELL_2L = {32: 1100, 64: 1290}
+# FP32 FMA peak of a GB300: 152 SMs x 128 lanes x 2 flops x 2.07 GHz;
+# FP64: the nominal 1.25 TFLOP/s of the part.
+ALU_PEAK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
 DTYPE_NAME = {32: "f32", 64: "f64"}
 KERNEL = "cart1_step_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cart1_step_traffic.txt")
@@ -53,7 +65,20 @@ DESCR = {
     "hills2048": "2048x2048 Cartesian, dx=10 m, 8 seeded Gaussian hills, 3 surface bumps, "
                  "q=0, pollutant per 16x16 block, reflective walls",
     "dam128": "128x128 Cartesian, dx=1 m, circular dam break, flat bottom, reflective walls",
+    "interface2048": "two layers, 2048x2048 Cartesian, dx=10 m, flat bottom 10 m, interface "
+                     "dam break h1=6/4 m at x=L/2, r=0.98, at rest, reflective walls",
 }
+
+
+def state_fields(I, d):
+    """The conserved fields of a workload dict (one or two layers)."""
+    return I.fields2_of(d) if d.get("n_layers") == 2 else I.fields_of(d)
+
+
+def oracle_run(O, d, nx, rows, H, W, nsteps):
+    if d.get("n_layers") == 2:
+        return O.grid_run2(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["r"], d["cfl"], nsteps)
+    return O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], nsteps)
 
 
 def parse():
@@ -192,16 +217,16 @@ def cpu_baseline(d, budget_s=12.0):
     rows = min(d["ny"], 64)
     def window(r):
         sl = slice(0, r * nx)
-        return d["H"][sl], [f[sl] for f in I.fields_of(d)]
+        return d["H"][sl], [f[sl] for f in state_fields(I, d)]
     H, W = window(rows)
     t0 = time.perf_counter()
-    O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], 1)
+    oracle_run(O, d, nx, rows, H, W, 1)
     per_cell = (time.perf_counter() - t0) / (nx * rows)
     rows = int(max(8, min(d["ny"], budget_s / 4 / (per_cell * nx))))
     steps = max(1, int(budget_s / (per_cell * nx * rows)))
     H, W = window(rows)
     t0 = time.perf_counter()
-    _, dts, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], steps)
+    _, dts, st = oracle_run(O, d, nx, rows, H, W, steps)
     el = time.perf_counter() - t0
     return {"value": nx * rows * steps / el / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of the {d['nx']}x{d['ny']} initial state as a "
@@ -225,17 +250,16 @@ def run_reference(args, rank, world):
     cal_rows = min(d["ny"], 16)
     sl = slice(0, cal_rows * nx)
     t0 = time.perf_counter()
-    O.grid_run1(nx, cal_rows, d["dx"], d["dy"], d["H"][sl], [f[sl] for f in I.fields_of(d)],
-                d["g"], d["cfl"], 1)
+    oracle_run(O, d, nx, cal_rows, d["H"][sl], [f[sl] for f in state_fields(I, d)], 1)
     per_cell = (time.perf_counter() - t0) / (nx * cal_rows)
     budget = 150.0
     rows = int(max(4, min(d["ny"], budget / ((args.steps + args.warmup) * per_cell * nx))))
     sl = slice(0, rows * nx)
     H = d["H"][sl]
-    W = [f[sl] for f in I.fields_of(d)]
-    W, _, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], args.warmup)
+    W = [f[sl] for f in state_fields(I, d)]
+    W, _, st = oracle_run(O, d, nx, rows, H, W, args.warmup)
     t0 = time.perf_counter()
-    W, _, st = O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], args.steps)
+    W, _, st = oracle_run(O, d, nx, rows, H, W, args.steps)
     el = time.perf_counter() - t0
     value = nx * rows * args.steps / el / 1e6
     sample = (f"each step: one oracle step over rows 0..{rows - 1} of the {d['nx']}x{d['ny']} "
@@ -283,11 +307,13 @@ def main():
     npdt = np.float32 if precision == 32 else np.float64
     tdt = torch.float32 if precision == 32 else torch.float64
     n = d["nx"] * d["ny"]
-    fields = [f.astype(npdt) for f in I.fields_of(d)]
+    two = d.get("n_layers") == 2
+    fields = [f.astype(npdt) for f in state_fields(I, d)]
     stream = torch.cuda.Stream()
     st = S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(npdt), fields,
                            precision=precision, g=d["g"], cfl=d["cfl"],
-                           stream=stream.cuda_stream)
+                           stream=stream.cuda_stream, n_layers=2 if two else 1,
+                           pollutant=0 if two else 1, r=d.get("r", 0.0))
     info = S.swe_get_info(st)
 
     # warm-up (also gives a step-time estimate for the busy window below)
@@ -347,17 +373,29 @@ def main():
         torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
     e2e_s = float(te.item())
     esz = 4 if precision == 32 else 8
+    nf = len(fields)
     e2e = {"value": world * n * ke / e2e_s / 1e6, "unit": UNIT, "steps": ke,
-           "h2d_bytes_per_step": 4 * n * esz + 8, "d2h_bytes_per_step": 4 * n * esz + 8 + 8 + 4,
+           "h2d_bytes_per_step": nf * n * esz + 8, "d2h_bytes_per_step": nf * n * esz + 8 + 8 + 4,
            "api": "swe_set_state + swe_step + swe_get_state, pinned host buffers"}
     S.swe_destroy(st)
 
     peak, peak_kind = load_peaks()
-    achieved = BYTES_PER_CELL[precision] * n / (ms_per_step / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "peak_source": peak_kind,
-            "traffic": traffic_per_launch(precision, args.workload),
-            "kernel": KERNEL, "algorithmic_bytes_per_launch": BYTES_PER_CELL[precision] * n}
+    if two:
+        fl = FLOPS_PER_CELL_2L[precision] * n / (ms_per_step / 1e3) / 1e12
+        pk = ALU_PEAK_TFLOPS[precision]
+        roof = {"bound": "alu", "achieved": fl, "peak": pk, "unit": "TFLOP/s",
+                "frac": fl / pk, "peak_source": "derived from unit counts and the 2.07 GHz "
+                "maximum SM clock (fp32) / the part's nominal FP64 rate (fp64)",
+                "traffic": None, "kernel": "cart2_flux_kernel + cart2_update_kernel",
+                "flops_per_cell": FLOPS_PER_CELL_2L[precision],
+                "algorithmic_bytes_per_step": BYTES_PER_CELL_2L[precision] * n,
+                "achieved_gbs": BYTES_PER_CELL_2L[precision] * n / (ms_per_step / 1e3) / 1e9}
+    else:
+        achieved = BYTES_PER_CELL[precision] * n / (ms_per_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": peak_kind,
+                "traffic": traffic_per_launch(precision, args.workload),
+                "kernel": KERNEL, "algorithmic_bytes_per_launch": BYTES_PER_CELL[precision] * n}
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -373,12 +411,12 @@ def main():
                                    + (f", reduced to {d['nx']}x{d['ny']}" if args.nx or args.ny
                                       else ""),
                        "cells": n, "nx": d["nx"], "ny": d["ny"], "parallelism": "replicas",
-                       "l2": "inputs larger than L2" if n * BYTES_PER_CELL[precision] > 129e6
+                       "l2": "inputs larger than L2" if n * (BYTES_PER_CELL_2L if two else BYTES_PER_CELL)[precision] > 129e6
                              else "inputs fit in L2 (no flush)",
                        "launch": {"bands": info["bands"], "segments": info["segments"],
                                   "warps_per_block": info["warps_per_block"]}},
             "e2e": e2e, "roofline": roof, "cpu_baseline": base, "clocks": clocks,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if two else 1),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

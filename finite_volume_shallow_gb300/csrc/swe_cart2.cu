@@ -42,7 +42,11 @@ constexpr unsigned kFull2 = 0xffffffffu;
 template <typename T> struct M2;
 template <> struct M2<float> {
   __device__ static __forceinline__ float rsq(float x) { return rsqrtf(x); }
-  __device__ static __forceinline__ float rcp(float x) { return __frcp_rn(x); }
+  __device__ static __forceinline__ float rcp(float x) {  // MUFU approximation
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+  }
   __device__ static __forceinline__ float sq(float x) { return sqrtf(x); }
   __device__ static __forceinline__ float big() { return 3.402823466e38f; }
 };
@@ -115,8 +119,8 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   T l4 = fmax(un[0] + T(1.5) * c1, un[1] + T(1.5) * c2);
 #pragma unroll
   for (int it = 0; it < Iters<T>::outer; ++it) {
-    l1 -= q.p(l1) / q.dp(l1);
-    l4 -= q.p(l4) / q.dp(l4);
+    l1 -= q.p(l1) * M2<T>::rcp(q.dp(l1));
+    l4 -= q.p(l4) * M2<T>::rcp(q.dp(l4));
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const T p3 = T(-2) * (un[0] + un[1]);
@@ -130,8 +134,8 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   T l2 = T(0.5) * (-bb - sd), l3 = T(0.5) * (-bb + sd);
 #pragma unroll
   for (int it = 0; it < Iters<T>::inner; ++it) {
-    l2 -= q.p(l2) / q.dp(l2);
-    l3 -= q.p(l3) / q.dp(l3);
+    l2 -= q.p(l2) * M2<T>::rcp(q.dp(l2));
+    l3 -= q.p(l3) * M2<T>::rcp(q.dp(l3));
   }
   // fluctuation d = F_1(W_j) - F_1(W_i) - B_ij (W_j - W_i) - S_ij (H_j - H_i)
   // (pressure differences written g hbar_k (h_k,j - h_k,i))
@@ -142,6 +146,7 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   const T d4 = (qu_b[1] - qu_a[1]) + cs[1] * ((dh2 + r * dh1) - dH);
   // P^- d = sum_k w_k alpha_k K_k
   const T lam[4] = {l1, l2, l3, l4};
+  const T ic1s = M2<T>::rcp(cs[0]);
   T pd0 = T(0), pd1 = T(0), pd2 = T(0), pd3 = T(0);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -149,8 +154,8 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     const T w = (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
     const T Q1 = q.q1(l), Q2 = q.q2(l);
     const T num = Q2 * ((l - T(2) * un[0]) * d1 + d2) + cs[0] * ((l - T(2) * un[1]) * d3 + d4);
-    const T alpha = w * num / q.dp(l);
-    const T mu = Q1 / cs[0];
+    const T alpha = w * num * M2<T>::rcp(q.dp(l));
+    const T mu = Q1 * ic1s;
     pd0 += alpha;
     pd1 += alpha * l;
     pd2 += alpha * mu;

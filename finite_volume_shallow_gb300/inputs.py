@@ -39,8 +39,9 @@ WORKLOADS = {
     "hills2048": dict(nx=2048, ny=2048, dx=10.0, steps=1000, seed=1002, precision=32),
     "pulses8192": dict(nx=8192, ny=8192, dx=10.0, steps=200, seed=1003, precision=32),
     "interface2048": dict(nx=2048, ny=2048, dx=10.0, steps=500, seed=1004, precision=64),
+    "tri1024": dict(nx=1024, ny=1024, dx=1.0, steps=500, seed=1005, precision=32),
 }
-TWO_LAYER = ("interface2048",)
+TWO_LAYER = ("interface2048", "tri1024")
 
 
 def _gaussian_sum(nx, ny, dx, dy, amp, sigma, cx, cy, cutoff=8.0):
@@ -211,6 +212,71 @@ def two_layer_hills(nx, ny, dx=10.0, seed=1005, interface_depth=3.0, umax=0.0,
 TWO_LAYER_FIELDS = ("h1", "q1x", "q1y", "h2", "q2x", "q2y")
 
 
+def square_tri_mesh(n, m=None, side=1.0, jitter=0.2, seed=1005, shuffle=True):
+    """Triangle mesh of n x m squares of size ``side``: (n+1)(m+1) vertices,
+    vertex (i, j) at index j*(n+1) + i; square (i, j) split along its lower-left
+    to upper-right diagonal into the counter-clockwise triangles (a, b, c) and
+    (a, c, d) with a = (i, j), b = (i+1, j), c = (i+1, j+1), d = (i, j+1).
+    Interior vertices move by U[-jitter, jitter] * side in x then in y (one
+    array of draws each); with ``shuffle`` the cells are then reordered by a
+    seeded permutation (drawn after the jitter).  Returns (xy, tri) with xy of
+    shape (nv, 2) and tri of shape (nc, 3)."""
+    m = n if m is None else m
+    rng = np.random.default_rng(seed)
+    i, j = np.meshgrid(np.arange(n + 1), np.arange(m + 1))
+    x = i.astype(np.float64) * side
+    y = j.astype(np.float64) * side
+    inner = (i > 0) & (i < n) & (j > 0) & (j < m)
+    jx = rng.uniform(-jitter, jitter, x.shape) * side
+    jy = rng.uniform(-jitter, jitter, y.shape) * side
+    x = np.where(inner, x + jx, x)
+    y = np.where(inner, y + jy, y)
+    xy = np.stack([x.reshape(-1), y.reshape(-1)], axis=1)
+    si, sj = np.meshgrid(np.arange(n), np.arange(m))
+    a = (sj * (n + 1) + si).reshape(-1)
+    b, c, d = a + 1, a + n + 2, a + n + 1
+    tri = np.empty((2 * n * m, 3), dtype=np.int32)
+    tri[0::2] = np.stack([a, b, c], axis=1)
+    tri[1::2] = np.stack([a, c, d], axis=1)
+    if shuffle:
+        tri = tri[rng.permutation(tri.shape[0])]
+    return xy, np.ascontiguousarray(tri)
+
+
+def tri_centroids(xy, tri):
+    """Vertex mean of each triangle (where the initial state is sampled)."""
+    return xy[tri].mean(axis=1)
+
+
+def tri_workload(n, seed=1005, jitter=0.2, r=0.98, n_hills=8, bump=0.5):
+    """The two-layer triangle-mesh workload on n x n unit squares (see the
+    module docstring); the state is sampled at cell centroids.  Draw order:
+    the mesh (jitter, permutation), then the hills (amplitude, width, centre)
+    and the interface bump (width, centre)."""
+    xy, tri = square_tri_mesh(n, side=1.0, jitter=jitter, seed=seed)
+    rng = np.random.default_rng(seed + 7919)
+    L = float(n)
+    scale = n / 20480.0
+    amp = rng.uniform(0.2, 0.8, n_hills)
+    sig = rng.uniform(50.0, 300.0, n_hills) * scale
+    cx = rng.uniform(0.0, L, n_hills)
+    cy = rng.uniform(0.0, L, n_hills)
+    bs = rng.uniform(50.0, 300.0) * scale
+    bx, by = rng.uniform(0.0, L, 2)
+    cxy = tri_centroids(xy, tri)
+    zb = np.zeros(tri.shape[0])
+    for a_, s_, x0, y0 in zip(amp, sig, cx, cy):
+        zb += a_ * np.exp(-((cxy[:, 0] - x0) ** 2 + (cxy[:, 1] - y0) ** 2) / (2 * s_ * s_))
+    H = 10.0 - zb
+    h1 = 5.0 + bump * np.exp(-((cxy[:, 0] - bx) ** 2 + (cxy[:, 1] - by) ** 2) / (2 * bs * bs))
+    z = np.zeros_like(H)
+    d = dict(xy=xy, tri=tri, n_cells=tri.shape[0], r=r, n_layers=2, mesh=True)
+    for k, v in (("H", H), ("h1", h1), ("q1x", z), ("q1y", z), ("h2", H - h1), ("q2x", z),
+                 ("q2y", z)):
+        d[k] = np.ascontiguousarray(v, dtype=np.float64)
+    return d
+
+
 def fields2_of(d, dtype=np.float64):
     """The six fields of a two-layer workload dict, cast."""
     return [np.ascontiguousarray(d[k], dtype=dtype) for k in TWO_LAYER_FIELDS]
@@ -230,6 +296,11 @@ def make_workload(name, nx=None, ny=None, lake_at_rest=False):
     nx = w["nx"] if nx is None else int(nx)
     ny = w["ny"] if ny is None else int(ny)
     dx = w["dx"]
+    if name == "tri1024":
+        d = tri_workload(nx)
+        d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
+                 name=name)
+        return d
     if name == "interface2048":
         d = interface_dam(nx, ny, dx)
         d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],

@@ -100,6 +100,8 @@ def lib():
         _lib.om_grid_run2.restype = C.c_int
         _lib.om_grid_run2.argtypes = [i64, i64, d, d, vp, vp, d, d, d, i64, vp, vp,
                                       C.POINTER(C.c_int64)]
+        _lib.om_tri_mesh.restype = C.c_int
+        _lib.om_tri_mesh.argtypes = [i64, vp, i64, vp, vp, vp, vp, vp, vp, vp]
         _lib.om_grid_dt1.restype = d
         _lib.om_grid_dt1.argtypes = [i64, i64, d, d, vp, vp, d, d]
         _lib.om_grid_update1.restype = C.c_int
@@ -155,6 +157,25 @@ def grid_mesh(nx, ny, dx, dy=None) -> Mesh:
     ln = np.empty(ne)
     L.om_grid_mesh(nx, ny, float(dx), float(dy), _ptr(area), _ptr(es), _ptr(nbr),
                    _ptr(ex), _ptr(ey), _ptr(ln))
+    return Mesh(area, es, nbr, ex, ey, ln)
+
+
+def tri_mesh(xy, tri) -> Mesh:
+    """Polygon-mesh arrays of a counter-clockwise triangle mesh (edges of cell
+    c: (v0 v1), (v1 v2), (v2 v0))."""
+    xy = np.ascontiguousarray(xy, dtype=np.float64).reshape(-1)
+    tri = np.ascontiguousarray(tri, dtype=np.int32).reshape(-1)
+    nv, nc = xy.size // 2, tri.size // 3
+    area = np.empty(nc)
+    es = np.empty(nc + 1, dtype=np.int64)
+    nbr = np.empty(3 * nc, dtype=np.int64)
+    ex = np.empty(3 * nc)
+    ey = np.empty(3 * nc)
+    ln = np.empty(3 * nc)
+    st = lib().om_tri_mesh(nv, _ptr(xy), nc, _ptr(tri), _ptr(area), _ptr(es), _ptr(nbr),
+                           _ptr(ex), _ptr(ey), _ptr(ln))
+    if st != OM_OK:
+        raise ValueError("invalid triangle mesh (index, orientation or non-manifold edge)")
     return Mesh(area, es, nbr, ex, ey, ln)
 
 

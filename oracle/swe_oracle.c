@@ -709,3 +709,74 @@ int om_grid_run2(int64_t nx, int64_t ny, double dx, double dy, double *const *W,
   view v = grid_view(nx, ny, dx, dy);
   return run_view2(&v, W, H, g, r, cfl, nsteps, dts, work, steps_done);
 }
+
+/* ======================================================================
+ * Triangle meshes: geometry of the finite volumes of [P1] Sec. 2.2 (cells
+ * V_i with area |V_i|, edges Gamma_ij with length and unit normal pointing
+ * from V_i to V_j).
+ * ====================================================================== */
+
+typedef struct {
+  int64_t key;   /* min vertex * n_vertices + max vertex */
+  int64_t cell;
+  int local;     /* 0, 1, 2: edge (v0 v1), (v1 v2), (v2 v0) */
+} half_edge;
+
+static int cmp_half_edge(const void *a, const void *b) {
+  const half_edge *x = (const half_edge *)a, *y = (const half_edge *)b;
+  if (x->key != y->key) return x->key < y->key ? -1 : 1;
+  if (x->cell != y->cell) return x->cell < y->cell ? -1 : 1;
+  return x->local - y->local;
+}
+
+int om_tri_mesh(int64_t n_vertices, const double *xy, int64_t n_cells,
+                const int32_t *tri, double *area, int64_t *edge_start,
+                int64_t *nbr, double *eta_x, double *eta_y, double *len) {
+  for (int64_t c = 0; c < 3 * n_cells; ++c)
+    if (tri[c] < 0 || tri[c] >= n_vertices) return OM_ERR_ARG;
+  half_edge *he = (half_edge *)malloc((size_t)(3 * n_cells) * sizeof(half_edge));
+  if (!he) return OM_ERR_ARG;
+  for (int64_t c = 0; c < n_cells; ++c) {
+    const int32_t *v = tri + 3 * c;
+    double x0 = xy[2 * v[0]], y0 = xy[2 * v[0] + 1];
+    double x1 = xy[2 * v[1]], y1 = xy[2 * v[1] + 1];
+    double x2 = xy[2 * v[2]], y2 = xy[2 * v[2] + 1];
+    /* shoelace area; counter-clockwise triangles have a positive one */
+    area[c] = 0.5 * ((x1 - x0) * (y2 - y0) - (x2 - x0) * (y1 - y0));
+    if (!(area[c] > 0.0)) {
+      free(he);
+      return OM_ERR_ARG;
+    }
+    edge_start[c] = 3 * c;
+    for (int k = 0; k < 3; ++k) {
+      int64_t a = v[k], b = v[(k + 1) % 3];
+      int64_t e = 3 * c + k;
+      double ex = xy[2 * b] - xy[2 * a], ey = xy[2 * b + 1] - xy[2 * a + 1];
+      double l = sqrt(ex * ex + ey * ey);
+      /* outward normal of a counter-clockwise edge a -> b: (ey, -ex) / l */
+      eta_x[e] = ey / l;
+      eta_y[e] = -ex / l;
+      len[e] = l;
+      nbr[e] = -1;
+      he[e].key = (a < b ? a : b) * n_vertices + (a < b ? b : a);
+      he[e].cell = c;
+      he[e].local = k;
+    }
+  }
+  edge_start[n_cells] = 3 * n_cells;
+  /* pair the half-edges that share their two vertices */
+  qsort(he, (size_t)(3 * n_cells), sizeof(half_edge), cmp_half_edge);
+  int status = OM_OK;
+  for (int64_t s = 0; s < 3 * n_cells;) {
+    int64_t t = s + 1;
+    while (t < 3 * n_cells && he[t].key == he[s].key) ++t;
+    if (t - s > 2) status = OM_ERR_ARG;
+    if (t - s == 2) {
+      nbr[3 * he[s].cell + he[s].local] = he[s + 1].cell;
+      nbr[3 * he[s + 1].cell + he[s + 1].local] = he[s].cell;
+    }
+    s = t;
+  }
+  free(he);
+  return status;
+}

@@ -57,6 +57,19 @@ void om_grid_mesh(int64_t nx, int64_t ny, double dx, double dy, double *area,
                   int64_t *edge_start, int64_t *nbr, double *eta_x,
                   double *eta_y, double *len);
 
+/* Polygon-mesh arrays of a triangle mesh: n_vertices points xy (2 per
+ * vertex) and n_cells triangles tri (3 vertex indices each, counter-
+ * clockwise).  Cell c lists its edges in the order (v0 v1), (v1 v2),
+ * (v2 v0); the neighbour across an edge is the other triangle sharing both
+ * vertices (-1 on the boundary: a wall), the normal is the outward unit
+ * normal of the edge, the length its length; area is the shoelace area.
+ * Returns OM_OK, or OM_ERR_ARG for a vertex index out of range, a triangle
+ * that is not counter-clockwise, or an edge shared by more than two
+ * triangles.  The arrays must hold 3 * n_cells edge entries. */
+int om_tri_mesh(int64_t n_vertices, const double *xy, int64_t n_cells,
+                const int32_t *tri, double *area, int64_t *edge_start,
+                int64_t *nbr, double *eta_x, double *eta_y, double *len);
+
 /* Numerical flux F_ij^- of eq. (4) (one layer + pollutant) for the state
  * Wi = (h, qx, qy, hC) of cell i, Wj of cell j, bathymetry Hi, Hj and unit
  * normal (ex, ey) from i to j.  Writes the Cartesian flux F[4] and the

@@ -70,6 +70,16 @@ MUTANTS = {
     "tangential_other_layer": ("double m = phi[2 * k];", "double m = phi[2 * (1 - k)];"),
     # two layers: characteristic polynomial without the density ratio
     "charpoly_no_r": ("- q->r * q->c1s * q->c2s;", "- q->c1s * q->c2s;"),
+    # triangle meshes: inward instead of outward normals
+    "tri_normal_inward": ("eta_x[e] = ey / l;\n      eta_y[e] = -ex / l;",
+                          "eta_x[e] = -ey / l;\n      eta_y[e] = ex / l;"),
+    # triangle meshes: shoelace area without its factor 1/2
+    "tri_area_half": ("area[c] = 0.5 * ((x1 - x0)", "area[c] = ((x1 - x0)"),
+    # triangle meshes: a half-edge paired with its own cell
+    "tri_pair_self": ("nbr[3 * he[s].cell + he[s].local] = he[s + 1].cell;",
+                      "nbr[3 * he[s].cell + he[s].local] = he[s].cell;"),
+    # triangle meshes: unit edge lengths
+    "tri_len_unit": ("len[e] = l;", "len[e] = 1.0;"),
 }
 
 
@@ -101,6 +111,7 @@ def test_pins_catch_mutant(name, workdir):
     env = dict(os.environ, SWE_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_pins.py"),
-                        os.path.join(HERE, "test_oracle_pins2.py")],
+                        os.path.join(HERE, "test_oracle_pins2.py"),
+                        os.path.join(HERE, "test_oracle_pins_tri.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

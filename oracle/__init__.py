@@ -90,6 +90,7 @@ def lib():
         _lib.om_dt2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, C.POINTER(C.c_int)]
         _lib.om_update2.restype = C.c_int
         _lib.om_update2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, vp]
+        _lib.om_update2_at.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, vp, i64, vp]
         _lib.om_run2.restype = C.c_int
         _lib.om_run2.argtypes = [C.POINTER(_Mesh), vp, vp, d, d, d, i64, vp, vp,
                                  C.POINTER(C.c_int64)]
@@ -334,6 +335,18 @@ def update2(mesh: Mesh, H, W, g, r, dt):
     st = lib().om_update2(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(r), float(dt),
                           _ptr(work))
     return Wf, int(st)
+
+
+def update2_at(mesh: Mesh, H, W, g, r, dt, cells):
+    """The six fields after one step of size dt, at the given cells only:
+    (array of shape (6, len(cells)), status)."""
+    Wf = [np.ascontiguousarray(w, dtype=np.float64).reshape(-1) for w in W]
+    Hf = np.ascontiguousarray(H, dtype=np.float64).reshape(-1)
+    cells = np.ascontiguousarray(cells, dtype=np.int64)
+    out = np.empty(6 * cells.size)
+    st = lib().om_update2_at(mesh.c, _field_ptrs(Wf), _ptr(Hf), float(g), float(r), float(dt),
+                             _ptr(cells), cells.size, _ptr(out))
+    return out.reshape(6, cells.size), int(st)
 
 
 def run2(mesh: Mesh, H, W, g, r, cfl, nsteps):

@@ -391,6 +391,23 @@ static double bisect(const quartic *q, double (*f)(const quartic *, double), dou
   return 0.5 * (lo + hi);
 }
 
+/* the local maximum of p in [a1, a2]: p has its two local minima in
+ * [a0, a1] and [a2, a3] (p < -r c1s c2s where exactly one Q_k is negative)
+ * and its local maximum between them, so p' > 0 left of the maximum and
+ * p' < 0 right of it; the bisection follows that sign alone (the end values
+ * of p' vanish when roots of Q1 and Q2 coincide, e.g. equal layers) */
+static double local_max(const quartic *q, double lo, double hi) {
+  for (int it = 0; it < 200; ++it) {
+    double mid = 0.5 * (lo + hi);
+    if (!(mid > lo && mid < hi)) break;
+    double fm = dpq(q, mid);
+    if (fm == 0.0) return mid;
+    if (fm > 0.0) lo = mid;
+    else hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
 /* two Newton steps on p, kept inside [lo, hi] */
 static double polish(const quartic *q, double l, double lo, double hi) {
   for (int it = 0; it < 2; ++it) {
@@ -442,7 +459,7 @@ int om_roots2(double u1, double u2, double c1s, double c2s, double r, double *la
   /* inner pair: p has its local maximum m in (a[1], a[2]) (p' > 0 at a[1],
    * < 0 at a[2]); real roots need p(m) > 0 */
   if (!(a[2] > a[1])) return OM_ERR_HYPERBOLIC;
-  double m = bisect(&q, dpq, a[1], a[2]);
+  double m = local_max(&q, a[1], a[2]);
   if (!(pq(&q, m) > 0.0)) return OM_ERR_HYPERBOLIC;
   lam[1] = (pq(&q, a[1]) < 0.0) ? polish(&q, bisect(&q, pq, a[1], m), a[1], m) : a[1];
   lam[2] = (pq(&q, a[2]) < 0.0) ? polish(&q, bisect(&q, pq, m, a[2]), m, a[2]) : a[2];
@@ -653,6 +670,21 @@ static int update_view2(const view *v, double *const *W, const double *H, double
   return status;
 }
 
+static int update_at_view2(const view *v, const double *const *W, const double *H, double g,
+                           double r, double dt, const int64_t *cells, int64_t n_sel,
+                           double *out) {
+  double Fl[6][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
+  for (int64_t s = 0; s < n_sel; ++s) {
+    int64_t i = cells[s];
+    int n;
+    int st = cell_terms2(v, W, H, g, r, i, Fl, Dl, &n);
+    if (st != OM_OK) return st;
+    for (int c = 0; c < 6; ++c)
+      out[c * n_sel + s] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
+  }
+  return OM_OK;
+}
+
 static int run_view2(const view *v, double *const *W, const double *H, double g, double r,
                      double cfl, int64_t nsteps, double *dts, double *work,
                      int64_t *steps_done) {
@@ -687,6 +719,11 @@ int om_update2(const om_mesh *m, double *const *W, const double *H, double g, do
                double dt, double *work) {
   view v = mesh_view(m);
   return update_view2(&v, W, H, g, r, dt, work);
+}
+int om_update2_at(const om_mesh *m, const double *const *W, const double *H, double g,
+                  double r, double dt, const int64_t *cells, int64_t n_sel, double *out) {
+  view v = mesh_view(m);
+  return update_at_view2(&v, W, H, g, r, dt, cells, n_sel, out);
 }
 int om_run2(const om_mesh *m, double *const *W, const double *H, double g, double r,
             double cfl, int64_t nsteps, double *dts, double *work, int64_t *steps_done) {

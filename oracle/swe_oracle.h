@@ -139,6 +139,12 @@ double om_dt2(const om_mesh *m, const double *const *W, const double *H,
               double g, double r, double cfl, int *status);
 int om_update2(const om_mesh *m, double *const *W, const double *H, double g,
                double r, double dt, double *work);
+/* The update of eq. (4) of the listed cells only, from the state W (which is
+ * not modified): out[c * n_sel + s] is field c of cells[s] after one step of
+ * size dt.  Returns OM_ERR_HYPERBOLIC if an edge of a listed cell has a
+ * complex pair of eigenvalues. */
+int om_update2_at(const om_mesh *m, const double *const *W, const double *H, double g,
+                  double r, double dt, const int64_t *cells, int64_t n_sel, double *out);
 int om_run2(const om_mesh *m, double *const *W, const double *H, double g,
             double r, double cfl, int64_t nsteps, double *dts, double *work,
             int64_t *steps_done);

@@ -70,6 +70,10 @@ MUTANTS = {
     "tangential_other_layer": ("double m = phi[2 * k];", "double m = phi[2 * (1 - k)];"),
     # two layers: characteristic polynomial without the density ratio
     "charpoly_no_r": ("- q->r * q->c1s * q->c2s;", "- q->c1s * q->c2s;"),
+    # two layers: the inner pair's bracket taken from the end signs of p'
+    # (fails when roots of Q1 and Q2 coincide)
+    "inner_max_by_end_signs": ("double m = local_max(&q, a[1], a[2]);",
+                               "double m = bisect(&q, dpq, a[1], a[2]);"),
     # triangle meshes: inward instead of outward normals
     "tri_normal_inward": ("eta_x[e] = ey / l;\n      eta_y[e] = -ex / l;",
                           "eta_x[e] = -ey / l;\n      eta_y[e] = ex / l;"),

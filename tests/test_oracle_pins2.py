@@ -60,6 +60,25 @@ def test_roots_decouple_at_r0():
         assert np.abs(lam - want).max() <= 1e-14 * np.abs(want).max()
 
 
+def test_roots_of_equal_layers():
+    # c1 = c2 = c and u1 = u2 = u: p = Q^2 - r c^4, so the roots are
+    # u -+ c sqrt(1 +- sqrt(r)) in closed form; the roots of Q1 and Q2
+    # coincide here (the inner pair must still be found), also after
+    # perturbations at the rounding level
+    rng = np.random.default_rng(18)
+    for _ in range(300):
+        u = rng.uniform(-1, 1) * 10.0 ** rng.integers(-14, 1)
+        cs = rng.uniform(1, 80)
+        r = rng.uniform(0, 0.999)
+        eps = rng.uniform(-1, 1, 3) * 1e-14 * np.array([1.0, cs, cs])
+        st, lam = O.roots2(u, u + eps[0], cs + eps[1], cs + eps[2], r)
+        c = math.sqrt(cs)
+        want = np.sort([u - c * math.sqrt(1 + math.sqrt(r)), u - c * math.sqrt(1 - math.sqrt(r)),
+                        u + c * math.sqrt(1 - math.sqrt(r)), u + c * math.sqrt(1 + math.sqrt(r))])
+        assert st == O.OM_OK, (u, cs, r)
+        assert np.abs(lam - want).max() <= 1e-9 * c
+
+
 def phys_flux2(W, eta, g=G):
     out = np.zeros(6)
     for k in range(2):

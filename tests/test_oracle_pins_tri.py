@@ -195,3 +195,16 @@ def test_numbering_independence_on_triangles():
     assert np.allclose(da, db, rtol=1e-13, atol=0)
     for a, b in zip(Wa, Wb):
         assert np.abs(a[cp] - b).max() <= 1e-12 * np.abs(a).max()
+
+
+def test_update2_at_is_the_update_restricted_to_the_cells():
+    d = I.tri_workload(12)
+    m = O.tri_mesh(d["xy"], d["tri"])
+    W = I.fields2_of(d)
+    full, st = O.update2(m, d["H"], W, G, d["r"], 0.05)
+    assert st == O.OM_OK
+    cells = np.array([0, 5, 77, d["n_cells"] - 1])
+    part, st = O.update2_at(m, d["H"], W, G, d["r"], 0.05, cells)
+    assert st == O.OM_OK
+    for k in range(6):
+        assert np.array_equal(part[k], full[k][cells])

@@ -16,8 +16,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswe.so")
-SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_cart2.cu", "swe_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "swe_internal.h"), os.path.join(ROOT, "include", "swe.h")]
+SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_cart2.cu", "swe_mesh.cu", "swe_mesh_prep.cpp",
+           "swe_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "swe_internal.h"), os.path.join(CSRC, "swe_roe2.cuh"),
+           os.path.join(ROOT, "include", "swe.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-ftz=true",
@@ -49,7 +51,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:

@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <new>
+#include <vector>
 
 #include "../../include/swe.h"
 #include "swe_internal.h"
@@ -44,6 +45,21 @@ struct swe_state {
   unsigned* h_err = nullptr;
   double* h_t = nullptr;
   unsigned sticky = 0;
+  // triangle meshes
+  bool mesh = false;
+  int64_t ncells = 0, nedges = 0;
+  int64_t estride = 0;               // elements between per-edge result arrays
+  void* ea = nullptr;                // int32 [nedges]
+  void* eb = nullptr;
+  void* enx = nullptr;               // T [nedges]
+  void* eny = nullptr;
+  void* elen = nullptr;
+  void* ebuf = nullptr;              // T [ne_fields * estride]
+  void* ref[3] = {nullptr};          // int32 [ncells]
+  void* inv_area = nullptr;          // T [ncells]
+  int32_t* new_of_old = nullptr;     // device [ncells]
+  int32_t* old_of_new = nullptr;
+  std::vector<int32_t> h_new_of_old;  // host copy (swe_cell_index)
 };
 
 namespace {
@@ -185,11 +201,64 @@ swe_status enqueue_step2(swe_state* s, double cfl) {
   return SWE_OK;
 }
 
+// Meshes: the gather pass of step n reduces into slot n % 3, the update of
+// step n reads it and zeroes slot (n + 1) % 3 (as for two layers on a grid).
+template <typename T>
+swe_status enqueue_mesh_check(swe_state* s) {
+  CK(cudaMemsetAsync(s->slots, 0, 3 * sizeof(uint64_t), s->stream));
+  Fields6<T> w{};
+  for (int f = 0; f < s->nf; ++f) w.p[f] = (const T*)s->w[0][f];
+  CK(launch_mesh_check<T>(w, s->nl, s->ncells, s->err, s->stream));
+  return SWE_OK;
+}
+
+template <typename T>
+swe_status enqueue_mesh_step(swe_state* s, double cfl) {
+  MeshStepArgs<T> f{};
+  MeshUpdateArgs<T> u{};
+  char* sl = (char*)s->slots;
+  for (int k = 0; k < s->nf; ++k) {
+    f.w[k] = (const T*)s->w[0][k];
+    f.R[k] = (T*)s->R[k];
+    u.w[k] = (T*)s->w[0][k];
+    u.R[k] = (const T*)s->R[k];
+  }
+  f.H = (const T*)s->H;
+  f.ea = (const int32_t*)s->ea;
+  f.eb = (const int32_t*)s->eb;
+  f.enx = (const T*)s->enx;
+  f.eny = (const T*)s->eny;
+  f.elen = (const T*)s->elen;
+  f.ebuf = (T*)s->ebuf;
+  f.estride = s->estride;
+  for (int k = 0; k < 3; ++k) f.ref[k] = (const int32_t*)s->ref[k];
+  f.inv_area = (const T*)s->inv_area;
+  f.ncells = u.ncells = s->ncells;
+  f.nedges = s->nedges;
+  f.g = (T)s->p.g;
+  f.r = (T)s->p.r;
+  f.tmax_out = sl + (s->step % 3) * sizeof(uint64_t);
+  f.err = u.err = s->err;
+  u.two_cfl = 2.0 * cfl;
+  u.tmax_in = sl + (s->step % 3) * sizeof(uint64_t);
+  u.tmax_clear = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
+  u.dt_hist = s->dt_hist;
+  u.t_dev = s->t_dev;
+  u.step = s->step;
+  CK(launch_mesh_step<T>(f, u, s->nl, s->stream));
+  s->step += 1;
+  return SWE_OK;
+}
+
 swe_status enqueue_dt0_any(swe_state* s) {
+  if (s->mesh)
+    return s->prec == 32 ? enqueue_mesh_check<float>(s) : enqueue_mesh_check<double>(s);
   if (s->nl == 2) return s->prec == 32 ? enqueue_check2<float>(s) : enqueue_check2<double>(s);
   return s->prec == 32 ? enqueue_dt0<float>(s) : enqueue_dt0<double>(s);
 }
 swe_status enqueue_step_any(swe_state* s, double cfl) {
+  if (s->mesh)
+    return s->prec == 32 ? enqueue_mesh_step<float>(s, cfl) : enqueue_mesh_step<double>(s, cfl);
   if (s->nl == 2)
     return s->prec == 32 ? enqueue_step2<float>(s, cfl) : enqueue_step2<double>(s, cfl);
   return s->prec == 32 ? enqueue_step<float>(s, cfl) : enqueue_step<double>(s, cfl);
@@ -203,6 +272,34 @@ swe_status upload(swe_state* s, void* const* dst, const void* const* src, int n)
   for (int f = 0; f < n; ++f)
     CK(cudaMemcpy2DAsync((char*)dst[f] + off, dpitch, src[f], row, row, (size_t)s->ny,
                          cudaMemcpyHostToDevice, s->stream));
+  return SWE_OK;
+}
+
+// Mesh fields: host (caller numbering) -> staging R -> internal order, and
+// back.  R is scratch that every step rewrites before reading.
+swe_status mesh_upload(swe_state* s, void* const* dst, const void* const* src, int n) {
+  const size_t bytes = (size_t)s->ncells * s->esz;
+  for (int f = 0; f < n; ++f)
+    CK(cudaMemcpyAsync(s->R[f], src[f], bytes, cudaMemcpyHostToDevice, s->stream));
+  if (s->prec == 32)
+    CK(launch_mesh_permute<float>((float* const*)dst, (const float* const*)s->R, n,
+                                  s->old_of_new, s->ncells, s->stream));
+  else
+    CK(launch_mesh_permute<double>((double* const*)dst, (const double* const*)s->R, n,
+                                   s->old_of_new, s->ncells, s->stream));
+  return SWE_OK;
+}
+
+swe_status mesh_download(swe_state* s, void* const* dst) {
+  if (s->prec == 32)
+    CK(launch_mesh_permute<float>((float* const*)s->R, (const float* const*)s->w[0], s->nf,
+                                  s->new_of_old, s->ncells, s->stream));
+  else
+    CK(launch_mesh_permute<double>((double* const*)s->R, (const double* const*)s->w[0], s->nf,
+                                   s->new_of_old, s->ncells, s->stream));
+  const size_t bytes = (size_t)s->ncells * s->esz;
+  for (int f = 0; f < s->nf; ++f)
+    CK(cudaMemcpyAsync(dst[f], s->R[f], bytes, cudaMemcpyDeviceToHost, s->stream));
   return SWE_OK;
 }
 
@@ -231,6 +328,62 @@ swe_status fill_pads(swe_state* s) {
   CK(launch_fill<T>((T*)s->H, n, T(0), s->stream));
   return SWE_OK;
 }
+
+swe_status check_params(const swe_params* params) {
+  if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
+  if (!finite_pos(params->g)) return SWE_ERR_ARG;
+  if (!(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
+  if (params->n_layers != 1 && params->n_layers != 2) return SWE_ERR_ARG;
+  if (params->n_layers == 1 && params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->n_layers == 2) {
+    if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
+    if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
+  }
+  return SWE_OK;
+}
+
+void init_common(swe_state* s, const swe_params* params) {
+  s->p = *params;
+  s->prec = params->precision;
+  s->nl = params->n_layers;
+  s->nf = s->nl == 2 ? 6 : 4;
+  s->esz = s->prec == 32 ? 4 : 8;
+  s->stream = (cudaStream_t)params->stream;
+}
+
+// Carve the slots, dt history, clock and error word from p; pinned readback.
+swe_status carve_aux(swe_state* s, char* p) {
+  s->slots = p;
+  p += 256;
+  s->dt_hist = (double*)p;
+  p += round_up((int64_t)kHistCap * 8, 256);
+  s->t_dev = (double*)p;
+  p += 256;
+  s->err = (unsigned*)p;
+  cudaError_t e = cudaMallocHost(&s->h_dt, 64);
+  if (e != cudaSuccess) {
+    s->h_dt = nullptr;
+    return cuda_status(e);
+  }
+  s->h_err = (unsigned*)(s->h_dt + 1);
+  s->h_t = s->h_dt + 2;
+  return SWE_OK;
+}
+constexpr int64_t kAuxBytes = 256 + ((int64_t)kHistCap * 8 + 255) / 256 * 256 + 256 + 256;
+
+// Synchronous copy of a double host array to the device as T.
+template <typename T>
+swe_status put_as(void* dst, const std::vector<double>& src) {
+  if (sizeof(T) == sizeof(double)) {
+    CK(cudaMemcpy(dst, src.data(), src.size() * sizeof(double), cudaMemcpyHostToDevice));
+    return SWE_OK;
+  }
+  std::vector<T> tmp(src.begin(), src.end());
+  CK(cudaMemcpy(dst, tmp.data(), tmp.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return SWE_OK;
+}
+
+constexpr int64_t kMaxMeshCells = (int64_t)1 << 28;
 
 }  // namespace
 
@@ -269,14 +422,9 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
     if (!W0[f]) return SWE_ERR_ARG;
   if (grid->nx < 1 || grid->ny < 1) return SWE_ERR_ARG;
   if (!finite_pos(grid->dx) || !finite_pos(grid->dy)) return SWE_ERR_ARG;
-  if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
-  if (!finite_pos(params->g)) return SWE_ERR_ARG;
-  if (!(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
-  if (params->n_layers != 1 && params->n_layers != 2) return SWE_ERR_ARG;
-  if (params->n_layers == 1 && params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
-  if (params->n_layers == 2) {
-    if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
-    if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
+  {
+    const swe_status pst = check_params(params);
+    if (pst != SWE_OK) return pst;
   }
   // index arithmetic inside the kernels is 32-bit per row and column
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
@@ -287,12 +435,7 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   s->ny = grid->ny;
   s->dx = grid->dx;
   s->dy = grid->dy;
-  s->p = *params;
-  s->prec = params->precision;
-  s->nl = params->n_layers;
-  s->nf = s->nl == 2 ? 6 : 4;
-  s->esz = s->prec == 32 ? 4 : 8;
-  s->stream = (cudaStream_t)params->stream;
+  init_common(s, params);
   if (s->nl == 1) {
     s->pitch = (int)(s->prec == 32 ? grid_pitch<float>(s->nx) : grid_pitch<double>(s->nx));
     s->rows = s->ny + 2 * kPadY;
@@ -309,7 +452,7 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   const int64_t felems = s->rows * s->pitch;
   const int64_t fbytes = round_up(felems * (int64_t)s->esz, 256);
   s->field_stride = fbytes / (int64_t)s->esz;
-  const int64_t aux = 256 + round_up((int64_t)kHistCap * 8, 256) + 256 + 256;
+  const int64_t aux = kAuxBytes;
   const int nalloc = s->nl == 2 ? 13 : 9;  // fields (+ scratch) + H
   s->dev_bytes = (size_t)(nalloc * fbytes + aux);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
@@ -336,20 +479,7 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   s->H = p;
   p += fbytes;
-  s->slots = p;
-  p += 256;
-  s->dt_hist = (double*)p;
-  p += round_up((int64_t)kHistCap * 8, 256);
-  s->t_dev = (double*)p;
-  p += 256;
-  s->err = (unsigned*)p;
-  e = cudaMallocHost(&s->h_dt, 64);
-  if (e != cudaSuccess) {
-    s->h_dt = nullptr;
-    return fail(cuda_status(e));
-  }
-  s->h_err = (unsigned*)(s->h_dt + 1);
-  s->h_t = s->h_dt + 2;
+  if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
 
   if (s->nl == 1) {
     st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
@@ -372,13 +502,159 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   return SWE_OK;
 }
 
+swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* const* W0,
+                           const swe_params* params, swe_state** out) {
+  if (!out) return SWE_ERR_ARG;
+  *out = nullptr;
+  if (!mesh || !H || !W0 || !params) return SWE_ERR_ARG;
+  {
+    const swe_status pst = check_params(params);
+    if (pst != SWE_OK) return pst;
+  }
+  const int nfields = params->n_layers == 2 ? 6 : 4;
+  for (int f = 0; f < nfields; ++f)
+    if (!W0[f]) return SWE_ERR_ARG;
+  if (!mesh->xy || !mesh->tri || mesh->n_vertices < 3 || mesh->n_cells < 1) return SWE_ERR_ARG;
+  if (mesh->n_vertices > INT32_MAX || mesh->n_cells > kMaxMeshCells) return SWE_ERR_ARG;
+  if (mesh->reorder != 0 && mesh->reorder != 1) return SWE_ERR_ARG;
+
+  MeshPrep prep;
+  const int rc = prepare_mesh(mesh->n_vertices, mesh->xy, mesh->n_cells, mesh->tri,
+                              mesh->reorder == 1, &prep);
+  if (rc == -3) return SWE_ERR_OOM;
+  if (rc != 0) return SWE_ERR_ARG;
+
+  swe_state* s = new (std::nothrow) swe_state();
+  if (!s) return SWE_ERR_OOM;
+  auto fail = [&](swe_status e) {
+    swe_destroy(s);
+    return e;
+  };
+  init_common(s, params);
+  s->mesh = true;
+  s->ncells = prep.ncells;
+  s->nedges = prep.nedges;
+  s->nx = (int)prep.ncells;
+  s->ny = 1;
+  try {
+    s->h_new_of_old = prep.new_of_old;
+  } catch (const std::bad_alloc&) {
+    return fail(SWE_ERR_OOM);
+  }
+  const int64_t nc = s->ncells, ne = s->nedges, esz = (int64_t)s->esz;
+  const int nef = s->nl == 2 ? MeshLayout<2>::ne : MeshLayout<1>::ne;
+  const int64_t fb = round_up(nc * esz, 256), ib = round_up(nc * 4, 256);
+  const int64_t et = round_up(ne * esz, 256), ei = round_up(ne * 4, 256);
+  s->field_stride = fb / esz;
+  s->estride = et / esz;
+  s->dev_bytes = (size_t)((2 * s->nf + 2) * fb + 5 * ib + 2 * ei + (3 + nef) * et + kAuxBytes);
+  cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
+  if (e != cudaSuccess) {
+    s->dev = nullptr;
+    return fail(cuda_status(e));
+  }
+  char* p = (char*)s->dev;
+  auto take = [&](int64_t bytes) {
+    void* q = p;
+    p += bytes;
+    return q;
+  };
+  for (int f = 0; f < s->nf; ++f) s->w[0][f] = take(fb);
+  for (int f = 0; f < s->nf; ++f) s->R[f] = take(fb);
+  s->H = take(fb);
+  s->inv_area = take(fb);
+  for (int k = 0; k < 3; ++k) s->ref[k] = take(ib);
+  s->new_of_old = (int32_t*)take(ib);
+  s->old_of_new = (int32_t*)take(ib);
+  s->ea = take(ei);
+  s->eb = take(ei);
+  s->enx = take(et);
+  s->eny = take(et);
+  s->elen = take(et);
+  s->ebuf = take(nef * et);
+  swe_status st;
+  if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
+
+  // geometry and orderings (synchronous copies from the temporary arrays)
+  auto put_i32 = [&](void* dst, const int32_t* src, int64_t n) {
+    return cuda_status(cudaMemcpy(dst, src, (size_t)n * 4, cudaMemcpyHostToDevice));
+  };
+  if ((st = put_i32(s->ea, prep.ea.data(), ne)) != SWE_OK) return fail(st);
+  if ((st = put_i32(s->eb, prep.eb.data(), ne)) != SWE_OK) return fail(st);
+  for (int k = 0; k < 3; ++k)
+    if ((st = put_i32(s->ref[k], prep.ref.data() + k * nc, nc)) != SWE_OK) return fail(st);
+  if ((st = put_i32(s->new_of_old, prep.new_of_old.data(), nc)) != SWE_OK) return fail(st);
+  if ((st = put_i32(s->old_of_new, prep.old_of_new.data(), nc)) != SWE_OK) return fail(st);
+  try {
+    void* dsts[4] = {s->enx, s->eny, s->elen, s->inv_area};
+    const std::vector<double>* srcs[4] = {&prep.enx, &prep.eny, &prep.elen, &prep.inv_area};
+    for (int k = 0; k < 4; ++k) {
+      st = s->prec == 32 ? put_as<float>(dsts[k], *srcs[k]) : put_as<double>(dsts[k], *srcs[k]);
+      if (st != SWE_OK) return fail(st);
+    }
+  } catch (const std::bad_alloc&) {
+    return fail(SWE_ERR_OOM);
+  }
+  // H and the initial state, caller numbering -> internal order
+  void* hdst[1] = {s->H};
+  const void* hsrc[1] = {H};
+  if ((st = mesh_upload(s, hdst, hsrc, 1)) != SWE_OK) return fail(st);
+  if ((st = mesh_upload(s, s->w[0], W0, s->nf)) != SWE_OK) return fail(st);
+  if ((e = cudaMemsetAsync(s->t_dev, 0, 256 + 256, s->stream)) != cudaSuccess)
+    return fail(cuda_status(e));
+  s->cur = 0;
+  s->step = 0;
+  if ((st = enqueue_dt0_any(s)) != SWE_OK) return fail(st);
+  if ((st = read_err(s)) != SWE_OK) return fail(st);
+  if (s->sticky) return fail(SWE_ERR_ARG);
+  *out = s;
+  return SWE_OK;
+}
+
+swe_status swe_mesh_info(const swe_mesh* mesh, int32_t* new_of_old, int64_t* n_edges,
+                         int64_t* bandwidth) {
+  if (!mesh || !mesh->xy || !mesh->tri || mesh->n_vertices < 3 || mesh->n_cells < 1)
+    return SWE_ERR_ARG;
+  if (mesh->n_vertices > INT32_MAX || mesh->n_cells > kMaxMeshCells) return SWE_ERR_ARG;
+  if (mesh->reorder != 0 && mesh->reorder != 1) return SWE_ERR_ARG;
+  MeshPrep prep;
+  const int rc = prepare_mesh(mesh->n_vertices, mesh->xy, mesh->n_cells, mesh->tri,
+                              mesh->reorder == 1, &prep);
+  if (rc == -3) return SWE_ERR_OOM;
+  if (rc != 0) return SWE_ERR_ARG;
+  if (new_of_old)
+    memcpy(new_of_old, prep.new_of_old.data(), (size_t)prep.ncells * sizeof(int32_t));
+  if (n_edges) *n_edges = prep.nedges;
+  if (bandwidth) {
+    int64_t bw = 0;
+    for (int64_t e = 0; e < prep.nedges; ++e)
+      if (prep.eb[e] >= 0 && prep.eb[e] - prep.ea[e] > bw) bw = prep.eb[e] - prep.ea[e];
+    *bandwidth = bw;
+  }
+  return SWE_OK;
+}
+
+swe_status swe_cell_index(const swe_state* s, int64_t* idx) {
+  if (!s || !idx) return SWE_ERR_ARG;
+  if (s->mesh) {
+    for (int64_t c = 0; c < s->ncells; ++c) idx[c] = s->h_new_of_old[c];
+    return SWE_OK;
+  }
+  for (int64_t j = 0; j < s->ny; ++j)
+    for (int64_t i = 0; i < s->nx; ++i)
+      idx[j * s->nx + i] = (j + kPadY) * s->pitch + i + kPadX;
+  return SWE_OK;
+}
+
 swe_status swe_set_state(swe_state* s, const void* const* fields, double t) {
   if (!s || !fields) return SWE_ERR_ARG;
   for (int f = 0; f < s->nf; ++f)
     if (!fields[f]) return SWE_ERR_ARG;
   if (!isfinite(t)) return SWE_ERR_ARG;
   swe_status st;
-  if ((st = upload(s, s->w[s->cur], fields, s->nf)) != SWE_OK) return st;
+  if (s->mesh) st = mesh_upload(s, s->w[0], fields, s->nf);
+  else st = upload(s, s->w[s->cur], fields, s->nf);
+  if (st != SWE_OK) return st;
   *s->h_t = t;
   CK(cudaMemcpyAsync(s->t_dev, s->h_t, sizeof(double), cudaMemcpyHostToDevice, s->stream));
   CK(cudaMemsetAsync(s->err, 0, sizeof(unsigned), s->stream));
@@ -423,12 +699,17 @@ swe_status swe_get_state(const swe_state* cs, void* const* fields_out, double* t
   if (!s || !fields_out) return SWE_ERR_ARG;
   for (int f = 0; f < s->nf; ++f)
     if (!fields_out[f]) return SWE_ERR_ARG;
-  const size_t row = (size_t)s->nx * s->esz;
-  const size_t spitch = (size_t)s->pitch * s->esz;
-  const size_t off = ((size_t)kPadY * s->pitch + kPadX) * s->esz;
-  for (int f = 0; f < s->nf; ++f)
-    CK(cudaMemcpy2DAsync(fields_out[f], row, (const char*)s->w[s->cur][f] + off, spitch, row,
-                         (size_t)s->ny, cudaMemcpyDeviceToHost, s->stream));
+  if (s->mesh) {
+    swe_status st = mesh_download(s, fields_out);
+    if (st != SWE_OK) return st;
+  } else {
+    const size_t row = (size_t)s->nx * s->esz;
+    const size_t spitch = (size_t)s->pitch * s->esz;
+    const size_t off = ((size_t)kPadY * s->pitch + kPadX) * s->esz;
+    for (int f = 0; f < s->nf; ++f)
+      CK(cudaMemcpy2DAsync(fields_out[f], row, (const char*)s->w[s->cur][f] + off, spitch, row,
+                           (size_t)s->ny, cudaMemcpyDeviceToHost, s->stream));
+  }
   CK(cudaMemcpyAsync(s->h_t, s->t_dev, sizeof(double), cudaMemcpyDeviceToHost, s->stream));
   CK(cudaStreamSynchronize(s->stream));
   if (t_out) *t_out = *s->h_t;
@@ -473,6 +754,17 @@ swe_status swe_get_info(const swe_state* s, swe_info* info) {
   info->segments = s->nsegs;
   info->warps_per_block = kWarpsPerBlock;
   info->n_layers = s->nl;
+  if (s->mesh) {
+    info->pitch = 0;
+    info->field_offset = 0;
+    info->n_cells = s->ncells;
+    info->n_edges = s->nedges;
+    info->mesh = 1;
+  } else {
+    info->n_cells = (int64_t)s->nx * s->ny;
+    info->n_edges = (int64_t)(s->nx + 1) * s->ny + (int64_t)s->nx * (s->ny + 1);
+    info->mesh = 0;
+  }
   return SWE_OK;
 }
 

@@ -16,184 +16,19 @@
 //                        which fixes dt of this step;
 //   cart2_update_kernel  W -= (dt/dx) R in place, checks, dt bookkeeping.
 //
-// The eigenvalues of A_ij are the roots of the quartic
-//   p(l) = Q1(l) Q2(l) - r c1^2 c2^2,   Q_k(l) = (l - u_k)^2 - c_k^2.
-// The outer two are found by Newton from bounds where p > 0 (p is convex and
-// monotone there, so the iterates approach the root from outside without
-// overshooting); the inner pair comes from deflating p by the outer pair and
-// is polished by Newton on p.  A complex inner pair (loss of hyperbolicity)
-// sets an error bit.  With right eigenvectors K_k = (1, l_k, m_k, l_k m_k),
-// m_k = Q1(l_k)/c1^2, the left eigenvectors of A_ij are proportional to
-// (l - 2u1, 1, c1^2 (l - 2u2)/Q2, c1^2/Q2), which gives the coordinates of d
-// in the eigenvector basis without a linear solve:
-//   alpha_k = [Q2(l_k)((l_k - 2u1) d1 + d2) + c1^2 ((l_k - 2u2) d3 + d4)] / p'(l_k).
-// Then P^- d = sum_k w_k alpha_k K_k with w_k = (1 - sgn l_k)/2.
+// The edge flux itself (quartic roots, closed-form P^- d) is in swe_roe2.cuh.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "swe_internal.h"
+#include "swe_roe2.cuh"
 
 namespace swe {
 namespace {
 
-constexpr unsigned kFull2 = 0xffffffffu;
-
-template <typename T> struct M2;
-template <> struct M2<float> {
-  __device__ static __forceinline__ float rsq(float x) { return rsqrtf(x); }
-  __device__ static __forceinline__ float rcp(float x) {  // MUFU approximation
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-  }
-  __device__ static __forceinline__ float sq(float x) { return sqrtf(x); }
-  __device__ static __forceinline__ float big() { return 3.402823466e38f; }
-};
-template <> struct M2<double> {
-  __device__ static __forceinline__ double rsq(double x) { return rsqrt(x); }
-  __device__ static __forceinline__ double rcp(double x) { return __drcp_rn(x); }
-  __device__ static __forceinline__ double sq(double x) { return sqrt(x); }
-  __device__ static __forceinline__ double big() { return 1.7976931348623157e308; }
-};
-
-// Newton iterations: the outer roots converge quadratically from a bound a
-// fixed fraction of c away; the inner ones start from the deflated estimate.
-template <typename T> struct Iters;
-template <> struct Iters<float> { static constexpr int outer = 7, inner = 2; };
-template <> struct Iters<double> { static constexpr int outer = 9, inner = 3; };
-
 // per-cell quantities in shared memory
 enum { C_H1, C_Q1X, C_Q1Y, C_H2, C_Q2X, C_Q2Y, C_H, C_S1, C_S2, C_RS1, C_RS2, NCQ };
-// per-edge results in shared memory
-enum { E_M1, E_PM1, E_PS1, E_T1, E_M2, E_PM2, E_PS2, E_T2, E_D, NEQ };
-
-// One side of an edge in the frame of its normal: per layer the depth, its
-// square root and inverse square root, the normal and tangential discharge.
-template <typename T>
-struct Side2 {
-  T h[2], s[2], rs[2], qn[2], qt[2], H;
-};
-
-template <typename T>
-__device__ __forceinline__ void mirror2(Side2<T>& g, const Side2<T>& a) {
-  g = a;
-  g.qn[0] = -a.qn[0];
-  g.qn[1] = -a.qn[1];
-}
-
-template <typename T>
-struct Quartic {
-  T u1, u2, c1s, c2s, rc;
-  __device__ __forceinline__ T q1(T l) const { return (l - u1) * (l - u1) - c1s; }
-  __device__ __forceinline__ T q2(T l) const { return (l - u2) * (l - u2) - c2s; }
-  __device__ __forceinline__ T p(T l) const { return q1(l) * q2(l) - rc; }
-  __device__ __forceinline__ T dp(T l) const {
-    return T(2) * ((l - u1) * q2(l) + (l - u2) * q1(l));
-  }
-};
-
-// IR-Roe flux of one edge, two layers.  Writes the edge results; returns
-// false when A_ij has a complex pair of eigenvalues.
-template <typename T>
-__device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
-                                      bool wall, T* out) {
-  // Roe averages per layer: sqrt(h)-weighted normal velocity, arithmetic
-  // depth; c_k^2 = g hbar_k
-  T un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const T va = a.qn[k] * a.rs[k], vb = b.qn[k] * b.rs[k];
-    un[k] = (va + vb) * M2<T>::rcp(a.s[k] + b.s[k]);
-    cs[k] = gh * (a.h[k] + b.h[k]);
-    const T iha = a.rs[k] * a.rs[k], ihb = b.rs[k] * b.rs[k];
-    qu_a[k] = a.qn[k] * a.qn[k] * iha;
-    qu_b[k] = b.qn[k] * b.qn[k] * ihb;
-    ut_a[k] = a.qt[k] * iha;
-    ut_b[k] = b.qt[k] * ihb;
-  }
-  Quartic<T> q{un[0], un[1], cs[0], cs[1], r * cs[0] * cs[1]};
-  const T c1 = M2<T>::sq(cs[0]), c2 = M2<T>::sq(cs[1]);
-  // outer roots: from below / above, where p > 0, p convex and monotone
-  T l1 = fmin(un[0] - T(1.5) * c1, un[1] - T(1.5) * c2);
-  T l4 = fmax(un[0] + T(1.5) * c1, un[1] + T(1.5) * c2);
-#pragma unroll
-  for (int it = 0; it < Iters<T>::outer; ++it) {
-    l1 -= q.p(l1) * M2<T>::rcp(q.dp(l1));
-    l4 -= q.p(l4) * M2<T>::rcp(q.dp(l4));
-  }
-  // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
-  const T p3 = T(-2) * (un[0] + un[1]);
-  const T p2 = (un[0] * un[0] - cs[0]) + (un[1] * un[1] - cs[1]) + T(4) * un[0] * un[1];
-  const T ss = l1 + l4, pp = l1 * l4;
-  const T bb = p3 + ss;
-  const T cc = p2 + ss * bb - pp;
-  const T disc = bb * bb - T(4) * cc;
-  const bool hyper = disc > T(0);
-  const T sd = M2<T>::sq(hyper ? disc : T(0));
-  T l2 = T(0.5) * (-bb - sd), l3 = T(0.5) * (-bb + sd);
-#pragma unroll
-  for (int it = 0; it < Iters<T>::inner; ++it) {
-    l2 -= q.p(l2) * M2<T>::rcp(q.dp(l2));
-    l3 -= q.p(l3) * M2<T>::rcp(q.dp(l3));
-  }
-  // fluctuation d = F_1(W_j) - F_1(W_i) - B_ij (W_j - W_i) - S_ij (H_j - H_i)
-  // (pressure differences written g hbar_k (h_k,j - h_k,i))
-  const T dh1 = b.h[0] - a.h[0], dh2 = b.h[1] - a.h[1], dH = b.H - a.H;
-  const T d1 = b.qn[0] - a.qn[0];
-  const T d2 = (qu_b[0] - qu_a[0]) + cs[0] * ((dh1 + dh2) - dH);
-  const T d3 = b.qn[1] - a.qn[1];
-  const T d4 = (qu_b[1] - qu_a[1]) + cs[1] * ((dh2 + r * dh1) - dH);
-  // P^- d = sum_k w_k alpha_k K_k
-  const T lam[4] = {l1, l2, l3, l4};
-  const T ic1s = M2<T>::rcp(cs[0]);
-  T pd0 = T(0), pd1 = T(0), pd2 = T(0), pd3 = T(0);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const T l = lam[k];
-    const T w = (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
-    const T Q1 = q.q1(l), Q2 = q.q2(l);
-    const T num = Q2 * ((l - T(2) * un[0]) * d1 + d2) + cs[0] * ((l - T(2) * un[1]) * d3 + d4);
-    const T alpha = w * num * M2<T>::rcp(q.dp(l));
-    const T mu = Q1 * ic1s;
-    pd0 += alpha;
-    pd1 += alpha * l;
-    pd2 += alpha * mu;
-    pd3 += alpha * l * mu;
-  }
-  T m1 = a.qn[0] + pd0;
-  T m2 = a.qn[1] + pd2;
-  if (wall) {  // a reflective wall passes no mass (algebraically 0)
-    m1 = T(0);
-    m2 = T(0);
-  }
-  out[E_M1] = m1;
-  out[E_PM1] = pd1;
-  out[E_PS1] = d2 - pd1;
-  out[E_T1] = m1 * (m1 > T(0) ? ut_a[0] : ut_b[0]);
-  out[E_M2] = m2;
-  out[E_PM2] = pd3;
-  out[E_PS2] = d4 - pd3;
-  out[E_T2] = m2 * (m2 > T(0) ? ut_a[1] : ut_b[1]);
-  out[E_D] = fmax(fabs(l1), fabs(l4));
-  return hyper;
-}
-
-template <typename T>
-__device__ __forceinline__ void atomic_max_pos2(void* slot, T v);
-template <>
-__device__ __forceinline__ void atomic_max_pos2<float>(void* slot, float v) {
-  atomicMax(reinterpret_cast<unsigned int*>(slot), __float_as_uint(v));
-}
-template <>
-__device__ __forceinline__ void atomic_max_pos2<double>(void* slot, double v) {
-  atomicMax(reinterpret_cast<unsigned long long*>(slot),
-            static_cast<unsigned long long>(__double_as_longlong(v)));
-}
-template <typename T>
-__device__ __forceinline__ T nanmax2(T acc, T x) {
-  return (x > acc || x != x) ? x : acc;
-}
 
 constexpr int TX = kTile2X;
 

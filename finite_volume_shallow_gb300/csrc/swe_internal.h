@@ -14,6 +14,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace swe {
 
 constexpr int kPadX = 2;
@@ -123,6 +125,92 @@ cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStr
 template <typename T>
 cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsigned* err,
                           cudaStream_t st);
+
+// ---- triangle meshes (swe_mesh.cu, swe_mesh_prep.cpp) ------------------------
+// A mesh state keeps its cells in an internal order (reverse Cuthill-McKee
+// unless the caller asked for its own), one contiguous array per field.
+// Every edge is stored once: cells a < b (b = -1 on a wall), the unit normal
+// (nx, ny) pointing from a to b and the length L.  Each cell lists its three
+// edges as ref = 2 * edge + side (side 0: the cell is a, 1: it is b), in the
+// order of its vertices (edge k joins vertex k and vertex k + 1).
+//
+// The edge pass writes per edge, already multiplied by L and rotated back to
+// x / y components, what each side adds to its residual:
+//   two layers  [0] m1  [1] m2           mass fluxes a -> b (a adds, b subtracts)
+//               [2..5] a: (x, y) momentum of layer 1, then of layer 2
+//               [6..9] b: the same for b
+//               [10] L * max |lambda|
+//   one layer   [0] m  [1] m C_upwind    mass and pollutant fluxes a -> b
+//               [2, 3] a: (x, y) momentum   [4, 5] b: (x, y) momentum
+//               [6] L * max |lambda|
+template <int NL> struct MeshLayout;
+template <> struct MeshLayout<1> {
+  static constexpr int nf = 4, ne = 7, a_mom = 2, b_mom = 4, d = 6;
+};
+template <> struct MeshLayout<2> {
+  static constexpr int nf = 6, ne = 11, a_mom = 2, b_mom = 6, d = 10;
+};
+
+template <typename T>
+struct MeshStepArgs {
+  const T* w[6];          // state, internal cell order
+  const T* H;
+  T* R[6];                // residual / area (scratch)
+  const int32_t* ea;      // edge -> cell a
+  const int32_t* eb;      // edge -> cell b, or -1 (wall)
+  const T* enx;           // unit normal from a to b
+  const T* eny;
+  const T* elen;          // edge length
+  T* ebuf;                // per-edge results: field q of edge e at q * estride + e
+  int64_t estride;
+  const int32_t* ref[3];  // per cell: 2 * edge + side
+  const T* inv_area;      // 1 / |V_i|
+  int64_t ncells, nedges;
+  T g, r;
+  void* tmax_out;         // max over cells of sum L max|lambda| / |V_i| (starts at 0)
+  unsigned* err;
+};
+template <typename T>
+struct MeshUpdateArgs {
+  T* w[6];
+  const T* R[6];
+  int64_t ncells;
+  double two_cfl;
+  const void* tmax_in;
+  void* tmax_clear;
+  double* dt_hist;
+  double* t_dev;
+  int64_t step;
+  unsigned* err;
+};
+
+template <typename T>
+cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& u, int n_layers,
+                             cudaStream_t st);
+template <typename T>
+cudaError_t launch_mesh_check(const Fields6<T>& w, int n_layers, int64_t ncells, unsigned* err,
+                              cudaStream_t st);
+// dst[f][i] = src[f][idx[i]] for f < nf, i < n
+template <typename T>
+cudaError_t launch_mesh_permute(T* const* dst, const T* const* src, int nf, const int32_t* idx,
+                                int64_t n, cudaStream_t st);
+
+// Host preparation of a triangle mesh (swe_mesh_prep.cpp): geometry in
+// double precision, edges, cell order and the per-cell edge references.
+struct MeshPrep {
+  int64_t ncells = 0, nedges = 0;
+  std::vector<int32_t> ea, eb;            // [nedges]
+  std::vector<double> enx, eny, elen;     // [nedges]
+  std::vector<int32_t> ref;               // [3 * ncells]: ref k of cell c at k * ncells + c
+  std::vector<double> inv_area;           // [ncells], internal order
+  std::vector<int32_t> new_of_old;        // caller cell -> internal cell
+  std::vector<int32_t> old_of_new;        // internal cell -> caller cell
+};
+// 0 on success; -1 for an invalid mesh (index out of range, non-finite
+// coordinate, clockwise or degenerate triangle, an edge used by more than two
+// triangles or twice in the same direction); -3 when host memory runs out.
+int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const int32_t* tri,
+                 bool reorder, MeshPrep* out);
 
 // host-side launchers (swe_cart1.cu)
 template <typename T>

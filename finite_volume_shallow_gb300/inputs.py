@@ -248,15 +248,18 @@ def tri_centroids(xy, tri):
     return xy[tri].mean(axis=1)
 
 
-def tri_workload(n, seed=1005, jitter=0.2, r=0.98, n_hills=8, bump=0.5):
+def tri_workload(n, seed=1005, jitter=0.2, r=0.98, n_hills=8, bump=0.5, sigma_scale=None):
     """The two-layer triangle-mesh workload on n x n unit squares (see the
     module docstring); the state is sampled at cell centroids.  Draw order:
     the mesh (jitter, permutation), then the hills (amplitude, width, centre)
-    and the interface bump (width, centre)."""
+    and the interface bump (width, centre).  Widths are U[50, 300] times
+    ``sigma_scale``, by default n / 20480 (the 2048 x 10 m domain of the hills
+    workload mapped onto the n x n square: 2.5 to 15 squares at n = 1024);
+    small test meshes pass a larger scale to keep their features resolved."""
     xy, tri = square_tri_mesh(n, side=1.0, jitter=jitter, seed=seed)
     rng = np.random.default_rng(seed + 7919)
     L = float(n)
-    scale = n / 20480.0
+    scale = n / 20480.0 if sigma_scale is None else float(sigma_scale)
     amp = rng.uniform(0.2, 0.8, n_hills)
     sig = rng.uniform(50.0, 300.0, n_hills) * scale
     cx = rng.uniform(0.0, L, n_hills)
@@ -273,6 +276,48 @@ def tri_workload(n, seed=1005, jitter=0.2, r=0.98, n_hills=8, bump=0.5):
     d = dict(xy=xy, tri=tri, n_cells=tri.shape[0], r=r, n_layers=2, mesh=True)
     for k, v in (("H", H), ("h1", h1), ("q1x", z), ("q1y", z), ("h2", H - h1), ("q2x", z),
                  ("q2y", z)):
+        d[k] = np.ascontiguousarray(v, dtype=np.float64)
+    return d
+
+
+def tri_workload1(n, m=None, seed=1006, jitter=0.2, umax=0.1, n_hills=6, n_pulses=4):
+    """A one-layer triangle-mesh workload with a pollutant on n x m unit
+    squares: Gaussian hills under a 2 m deep surface (H = 3 - z_b, surface at
+    h - H = 2), Gaussian surface pulses of 0.5 m, velocities U[-umax, umax]
+    per component, C uniform in [0, 1] per block of 4 x 4 squares.  Draw
+    order: the mesh (jitter, permutation), hills (amplitude, width, centre x,
+    centre y), pulses (width, centre x, centre y), velocities (x, then y),
+    block concentrations."""
+    m = n if m is None else m
+    xy, tri = square_tri_mesh(n, m, side=1.0, jitter=jitter, seed=seed)
+    rng = np.random.default_rng(seed + 7919)
+    cxy = tri_centroids(xy, tri)
+    size = float(min(n, m))
+    zb = np.zeros(tri.shape[0])
+    amp = rng.uniform(0.2, 0.8, n_hills)
+    sig = rng.uniform(0.05, 0.2, n_hills) * size
+    hx = rng.uniform(0.0, n, n_hills)
+    hy = rng.uniform(0.0, m, n_hills)
+    for a_, s_, x0, y0 in zip(amp, sig, hx, hy):
+        zb += a_ * np.exp(-((cxy[:, 0] - x0) ** 2 + (cxy[:, 1] - y0) ** 2) / (2 * s_ * s_))
+    eta = np.full(tri.shape[0], 2.0)
+    ps = rng.uniform(0.05, 0.15, n_pulses) * size
+    px = rng.uniform(0.0, n, n_pulses)
+    py = rng.uniform(0.0, m, n_pulses)
+    for s_, x0, y0 in zip(ps, px, py):
+        eta += 0.5 * np.exp(-((cxy[:, 0] - x0) ** 2 + (cxy[:, 1] - y0) ** 2) / (2 * s_ * s_))
+    H = 3.0 - zb
+    h = H + eta
+    ux = rng.uniform(-umax, umax, h.size)
+    uy = rng.uniform(-umax, umax, h.size)
+    nbx, nby = (n + 3) // 4, (m + 3) // 4
+    table = rng.uniform(0.0, 1.0, (nby, nbx))
+    bx = np.minimum((cxy[:, 0] // 4).astype(np.int64), nbx - 1)
+    by = np.minimum((cxy[:, 1] // 4).astype(np.int64), nby - 1)
+    C = table[by, bx]
+    d = dict(xy=xy, tri=tri, n_cells=tri.shape[0], n_layers=1, mesh=True, g=G_DEFAULT,
+             cfl=CFL_DEFAULT)
+    for k, v in (("H", H), ("h", h), ("qx", h * ux), ("qy", h * uy), ("hC", h * C)):
         d[k] = np.ascontiguousarray(v, dtype=np.float64)
     return d
 

@@ -5,7 +5,8 @@ built or loaded, every call raises.
 
 Host arrays may be numpy arrays or CPU torch tensors (pinned or not) of the
 state's precision (float32 for precision 32, float64 for 64), each holding
-nx*ny values in row-major (x fastest) order.
+nx*ny values in row-major (x fastest) order on a grid, or one value per
+triangle in the caller's numbering on a mesh.
 """
 from __future__ import annotations
 
@@ -39,6 +40,11 @@ class _Grid(C.Structure):
     _fields_ = [("nx", C.c_int32), ("ny", C.c_int32), ("dx", C.c_double), ("dy", C.c_double)]
 
 
+class _Mesh(C.Structure):
+    _fields_ = [("n_vertices", C.c_int64), ("xy", C.c_void_p), ("n_cells", C.c_int64),
+                ("tri", C.c_void_p), ("reorder", C.c_int32)]
+
+
 class _Params(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("precision", C.c_int32), ("pollutant", C.c_int32),
                 ("g", C.c_double), ("r", C.c_double), ("cfl", C.c_double),
@@ -49,7 +55,8 @@ class _Info(C.Structure):
     _fields_ = [("steps", C.c_int64), ("t", C.c_double), ("nx", C.c_int32), ("ny", C.c_int32),
                 ("precision", C.c_int32), ("pitch", C.c_int32), ("field_offset", C.c_int64),
                 ("device_bytes", C.c_int64), ("bands", C.c_int32), ("segments", C.c_int32),
-                ("warps_per_block", C.c_int32), ("n_layers", C.c_int32)]
+                ("warps_per_block", C.c_int32), ("n_layers", C.c_int32),
+                ("n_cells", C.c_int64), ("n_edges", C.c_int64), ("mesh", C.c_int32)]
 
 
 _lib = None
@@ -70,6 +77,9 @@ def load(build_if_needed: bool = True):
     L = C.CDLL(path)
     vp, i32, i64, d = C.c_void_p, C.c_int32, C.c_int64, C.c_double
     L.swe_create_grid.argtypes = [C.POINTER(_Grid), vp, vp, C.POINTER(_Params), C.POINTER(vp)]
+    L.swe_create_mesh.argtypes = [C.POINTER(_Mesh), vp, vp, C.POINTER(_Params), C.POINTER(vp)]
+    L.swe_cell_index.argtypes = [vp, vp]
+    L.swe_mesh_info.argtypes = [C.POINTER(_Mesh), vp, vp, vp]
     L.swe_step.argtypes = [vp, d, C.POINTER(d)]
     L.swe_run.argtypes = [vp, i64]
     L.swe_get_state.argtypes = [vp, vp, C.POINTER(d)]
@@ -82,8 +92,10 @@ def load(build_if_needed: bool = True):
     L.swe_destroy.restype = None
     L.swe_status_str.argtypes = [i32]
     L.swe_status_str.restype = C.c_char_p
-    for name in ("swe_create_grid", "swe_step", "swe_run", "swe_get_state", "swe_set_state",
-                 "swe_get_dt_history", "swe_get_info", "swe_device_fields", "swe_run_noalloc"):
+    for name in ("swe_create_grid", "swe_create_mesh", "swe_cell_index", "swe_mesh_info",
+                 "swe_step", "swe_run",
+                 "swe_get_state", "swe_set_state", "swe_get_dt_history", "swe_get_info",
+                 "swe_device_fields", "swe_run_noalloc"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -160,6 +172,55 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
     _check(L.swe_create_grid(C.byref(grid), C.c_void_p(Hp), W, C.byref(params), C.byref(out)),
            "swe_create_grid")
     return State(out.value, int(nx), int(ny), int(precision), int(n_layers))
+
+
+def swe_create_mesh(xy, tri, H, W0, precision=64, g=9.81, cfl=0.9, stream=None, n_layers=1,
+                    pollutant=1, r=0.0, reorder=1) -> State:
+    """Create a simulation on a triangle mesh (see swe_create_mesh in swe.h):
+    ``xy`` is an (n_vertices, 2) float64 array, ``tri`` an (n_cells, 3) int32
+    array of counter-clockwise vertex indices; H and the fields of W0 hold
+    n_cells values in the same numbering as ``tri``."""
+    L = load()
+    dt = _dtype(precision)
+    mesh, xy, tri = _mesh_struct(xy, tri, reorder)
+    n = int(tri.shape[0])
+    params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
+                     float(cfl), C.c_void_p(stream) if stream else None)
+    Hp = _host_ptr(H, dt, n)
+    W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
+    out = C.c_void_p()
+    _check(L.swe_create_mesh(C.byref(mesh), C.c_void_p(Hp), W, C.byref(params), C.byref(out)),
+           "swe_create_mesh")
+    return State(out.value, n, 1, int(precision), int(n_layers))
+
+
+def _mesh_struct(xy, tri, reorder):
+    xy = np.asarray(xy)
+    tri = np.asarray(tri)
+    if xy.dtype != np.float64 or xy.ndim != 2 or xy.shape[1] != 2 or not xy.flags.c_contiguous:
+        raise ValueError("xy must be a C-contiguous (n_vertices, 2) float64 array")
+    if tri.dtype != np.int32 or tri.ndim != 2 or tri.shape[1] != 3 or not tri.flags.c_contiguous:
+        raise ValueError("tri must be a C-contiguous (n_cells, 3) int32 array")
+    return _Mesh(int(xy.shape[0]), xy.ctypes.data, int(tri.shape[0]), tri.ctypes.data,
+                 int(reorder)), xy, tri
+
+
+def swe_mesh_info(xy, tri, reorder=1):
+    """Host-only preview of the mesh preparation: (new_of_old, n_edges,
+    bandwidth); see swe_mesh_info in swe.h."""
+    mesh, xy, tri = _mesh_struct(xy, tri, reorder)
+    order = np.empty(tri.shape[0], dtype=np.int32)
+    ne, bw = C.c_int64(), C.c_int64()
+    _check(load().swe_mesh_info(C.byref(mesh), order.ctypes.data, C.byref(ne), C.byref(bw)),
+           "swe_mesh_info")
+    return order, ne.value, bw.value
+
+
+def swe_cell_index(s: State):
+    """Element index of every cell (caller numbering) within the device fields."""
+    idx = np.empty(s.n, dtype=np.int64)
+    _check(load().swe_cell_index(s.ptr, idx.ctypes.data), "swe_cell_index")
+    return idx
 
 
 def swe_step(s: State, cfl) -> float:

@@ -34,7 +34,10 @@
  *    during the call.  Their element type is the state's precision: float
  *    when swe_params.precision == 32, double when it is 64.
  *  - Grid fields are nx*ny values, cell (i, j) at index j*nx + i (row-major,
- *    x fastest), centre ((i+1/2) dx, (j+1/2) dy).
+ *    x fastest), centre ((i+1/2) dx, (j+1/2) dy).  Mesh fields are n_cells
+ *    values, triangle c at index c of the caller's numbering (the library
+ *    may reorder cells internally; every host array in and out of it is in
+ *    the caller's numbering).
  *  - Field order: h, qx, qy, hC (one layer); h1, q1x, q1y, h2, q2x, q2y (two).
  *  - A handle is not thread-safe; it may be used from any one thread at a
  *    time.  All device work of a handle is ordered on swe_params.stream.
@@ -72,6 +75,27 @@ typedef struct {
   int32_t nx, ny;
   double dx, dy;
 } swe_grid;
+
+/* Unstructured mesh of triangles ([P1] Sec. 2.2: finite volumes V_i, here
+ * triangles; the edge Gamma_ij shared by V_i and V_j has length |Gamma_ij|
+ * and the unit normal eta_ij pointing from V_i to V_j; an edge of a single
+ * triangle is a reflective wall).
+ *  n_vertices  >= 3
+ *  xy          host, 2*n_vertices doubles: vertex v at (xy[2v], xy[2v+1])
+ *  n_cells     1 <= n_cells <= 2^28: number of triangles
+ *  tri         host, 3*n_cells int32: the vertices of triangle c at
+ *              tri[3c], tri[3c+1], tri[3c+2], counter-clockwise
+ *  reorder     1: store the cells in reverse Cuthill-McKee order (breadth-
+ *              first from a pseudo-peripheral cell, then reversed) for
+ *              memory locality; 0: keep the caller's order.  Results are in
+ *              the caller's numbering either way. */
+typedef struct {
+  int64_t n_vertices;
+  const double *xy;
+  int64_t n_cells;
+  const int32_t *tri;
+  int32_t reorder;
+} swe_mesh;
 
 /* Model and run parameters.
  *  n_layers   1, or 2 for the two-layer system of [P1] eq. (1)
@@ -111,6 +135,40 @@ typedef struct swe_state swe_state;
 swe_status swe_create_grid(const swe_grid *grid, const void *H,
                            const void *const *W0, const swe_params *params,
                            swe_state **out);
+
+/* Create a simulation on a triangle mesh ([P1] Algorithm 1, before the time
+ * loop; the mesh of [P1] Sec. 2.2).
+ *  mesh    see swe_mesh
+ *  H, W0   host, n_cells values per field in the caller's numbering, with
+ *          the field order and precision of swe_create_grid
+ *  params  see swe_params
+ *  out     receives the handle (NULL on failure)
+ * Computes on the host, in double precision, every triangle's area and every
+ * edge's length and unit normal, pairs the triangles across their shared
+ * edges, orders the cells (swe_mesh.reorder) and stores each edge once; then
+ * allocates the device state and copies the geometry, H and W0 there.  Each
+ * step runs three kernels: one thread per edge for its Roe flux, one thread
+ * per cell to sum its three edges in a fixed order and reduce dt, and the
+ * update.  The device keeps about (2 nf + 5) values per cell and (3 + 7)
+ * (one layer) or (3 + 11) (two layers) values per edge, plus 5 int32 per
+ * cell and 2 per edge.
+ * Errors: SWE_ERR_ARG (bad argument; an index out of range, a non-finite
+ * coordinate, a clockwise or degenerate triangle, an edge traversed twice in
+ * the same direction -- which includes any edge of three or more triangles;
+ * h <= 0 or non-finite input), SWE_ERR_UNSUPPORTED, SWE_ERR_OOM,
+ * SWE_ERR_CUDA. */
+swe_status swe_create_mesh(const swe_mesh *mesh, const void *H,
+                           const void *const *W0, const swe_params *params,
+                           swe_state **out);
+
+/* Host-only preview of the preparation swe_create_mesh does (no device
+ * work): checks the mesh and reports, for each caller cell, its internal
+ * index (new_of_old, n_cells int32, may be NULL), the number of edges walls
+ * included (*n_edges, may be NULL) and the largest index distance between
+ * the two cells of an interior edge in the internal order (*bandwidth, may
+ * be NULL).  Errors: SWE_ERR_ARG as for swe_create_mesh, SWE_ERR_OOM. */
+swe_status swe_mesh_info(const swe_mesh *mesh, int32_t *new_of_old,
+                         int64_t *n_edges, int64_t *bandwidth);
 
 /* Advance one step of eq. (4) with dt_n from eq. (5) evaluated on the
  * current state with CFL number cfl (0 < cfl <= 1).  Waits for the step to
@@ -154,15 +212,26 @@ typedef struct {
   int64_t device_bytes; /* device memory held by the handle                */
   int32_t bands, segments, warps_per_block; /* launch shape (one layer)   */
   int32_t n_layers;
+  int64_t n_cells;      /* nx*ny, or the mesh's triangles                  */
+  int64_t n_edges;      /* edges, walls included                           */
+  int32_t mesh;         /* 1 for a triangle mesh (nx = n_cells, ny = 1,     */
+                        /* pitch = field_offset = 0), 0 for a grid         */
 } swe_info;
 swe_status swe_get_info(const swe_state *s, swe_info *info);
 
 /* Device pointers of the current state's fields followed by H (5 pointers
  * for one layer: h, qx, qy, hC, H; 7 for two), for zero-copy inspection on
  * the device; ptrs must hold that many entries.  Cell (i, j) of field k is at
- * ptrs[k] + field_offset + j*pitch + i (see swe_info).  The pointers stay
- * owned by the handle and change after every step (double buffering). */
+ * ptrs[k] + field_offset + j*pitch + i (see swe_info); on a mesh, cell c is
+ * at ptrs[k] + idx[c] with idx from swe_cell_index.  The pointers stay owned
+ * by the handle; a one-layer grid's change after every step (double
+ * buffering), the others' stay fixed. */
 swe_status swe_device_fields(swe_state *s, void **ptrs);
+
+/* idx (host, n_cells int64 values, see swe_info) receives, for every cell in
+ * the caller's numbering, the element index of that cell within each device
+ * field of swe_device_fields. */
+swe_status swe_cell_index(const swe_state *s, int64_t *idx);
 
 /* Allocation-free time loop.  The papers have no counterpart of this entry
  * point: it exists for callers that must not allocate device memory after

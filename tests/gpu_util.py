@@ -125,3 +125,59 @@ def assert_parity2(d, precision, nsteps):
     dte = float(np.abs(dtg / dto - 1.0).max())
     assert dte <= tol["dt"], dte
     return errs, dte
+
+
+# ---- triangle meshes ----------------------------------------------------------
+def mesh_fields(d, dtype=np.float64):
+    return I.fields2_of(d, dtype) if d["n_layers"] == 2 else I.fields_of(d, dtype)
+
+
+def gpu_create_mesh(d, precision, reorder=1, stream=None):
+    dt = np_dtype(precision)
+    two = d["n_layers"] == 2
+    return S.swe_create_mesh(d["xy"], d["tri"], d["H"].astype(dt), mesh_fields(d, dt),
+                             precision=precision, g=d.get("g", 9.81), cfl=d.get("cfl", 0.9),
+                             stream=stream, n_layers=d["n_layers"], pollutant=0 if two else 1,
+                             r=d.get("r", 0.0), reorder=reorder)
+
+
+def gpu_run_mesh(d, precision, nsteps, reorder=1):
+    st = gpu_create_mesh(d, precision, reorder=reorder)
+    S.swe_run(st, nsteps)
+    dts = S.swe_get_dt_history(st, nsteps)
+    W, t = S.swe_get_state(st)
+    S.swe_destroy(st)
+    return [w.astype(np.float64) for w in W], np.asarray(dts), t
+
+
+def oracle_run_mesh(d, precision, nsteps):
+    dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
+    m = O.tri_mesh(d["xy"], d["tri"])
+    if d["n_layers"] == 2:
+        W, dts, st = O.run2(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d["r"],
+                            d.get("cfl", 0.9), nsteps)
+    else:
+        W, dts, st, _ = O.run1(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d.get("cfl", 0.9),
+                               nsteps)
+    assert st == O.OM_OK, st
+    return W, dts
+
+
+def assert_parity_mesh(d, precision, nsteps, reorder=1):
+    Wg, dtg, tg = gpu_run_mesh(d, precision, nsteps, reorder=reorder)
+    Wo, dto = oracle_run_mesh(d, precision, nsteps)
+    if d["n_layers"] == 2:
+        tol = TOL2[precision]
+        errs = rel_errors2(Wg, Wo, mesh_fields(d))
+        names = I.TWO_LAYER_FIELDS
+    else:
+        tol = TOL[precision]
+        errs = rel_errors(Wg, Wo, mesh_fields(d))
+        names = ("h", "qx", "qy", "hC")
+    for k in names:
+        assert errs[k] <= tol[k], (k, errs)
+    assert len(dtg) == len(dto) == nsteps
+    dte = float(np.abs(dtg / dto - 1.0).max())
+    assert dte <= tol["dt"], dte
+    assert abs(tg - dto.sum()) <= tol["dt"] * dto.sum()
+    return errs, dte

@@ -2,22 +2,25 @@
 """Throughput of the Roe finite-volume shallow-water step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload pulses8192|hills2048|dam128] [--precision 32|64]
+                    [--workload pulses8192|hills2048|dam128|interface2048|tri1024]
+                    [--precision 32|64]
 
-One "step" is one explicit time step of the one-layer + pollutant IR-Roe
-scheme over the whole grid: edge fluxes with the bathymetry source, per-cell
-accumulation, the global CFL dt reduced on the device, and the update of h,
-q and hC (one fused kernel launch).  The default workload is the 8192 x 8192
-fp32 grid of seeded Gaussian hills and surface pulses with small random
-velocities (2.4 GB of state per step, far beyond the 129 MB L2).
+One "step" is one explicit time step of the IR-Roe scheme over the whole
+domain: edge fluxes with the bathymetry source, per-cell accumulation, the
+global CFL dt reduced on the device, and the update of the state (one layer
+with pollutant: one fused kernel launch; two layers on a grid: flux pass and
+update; triangles: edge, gather and update kernels).  The default workload
+is the 8192 x 8192 fp32 grid of seeded Gaussian hills and surface pulses with
+small random velocities (2.4 GB of state per step, far beyond the 129 MB L2).
 
 Prints one JSON line on rank 0.  ``value`` is cell-updates per second over all
 ranks (Mcell-updates/s), timed with CUDA events on the stream the kernels run
 on, inputs resident in HBM.  ``e2e`` is the same metric through the C ABI with
 host buffers (pinned): every step uploads the state, steps once and reads the
-state back.  ``roofline`` compares the step kernel's algorithmic bytes (5
-fields read + 4 written per cell) per launch with the measured HBM copy
-bandwidth.  ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of
+state back.  ``roofline`` is that of the dominant kernel (the largest share
+of device time, per-kernel CUDA events through swe_set_timing): algorithmic
+bytes per launch against the measured HBM copy bandwidth, or algorithmic
+flops against the FP32/FP64 pipe peak where the kernel is arithmetic-bound.  ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of
 the same workload on one host core.
 
 Several GPUs run independent replicas (the step has no exchange that would
@@ -42,9 +45,6 @@ sys.path.insert(0, ROOT)
 METRIC = "cell-updates/s (Mcell-steps/s) of the Roe FV step; achieved HBM GB/s vs peak"
 UNIT = "Mcell-updates/s"
 BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC written
-# Two layers (flux pass + update pass): 7 fields + residual 6 written, then
-# 6 state + 6 residual read and 6 written: 31 fields per cell.
-BYTES_PER_CELL_2L = {32: 124, 64: 248}
 # Floating-point operations per cell-update of the two-layer step, counted
 # from the kernel's formulas (an FMA counts 2, a division or square root 1):
 # about 2.16 edge evaluations per cell (tile halo included) of ~494 (fp32,
@@ -55,9 +55,24 @@ FLOPS_PER_CELL_2L = {32: 1100, 64: 1290}
 # FP64: the nominal 1.25 TFLOP/s of the part.
 ALU_PEAK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
 DTYPE_NAME = {32: "f32", 64: "f64"}
-KERNEL = "cart1_step_kernel"
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cart1_step_traffic.txt")
-STEP_SOURCE = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc", "swe_cart1.cu")
+CSRC = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc")
+# kernel -> (source file whose hash keys its traffic record, traffic record)
+KERNEL_SOURCES = {
+    "cart1_step_kernel": ("swe_cart1.cu", "cart1_step_traffic.txt"),
+    "cart2_flux_kernel": ("swe_cart2.cu", "cart2_flux_traffic.txt"),
+    "cart2_update_kernel": ("swe_cart2.cu", "cart2_flux_traffic.txt"),
+    "mesh_edge_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
+    "mesh_gather_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
+    "mesh_update_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
+}
+# Triangle meshes, per edge: floating-point operations of the edge kernel,
+# counted from its formulas (an FMA counts 2; square roots, reciprocals and
+# reciprocal square roots, about 29 of them for two layers, are not counted):
+# two layers 494 (fp32: 7 + 2 Newton iterations per outer / inner root) or
+# 584 (fp64: 9 + 3) in the Roe flux, plus 79 for the rotations into and out
+# of the edge frame, the fluctuation terms and the edge-length scaling; one
+# layer 88.
+FLOPS_PER_EDGE_MESH = {(2, 32): 573, (2, 64): 663, (1, 32): 88, (1, 64): 88}
 
 DESCR = {
     "pulses8192": "8192x8192 Cartesian, dx=10 m, 128 seeded Gaussian hills, 16 surface pulses, "
@@ -67,7 +82,36 @@ DESCR = {
     "dam128": "128x128 Cartesian, dx=1 m, circular dam break, flat bottom, reflective walls",
     "interface2048": "two layers, 2048x2048 Cartesian, dx=10 m, flat bottom 10 m, interface "
                      "dam break h1=6/4 m at x=L/2, r=0.98, at rest, reflective walls",
+    "tri1024": "two layers on 1024x1024 unit squares split into 2,097,152 triangles, interior "
+               "vertices jittered by +-0.2, cells shuffled then RCM-reordered, r=0.98, "
+               "8 Gaussian hills, 0.5 m interface bump, at rest, reflective walls",
 }
+
+
+def kernel_model(kernel, precision, nl, n_cells, n_edges):
+    """(bound, algorithmic amount per launch, unit) of one kernel: bytes that
+    must cross HBM at least once, or floating-point operations."""
+    e = 4 if precision == 32 else 8
+    nf = 6 if nl == 2 else 4
+    if kernel == "cart1_step_kernel":
+        return "hbm", BYTES_PER_CELL[precision] * n_cells, "B"
+    if kernel == "cart2_flux_kernel":
+        return "alu", FLOPS_PER_CELL_2L[precision] * n_cells, "flop"
+    if kernel == "cart2_update_kernel":
+        return "hbm", 3 * 6 * e * n_cells, "B"
+    ne = 11 if nl == 2 else 7
+    if kernel == "mesh_edge_kernel":
+        return "alu", FLOPS_PER_EDGE_MESH[(nl, precision)] * n_edges, "flop"
+    if kernel == "mesh_gather_kernel":
+        # three int32 references, every edge record once, 1/|V|, R written
+        return "hbm", (12 + e + nf * e) * n_cells + ne * e * n_edges, "B"
+    if kernel == "mesh_update_kernel":
+        return "hbm", 3 * nf * e * n_cells, "B"
+    raise KeyError(kernel)
+
+
+def alu_peak_tflops(precision):
+    return ALU_PEAK_TFLOPS[precision]
 
 
 def state_fields(I, d):
@@ -79,6 +123,63 @@ def oracle_run(O, d, nx, rows, H, W, nsteps):
     if d.get("n_layers") == 2:
         return O.grid_run2(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["r"], d["cfl"], nsteps)
     return O.grid_run1(nx, rows, d["dx"], d["dy"], H, W, d["g"], d["cfl"], nsteps)
+
+
+def n_cells_of(d):
+    return d["n_cells"] if d.get("mesh") else d["nx"] * d["ny"]
+
+
+class Sample:
+    """A bounded sample of a workload for the CPU oracle: the first rows of a
+    grid, or the triangles with the lowest centroids of a mesh (as a walled
+    domain of their own), with their initial values."""
+
+    def __init__(self, I, d, cells):
+        import numpy as np
+        self.d = d
+        fields = state_fields(I, d)
+        if d.get("mesh"):
+            cy = I.tri_centroids(d["xy"], d["tri"])[:, 1]
+            sel = np.sort(np.argsort(cy, kind="stable")[:max(1, min(cells, d["n_cells"]))])
+            tri = d["tri"][sel]
+            used, inv = np.unique(tri, return_inverse=True)
+            self.xy = np.ascontiguousarray(d["xy"][used])
+            self.tri = np.ascontiguousarray(inv.reshape(-1, 3).astype(np.int32))
+            self.cells = len(sel)
+            self.H = d["H"][sel]
+            self.W = [f[sel] for f in fields]
+            self.what = (f"the {self.cells} triangles of lowest centroid of the "
+                         f"{d['n_cells']}-triangle mesh as a walled mesh")
+        else:
+            nx = d["nx"]
+            rows = int(max(1, min(d["ny"], cells // nx)))
+            sl = slice(0, rows * nx)
+            self.rows, self.cells = rows, rows * nx
+            self.H = d["H"][sl]
+            self.W = [f[sl] for f in fields]
+            self.what = (f"rows 0..{rows - 1} of the {d['nx']}x{d['ny']} initial state as a "
+                         f"walled {nx}x{rows} grid")
+
+    def run(self, O, nsteps, W=None):
+        d = self.d
+        W = self.W if W is None else W
+        if d.get("mesh"):
+            m = getattr(self, "_mesh", None) or O.tri_mesh(self.xy, self.tri)
+            self._mesh = m
+            if d.get("n_layers") == 2:
+                return O.run2(m, self.H, W, d["g"], d["r"], d["cfl"], nsteps)
+            Wf, dts, st, _ = O.run1(m, self.H, W, d["g"], d["cfl"], nsteps)
+            return Wf, dts, st
+        return oracle_run(O, d, d["nx"], self.rows, self.H, W, nsteps)
+
+
+def calibrate(O, I, d, cal_cells):
+    """Seconds per cell-update of the oracle on this workload."""
+    smp = Sample(I, d, cal_cells)
+    smp.run(O, 1)   # builds the sample mesh
+    t0 = time.perf_counter()
+    smp.run(O, 1)
+    return (time.perf_counter() - t0) / smp.cells
 
 
 def parse():
@@ -118,19 +219,22 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def traffic_per_launch(precision, workload):
-    """DRAM bytes per launch of the step kernel from the committed ncu summary,
-    or None when the kernel source changed since it was captured."""
+def traffic_per_launch(kernel, precision, workload):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None when the kernel's source changed since it was captured."""
     try:
-        src_hash = hashlib.sha256(open(STEP_SOURCE, "rb").read()).hexdigest()[:16]
+        src, rec = KERNEL_SOURCES[kernel]
+        src_hash = hashlib.sha256(open(os.path.join(CSRC, src), "rb").read()).hexdigest()[:16]
         vals = {}
-        for line in open(TRAFFIC_FILE):
+        for line in open(os.path.join(ROOT, "profiles", rec)):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
         if vals.get("source_sha256_16") != src_hash:
             return None
-        key = f"bytes_per_launch_{workload}_f{precision}"
+        key = f"bytes_per_launch_{kernel}_{workload}_f{precision}"
+        if key not in vals and kernel == "cart1_step_kernel":
+            key = f"bytes_per_launch_{workload}_f{precision}"
         return float(vals[key]) if key in vals else None
     except Exception:
         return None
@@ -207,31 +311,20 @@ def physical_gpu(local):
 
 
 def cpu_baseline(d, budget_s=12.0):
-    """The oracle (fp64, one thread) on a band of the workload's first rows."""
-    import numpy as np
-
+    """The oracle (fp64, one thread) on a bounded sample of the workload."""
     import oracle as O
     from finite_volume_shallow_gb300 import inputs as I
 
-    nx = d["nx"]
-    rows = min(d["ny"], 64)
-    def window(r):
-        sl = slice(0, r * nx)
-        return d["H"][sl], [f[sl] for f in state_fields(I, d)]
-    H, W = window(rows)
+    per_cell = calibrate(O, I, d, 64 * (d.get("nx") or 1024) if not d.get("mesh") else 65536)
+    cells = int(max(512, min(n_cells_of(d), budget_s / 4 / per_cell)))
+    smp = Sample(I, d, cells)
+    steps = max(1, int(budget_s / (per_cell * smp.cells)))
+    smp.run(O, 1)
     t0 = time.perf_counter()
-    oracle_run(O, d, nx, rows, H, W, 1)
-    per_cell = (time.perf_counter() - t0) / (nx * rows)
-    rows = int(max(8, min(d["ny"], budget_s / 4 / (per_cell * nx))))
-    steps = max(1, int(budget_s / (per_cell * nx * rows)))
-    H, W = window(rows)
-    t0 = time.perf_counter()
-    _, dts, st = oracle_run(O, d, nx, rows, H, W, steps)
+    _, dts, st = smp.run(O, steps)
     el = time.perf_counter() - t0
-    return {"value": nx * rows * steps / el / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of the {d['nx']}x{d['ny']} initial state as a "
-                      f"walled {nx}x{rows} grid, {steps} steps, fp64, single thread, "
-                      f"{el:.1f} s"}
+    return {"value": smp.cells * steps / el / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{smp.what}, {steps} steps, fp64, single thread, {el:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -239,38 +332,28 @@ def run_reference(args, rank, world):
     bounded sample of the workload per step."""
     if rank != 0:
         return 0
-    import numpy as np
-
     import oracle as O
     from finite_volume_shallow_gb300 import inputs as I
 
     d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
     precision = args.precision or d["precision"]
-    nx = d["nx"]
-    cal_rows = min(d["ny"], 16)
-    sl = slice(0, cal_rows * nx)
-    t0 = time.perf_counter()
-    oracle_run(O, d, nx, cal_rows, d["H"][sl], [f[sl] for f in state_fields(I, d)], 1)
-    per_cell = (time.perf_counter() - t0) / (nx * cal_rows)
+    per_cell = calibrate(O, I, d, 16 * (d.get("nx") or 1024) if not d.get("mesh") else 16384)
     budget = 150.0
-    rows = int(max(4, min(d["ny"], budget / ((args.steps + args.warmup) * per_cell * nx))))
-    sl = slice(0, rows * nx)
-    H = d["H"][sl]
-    W = [f[sl] for f in state_fields(I, d)]
-    W, _, st = oracle_run(O, d, nx, rows, H, W, args.warmup)
+    cells = int(max(256, min(n_cells_of(d), budget / ((args.steps + args.warmup) * per_cell))))
+    smp = Sample(I, d, cells)
+    W, _, st = smp.run(O, args.warmup)
     t0 = time.perf_counter()
-    W, _, st = oracle_run(O, d, nx, rows, H, W, args.steps)
+    W, _, st = smp.run(O, args.steps, W)
     el = time.perf_counter() - t0
-    value = nx * rows * args.steps / el / 1e6
-    sample = (f"each step: one oracle step over rows 0..{rows - 1} of the {d['nx']}x{d['ny']} "
-              f"workload as a walled {nx}x{rows} grid (fp64, single thread)")
+    value = smp.cells * args.steps / el / 1e6
+    sample = f"each step: one oracle step over {smp.what} (fp64, single thread)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}",
-                   "cells": d["nx"] * d["ny"], "parallelism": "replicas"},
+                   "cells": n_cells_of(d), "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -306,14 +389,21 @@ def main():
     precision = args.precision or d["precision"]
     npdt = np.float32 if precision == 32 else np.float64
     tdt = torch.float32 if precision == 32 else torch.float64
-    n = d["nx"] * d["ny"]
+    n = n_cells_of(d)
     two = d.get("n_layers") == 2
+    nl = 2 if two else 1
     fields = [f.astype(npdt) for f in state_fields(I, d)]
     stream = torch.cuda.Stream()
-    st = S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(npdt), fields,
-                           precision=precision, g=d["g"], cfl=d["cfl"],
-                           stream=stream.cuda_stream, n_layers=2 if two else 1,
-                           pollutant=0 if two else 1, r=d.get("r", 0.0))
+    if d.get("mesh"):
+        st = S.swe_create_mesh(d["xy"], d["tri"], d["H"].astype(npdt), fields,
+                               precision=precision, g=d["g"], cfl=d["cfl"],
+                               stream=stream.cuda_stream, n_layers=nl,
+                               pollutant=0 if two else 1, r=d.get("r", 0.0), reorder=1)
+    else:
+        st = S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(npdt), fields,
+                               precision=precision, g=d["g"], cfl=d["cfl"],
+                               stream=stream.cuda_stream, n_layers=nl,
+                               pollutant=0 if two else 1, r=d.get("r", 0.0))
     info = S.swe_get_info(st)
 
     # warm-up (also gives a step-time estimate for the busy window below)
@@ -333,6 +423,8 @@ def main():
         S.swe_run(st, pre)
     barrier()
     torch.cuda.synchronize()
+    # per-kernel CUDA events on the kernels' stream over the timed steps
+    S.swe_set_timing(st, True)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -341,6 +433,8 @@ def main():
     torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
+    ktimes = S.swe_get_timing(st)
+    S.swe_set_timing(st, False)
     if args.no_clocks:
         clocks = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled (--no-clocks)"]}
     else:
@@ -380,22 +474,30 @@ def main():
     S.swe_destroy(st)
 
     peak, peak_kind = load_peaks()
-    if two:
-        fl = FLOPS_PER_CELL_2L[precision] * n / (ms_per_step / 1e3) / 1e12
-        pk = ALU_PEAK_TFLOPS[precision]
-        roof = {"bound": "alu", "achieved": fl, "peak": pk, "unit": "TFLOP/s",
-                "frac": fl / pk, "peak_source": "derived from unit counts and the 2.07 GHz "
-                "maximum SM clock (fp32) / the part's nominal FP64 rate (fp64)",
-                "traffic": None, "kernel": "cart2_flux_kernel + cart2_update_kernel",
-                "flops_per_cell": FLOPS_PER_CELL_2L[precision],
-                "algorithmic_bytes_per_step": BYTES_PER_CELL_2L[precision] * n,
-                "achieved_gbs": BYTES_PER_CELL_2L[precision] * n / (ms_per_step / 1e3) / 1e9}
-    else:
-        achieved = BYTES_PER_CELL[precision] * n / (ms_per_step / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": traffic_per_launch(precision, args.workload),
-                "kernel": KERNEL, "algorithmic_bytes_per_launch": BYTES_PER_CELL[precision] * n}
+    kernels = {}
+    for name, (launches, kms) in ktimes.items():
+        bound, amount, unit = kernel_model(name, precision, nl, n, info["n_edges"])
+        avg = kms / max(launches, 1)
+        rate = amount / (avg / 1e3)
+        if unit == "B":
+            kernels[name] = {"bound": "hbm", "achieved": rate / 1e9, "peak": peak, "unit": "GB/s",
+                             "frac": rate / 1e9 / peak, "peak_source": peak_kind,
+                             "algorithmic_bytes_per_launch": amount}
+        else:
+            pk = alu_peak_tflops(precision)
+            kernels[name] = {"bound": "alu", "achieved": rate / 1e12, "peak": pk,
+                             "unit": "TFLOP/s", "frac": rate / 1e12 / pk,
+                             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz "
+                                            "(fp32); the part's nominal FP64 rate (fp64)",
+                             "algorithmic_flops_per_launch": amount}
+        kernels[name].update({"kernel": name, "launches": launches, "ms_per_launch": avg,
+                              "share": kms / max(sum(v[1] for v in ktimes.values()), 1e-30),
+                              "traffic": traffic_per_launch(name, precision, args.workload)})
+    dominant = max(ktimes, key=lambda k: ktimes[k][1])
+    roof = dict(kernels[dominant])
+    roof["other_kernels"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "unit", "frac",
+                                                      "ms_per_launch", "share")}
+                             for k, v in kernels.items() if k != dominant}
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -408,15 +510,18 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_NAME[precision], "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}"
-                                   + (f", reduced to {d['nx']}x{d['ny']}" if args.nx or args.ny
+                                   + (f", reduced to {args.nx or d.get('nx')}x"
+                                      f"{args.ny or d.get('ny')}" if args.nx or args.ny
                                       else ""),
-                       "cells": n, "nx": d["nx"], "ny": d["ny"], "parallelism": "replicas",
-                       "l2": "inputs larger than L2" if n * (BYTES_PER_CELL_2L if two else BYTES_PER_CELL)[precision] > 129e6
-                             else "inputs fit in L2 (no flush)",
+                       "cells": n, "edges": info["n_edges"], "nx": d.get("nx"),
+                       "ny": d.get("ny"), "parallelism": "replicas",
+                       "l2": "inputs larger than L2 (no flush needed)"
+                             if info["device_bytes"] > 129e6 else "inputs fit in L2 (no flush)",
+                       "device_bytes": info["device_bytes"],
                        "launch": {"bands": info["bands"], "segments": info["segments"],
                                   "warps_per_block": info["warps_per_block"]}},
             "e2e": e2e, "roofline": roof, "cpu_baseline": base, "clocks": clocks,
-            "gpu_launches": args.steps * (2 if two else 1),
+            "gpu_launches": sum(v[0] for v in ktimes.values()),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

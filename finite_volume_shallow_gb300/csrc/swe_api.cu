@@ -60,6 +60,22 @@ struct swe_state {
   int32_t* new_of_old = nullptr;     // device [ncells]
   int32_t* old_of_new = nullptr;
   std::vector<int32_t> h_new_of_old;  // host copy (swe_cell_index)
+  struct Timing* timing = nullptr;    // per-kernel event ring (swe_set_timing)
+  const cudaEvent_t* marks = nullptr; // events of the step being enqueued, or null
+};
+
+// Per-kernel device time: a ring of event sets, one set per step; a set is
+// read back when its slot comes round again (so the host runs at most
+// kSlots steps ahead while timing) and on swe_get_timing.
+struct Timing {
+  static constexpr int kSlots = 64, kMaxK = 3;
+  cudaEvent_t ev[kSlots][kMaxK + 1] = {};
+  bool pending[kSlots] = {};
+  int next = 0, nk = 0;
+  const char* names[kMaxK] = {};
+  double ms[kMaxK] = {};
+  int64_t launches[kMaxK] = {};
+  bool on = false;
 };
 
 namespace {
@@ -151,7 +167,9 @@ swe_status enqueue_step(swe_state* s, double cfl) {
   a.t_dev = s->t_dev;
   a.step = s->step;
   a.err = s->err;
+  if (s->marks) CK(cudaEventRecord(s->marks[0], s->stream));
   CK(launch_step<T>(a, s->blocks, s->stream));
+  if (s->marks) CK(cudaEventRecord(s->marks[1], s->stream));
   s->cur ^= 1;
   s->step += 1;
   return SWE_OK;
@@ -196,7 +214,7 @@ swe_status enqueue_step2(swe_state* s, double cfl) {
   u.dt_hist = s->dt_hist;
   u.t_dev = s->t_dev;
   u.step = s->step;
-  CK(launch_step2<T>(f, u, s->stream));
+  CK(launch_step2<T>(f, u, s->stream, s->marks));
   s->step += 1;
   return SWE_OK;
 }
@@ -245,7 +263,7 @@ swe_status enqueue_mesh_step(swe_state* s, double cfl) {
   u.dt_hist = s->dt_hist;
   u.t_dev = s->t_dev;
   u.step = s->step;
-  CK(launch_mesh_step<T>(f, u, s->nl, s->stream));
+  CK(launch_mesh_step<T>(f, u, s->nl, s->stream, s->marks));
   s->step += 1;
   return SWE_OK;
 }
@@ -256,12 +274,79 @@ swe_status enqueue_dt0_any(swe_state* s) {
   if (s->nl == 2) return s->prec == 32 ? enqueue_check2<float>(s) : enqueue_check2<double>(s);
   return s->prec == 32 ? enqueue_dt0<float>(s) : enqueue_dt0<double>(s);
 }
+swe_status timing_harvest(Timing* tm, int slot) {
+  if (!tm->pending[slot]) return SWE_OK;
+  CK(cudaEventSynchronize(tm->ev[slot][tm->nk]));
+  for (int k = 0; k < tm->nk; ++k) {
+    float f = 0.f;
+    CK(cudaEventElapsedTime(&f, tm->ev[slot][k], tm->ev[slot][k + 1]));
+    tm->ms[k] += f;
+    tm->launches[k] += 1;
+  }
+  tm->pending[slot] = false;
+  return SWE_OK;
+}
+
+swe_status timing_harvest_all(swe_state* s) {
+  Timing* tm = s->timing;
+  if (!tm) return SWE_OK;
+  for (int i = 0; i < Timing::kSlots; ++i) {
+    const int slot = (tm->next + i) % Timing::kSlots;  // oldest first
+    const swe_status st = timing_harvest(tm, slot);
+    if (st != SWE_OK) return st;
+  }
+  return SWE_OK;
+}
+
+swe_status enqueue_step_timed(swe_state* s, double cfl);
+
 swe_status enqueue_step_any(swe_state* s, double cfl) {
+  if (s->timing && s->timing->on) return enqueue_step_timed(s, cfl);
   if (s->mesh)
     return s->prec == 32 ? enqueue_mesh_step<float>(s, cfl) : enqueue_mesh_step<double>(s, cfl);
   if (s->nl == 2)
     return s->prec == 32 ? enqueue_step2<float>(s, cfl) : enqueue_step2<double>(s, cfl);
   return s->prec == 32 ? enqueue_step<float>(s, cfl) : enqueue_step<double>(s, cfl);
+}
+
+swe_status enqueue_step_timed(swe_state* s, double cfl) {
+  Timing* tm = s->timing;
+  const int slot = tm->next;
+  swe_status st = timing_harvest(tm, slot);  // the slot's previous step
+  if (st != SWE_OK) return st;
+  s->marks = tm->ev[slot];
+  tm->on = false;  // plain enqueue below
+  st = enqueue_step_any(s, cfl);
+  tm->on = true;
+  s->marks = nullptr;
+  if (st != SWE_OK) return st;
+  tm->pending[slot] = true;
+  tm->next = (slot + 1) % Timing::kSlots;
+  return SWE_OK;
+}
+
+void timing_names(swe_state* s, Timing* tm) {
+  if (s->mesh) {
+    tm->nk = 3;
+    tm->names[0] = "mesh_edge_kernel";
+    tm->names[1] = "mesh_gather_kernel";
+    tm->names[2] = "mesh_update_kernel";
+  } else if (s->nl == 2) {
+    tm->nk = 2;
+    tm->names[0] = "cart2_flux_kernel";
+    tm->names[1] = "cart2_update_kernel";
+  } else {
+    tm->nk = 1;
+    tm->names[0] = "cart1_step_kernel";
+  }
+}
+
+void timing_destroy(Timing* tm) {
+  if (!tm) return;
+  for (int i = 0; i < Timing::kSlots; ++i)
+    for (int k = 0; k <= Timing::kMaxK; ++k)
+      if (tm->ev[i][k]) cudaEventDestroy(tm->ev[i][k]);
+  delete tm;
 }
 
 // Copy n host fields into the padded layout of `dst`.
@@ -407,6 +492,7 @@ const char* swe_status_str(swe_status st) {
 void swe_destroy(swe_state* s) {
   if (!s) return;
   if (s->stream || s->dev) cudaStreamSynchronize(s->stream);
+  timing_destroy(s->timing);
   if (s->dev) cudaFree(s->dev);
   if (s->h_dt) cudaFreeHost(s->h_dt);
   delete s;
@@ -631,6 +717,59 @@ swe_status swe_mesh_info(const swe_mesh* mesh, int32_t* new_of_old, int64_t* n_e
       if (prep.eb[e] >= 0 && prep.eb[e] - prep.ea[e] > bw) bw = prep.eb[e] - prep.ea[e];
     *bandwidth = bw;
   }
+  return SWE_OK;
+}
+
+swe_status swe_set_timing(swe_state* s, int32_t on) {
+  if (!s || (on != 0 && on != 1)) return SWE_ERR_ARG;
+  if (!on) {
+    if (!s->timing) return SWE_OK;
+    const swe_status st = timing_harvest_all(s);
+    s->timing->on = false;
+    return st;
+  }
+  if (!s->timing) {
+    Timing* tm = new (std::nothrow) Timing();
+    if (!tm) return SWE_ERR_OOM;
+    for (int i = 0; i < Timing::kSlots; ++i)
+      for (int k = 0; k <= Timing::kMaxK; ++k) {
+        const cudaError_t e = cudaEventCreate(&tm->ev[i][k]);
+        if (e != cudaSuccess) {
+          tm->ev[i][k] = nullptr;
+          timing_destroy(tm);
+          return cuda_status(e);
+        }
+      }
+    s->timing = tm;
+  }
+  Timing* tm = s->timing;
+  const swe_status st = timing_harvest_all(s);
+  if (st != SWE_OK) return st;
+  timing_names(s, tm);
+  for (int k = 0; k < Timing::kMaxK; ++k) {
+    tm->ms[k] = 0.0;
+    tm->launches[k] = 0;
+  }
+  tm->on = true;
+  return SWE_OK;
+}
+
+swe_status swe_get_timing(const swe_state* cs, swe_kernel_time* out, int32_t max, int32_t* n) {
+  swe_state* s = const_cast<swe_state*>(cs);
+  if (!s || !n || max < 0 || (max > 0 && !out)) return SWE_ERR_ARG;
+  *n = 0;
+  if (!s->timing) return SWE_OK;
+  const swe_status st = timing_harvest_all(s);
+  if (st != SWE_OK) return st;
+  const Timing* tm = s->timing;
+  const int cnt = tm->nk < max ? tm->nk : max;
+  for (int k = 0; k < cnt; ++k) {
+    memset(out[k].name, 0, sizeof(out[k].name));
+    strncpy(out[k].name, tm->names[k], sizeof(out[k].name) - 1);
+    out[k].launches = tm->launches[k];
+    out[k].ms = tm->ms[k];
+  }
+  *n = cnt;
   return SWE_OK;
 }
 

@@ -145,16 +145,23 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
 
 template <typename T>
 __global__ void cart2_update_kernel(const Update2Args<T> A) {
-  const T tm = *reinterpret_cast<const T*>(A.tmax_in);
-  const double dtdx = A.two_cfl / (double)tm;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) {
-    const double dt = dtdx * A.dx;
-    A.dt_hist[A.step % kHistCap] = dt;
-    *A.t_dev += dt;
-    if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
-    else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+  // dt / dx = 2 cfl / max T, once per block (a double division per thread
+  // would cost more than the update on GB300's FP64 pipe)
+  __shared__ T k_sh;
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
+    const double dtdx = A.two_cfl / (double)tm;
+    k_sh = (T)dtdx;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      const double dt = dtdx * A.dx;
+      A.dt_hist[A.step % kHistCap] = dt;
+      *A.t_dev += dt;
+      if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
+      else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+    }
   }
-  const T k = (T)dtdx;
+  __syncthreads();
+  const T k = k_sh;
   const int gi = blockIdx.x * blockDim.x + threadIdx.x;
   unsigned bad = 0;
   for (int gj = blockIdx.y * blockDim.y + threadIdx.y; gi < A.nx && gj < A.ny;
@@ -192,17 +199,21 @@ __global__ void cart2_check_kernel(const Fields6<T> w6, int nx, int ny, int pitc
 }  // namespace
 
 template <typename T>
-cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st) {
+cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st,
+                         const cudaEvent_t* marks) {
   constexpr int TY = Tile2Y<T>::v;
   dim3 block(TX, TY);
   dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
+  if (marks) cudaEventRecord(marks[0], st);
   if (f.rho == T(1)) cart2_flux_kernel<T, false><<<grid, block, 0, st>>>(f);
   else cart2_flux_kernel<T, true><<<grid, block, 0, st>>>(f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 ub(64, 4);
   dim3 ug((unsigned)((u.nx + 63) / 64), (unsigned)min((u.ny + 3) / 4, 4096));
+  if (marks) cudaEventRecord(marks[1], st);
   cart2_update_kernel<T><<<ug, ub, 0, st>>>(u);
+  if (marks) cudaEventRecord(marks[2], st);
   return cudaGetLastError();
 }
 
@@ -215,9 +226,9 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
 }
 
 template cudaError_t launch_step2<float>(const Step2Args<float>&, const Update2Args<float>&,
-                                         cudaStream_t);
+                                         cudaStream_t, const cudaEvent_t*);
 template cudaError_t launch_step2<double>(const Step2Args<double>&, const Update2Args<double>&,
-                                          cudaStream_t);
+                                          cudaStream_t, const cudaEvent_t*);
 template cudaError_t launch_check2<float>(const Fields6<float>&, int, int, int, unsigned*,
                                           cudaStream_t);
 template cudaError_t launch_check2<double>(const Fields6<double>&, int, int, int, unsigned*,

@@ -121,7 +121,8 @@ struct Update2Args {
 };
 
 template <typename T>
-cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st);
+cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st,
+                         const cudaEvent_t* marks = nullptr);
 template <typename T>
 cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsigned* err,
                           cudaStream_t st);
@@ -186,7 +187,7 @@ struct MeshUpdateArgs {
 
 template <typename T>
 cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& u, int n_layers,
-                             cudaStream_t st);
+                             cudaStream_t st, const cudaEvent_t* marks = nullptr);
 template <typename T>
 cudaError_t launch_mesh_check(const Fields6<T>& w, int n_layers, int64_t ncells, unsigned* err,
                               cudaStream_t st);
@@ -211,6 +212,10 @@ struct MeshPrep {
 // triangles or twice in the same direction); -3 when host memory runs out.
 int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const int32_t* tri,
                  bool reorder, MeshPrep* out);
+
+// The multi-kernel launchers take an optional array of events: when given,
+// marks[k] is recorded on the stream before kernel k and marks[nk] after the
+// last one (per-kernel device time, swe_set_timing).
 
 // host-side launchers (swe_cart1.cu)
 template <typename T>

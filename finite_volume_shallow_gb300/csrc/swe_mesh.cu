@@ -212,32 +212,75 @@ __global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshSte
   if ((threadIdx.x & 31) == 0 && (m > T(0) || m != m)) atomic_max_pos2<T>(A.tmax_out, m);
 }
 
+// Vector width of the update: 16-byte loads and stores.
+template <typename T> struct Vec;
+template <> struct Vec<float> { using type = float4; static constexpr int n = 4; };
+template <> struct Vec<double> { using type = double2; static constexpr int n = 2; };
+
 template <typename T, int NL>
-__global__ void mesh_update_kernel(const MeshUpdateArgs<T> A) {
+__global__ void __launch_bounds__(256) mesh_update_kernel(const MeshUpdateArgs<T> A) {
   constexpr int NF = MeshLayout<NL>::nf;
-  const T tm = *reinterpret_cast<const T*>(A.tmax_in);
-  const double dt = A.two_cfl / (double)tm;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    A.dt_hist[A.step % kHistCap] = dt;
-    *A.t_dev += dt;
-    if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
-    else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+  using V = typename Vec<T>::type;
+  constexpr int VN = Vec<T>::n;
+  // dt = 2 cfl / max_i (sum L max|lambda| / |V_i|), once per block
+  __shared__ T k_sh;
+  if (threadIdx.x == 0) {
+    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
+    const double dt = A.two_cfl / (double)tm;
+    k_sh = (T)dt;
+    if (blockIdx.x == 0) {
+      A.dt_hist[A.step % kHistCap] = dt;
+      *A.t_dev += dt;
+      if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
+      else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+    }
   }
-  const T k = (T)dt;
+  __syncthreads();
+  const T k = k_sh;
   unsigned bad = 0;
-  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < A.ncells;
-       c += (int64_t)gridDim.x * blockDim.x) {
-    T w[NF];
+  auto check = [&](const T* w) {
     T sum = T(0);
+#pragma unroll
+    for (int f = 0; f < NF; ++f) sum += w[f];
+    if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
+    if (!(w[0] > T(0))) bad |= kErrDepth;
+    if (NL == 2 && !(w[3] > T(0))) bad |= kErrDepth;
+  };
+  // field arrays start 256-byte aligned: whole vectors, then a scalar tail
+  const int64_t nvec = A.ncells / VN;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    V wv[NF], rv[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+      wv[f] = reinterpret_cast<const V*>(A.w[f])[i];
+      rv[f] = reinterpret_cast<const V*>(A.R[f])[i];
+    }
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+      T* w = reinterpret_cast<T*>(&wv[f]);
+      const T* r = reinterpret_cast<const T*>(&rv[f]);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) w[j] = w[j] - k * r[j];
+      reinterpret_cast<V*>(A.w[f])[i] = wv[f];
+    }
+#pragma unroll
+    for (int j = 0; j < VN; ++j) {
+      T w[NF];
+#pragma unroll
+      for (int f = 0; f < NF; ++f) w[f] = reinterpret_cast<const T*>(&wv[f])[j];
+      check(w);
+    }
+  }
+  for (int64_t c = nvec * VN + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < A.ncells;
+       c += stride) {
+    T w[NF];
 #pragma unroll
     for (int f = 0; f < NF; ++f) {
       w[f] = A.w[f][c] - k * A.R[f][c];
       A.w[f][c] = w[f];
-      sum += w[f];
     }
-    if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
-    if (!(w[0] > T(0))) bad |= kErrDepth;
-    if (NL == 2 && !(w[3] > T(0))) bad |= kErrDepth;
+    check(w);
   }
   if (bad) atomicOr(A.err, bad);
 }
@@ -282,19 +325,23 @@ unsigned grid_1d(int64_t n, int threads, int64_t cap) {
 
 template <typename T>
 cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& u, int n_layers,
-                             cudaStream_t st) {
+                             cudaStream_t st, const cudaEvent_t* marks) {
   const unsigned ge = grid_1d(f.nedges, kEdgeThreads, INT32_MAX);
   const unsigned gc = grid_1d(f.ncells, kCellThreads, INT32_MAX);
-  const unsigned gu = grid_1d(u.ncells, 256, 152 * 16);
-  if (n_layers == 2) {
-    mesh_edge_kernel<T, 2><<<ge, kEdgeThreads, 0, st>>>(f);
-    mesh_gather_kernel<T, 2><<<gc, kCellThreads, 0, st>>>(f);
-    mesh_update_kernel<T, 2><<<gu, 256, 0, st>>>(u);
-  } else {
-    mesh_edge_kernel<T, 1><<<ge, kEdgeThreads, 0, st>>>(f);
-    mesh_gather_kernel<T, 1><<<gc, kCellThreads, 0, st>>>(f);
-    mesh_update_kernel<T, 1><<<gu, 256, 0, st>>>(u);
-  }
+  const unsigned gu = grid_1d((u.ncells + Vec<T>::n - 1) / Vec<T>::n, 256, 152 * 8);
+  auto mark = [&](int k) {
+    if (marks) cudaEventRecord(marks[k], st);
+  };
+  mark(0);
+  if (n_layers == 2) mesh_edge_kernel<T, 2><<<ge, kEdgeThreads, 0, st>>>(f);
+  else mesh_edge_kernel<T, 1><<<ge, kEdgeThreads, 0, st>>>(f);
+  mark(1);
+  if (n_layers == 2) mesh_gather_kernel<T, 2><<<gc, kCellThreads, 0, st>>>(f);
+  else mesh_gather_kernel<T, 1><<<gc, kCellThreads, 0, st>>>(f);
+  mark(2);
+  if (n_layers == 2) mesh_update_kernel<T, 2><<<gu, 256, 0, st>>>(u);
+  else mesh_update_kernel<T, 1><<<gu, 256, 0, st>>>(u);
+  mark(3);
   return cudaGetLastError();
 }
 
@@ -320,9 +367,11 @@ cudaError_t launch_mesh_permute(T* const* dst, const T* const* src, int nf, cons
 }
 
 template cudaError_t launch_mesh_step<float>(const MeshStepArgs<float>&,
-                                             const MeshUpdateArgs<float>&, int, cudaStream_t);
+                                             const MeshUpdateArgs<float>&, int, cudaStream_t,
+                                             const cudaEvent_t*);
 template cudaError_t launch_mesh_step<double>(const MeshStepArgs<double>&,
-                                              const MeshUpdateArgs<double>&, int, cudaStream_t);
+                                              const MeshUpdateArgs<double>&, int, cudaStream_t,
+                                              const cudaEvent_t*);
 template cudaError_t launch_mesh_check<float>(const Fields6<float>&, int, int64_t, unsigned*,
                                               cudaStream_t);
 template cudaError_t launch_mesh_check<double>(const Fields6<double>&, int, int64_t, unsigned*,

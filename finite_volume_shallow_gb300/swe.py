@@ -59,6 +59,10 @@ class _Info(C.Structure):
                 ("n_cells", C.c_int64), ("n_edges", C.c_int64), ("mesh", C.c_int32)]
 
 
+class _KernelTime(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int64), ("ms", C.c_double)]
+
+
 _lib = None
 
 
@@ -80,6 +84,8 @@ def load(build_if_needed: bool = True):
     L.swe_create_mesh.argtypes = [C.POINTER(_Mesh), vp, vp, C.POINTER(_Params), C.POINTER(vp)]
     L.swe_cell_index.argtypes = [vp, vp]
     L.swe_mesh_info.argtypes = [C.POINTER(_Mesh), vp, vp, vp]
+    L.swe_set_timing.argtypes = [vp, i32]
+    L.swe_get_timing.argtypes = [vp, vp, i32, C.POINTER(i32)]
     L.swe_step.argtypes = [vp, d, C.POINTER(d)]
     L.swe_run.argtypes = [vp, i64]
     L.swe_get_state.argtypes = [vp, vp, C.POINTER(d)]
@@ -95,7 +101,7 @@ def load(build_if_needed: bool = True):
     for name in ("swe_create_grid", "swe_create_mesh", "swe_cell_index", "swe_mesh_info",
                  "swe_step", "swe_run",
                  "swe_get_state", "swe_set_state", "swe_get_dt_history", "swe_get_info",
-                 "swe_device_fields", "swe_run_noalloc"):
+                 "swe_device_fields", "swe_run_noalloc", "swe_set_timing", "swe_get_timing"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -221,6 +227,19 @@ def swe_cell_index(s: State):
     idx = np.empty(s.n, dtype=np.int64)
     _check(load().swe_cell_index(s.ptr, idx.ctypes.data), "swe_cell_index")
     return idx
+
+
+def swe_set_timing(s: State, on=True):
+    """Start (from zero) or stop per-kernel device timing of later steps."""
+    _check(load().swe_set_timing(s.ptr, 1 if on else 0), "swe_set_timing")
+
+
+def swe_get_timing(s: State) -> dict:
+    """{kernel name: (launches, summed milliseconds)} of the timed steps."""
+    buf = (_KernelTime * 8)()
+    n = C.c_int32()
+    _check(load().swe_get_timing(s.ptr, buf, 8, C.byref(n)), "swe_get_timing")
+    return {buf[k].name.decode(): (int(buf[k].launches), float(buf[k].ms)) for k in range(n.value)}
 
 
 def swe_step(s: State, cfl) -> float:

@@ -233,6 +233,23 @@ swe_status swe_device_fields(swe_state *s, void **ptrs);
  * field of swe_device_fields. */
 swe_status swe_cell_index(const swe_state *s, int64_t *idx);
 
+/* Per-kernel device time.  swe_set_timing(s, 1) starts (or restarts, from
+ * zero) accounting: every step enqueued afterwards records CUDA events on the
+ * handle's stream before, between and after its kernels, and the elapsed
+ * times are summed per kernel; while on, swe_run keeps at most 64 steps in
+ * flight ahead of the host.  swe_set_timing(s, 0) stops it (the sums stay).
+ * swe_get_timing waits for the recorded steps and writes up to max entries
+ * (one per kernel of the handle's step, in launch order) to out; *n receives
+ * the count.  Errors: SWE_ERR_ARG, SWE_ERR_OOM, SWE_ERR_CUDA. */
+typedef struct {
+  char name[32];     /* kernel name, NUL-terminated                        */
+  int64_t launches;  /* launches timed                                      */
+  double ms;         /* summed device time of those launches, milliseconds */
+} swe_kernel_time;
+swe_status swe_set_timing(swe_state *s, int32_t on);
+swe_status swe_get_timing(const swe_state *s, swe_kernel_time *out, int32_t max,
+                          int32_t *n);
+
 /* Allocation-free time loop.  The papers have no counterpart of this entry
  * point: it exists for callers that must not allocate device memory after
  * start-up -- a framework whose memory pool already holds (nearly) all of the

@@ -423,8 +423,6 @@ def main():
         S.swe_run(st, pre)
     barrier()
     torch.cuda.synchronize()
-    # per-kernel CUDA events on the kernels' stream over the timed steps
-    S.swe_set_timing(st, True)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -433,8 +431,15 @@ def main():
     torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
+    # the same K steps again with CUDA events between the kernels of every
+    # step (swe_set_timing, on the kernels' stream): each kernel's average
+    # launch duration for the roofline.  Kept out of `value`, which the
+    # extra event records would slow by about 1 %.
+    S.swe_set_timing(st, True)
+    S.swe_run(st, args.steps)
     ktimes = S.swe_get_timing(st)
     S.swe_set_timing(st, False)
+    torch.cuda.synchronize()
     if args.no_clocks:
         clocks = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled (--no-clocks)"]}
     else:
@@ -491,6 +496,8 @@ def main():
                                             "(fp32); the part's nominal FP64 rate (fp64)",
                              "algorithmic_flops_per_launch": amount}
         kernels[name].update({"kernel": name, "launches": launches, "ms_per_launch": avg,
+                              "timing": "CUDA events between the kernels of each of K "
+                                        "further steps, right after the timed region",
                               "share": kms / max(sum(v[1] for v in ktimes.values()), 1e-30),
                               "traffic": traffic_per_launch(name, precision, args.workload)})
     dominant = max(ktimes, key=lambda k: ktimes[k][1])

@@ -763,17 +763,24 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
   const int warp = threadIdx.x >> 5;
 
   // dt of this step from the previous step's wave-speed maximum (eq. (5)):
-  // dt / dx = 2 cfl / max_i (sum_x D + (dx/dy) sum_y D)
-  const T tm = *reinterpret_cast<const T*>(A.tmax_in);
-  const double dtdx = A.two_cfl / (double)tm;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    const double dt = dtdx * A.dx;
-    A.dt_hist[A.step % kHistCap] = dt;
-    *A.t_dev += dt;
-    if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
-    else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+  // dt / dx = 2 cfl / max_i (sum_x D + (dx/dy) sum_y D), computed once per
+  // block (a double division in every thread would hold up the start of the
+  // march on GB300's FP64 pipe)
+  __shared__ T kdt_sh;
+  if (threadIdx.x == 0) {
+    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
+    const double dtdx = A.two_cfl / (double)tm;
+    kdt_sh = (T)dtdx;
+    if (blockIdx.x == 0) {
+      const double dt = dtdx * A.dx;
+      A.dt_hist[A.step % kHistCap] = dt;
+      *A.t_dev += dt;
+      if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
+      else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+    }
   }
-  const T kdt = (T)dtdx;
+  __syncthreads();
+  const T kdt = kdt_sh;
 
   const int unit = blockIdx.x * kWarpsPerBlock + warp;
   if (unit >= A.nbands * A.nsegs) return;

@@ -138,9 +138,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
   // hyperbolicity of every edge of this block, and the block's max of T
   if (!__all_sync(kFull2, hyper_ok) && (tx & 31) == 0) atomicOr(A.err, kErrHyperbolic);
   T m = own ? Tsum : T(0);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = nanmax2(m, __shfl_xor_sync(kFull2, m, o));
-  if ((t & 31) == 0 && (m > T(0) || m != m)) atomic_max_pos2<T>(A.tmax_out, m);
+  block_max_publish<T, TX * TY / 32>(m, A.tmax_out);
 }
 
 template <typename T>

@@ -169,6 +169,199 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
   if (NL == 2 && !__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
 }
 
+// ---- two layers, fp32: two edges per thread on the packed FP32x2 pipe -------
+// The same arithmetic as edge2<float> (swe_roe2.cuh), written with
+// FADD2 / FMUL2 / FFMA2 so that one instruction serves both edges; the
+// square roots and reciprocals stay per component.
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+__device__ __forceinline__ float2 s2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, s2(-1.f), a); }
+__device__ __forceinline__ float2 rcp2(float2 a) { return f2(M2<float>::rcp(a.x), M2<float>::rcp(a.y)); }
+__device__ __forceinline__ float2 rsq2(float2 a) { return f2(M2<float>::rsq(a.x), M2<float>::rsq(a.y)); }
+__device__ __forceinline__ float2 sqrt2(float2 a) { return f2(sqrtf(a.x), sqrtf(a.y)); }
+__device__ __forceinline__ float2 min2(float2 a, float2 b) { return f2(fminf(a.x, b.x), fminf(a.y, b.y)); }
+__device__ __forceinline__ float2 max2(float2 a, float2 b) { return f2(fmaxf(a.x, b.x), fmaxf(a.y, b.y)); }
+__device__ __forceinline__ float sgnw1(float l) { return l < 0.f ? 1.f : (l > 0.f ? 0.f : 0.5f); }
+
+struct Side2P {
+  float2 h[2], s[2], rs[2], qn[2], qt[2], H;
+};
+
+struct QuarticP {
+  float2 u1, u2, c1s, c2s, rc;
+  __device__ __forceinline__ void qq(float2 l, float2& d1, float2& d2, float2& q1,
+                                     float2& q2) const {
+    d1 = sub2(l, u1);
+    d2 = sub2(l, u2);
+    q1 = fma2(d1, d1, f2(-c1s.x, -c1s.y));
+    q2 = fma2(d2, d2, f2(-c2s.x, -c2s.y));
+  }
+  // one Newton step on p = q1 q2 - rc, p' = 2 (d1 q2 + d2 q1)
+  __device__ __forceinline__ float2 newton(float2 l) const {
+    float2 d1, d2, q1, q2;
+    qq(l, d1, d2, q1, q2);
+    const float2 p = fma2(q1, q2, f2(-rc.x, -rc.y));
+    const float2 dp = mul2(s2(2.f), fma2(d1, q2, mul2(d2, q1)));
+    return fma2(f2(-p.x, -p.y), rcp2(dp), l);
+  }
+};
+
+// Flux of two edges at once; walls per component.  Returns false if either
+// edge's A_ij has a complex pair of eigenvalues.
+__device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g, float gh,
+                                       float r, bool w0, bool w1, float2* out) {
+  float2 un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float2 va = mul2(a.qn[k], a.rs[k]), vb = mul2(b.qn[k], b.rs[k]);
+    un[k] = mul2(add2(va, vb), rcp2(add2(a.s[k], b.s[k])));
+    cs[k] = mul2(s2(gh), add2(a.h[k], b.h[k]));
+    const float2 iha = mul2(a.rs[k], a.rs[k]), ihb = mul2(b.rs[k], b.rs[k]);
+    qu_a[k] = mul2(mul2(a.qn[k], a.qn[k]), iha);
+    qu_b[k] = mul2(mul2(b.qn[k], b.qn[k]), ihb);
+    ut_a[k] = mul2(a.qt[k], iha);
+    ut_b[k] = mul2(b.qt[k], ihb);
+  }
+  const QuarticP q{un[0], un[1], cs[0], cs[1], mul2(mul2(s2(r), cs[0]), cs[1])};
+  const float2 c1 = sqrt2(cs[0]), c2 = sqrt2(cs[1]);
+  // outer roots: from below / above, where p > 0, p convex and monotone
+  float2 l1 = min2(fma2(s2(-1.5f), c1, un[0]), fma2(s2(-1.5f), c2, un[1]));
+  float2 l4 = max2(fma2(s2(1.5f), c1, un[0]), fma2(s2(1.5f), c2, un[1]));
+#pragma unroll
+  for (int it = 0; it < Iters<float>::outer; ++it) {
+    l1 = q.newton(l1);
+    l4 = q.newton(l4);
+  }
+  // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
+  const float2 p3 = mul2(s2(-2.f), add2(un[0], un[1]));
+  const float2 p2 = add2(add2(fma2(un[0], un[0], f2(-cs[0].x, -cs[0].y)),
+                              fma2(un[1], un[1], f2(-cs[1].x, -cs[1].y))),
+                         mul2(mul2(s2(4.f), un[0]), un[1]));
+  const float2 ss = add2(l1, l4), pp = mul2(l1, l4);
+  const float2 bb = add2(p3, ss);
+  const float2 cc = sub2(fma2(ss, bb, p2), pp);
+  const float2 disc = fma2(bb, bb, mul2(s2(-4.f), cc));
+  const bool hyper = (disc.x > 0.f) & (disc.y > 0.f);
+  const float2 sd = sqrt2(max2(disc, s2(0.f)));
+  float2 l2 = mul2(s2(0.5f), sub2(f2(-bb.x, -bb.y), sd));
+  float2 l3 = mul2(s2(0.5f), sub2(sd, bb));
+#pragma unroll
+  for (int it = 0; it < Iters<float>::inner; ++it) {
+    l2 = q.newton(l2);
+    l3 = q.newton(l3);
+  }
+  // fluctuation d (pressure differences written g hbar_k dh_k)
+  const float2 dh1 = sub2(b.h[0], a.h[0]), dh2 = sub2(b.h[1], a.h[1]), dH = sub2(b.H, a.H);
+  const float2 d1 = sub2(b.qn[0], a.qn[0]);
+  const float2 d2 = fma2(cs[0], sub2(add2(dh1, dh2), dH), sub2(qu_b[0], qu_a[0]));
+  const float2 d3 = sub2(b.qn[1], a.qn[1]);
+  const float2 d4 = fma2(cs[1], sub2(fma2(s2(r), dh1, dh2), dH), sub2(qu_b[1], qu_a[1]));
+  // P^- d = sum_k w_k alpha_k K_k
+  const float2 lam[4] = {l1, l2, l3, l4};
+  const float2 ic1s = rcp2(cs[0]);
+  const float2 tu1 = mul2(s2(2.f), un[0]), tu2 = mul2(s2(2.f), un[1]);
+  float2 pd0 = s2(0.f), pd1 = s2(0.f), pd2 = s2(0.f), pd3 = s2(0.f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 l = lam[k];
+    const float2 w = f2(sgnw1(l.x), sgnw1(l.y));
+    float2 e1, e2, Q1, Q2;
+    q.qq(l, e1, e2, Q1, Q2);
+    const float2 dp = mul2(s2(2.f), fma2(e1, Q2, mul2(e2, Q1)));
+    const float2 num = fma2(Q2, fma2(sub2(l, tu1), d1, d2),
+                            mul2(cs[0], fma2(sub2(l, tu2), d3, d4)));
+    const float2 alpha = mul2(mul2(w, num), rcp2(dp));
+    const float2 mu = mul2(Q1, ic1s);
+    pd0 = add2(pd0, alpha);
+    pd1 = fma2(alpha, l, pd1);
+    pd2 = fma2(alpha, mu, pd2);
+    pd3 = fma2(mul2(alpha, l), mu, pd3);
+  }
+  float2 m1 = add2(a.qn[0], pd0);
+  float2 m2 = add2(a.qn[1], pd2);
+  if (w0) { m1.x = 0.f; m2.x = 0.f; }  // a reflective wall passes no mass
+  if (w1) { m1.y = 0.f; m2.y = 0.f; }
+  out[E_M1] = m1;
+  out[E_PM1] = pd1;
+  out[E_PS1] = sub2(d2, pd1);
+  out[E_T1] = mul2(m1, f2(m1.x > 0.f ? ut_a[0].x : ut_b[0].x, m1.y > 0.f ? ut_a[0].y : ut_b[0].y));
+  out[E_M2] = m2;
+  out[E_PM2] = pd3;
+  out[E_PS2] = sub2(d4, pd3);
+  out[E_T2] = mul2(m2, f2(m2.x > 0.f ? ut_a[1].x : ut_b[1].x, m2.y > 0.f ? ut_a[1].y : ut_b[1].y));
+  out[E_D] = max2(f2(fabsf(l1.x), fabsf(l1.y)), f2(fabsf(l4.x), fabsf(l4.y)));
+  return hyper;
+}
+
+__device__ __forceinline__ void load_side2p(const MeshStepArgs<float>& A, int32_t c0, int32_t c1,
+                                            float2 ex, float2 ey, Side2P& s) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float2 h = f2(A.w[3 * k][c0], A.w[3 * k][c1]);
+    const float2 qx = f2(A.w[3 * k + 1][c0], A.w[3 * k + 1][c1]);
+    const float2 qy = f2(A.w[3 * k + 2][c0], A.w[3 * k + 2][c1]);
+    s.h[k] = h;
+    s.rs[k] = rsq2(h);
+    s.s[k] = mul2(h, s.rs[k]);
+    s.qn[k] = fma2(qx, ex, mul2(qy, ey));
+    s.qt[k] = fma2(qy, ex, f2(-(qx.x * ey.x), -(qx.y * ey.y)));
+  }
+  s.H = f2(A.H[c0], A.H[c1]);
+}
+
+// Two layers, fp32: edges 2t and 2t + 1.  Every edge array is 256-byte
+// aligned with room for one element past an odd count, so the pair loads
+// and stores stay inside the allocation; the missing second edge of an odd
+// count takes the first edge's data and its results land in that padding.
+constexpr int kPairThreads = 128;
+__global__ void __launch_bounds__(kPairThreads, 5) mesh_edge2_pair_kernel(const MeshStepArgs<float> A) {
+  const int64_t e0 = 2 * ((int64_t)blockIdx.x * kPairThreads + threadIdx.x);
+  bool ok = true;
+  if (e0 < A.nedges) {
+    const bool both = e0 + 1 < A.nedges;
+    int2 ia = *reinterpret_cast<const int2*>(A.ea + e0);
+    int2 ib = *reinterpret_cast<const int2*>(A.eb + e0);
+    float2 ex = *reinterpret_cast<const float2*>(A.enx + e0);
+    float2 ey = *reinterpret_cast<const float2*>(A.eny + e0);
+    float2 L = *reinterpret_cast<const float2*>(A.elen + e0);
+    if (!both) {
+      ia.y = ia.x; ib.y = ib.x; ex.y = ex.x; ey.y = ey.x; L.y = L.x;
+    }
+    const bool w0 = ib.x < 0, w1 = ib.y < 0;
+    Side2P sa, sb;
+    load_side2p(A, ia.x, ia.y, ex, ey, sa);
+    load_side2p(A, w0 ? ia.x : ib.x, w1 ? ia.y : ib.y, ex, ey, sb);
+    // walls: the mirror ghost has the normal discharge negated
+    if (w0) { sb.qn[0].x = -sa.qn[0].x; sb.qn[1].x = -sa.qn[1].x; }
+    if (w1) { sb.qn[0].y = -sa.qn[0].y; sb.qn[1].y = -sa.qn[1].y; }
+    float2 out[NEQ];
+    ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out);
+    float* buf = A.ebuf;
+    const int64_t st = A.estride;
+    auto put = [&](int q, float2 v) { *reinterpret_cast<float2*>(buf + q * st + e0) = v; };
+    using Lay = MeshLayout<2>;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 m = out[k ? E_M2 : E_M1];
+      const float2 t = out[k ? E_T2 : E_T1];
+      put(k, mul2(L, m));
+      const float2 ta = sub2(t, mul2(sa.qn[k], mul2(sa.qt[k], mul2(sa.rs[k], sa.rs[k]))));
+      const float2 tb = sub2(mul2(sb.qn[k], mul2(sb.qt[k], mul2(sb.rs[k], sb.rs[k]))), t);
+      const float2 pa = out[k ? E_PM2 : E_PM1], pb = out[k ? E_PS2 : E_PS1];
+      // (normal, tangential) -> (x, y), times L
+      put(Lay::a_mom + 2 * k, mul2(L, fma2(pa, ex, f2(-(ta.x * ey.x), -(ta.y * ey.y)))));
+      put(Lay::a_mom + 2 * k + 1, mul2(L, fma2(pa, ey, mul2(ta, ex))));
+      put(Lay::b_mom + 2 * k, mul2(L, fma2(pb, ex, f2(-(tb.x * ey.x), -(tb.y * ey.y)))));
+      put(Lay::b_mom + 2 * k + 1, mul2(L, fma2(pb, ey, mul2(tb, ex))));
+    }
+    put(Lay::d, mul2(L, out[E_D]));
+  }
+  if (!__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
+}
+
 // residual of one cell: its three edges, summed as e0 + (e1 + e2)
 template <typename T, int NL>
 __global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshStepArgs<T> A) {
@@ -207,9 +400,7 @@ __global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshSte
     for (int f = 0; f < NF; ++f) A.R[f][c] = (v[0][f] + (v[1][f] + v[2][f])) * ia;
     m = (d[0] + (d[1] + d[2])) * ia;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = nanmax2(m, __shfl_xor_sync(kFull2, m, o));
-  if ((threadIdx.x & 31) == 0 && (m > T(0) || m != m)) atomic_max_pos2<T>(A.tmax_out, m);
+  block_max_publish<T, kCellThreads / 32>(m, A.tmax_out);
 }
 
 // Vector width of the update: 16-byte loads and stores.
@@ -333,8 +524,16 @@ cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& 
     if (marks) cudaEventRecord(marks[k], st);
   };
   mark(0);
-  if (n_layers == 2) mesh_edge_kernel<T, 2><<<ge, kEdgeThreads, 0, st>>>(f);
-  else mesh_edge_kernel<T, 1><<<ge, kEdgeThreads, 0, st>>>(f);
+  if (n_layers == 2) {
+    if constexpr (sizeof(T) == 4) {
+      const unsigned gp = grid_1d((f.nedges + 1) / 2, kPairThreads, INT32_MAX);
+      mesh_edge2_pair_kernel<<<gp, kPairThreads, 0, st>>>(f);
+    } else {
+      mesh_edge_kernel<T, 2><<<ge, kEdgeThreads, 0, st>>>(f);
+    }
+  } else {
+    mesh_edge_kernel<T, 1><<<ge, kEdgeThreads, 0, st>>>(f);
+  }
   mark(1);
   if (n_layers == 2) mesh_gather_kernel<T, 2><<<gc, kCellThreads, 0, st>>>(f);
   else mesh_gather_kernel<T, 1><<<gc, kCellThreads, 0, st>>>(f);

@@ -29,7 +29,7 @@ struct Graph {
   std::vector<uint8_t> deg;
 };
 
-// Breadth-first levels from r over unvisited-agnostic adjacency; returns the
+// Breadth-first levels from r over the cell adjacency; returns the
 // eccentricity of r and leaves the last level in `last`.
 int bfs_levels(const Graph& G, int32_t r, std::vector<int32_t>& level, std::vector<int32_t>& queue,
                std::vector<int32_t>& last) {

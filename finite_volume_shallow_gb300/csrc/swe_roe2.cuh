@@ -180,5 +180,25 @@ __device__ __forceinline__ T nanmax2(T acc, T x) {
   return (x > acc || x != x) ? x : acc;
 }
 
+// Block-wide maximum (NaN wins) published with one atomic per block: the
+// atomics of a grid all go to one address, so one per warp would serialise
+// tens of thousands of them in a single L2 slice.  Every thread of the block
+// must call it (it synchronises the block).
+template <typename T, int NWARPS>
+__device__ __forceinline__ void block_max_publish(T m, void* slot) {
+  __shared__ T part[NWARPS];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = nanmax2(m, __shfl_xor_sync(kFull2, m, o));
+  const int t = threadIdx.x + blockDim.x * threadIdx.y;
+  if ((t & 31) == 0) part[t >> 5] = m;
+  __syncthreads();
+  if (t < 32) {
+    m = t < NWARPS ? part[t] : T(0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = nanmax2(m, __shfl_xor_sync(kFull2, m, o));
+    if (t == 0 && (m > T(0) || m != m)) atomic_max_pos2<T>(slot, m);
+  }
+}
+
 }  // namespace
 }  // namespace swe

@@ -56,15 +56,28 @@ FLOPS_PER_CELL_2L = {32: 1100, 64: 1290}
 ALU_PEAK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
 DTYPE_NAME = {32: "f32", 64: "f64"}
 CSRC = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc")
-# kernel -> (source file whose hash keys its traffic record, traffic record)
+# kernel -> (sources whose concatenation's hash keys its traffic record,
+# traffic record); see source_hash()
 KERNEL_SOURCES = {
-    "cart1_step_kernel": ("swe_cart1.cu", "cart1_step_traffic.txt"),
-    "cart2_flux_kernel": ("swe_cart2.cu", "cart2_flux_traffic.txt"),
-    "cart2_update_kernel": ("swe_cart2.cu", "cart2_flux_traffic.txt"),
-    "mesh_edge_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
-    "mesh_gather_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
-    "mesh_update_kernel": ("swe_mesh.cu", "mesh_traffic.txt"),
+    "cart1_step_kernel": (("swe_cart1.cu", "swe_internal.h"), "cart1_step_traffic.txt"),
+    "cart2_flux_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
+                          "cart2_flux_traffic.txt"),
+    "cart2_update_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
+                            "cart2_flux_traffic.txt"),
+    "mesh_edge_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"), "mesh_traffic.txt"),
+    "mesh_gather_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"),
+                           "mesh_traffic.txt"),
+    "mesh_update_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"),
+                           "mesh_traffic.txt"),
 }
+
+
+def source_hash(files):
+    """First 16 hex digits of the sha256 of the listed csrc files, concatenated."""
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
 # Triangle meshes, per edge: floating-point operations of the edge kernel,
 # counted from its formulas (an FMA counts 2; square roots, reciprocals and
 # reciprocal square roots, about 29 of them for two layers, are not counted):
@@ -223,8 +236,8 @@ def traffic_per_launch(kernel, precision, workload):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or
     None when the kernel's source changed since it was captured."""
     try:
-        src, rec = KERNEL_SOURCES[kernel]
-        src_hash = hashlib.sha256(open(os.path.join(CSRC, src), "rb").read()).hexdigest()[:16]
+        srcs, rec = KERNEL_SOURCES[kernel]
+        src_hash = source_hash(srcs)
         vals = {}
         for line in open(os.path.join(ROOT, "profiles", rec)):
             if ":" in line and not line.startswith("#"):

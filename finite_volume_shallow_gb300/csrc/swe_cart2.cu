@@ -14,7 +14,9 @@
 //                        4); each cell sums its four edges into the residual
 //                        R (global scratch) and max-reduces sum |Gamma| ||D||,
 //                        which fixes dt of this step;
-//   cart2_update_kernel  W -= (dt/dx) R in place, checks, dt bookkeeping.
+//   cart2_update_kernel  W -= (dt/dx) R in place (16-byte vectors over whole
+//                        rows, the padding left as it is), checks, dt
+//                        bookkeeping.
 //
 // The edge flux itself (quartic roots, closed-form P^- d) is in swe_roe2.cuh.
 #include <cuda_runtime.h>
@@ -31,6 +33,10 @@ namespace {
 enum { C_H1, C_Q1X, C_Q1Y, C_H2, C_Q2X, C_Q2Y, C_H, C_S1, C_S2, C_RS1, C_RS2, NCQ };
 
 constexpr int TX = kTile2X;
+
+template <typename T> struct Vec2;
+template <> struct Vec2<float> { using type = float4; static constexpr int n = 4; };
+template <> struct Vec2<double> { using type = double2; static constexpr int n = 2; };
 
 template <typename T, int TY>
 __device__ __forceinline__ Side2<T> side_of(const T (*c)[TY + 2][TX + 2], int lj, int li,
@@ -160,20 +166,40 @@ __global__ void cart2_update_kernel(const Update2Args<T> A) {
   }
   __syncthreads();
   const T k = k_sh;
-  const int gi = blockIdx.x * blockDim.x + threadIdx.x;
+  // whole rows in 16-byte vectors (the pitch is a multiple of 32); elements
+  // of the padding keep their value exactly (even if k is not finite)
+  using V = typename Vec2<T>::type;
+  constexpr int VN = Vec2<T>::n;
+  const int nvr = A.pitch / VN;
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c0 = v * VN - kPadX;  // logical column of the vector's first element
   unsigned bad = 0;
-  for (int gj = blockIdx.y * blockDim.y + threadIdx.y; gi < A.nx && gj < A.ny;
+  for (int gj = blockIdx.y * blockDim.y + threadIdx.y; v < nvr && gj < A.ny;
        gj += gridDim.y * blockDim.y) {
-    const int64_t o = (int64_t)(gj + kPadY) * A.pitch + gi + kPadX;
-    T w[6];
+    const int64_t o = (int64_t)(gj + kPadY) * nvr + v;
+    T w[6][VN];
 #pragma unroll
     for (int f = 0; f < 6; ++f) {
-      w[f] = A.w[f][o] - k * A.R[f][o];
-      A.w[f][o] = w[f];
+      V wv = reinterpret_cast<const V*>(A.w[f])[o];
+      const V rv = reinterpret_cast<const V*>(A.R[f])[o];
+      T* wp = reinterpret_cast<T*>(&wv);
+      const T* rp = reinterpret_cast<const T*>(&rv);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) {
+        const bool in = c0 + j >= 0 && c0 + j < A.nx;
+        const T nw = wp[j] - k * rp[j];
+        wp[j] = in ? nw : wp[j];
+        w[f][j] = wp[j];
+      }
+      reinterpret_cast<V*>(A.w[f])[o] = wv;
     }
-    const T sum = ((w[0] + w[1]) + (w[2] + w[3])) + (w[4] + w[5]);
-    if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
-    if (!(w[0] > T(0)) || !(w[3] > T(0))) bad |= kErrDepth;
+#pragma unroll
+    for (int j = 0; j < VN; ++j) {
+      if (!(c0 + j >= 0 && c0 + j < A.nx)) continue;
+      const T sum = ((w[0][j] + w[1][j]) + (w[2][j] + w[3][j])) + (w[4][j] + w[5][j]);
+      if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
+      if (!(w[0][j] > T(0)) || !(w[3][j] > T(0))) bad |= kErrDepth;
+    }
   }
   if (bad) atomicOr(A.err, bad);
 }
@@ -207,8 +233,9 @@ cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStr
   else cart2_flux_kernel<T, true><<<grid, block, 0, st>>>(f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  constexpr int VN = Vec2<T>::n;
   dim3 ub(64, 4);
-  dim3 ug((unsigned)((u.nx + 63) / 64), (unsigned)min((u.ny + 3) / 4, 4096));
+  dim3 ug((unsigned)((u.pitch / VN + 63) / 64), (unsigned)min((u.ny + 3) / 4, 1024));
   if (marks) cudaEventRecord(marks[1], st);
   cart2_update_kernel<T><<<ug, ub, 0, st>>>(u);
   if (marks) cudaEventRecord(marks[2], st);

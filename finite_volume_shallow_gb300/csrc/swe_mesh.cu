@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
       if (wall) mirror2(sb, sa);
       else sb = load_side2(A, b, ex, ey);
       T out[NEQ];
-      ok = edge2<T>(sa, sb, A.g, gh, A.r, wall, out);
+      ok = edge2<T, true>(sa, sb, A.g, gh, A.r, wall, out);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const T m = out[k ? E_M2 : E_M1];
@@ -199,14 +199,15 @@ struct QuarticP {
     q1 = fma2(d1, d1, f2(-c1s.x, -c1s.y));
     q2 = fma2(d2, d2, f2(-c2s.x, -c2s.y));
   }
-  // one Newton step on p = q1 q2 - rc, p' = 2 (d1 q2 + d2 q1)
-  __device__ __forceinline__ float2 newton(float2 l) const {
+  // the Newton step p / p' at l (p = q1 q2 - rc, p' = 2 (d1 q2 + d2 q1))
+  __device__ __forceinline__ float2 step(float2 l) const {
     float2 d1, d2, q1, q2;
     qq(l, d1, d2, q1, q2);
     const float2 p = fma2(q1, q2, f2(-rc.x, -rc.y));
     const float2 dp = mul2(s2(2.f), fma2(d1, q2, mul2(d2, q1)));
-    return fma2(f2(-p.x, -p.y), rcp2(dp), l);
+    return mul2(p, rcp2(dp));
   }
+  __device__ __forceinline__ float2 newton(float2 l) const { return sub2(l, step(l)); }
 };
 
 // Flux of two edges at once; walls per component.  Returns false if either
@@ -230,10 +231,16 @@ __device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g
   // outer roots: from below / above, where p > 0, p convex and monotone
   float2 l1 = min2(fma2(s2(-1.5f), c1, un[0]), fma2(s2(-1.5f), c2, un[1]));
   float2 l4 = max2(fma2(s2(1.5f), c1, un[0]), fma2(s2(1.5f), c2, un[1]));
+  const float2 tol = mul2(s2(Iters<float>::tol), max2(c1, c2));
+  const unsigned act = __activemask();
 #pragma unroll
   for (int it = 0; it < Iters<float>::outer; ++it) {
-    l1 = q.newton(l1);
-    l4 = q.newton(l4);
+    const float2 t1 = q.step(l1), t4 = q.step(l4);
+    l1 = sub2(l1, t1);
+    l4 = sub2(l4, t4);
+    const bool conv = (fabsf(t1.x) <= tol.x) & (fabsf(t1.y) <= tol.y) &
+                      (fabsf(t4.x) <= tol.x) & (fabsf(t4.y) <= tol.y);
+    if (it >= 2 && __all_sync(act, conv)) break;
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const float2 p3 = mul2(s2(-2.f), add2(un[0], un[1]));
@@ -317,7 +324,11 @@ __device__ __forceinline__ void load_side2p(const MeshStepArgs<float>& A, int32_
 // and stores stay inside the allocation; the missing second edge of an odd
 // count takes the first edge's data and its results land in that padding.
 constexpr int kPairThreads = 128;
-__global__ void __launch_bounds__(kPairThreads, 5) mesh_edge2_pair_kernel(const MeshStepArgs<float> A) {
+#ifndef SWE_PAIR_MIN_BLOCKS
+#define SWE_PAIR_MIN_BLOCKS 7
+#endif
+__global__ void __launch_bounds__(kPairThreads, SWE_PAIR_MIN_BLOCKS)
+    mesh_edge2_pair_kernel(const MeshStepArgs<float> A) {
   const int64_t e0 = 2 * ((int64_t)blockIdx.x * kPairThreads + threadIdx.x);
   bool ok = true;
   if (e0 < A.nedges) {

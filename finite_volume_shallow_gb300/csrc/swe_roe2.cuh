@@ -46,9 +46,18 @@ template <> struct M2<double> {
 
 // Newton iterations: the outer roots converge quadratically from a bound a
 // fixed fraction of c away; the inner ones start from the deflated estimate.
+// The outer iteration stops early once every edge of the warp has taken a
+// step below tol * max(c1, c2) (after that the error is of the order of the
+// type's rounding), at most `outer` iterations.
 template <typename T> struct Iters;
-template <> struct Iters<float> { static constexpr int outer = 7, inner = 2; };
-template <> struct Iters<double> { static constexpr int outer = 9, inner = 3; };
+template <> struct Iters<float> {
+  static constexpr int outer = 7, inner = 2;
+  static constexpr float tol = 2.44140625e-4f;  // 2^-12
+};
+template <> struct Iters<double> {
+  static constexpr int outer = 9, inner = 3;
+  static constexpr double tol = 1.4901161193847656e-8;  // 2^-26
+};
 
 // per-edge results in shared memory
 enum { E_M1, E_PM1, E_PS1, E_T1, E_M2, E_PM2, E_PS2, E_T2, E_D, NEQ };
@@ -79,8 +88,10 @@ struct Quartic {
 };
 
 // IR-Roe flux of one edge, two layers.  Writes the edge results; returns
-// false when A_ij has a complex pair of eigenvalues.
-template <typename T>
+// false when A_ij has a complex pair of eigenvalues.  ADAPT: stop the outer
+// Newton iteration early (warp vote); the tile kernel of the grid runs the
+// fixed count, which measured faster there.
+template <typename T, bool ADAPT = false>
 __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
                                       bool wall, T* out) {
   // Roe averages per layer: sqrt(h)-weighted normal velocity, arithmetic
@@ -102,10 +113,15 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   // outer roots: from below / above, where p > 0, p convex and monotone
   T l1 = fmin(un[0] - T(1.5) * c1, un[1] - T(1.5) * c2);
   T l4 = fmax(un[0] + T(1.5) * c1, un[1] + T(1.5) * c2);
+  const T tol = Iters<T>::tol * fmax(c1, c2);
+  const unsigned act = ADAPT ? __activemask() : 0u;
 #pragma unroll
   for (int it = 0; it < Iters<T>::outer; ++it) {
-    l1 -= q.p(l1) * M2<T>::rcp(q.dp(l1));
-    l4 -= q.p(l4) * M2<T>::rcp(q.dp(l4));
+    const T s1 = q.p(l1) * M2<T>::rcp(q.dp(l1));
+    const T s4 = q.p(l4) * M2<T>::rcp(q.dp(l4));
+    l1 -= s1;
+    l4 -= s4;
+    if (ADAPT && it >= 2 && __all_sync(act, (fabs(s1) <= tol) & (fabs(s4) <= tol))) break;
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const T p3 = T(-2) * (un[0] + un[1]);

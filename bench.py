@@ -86,6 +86,13 @@ def source_hash(files):
 # of the edge frame, the fluctuation terms and the edge-length scaling; one
 # layer 88.
 FLOPS_PER_EDGE_MESH = {(2, 32): 573, (2, 64): 663, (1, 32): 88, (1, 64): 88}
+# One layer on a grid: floating-point operations per cell-update of the
+# fused step, counted from its formulas (FMA = 2; the 10 reciprocals and
+# reciprocal square roots per cell not counted): 36 per edge flux pair in the
+# Roe head, 10 in its tail, 18 for the per-cell quantities, 40 for the next
+# step's wave speeds, 34 for accumulation, update and checks -> 200 per two
+# cells.  The fp32 step is bound by HBM; the fp64 one by GB300's FP64 pipe.
+FLOPS_PER_CELL_1L = 100
 
 DESCR = {
     "pulses8192": "8192x8192 Cartesian, dx=10 m, 128 seeded Gaussian hills, 16 surface pulses, "
@@ -107,6 +114,8 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
     e = 4 if precision == 32 else 8
     nf = 6 if nl == 2 else 4
     if kernel == "cart1_step_kernel":
+        if precision == 64:
+            return "alu", FLOPS_PER_CELL_1L * n_cells, "flop"
         return "hbm", BYTES_PER_CELL[precision] * n_cells, "B"
     if kernel == "cart2_flux_kernel":
         return "alu", FLOPS_PER_CELL_2L[precision] * n_cells, "flop"

@@ -40,7 +40,7 @@ struct swe_state {
   int cur = 0;
   int64_t step = 0;
   cudaStream_t stream = nullptr;
-  int nbands = 0, nsegs = 0, blocks = 0;
+  int nbands = 0, nsegs = 0, nsegs_wall = 0, blocks = 0;
   double* h_dt = nullptr;     // pinned readback
   unsigned* h_err = nullptr;
   double* h_t = nullptr;
@@ -102,10 +102,7 @@ swe_status cuda_status(cudaError_t e) {
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-// Launch shape: one warp per (column band, row segment); enough segments to
-// give every resident warp slot one unit, but no segment shorter than
-// kMinSegRows rows (each segment re-reads four halo rows).
-constexpr int kMinSegRows = 32;
+// Launch shape: one warp per (column band, row segment), see plan_step.
 
 template <typename T>
 swe_status plan_launch(swe_state* s) {
@@ -118,15 +115,11 @@ swe_status plan_launch(swe_state* s) {
   if (bpsm < 1) return SWE_ERR_CUDA;
   const int64_t slots = (int64_t)sms * bpsm * kWarpsPerBlock;
   const int own = band_owned<T>();
-  s->nbands = (s->nx + own - 1) / own;
-  int64_t nsegs = slots / s->nbands;
-  int64_t max_segs = s->ny / kMinSegRows;
-  if (nsegs > max_segs) nsegs = max_segs;
-  if (nsegs < 1) nsegs = 1;
-  if (nsegs > s->ny) nsegs = s->ny;
-  s->nsegs = (int)nsegs;
-  const int64_t units = (int64_t)s->nbands * s->nsegs;
-  s->blocks = (int)((units + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const StepPlan pl = plan_step(slots, (s->nx + own - 1) / own, s->ny);
+  s->nbands = pl.nbands;
+  s->nsegs = pl.nsegs;
+  s->nsegs_wall = pl.nsegs_wall;
+  s->blocks = (pl.units + kWarpsPerBlock - 1) / kWarpsPerBlock;
   return SWE_OK;
 }
 
@@ -155,6 +148,7 @@ swe_status enqueue_step(swe_state* s, double cfl) {
   a.pitch = s->pitch;
   a.nbands = s->nbands;
   a.nsegs = s->nsegs;
+  a.nsegs_wall = s->nsegs_wall;
   a.ghalf = (T)(0.5 * s->p.g);
   a.rho = (T)(s->dx / s->dy);
   a.two_cfl = 2.0 * cfl;

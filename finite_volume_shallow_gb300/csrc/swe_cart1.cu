@@ -782,12 +782,25 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
   __syncthreads();
   const T kdt = kdt_sh;
 
+  // warp -> (band, segment): segment-major, band fastest (warps resident
+  // together stream the same rows of adjacent bands), then the extra, shorter
+  // segments of the two wall bands
+  const int nb = A.nbands, S = A.nsegs, Sw = A.nsegs_wall;
+  const int nw = nb > 1 ? 2 : 1;
   const int unit = blockIdx.x * kWarpsPerBlock + warp;
-  if (unit >= A.nbands * A.nsegs) return;
-  const int band = unit % A.nbands;
-  const int seg = unit / A.nbands;
-  const int y0 = (int)((int64_t)seg * A.ny / A.nsegs);
-  const int y1 = (int)((int64_t)(seg + 1) * A.ny / A.nsegs);
+  if (unit >= nb * S + nw * (Sw - S)) return;
+  int band, seg;
+  if (unit < nb * S) {
+    band = unit % nb;
+    seg = unit / nb;
+  } else {
+    const int i = unit - nb * S;
+    band = i / (Sw - S) == 0 ? 0 : nb - 1;
+    seg = S + i % (Sw - S);
+  }
+  const int ns = (band == 0 || band == nb - 1) ? Sw : S;
+  const int y0 = (int)((int64_t)seg * A.ny / ns);
+  const int y1 = (int)((int64_t)(seg + 1) * A.ny / ns);
   unsigned char* wsm = smem + warp * (kStages * stage_bytes<T>());
   uint64_t* mbar =
       reinterpret_cast<uint64_t*>(smem + kWarpsPerBlock * kStages * stage_bytes<T>()) +

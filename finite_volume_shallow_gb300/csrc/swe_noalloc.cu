@@ -94,10 +94,8 @@ swe_status run(const swe_grid* g, const swe_params* p, const void* H, void* cons
   // row segment, about one unit per resident warp, segments >= 32 rows)
   const int own = band_owned<T>();
   const int nbands = (g->nx + own - 1) / own;
-  int64_t nsegs = (int64_t)sms * bpsm * kWarpsPerBlock / nbands;
-  if (nsegs > g->ny / 32) nsegs = g->ny / 32;
-  if (nsegs < 1) nsegs = 1;
-  const int blocks = (int)(((int64_t)nbands * nsegs + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const StepPlan pl = plan_step((int64_t)sms * bpsm * kWarpsPerBlock, nbands, g->ny);
+  const int blocks = (pl.units + kWarpsPerBlock - 1) / kWarpsPerBlock;
 
   // scratch that must start at zero: maxima, error word, clock
   CKN(cudaMemsetAsync(scr, 0, kDtsOff, stream));
@@ -123,7 +121,8 @@ swe_status run(const swe_grid* g, const swe_params* p, const void* H, void* cons
     s.ny = g->ny;
     s.pitch = pitch;
     s.nbands = nbands;
-    s.nsegs = (int)nsegs;
+    s.nsegs = pl.nsegs;
+    s.nsegs_wall = pl.nsegs_wall;
     s.ghalf = gh;
     s.rho = rho;
     s.two_cfl = 2.0 * p->cfl;

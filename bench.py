@@ -60,6 +60,8 @@ CSRC = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc")
 # traffic record); see source_hash()
 KERNEL_SOURCES = {
     "cart1_step_kernel": (("swe_cart1.cu", "swe_internal.h"), "cart1_step_traffic.txt"),
+    # (swe_fastmath.cuh is used by the fp64 kernels only, which have no
+    # traffic record)
     "cart2_flux_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
                           "cart2_flux_traffic.txt"),
     "cart2_update_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, sizeof(T) == 8>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ex[q][row][e] = out[q];
   }
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, sizeof(T) == 8>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ey[q][e][col] = out[q];
   }

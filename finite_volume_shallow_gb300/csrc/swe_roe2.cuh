@@ -21,6 +21,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "swe_fastmath.cuh"
+
 namespace swe {
 namespace {
 
@@ -37,9 +39,9 @@ template <> struct M2<float> {
   __device__ static __forceinline__ float sq(float x) { return sqrtf(x); }
   __device__ static __forceinline__ float big() { return 3.402823466e38f; }
 };
-template <> struct M2<double> {
+template <> struct M2<double> {  // Newton-refined reciprocal (swe_fastmath.cuh)
   __device__ static __forceinline__ double rsq(double x) { return rsqrt(x); }
-  __device__ static __forceinline__ double rcp(double x) { return __drcp_rn(x); }
+  __device__ static __forceinline__ double rcp(double x) { return rcp_nr(x); }
   __device__ static __forceinline__ double sq(double x) { return sqrt(x); }
   __device__ static __forceinline__ double big() { return 1.7976931348623157e308; }
 };
@@ -89,8 +91,8 @@ struct Quartic {
 
 // IR-Roe flux of one edge, two layers.  Writes the edge results; returns
 // false when A_ij has a complex pair of eigenvalues.  ADAPT: stop the outer
-// Newton iteration early (warp vote); the tile kernel of the grid runs the
-// fixed count, which measured faster there.
+// Newton iteration early (warp vote); the fp32 tile kernel of the grid runs
+// the fixed count, which measured faster there.
 template <typename T, bool ADAPT = false>
 __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
                                       bool wall, T* out) {

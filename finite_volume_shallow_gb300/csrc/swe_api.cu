@@ -14,6 +14,7 @@
 
 #include "../../include/swe.h"
 #include "swe_internal.h"
+#include "swe_plan.h"
 
 using namespace swe;
 

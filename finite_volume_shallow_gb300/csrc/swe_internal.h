@@ -45,37 +45,6 @@ template <typename T> constexpr int band_owned() { return 32 * Cpt<T>::v - 4; }
 constexpr int kStages = SWE_STAGES;
 constexpr int kWarpsPerBlock = SWE_WARPS_PER_BLOCK;
 
-// Launch shape of the one-layer step: one warp per (band, row segment),
-// every band cut into nsegs segments, the first and the last band (whose
-// warps also handle the side walls, a slower code path) into nsegs_wall
-// shorter ones, so that all warps of the single wave finish together.  No
-// segment is shorter than 32 rows, 16 in the wall bands (each segment
-// re-reads four halo rows).
-#ifndef SWE_WALL_EXTRA_PCT
-#define SWE_WALL_EXTRA_PCT 25
-#endif
-struct StepPlan {
-  int nbands, nsegs, nsegs_wall, units;
-};
-inline StepPlan plan_step(int64_t slots, int64_t nbands, int64_t ny) {
-  StepPlan p;
-  p.nbands = (int)nbands;
-  const int64_t most = ny / 32 > 1 ? ny / 32 : 1;
-  int64_t S = slots / nbands;
-  if (S > most) S = most;
-  if (S < 1) S = 1;
-  const int64_t nw = nbands > 1 ? 2 : 1;
-  int64_t Sw = (S * (100 + SWE_WALL_EXTRA_PCT) + 99) / 100;
-  const int64_t most_wall = ny / 16 > 1 ? ny / 16 : 1;  // wall bands: down to 16 rows
-  if (Sw > most_wall) Sw = most_wall;
-  while (Sw > S && nbands * S + nw * (Sw - S) > slots) --Sw;
-  if (Sw < S) Sw = S;
-  p.nsegs = (int)S;
-  p.nsegs_wall = (int)Sw;
-  p.units = (int)(nbands * S + nw * (Sw - S));
-  return p;
-}
-
 // Row pitch (elements) for an nx-wide grid of element type T.
 template <typename T>
 inline int64_t grid_pitch(int nx) {

@@ -228,6 +228,26 @@ def parse():
     return a
 
 
+def max_over_ranks(x, world):
+    """Maximum of a per-rank float over all ranks (the slowest replica sets the
+    whole job's time); identity on one rank.  Works with the NCCL process
+    group of the GPU runs and with a gloo group on CPU."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, cells_per_rank, steps, seconds):
+    """Cell-updates per second of all ranks together (Mcell-updates/s): every
+    replica advances its own copy of the workload by `steps` steps."""
+    return world * cells_per_rank * steps / seconds / 1e6
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -469,12 +489,9 @@ def main():
     else:
         clocks = ClockSampler.summarise(sampler.stop(), None)
 
-    t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world)
     ms_per_step = ms_max / args.steps
-    value = world * n * args.steps / (ms_max / 1e3) / 1e6
+    value = whole_job_rate(world, n, args.steps, ms_max / 1e3)
 
     # end to end through the C ABI with pinned host buffers
     ke = max(3, min(args.e2e_steps, args.steps))
@@ -491,13 +508,10 @@ def main():
         S.swe_get_state(st, out=host)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_s = float(te.item())
+    e2e_s = max_over_ranks(e2e_s, world)
     esz = 4 if precision == 32 else 8
     nf = len(fields)
-    e2e = {"value": world * n * ke / e2e_s / 1e6, "unit": UNIT, "steps": ke,
+    e2e = {"value": whole_job_rate(world, n, ke, e2e_s), "unit": UNIT, "steps": ke,
            "h2d_bytes_per_step": nf * n * esz + 8, "d2h_bytes_per_step": nf * n * esz + 8 + 8 + 4,
            "api": "swe_set_state + swe_step + swe_get_state, pinned host buffers"}
     S.swe_destroy(st)

@@ -772,6 +772,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
   // block (a double division in every thread would hold up the start of the
   // march on GB300's FP64 pipe)
   __shared__ T kdt_sh;
+  pdl_wait();
   if (threadIdx.x == 0) {
     const T tm = *reinterpret_cast<const T*>(A.tmax_in);
     const double dtdx = A.two_cfl / (double)tm;
@@ -793,7 +794,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
   const int nb = A.nbands, S = A.nsegs, Sw = A.nsegs_wall;
   const int nw = nb > 1 ? 2 : 1;
   const int unit = blockIdx.x * kWarpsPerBlock + warp;
-  if (unit >= nb * S + nw * (Sw - S)) return;
+  if (unit >= nb * S + nw * (Sw - S)) {
+    pdl_trigger();
+    return;
+  }
   int band, seg;
   if (unit < nb * S) {
     band = unit % nb;
@@ -814,6 +818,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
   const bool wallx = band == 0 || band * OWN + 64 - 2 > A.nx - 1;
   if (wallx) march<T, ANISO, true>(A, wsm, mbar, band, y0, y1, kdt);
   else march<T, ANISO, false>(A, wsm, mbar, band, y0, y1, kdt);
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -897,11 +902,9 @@ cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes) {
 template <typename T>
 cudaError_t launch_step(const StepArgs<T>& a, int blocks, cudaStream_t st) {
   const size_t smem = step_smem_bytes<T>();
-  if (a.rho == T(1))
-    cart1_step_kernel<T, false><<<blocks, kWarpsPerBlock * 32, smem, st>>>(a);
-  else
-    cart1_step_kernel<T, true><<<blocks, kWarpsPerBlock * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return a.rho == T(1)
+             ? launch_pdl(cart1_step_kernel<T, false>, blocks, kWarpsPerBlock * 32, smem, st, a)
+             : launch_pdl(cart1_step_kernel<T, true>, blocks, kWarpsPerBlock * 32, smem, st, a);
 }
 
 template <typename T>

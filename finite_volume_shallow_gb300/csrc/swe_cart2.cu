@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
   const int i0 = blockIdx.x * TX, j0 = blockIdx.y * TY;
   const int nx = A.nx, ny = A.ny;
   const T g = A.g, gh = T(0.5) * A.g, r = A.r;
+  pdl_wait();
 
   // tile + one-cell halo (the padded layout keeps every read in bounds)
   for (int idx = t; idx < (TX + 2) * (TY + 2); idx += TX * TY) {
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
   // hyperbolicity of every edge of this block, and the block's max of T
   if (!__all_sync(kFull2, hyper_ok) && (tx & 31) == 0) atomicOr(A.err, kErrHyperbolic);
   T m = own ? Tsum : T(0);
+  pdl_trigger();
   block_max_publish<T, TX * TY / 32>(m, A.tmax_out);
 }
 
@@ -152,6 +154,7 @@ __global__ void cart2_update_kernel(const Update2Args<T> A) {
   // dt / dx = 2 cfl / max T, once per block (a double division per thread
   // would cost more than the update on GB300's FP64 pipe)
   __shared__ T k_sh;
+  pdl_wait();
   if (threadIdx.x == 0 && threadIdx.y == 0) {
     const T tm = *reinterpret_cast<const T*>(A.tmax_in);
     const double dtdx = A.two_cfl / (double)tm;
@@ -201,6 +204,7 @@ __global__ void cart2_update_kernel(const Update2Args<T> A) {
       if (!(w[0][j] > T(0)) || !(w[3][j] > T(0))) bad |= kErrDepth;
     }
   }
+  pdl_trigger();
   if (bad) atomicOr(A.err, bad);
 }
 
@@ -229,15 +233,15 @@ cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStr
   dim3 block(TX, TY);
   dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
   if (marks) cudaEventRecord(marks[0], st);
-  if (f.rho == T(1)) cart2_flux_kernel<T, false><<<grid, block, 0, st>>>(f);
-  else cart2_flux_kernel<T, true><<<grid, block, 0, st>>>(f);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false>, grid, block, 0, st, f)
+                                : launch_pdl(cart2_flux_kernel<T, true>, grid, block, 0, st, f);
   if (e != cudaSuccess) return e;
   constexpr int VN = Vec2<T>::n;
   dim3 ub(64, 4);
   dim3 ug((unsigned)((u.pitch / VN + 63) / 64), (unsigned)min((u.ny + 3) / 4, 1024));
   if (marks) cudaEventRecord(marks[1], st);
-  cart2_update_kernel<T><<<ug, ub, 0, st>>>(u);
+  e = launch_pdl(cart2_update_kernel<T>, ug, ub, 0, st, u);
+  if (e != cudaSuccess) return e;
   if (marks) cudaEventRecord(marks[2], st);
   return cudaGetLastError();
 }

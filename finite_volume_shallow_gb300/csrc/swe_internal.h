@@ -214,6 +214,41 @@ struct MeshPrep {
 int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const int32_t* tri,
                  bool reorder, MeshPrep* out);
 
+// Programmatic dependent launch: consecutive step kernels on a stream are
+// launched with programmatic stream serialisation, so the next kernel's
+// launch overlaps the end of the previous one.  Each such kernel waits
+// (griddepcontrol.wait: until the previous grid has completed and its memory
+// is visible) before it reads anything, and lets its dependent launch once
+// its own main work is issued.
+#ifndef SWE_PDL
+#define SWE_PDL 1
+#endif
+__device__ __forceinline__ void pdl_wait() {
+#if SWE_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#if SWE_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = SWE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // The multi-kernel launchers take an optional array of events: when given,
 // marks[k] is recorded on the stream before kernel k and marks[nk] after the
 // last one (per-kernel device time, swe_set_timing).

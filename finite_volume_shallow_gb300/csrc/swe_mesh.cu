@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
   using Lay = MeshLayout<NL>;
   const int64_t e = (int64_t)blockIdx.x * kEdgeThreads + threadIdx.x;
   bool ok = true;
+  pdl_wait();
   if (e < A.nedges) {
     const int32_t a = A.ea[e], b = A.eb[e];
     const T ex = A.enx[e], ey = A.eny[e], L = A.elen[e];
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
       buf[Lay::d * st + e] = L * out[E_D];
     }
   }
+  pdl_trigger();
   if (NL == 2 && !__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
 }
 
@@ -331,6 +333,7 @@ __global__ void __launch_bounds__(kPairThreads, SWE_PAIR_MIN_BLOCKS)
     mesh_edge2_pair_kernel(const MeshStepArgs<float> A) {
   const int64_t e0 = 2 * ((int64_t)blockIdx.x * kPairThreads + threadIdx.x);
   bool ok = true;
+  pdl_wait();
   if (e0 < A.nedges) {
     const bool both = e0 + 1 < A.nedges;
     int2 ia = *reinterpret_cast<const int2*>(A.ea + e0);
@@ -370,6 +373,7 @@ __global__ void __launch_bounds__(kPairThreads, SWE_PAIR_MIN_BLOCKS)
     }
     put(Lay::d, mul2(L, out[E_D]));
   }
+  pdl_trigger();
   if (!__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
 }
 
@@ -380,6 +384,7 @@ __global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshSte
   constexpr int NF = Lay::nf;
   const int64_t c = (int64_t)blockIdx.x * kCellThreads + threadIdx.x;
   T m = T(0);
+  pdl_wait();
   if (c < A.ncells) {
     const T* buf = A.ebuf;
     const int64_t st = A.estride;
@@ -411,6 +416,7 @@ __global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshSte
     for (int f = 0; f < NF; ++f) A.R[f][c] = (v[0][f] + (v[1][f] + v[2][f])) * ia;
     m = (d[0] + (d[1] + d[2])) * ia;
   }
+  pdl_trigger();
   block_max_publish<T, kCellThreads / 32>(m, A.tmax_out);
 }
 
@@ -426,6 +432,7 @@ __global__ void __launch_bounds__(256) mesh_update_kernel(const MeshUpdateArgs<T
   constexpr int VN = Vec<T>::n;
   // dt = 2 cfl / max_i (sum L max|lambda| / |V_i|), once per block
   __shared__ T k_sh;
+  pdl_wait();
   if (threadIdx.x == 0) {
     const T tm = *reinterpret_cast<const T*>(A.tmax_in);
     const double dt = A.two_cfl / (double)tm;
@@ -484,6 +491,7 @@ __global__ void __launch_bounds__(256) mesh_update_kernel(const MeshUpdateArgs<T
     }
     check(w);
   }
+  pdl_trigger();
   if (bad) atomicOr(A.err, bad);
 }
 
@@ -535,22 +543,26 @@ cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& 
     if (marks) cudaEventRecord(marks[k], st);
   };
   mark(0);
+  cudaError_t e;
   if (n_layers == 2) {
     if constexpr (sizeof(T) == 4) {
       const unsigned gp = grid_1d((f.nedges + 1) / 2, kPairThreads, INT32_MAX);
-      mesh_edge2_pair_kernel<<<gp, kPairThreads, 0, st>>>(f);
+      e = launch_pdl(mesh_edge2_pair_kernel, gp, kPairThreads, 0, st, f);
     } else {
-      mesh_edge_kernel<T, 2><<<ge, kEdgeThreads, 0, st>>>(f);
+      e = launch_pdl(mesh_edge_kernel<T, 2>, ge, kEdgeThreads, 0, st, f);
     }
   } else {
-    mesh_edge_kernel<T, 1><<<ge, kEdgeThreads, 0, st>>>(f);
+    e = launch_pdl(mesh_edge_kernel<T, 1>, ge, kEdgeThreads, 0, st, f);
   }
+  if (e != cudaSuccess) return e;
   mark(1);
-  if (n_layers == 2) mesh_gather_kernel<T, 2><<<gc, kCellThreads, 0, st>>>(f);
-  else mesh_gather_kernel<T, 1><<<gc, kCellThreads, 0, st>>>(f);
+  e = n_layers == 2 ? launch_pdl(mesh_gather_kernel<T, 2>, gc, kCellThreads, 0, st, f)
+                    : launch_pdl(mesh_gather_kernel<T, 1>, gc, kCellThreads, 0, st, f);
+  if (e != cudaSuccess) return e;
   mark(2);
-  if (n_layers == 2) mesh_update_kernel<T, 2><<<gu, 256, 0, st>>>(u);
-  else mesh_update_kernel<T, 1><<<gu, 256, 0, st>>>(u);
+  e = n_layers == 2 ? launch_pdl(mesh_update_kernel<T, 2>, gu, 256, 0, st, u)
+                    : launch_pdl(mesh_update_kernel<T, 1>, gu, 256, 0, st, u);
+  if (e != cudaSuccess) return e;
   mark(3);
   return cudaGetLastError();
 }

@@ -34,6 +34,15 @@ enum { C_H1, C_Q1X, C_Q1Y, C_H2, C_Q2X, C_Q2Y, C_H, C_S1, C_S2, C_RS1, C_RS2, NC
 
 constexpr int TX = kTile2X;
 
+// Early exit of the outer Newton iteration (warp vote): always for fp64;
+// for fp32 a compile-time choice (SWE_CART2_ADAPT32; on by default: 162 us
+// per flux launch on the 2048^2 interface dam break against 167 us with the
+// fixed count).
+#ifndef SWE_CART2_ADAPT32
+#define SWE_CART2_ADAPT32 1
+#endif
+template <typename T> constexpr bool kAdapt2 = sizeof(T) == 8 || SWE_CART2_ADAPT32 != 0;
+
 template <typename T> struct Vec2;
 template <> struct Vec2<float> { using type = float4; static constexpr int n = 4; };
 template <> struct Vec2<double> { using type = double2; static constexpr int n = 2; };
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T, sizeof(T) == 8>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, kAdapt2<T>>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ex[q][row][e] = out[q];
   }
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T, sizeof(T) == 8>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, kAdapt2<T>>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ey[q][e][col] = out[q];
   }

@@ -183,7 +183,7 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __
 __device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, s2(-1.f), a); }
 __device__ __forceinline__ float2 rcp2(float2 a) { return f2(M2<float>::rcp(a.x), M2<float>::rcp(a.y)); }
 __device__ __forceinline__ float2 rsq2(float2 a) { return f2(M2<float>::rsq(a.x), M2<float>::rsq(a.y)); }
-__device__ __forceinline__ float2 sqrt2(float2 a) { return f2(sqrtf(a.x), sqrtf(a.y)); }
+__device__ __forceinline__ float2 sqrt2(float2 a) { return f2(sqrt_approx(a.x), sqrt_approx(a.y)); }
 __device__ __forceinline__ float2 min2(float2 a, float2 b) { return f2(fminf(a.x, b.x), fminf(a.y, b.y)); }
 __device__ __forceinline__ float2 max2(float2 a, float2 b) { return f2(fmaxf(a.x, b.x), fmaxf(a.y, b.y)); }
 __device__ __forceinline__ float sgnw1(float l) { return l < 0.f ? 1.f : (l > 0.f ? 0.f : 0.5f); }
@@ -230,9 +230,13 @@ __device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g
   }
   const QuarticP q{un[0], un[1], cs[0], cs[1], mul2(mul2(s2(r), cs[0]), cs[1])};
   const float2 c1 = sqrt2(cs[0]), c2 = sqrt2(cs[1]);
-  // outer roots: from below / above, where p > 0, p convex and monotone
-  float2 l1 = min2(fma2(s2(-1.5f), c1, un[0]), fma2(s2(-1.5f), c2, un[1]));
-  float2 l4 = max2(fma2(s2(1.5f), c1, un[0]), fma2(s2(1.5f), c2, un[1]));
+  const float2 sc = sqrt2(add2(cs[0], cs[1]));
+  const float kr2 = 1.4142135623730951f * (1.f + 1.f / 4096), ks = 1.f + 1.f / 4096;
+  // outer roots: the safe starts of edge2 (swe_roe2.cuh)
+  float2 l1 = max2(min2(fma2(s2(-kr2), c1, un[0]), fma2(s2(-kr2), c2, un[1])),
+                   fma2(s2(-ks), sc, min2(un[0], un[1])));
+  float2 l4 = min2(max2(fma2(s2(kr2), c1, un[0]), fma2(s2(kr2), c2, un[1])),
+                   fma2(s2(ks), sc, max2(un[0], un[1])));
   const float2 tol = mul2(s2(Iters<float>::tol), max2(c1, c2));
   const unsigned act = __activemask();
 #pragma unroll
@@ -242,7 +246,7 @@ __device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g
     l4 = sub2(l4, t4);
     const bool conv = (fabsf(t1.x) <= tol.x) & (fabsf(t1.y) <= tol.y) &
                       (fabsf(t4.x) <= tol.x) & (fabsf(t4.y) <= tol.y);
-    if (it >= 2 && __all_sync(act, conv)) break;
+    if (it >= 1 && __all_sync(act, conv)) break;
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const float2 p3 = mul2(s2(-2.f), add2(un[0], un[1]));

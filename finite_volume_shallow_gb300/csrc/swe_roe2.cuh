@@ -9,7 +9,14 @@
 // The outer two are found by Newton from bounds where p > 0 (p is convex and
 // monotone there, so the iterates approach the root from outside without
 // overshooting); the inner pair comes from deflating p by the outer pair and
-// is polished by Newton on p.  A complex inner pair (loss of hyperbolicity)
+// is polished by Newton on p.  Beyond max_k (u_k + c_k) both Q_k are positive
+// and increasing, so p is increasing and convex there; for r < 1 it is
+// positive wherever Q1 Q2 >= c1^2 c2^2, which holds at
+//   l = max_k (u_k + sqrt(2) c_k)   (each Q_k >= c_k^2) and at
+//   l = max_k u_k + sqrt(c1^2 + c2^2)   (Q1 >= c2^2, Q2 >= c1^2),
+// so the smaller of the two is a safe start for the largest root (mirrored
+// for the smallest).  The second is within a fraction of a percent of the
+// root when the layers move together, the first when one layer is thin.  A complex inner pair (loss of hyperbolicity)
 // is reported to the caller.  With right eigenvectors K_k = (1, l_k, m_k,
 // l_k m_k), m_k = Q1(l_k)/c1^2, the left eigenvectors of A_ij are
 // proportional to (l - 2u1, 1, c1^2 (l - 2u2)/Q2, c1^2/Q2), which gives the
@@ -28,36 +35,49 @@ namespace {
 
 constexpr unsigned kFull2 = 0xffffffffu;
 
+__device__ __forceinline__ float sqrt_approx(float x) {  // MUFU approximation
+  float r;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// sq: a square root that enters the flux; sqa: one that only seeds an
+// iteration (Newton start, deflated inner roots), where a single-precision
+// approximation is enough in either type.
 template <typename T> struct M2;
-template <> struct M2<float> {
+template <> struct M2<float> {  // MUFU approximations (a few ulp)
   __device__ static __forceinline__ float rsq(float x) { return rsqrtf(x); }
-  __device__ static __forceinline__ float rcp(float x) {  // MUFU approximation
+  __device__ static __forceinline__ float rcp(float x) {
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
   }
-  __device__ static __forceinline__ float sq(float x) { return sqrtf(x); }
+  __device__ static __forceinline__ float sq(float x) { return sqrt_approx(x); }
+  __device__ static __forceinline__ float sqa(float x) { return sqrt_approx(x); }
   __device__ static __forceinline__ float big() { return 3.402823466e38f; }
 };
 template <> struct M2<double> {  // Newton-refined reciprocal (swe_fastmath.cuh)
   __device__ static __forceinline__ double rsq(double x) { return rsqrt(x); }
   __device__ static __forceinline__ double rcp(double x) { return rcp_nr(x); }
   __device__ static __forceinline__ double sq(double x) { return sqrt(x); }
+  __device__ static __forceinline__ double sqa(double x) { return (double)sqrt_approx((float)x); }
   __device__ static __forceinline__ double big() { return 1.7976931348623157e308; }
 };
 
-// Newton iterations: the outer roots converge quadratically from a bound a
-// fixed fraction of c away; the inner ones start from the deflated estimate.
-// The outer iteration stops early once every edge of the warp has taken a
+// Newton iterations: the outer roots converge quadratically from the safe
+// start; the inner ones start from the deflated estimate.  `outer` reaches
+// the type's rounding from the start above over depths 0.1-10 m and layer
+// velocities up to 6 m/s (checked against extended-precision roots).  The
+// outer iteration may stop early once every edge of the warp has taken a
 // step below tol * max(c1, c2) (after that the error is of the order of the
-// type's rounding), at most `outer` iterations.
+// type's rounding).
 template <typename T> struct Iters;
 template <> struct Iters<float> {
-  static constexpr int outer = 7, inner = 2;
+  static constexpr int outer = 6, inner = 2;
   static constexpr float tol = 2.44140625e-4f;  // 2^-12
 };
 template <> struct Iters<double> {
-  static constexpr int outer = 9, inner = 3;
+  static constexpr int outer = 8, inner = 3;
   static constexpr double tol = 1.4901161193847656e-8;  // 2^-26
 };
 
@@ -91,8 +111,7 @@ struct Quartic {
 
 // IR-Roe flux of one edge, two layers.  Writes the edge results; returns
 // false when A_ij has a complex pair of eigenvalues.  ADAPT: stop the outer
-// Newton iteration early (warp vote); the fp32 tile kernel of the grid runs
-// the fixed count, which measured faster there.
+// Newton iteration early (warp vote) instead of running the fixed count.
 template <typename T, bool ADAPT = false>
 __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
                                       bool wall, T* out) {
@@ -111,10 +130,14 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     ut_b[k] = b.qt[k] * ihb;
   }
   Quartic<T> q{un[0], un[1], cs[0], cs[1], r * cs[0] * cs[1]};
-  const T c1 = M2<T>::sq(cs[0]), c2 = M2<T>::sq(cs[1]);
+  const T c1 = M2<T>::sqa(cs[0]), c2 = M2<T>::sqa(cs[1]);
+  const T sc = M2<T>::sqa(cs[0] + cs[1]);
   // outer roots: from below / above, where p > 0, p convex and monotone
-  T l1 = fmin(un[0] - T(1.5) * c1, un[1] - T(1.5) * c2);
-  T l4 = fmax(un[0] + T(1.5) * c1, un[1] + T(1.5) * c2);
+  // (the approximate square roots widened by 2^-12, far more than their
+  // error, so the starts stay outside)
+  const T kr2 = T(1.4142135623730951 * (1.0 + 1.0 / 4096)), ks = T(1.0 + 1.0 / 4096);
+  T l1 = fmax(fmin(un[0] - kr2 * c1, un[1] - kr2 * c2), fmin(un[0], un[1]) - ks * sc);
+  T l4 = fmin(fmax(un[0] + kr2 * c1, un[1] + kr2 * c2), fmax(un[0], un[1]) + ks * sc);
   const T tol = Iters<T>::tol * fmax(c1, c2);
   const unsigned act = ADAPT ? __activemask() : 0u;
 #pragma unroll
@@ -123,7 +146,7 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     const T s4 = q.p(l4) * M2<T>::rcp(q.dp(l4));
     l1 -= s1;
     l4 -= s4;
-    if (ADAPT && it >= 2 && __all_sync(act, (fabs(s1) <= tol) & (fabs(s4) <= tol))) break;
+    if (ADAPT && it >= 1 && __all_sync(act, (fabs(s1) <= tol) & (fabs(s4) <= tol))) break;
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const T p3 = T(-2) * (un[0] + un[1]);
@@ -133,7 +156,7 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   const T cc = p2 + ss * bb - pp;
   const T disc = bb * bb - T(4) * cc;
   const bool hyper = disc > T(0);
-  const T sd = M2<T>::sq(hyper ? disc : T(0));
+  const T sd = M2<T>::sqa(hyper ? disc : T(0));
   T l2 = T(0.5) * (-bb - sd), l3 = T(0.5) * (-bb + sd);
 #pragma unroll
   for (int it = 0; it < Iters<T>::inner; ++it) {

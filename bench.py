@@ -45,12 +45,19 @@ sys.path.insert(0, ROOT)
 METRIC = "cell-updates/s (Mcell-steps/s) of the Roe FV step; achieved HBM GB/s vs peak"
 UNIT = "Mcell-updates/s"
 BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC written
-# Floating-point operations per cell-update of the two-layer step, counted
-# from the kernel's formulas (an FMA counts 2, a division or square root 1):
-# about 2.16 edge evaluations per cell (tile halo included) of ~494 (fp32,
-# 7 + 2 Newton iterations per outer / inner root) or ~584 (fp64, 9 + 3)
-# flops, plus the residual sums and the update.
-FLOPS_PER_CELL_2L = {32: 1100, 64: 1290}
+# Floating-point operations of one two-layer edge flux, counted from its
+# formulas (an add or a multiply 1, an FMA 2; square
+# roots, reciprocals and reciprocal square roots not counted): 213 outside
+# the root iterations, 28 per outer Newton iteration (two roots x 14) and 28
+# per inner one.  The outer iteration stops once every edge of the warp has
+# converged: on the interface dam break and the triangle workload it takes
+# 2.01 iterations per edge in fp32 and 3.01 in fp64 (counted on the GPU with
+# an instrumented build); the inner one runs 2 (fp32) or 3 (fp64).
+FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2, 64: 213 + 28 * 3.01 + 28 * 3}
+# Per cell-update on a grid: two edges (each edge once; the tiles' halo
+# recomputation not counted) plus 25 for the per-cell quantities and the
+# residual sums.
+FLOPS_PER_CELL_2L = {p: 2 * FLOPS_PER_EDGE_2L[p] + 25 for p in (32, 64)}
 # FP32 FMA peak of a GB300: 152 SMs x 128 lanes x 2 flops x 2.07 GHz;
 # FP64: the nominal 1.25 TFLOP/s of the part.
 ALU_PEAK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
@@ -63,6 +70,8 @@ KERNEL_SOURCES = {
     # (swe_fastmath.cuh is used by the fp64 kernels only, which have no
     # traffic record)
     "cart2_flux_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
+                          "cart2_flux_traffic.txt"),
+    "cart2_step_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
                           "cart2_flux_traffic.txt"),
     "cart2_update_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
                             "cart2_flux_traffic.txt"),
@@ -81,13 +90,12 @@ def source_hash(files):
         h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
 # Triangle meshes, per edge: floating-point operations of the edge kernel,
-# counted from its formulas (an FMA counts 2; square roots, reciprocals and
-# reciprocal square roots, about 29 of them for two layers, are not counted):
-# two layers 494 (fp32: 7 + 2 Newton iterations per outer / inner root) or
-# 584 (fp64: 9 + 3) in the Roe flux, plus 79 for the rotations into and out
-# of the edge frame, the fluctuation terms and the edge-length scaling; one
-# layer 88.
-FLOPS_PER_EDGE_MESH = {(2, 32): 573, (2, 64): 663, (1, 32): 88, (1, 64): 88}
+# counted from its formulas: two layers the Roe flux above (2.0 outer
+# iterations per edge in fp32, 3.0 in fp64 on the triangle workload) plus 79
+# for the rotations into and out of the edge frame, the fluctuation terms and
+# the edge-length scaling; one layer 88.
+FLOPS_PER_EDGE_MESH = {(2, 32): 213 + 28 * 2.0 + 28 * 2 + 79,
+                       (2, 64): 213 + 28 * 3.0 + 28 * 3 + 79, (1, 32): 88, (1, 64): 88}
 # One layer on a grid: floating-point operations per cell-update of the
 # fused step, counted from its formulas (FMA = 2; the 10 reciprocals and
 # reciprocal square roots per cell not counted): 36 per edge flux pair in the
@@ -121,6 +129,8 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
         return "hbm", BYTES_PER_CELL[precision] * n_cells, "B"
     if kernel == "cart2_flux_kernel":
         return "alu", FLOPS_PER_CELL_2L[precision] * n_cells, "flop"
+    if kernel == "cart2_step_kernel":   # + the fused update, 6 FMAs per cell
+        return "alu", (FLOPS_PER_CELL_2L[precision] + 12) * n_cells, "flop"
     if kernel == "cart2_update_kernel":
         return "hbm", 3 * 6 * e * n_cells, "B"
     ne = 11 if nl == 2 else 7
@@ -518,6 +528,7 @@ def main():
 
     peak, peak_kind = load_peaks()
     kernels = {}
+    ktimes = {k: v for k, v in ktimes.items() if v[0] > 0}
     for name, (launches, kms) in ktimes.items():
         bound, amount, unit = kernel_model(name, precision, nl, n, info["n_edges"])
         avg = kms / max(launches, 1)

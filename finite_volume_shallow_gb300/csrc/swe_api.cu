@@ -31,8 +31,12 @@ struct swe_state {
   int64_t field_stride = 0;  // elements between field bases in the allocation
   void* dev = nullptr;
   size_t dev_bytes = 0;
-  void* w[2][6] = {{nullptr}};  // one layer: two buffers of 4; two layers: w[0][0..5]
-  void* R[6] = {nullptr};        // two layers: residual scratch
+  void* w[2][6] = {{nullptr}};  // two buffers of the 4 (one layer) or 6 fields
+  void* R[6] = {nullptr};        // residual scratch (two layers: buffer 0; meshes)
+  void* R1[6] = {nullptr};       // two layers on a grid: residual buffer 1
+  int lazy2 = -1;     // two layers on a grid: buffer holding a step whose
+                      // update is still to be applied (inside swe_run only)
+  double cfl2 = 0;    // the cfl of that step
   void* H = nullptr;
   void* slots = nullptr;      // 3 wave-speed maxima (8 bytes each)
   double* dt_hist = nullptr;
@@ -63,6 +67,8 @@ struct swe_state {
   std::vector<int32_t> h_new_of_old;  // host copy (swe_cell_index)
   struct Timing* timing = nullptr;    // per-kernel event ring (swe_set_timing)
   const cudaEvent_t* marks = nullptr; // events of the step being enqueued, or null
+  int* mark_kid = nullptr;            // with marks: kernel index of each interval
+  int* mark_n = nullptr;              // with marks: intervals recorded so far
 };
 
 // Per-kernel device time: a ring of event sets, one set per step; a set is
@@ -71,6 +77,8 @@ struct swe_state {
 struct Timing {
   static constexpr int kSlots = 64, kMaxK = 3;
   cudaEvent_t ev[kSlots][kMaxK + 1] = {};
+  int kid[kSlots][kMaxK] = {};  // kernel of the interval ev[k] .. ev[k + 1]
+  int cnt[kSlots] = {};         // intervals of the slot's step
   bool pending[kSlots] = {};
   int next = 0, nk = 0;
   const char* names[kMaxK] = {};
@@ -182,36 +190,99 @@ swe_status enqueue_check2(swe_state* s) {
   return SWE_OK;
 }
 
+// Per-kernel timing of a step whose kernels vary: mark(k) before kernel k,
+// mark_end() after the last.
+swe_status mark(swe_state* s, int kid) {
+  if (!s->marks) return SWE_OK;
+  const int n = *s->mark_n;
+  CK(cudaEventRecord(s->marks[n], s->stream));
+  s->mark_kid[n] = kid;
+  *s->mark_n = n + 1;
+  return SWE_OK;
+}
+swe_status mark_end(swe_state* s) {
+  if (!s->marks) return SWE_OK;
+  CK(cudaEventRecord(s->marks[*s->mark_n], s->stream));
+  return SWE_OK;
+}
+
+// Step m of a two-layer grid.  Without a pending update: the flux pass of
+// W^m (buffer 0).  With one (step m - 1 left W^{m-1}, R^{m-1} in buffer a):
+// the fused pass, which applies it and evaluates the fluxes of W^m into
+// buffer a ^ 1.  `last`: then apply step m's own update into buffer 0.
+// Wave-speed slots: the flux of step m reduces into slot m % 3, which must
+// be zero; the update of step m (fused or not) reads it and zeroes slot
+// (m + 1) % 3; the update that ends a run also zeroes slot (m + 2) % 3, the
+// one the first fused pass of the next run reduces into (the set-up zeroes
+// all three).
 template <typename T>
-swe_status enqueue_step2(swe_state* s, double cfl) {
-  Step2Args<T> f;
-  Update2Args<T> u;
+swe_status enqueue_step2(swe_state* s, double cfl, bool last) {
   char* sl = (char*)s->slots;
-  for (int k = 0; k < 6; ++k) {
-    f.w[k] = (const T*)s->w[0][k];
-    f.R[k] = (T*)s->R[k];
-    u.w[k] = (T*)s->w[0][k];
-    u.R[k] = (const T*)s->R[k];
-  }
+  auto slot = [&](int64_t m) { return (void*)(sl + (m % 3) * sizeof(uint64_t)); };
+  auto rbuf = [&](int b) { return b == 0 ? s->R : s->R1; };
+  const int64_t m = s->step;
+  Step2Args<T> f;
   f.H = (const T*)s->H;
-  f.nx = u.nx = s->nx;
-  f.ny = u.ny = s->ny;
-  f.pitch = u.pitch = s->pitch;
+  f.nx = s->nx;
+  f.ny = s->ny;
+  f.pitch = s->pitch;
   f.g = (T)s->p.g;
   f.r = (T)s->p.r;
   f.rho = (T)(s->dx / s->dy);
-  f.tmax_out = sl + (s->step % 3) * sizeof(uint64_t);
-  f.err = u.err = s->err;
-  u.two_cfl = 2.0 * cfl;
-  u.dx = s->dx;
-  u.tmax_in = sl + (s->step % 3) * sizeof(uint64_t);
-  u.tmax_clear = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
-  u.dt_hist = s->dt_hist;
-  u.t_dev = s->t_dev;
-  u.step = s->step;
-  CK(launch_step2<T>(f, u, s->stream, s->marks));
-  s->step += 1;
-  return SWE_OK;
+  f.tmax_out = slot(m);
+  f.err = s->err;
+  auto upd_args = [&](Update2Args<T>& u, int a, int dst, int64_t step, double c, bool end) {
+    for (int k = 0; k < 6; ++k) {
+      u.win[k] = (const T*)s->w[a][k];
+      u.w[k] = (T*)s->w[dst][k];
+      u.R[k] = (const T*)rbuf(a)[k];
+    }
+    u.nx = s->nx;
+    u.ny = s->ny;
+    u.pitch = s->pitch;
+    u.two_cfl = 2.0 * c;
+    u.dx = s->dx;
+    u.tmax_in = slot(step);
+    u.tmax_clear = slot(m + 1);
+    u.tmax_clear2 = end ? slot(m + 2) : nullptr;
+    u.dt_hist = s->dt_hist;
+    u.t_dev = s->t_dev;
+    u.step = step;
+    u.err = s->err;
+  };
+  int a;
+  swe_status st;
+  if (s->lazy2 < 0) {
+    a = 0;
+    for (int k = 0; k < 6; ++k) {
+      f.w[k] = (const T*)s->w[0][k];
+      f.R[k] = (T*)s->R[k];
+    }
+    if ((st = mark(s, 0)) != SWE_OK) return st;
+    CK(launch_flux2<T>(f, s->stream));
+  } else {
+    const int p = s->lazy2;
+    a = p ^ 1;
+    for (int k = 0; k < 6; ++k) {
+      f.w[k] = (const T*)s->w[p][k];
+      f.R[k] = (T*)rbuf(a)[k];
+    }
+    Update2Args<T> u;
+    upd_args(u, p, a, m - 1, s->cfl2, false);
+    if ((st = mark(s, 1)) != SWE_OK) return st;
+    CK(launch_fused2<T>(f, u, s->stream));
+  }
+  s->step = m + 1;
+  s->lazy2 = a;
+  s->cfl2 = cfl;
+  if (last) {
+    Update2Args<T> u;
+    upd_args(u, a, 0, m, cfl, true);
+    if ((st = mark(s, 2)) != SWE_OK) return st;
+    CK(launch_update2<T>(u, s->stream));
+    s->lazy2 = -1;
+  }
+  return mark_end(s);
 }
 
 // Meshes: the gather pass of step n reduces into slot n % 3, the update of
@@ -271,12 +342,13 @@ swe_status enqueue_dt0_any(swe_state* s) {
 }
 swe_status timing_harvest(Timing* tm, int slot) {
   if (!tm->pending[slot]) return SWE_OK;
-  CK(cudaEventSynchronize(tm->ev[slot][tm->nk]));
-  for (int k = 0; k < tm->nk; ++k) {
+  const int n = tm->cnt[slot];
+  CK(cudaEventSynchronize(tm->ev[slot][n]));
+  for (int k = 0; k < n; ++k) {
     float f = 0.f;
     CK(cudaEventElapsedTime(&f, tm->ev[slot][k], tm->ev[slot][k + 1]));
-    tm->ms[k] += f;
-    tm->launches[k] += 1;
+    tm->ms[tm->kid[slot][k]] += f;
+    tm->launches[tm->kid[slot][k]] += 1;
   }
   tm->pending[slot] = false;
   return SWE_OK;
@@ -293,28 +365,40 @@ swe_status timing_harvest_all(swe_state* s) {
   return SWE_OK;
 }
 
-swe_status enqueue_step_timed(swe_state* s, double cfl);
+swe_status enqueue_step_timed(swe_state* s, double cfl, bool last);
 
-swe_status enqueue_step_any(swe_state* s, double cfl) {
-  if (s->timing && s->timing->on) return enqueue_step_timed(s, cfl);
+// `last`: the last step of a swe_run / swe_step call (a two-layer grid then
+// applies its pending update).
+swe_status enqueue_step_any(swe_state* s, double cfl, bool last) {
+  if (s->timing && s->timing->on) return enqueue_step_timed(s, cfl, last);
   if (s->mesh)
     return s->prec == 32 ? enqueue_mesh_step<float>(s, cfl) : enqueue_mesh_step<double>(s, cfl);
   if (s->nl == 2)
-    return s->prec == 32 ? enqueue_step2<float>(s, cfl) : enqueue_step2<double>(s, cfl);
+    return s->prec == 32 ? enqueue_step2<float>(s, cfl, last)
+                         : enqueue_step2<double>(s, cfl, last);
   return s->prec == 32 ? enqueue_step<float>(s, cfl) : enqueue_step<double>(s, cfl);
 }
 
-swe_status enqueue_step_timed(swe_state* s, double cfl) {
+swe_status enqueue_step_timed(swe_state* s, double cfl, bool last) {
   Timing* tm = s->timing;
   const int slot = tm->next;
   swe_status st = timing_harvest(tm, slot);  // the slot's previous step
   if (st != SWE_OK) return st;
   s->marks = tm->ev[slot];
+  s->mark_kid = tm->kid[slot];
+  s->mark_n = &tm->cnt[slot];
+  tm->cnt[slot] = 0;
   tm->on = false;  // plain enqueue below
-  st = enqueue_step_any(s, cfl);
+  st = enqueue_step_any(s, cfl, last);
   tm->on = true;
   s->marks = nullptr;
+  s->mark_kid = nullptr;
+  s->mark_n = nullptr;
   if (st != SWE_OK) return st;
+  if (s->mesh || s->nl == 1) {  // a fixed kernel sequence, marked by the launcher
+    tm->cnt[slot] = tm->nk;
+    for (int k = 0; k < tm->nk; ++k) tm->kid[slot][k] = k;
+  }
   tm->pending[slot] = true;
   tm->next = (slot + 1) % Timing::kSlots;
   return SWE_OK;
@@ -327,9 +411,10 @@ void timing_names(swe_state* s, Timing* tm) {
     tm->names[1] = "mesh_gather_kernel";
     tm->names[2] = "mesh_update_kernel";
   } else if (s->nl == 2) {
-    tm->nk = 2;
+    tm->nk = 3;
     tm->names[0] = "cart2_flux_kernel";
-    tm->names[1] = "cart2_update_kernel";
+    tm->names[1] = "cart2_step_kernel";
+    tm->names[2] = "cart2_update_kernel";
   } else {
     tm->nk = 1;
     tm->names[0] = "cart1_step_kernel";
@@ -397,14 +482,16 @@ swe_status fill_pads(swe_state* s) {
   // whole padded arrays: depths 1, everything else 0; interiors are then
   // copied (a resting state in the padding keeps every padded edge benign)
   const int64_t n = s->field_stride;
-  const int nbuf = s->nl == 2 ? 1 : 2;
-  for (int b = 0; b < nbuf; ++b)
+  for (int b = 0; b < 2; ++b)
     for (int f = 0; f < s->nf; ++f) {
       const bool depth = f == 0 || (s->nl == 2 && f == 3);
       CK(launch_fill<T>((T*)s->w[b][f], n, depth ? T(1) : T(0), s->stream));
     }
   if (s->nl == 2)
-    for (int f = 0; f < 6; ++f) CK(launch_fill<T>((T*)s->R[f], n, T(0), s->stream));
+    for (int f = 0; f < 6; ++f) {
+      CK(launch_fill<T>((T*)s->R[f], n, T(0), s->stream));
+      CK(launch_fill<T>((T*)s->R1[f], n, T(0), s->stream));
+    }
   CK(launch_fill<T>((T*)s->H, n, T(0), s->stream));
   return SWE_OK;
 }
@@ -534,7 +621,8 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   const int64_t fbytes = round_up(felems * (int64_t)s->esz, 256);
   s->field_stride = fbytes / (int64_t)s->esz;
   const int64_t aux = kAuxBytes;
-  const int nalloc = s->nl == 2 ? 13 : 9;  // fields (+ scratch) + H
+  // two buffers of the fields (+ two of the residual for two layers) + H
+  const int nalloc = s->nl == 2 ? 25 : 9;
   s->dev_bytes = (size_t)(nalloc * fbytes + aux);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
   if (e != cudaSuccess) {
@@ -549,12 +637,17 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
         p += fbytes;
       }
   } else {
+    for (int b = 0; b < 2; ++b)
+      for (int f = 0; f < 6; ++f) {
+        s->w[b][f] = p;
+        p += fbytes;
+      }
     for (int f = 0; f < 6; ++f) {
-      s->w[0][f] = p;
+      s->R[f] = p;
       p += fbytes;
     }
     for (int f = 0; f < 6; ++f) {
-      s->R[f] = p;
+      s->R1[f] = p;
       p += fbytes;
     }
   }
@@ -807,8 +900,11 @@ swe_status swe_step(swe_state* s, double cfl, double* dt_out) {
   if (!s) return SWE_ERR_ARG;
   if (!(cfl > 0.0 && cfl <= 1.0)) return SWE_ERR_ARG;
   if (s->sticky) return status_of_bits(s->sticky);
-  swe_status st = enqueue_step_any(s, cfl);
-  if (st != SWE_OK) return st;
+  swe_status st = enqueue_step_any(s, cfl, true);
+  if (st != SWE_OK) {
+    s->lazy2 = -1;
+    return st;
+  }
   CK(cudaMemcpyAsync(s->h_dt, s->dt_hist + ((s->step - 1) % kHistCap), sizeof(double),
                      cudaMemcpyDeviceToHost, s->stream));
   if ((st = read_err(s)) != SWE_OK) return st;
@@ -820,8 +916,11 @@ swe_status swe_run(swe_state* s, int64_t nsteps) {
   if (!s || nsteps < 0) return SWE_ERR_ARG;
   if (s->sticky) return status_of_bits(s->sticky);
   for (int64_t n = 0; n < nsteps; ++n) {
-    swe_status st = enqueue_step_any(s, s->p.cfl);
-    if (st != SWE_OK) return st;
+    swe_status st = enqueue_step_any(s, s->p.cfl, n == nsteps - 1);
+    if (st != SWE_OK) {
+      s->lazy2 = -1;  // a failed launch leaves the state undefined
+      return st;
+    }
   }
   swe_status st = read_err(s);
   if (st != SWE_OK) return st;

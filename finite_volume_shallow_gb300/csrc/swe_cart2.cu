@@ -6,7 +6,7 @@
 // coupled through -g h1 dh2 and -r g h2 dh1) and Sec. 2.2 (eq. (4), steps 1-4
 // with the 4x4 Roe matrix A_ij of the rotated system, CFL eq. (5)).
 //
-// Two launches per step:
+// Kernels:
 //   cart2_flux_kernel    a 32 x 8 tile of cells and its one-cell halo in
 //                        shared memory; every edge of the tile evaluated once
 //                        (as in the tile scheme of A multi-GPU shallow-water
@@ -14,9 +14,19 @@
 //                        4); each cell sums its four edges into the residual
 //                        R (global scratch) and max-reduces sum |Gamma| ||D||,
 //                        which fixes dt of this step;
-//   cart2_update_kernel  W -= (dt/dx) R in place (16-byte vectors over whole
-//                        rows, the padding left as it is), checks, dt
-//                        bookkeeping.
+//   cart2_step_kernel    the same with the update of the previous step fused
+//                        into the tile load: it reads W^{n-1}, R^{n-1} and
+//                        the wave-speed maximum of W^{n-1}, forms W^n =
+//                        W^{n-1} - (dt/dx) R^{n-1} for the tile and its halo,
+//                        writes W^n of its own cells to the other buffer and
+//                        evaluates the fluxes of W^n (W and R alternate
+//                        between two buffers);
+//   cart2_update_kernel  W -= (dt/dx) R (16-byte vectors over whole rows, the
+//                        padding left as it is), checks, dt bookkeeping: a
+//                        lone step, and the last step of a run.
+// A run of n >= 2 steps is one flux launch, n - 1 fused launches and one
+// update; every form applies the update with the same rounding (upd below),
+// so a run and the same steps taken one at a time agree bit for bit.
 //
 // The edge flux itself (quartic roots, closed-form P^- d) is in swe_roe2.cuh.
 #include <cuda_runtime.h>
@@ -43,6 +53,36 @@ constexpr int TX = kTile2X;
 #endif
 template <typename T> constexpr bool kAdapt2 = sizeof(T) == 8 || SWE_CART2_ADAPT32 != 0;
 
+// W^{n+1} = W^n - (dt/dx) R, one fused multiply-add
+__device__ __forceinline__ float upd(float w, float k, float r) { return __fmaf_rn(-k, r, w); }
+__device__ __forceinline__ double upd(double w, double k, double r) { return __fma_rn(-k, r, w); }
+
+// dt of a finished flux pass from its wave-speed maximum (eq. (5)) as
+// dt/dx = 2 cfl / max, computed by one thread per block; block (0, 0) also
+// records dt, advances the clock and zeroes the slot(s) the next flux
+// passes will reduce into.
+template <typename T>
+__device__ __forceinline__ T dt_of_step(const Update2Args<T>& A, T* k_sh) {
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
+    const double dtdx = A.two_cfl / (double)tm;
+    *k_sh = (T)dtdx;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      const double dt = dtdx * A.dx;
+      A.dt_hist[A.step % kHistCap] = dt;
+      *A.t_dev += dt;
+      if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
+      else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
+      if (A.tmax_clear2) {
+        if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear2) = 0u;
+        else *reinterpret_cast<unsigned long long*>(A.tmax_clear2) = 0ull;
+      }
+    }
+  }
+  __syncthreads();
+  return *k_sh;
+}
+
 template <typename T> struct Vec2;
 template <> struct Vec2<float> { using type = float4; static constexpr int n = 4; };
 template <> struct Vec2<double> { using type = double2; static constexpr int n = 2; };
@@ -67,30 +107,54 @@ __device__ __forceinline__ Side2<T> side_of(const T (*c)[TY + 2][TX + 2], int lj
   return s;
 }
 
-template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(const Step2Args<T> A) {
+// FUSED: the cart2_step_kernel form (U carries the previous step's update);
+// otherwise U is unused.
+template <typename T, bool ANISO, bool FUSED>
+__device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Args<T>& U) {
   constexpr int TY = Tile2Y<T>::v;
   __shared__ T cq[NCQ][TY + 2][TX + 2];
   __shared__ T ex[NEQ][TY][TX + 1];   // x-edge e joins local columns e and e + 1
   __shared__ T ey[NEQ][TY + 1][TX];   // y-edge e joins local rows e and e + 1
+  __shared__ T k_sh;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int t = ty * TX + tx;
   const int i0 = blockIdx.x * TX, j0 = blockIdx.y * TY;
   const int nx = A.nx, ny = A.ny;
   const T g = A.g, gh = T(0.5) * A.g, r = A.r;
   pdl_wait();
+  const T k = FUSED ? dt_of_step<T>(U, &k_sh) : T(0);
+  unsigned bad = 0;
 
   // tile + one-cell halo (the padded layout keeps every read in bounds)
   for (int idx = t; idx < (TX + 2) * (TY + 2); idx += TX * TY) {
     const int li = idx % (TX + 2), lj = idx / (TX + 2);
     const int64_t o = (int64_t)(j0 - 1 + lj + kPadY) * A.pitch + (i0 - 1 + li + kPadX);
-    const T h1 = A.w[0][o], h2 = A.w[3][o];
+    T w[6];
+#pragma unroll
+    for (int f = 0; f < 6; ++f) w[f] = A.w[f][o];
+    if (FUSED) {
+      // the previous step's update, on cells of the grid only (the padding
+      // keeps its resting state); the tile's own cells are written out
+      const int gi = i0 - 1 + li, gj = j0 - 1 + lj;
+      if (gi >= 0 && gi < nx && gj >= 0 && gj < ny) {
+#pragma unroll
+        for (int f = 0; f < 6; ++f) w[f] = upd(w[f], k, U.R[f][o]);
+        if (li >= 1 && li <= TX && lj >= 1 && lj <= TY) {
+#pragma unroll
+          for (int f = 0; f < 6; ++f) U.w[f][o] = w[f];
+          const T sum = ((w[0] + w[1]) + (w[2] + w[3])) + (w[4] + w[5]);
+          if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
+          if (!(w[0] > T(0)) || !(w[3] > T(0))) bad |= kErrDepth;
+        }
+      }
+    }
+    const T h1 = w[0], h2 = w[3];
     cq[C_H1][lj][li] = h1;
-    cq[C_Q1X][lj][li] = A.w[1][o];
-    cq[C_Q1Y][lj][li] = A.w[2][o];
+    cq[C_Q1X][lj][li] = w[1];
+    cq[C_Q1Y][lj][li] = w[2];
     cq[C_H2][lj][li] = h2;
-    cq[C_Q2X][lj][li] = A.w[4][o];
-    cq[C_Q2Y][lj][li] = A.w[5][o];
+    cq[C_Q2X][lj][li] = w[4];
+    cq[C_Q2Y][lj][li] = w[5];
     cq[C_H][lj][li] = A.H[o];
     const T r1 = M2<T>::rsq(h1), r2 = M2<T>::rsq(h2);
     cq[C_RS1][lj][li] = r1;
@@ -153,9 +217,21 @@ __global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(cons
   }
   // hyperbolicity of every edge of this block, and the block's max of T
   if (!__all_sync(kFull2, hyper_ok) && (tx & 31) == 0) atomicOr(A.err, kErrHyperbolic);
+  if (FUSED && bad) atomicOr(A.err, bad);
   T m = own ? Tsum : T(0);
   pdl_trigger();
   block_max_publish<T, TX * TY / 32>(m, A.tmax_out);
+}
+
+template <typename T, bool ANISO>
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(const Step2Args<T> A) {
+  flux_tile<T, ANISO, false>(A, Update2Args<T>{});
+}
+
+template <typename T, bool ANISO>
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v)
+    cart2_step_kernel(const Step2Args<T> A, const Update2Args<T> U) {
+  flux_tile<T, ANISO, true>(A, U);
 }
 
 template <typename T>
@@ -164,20 +240,7 @@ __global__ void cart2_update_kernel(const Update2Args<T> A) {
   // would cost more than the update on GB300's FP64 pipe)
   __shared__ T k_sh;
   pdl_wait();
-  if (threadIdx.x == 0 && threadIdx.y == 0) {
-    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
-    const double dtdx = A.two_cfl / (double)tm;
-    k_sh = (T)dtdx;
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
-      const double dt = dtdx * A.dx;
-      A.dt_hist[A.step % kHistCap] = dt;
-      *A.t_dev += dt;
-      if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
-      else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
-    }
-  }
-  __syncthreads();
-  const T k = k_sh;
+  const T k = dt_of_step<T>(A, &k_sh);
   // whole rows in 16-byte vectors (the pitch is a multiple of 32); elements
   // of the padding keep their value exactly (even if k is not finite)
   using V = typename Vec2<T>::type;
@@ -192,14 +255,14 @@ __global__ void cart2_update_kernel(const Update2Args<T> A) {
     T w[6][VN];
 #pragma unroll
     for (int f = 0; f < 6; ++f) {
-      V wv = reinterpret_cast<const V*>(A.w[f])[o];
+      V wv = reinterpret_cast<const V*>(A.win[f])[o];
       const V rv = reinterpret_cast<const V*>(A.R[f])[o];
       T* wp = reinterpret_cast<T*>(&wv);
       const T* rp = reinterpret_cast<const T*>(&rv);
 #pragma unroll
       for (int j = 0; j < VN; ++j) {
         const bool in = c0 + j >= 0 && c0 + j < A.nx;
-        const T nw = wp[j] - k * rp[j];
+        const T nw = upd(wp[j], k, rp[j]);
         wp[j] = in ? nw : wp[j];
         w[f][j] = wp[j];
       }
@@ -236,23 +299,29 @@ __global__ void cart2_check_kernel(const Fields6<T> w6, int nx, int ny, int pitc
 }  // namespace
 
 template <typename T>
-cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st,
-                         const cudaEvent_t* marks) {
+cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st) {
   constexpr int TY = Tile2Y<T>::v;
   dim3 block(TX, TY);
   dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
-  if (marks) cudaEventRecord(marks[0], st);
-  cudaError_t e = f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false>, grid, block, 0, st, f)
-                                : launch_pdl(cart2_flux_kernel<T, true>, grid, block, 0, st, f);
-  if (e != cudaSuccess) return e;
+  return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false>, grid, block, 0, st, f)
+                       : launch_pdl(cart2_flux_kernel<T, true>, grid, block, 0, st, f);
+}
+
+template <typename T>
+cudaError_t launch_fused2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st) {
+  constexpr int TY = Tile2Y<T>::v;
+  dim3 block(TX, TY);
+  dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
+  return f.rho == T(1) ? launch_pdl(cart2_step_kernel<T, false>, grid, block, 0, st, f, u)
+                       : launch_pdl(cart2_step_kernel<T, true>, grid, block, 0, st, f, u);
+}
+
+template <typename T>
+cudaError_t launch_update2(const Update2Args<T>& u, cudaStream_t st) {
   constexpr int VN = Vec2<T>::n;
   dim3 ub(64, 4);
   dim3 ug((unsigned)((u.pitch / VN + 63) / 64), (unsigned)min((u.ny + 3) / 4, 1024));
-  if (marks) cudaEventRecord(marks[1], st);
-  e = launch_pdl(cart2_update_kernel<T>, ug, ub, 0, st, u);
-  if (e != cudaSuccess) return e;
-  if (marks) cudaEventRecord(marks[2], st);
-  return cudaGetLastError();
+  return launch_pdl(cart2_update_kernel<T>, ug, ub, 0, st, u);
 }
 
 template <typename T>
@@ -263,10 +332,14 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
   return cudaGetLastError();
 }
 
-template cudaError_t launch_step2<float>(const Step2Args<float>&, const Update2Args<float>&,
-                                         cudaStream_t, const cudaEvent_t*);
-template cudaError_t launch_step2<double>(const Step2Args<double>&, const Update2Args<double>&,
-                                          cudaStream_t, const cudaEvent_t*);
+template cudaError_t launch_flux2<float>(const Step2Args<float>&, cudaStream_t);
+template cudaError_t launch_flux2<double>(const Step2Args<double>&, cudaStream_t);
+template cudaError_t launch_fused2<float>(const Step2Args<float>&, const Update2Args<float>&,
+                                          cudaStream_t);
+template cudaError_t launch_fused2<double>(const Step2Args<double>&, const Update2Args<double>&,
+                                           cudaStream_t);
+template cudaError_t launch_update2<float>(const Update2Args<float>&, cudaStream_t);
+template cudaError_t launch_update2<double>(const Update2Args<double>&, cudaStream_t);
 template cudaError_t launch_check2<float>(const Fields6<float>&, int, int, int, unsigned*,
                                           cudaStream_t);
 template cudaError_t launch_check2<double>(const Fields6<double>&, int, int, int, unsigned*,

@@ -107,14 +107,20 @@ struct Step2Args {
   void* tmax_out;  // max over cells of sum_x D + rho sum_y D (must start at 0)
   unsigned* err;
 };
+// The update W_out = W_in - (dt/dx) R of step `step`, dt from the wave-speed
+// maximum in tmax_in.  cart2_update_kernel reads win and writes w (the same
+// buffer, or buffer 0 at the end of a run); cart2_step_kernel writes the
+// updated cells of its tiles to w.
 template <typename T>
 struct Update2Args {
+  const T* win[6];
   T* w[6];
   const T* R[6];
   int nx, ny, pitch;
   double two_cfl, dx;
   const void* tmax_in;
   void* tmax_clear;
+  void* tmax_clear2;  // a second slot to zero, or null
   double* dt_hist;
   double* t_dev;
   int64_t step;
@@ -122,8 +128,11 @@ struct Update2Args {
 };
 
 template <typename T>
-cudaError_t launch_step2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st,
-                         const cudaEvent_t* marks = nullptr);
+cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st);
+template <typename T>
+cudaError_t launch_fused2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st);
+template <typename T>
+cudaError_t launch_update2(const Update2Args<T>& u, cudaStream_t st);
 template <typename T>
 cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsigned* err,
                           cudaStream_t st);

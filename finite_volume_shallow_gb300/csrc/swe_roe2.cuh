@@ -65,19 +65,23 @@ template <> struct M2<double> {  // Newton-refined reciprocal (swe_fastmath.cuh)
 };
 
 // Newton iterations: the outer roots converge quadratically from the safe
-// start; the inner ones start from the deflated estimate.  `outer` reaches
-// the type's rounding from the start above over depths 0.1-10 m and layer
-// velocities up to 6 m/s (checked against extended-precision roots).  The
-// outer iteration may stop early once every edge of the warp has taken a
-// step below tol * max(c1, c2) (after that the error is of the order of the
-// type's rounding).
+// start; the inner ones start from the deflated estimate.  The outer
+// iteration stops once every edge of the warp has taken a step below
+// tol * max(c1, c2) (after that the error is of the order of the type's
+// rounding), after 2 iterations on typical states.  `outer` bounds it: at
+// small density ratios the two largest roots of p sit close together when
+// u1 + c1 ~ u2 + c2, and Newton first converges linearly there; checked
+// against extended-precision roots over depths 0.1-10 m, layer velocities up
+// to 3 m/s and r from 0.001 to 0.98, 9 iterations reach fp32 rounding and 11
+// fp64 rounding.  (At r = 0 with u1 + c1 = u2 + c2 the root is double and the
+// eigenvector basis of A_ij degenerates.)
 template <typename T> struct Iters;
 template <> struct Iters<float> {
-  static constexpr int outer = 6, inner = 2;
+  static constexpr int outer = 10, inner = 2;
   static constexpr float tol = 2.44140625e-4f;  // 2^-12
 };
 template <> struct Iters<double> {
-  static constexpr int outer = 8, inner = 3;
+  static constexpr int outer = 12, inner = 3;
   static constexpr double tol = 1.4901161193847656e-8;  // 2^-26
 };
 

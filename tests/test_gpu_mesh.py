@@ -35,6 +35,19 @@ def test_two_layer_triangles(precision):
 
 
 @pytest.mark.parametrize("precision", [64, 32])
+def test_small_density_ratio_on_triangles(precision):
+    # layers of nearly equal depth at r = 0.01 (interface near mid-depth,
+    # tilted so that it moves): nearly coinciding outer roots
+    d = I.tri_workload(16, r=0.01, bump=0.0, sigma_scale=0.05)
+    x = I.tri_centroids(d["xy"], d["tri"])[:, 0]
+    d["h1"] = d["H"] * (0.5 + 0.02 * (x - x.mean()) / np.ptp(x))
+    d["h2"] = d["H"] - d["h1"]
+    rel = np.abs(np.sqrt(d["h1"]) - np.sqrt(d["h2"])) / np.sqrt(d["h1"])
+    assert rel.min() < 1e-3
+    assert_parity_mesh(d, precision, 20)
+
+
+@pytest.mark.parametrize("precision", [64, 32])
 def test_one_layer_triangles_with_pollutant(precision):
     d = I.tri_workload1(36, 22)
     assert_parity_mesh(d, precision, 60)

@@ -34,6 +34,19 @@ def test_moving_layers_over_hills(precision):
 
 
 @pytest.mark.parametrize("precision", [64, 32])
+@pytest.mark.parametrize("r", [0.01, 0.1])
+def test_small_density_ratio_near_double_roots(precision, r):
+    """Layers of nearly equal depth at a small density ratio: u1 + c1 and
+    u2 + c2 nearly coincide, so the two largest eigenvalues of A_ij sit close
+    together, where the outer Newton iteration converges slowly."""
+    d = I.two_layer_hills(41, 29, interface_depth=6.5, umax=0.05, bump=0.3, r=r)
+    c1 = np.sqrt(9.81 * d["h1"])
+    c2 = np.sqrt(9.81 * d["h2"])
+    assert np.min(np.abs(c1 - c2) / c1) < 1e-2
+    assert_parity2(d, precision, 20)
+
+
+@pytest.mark.parametrize("precision", [64, 32])
 @pytest.mark.parametrize("nx,ny", [(1, 1), (1, 7), (7, 1), (33, 9), (32, 8), (31, 5)])
 def test_small_and_ragged_grids(precision, nx, ny):
     d = I.two_layer_hills(nx, ny, umax=0.05, bump=0.3)

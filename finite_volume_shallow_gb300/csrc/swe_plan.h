@@ -16,13 +16,17 @@ namespace swe {
 #ifndef SWE_WALL_EXTRA_PCT
 #define SWE_WALL_EXTRA_PCT 25
 #endif
+#ifndef SWE_MIN_SEG_ROWS
+#define SWE_MIN_SEG_ROWS 32
+#endif
 struct StepPlan {
   int nbands, nsegs, nsegs_wall, units;
 };
 inline StepPlan plan_step(int64_t slots, int64_t nbands, int64_t ny) {
   StepPlan p;
   p.nbands = (int)nbands;
-  const int64_t min_rows = nbands * (ny / 32) * 4 <= slots ? 8 : 32;
+  const int64_t min_rows =
+      nbands * (ny / SWE_MIN_SEG_ROWS) * 4 <= slots ? 8 : SWE_MIN_SEG_ROWS;
   const int64_t most = ny / min_rows > 1 ? ny / min_rows : 1;
   int64_t S = slots / nbands;
   if (S > most) S = most;

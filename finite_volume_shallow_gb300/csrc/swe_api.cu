@@ -571,6 +571,20 @@ const char* swe_status_str(swe_status st) {
   return "unknown status";
 }
 
+swe_status swe_selftest_wait(int64_t budget_cycles) {
+  if (budget_cycles < 1 || budget_cycles > 4000000000LL) return SWE_ERR_ARG;
+  unsigned* err = nullptr;
+  cudaError_t e = cudaMalloc(&err, sizeof(unsigned));
+  if (e != cudaSuccess) return cuda_status(e);
+  unsigned bits = 0;
+  e = cudaMemset(err, 0, sizeof(unsigned));
+  if (e == cudaSuccess) e = launch_wait_selftest((long long)budget_cycles, err, nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(&bits, err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  cudaFree(err);
+  if (e != cudaSuccess) return cuda_status(e);
+  return status_of_bits(bits);
+}
+
 void swe_destroy(swe_state* s) {
   if (!s) return;
   if (s->stream || s->dev) cudaStreamSynchronize(s->stream);

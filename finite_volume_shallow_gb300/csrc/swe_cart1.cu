@@ -869,6 +869,20 @@ __global__ void cart1_dt0_kernel(const T* __restrict__ h, const T* __restrict__ 
   warp_max_publish<T>(tmax, tmax_out);
 }
 
+// The bounded wait of the march on a barrier nothing arrives on: it must
+// give up after `budget` cycles and report kErrTimeout.
+__global__ void wait_selftest_kernel(long long budget, unsigned* err) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_bounded(b, 0u, budget);
+  if (!__all_sync(kFull, ok) && threadIdx.x == 0) atomicOr(err, kErrTimeout);
+}
+
 template <typename T>
 __global__ void fill_kernel(T* p, int64_t n, T v) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -914,6 +928,11 @@ cudaError_t launch_dt0(const T* const* w, const T* H, int nx, int ny, int pitch,
   dim3 grid((unsigned)((nx + 127) / 128), (unsigned)(ny < 1024 ? ny : 1024));
   cart1_dt0_kernel<T><<<grid, 128, 0, st>>>(w[0], w[1], w[2], w[3], nx, ny, pitch, ghalf, rho,
                                             tmax_out, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(long long budget_cycles, unsigned* err, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(budget_cycles, err);
   return cudaGetLastError();
 }
 

@@ -271,6 +271,9 @@ cudaError_t launch_dt0(const T* const* w, const T* H, int nx, int ny, int pitch,
                        cudaStream_t st);
 template <typename T>
 cudaError_t launch_fill(T* base, int64_t count, T value, cudaStream_t st);
+// One warp running the step kernel's bounded mbarrier wait on a barrier
+// nothing arrives on; sets kErrTimeout in *err when the wait gives up.
+cudaError_t launch_wait_selftest(long long budget_cycles, unsigned* err, cudaStream_t st);
 template <typename T>
 cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes);
 

@@ -94,6 +94,7 @@ def load(build_if_needed: bool = True):
     L.swe_get_info.argtypes = [vp, C.POINTER(_Info)]
     L.swe_device_fields.argtypes = [vp, vp]
     L.swe_run_noalloc.argtypes = [C.POINTER(_Grid), C.POINTER(_Params), vp, vp, vp, i32, i64, vp]
+    L.swe_selftest_wait.argtypes = [i64]
     L.swe_destroy.argtypes = [vp]
     L.swe_destroy.restype = None
     L.swe_status_str.argtypes = [i32]
@@ -101,7 +102,8 @@ def load(build_if_needed: bool = True):
     for name in ("swe_create_grid", "swe_create_mesh", "swe_cell_index", "swe_mesh_info",
                  "swe_step", "swe_run",
                  "swe_get_state", "swe_set_state", "swe_get_dt_history", "swe_get_info",
-                 "swe_device_fields", "swe_run_noalloc", "swe_set_timing", "swe_get_timing"):
+                 "swe_device_fields", "swe_run_noalloc", "swe_set_timing", "swe_get_timing",
+                 "swe_selftest_wait"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -313,6 +315,13 @@ def swe_run_noalloc(nx, ny, dx, dy, H, W_a, W_b, pitch, nsteps, precision=64, g=
     _check(load().swe_run_noalloc(C.byref(grid), C.byref(params), C.c_void_p(int(H)), wa, wb,
                                   int(pitch), int(nsteps), dts.ctypes.data), "swe_run_noalloc")
     return dts[: int(nsteps)]
+
+
+def swe_selftest_wait(budget_cycles) -> int:
+    """Run the step kernel's bounded device wait on a barrier nothing arrives
+    on (see swe.h); returns the status, SWE_ERR_TIMEOUT when the wait gave up
+    as designed."""
+    return int(load().swe_selftest_wait(int(budget_cycles)))
 
 
 def swe_destroy(s: State):

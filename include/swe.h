@@ -290,6 +290,20 @@ swe_status swe_run_noalloc(const swe_grid *grid, const swe_params *params,
                            const void *H, void *const *W_a, void *const *W_b,
                            int32_t pitch, int64_t nsteps, double *dts_out);
 
+/* Failure-detection self test of the step kernel's bounded device wait.
+ * The one-layer step kernel waits on an mbarrier for each row staged into
+ * shared memory; if the copy never lands, the wait gives up after a budget
+ * of SM clock cycles (about two seconds in the step kernel) and the step
+ * reports SWE_ERR_TIMEOUT instead of hanging.  This call runs that same
+ * bounded wait, on the current device, in a one-warp kernel on a barrier that
+ * nothing ever arrives on, with the given budget.
+ *  budget_cycles  1 <= budget_cycles <= 4e9 (SM clock cycles)
+ * Returns SWE_ERR_TIMEOUT when the wait gave up as designed (the expected
+ * outcome; the CUDA context stays usable), SWE_OK if the barrier completed
+ * (never expected), SWE_ERR_ARG, SWE_ERR_OOM or SWE_ERR_CUDA.  Allocates and
+ * frees one word of device memory; synchronises the device. */
+swe_status swe_selftest_wait(int64_t budget_cycles);
+
 /* Release every resource of the handle.  NULL is accepted. */
 void swe_destroy(swe_state *s);
 

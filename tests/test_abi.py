@@ -139,3 +139,8 @@ def test_noalloc_rejects_bad_arguments_before_touching_the_gpu(lib):
         S.swe_run_noalloc(64, 40, 1.0, 1.0, fake[0], fake[1:5], fake[5:9], S.noalloc_pitch(64), 3,
                           precision=16)
     assert e.value.status == S.SWE_ERR_ARG
+
+
+def test_wait_selftest_rejects_bad_budgets_before_touching_the_gpu(lib):
+    for budget in (0, -5, 4_000_000_001):
+        assert S.swe_selftest_wait(budget) == S.SWE_ERR_ARG

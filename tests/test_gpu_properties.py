@@ -1,6 +1,8 @@
 """Properties the scheme guarantees at any size, checked on the CUDA path
 (through the C ABI), including full-size grids in the launch configuration
 the bench times, plus the API's restart, history, stream and error paths."""
+import time
+
 import numpy as np
 import pytest
 
@@ -201,3 +203,18 @@ def test_fullsize_hills2048_one_step(precision):
     errs = rel_errors([w.astype(np.float64) for w in W1], Wo1)
     for k in ("h", "qx", "qy", "hC"):
         assert errs[k] <= TOL[precision][k], errs
+
+
+def test_bounded_device_wait_gives_up_and_the_context_survives():
+    """Failure detection without a GPU fault: the step kernel's bounded
+    mbarrier wait, run on a barrier nothing arrives on, gives up after its
+    budget and reports SWE_ERR_TIMEOUT; the context then runs steps as
+    before."""
+    t0 = time.perf_counter()
+    assert S.swe_selftest_wait(20_000_000) == S.SWE_ERR_TIMEOUT  # ~10 ms of SM clock
+    assert time.perf_counter() - t0 < 10.0
+    d = I.make_workload("dam128", nx=48, ny=40)
+    W, dts, _ = gpu_run(d, 64, 5)
+    Wo, dto = oracle_run(d, 64, 5)
+    assert max(rel_errors(W, Wo).values()) <= TOL[64]["h"]
+    assert np.abs(dts / dto - 1).max() <= TOL[64]["dt"]

@@ -610,6 +610,11 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   // index arithmetic inside the kernels is 32-bit per row and column
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
+  // two layers: one block per tile row in the grid's y dimension (<= 65535)
+  if (params->n_layers == 2) {
+    const int64_t ty = params->precision == 32 ? Tile2Y<float>::v : Tile2Y<double>::v;
+    if (((int64_t)grid->ny + ty - 1) / ty > 65535) return SWE_ERR_ARG;
+  }
 
   swe_state* s = new (std::nothrow) swe_state();
   if (!s) return SWE_ERR_OOM;

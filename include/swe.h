@@ -121,15 +121,18 @@ typedef struct swe_state swe_state;
 
 /* Create a simulation on a Cartesian grid ([P1] Algorithm 1, before the time
  * loop: mesh construction and initial state).
- *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite
+ *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite;
+ *          nx <= 2^30, ny <= 2^30 - 8; two layers also ny <= 524280 (fp32)
+ *          or 262140 (fp64): 65535 tiles of 8 (fp32) or 4 (fp64) rows
  *  H       host, nx*ny values: bottom depth below the reference level
  *  W0      host, array of 4 pointers (h, qx, qy, hC), or 6 (h1, q1x, q1y,
  *          h2, q2x, q2y) for two layers, nx*ny values each; depths > 0
  *  params  see swe_params
  *  out     receives the handle (NULL on failure)
  * Allocates the device state (9 padded fields of the chosen precision for one
- * layer, 13 for two), copies H and W0 to the device and checks the state
- * there (one layer: also dt_0).
+ * layer: two buffers of the 4 fields and H; 25 for two: two buffers of the 6
+ * fields and of their residuals, and H), copies H and W0 to the device and
+ * checks the state there (one layer: also dt_0).
  * Errors: SWE_ERR_ARG (bad argument, h <= 0 or non-finite input),
  * SWE_ERR_UNSUPPORTED, SWE_ERR_OOM, SWE_ERR_CUDA. */
 swe_status swe_create_grid(const swe_grid *grid, const void *H,

@@ -144,3 +144,17 @@ def test_noalloc_rejects_bad_arguments_before_touching_the_gpu(lib):
 def test_wait_selftest_rejects_bad_budgets_before_touching_the_gpu(lib):
     for budget in (0, -5, 4_000_000_001):
         assert S.swe_selftest_wait(budget) == S.SWE_ERR_ARG
+
+
+@pytest.mark.parametrize("precision,ny_ok", [(32, 524280), (64, 262140)])
+def test_two_layer_grid_height_limit(lib, precision, ny_ok):
+    # the tile kernels put one block per tile row in the launch's y dimension
+    # (at most 65535): one row more is refused before any CUDA call
+    dt = np.float32 if precision == 32 else np.float64
+    n = ny_ok + 1
+    H = np.full(n, 10.0, dt)
+    W = [np.full(n, v, dt) for v in (6.0, 0.0, 0.0, 4.0, 0.0, 0.0)]
+    with pytest.raises(S.SweError) as e:
+        S.swe_create_grid(1, n, 10.0, 10.0, H, W, precision=precision, n_layers=2,
+                          pollutant=0, r=0.98)
+    assert e.value.status == S.SWE_ERR_ARG

@@ -112,6 +112,41 @@ def test_user_stream():
         assert np.array_equal(x, y.astype(np.float64))
 
 
+@pytest.mark.parametrize("kind", ["grid2", "mesh2", "mesh1"])
+def test_user_stream_two_layers_and_meshes(kind):
+    """The fused two-layer passes and the mesh passes (chained by
+    programmatic dependent launch) on a caller's stream give the default
+    stream's results bit for bit, also with work queued on the stream ahead
+    of them."""
+    import torch
+    from gpu_util import gpu_create2, gpu_create_mesh
+    if kind == "grid2":
+        d = I.two_layer_hills(70, 44, umax=0.05, bump=0.5)
+        make = lambda st: gpu_create2(d, 32, stream=st)
+    elif kind == "mesh2":
+        d = I.tri_workload(20, sigma_scale=0.05, bump=1.0)
+        make = lambda st: gpu_create_mesh(d, 32, stream=st)
+    else:
+        d = I.tri_workload1(24, 18, seed=3)
+        make = lambda st: gpu_create_mesh(d, 64, stream=st)
+    a = make(None)
+    S.swe_run(a, 25)
+    ref, ta = S.swe_get_state(a)
+    stream = torch.cuda.Stream()
+    b = make(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        x = torch.ones(1 << 22, device="cuda")
+        for _ in range(20):   # keep the stream busy when the steps are queued
+            x = x * 1.0000001
+    S.swe_run(b, 25)
+    W, tb = S.swe_get_state(b)
+    for u, v in zip(ref, W):
+        assert np.array_equal(u, v)
+    assert ta == tb
+    S.swe_destroy(a)
+    S.swe_destroy(b)
+
+
 def test_pinned_torch_buffers():
     import torch
     d = I.make_workload("pulses8192", nx=190, ny=70)

@@ -223,13 +223,20 @@ __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Ar
   block_max_publish<T, TX * TY / 32>(m, A.tmax_out);
 }
 
+// Resident blocks per SM the registers are held to: five 256-thread fp32
+// tiles (48 registers) fit next to their 35 KB of shared memory each; fp64
+// tiles are bounded by shared memory and the FP64 pipe.
+template <typename T> struct MinBlocks2 { static constexpr int v = 1; };
+template <> struct MinBlocks2<float> { static constexpr int v = 5; };
+
 template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v) cart2_flux_kernel(const Step2Args<T> A) {
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T>::v)
+    cart2_flux_kernel(const Step2Args<T> A) {
   flux_tile<T, ANISO, false>(A, Update2Args<T>{});
 }
 
 template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v)
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T>::v)
     cart2_step_kernel(const Step2Args<T> A, const Update2Args<T> U) {
   flux_tile<T, ANISO, true>(A, U);
 }

@@ -209,7 +209,6 @@ struct QuarticP {
     const float2 dp = mul2(s2(2.f), fma2(d1, q2, mul2(d2, q1)));
     return mul2(p, rcp2(dp));
   }
-  __device__ __forceinline__ float2 newton(float2 l) const { return sub2(l, step(l)); }
 };
 
 // Flux of two edges at once; walls per component.  Returns false if either
@@ -261,10 +260,12 @@ __device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g
   const float2 sd = sqrt2(max2(disc, s2(0.f)));
   float2 l2 = mul2(s2(0.5f), sub2(f2(-bb.x, -bb.y), sd));
   float2 l3 = mul2(s2(0.5f), sub2(sd, bb));
+  const float2 lim = mul2(s2(0.5f), sd);  // steps clamped as in edge2
+  const float2 nlim = f2(-lim.x, -lim.y);
 #pragma unroll
   for (int it = 0; it < Iters<float>::inner; ++it) {
-    l2 = q.newton(l2);
-    l3 = q.newton(l3);
+    l2 = sub2(l2, min2(max2(q.step(l2), nlim), lim));
+    l3 = sub2(l3, min2(max2(q.step(l3), nlim), lim));
   }
   // fluctuation d (pressure differences written g hbar_k dh_k)
   const float2 dh1 = sub2(b.h[0], a.h[0]), dh2 = sub2(b.h[1], a.h[1]), dH = sub2(b.H, a.H);

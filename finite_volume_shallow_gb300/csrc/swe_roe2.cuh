@@ -74,14 +74,16 @@ template <> struct M2<double> {  // Newton-refined reciprocal (swe_fastmath.cuh)
 // against extended-precision roots over depths 0.1-10 m, layer velocities up
 // to 3 m/s and r from 0.001 to 0.98, 9 iterations reach fp32 rounding and 11
 // fp64 rounding.  (At r = 0 with u1 + c1 = u2 + c2 the root is double and the
-// eigenvector basis of A_ij degenerates.)
+// eigenvector basis of A_ij degenerates.)  The inner pair, deflated from
+// converged outer roots, reaches the type's rounding after one Newton step
+// in fp64 (same check); `inner` keeps one more.
 template <typename T> struct Iters;
 template <> struct Iters<float> {
   static constexpr int outer = 10, inner = 2;
   static constexpr float tol = 2.44140625e-4f;  // 2^-12
 };
 template <> struct Iters<double> {
-  static constexpr int outer = 12, inner = 3;
+  static constexpr int outer = 12, inner = 2;
   static constexpr double tol = 1.4901161193847656e-8;  // 2^-26
 };
 
@@ -162,10 +164,14 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   const bool hyper = disc > T(0);
   const T sd = M2<T>::sqa(hyper ? disc : T(0));
   T l2 = T(0.5) * (-bb - sd), l3 = T(0.5) * (-bb + sd);
+  // each step at most half the pair's separation: near a double inner root
+  // p' vanishes and an unclamped step can jump past the other root (or be
+  // 0/0); the clamp also keeps a non-finite step finite
+  const T lim = T(0.5) * sd;
 #pragma unroll
   for (int it = 0; it < Iters<T>::inner; ++it) {
-    l2 -= q.p(l2) * M2<T>::rcp(q.dp(l2));
-    l3 -= q.p(l3) * M2<T>::rcp(q.dp(l3));
+    l2 -= fmin(fmax(q.p(l2) * M2<T>::rcp(q.dp(l2)), -lim), lim);
+    l3 -= fmin(fmax(q.p(l3) * M2<T>::rcp(q.dp(l3)), -lim), lim);
   }
   // fluctuation d = F_1(W_j) - F_1(W_i) - B_ij (W_j - W_i) - S_ij (H_j - H_i)
   // (pressure differences written g hbar_k (h_k,j - h_k,i))

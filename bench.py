@@ -52,8 +52,8 @@ BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC writt
 # per inner one.  The outer iteration stops once every edge of the warp has
 # converged: on the interface dam break and the triangle workload it takes
 # 2.01 iterations per edge in fp32 and 3.01 in fp64 (counted on the GPU with
-# an instrumented build); the inner one runs 2 (fp32) or 3 (fp64).
-FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2, 64: 213 + 28 * 3.01 + 28 * 3}
+# an instrumented build); the inner one runs 2.
+FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2, 64: 213 + 28 * 3.01 + 28 * 2}
 # Per cell-update on a grid: two edges (each edge once; the tiles' halo
 # recomputation not counted) plus 25 for the per-cell quantities and the
 # residual sums.
@@ -95,7 +95,7 @@ def source_hash(files):
 # for the rotations into and out of the edge frame, the fluctuation terms and
 # the edge-length scaling; one layer 88.
 FLOPS_PER_EDGE_MESH = {(2, 32): 213 + 28 * 2.0 + 28 * 2 + 79,
-                       (2, 64): 213 + 28 * 3.0 + 28 * 3 + 79, (1, 32): 88, (1, 64): 88}
+                       (2, 64): 213 + 28 * 3.0 + 28 * 2 + 79, (1, 32): 88, (1, 64): 88}
 # One layer on a grid: floating-point operations per cell-update of the
 # fused step, counted from its formulas (FMA = 2; the 10 reciprocals and
 # reciprocal square roots per cell not counted): 36 per edge flux pair in the

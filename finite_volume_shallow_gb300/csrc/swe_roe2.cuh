@@ -65,10 +65,10 @@ template <> struct M2<double> {  // Newton-refined reciprocal (swe_fastmath.cuh)
 };
 
 // Newton iterations: the outer roots converge quadratically from the safe
-// start; the inner ones start from the deflated estimate.  The outer
-// iteration stops once every edge of the warp has taken a step below
-// tol * max(c1, c2) (after that the error is of the order of the type's
-// rounding), after 2 iterations on typical states.  `outer` bounds it: at
+// start; the inner ones start from the deflated estimate.  An edge's outer
+// iteration stops once it has taken a step below tol * max(c1, c2) (after
+// that the error is of the order of the type's rounding), after 2
+// iterations on typical states.  `outer` bounds it: at
 // small density ratios the two largest roots of p sit close together when
 // u1 + c1 ~ u2 + c2, and Newton first converges linearly there; checked
 // against extended-precision roots over depths 0.1-10 m, layer velocities up
@@ -146,13 +146,22 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   T l4 = fmin(fmax(un[0] + kr2 * c1, un[1] + kr2 * c2), fmax(un[0], un[1]) + ks * sc);
   const T tol = Iters<T>::tol * fmax(c1, c2);
   const unsigned act = ADAPT ? __activemask() : 0u;
+  // ADAPT: an edge keeps its roots once its own step fell below tol (so the
+  // result depends on the edge's state alone, not on the warp it shares);
+  // the loop ends when every edge of the warp has
+  bool done = false;
 #pragma unroll
   for (int it = 0; it < Iters<T>::outer; ++it) {
     const T s1 = q.p(l1) * M2<T>::rcp(q.dp(l1));
     const T s4 = q.p(l4) * M2<T>::rcp(q.dp(l4));
-    l1 -= s1;
-    l4 -= s4;
-    if (ADAPT && it >= 1 && __all_sync(act, (fabs(s1) <= tol) & (fabs(s4) <= tol))) break;
+    if (!done) {
+      l1 -= s1;
+      l4 -= s4;
+    }
+    if (ADAPT) {
+      done |= it >= 1 && (fabs(s1) <= tol) & (fabs(s4) <= tol);
+      if (__all_sync(act, done)) break;
+    }
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
   const T p3 = T(-2) * (un[0] + un[1]);

@@ -179,8 +179,11 @@ __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Ar
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ex[q][row][e] = out[q];
   }
-  // y-edges: TY + 1 per column; global row of the lower cell j0 - 1 + e
-  for (int k = t; k < TX * (TY + 1); k += TX * TY) {
+  // y-edges: TY + 1 per column; global row of the lower cell j0 - 1 + e.
+  // The thread index is rotated by one warp, so that the second pass of the
+  // y-edges falls on the last warp, not on the one that took the x-edges'
+  // second pass.
+  for (int k = (t + TX * TY - 32) % (TX * TY); k < TX * (TY + 1); k += TX * TY) {
     const int col = k % TX, e = k / TX;
     const int gl = j0 - 1 + e;
     Side2<T> a = side_of<T, TY>(cq, e, col + 1, false);

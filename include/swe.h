@@ -182,7 +182,9 @@ swe_status swe_step(swe_state *s, double cfl, double *dt_out);
 
 /* Advance nsteps >= 0 steps with params.cfl.  Enqueues all steps on the
  * handle's stream without host synchronisation, then waits once and reports
- * the sticky device error. */
+ * the sticky device error.  On a two-layer grid the update of each step is
+ * applied inside the next step's flux pass (and the last one by a separate
+ * pass); the result equals nsteps calls of swe_step bit for bit. */
 swe_status swe_run(swe_state *s, int64_t nsteps);
 
 /* Copy the current state to the host.  fields_out: array of 4 host pointers
@@ -242,8 +244,10 @@ swe_status swe_cell_index(const swe_state *s, int64_t *idx);
  * times are summed per kernel; while on, swe_run keeps at most 64 steps in
  * flight ahead of the host.  swe_set_timing(s, 0) stops it (the sums stay).
  * swe_get_timing waits for the recorded steps and writes up to max entries
- * (one per kernel of the handle's step, in launch order) to out; *n receives
- * the count.  Errors: SWE_ERR_ARG, SWE_ERR_OOM, SWE_ERR_CUDA. */
+ * (one per kernel the handle's steps launch, in launch order: one for a
+ * one-layer grid; flux pass, fused update-and-flux pass and update for a
+ * two-layer grid; edge, gather and update passes for a mesh) to out; *n
+ * receives the count.  Errors: SWE_ERR_ARG, SWE_ERR_OOM, SWE_ERR_CUDA. */
 typedef struct {
   char name[32];     /* kernel name, NUL-terminated                        */
   int64_t launches;  /* launches timed                                      */

@@ -69,6 +69,8 @@ def lib():
         _lib.om_grid_mesh.argtypes = [i64, i64, d, d, vp, vp, vp, vp, vp, vp]
         _lib.om_flux1.restype = None
         _lib.om_flux1.argtypes = [vp, vp, d, d, d, d, d, vp, vp]
+        _lib.om_set_entropy_fix.restype = None
+        _lib.om_set_entropy_fix.argtypes = [C.c_int]
         _lib.om_wall_ghost1.restype = None
         _lib.om_wall_ghost1.argtypes = [vp, d, d, vp]
         _lib.om_dt1.restype = d
@@ -111,6 +113,22 @@ def lib():
         _lib.om_grid_run1.argtypes = [i64, i64, d, d, vp, vp, d, d, i64, vp, vp,
                                       C.POINTER(C.c_int64)]
     return _lib
+
+
+class entropy_fix:
+    """Context manager: the one-layer flux of the oracle with the
+    Harten-Hyman entropy fix switched on (see om_set_entropy_fix)."""
+
+    def __init__(self, on=True):
+        self.on = bool(on)
+
+    def __enter__(self):
+        lib().om_set_entropy_fix(1 if self.on else 0)
+        return self
+
+    def __exit__(self, *exc):
+        lib().om_set_entropy_fix(0)
+        return False
 
 
 def _ptr(a):

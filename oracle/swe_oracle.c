@@ -66,6 +66,28 @@ void om_grid_mesh(int64_t nx, int64_t ny, double dx, double dy, double *area,
 
 static double sgn(double x) { return (x > 0.0) ? 1.0 : ((x < 0.0) ? -1.0 : 0.0); }
 
+/* Optional entropy fix of the one-layer flux (off unless switched on).
+ * [P1] Sec. 2.2 remarks that an entropy fix of Harten-Hyman type can be
+ * adapted to the scheme but gives no formula; this is the published one:
+ * Harten's regularised absolute value |lambda|_d = |lambda| when
+ * |lambda| >= delta, (lambda^2 + delta^2) / (2 delta) otherwise, with the
+ * Harten-Hyman choice delta_k = max(0, lambda_k - lambda_k(W_i),
+ * lambda_k(W_j) - lambda_k), lambda_k(W) being the eigenvalue of the
+ * physical Jacobian of the state W itself (u_eta -/+ sqrt(g h)).  Adapted to
+ * Phi^- = P^- d + F(W_i) as added numerical viscosity along each wave,
+ * measured on the state jump: Phi^- += 1/2 (|lambda_k| - |lambda_k|_d)
+ * beta_k K_k with beta = K^-1 (W_j - W_i).  With a flat bottom this is the
+ * Roe fluctuation with |lambda| replaced by |lambda|_d; it vanishes wherever
+ * |lambda_k| >= delta_k (so water at rest stays at rest). */
+static int g_entropy_fix = 0;
+void om_set_entropy_fix(int on) { g_entropy_fix = on ? 1 : 0; }
+
+static double harten_abs(double lam, double lamL, double lamR) {
+  double delta = fmax(0.0, fmax(lam - lamL, lamR - lam));
+  double a = fabs(lam);
+  return (a < delta) ? (lam * lam + delta * delta) / (2.0 * delta) : a;
+}
+
 void om_wall_ghost1(const double *Wi, double ex, double ey, double *Wg) {
   /* reflect the discharge about the wall: q - 2 (q . eta) eta */
   double qn = Wi[1] * ex + Wi[2] * ey;
@@ -124,6 +146,18 @@ void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
   /* Phi^- = P^- d + F_1(W_eta,i) */
   double phi[2];
   for (int r = 0; r < 2; ++r) phi[r] = P[r][0] * d[0] + P[r][1] * d[1] + Fi[r];
+  if (g_entropy_fix) {
+    /* the eigenvalues of each side's own Jacobian, u_eta -/+ sqrt(g h) */
+    double uni = qni / hi, unj = qnj / hj;
+    double ci = sqrt(g * hi), cj = sqrt(g * hj);
+    double lamL[2] = {uni - ci, uni + ci}, lamR[2] = {unj - cj, unj + cj};
+    double dW[2] = {hj - hi, qnj - qni};
+    for (int k = 0; k < 2; ++k) {
+      double beta = Kinv[k][0] * dW[0] + Kinv[k][1] * dW[1];
+      double nu = 0.5 * (fabs(lam[k]) - harten_abs(lam[k], lamL[k], lamR[k])) * beta;
+      for (int r = 0; r < 2; ++r) phi[r] += nu * K[r][k];
+    }
+  }
 
   /* Step 3: tangential discharge and pollutant as passive scalars carried
    * by the mass flux, upwinded on its sign. */

@@ -17,6 +17,12 @@ SRC = os.path.join(ROOT, "oracle", "swe_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "swe_oracle.h")
 
 MUTANTS = {
+    # the entropy fix: anti-diffusion, delta from the wrong sides, beta from
+    # the jump with its components swapped
+    "efix_sign": ("0.5 * (fabs(lam[k]) - harten_abs(lam[k], lamL[k], lamR[k])) * beta",
+                  "0.5 * (harten_abs(lam[k], lamL[k], lamR[k]) - fabs(lam[k])) * beta"),
+    "efix_delta": ("fmax(lam - lamL, lamR - lam)", "fmax(lamL - lam, lam - lamR)"),
+    "efix_beta": ("Kinv[k][0] * dW[0] + Kinv[k][1] * dW[1]", "Kinv[k][0] * dW[1] + Kinv[k][1] * dW[0]"),
     # bathymetry source with the wrong sign
     "source_sign": ("- g * hbar * (Hj - Hi)", "+ g * hbar * (Hj - Hi)"),
     # source term dropped

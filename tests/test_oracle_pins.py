@@ -357,3 +357,74 @@ def test_update_at_selected_cells_equals_full_update():
     sel = O.update1_at(m, d["H"], W0, G, dt, cells)
     for k in range(4):
         assert np.array_equal(sel[k], Wf[k][cells])
+
+
+# ---- the Harten-Hyman entropy fix (switched on with O.entropy_fix) ----------
+def _transonic_dam(nx, fix, T=20.0, hl=10.0, hr=0.5):
+    d = I.dam_break_1d(nx, h_left=hl, h_right=hr)
+    mesh = O.grid_mesh(nx, 4, d["dx"], d["dy"])
+    W = [d["h"], d["qx"], d["qy"], d["hC"]]
+    t = 0.0
+    with O.entropy_fix(fix):
+        while t < T:
+            W, dts, st, _ = O.run1(mesh, d["H"], W, G, 0.9, 1)
+            assert st == O.OM_OK
+            t += dts[0]
+    x = (np.arange(nx) + 0.5) * d["dx"]
+    ha, _ = stoker.solution(x, t, 1000.0, hl, hr, G)
+    err = np.abs(W[0].reshape(4, nx)[0] - ha)
+    return np.sum(err) * d["dx"], float(err[np.abs(x - 1000.0) < 60.0].max())
+
+
+def test_entropy_fix_removes_the_transonic_glitch():
+    # h_r / h_l = 0.05: the middle state is supercritical (u_m > c_m), so the
+    # rarefaction fan contains the sonic point at the dam.  Roe's scheme alone
+    # keeps an entropy-violating jump there that does not shrink under
+    # refinement; with the fix the solution converges to Stoker's at first
+    # order, near the dam too.
+    hm, um, _ = stoker.middle_state(10.0, 0.5, G)
+    assert um > math.sqrt(G * hm)
+    plain = [_transonic_dam(nx, False) for nx in (200, 400, 800, 1600)]
+    fixed = [_transonic_dam(nx, True) for nx in (200, 400, 800, 1600)]
+    assert all(near >= 0.6 for _, near in plain), plain
+    l1 = [e for e, _ in fixed]
+    near = [n for _, n in fixed]
+    assert all(l1[k] / l1[k + 1] >= 1.5 for k in range(3)), fixed
+    assert all(near[k] / near[k + 1] >= 1.4 for k in range(3)), fixed
+    assert l1[-1] < 0.6 * plain[-1][0]
+
+
+def test_entropy_fix_leaves_subcritical_flow_and_rest_alone():
+    # the fix acts only where |lambda_k| < delta_k, i.e. at sonic points: the
+    # subcritical Stoker problem is unchanged to the last bit and water at rest
+    # over hills stays at rest
+    d = I.dam_break_1d(400)
+    mesh = O.grid_mesh(400, 4, d["dx"], d["dy"])
+    W0 = [d["h"], d["qx"], d["qy"], d["hC"]]
+    Wa, dta, _, _ = O.run1(mesh, d["H"], W0, G, 0.9, 300)
+    with O.entropy_fix():
+        Wb, dtb, _, _ = O.run1(mesh, d["H"], W0, G, 0.9, 300)
+    assert all(np.array_equal(a, b) for a, b in zip(Wa, Wb))
+    assert np.array_equal(dta, dtb)
+    dl = I.make_workload("hills2048", nx=48, ny=40, lake_at_rest=True)
+    W0 = I.fields_of(dl)
+    with O.entropy_fix():
+        W, _, st = O.grid_run1(dl["nx"], dl["ny"], dl["dx"], dl["dy"], dl["H"], W0, G, 0.9, 100)
+    assert st == O.OM_OK
+    for a, b in zip(W, W0):
+        assert np.abs(a - b).max() <= 1e-13 * max(np.abs(b).max(), 1.0)
+
+
+def test_entropy_fix_conserves_mass_and_pollutant():
+    # a strong radial dam break (sonic points all round the dam) with the fix
+    d = I.circular_dam(64, 64, radius=12.0, h_in=10.0, h_out=0.5)
+    mesh = O.grid_mesh(64, 64, 1.0, 1.0)
+    W0 = I.fields_of(d)
+    with O.entropy_fix():
+        W, _, st, _ = O.run1(mesh, d["H"], W0, G, 0.9, 60)
+    assert st == O.OM_OK
+    for k in (0, 3):
+        assert abs(W[k].sum() - W0[k].sum()) <= 1e-12 * W0[k].sum()
+    # and it changed the flow (sonic points were crossed)
+    Wp, _, _, _ = O.run1(mesh, d["H"], W0, G, 0.9, 60)
+    assert np.abs(W[0] - Wp[0]).max() > 1e-3

@@ -3,7 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload pulses8192|hills2048|dam128|interface2048|tri1024]
-                    [--precision 32|64]
+                    [--precision 32|64] [--entropy-fix]
 
 One "step" is one explicit time step of the IR-Roe scheme over the whole
 domain: edge fluxes with the bathymetry source, per-cell accumulation, the
@@ -116,6 +116,7 @@ DESCR = {
                "vertices jittered by +-0.2, cells shuffled then RCM-reordered, r=0.98, "
                "8 Gaussian hills, 0.5 m interface bump, at rest, reflective walls",
 }
+TWO_LAYER_WORKLOADS = ("interface2048", "tri1024")
 
 
 def kernel_model(kernel, precision, nl, n_cells, n_edges):
@@ -195,6 +196,10 @@ class Sample:
                          f"walled {nx}x{rows} grid")
 
     def run(self, O, nsteps, W=None):
+        with O.entropy_fix(self.d.get("entropy_fix", 0)):
+            return self._run(O, nsteps, W)
+
+    def _run(self, O, nsteps, W=None):
         d = self.d
         W = self.W if W is None else W
         if d.get("mesh"):
@@ -228,6 +233,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--nx", type=int, default=None, help="reduced grid (same recipe)")
     p.add_argument("--ny", type=int, default=None)
+    p.add_argument("--entropy-fix", action="store_true",
+                   help="one layer: the Harten-Hyman entropy fix of the flux")
     p.add_argument("--no-clocks", action="store_true",
                    help="skip the nvidia-smi clock window (profiling runs)")
     a = p.parse_args()
@@ -235,7 +242,23 @@ def parse():
         p.error("--warmup must be at least 3")
     if a.steps < 1:
         p.error("--steps must be at least 1")
+    if a.entropy_fix and a.workload in TWO_LAYER_WORKLOADS:
+        p.error("--entropy-fix applies to one-layer workloads only")
     return a
+
+
+def workload_of(I, args):
+    d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
+    if args.entropy_fix:
+        d["entropy_fix"] = 1
+    return d
+
+
+def workload_name(args, d, precision):
+    s = f"{args.workload}: {DESCR[args.workload]}, fp{precision}"
+    if d.get("entropy_fix"):
+        s += ", Harten-Hyman entropy fix"
+    return s
 
 
 def max_over_ranks(x, world):
@@ -389,7 +412,7 @@ def run_reference(args, rank, world):
     import oracle as O
     from finite_volume_shallow_gb300 import inputs as I
 
-    d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
+    d = workload_of(I, args)
     precision = args.precision or d["precision"]
     per_cell = calibrate(O, I, d, 16 * (d.get("nx") or 1024) if not d.get("mesh") else 16384)
     budget = 150.0
@@ -406,7 +429,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}",
+        "config": {"workload": workload_name(args, d, precision),
                    "cells": n_cells_of(d), "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -439,7 +462,7 @@ def main():
             torch.distributed.barrier()
 
     S.load()
-    d = I.make_workload(args.workload, nx=args.nx, ny=args.ny)
+    d = workload_of(I, args)
     precision = args.precision or d["precision"]
     npdt = np.float32 if precision == 32 else np.float64
     tdt = torch.float32 if precision == 32 else torch.float64
@@ -452,12 +475,14 @@ def main():
         st = S.swe_create_mesh(d["xy"], d["tri"], d["H"].astype(npdt), fields,
                                precision=precision, g=d["g"], cfl=d["cfl"],
                                stream=stream.cuda_stream, n_layers=nl,
-                               pollutant=0 if two else 1, r=d.get("r", 0.0), reorder=1)
+                               pollutant=0 if two else 1, r=d.get("r", 0.0), reorder=1,
+                               entropy_fix=d.get("entropy_fix", 0))
     else:
         st = S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(npdt), fields,
                                precision=precision, g=d["g"], cfl=d["cfl"],
                                stream=stream.cuda_stream, n_layers=nl,
-                               pollutant=0 if two else 1, r=d.get("r", 0.0))
+                               pollutant=0 if two else 1, r=d.get("r", 0.0),
+                               entropy_fix=d.get("entropy_fix", 0))
     info = S.swe_get_info(st)
 
     # warm-up (also gives a step-time estimate for the busy window below)
@@ -548,7 +573,9 @@ def main():
                               "timing": "CUDA events between the kernels of each of K "
                                         "further steps, right after the timed region",
                               "share": kms / max(sum(v[1] for v in ktimes.values()), 1e-30),
-                              "traffic": traffic_per_launch(name, precision, args.workload)})
+                              "traffic": traffic_per_launch(
+                                  name, precision,
+                                  args.workload + ("_efix" if d.get("entropy_fix") else ""))})
     dominant = max(ktimes, key=lambda k: ktimes[k][1])
     roof = dict(kernels[dominant])
     roof["other_kernels"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "unit", "frac",
@@ -565,7 +592,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_NAME[precision], "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}, fp{precision}"
+            "config": {"workload": workload_name(args, d, precision)
                                    + (f", reduced to {args.nx or d.get('nx')}x"
                                       f"{args.ny or d.get('ny')}" if args.nx or args.ny
                                       else ""),

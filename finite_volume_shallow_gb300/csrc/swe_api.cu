@@ -117,7 +117,7 @@ template <typename T>
 swe_status plan_launch(swe_state* s) {
   int bpsm = 0;
   size_t smem = 0;
-  CK(step_occupancy<T>(&bpsm, &smem));
+  CK(step_occupancy<T>(&bpsm, &smem, s->p.entropy_fix != 0));
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -170,6 +170,7 @@ swe_status enqueue_step(swe_state* s, double cfl) {
   a.t_dev = s->t_dev;
   a.step = s->step;
   a.err = s->err;
+  a.efix = s->p.entropy_fix;
   if (s->marks) CK(cudaEventRecord(s->marks[0], s->stream));
   CK(launch_step<T>(a, s->blocks, s->stream));
   if (s->marks) CK(cudaEventRecord(s->marks[1], s->stream));
@@ -323,6 +324,7 @@ swe_status enqueue_mesh_step(swe_state* s, double cfl) {
   f.r = (T)s->p.r;
   f.tmax_out = sl + (s->step % 3) * sizeof(uint64_t);
   f.err = u.err = s->err;
+  f.efix = s->p.entropy_fix;
   u.two_cfl = 2.0 * cfl;
   u.tmax_in = sl + (s->step % 3) * sizeof(uint64_t);
   u.tmax_clear = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
@@ -502,9 +504,11 @@ swe_status check_params(const swe_params* params) {
   if (!(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
   if (params->n_layers != 1 && params->n_layers != 2) return SWE_ERR_ARG;
   if (params->n_layers == 1 && params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->entropy_fix != 0 && params->entropy_fix != 1) return SWE_ERR_ARG;
   if (params->n_layers == 2) {
     if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
     if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
+    if (params->entropy_fix) return SWE_ERR_UNSUPPORTED;
   }
   return SWE_OK;
 }

@@ -214,10 +214,11 @@ __device__ __forceinline__ Pr<T> lds_pair(const unsigned char* p) {
 // ---------------------------------------------------------------------------
 // Two edges (one per component) seen in the frame of their normals eta:
 // depth h, s = sqrt(h), v = q_eta / sqrt(h), normal discharge q_eta,
-// qu = q_eta^2 / h, tangential velocity ut, concentration C, bottom H.
+// qu = q_eta^2 / h, tangential velocity ut, concentration C, bottom H, and
+// (read by the entropy fix only) the normal velocity u = q_eta / h.
 template <typename T>
 struct SideP {
-  Pr<T> h, s, v, qn, qu, ut, C, H;
+  Pr<T> h, s, v, qn, qu, ut, C, H, u;
 };
 // Reflective wall: the ghost is the cell with its normal discharge negated.
 template <typename T>
@@ -225,6 +226,7 @@ __device__ __forceinline__ SideP<T> mirror(const SideP<T>& a) {
   SideP<T> m = a;
   m.v = pneg(a.v);
   m.qn = pneg(a.qn);
+  m.u = pneg(a.u);
   return m;
 }
 // the same, for one component only (k = 0: .x, 1: .y)
@@ -233,9 +235,11 @@ __device__ __forceinline__ void mirror_into(SideP<T>& dst, const SideP<T>& src, 
   if (k == 0) {
     dst.h.x = src.h.x; dst.s.x = src.s.x; dst.v.x = -src.v.x; dst.qn.x = -src.qn.x;
     dst.qu.x = src.qu.x; dst.ut.x = src.ut.x; dst.C.x = src.C.x; dst.H.x = src.H.x;
+    dst.u.x = -src.u.x;
   } else {
     dst.h.y = src.h.y; dst.s.y = src.s.y; dst.v.y = -src.v.y; dst.qn.y = -src.qn.y;
     dst.qu.y = src.qu.y; dst.ut.y = src.ut.y; dst.C.y = src.C.y; dst.H.y = src.H.y;
+    dst.u.y = -src.u.y;
   }
 }
 
@@ -263,8 +267,31 @@ __device__ __forceinline__ T sgn_weight(T l) {  // (1 - sgn l) / 2, sgn 0 = 0
 template <typename T>
 struct RoeHead {
   Pr<T> l1, l2, d0, d1n, a1, i2c;
+  Pr<T> del1, del2;  // entropy fix: Harten-Hyman delta of each wave
 };
+// Entropy fix (EFIX; [P1] Sec. 2.2 remarks that a Harten-Hyman fix can be
+// adapted, without a formula): Harten's regularised |l|_d = |l| when
+// |l| >= delta, (l^2 + delta^2) / (2 delta) otherwise, with delta_k =
+// max(0, l_k - l_k(W_a), l_k(W_b) - l_k), l_k(W) = u_eta -/+ sqrt(g h) of the
+// state itself; it adds 1/2 (|l_k| - |l_k|_d) beta_k K_k to Phi^-, with
+// beta = K^-1 (W_b - W_a).  Zero wherever |l_k| >= delta_k.
 template <typename T>
+__device__ __forceinline__ T hh_delta(T l, T lL, T lR) {
+  return fmax(T(0), fmax(l - lL, lR - l));
+}
+template <typename T>
+__device__ __forceinline__ bool no_fix(const RoeHead<T>& e) {
+  return (fabs(e.l1.x) >= e.del1.x) & (fabs(e.l1.y) >= e.del1.y) &
+         (fabs(e.l2.x) >= e.del2.x) & (fabs(e.l2.y) >= e.del2.y);
+}
+// 1/2 (|l| - |l|_d) for one edge (0 where the fix is not active)
+template <typename T>
+__device__ __forceinline__ T hh_visc(T l, T del) {
+  const T a = fabs(l);
+  if (!(a < del)) return T(0);
+  return T(0.5) * (a - (l * l + del * del) * Fm<T>::rcp(del + del));
+}
+template <typename T, bool EFIX = false>
 __device__ __forceinline__ RoeHead<T> roe_head(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
   using P = Pr<T>;
   RoeHead<T> e;
@@ -278,6 +305,15 @@ __device__ __forceinline__ RoeHead<T> roe_head(const SideP<T>& a, const SideP<T>
   e.d0 = psub(b.qn, a.qn);
   e.d1n = pfma(c2, psub(psub(b.H, a.H), psub(b.h, a.h)), psub(a.qu, b.qu));
   e.a1 = pmul(pfma(e.l2, e.d0, e.d1n), e.i2c);
+  if (EFIX) {
+    // sqrt(g h) of each side: sqrt(2 gh) s
+    const T sg = sqrt(T(2) * gh.x);
+    const P ca = pmul(psplat<T>(sg), a.s), cb = pmul(psplat<T>(sg), b.s);
+    const P lL1 = psub(a.u, ca), lR1 = psub(b.u, cb);
+    const P lL2 = padd(a.u, ca), lR2 = padd(b.u, cb);
+    e.del1 = pr(hh_delta(e.l1.x, lL1.x, lR1.x), hh_delta(e.l1.y, lL1.y, lR1.y));
+    e.del2 = pr(hh_delta(e.l2.x, lL2.x, lR2.x), hh_delta(e.l2.y, lL2.y, lR2.y));
+  }
   return e;
 }
 template <typename T>
@@ -288,7 +324,7 @@ __device__ __forceinline__ bool subcritical(const RoeHead<T>& e) {
 // `fast` (every edge of the warp has l1 < 0 < l2) takes w = (1, 0), which is
 // the general branch bit for bit.  Then the passive upwinding of the
 // tangential velocity and of the concentration.
-template <typename T>
+template <typename T, bool EFIX = false>
 __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>& a,
                                              const SideP<T>& b, bool fast) {
   using P = Pr<T>;
@@ -302,6 +338,16 @@ __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>
     const P b2n = pmul(pr(sgn_weight(e.l2.x), sgn_weight(e.l2.y)), a2n);
     f.m = psub(padd(a.qn, b1), b2n);
     f.pm = psub(pmul(b1, e.l1), pmul(b2n, e.l2));
+    if (EFIX) {
+      // beta = K^-1 (W_b - W_a): (l2 dh - dq, dq - l1 dh) / (2c)
+      const P dh = psub(b.h, a.h);
+      const P be1 = pmul(psub(pmul(e.l2, dh), e.d0), e.i2c);
+      const P be2 = pmul(psub(e.d0, pmul(e.l1, dh)), e.i2c);
+      const P n1 = pmul(pr(hh_visc(e.l1.x, e.del1.x), hh_visc(e.l1.y, e.del1.y)), be1);
+      const P n2 = pmul(pr(hh_visc(e.l2.x, e.del2.x), hh_visc(e.l2.y, e.del2.y)), be2);
+      f.m = padd(f.m, padd(n1, n2));
+      f.pm = padd(f.pm, padd(pmul(n1, e.l1), pmul(n2, e.l2)));
+    }
   }
   f.dsum = padd(e.d1n, f.pm);
   const P ut = pr(f.m.x > T(0) ? a.ut.x : b.ut.x, f.m.y > T(0) ? a.ut.y : b.ut.y);
@@ -310,21 +356,25 @@ __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>
   f.c = pmul(f.m, cc);
   return f;
 }
-template <typename T>
+template <typename T, bool EFIX = false>
 __device__ __forceinline__ FluxP<T> roe_pair(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
-  const RoeHead<T> e = roe_head<T>(a, b, gh);
-  return roe_tail<T>(e, a, b, __all_sync(kFull, subcritical(e)));
+  const RoeHead<T> e = roe_head<T, EFIX>(a, b, gh);
+  bool ok = subcritical(e);
+  if (EFIX) ok &= no_fix(e);
+  return roe_tail<T, EFIX>(e, a, b, __all_sync(kFull, ok));
 }
 // Two pairs at once (the x-edges and the y-edges of a row), one vote.
-template <typename T>
+template <typename T, bool EFIX = false>
 __device__ __forceinline__ void roe_two(const SideP<T>& ax, const SideP<T>& bx,
                                         const SideP<T>& ay, const SideP<T>& by, Pr<T> gh,
                                         FluxP<T>& fx, FluxP<T>& fy) {
-  const RoeHead<T> ex = roe_head<T>(ax, bx, gh);
-  const RoeHead<T> ey = roe_head<T>(ay, by, gh);
-  const bool fast = __all_sync(kFull, subcritical(ex) & subcritical(ey));
-  fx = roe_tail<T>(ex, ax, bx, fast);
-  fy = roe_tail<T>(ey, ay, by, fast);
+  const RoeHead<T> ex = roe_head<T, EFIX>(ax, bx, gh);
+  const RoeHead<T> ey = roe_head<T, EFIX>(ay, by, gh);
+  bool ok = subcritical(ex) & subcritical(ey);
+  if (EFIX) ok &= no_fix(ex) & no_fix(ey);
+  const bool fast = __all_sync(kFull, ok);
+  fx = roe_tail<T, EFIX>(ex, ax, bx, fast);
+  fy = roe_tail<T, EFIX>(ey, ay, by, fast);
 }
 
 // ||D_ij||_inf = |u_eta| + c of the Roe matrix of an edge (eq. (5)); the
@@ -387,11 +437,11 @@ struct RowW {
 
 template <typename T>
 __device__ __forceinline__ SideP<T> side_x(const RowN<T>& q) {
-  return SideP<T>{q.h, q.s, q.vx, q.qx, q.qux, q.uy, q.C, q.H};
+  return SideP<T>{q.h, q.s, q.vx, q.qx, q.qux, q.uy, q.C, q.H, q.ux};
 }
 template <typename T>
 __device__ __forceinline__ SideP<T> side_y(const RowN<T>& q) {
-  return SideP<T>{q.h, q.s, q.vy, q.qy, q.quy, q.ux, q.C, q.H};
+  return SideP<T>{q.h, q.s, q.vy, q.qy, q.quy, q.ux, q.C, q.H, q.uy};
 }
 
 // Everything a warp keeps while it marches.
@@ -433,10 +483,11 @@ __device__ __forceinline__ void issue_stage(const Ctx<T>& c, int s) {
 
 // x-edges of a row: edge pair (cell0|cell1, cell1|next lane's cell0).
 // Vertical walls (WALLX bands) take the mirror state; w0/w1 mark them.
-template <typename T, bool WALLX>
+template <typename T, bool WALLX, bool EFIX>
 __device__ __forceinline__ void xsides(const Ctx<T>& c, const RowN<T>& q, SideP<T>& a,
                                        SideP<T>& b, bool& w0, bool& w1) {
   a = side_x(q);
+  b.u = EFIX ? pr(q.ux.y, shdn(q.ux.x)) : a.u;
   b.h = pr(q.h.y, shdn(q.h.x));
   b.s = pr(q.s.y, shdn(q.s.x));
   b.v = pr(q.vx.y, shdn(q.vx.x));
@@ -471,12 +522,12 @@ __device__ __forceinline__ void xaccum(RowN<T>& q, FluxP<T> f, bool w0, bool w1)
   q.Ry = psub(q.Ry, pshup(f.t));
   q.Rc = psub(q.Rc, pshup(f.c));
 }
-template <typename T, bool WALLX, bool INIT>
+template <typename T, bool WALLX, bool INIT, bool EFIX>
 __device__ __forceinline__ void row_xedges(const Ctx<T>& c, RowN<T>& q) {
   SideP<T> a, b;
   bool w0, w1;
-  xsides<T, WALLX>(c, q, a, b, w0, w1);
-  xaccum<T, WALLX, INIT>(q, roe_pair<T>(a, b, c.gh), w0, w1);
+  xsides<T, WALLX, EFIX>(c, q, a, b, w0, w1);
+  xaccum<T, WALLX, INIT>(q, roe_pair<T, EFIX>(a, b, c.gh), w0, w1);
 }
 
 // y-edges between row p (below) and row q (above).  WALL: a horizontal
@@ -493,7 +544,7 @@ __device__ __forceinline__ void yaccum(const Ctx<T>& c, RowN<T>& p, RowN<T>& q, 
   p.Rm = padd(p.Rm, f.m); p.Ry = padd(p.Ry, f.pm); p.Rx = padd(p.Rx, f.t); p.Rc = padd(p.Rc, f.c);
   q.Rm = psub(q.Rm, f.m); q.Ry = psub(q.Ry, f.dsum); q.Rx = psub(q.Rx, f.t); q.Rc = psub(q.Rc, f.c);
 }
-template <typename T, bool ANISO, bool WALL>
+template <typename T, bool ANISO, bool WALL, bool EFIX>
 __device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q,
                                            bool lower_is_ghost) {
   SideP<T> a = side_y(p);
@@ -502,19 +553,19 @@ __device__ __forceinline__ void row_yedges(const Ctx<T>& c, RowN<T>& p, RowN<T>&
     if (lower_is_ghost) a = mirror(b);
     else b = mirror(a);
   }
-  yaccum<T, ANISO, WALL>(c, p, q, roe_pair<T>(a, b, c.gh));
+  yaccum<T, ANISO, WALL>(c, p, q, roe_pair<T, EFIX>(a, b, c.gh));
 }
 // Steady rows: the x-edges of row q and the y-edges between p and q
 // evaluated together (one vote, two independent streams of work).
-template <typename T, bool ANISO, bool WALLX>
+template <typename T, bool ANISO, bool WALLX, bool EFIX>
 __device__ __forceinline__ void row_xyedges(const Ctx<T>& c, RowN<T>& p, RowN<T>& q) {
   SideP<T> ax, bx;
   bool w0, w1;
-  xsides<T, WALLX>(c, q, ax, bx, w0, w1);
+  xsides<T, WALLX, EFIX>(c, q, ax, bx, w0, w1);
   const SideP<T> ay = side_y(p);
   const SideP<T> by = side_y(q);
   FluxP<T> fx, fy;
-  roe_two<T>(ax, bx, ay, by, c.gh, fx, fy);
+  roe_two<T, EFIX>(ax, bx, ay, by, c.gh, fx, fy);
   xaccum<T, WALLX, true>(q, fx, w0, w1);
   yaccum<T, ANISO, false>(c, p, q, fy);
 }
@@ -539,7 +590,7 @@ __device__ __forceinline__ void row_yspeeds(const Ctx<T>& c, RowW<T>& u, RowW<T>
 //   STEADY  r in [y0+2, y1-1]: every part runs, no horizontal wall
 //   PAR     0 / 1: k even / odd; 2: decided at run time
 // Returns false if a bounded wait gave up.
-template <typename T, bool ANISO, bool WALLX, bool STEADY, int PAR>
+template <typename T, bool ANISO, bool WALLX, bool EFIX, bool STEADY, int PAR>
 __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>& q, RowW<T>& u,
                                           RowW<T>& w) {
   const StepArgs<T>& A = *c.A;
@@ -581,16 +632,16 @@ __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>&
   }
   // ---- a2/a3: x-edges of row r, y-edges between rows r-1 and r ----------
   if (STEADY) {
-    row_xyedges<T, ANISO, WALLX>(c, p, q);
+    row_xyedges<T, ANISO, WALLX, EFIX>(c, p, q);
   } else {
     if (r >= c.y0 - 1 && r <= c.y1) {
-      row_xedges<T, WALLX, true>(c, q);
+      row_xedges<T, WALLX, true, EFIX>(c, q);
     } else {
       q.Rm = q.Rx = q.Ry = q.Rc = psplat<T>(T(0));
     }
     if (r >= c.y0 - 1) {
-      if (r == 0 || r == A.ny) row_yedges<T, ANISO, true>(c, p, q, r == 0);
-      else row_yedges<T, ANISO, false>(c, p, q, false);
+      if (r == 0 || r == A.ny) row_yedges<T, ANISO, true, EFIX>(c, p, q, r == 0);
+      else row_yedges<T, ANISO, false, EFIX>(c, p, q, false);
     }
     if (r < c.y0) return true;
   }
@@ -660,14 +711,14 @@ __device__ __forceinline__ bool march_row(Ctx<T>& c, int k, RowN<T>& p, RowN<T>&
   return true;
 }
 
-template <typename T, bool ANISO, bool WALLX>
+template <typename T, bool ANISO, bool WALLX, bool EFIX>
 __device__ __forceinline__ bool general_row(Ctx<T>& c, int k, RowN<T>& P, RowN<T>& Q,
                                             RowW<T>& U, RowW<T>& V) {
-  if (k & 1) return march_row<T, ANISO, WALLX, false, 2>(c, k, Q, P, V, U);
-  return march_row<T, ANISO, WALLX, false, 2>(c, k, P, Q, U, V);
+  if (k & 1) return march_row<T, ANISO, WALLX, EFIX, false, 2>(c, k, Q, P, V, U);
+  return march_row<T, ANISO, WALLX, EFIX, false, 2>(c, k, P, Q, U, V);
 }
 
-template <typename T, bool ANISO, bool WALLX>
+template <typename T, bool ANISO, bool WALLX, bool EFIX>
 __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, uint64_t* mbar,
                                       int band, int y0, int y1, T kdt) {
   constexpr int OWN = 64 - 4;
@@ -723,17 +774,17 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
   int k = 0;
   bool ok = true;
   for (; k < 4 && k < c.nrows; ++k) {
-    ok = general_row<T, ANISO, WALLX>(c, k, P, Q, U, V);
+    ok = general_row<T, ANISO, WALLX, EFIX>(c, k, P, Q, U, V);
     if (!ok) break;
   }
   for (; ok && k + 1 <= c.nrows - 3; k += 2) {
-    ok = march_row<T, ANISO, WALLX, true, 0>(c, k, P, Q, U, V);
+    ok = march_row<T, ANISO, WALLX, EFIX, true, 0>(c, k, P, Q, U, V);
     if (!ok) break;
-    ok = march_row<T, ANISO, WALLX, true, 1>(c, k + 1, Q, P, V, U);
+    ok = march_row<T, ANISO, WALLX, EFIX, true, 1>(c, k + 1, Q, P, V, U);
     if (!ok) { ++k; break; }
   }
   for (; ok && k < c.nrows; ++k) {
-    ok = general_row<T, ANISO, WALLX>(c, k, P, Q, U, V);
+    ok = general_row<T, ANISO, WALLX, EFIX>(c, k, P, Q, U, V);
     if (!ok) break;
   }
   if (!ok) {
@@ -757,11 +808,13 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
 #ifndef SWE_STEP_MIN_BLOCKS_F32
 #define SWE_STEP_MIN_BLOCKS_F32 4
 #endif
-template <typename T> struct MinBlocks { static constexpr int v = 1; };
-template <> struct MinBlocks<float> { static constexpr int v = SWE_STEP_MIN_BLOCKS_F32; };
+template <typename T, bool EFIX> struct MinBlocks { static constexpr int v = 1; };
+template <> struct MinBlocks<float, false> { static constexpr int v = SWE_STEP_MIN_BLOCKS_F32; };
+// with the entropy fix the fp32 step needs about 150 registers: 3 blocks
+template <> struct MinBlocks<float, true> { static constexpr int v = 3; };
 
-template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
+template <typename T, bool ANISO, bool EFIX>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T, EFIX>::v)
     cart1_step_kernel(const StepArgs<T> A) {
   constexpr int OWN = 64 - 4;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -816,8 +869,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T>::v)
       warp * kStages;
   // bands whose window reaches a vertical wall take the checked path
   const bool wallx = band == 0 || band * OWN + 64 - 2 > A.nx - 1;
-  if (wallx) march<T, ANISO, true>(A, wsm, mbar, band, y0, y1, kdt);
-  else march<T, ANISO, false>(A, wsm, mbar, band, y0, y1, kdt);
+  if (wallx) march<T, ANISO, true, EFIX>(A, wsm, mbar, band, y0, y1, kdt);
+  else march<T, ANISO, false, EFIX>(A, wsm, mbar, band, y0, y1, kdt);
   pdl_trigger();
 }
 
@@ -899,26 +952,32 @@ size_t step_smem_bytes() {
 }
 
 template <typename T>
-cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes) {
+cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes, bool efix) {
   const size_t smem = step_smem_bytes<T>();
   *smem_bytes = smem;
   cudaError_t e;
-  e = cudaFuncSetAttribute(cart1_step_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(cart1_step_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, cart1_step_kernel<T, false>,
-                                                       kWarpsPerBlock * 32, smem);
+  auto allow = [&](auto kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  };
+  if ((e = allow(cart1_step_kernel<T, false, false>)) != cudaSuccess) return e;
+  if ((e = allow(cart1_step_kernel<T, true, false>)) != cudaSuccess) return e;
+  if ((e = allow(cart1_step_kernel<T, false, true>)) != cudaSuccess) return e;
+  if ((e = allow(cart1_step_kernel<T, true, true>)) != cudaSuccess) return e;
+  return efix ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    blocks_per_sm, cart1_step_kernel<T, false, true>, kWarpsPerBlock * 32, smem)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    blocks_per_sm, cart1_step_kernel<T, false, false>, kWarpsPerBlock * 32, smem);
 }
 
 template <typename T>
 cudaError_t launch_step(const StepArgs<T>& a, int blocks, cudaStream_t st) {
   const size_t smem = step_smem_bytes<T>();
-  return a.rho == T(1)
-             ? launch_pdl(cart1_step_kernel<T, false>, blocks, kWarpsPerBlock * 32, smem, st, a)
-             : launch_pdl(cart1_step_kernel<T, true>, blocks, kWarpsPerBlock * 32, smem, st, a);
+  const dim3 nt(kWarpsPerBlock * 32);
+  if (a.efix)
+    return a.rho == T(1) ? launch_pdl(cart1_step_kernel<T, false, true>, blocks, nt, smem, st, a)
+                         : launch_pdl(cart1_step_kernel<T, true, true>, blocks, nt, smem, st, a);
+  return a.rho == T(1) ? launch_pdl(cart1_step_kernel<T, false, false>, blocks, nt, smem, st, a)
+                       : launch_pdl(cart1_step_kernel<T, true, false>, blocks, nt, smem, st, a);
 }
 
 template <typename T>
@@ -945,8 +1004,8 @@ cudaError_t launch_fill(T* base, int64_t count, T value, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template cudaError_t step_occupancy<float>(int*, size_t*);
-template cudaError_t step_occupancy<double>(int*, size_t*);
+template cudaError_t step_occupancy<float>(int*, size_t*, bool);
+template cudaError_t step_occupancy<double>(int*, size_t*, bool);
 template cudaError_t launch_step<float>(const StepArgs<float>&, int, cudaStream_t);
 template cudaError_t launch_step<double>(const StepArgs<double>&, int, cudaStream_t);
 template cudaError_t launch_dt0<float>(const float* const*, const float*, int, int, int, float,

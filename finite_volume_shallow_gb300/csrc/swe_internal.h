@@ -73,6 +73,7 @@ struct StepArgs {
   double* t_dev;        // simulated time
   int64_t step;         // index of this step (selects the history slot)
   unsigned* err;        // sticky error bits
+  int efix;             // 1: the Harten-Hyman entropy fix of the flux
 };
 
 // ---- two layers (swe_cart2.cu) ----------------------------------------------
@@ -180,6 +181,7 @@ struct MeshStepArgs {
   T g, r;
   void* tmax_out;         // max over cells of sum L max|lambda| / |V_i| (starts at 0)
   unsigned* err;
+  int efix;               // one layer: 1 for the Harten-Hyman entropy fix
 };
 template <typename T>
 struct MeshUpdateArgs {
@@ -274,7 +276,9 @@ cudaError_t launch_fill(T* base, int64_t count, T value, cudaStream_t st);
 // One warp running the step kernel's bounded mbarrier wait on a barrier
 // nothing arrives on; sets kErrTimeout in *err when the wait gives up.
 cudaError_t launch_wait_selftest(long long budget_cycles, unsigned* err, cudaStream_t st);
+// Resident blocks per SM of the one-layer step kernel (efix: the variant
+// with the entropy fix) and its dynamic shared memory; sets its attributes.
 template <typename T>
-cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes);
+cudaError_t step_occupancy(int* blocks_per_sm, size_t* smem_bytes, bool efix = false);
 
 }  // namespace swe

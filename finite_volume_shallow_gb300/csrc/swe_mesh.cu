@@ -50,7 +50,22 @@ struct Side1 {
 // (1, lambda_k)); tangential discharge and pollutant upwinded on the mass
 // flux.  out (not yet multiplied by L): m, m C_up, normal fluctuation of a
 // and of b, tangential transport m u_t,up, max|lambda|.
+//
+// EFIX adds the Harten-Hyman entropy fix ([P1] Sec. 2.2, after eq. (5)) as
+// numerical viscosity along each wave: with delta_k the spread of the
+// speed lambda_k between the two cells' own states (u_eta -+ sqrt(g h)),
+// |lambda_k| < delta_k replaces |lambda_k| by (lambda_k^2 + delta_k^2) /
+// (2 delta_k), and Phi^- gains nu_k K_k, nu_k = (|lambda_k| - |lambda_k|_d)
+// beta_k / 2, beta = K^-1 (W_j - W_i).  The same term leaves side b's
+// fluctuation P^+ d, so the pair stays conservative.
 template <typename T>
+__device__ __forceinline__ T hh_nu(T l, T lL, T lR, T beta) {
+  const T del = fmax(T(0), fmax(l - lL, lR - l));
+  const T al = fabs(l);
+  if (!(al < del)) return T(0);
+  return T(0.5) * (al - (l * l + del * del) * M2<T>::rcp(del + del)) * beta;
+}
+template <typename T, bool EFIX>
 __device__ __forceinline__ void edge1(const Side1<T>& a, const Side1<T>& b, T gh, bool wall,
                                       T& m, T& p, T& pa, T& pb, T& t, T& D) {
   const T un = (a.qn * a.rs + b.qn * b.rs) * M2<T>::rcp(a.s + b.s);
@@ -67,11 +82,23 @@ __device__ __forceinline__ void edge1(const Side1<T>& a, const Side1<T>& b, T gh
   const T w2 = (l2 < T(0)) ? T(1) : ((l2 > T(0)) ? T(0) : T(0.5));
   const T a1 = w1 * (l2 * d1 - d2) * i2c;
   const T a2 = w2 * (d2 - l1 * d1) * i2c;
-  const T pd0 = a1 + a2;
-  const T pd1 = a1 * l1 + a2 * l2;
+  T pd0 = a1 + a2;
+  T pd1 = a1 * l1 + a2 * l2;
+  pb = d2 - pd1;
+  if (EFIX) {
+    const T sg = M2<T>::sq(gh + gh);  // sqrt(g)
+    const T ua = a.qn * iha, ub = b.qn * ihb;
+    const T ca = sg * a.s, cb = sg * b.s;
+    const T dh = b.h - a.h;
+    const T n1 = hh_nu(l1, ua - ca, ub - cb, (l2 * dh - d1) * i2c);
+    const T n2 = hh_nu(l2, ua + ca, ub + cb, (d1 - l1 * dh) * i2c);
+    pd0 += n1 + n2;
+    const T cmom = n1 * l1 + n2 * l2;
+    pd1 += cmom;
+    pb -= cmom;
+  }
   m = wall ? T(0) : a.qn + pd0;
   pa = pd1;
-  pb = d2 - pd1;
   const bool up = m > T(0);
   t = m * (up ? a.qt * iha : b.qt * ihb);
   p = m * (up ? a.hc * iha : b.hc * ihb);
@@ -116,7 +143,7 @@ __device__ __forceinline__ void put_xy(T* buf, int64_t st, int64_t e, int q, T L
   buf[(q + 1) * st + e] = L * (fn * ey + ft * ex);
 }
 
-template <typename T, int NL>
+template <typename T, int NL, bool EFIX = false>
 __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepArgs<T> A) {
   using Lay = MeshLayout<NL>;
   const int64_t e = (int64_t)blockIdx.x * kEdgeThreads + threadIdx.x;
@@ -135,7 +162,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
       if (wall) sb.qn = -sa.qn;
       else sb = load_side1(A, b, ex, ey);
       T m, p, pa, pb, t, D;
-      edge1<T>(sa, sb, gh, wall, m, p, pa, pb, t, D);
+      edge1<T, EFIX>(sa, sb, gh, wall, m, p, pa, pb, t, D);
       buf[0 * st + e] = L * m;
       buf[1 * st + e] = L * p;
       const T ta = t - sa.qn * (sa.qt * sa.rs * sa.rs);
@@ -561,6 +588,8 @@ cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& 
     } else {
       e = launch_pdl(mesh_edge_kernel<T, 2>, ge, kEdgeThreads, 0, st, f);
     }
+  } else if (f.efix) {
+    e = launch_pdl(mesh_edge_kernel<T, 1, true>, ge, kEdgeThreads, 0, st, f);
   } else {
     e = launch_pdl(mesh_edge_kernel<T, 1>, ge, kEdgeThreads, 0, st, f);
   }

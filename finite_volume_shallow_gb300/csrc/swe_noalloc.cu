@@ -39,8 +39,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_dev[kMaxDevices] = {nullptr};
-bool g_attr_done[kMaxDevices][2] = {{false}};
-int g_blocks_per_sm[kMaxDevices][2] = {{0}};
+bool g_attr_done[kMaxDevices][4] = {{false}};  // [precision + 2 * entropy fix]
+int g_blocks_per_sm[kMaxDevices][4] = {{0}};
 int g_sms[kMaxDevices] = {0};
 
 swe_status cuda_st(cudaError_t e) {
@@ -58,9 +58,9 @@ swe_status cuda_st(cudaError_t e) {
 // Once per device (with that device current): the scratch array's device
 // address, the step kernel's shared-memory attribute and its occupancy.
 template <typename T>
-swe_status setup(int dev, unsigned char** scratch, int* bpsm, int* sms) {
+swe_status setup(int dev, bool efix, unsigned char** scratch, int* bpsm, int* sms) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  const int ti = sizeof(T) == 4 ? 0 : 1;
+  const int ti = (sizeof(T) == 4 ? 0 : 1) + (efix ? 2 : 0);
   if (!g_scratch_dev[dev]) {
     void* p = nullptr;
     CKN(cudaGetSymbolAddress(&p, g_noalloc_scratch));
@@ -69,7 +69,7 @@ swe_status setup(int dev, unsigned char** scratch, int* bpsm, int* sms) {
   }
   if (!g_attr_done[dev][ti]) {
     size_t smem = 0;
-    CKN(step_occupancy<T>(&g_blocks_per_sm[dev][ti], &smem));
+    CKN(step_occupancy<T>(&g_blocks_per_sm[dev][ti], &smem, efix));
     if (g_blocks_per_sm[dev][ti] < 1) return SWE_ERR_CUDA;
     g_attr_done[dev][ti] = true;
   }
@@ -87,7 +87,7 @@ swe_status run(const swe_grid* g, const swe_params* p, const void* H, void* cons
   if (dev < 0 || dev >= kMaxDevices) return SWE_ERR_UNSUPPORTED;
   unsigned char* scr = nullptr;
   int bpsm = 0, sms = 0;
-  swe_status st = setup<T>(dev, &scr, &bpsm, &sms);
+  swe_status st = setup<T>(dev, p->entropy_fix != 0, &scr, &bpsm, &sms);
   if (st != SWE_OK) return st;
   cudaStream_t stream = (cudaStream_t)p->stream;
 
@@ -135,6 +135,7 @@ swe_status run(const swe_grid* g, const swe_params* p, const void* H, void* cons
     s.t_dev = tdev;
     s.step = n;
     s.err = err;
+    s.efix = p->entropy_fix;
     CKN(launch_step<T>(s, blocks, stream));
   }
   if (nsteps % 2 == 1) {  // the state is in Wb: hand it back in Wa
@@ -170,6 +171,7 @@ extern "C" swe_status swe_run_noalloc(const swe_grid* grid, const swe_params* pa
   if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
   if (!pos_finite(params->g) || !(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
   if (params->n_layers == 2 || params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->entropy_fix != 0 && params->entropy_fix != 1) return SWE_ERR_ARG;
   if (params->n_layers != 1) return SWE_ERR_ARG;
   if (nsteps < 0 || nsteps > SWE_NOALLOC_MAX_STEPS) return SWE_ERR_ARG;
   const int64_t need =

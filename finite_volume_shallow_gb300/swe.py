@@ -48,7 +48,7 @@ class _Mesh(C.Structure):
 class _Params(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("precision", C.c_int32), ("pollutant", C.c_int32),
                 ("g", C.c_double), ("r", C.c_double), ("cfl", C.c_double),
-                ("stream", C.c_void_p)]
+                ("stream", C.c_void_p), ("entropy_fix", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -162,7 +162,7 @@ class State:
 
 
 def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream=None,
-                    n_layers=1, pollutant=1, r=0.0) -> State:
+                    n_layers=1, pollutant=1, r=0.0, entropy_fix=0) -> State:
     """Create a simulation on an nx x ny grid (see swe_create_grid in swe.h).
     H and the fields of W0 (h, qx, qy, hC; or h1, q1x, q1y, h2, q2x, q2y with
     n_layers=2, pollutant=0) are host arrays of the state's precision;
@@ -173,7 +173,7 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
     n = int(nx) * int(ny)
     grid = _Grid(int(nx), int(ny), float(dx), float(dy))
     params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
-                     float(cfl), C.c_void_p(stream) if stream else None)
+                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix))
     Hp = _host_ptr(H, dt, n)
     W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
     out = C.c_void_p()
@@ -183,7 +183,7 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
 
 
 def swe_create_mesh(xy, tri, H, W0, precision=64, g=9.81, cfl=0.9, stream=None, n_layers=1,
-                    pollutant=1, r=0.0, reorder=1) -> State:
+                    pollutant=1, r=0.0, reorder=1, entropy_fix=0) -> State:
     """Create a simulation on a triangle mesh (see swe_create_mesh in swe.h):
     ``xy`` is an (n_vertices, 2) float64 array, ``tri`` an (n_cells, 3) int32
     array of counter-clockwise vertex indices; H and the fields of W0 hold
@@ -193,7 +193,7 @@ def swe_create_mesh(xy, tri, H, W0, precision=64, g=9.81, cfl=0.9, stream=None, 
     mesh, xy, tri = _mesh_struct(xy, tri, reorder)
     n = int(tri.shape[0])
     params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
-                     float(cfl), C.c_void_p(stream) if stream else None)
+                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix))
     Hp = _host_ptr(H, dt, n)
     W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
     out = C.c_void_p()
@@ -302,13 +302,13 @@ def noalloc_pitch(nx) -> int:
 
 
 def swe_run_noalloc(nx, ny, dx, dy, H, W_a, W_b, pitch, nsteps, precision=64, g=9.81,
-                    cfl=0.9, stream=None):
+                    cfl=0.9, stream=None, entropy_fix=0):
     """Allocation-free run on caller-owned device buffers (see swe.h): H, W_a
     (4) and W_b (4) are device addresses (ints) in the padded layout.
     Returns the dt of each step."""
     grid = _Grid(int(nx), int(ny), float(dx), float(dy))
     params = _Params(1, int(precision), 1, float(g), 0.0, float(cfl),
-                     C.c_void_p(stream) if stream else None)
+                     C.c_void_p(stream) if stream else None, int(entropy_fix))
     wa = (C.c_void_p * 4)(*[int(p) for p in W_a])
     wb = (C.c_void_p * 4)(*[int(p) for p in W_b])
     dts = np.zeros(max(int(nsteps), 1), dtype=np.float64)

@@ -106,7 +106,17 @@ typedef struct {
  *  r          density ratio rho1/rho2, 0 <= r < 1, two layers; ignored for 1
  *  cfl        gamma of eq. (5), 0 < cfl <= 1, used by swe_run
  *  stream     cudaStream_t the handle orders its work on; NULL = legacy
- *             default stream */
+ *             default stream
+ *  entropy_fix  0: P^- of [P1] Sec. 2.2 as printed; 1 (one layer only): the
+ *             Harten-Hyman entropy fix that [P1] Sec. 2.2 (after eq. (5))
+ *             names for sonic rarefactions.  Per characteristic speed
+ *             lambda_k of the Roe matrix, delta_k = max(0, lambda_k -
+ *             lambda_k(W_i), lambda_k(W_j) - lambda_k); where |lambda_k| <
+ *             delta_k the scheme uses (lambda_k^2 + delta_k^2) / (2 delta_k)
+ *             in place of |lambda_k|, i.e. Phi^- gains
+ *             (|lambda_k| - |lambda_k|_d) beta_k K_k / 2 with beta = K^-1
+ *             (W_j - W_i).  1 with two layers returns SWE_ERR_UNSUPPORTED;
+ *             any value other than 0 or 1 returns SWE_ERR_ARG. */
 typedef struct {
   int32_t n_layers;
   int32_t precision;
@@ -115,6 +125,7 @@ typedef struct {
   double r;
   double cfl;
   void *stream;
+  int32_t entropy_fix;
 } swe_params;
 
 typedef struct swe_state swe_state;

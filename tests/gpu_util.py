@@ -21,7 +21,8 @@ def gpu_create(d, precision, cfl=None, stream=None):
     dt = np_dtype(precision)
     return S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(dt),
                              [f.astype(dt) for f in I.fields_of(d)], precision=precision,
-                             g=d["g"], cfl=d["cfl"] if cfl is None else cfl, stream=stream)
+                             g=d["g"], cfl=d["cfl"] if cfl is None else cfl, stream=stream,
+                             entropy_fix=d.get("entropy_fix", 0))
 
 
 def gpu_run(d, precision, nsteps, use_run=False):
@@ -40,8 +41,9 @@ def gpu_run(d, precision, nsteps, use_run=False):
 def oracle_run(d, precision, nsteps):
     """The oracle on the same inputs (rounded to the GPU's precision)."""
     dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
-    W, dts, st = O.grid_run1(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields_of(dr),
-                             d["g"], d["cfl"], nsteps)
+    with O.entropy_fix(d.get("entropy_fix", 0)):
+        W, dts, st = O.grid_run1(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields_of(dr),
+                                 d["g"], d["cfl"], nsteps)
     assert st == O.OM_OK, st
     return W, dts
 
@@ -138,7 +140,8 @@ def gpu_create_mesh(d, precision, reorder=1, stream=None):
     return S.swe_create_mesh(d["xy"], d["tri"], d["H"].astype(dt), mesh_fields(d, dt),
                              precision=precision, g=d.get("g", 9.81), cfl=d.get("cfl", 0.9),
                              stream=stream, n_layers=d["n_layers"], pollutant=0 if two else 1,
-                             r=d.get("r", 0.0), reorder=reorder)
+                             r=d.get("r", 0.0), reorder=reorder,
+                             entropy_fix=d.get("entropy_fix", 0))
 
 
 def gpu_run_mesh(d, precision, nsteps, reorder=1):
@@ -157,8 +160,9 @@ def oracle_run_mesh(d, precision, nsteps):
         W, dts, st = O.run2(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d["r"],
                             d.get("cfl", 0.9), nsteps)
     else:
-        W, dts, st, _ = O.run1(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d.get("cfl", 0.9),
-                               nsteps)
+        with O.entropy_fix(d.get("entropy_fix", 0)):
+            W, dts, st, _ = O.run1(m, dr["H"], mesh_fields(dr), d.get("g", 9.81),
+                                   d.get("cfl", 0.9), nsteps)
     assert st == O.OM_OK, st
     return W, dts
 

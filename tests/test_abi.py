@@ -57,10 +57,11 @@ def _grid(nx=4, ny=3, dx=1.0, dy=1.0):
 
 
 def _params(**kw):
-    p = dict(n_layers=1, precision=64, pollutant=1, g=9.81, r=0.0, cfl=0.9, stream=None)
+    p = dict(n_layers=1, precision=64, pollutant=1, g=9.81, r=0.0, cfl=0.9, stream=None,
+             entropy_fix=0)
     p.update(kw)
     return S._Params(p["n_layers"], p["precision"], p["pollutant"], p["g"], p["r"], p["cfl"],
-                     p["stream"])
+                     p["stream"], p["entropy_fix"])
 
 
 def _create(lib, grid, params, n=12, with_fields=True):
@@ -88,6 +89,9 @@ def _create(lib, grid, params, n=12, with_fields=True):
     (_grid(), _params(n_layers=3), S.SWE_ERR_ARG),
     (_grid(), _params(n_layers=2), S.SWE_ERR_UNSUPPORTED),
     (_grid(), _params(pollutant=0), S.SWE_ERR_UNSUPPORTED),
+    (_grid(), _params(entropy_fix=2), S.SWE_ERR_ARG),
+    (_grid(), _params(entropy_fix=-1), S.SWE_ERR_ARG),
+    (_grid(), _params(n_layers=2, pollutant=0, r=0.5, entropy_fix=1), S.SWE_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_arguments(lib, grid, params, expect):
     st, out = _create(lib, grid, params)
@@ -138,6 +142,10 @@ def test_noalloc_rejects_bad_arguments_before_touching_the_gpu(lib):
     with pytest.raises(S.SweError) as e:
         S.swe_run_noalloc(64, 40, 1.0, 1.0, fake[0], fake[1:5], fake[5:9], S.noalloc_pitch(64), 3,
                           precision=16)
+    assert e.value.status == S.SWE_ERR_ARG
+    with pytest.raises(S.SweError) as e:
+        S.swe_run_noalloc(64, 40, 1.0, 1.0, fake[0], fake[1:5], fake[5:9], S.noalloc_pitch(64), 3,
+                          entropy_fix=3)
     assert e.value.status == S.SWE_ERR_ARG
 
 

@@ -267,22 +267,41 @@ __device__ __forceinline__ T sgn_weight(T l) {  // (1 - sgn l) / 2, sgn 0 = 0
 template <typename T>
 struct RoeHead {
   Pr<T> l1, l2, d0, d1n, a1, i2c;
-  Pr<T> del1, del2;  // entropy fix: Harten-Hyman delta of each wave
 };
 // Entropy fix (EFIX; [P1] Sec. 2.2 remarks that a Harten-Hyman fix can be
 // adapted, without a formula): Harten's regularised |l|_d = |l| when
 // |l| >= delta, (l^2 + delta^2) / (2 delta) otherwise, with delta_k =
 // max(0, l_k - l_k(W_a), l_k(W_b) - l_k), l_k(W) = u_eta -/+ sqrt(g h) of the
 // state itself; it adds 1/2 (|l_k| - |l_k|_d) beta_k K_k to Phi^-, with
-// beta = K^-1 (W_b - W_a).  Zero wherever |l_k| >= delta_k.
+// beta = K^-1 (W_b - W_a).  Zero wherever |l_k| >= delta_k.  The deltas
+// are formed twice: once for the warp vote (is the fix inactive on every
+// edge?) and again in the general tail, so that none stays live in between.
 template <typename T>
 __device__ __forceinline__ T hh_delta(T l, T lL, T lR) {
   return fmax(T(0), fmax(l - lL, lR - l));
 }
 template <typename T>
-__device__ __forceinline__ bool no_fix(const RoeHead<T>& e) {
-  return (fabs(e.l1.x) >= e.del1.x) & (fabs(e.l1.y) >= e.del1.y) &
-         (fabs(e.l2.x) >= e.del2.x) & (fabs(e.l2.y) >= e.del2.y);
+struct HHDelta {
+  Pr<T> d1, d2;
+};
+template <typename T>
+__device__ __forceinline__ HHDelta<T> hh_deltas(const RoeHead<T>& e, const SideP<T>& a,
+                                                const SideP<T>& b, Pr<T> gh) {
+  using P = Pr<T>;
+  // sqrt(g h) of each side: sqrt(2 gh) s
+  const P sg = psplat<T>(sqrt(T(2) * gh.x));
+  const P ca = pmul(sg, a.s), cb = pmul(sg, b.s);
+  const P lL1 = psub(a.u, ca), lR1 = psub(b.u, cb);
+  const P lL2 = padd(a.u, ca), lR2 = padd(b.u, cb);
+  return {pr(hh_delta(e.l1.x, lL1.x, lR1.x), hh_delta(e.l1.y, lL1.y, lR1.y)),
+          pr(hh_delta(e.l2.x, lL2.x, lR2.x), hh_delta(e.l2.y, lL2.y, lR2.y))};
+}
+template <typename T>
+__device__ __forceinline__ bool no_fix(const RoeHead<T>& e, const SideP<T>& a, const SideP<T>& b,
+                                       Pr<T> gh) {
+  const HHDelta<T> d = hh_deltas(e, a, b, gh);
+  return (fabs(e.l1.x) >= d.d1.x) & (fabs(e.l1.y) >= d.d1.y) & (fabs(e.l2.x) >= d.d2.x) &
+         (fabs(e.l2.y) >= d.d2.y);
 }
 // 1/2 (|l| - |l|_d) for one edge (0 where the fix is not active)
 template <typename T>
@@ -291,7 +310,7 @@ __device__ __forceinline__ T hh_visc(T l, T del) {
   if (!(a < del)) return T(0);
   return T(0.5) * (a - (l * l + del * del) * Fm<T>::rcp(del + del));
 }
-template <typename T, bool EFIX = false>
+template <typename T>
 __device__ __forceinline__ RoeHead<T> roe_head(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
   using P = Pr<T>;
   RoeHead<T> e;
@@ -305,15 +324,6 @@ __device__ __forceinline__ RoeHead<T> roe_head(const SideP<T>& a, const SideP<T>
   e.d0 = psub(b.qn, a.qn);
   e.d1n = pfma(c2, psub(psub(b.H, a.H), psub(b.h, a.h)), psub(a.qu, b.qu));
   e.a1 = pmul(pfma(e.l2, e.d0, e.d1n), e.i2c);
-  if (EFIX) {
-    // sqrt(g h) of each side: sqrt(2 gh) s
-    const T sg = sqrt(T(2) * gh.x);
-    const P ca = pmul(psplat<T>(sg), a.s), cb = pmul(psplat<T>(sg), b.s);
-    const P lL1 = psub(a.u, ca), lR1 = psub(b.u, cb);
-    const P lL2 = padd(a.u, ca), lR2 = padd(b.u, cb);
-    e.del1 = pr(hh_delta(e.l1.x, lL1.x, lR1.x), hh_delta(e.l1.y, lL1.y, lR1.y));
-    e.del2 = pr(hh_delta(e.l2.x, lL2.x, lR2.x), hh_delta(e.l2.y, lL2.y, lR2.y));
-  }
   return e;
 }
 template <typename T>
@@ -326,7 +336,7 @@ __device__ __forceinline__ bool subcritical(const RoeHead<T>& e) {
 // tangential velocity and of the concentration.
 template <typename T, bool EFIX = false>
 __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>& a,
-                                             const SideP<T>& b, bool fast) {
+                                             const SideP<T>& b, Pr<T> gh, bool fast) {
   using P = Pr<T>;
   FluxP<T> f;
   if (fast) {
@@ -343,8 +353,9 @@ __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>
       const P dh = psub(b.h, a.h);
       const P be1 = pmul(psub(pmul(e.l2, dh), e.d0), e.i2c);
       const P be2 = pmul(psub(e.d0, pmul(e.l1, dh)), e.i2c);
-      const P n1 = pmul(pr(hh_visc(e.l1.x, e.del1.x), hh_visc(e.l1.y, e.del1.y)), be1);
-      const P n2 = pmul(pr(hh_visc(e.l2.x, e.del2.x), hh_visc(e.l2.y, e.del2.y)), be2);
+      const HHDelta<T> d = hh_deltas(e, a, b, gh);
+      const P n1 = pmul(pr(hh_visc(e.l1.x, d.d1.x), hh_visc(e.l1.y, d.d1.y)), be1);
+      const P n2 = pmul(pr(hh_visc(e.l2.x, d.d2.x), hh_visc(e.l2.y, d.d2.y)), be2);
       f.m = padd(f.m, padd(n1, n2));
       f.pm = padd(f.pm, padd(pmul(n1, e.l1), pmul(n2, e.l2)));
     }
@@ -358,23 +369,23 @@ __device__ __forceinline__ FluxP<T> roe_tail(const RoeHead<T>& e, const SideP<T>
 }
 template <typename T, bool EFIX = false>
 __device__ __forceinline__ FluxP<T> roe_pair(const SideP<T>& a, const SideP<T>& b, Pr<T> gh) {
-  const RoeHead<T> e = roe_head<T, EFIX>(a, b, gh);
+  const RoeHead<T> e = roe_head<T>(a, b, gh);
   bool ok = subcritical(e);
-  if (EFIX) ok &= no_fix(e);
-  return roe_tail<T, EFIX>(e, a, b, __all_sync(kFull, ok));
+  if (EFIX) ok &= no_fix(e, a, b, gh);
+  return roe_tail<T, EFIX>(e, a, b, gh, __all_sync(kFull, ok));
 }
 // Two pairs at once (the x-edges and the y-edges of a row), one vote.
 template <typename T, bool EFIX = false>
 __device__ __forceinline__ void roe_two(const SideP<T>& ax, const SideP<T>& bx,
                                         const SideP<T>& ay, const SideP<T>& by, Pr<T> gh,
                                         FluxP<T>& fx, FluxP<T>& fy) {
-  const RoeHead<T> ex = roe_head<T, EFIX>(ax, bx, gh);
-  const RoeHead<T> ey = roe_head<T, EFIX>(ay, by, gh);
+  const RoeHead<T> ex = roe_head<T>(ax, bx, gh);
+  const RoeHead<T> ey = roe_head<T>(ay, by, gh);
   bool ok = subcritical(ex) & subcritical(ey);
-  if (EFIX) ok &= no_fix(ex) & no_fix(ey);
+  if (EFIX) ok &= no_fix(ex, ax, bx, gh) & no_fix(ey, ay, by, gh);
   const bool fast = __all_sync(kFull, ok);
-  fx = roe_tail<T, EFIX>(ex, ax, bx, fast);
-  fy = roe_tail<T, EFIX>(ey, ay, by, fast);
+  fx = roe_tail<T, EFIX>(ex, ax, bx, gh, fast);
+  fy = roe_tail<T, EFIX>(ey, ay, by, gh, fast);
 }
 
 // ||D_ij||_inf = |u_eta| + c of the Roe matrix of an edge (eq. (5)); the
@@ -810,8 +821,10 @@ __device__ __forceinline__ void march(const StepArgs<T>& A, unsigned char* wsm, 
 #endif
 template <typename T, bool EFIX> struct MinBlocks { static constexpr int v = 1; };
 template <> struct MinBlocks<float, false> { static constexpr int v = SWE_STEP_MIN_BLOCKS_F32; };
-// with the entropy fix the fp32 step needs about 150 registers: 3 blocks
-template <> struct MinBlocks<float, true> { static constexpr int v = 3; };
+#ifndef SWE_STEP_MIN_BLOCKS_F32_EFIX
+#define SWE_STEP_MIN_BLOCKS_F32_EFIX 3
+#endif
+template <> struct MinBlocks<float, true> { static constexpr int v = SWE_STEP_MIN_BLOCKS_F32_EFIX; };
 
 template <typename T, bool ANISO, bool EFIX>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, MinBlocks<T, EFIX>::v)

@@ -45,6 +45,15 @@ def test_strong_radial_dam_break(precision):
 
 
 @pytest.mark.parametrize("precision", [64, 32])
+def test_strong_dam_break_on_anisotropic_cells(precision):
+    # dx != dy runs the anisotropic variant of the step with the fix
+    d = I.circular_dam(120, 64, dx=1.0, dy=2.5, radius=25.0, centre=(50.0, 70.0), h_in=10.0,
+                       h_out=0.5)
+    d.update(g=9.81, cfl=0.9, entropy_fix=1)
+    assert_parity(d, precision, 60)
+
+
+@pytest.mark.parametrize("precision", [64, 32])
 def test_supercritical_departure_from_a_wall(precision):
     # u = 3.6 m/s > sqrt(g h) = 3.1 m/s leaving the left wall: against its
     # mirror ghost the 2-speed of the wall edge has spread delta = u > c, so

@@ -40,6 +40,7 @@ WORKLOADS = {
     "pulses8192": dict(nx=8192, ny=8192, dx=10.0, steps=200, seed=1003, precision=32),
     "interface2048": dict(nx=2048, ny=2048, dx=10.0, steps=500, seed=1004, precision=64),
     "tri1024": dict(nx=1024, ny=1024, dx=1.0, steps=500, seed=1005, precision=32),
+    "tri1024_1l": dict(nx=1024, ny=1024, dx=1.0, steps=500, seed=1006, precision=32),
 }
 TWO_LAYER = ("interface2048", "tri1024")
 
@@ -345,6 +346,10 @@ def make_workload(name, nx=None, ny=None, lake_at_rest=False):
         d = tri_workload(nx)
         d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
                  name=name)
+        return d
+    if name == "tri1024_1l":
+        d = tri_workload1(nx, ny, seed=w["seed"])
+        d.update(steps=w["steps"], precision=w["precision"], name=name)
         return d
     if name == "interface2048":
         d = interface_dam(nx, ny, dx)

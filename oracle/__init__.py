@@ -116,7 +116,7 @@ def lib():
 
 
 class entropy_fix:
-    """Context manager: the one-layer flux of the oracle with the
+    """Context manager: the flux of the oracle (one layer or two) with the
     Harten-Hyman entropy fix switched on (see om_set_entropy_fix)."""
 
     def __init__(self, on=True):

@@ -66,7 +66,9 @@ void om_grid_mesh(int64_t nx, int64_t ny, double dx, double dy, double *area,
 
 static double sgn(double x) { return (x > 0.0) ? 1.0 : ((x < 0.0) ? -1.0 : 0.0); }
 
-/* Optional entropy fix of the one-layer flux (off unless switched on).
+/* Optional entropy fix of the flux (off unless switched on; om_flux1 and
+ * om_flux2, where lambda_k(W) is the k-th eigenvalue of the two-layer
+ * Jacobian of the state W).
  * [P1] Sec. 2.2 remarks that an entropy fix of Harten-Hyman type can be
  * adapted to the scheme but gives no formula; this is the published one:
  * Harten's regularised absolute value |lambda|_d = |lambda| when
@@ -605,6 +607,27 @@ int om_flux2(const double *Wi, const double *Wj, double Hi, double Hj,
     double acc = 0.0;
     for (int b = 0; b < 4; ++b) acc += P[a][b] * d[b];
     phi[a] = acc + Fi[a];
+  }
+  if (g_entropy_fix) {
+    /* the same Harten-Hyman viscosity as one layer, per wave of A_ij: the
+     * k-th speed of each side is the k-th smallest eigenvalue of the side's
+     * own Jacobian, i.e. the k-th root of the quartic with that side's
+     * normal velocities and c_k^2 = g h_k (an error if that side's own
+     * system is not hyperbolic); beta = K^-1 (W_j - W_i) */
+    double lamS[2][4];
+    for (int side = 0; side < 2; ++side) {
+      int st2 = om_roots2(qn[side][0] / h[side][0], qn[side][1] / h[side][1], g * h[side][0],
+                          g * h[side][1], r, lamS[side]);
+      if (st2 != OM_OK) return st2;
+    }
+    double dW[4] = {h[1][0] - h[0][0], qn[1][0] - qn[0][0], h[1][1] - h[0][1],
+                    qn[1][1] - qn[0][1]};
+    for (int k = 0; k < 4; ++k) {
+      double beta = 0.0;
+      for (int b = 0; b < 4; ++b) beta += Kinv[k][b] * dW[b];
+      double nu = 0.5 * (fabs(lam[k]) - harten_abs(lam[k], lamS[0][k], lamS[1][k])) * beta;
+      for (int a = 0; a < 4; ++a) phi[a] += nu * K[a][k];
+    }
   }
   /* step 3: tangential discharge of each layer upwinded with its mass flux */
   double pt[2];

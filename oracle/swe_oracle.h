@@ -80,8 +80,8 @@ void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
 /* Mirror ghost state of a reflective wall with outward normal (ex, ey). */
 void om_wall_ghost1(const double *Wi, double ex, double ey, double *Wg);
 
-/* Switch the Harten-Hyman entropy fix of the one-layer flux on (1) or off
- * (0, the default) for every later one-layer call. */
+/* Switch the Harten-Hyman entropy fix of the flux on (1) or off (0, the
+ * default) for every later call, one layer or two. */
 void om_set_entropy_fix(int on);
 
 /* Time step of eq. (5): min_i 2 cfl |V_i| / sum_j |Gamma_ij| ||D_ij||_inf.

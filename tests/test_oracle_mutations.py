@@ -23,6 +23,18 @@ MUTANTS = {
                   "0.5 * (harten_abs(lam[k], lamL[k], lamR[k]) - fabs(lam[k])) * beta"),
     "efix_delta": ("fmax(lam - lamL, lamR - lam)", "fmax(lamL - lam, lam - lamR)"),
     "efix_beta": ("Kinv[k][0] * dW[0] + Kinv[k][1] * dW[1]", "Kinv[k][0] * dW[1] + Kinv[k][1] * dW[0]"),
+    # two layers: the same three, and each side's speeds from the quartic
+    # with the layers' depths swapped
+    "efix2_sign": ("0.5 * (fabs(lam[k]) - harten_abs(lam[k], lamS[0][k], lamS[1][k])) * beta",
+                   "0.5 * (harten_abs(lam[k], lamS[0][k], lamS[1][k]) - fabs(lam[k])) * beta"),
+    "efix2_sides": ("harten_abs(lam[k], lamS[0][k], lamS[1][k])",
+                    "harten_abs(lam[k], lamS[1][k], lamS[0][k])"),
+    "efix2_beta": ("double dW[4] = {h[1][0] - h[0][0], qn[1][0] - qn[0][0], h[1][1] - h[0][1],\n"
+                   "                    qn[1][1] - qn[0][1]};",
+                   "double dW[4] = {h[1][1] - h[0][1], qn[1][1] - qn[0][1], h[1][0] - h[0][0],\n"
+                   "                    qn[1][0] - qn[0][0]};"),
+    "efix2_layer_speeds": ("g * h[side][0],\n                          g * h[side][1], r",
+                           "g * h[side][1],\n                          g * h[side][0], r"),
     # bathymetry source with the wrong sign
     "source_sign": ("- g * hbar * (Hj - Hi)", "+ g * hbar * (Hj - Hi)"),
     # source term dropped

@@ -252,3 +252,57 @@ def test_two_layer_numbering_independence():
     assert sa == sb == O.OM_OK and np.array_equal(da, db)
     for a, b in zip(Wa, Wb):
         assert np.abs(a[inv] - b).max() <= 1e-13 * np.abs(a).max()
+
+
+# ---- the Harten-Hyman entropy fix with two layers ---------------------------
+def test_entropy_fix_lower_layer_decouples_at_r0():
+    # With r = 0 the lower layer is the one-layer system over H, and the
+    # eigenvectors of its two waves have no upper-layer part in K^-1, so the
+    # two-layer fix must give the lower layer exactly the one-layer fix (whose
+    # own pins tie it to Stoker's solution).  The lower layer is the
+    # transonic dam break h 10 m / 0.5 m; the upper layer is 50-59.5 m thick
+    # with a flat surface, so its speeds (+-23 m/s) stay clear of the lower
+    # layer's and the eigenvector basis is well conditioned.
+    nx = 200
+    d = I.dam_break_1d(nx, h_left=10.0, h_right=0.5)
+    h2 = d["h"]
+    z = np.zeros(h2.size)
+    m = O.grid_mesh(nx, 4, d["dx"], d["dy"])
+    dt = 0.15   # below the CFL limit of the initial state (0.186 s)
+    lower = {}
+    for fix in (0, 1):
+        W2 = [60.0 - h2, z, z, h2, z, z]
+        W1 = [h2, z, z, d["hC"]]
+        with O.entropy_fix(fix):
+            for _ in range(40):
+                W2, s2 = O.update2(m, d["H"], W2, G, 0.0, dt)
+                W1, s1 = O.update1(m, d["H"], W1, G, dt)
+                assert s1 == s2 == O.OM_OK
+        for a, b in zip(W2[3:], W1[:3]):
+            assert np.abs(a - b).max() <= 1e-13 * np.abs(b).max()
+        lower[fix] = W2[3]
+    assert np.abs(lower[0] - lower[1]).max() > 0.1   # the fix acts here
+
+
+def test_entropy_fix_two_layers_at_rest_and_conservative():
+    nx, ny = 40, 32
+    H, W = lake2(nx, ny)
+    with O.entropy_fix():
+        Wf, _, st = O.grid_run2(nx, ny, 10.0, 10.0, H, W, G, 0.98, 0.9, 60)
+    assert st == O.OM_OK
+    for k in (0, 3):
+        assert np.abs(Wf[k] - W[k]).max() <= 1e-13 * W[k].max()
+    qs = W[3].max() * math.sqrt(G * W[3].max())
+    for k in (1, 2, 4, 5):
+        assert np.abs(Wf[k]).max() <= 1e-13 * qs
+    # a radial transonic dam break in the lower layer at r = 0.5: each
+    # layer's mass is conserved with the fix on
+    d = I.circular_dam(48, 40, dx=5.0, radius=60.0, h_in=10.0, h_out=0.5)
+    h2 = d["h"]
+    z = np.zeros(h2.size)
+    W = [30.0 - h2, z, z, h2, z, z]
+    with O.entropy_fix():
+        Wf, _, st = O.grid_run2(48, 40, 5.0, 5.0, d["H"], W, G, 0.5, 0.9, 60)
+    assert st == O.OM_OK
+    for k in (0, 3):
+        assert abs(Wf[k].sum() - W[k].sum()) <= 1e-12 * W[k].sum()

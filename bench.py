@@ -122,7 +122,6 @@ DESCR = {
                   "of 0.5 m, |u|<=0.1 m/s per component, pollutant per 4x4 block of squares, "
                   "reflective walls",
 }
-TWO_LAYER_WORKLOADS = ("interface2048", "tri1024")
 
 
 def kernel_model(kernel, precision, nl, n_cells, n_edges):
@@ -244,7 +243,7 @@ def parse():
     p.add_argument("--nx", type=int, default=None, help="reduced grid (same recipe)")
     p.add_argument("--ny", type=int, default=None)
     p.add_argument("--entropy-fix", action="store_true",
-                   help="one layer: the Harten-Hyman entropy fix of the flux")
+                   help="the Harten-Hyman entropy fix of the flux")
     p.add_argument("--no-clocks", action="store_true",
                    help="skip the nvidia-smi clock window (profiling runs)")
     a = p.parse_args()
@@ -252,8 +251,6 @@ def parse():
         p.error("--warmup must be at least 3")
     if a.steps < 1:
         p.error("--steps must be at least 1")
-    if a.entropy_fix and a.workload in TWO_LAYER_WORKLOADS:
-        p.error("--entropy-fix applies to one-layer workloads only")
     return a
 
 

@@ -232,6 +232,7 @@ swe_status enqueue_step2(swe_state* s, double cfl, bool last) {
   f.rho = (T)(s->dx / s->dy);
   f.tmax_out = slot(m);
   f.err = s->err;
+  f.efix = s->p.entropy_fix;
   auto upd_args = [&](Update2Args<T>& u, int a, int dst, int64_t step, double c, bool end) {
     for (int k = 0; k < 6; ++k) {
       u.win[k] = (const T*)s->w[a][k];
@@ -508,7 +509,6 @@ swe_status check_params(const swe_params* params) {
   if (params->n_layers == 2) {
     if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
     if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
-    if (params->entropy_fix) return SWE_ERR_UNSUPPORTED;
   }
   return SWE_OK;
 }

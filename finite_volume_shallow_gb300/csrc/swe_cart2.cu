@@ -108,8 +108,8 @@ __device__ __forceinline__ Side2<T> side_of(const T (*c)[TY + 2][TX + 2], int lj
 }
 
 // FUSED: the cart2_step_kernel form (U carries the previous step's update);
-// otherwise U is unused.
-template <typename T, bool ANISO, bool FUSED>
+// otherwise U is unused.  EFIX: the entropy fix of edge2.
+template <typename T, bool ANISO, bool FUSED, bool EFIX>
 __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Args<T>& U) {
   constexpr int TY = Tile2Y<T>::v;
   __shared__ T cq[NCQ][TY + 2][TX + 2];
@@ -175,7 +175,7 @@ __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Ar
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T, kAdapt2<T>>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, kAdapt2<T>, EFIX>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ex[q][row][e] = out[q];
   }
@@ -192,7 +192,7 @@ __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Ar
     if (lw) mirror2(a, b);
     if (rw) mirror2(b, a);
     T out[NEQ];
-    hyper_ok &= edge2<T, kAdapt2<T>>(a, b, g, gh, r, lw || rw, out);
+    hyper_ok &= edge2<T, kAdapt2<T>, EFIX>(a, b, g, gh, r, lw || rw, out);
 #pragma unroll
     for (int q = 0; q < NEQ; ++q) ey[q][e][col] = out[q];
   }
@@ -228,20 +228,21 @@ __device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Ar
 
 // Resident blocks per SM the registers are held to: five 256-thread fp32
 // tiles (48 registers) fit next to their 35 KB of shared memory each; fp64
-// tiles are bounded by shared memory and the FP64 pipe.
-template <typename T> struct MinBlocks2 { static constexpr int v = 1; };
-template <> struct MinBlocks2<float> { static constexpr int v = 5; };
+// tiles are bounded by shared memory and the FP64 pipe; the entropy-fix
+// variants (two more root solves per edge) are left to the compiler.
+template <typename T, bool EFIX> struct MinBlocks2 { static constexpr int v = 1; };
+template <> struct MinBlocks2<float, false> { static constexpr int v = 5; };
 
-template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T>::v)
+template <typename T, bool ANISO, bool EFIX>
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T, EFIX>::v)
     cart2_flux_kernel(const Step2Args<T> A) {
-  flux_tile<T, ANISO, false>(A, Update2Args<T>{});
+  flux_tile<T, ANISO, false, EFIX>(A, Update2Args<T>{});
 }
 
-template <typename T, bool ANISO>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T>::v)
+template <typename T, bool ANISO, bool EFIX>
+__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T, EFIX>::v)
     cart2_step_kernel(const Step2Args<T> A, const Update2Args<T> U) {
-  flux_tile<T, ANISO, true>(A, U);
+  flux_tile<T, ANISO, true, EFIX>(A, U);
 }
 
 template <typename T>
@@ -313,8 +314,11 @@ cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st) {
   constexpr int TY = Tile2Y<T>::v;
   dim3 block(TX, TY);
   dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
-  return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false>, grid, block, 0, st, f)
-                       : launch_pdl(cart2_flux_kernel<T, true>, grid, block, 0, st, f);
+  if (f.efix)
+    return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false, true>, grid, block, 0, st, f)
+                         : launch_pdl(cart2_flux_kernel<T, true, true>, grid, block, 0, st, f);
+  return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false, false>, grid, block, 0, st, f)
+                       : launch_pdl(cart2_flux_kernel<T, true, false>, grid, block, 0, st, f);
 }
 
 template <typename T>
@@ -322,8 +326,12 @@ cudaError_t launch_fused2(const Step2Args<T>& f, const Update2Args<T>& u, cudaSt
   constexpr int TY = Tile2Y<T>::v;
   dim3 block(TX, TY);
   dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
-  return f.rho == T(1) ? launch_pdl(cart2_step_kernel<T, false>, grid, block, 0, st, f, u)
-                       : launch_pdl(cart2_step_kernel<T, true>, grid, block, 0, st, f, u);
+  if (f.efix)
+    return f.rho == T(1)
+               ? launch_pdl(cart2_step_kernel<T, false, true>, grid, block, 0, st, f, u)
+               : launch_pdl(cart2_step_kernel<T, true, true>, grid, block, 0, st, f, u);
+  return f.rho == T(1) ? launch_pdl(cart2_step_kernel<T, false, false>, grid, block, 0, st, f, u)
+                       : launch_pdl(cart2_step_kernel<T, true, false>, grid, block, 0, st, f, u);
 }
 
 template <typename T>

@@ -107,6 +107,7 @@ struct Step2Args {
   T g, r, rho;     // gravity, density ratio, dx / dy
   void* tmax_out;  // max over cells of sum_x D + rho sum_y D (must start at 0)
   unsigned* err;
+  int efix;        // 1: the Harten-Hyman entropy fix
 };
 // The update W_out = W_in - (dt/dx) R of step `step`, dt from the wave-speed
 // maximum in tmax_in.  cart2_update_kernel reads win and writes w (the same
@@ -181,7 +182,7 @@ struct MeshStepArgs {
   T g, r;
   void* tmax_out;         // max over cells of sum L max|lambda| / |V_i| (starts at 0)
   unsigned* err;
-  int efix;               // one layer: 1 for the Harten-Hyman entropy fix
+  int efix;               // 1: the Harten-Hyman entropy fix
 };
 template <typename T>
 struct MeshUpdateArgs {

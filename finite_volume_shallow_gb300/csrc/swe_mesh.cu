@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
       if (wall) mirror2(sb, sa);
       else sb = load_side2(A, b, ex, ey);
       T out[NEQ];
-      ok = edge2<T, true>(sa, sb, A.g, gh, A.r, wall, out);
+      ok = edge2<T, true, EFIX>(sa, sb, A.g, gh, A.r, wall, out);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const T m = out[k ? E_M2 : E_M1];
@@ -581,7 +581,10 @@ cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& 
   };
   mark(0);
   cudaError_t e;
-  if (n_layers == 2) {
+  if (n_layers == 2 && f.efix) {
+    // with the entropy fix both precisions take the one-edge-per-thread form
+    e = launch_pdl(mesh_edge_kernel<T, 2, true>, ge, kEdgeThreads, 0, st, f);
+  } else if (n_layers == 2) {
     if constexpr (sizeof(T) == 4) {
       const unsigned gp = grid_1d((f.nedges + 1) / 2, kPairThreads, INT32_MAX);
       e = launch_pdl(mesh_edge2_pair_kernel, gp, kPairThreads, 0, st, f);

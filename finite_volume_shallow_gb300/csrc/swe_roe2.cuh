@@ -115,35 +115,19 @@ struct Quartic {
   }
 };
 
-// IR-Roe flux of one edge, two layers.  Writes the edge results; returns
-// false when A_ij has a complex pair of eigenvalues.  ADAPT: stop the outer
-// Newton iteration early (warp vote) instead of running the fixed count.
-template <typename T, bool ADAPT = false>
-__device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
-                                      bool wall, T* out) {
-  // Roe averages per layer: sqrt(h)-weighted normal velocity, arithmetic
-  // depth; c_k^2 = g hbar_k
-  T un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const T va = a.qn[k] * a.rs[k], vb = b.qn[k] * b.rs[k];
-    un[k] = (va + vb) * M2<T>::rcp(a.s[k] + b.s[k]);
-    cs[k] = gh * (a.h[k] + b.h[k]);
-    const T iha = a.rs[k] * a.rs[k], ihb = b.rs[k] * b.rs[k];
-    qu_a[k] = a.qn[k] * a.qn[k] * iha;
-    qu_b[k] = b.qn[k] * b.qn[k] * ihb;
-    ut_a[k] = a.qt[k] * iha;
-    ut_b[k] = b.qt[k] * ihb;
-  }
-  Quartic<T> q{un[0], un[1], cs[0], cs[1], r * cs[0] * cs[1]};
-  const T c1 = M2<T>::sqa(cs[0]), c2 = M2<T>::sqa(cs[1]);
-  const T sc = M2<T>::sqa(cs[0] + cs[1]);
+// The four roots of p, in increasing order; false when the inner pair is
+// complex (loss of hyperbolicity).  ADAPT: stop the outer Newton iteration
+// early (warp vote) instead of running the fixed count.
+template <typename T, bool ADAPT>
+__device__ __forceinline__ bool quartic_roots(const Quartic<T>& q, T lam[4]) {
+  const T c1 = M2<T>::sqa(q.c1s), c2 = M2<T>::sqa(q.c2s);
+  const T sc = M2<T>::sqa(q.c1s + q.c2s);
   // outer roots: from below / above, where p > 0, p convex and monotone
   // (the approximate square roots widened by 2^-12, far more than their
   // error, so the starts stay outside)
   const T kr2 = T(1.4142135623730951 * (1.0 + 1.0 / 4096)), ks = T(1.0 + 1.0 / 4096);
-  T l1 = fmax(fmin(un[0] - kr2 * c1, un[1] - kr2 * c2), fmin(un[0], un[1]) - ks * sc);
-  T l4 = fmin(fmax(un[0] + kr2 * c1, un[1] + kr2 * c2), fmax(un[0], un[1]) + ks * sc);
+  T l1 = fmax(fmin(q.u1 - kr2 * c1, q.u2 - kr2 * c2), fmin(q.u1, q.u2) - ks * sc);
+  T l4 = fmin(fmax(q.u1 + kr2 * c1, q.u2 + kr2 * c2), fmax(q.u1, q.u2) + ks * sc);
   const T tol = Iters<T>::tol * fmax(c1, c2);
   const unsigned act = ADAPT ? __activemask() : 0u;
   // ADAPT: an edge keeps its roots once its own step fell below tol (so the
@@ -164,8 +148,8 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     }
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
-  const T p3 = T(-2) * (un[0] + un[1]);
-  const T p2 = (un[0] * un[0] - cs[0]) + (un[1] * un[1] - cs[1]) + T(4) * un[0] * un[1];
+  const T p3 = T(-2) * (q.u1 + q.u2);
+  const T p2 = (q.u1 * q.u1 - q.c1s) + (q.u2 * q.u2 - q.c2s) + T(4) * q.u1 * q.u2;
   const T ss = l1 + l4, pp = l1 * l4;
   const T bb = p3 + ss;
   const T cc = p2 + ss * bb - pp;
@@ -182,6 +166,54 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     l2 -= fmin(fmax(q.p(l2) * M2<T>::rcp(q.dp(l2)), -lim), lim);
     l3 -= fmin(fmax(q.p(l3) * M2<T>::rcp(q.dp(l3)), -lim), lim);
   }
+  lam[0] = l1;
+  lam[1] = l2;
+  lam[2] = l3;
+  lam[3] = l4;
+  return hyper;
+}
+
+// The quartic of a side's own Jacobian A(W) (the same system with the side's
+// normal velocities and c_k^2 = g h_k): its roots are the speeds
+// lambda_k(W) of the entropy fix.
+template <typename T>
+__device__ __forceinline__ Quartic<T> side_quartic(const Side2<T>& a, T g, T r) {
+  const T c1s = g * a.h[0], c2s = g * a.h[1];
+  return Quartic<T>{a.qn[0] * (a.rs[0] * a.rs[0]), a.qn[1] * (a.rs[1] * a.rs[1]), c1s, c2s,
+                    r * c1s * c2s};
+}
+
+// IR-Roe flux of one edge, two layers.  Writes the edge results; returns
+// false when A_ij has a complex pair of eigenvalues.  ADAPT: early exit of
+// the Newton iterations (quartic_roots).  EFIX: the Harten-Hyman entropy fix
+// ([P1] Sec. 2.2, after eq. (5)) as numerical viscosity along each of the
+// four waves: delta_k = max(0, l_k - l_k(W_i), l_k(W_j) - l_k) with l_k(W)
+// the k-th root of the side's own quartic; where |l_k| < delta_k, Phi^-
+// gains (|l_k| - |l_k|_d) beta_k K_k / 2, |l_k|_d = (l_k^2 + delta_k^2) /
+// (2 delta_k), beta = K^-1 (W_j - W_i) from the left eigenvectors; side b's
+// fluctuation P^+ d loses the same term.  A side whose own system is not
+// hyperbolic is reported like A_ij.
+template <typename T, bool ADAPT = false, bool EFIX = false>
+__device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g, T gh, T r,
+                                      bool wall, T* out) {
+  // Roe averages per layer: sqrt(h)-weighted normal velocity, arithmetic
+  // depth; c_k^2 = g hbar_k
+  T un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const T va = a.qn[k] * a.rs[k], vb = b.qn[k] * b.rs[k];
+    un[k] = (va + vb) * M2<T>::rcp(a.s[k] + b.s[k]);
+    cs[k] = gh * (a.h[k] + b.h[k]);
+    const T iha = a.rs[k] * a.rs[k], ihb = b.rs[k] * b.rs[k];
+    qu_a[k] = a.qn[k] * a.qn[k] * iha;
+    qu_b[k] = b.qn[k] * b.qn[k] * ihb;
+    ut_a[k] = a.qt[k] * iha;
+    ut_b[k] = b.qt[k] * ihb;
+  }
+  Quartic<T> q{un[0], un[1], cs[0], cs[1], r * cs[0] * cs[1]};
+  T lam[4];
+  bool hyper = quartic_roots<T, ADAPT>(q, lam);
+  const T l1 = lam[0], l4 = lam[3];
   // fluctuation d = F_1(W_j) - F_1(W_i) - B_ij (W_j - W_i) - S_ij (H_j - H_i)
   // (pressure differences written g hbar_k (h_k,j - h_k,i))
   const T dh1 = b.h[0] - a.h[0], dh2 = b.h[1] - a.h[1], dH = b.H - a.H;
@@ -189,8 +221,13 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
   const T d2 = (qu_b[0] - qu_a[0]) + cs[0] * ((dh1 + dh2) - dH);
   const T d3 = b.qn[1] - a.qn[1];
   const T d4 = (qu_b[1] - qu_a[1]) + cs[1] * ((dh2 + r * dh1) - dH);
-  // P^- d = sum_k w_k alpha_k K_k
-  const T lam[4] = {l1, l2, l3, l4};
+  // entropy fix: each side's own speeds
+  T la[4], lb[4];
+  if (EFIX) {
+    hyper &= quartic_roots<T, ADAPT>(side_quartic(a, g, r), la);
+    hyper &= quartic_roots<T, ADAPT>(side_quartic(b, g, r), lb);
+  }
+  // P^- d = sum_k w_k alpha_k K_k (+ the fix's nu_k K_k)
   const T ic1s = M2<T>::rcp(cs[0]);
   T pd0 = T(0), pd1 = T(0), pd2 = T(0), pd3 = T(0);
 #pragma unroll
@@ -199,7 +236,17 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     const T w = (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
     const T Q1 = q.q1(l), Q2 = q.q2(l);
     const T num = Q2 * ((l - T(2) * un[0]) * d1 + d2) + cs[0] * ((l - T(2) * un[1]) * d3 + d4);
-    const T alpha = w * num * M2<T>::rcp(q.dp(l));
+    const T rdp = M2<T>::rcp(q.dp(l));
+    T alpha = w * num * rdp;
+    if (EFIX) {
+      const T del = fmax(T(0), fmax(l - la[k], lb[k] - l));
+      const T al = fabs(l);
+      if (al < del) {
+        // beta_k: the left eigenvector applied to the state jump
+        const T nb = Q2 * ((l - T(2) * un[0]) * dh1 + d1) + cs[0] * ((l - T(2) * un[1]) * dh2 + d3);
+        alpha += T(0.5) * (al - (l * l + del * del) * M2<T>::rcp(del + del)) * (nb * rdp);
+      }
+    }
     const T mu = Q1 * ic1s;
     pd0 += alpha;
     pd1 += alpha * l;

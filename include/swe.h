@@ -107,16 +107,20 @@ typedef struct {
  *  cfl        gamma of eq. (5), 0 < cfl <= 1, used by swe_run
  *  stream     cudaStream_t the handle orders its work on; NULL = legacy
  *             default stream
- *  entropy_fix  0: P^- of [P1] Sec. 2.2 as printed; 1 (one layer only): the
- *             Harten-Hyman entropy fix that [P1] Sec. 2.2 (after eq. (5))
- *             names for sonic rarefactions.  Per characteristic speed
- *             lambda_k of the Roe matrix, delta_k = max(0, lambda_k -
- *             lambda_k(W_i), lambda_k(W_j) - lambda_k); where |lambda_k| <
+ *  entropy_fix  0: P^- of [P1] Sec. 2.2 as printed; 1: the Harten-Hyman
+ *             entropy fix that [P1] Sec. 2.2 (after eq. (5)) names for
+ *             sonic rarefactions.  Per characteristic speed lambda_k of the
+ *             Roe matrix, delta_k = max(0, lambda_k - lambda_k(W_i),
+ *             lambda_k(W_j) - lambda_k), lambda_k(W) the k-th eigenvalue of
+ *             the Jacobian of the side's own state (u_eta -+ sqrt(g h) for
+ *             one layer; the k-th root of the same quartic with the side's
+ *             own velocities and depths for two); where |lambda_k| <
  *             delta_k the scheme uses (lambda_k^2 + delta_k^2) / (2 delta_k)
  *             in place of |lambda_k|, i.e. Phi^- gains
  *             (|lambda_k| - |lambda_k|_d) beta_k K_k / 2 with beta = K^-1
- *             (W_j - W_i).  1 with two layers returns SWE_ERR_UNSUPPORTED;
- *             any value other than 0 or 1 returns SWE_ERR_ARG. */
+ *             (W_j - W_i).  Two layers: a side state whose own system is
+ *             not hyperbolic is reported as SWE_ERR_HYPERBOLIC.  Any value
+ *             other than 0 or 1 returns SWE_ERR_ARG. */
 typedef struct {
   int32_t n_layers;
   int32_t precision;

@@ -88,7 +88,8 @@ def gpu_create2(d, precision, stream=None):
     return S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(dt),
                              [f.astype(dt) for f in I.fields2_of(d)], precision=precision,
                              g=d.get("g", 9.81), cfl=d.get("cfl", 0.9), stream=stream,
-                             n_layers=2, pollutant=0, r=d["r"])
+                             n_layers=2, pollutant=0, r=d["r"],
+                             entropy_fix=d.get("entropy_fix", 0))
 
 
 def gpu_run2(d, precision, nsteps):
@@ -102,8 +103,9 @@ def gpu_run2(d, precision, nsteps):
 
 def oracle_run2(d, precision, nsteps):
     dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
-    W, dts, st = O.grid_run2(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields2_of(dr),
-                             d.get("g", 9.81), d["r"], d.get("cfl", 0.9), nsteps)
+    with O.entropy_fix(d.get("entropy_fix", 0)):
+        W, dts, st = O.grid_run2(d["nx"], d["ny"], d["dx"], d["dy"], dr["H"], I.fields2_of(dr),
+                                 d.get("g", 9.81), d["r"], d.get("cfl", 0.9), nsteps)
     assert st == O.OM_OK, st
     return W, dts
 
@@ -157,8 +159,9 @@ def oracle_run_mesh(d, precision, nsteps):
     dr = I.rounded(d, np_dtype(precision)) if precision == 32 else d
     m = O.tri_mesh(d["xy"], d["tri"])
     if d["n_layers"] == 2:
-        W, dts, st = O.run2(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d["r"],
-                            d.get("cfl", 0.9), nsteps)
+        with O.entropy_fix(d.get("entropy_fix", 0)):
+            W, dts, st = O.run2(m, dr["H"], mesh_fields(dr), d.get("g", 9.81), d["r"],
+                                d.get("cfl", 0.9), nsteps)
     else:
         with O.entropy_fix(d.get("entropy_fix", 0)):
             W, dts, st, _ = O.run1(m, dr["H"], mesh_fields(dr), d.get("g", 9.81),

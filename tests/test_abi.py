@@ -91,7 +91,7 @@ def _create(lib, grid, params, n=12, with_fields=True):
     (_grid(), _params(pollutant=0), S.SWE_ERR_UNSUPPORTED),
     (_grid(), _params(entropy_fix=2), S.SWE_ERR_ARG),
     (_grid(), _params(entropy_fix=-1), S.SWE_ERR_ARG),
-    (_grid(), _params(n_layers=2, pollutant=0, r=0.5, entropy_fix=1), S.SWE_ERR_UNSUPPORTED),
+    (_grid(), _params(n_layers=2, pollutant=0, r=0.5, entropy_fix=2), S.SWE_ERR_ARG),
 ])
 def test_create_rejects_bad_arguments(lib, grid, params, expect):
     st, out = _create(lib, grid, params)

@@ -1,6 +1,6 @@
-"""Parity of the one-layer step with the Harten-Hyman entropy fix switched on
+"""Parity of the step with the Harten-Hyman entropy fix switched on
 (swe_params.entropy_fix = 1) against the oracle with its fix switched on, on
-flows that have sonic points: a transonic dam break (h_r / h_l = 0.05, the
+flows that have sonic points.  One layer: a transonic dam break (h_r / h_l = 0.05, the
 fan crosses the critical speed at the dam), a strong radial dam break on a
 grid and on triangles, and supercritical flow leaving a wall (the mirror
 ghost then makes the fix act on the wall edges).  Tolerances as in the other parity
@@ -12,8 +12,8 @@ import pytest
 
 from finite_volume_shallow_gb300 import inputs as I
 from finite_volume_shallow_gb300 import swe as S
-from gpu_util import (TOL, assert_parity, assert_parity_mesh, gpu_create, gpu_run, np_dtype,
-                      rel_errors)
+from gpu_util import (TOL, assert_parity, assert_parity2, assert_parity_mesh, gpu_create,
+                      gpu_run, gpu_run2, np_dtype, rel_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +128,49 @@ def test_fix_through_the_no_alloc_entry_point(precision):
     for k in ("h", "qx", "qy", "hC"):
         assert errs[k] <= TOL[precision][k], errs
     assert np.abs(dts / dts_ref - 1.0).max() <= TOL[precision]["dt"]
+
+
+# ---- two layers: a transonic dam break in the lower layer under a thick
+# upper layer with a flat surface (the fix acts on the lower layer's waves) --
+def _two_layer_dam(d, r, upper=60.0):
+    h2 = d["h"]
+    z = np.zeros(h2.size)
+    out = dict(nx=d["nx"], ny=d["ny"], dx=d["dx"], dy=d["dy"], H=d["H"], r=r, n_layers=2,
+               g=9.81, cfl=0.9, entropy_fix=1)
+    for k, v in (("h1", upper - h2), ("q1x", z), ("q1y", z), ("h2", h2), ("q2x", z),
+                 ("q2y", z)):
+        out[k] = np.ascontiguousarray(v, dtype=np.float64)
+    return out
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_two_layer_transonic_dam_break(precision):
+    d = _two_layer_dam(I.dam_break_1d(160, ny=6, h_left=10.0, h_right=0.5), r=0.3)
+    assert_parity2(d, precision, 60)
+
+
+def test_two_layer_fix_changes_the_solution():
+    d = _two_layer_dam(I.dam_break_1d(160, ny=6, h_left=10.0, h_right=0.5), r=0.3)
+    Wf, _, _ = gpu_run2(d, 64, 60)
+    Wp, _, _ = gpu_run2(dict(d, entropy_fix=0), 64, 60)
+    assert np.abs(Wf[3] - Wp[3]).max() > 0.1
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_two_layer_radial_dam_break_on_anisotropic_cells(precision):
+    d = _two_layer_dam(I.circular_dam(60, 40, dx=5.0, dy=8.0, radius=70.0, h_in=10.0,
+                                      h_out=0.5), r=0.5, upper=30.0)
+    assert_parity2(d, precision, 40)
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_two_layer_dam_break_on_triangles(precision):
+    xy, tri = I.square_tri_mesh(40, 30, jitter=0.2, seed=78)
+    c = I.tri_centroids(xy, tri)
+    inside = (c[:, 0] - 20.0) ** 2 + (c[:, 1] - 15.0) ** 2 < 8.0 ** 2
+    h2 = np.where(inside, 10.0, 0.5)
+    z = np.zeros_like(h2)
+    d = dict(xy=xy, tri=tri, n_cells=tri.shape[0], n_layers=2, mesh=True, g=9.81, cfl=0.9,
+             r=0.5, H=z, h1=30.0 - h2, q1x=z, q1y=z, h2=h2, q2x=z.copy(), q2y=z.copy(),
+             entropy_fix=1)
+    assert_parity_mesh(d, precision, 40)

@@ -167,7 +167,8 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
     H and the fields of W0 (h, qx, qy, hC; or h1, q1x, q1y, h2, q2x, q2y with
     n_layers=2, pollutant=0) are host arrays of the state's precision;
     ``stream`` is a cudaStream_t as an int (e.g.
-    ``torch.cuda.current_stream().cuda_stream``) or None."""
+    ``torch.cuda.current_stream().cuda_stream``) or None; ``entropy_fix=1``
+    switches on the Harten-Hyman entropy fix."""
     L = load()
     dt = _dtype(precision)
     n = int(nx) * int(ny)

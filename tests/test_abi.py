@@ -166,3 +166,21 @@ def test_two_layer_grid_height_limit(lib, precision, ny_ok):
         S.swe_create_grid(1, n, 10.0, 10.0, H, W, precision=precision, n_layers=2,
                           pollutant=0, r=0.98)
     assert e.value.status == S.SWE_ERR_ARG
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch):
+    # the binding never falls back to anything else when libswe is absent
+    monkeypatch.setattr(B, "LIB", os.path.join(ROOT, "no_such_dir", "libswe.so"))
+    monkeypatch.setattr(S, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        S.load(build_if_needed=False)
+
+
+def test_valid_create_without_a_gpu_is_a_cuda_error(lib):
+    # no CPU path: on a machine without a GPU a valid request fails with
+    # SWE_ERR_CUDA instead of computing anything
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, out = _create(lib, _grid(), _params())
+    assert st == S.SWE_ERR_CUDA and out is None

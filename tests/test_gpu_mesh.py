@@ -249,3 +249,10 @@ def test_full_size_triangle_workload(precision):
     for k in (0, 3):
         w0 = d[I.TWO_LAYER_FIELDS[k]].astype(np_dtype(precision)).astype(np.float64)
         assert abs(Wk1[k].astype(np.float64).dot(area) - w0.dot(area)) / w0.dot(area) <= 2e-6
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_cfl_limit_on_triangles(precision):
+    d = I.tri_workload1(30, 20, seed=41)
+    d["cfl"] = 1.0
+    assert_parity_mesh(d, precision, 40)

@@ -73,3 +73,11 @@ def test_low_cfl():
     d = I.make_workload("pulses8192", nx=140, ny=60)
     d["cfl"] = 0.25
     assert_parity(d, 64, 40)
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_cfl_limit(precision):
+    # gamma = 1, the largest value eq. (5) allows
+    d = I.make_workload("pulses8192", nx=140, ny=60)
+    d["cfl"] = 1.0
+    assert_parity(d, precision, 60)

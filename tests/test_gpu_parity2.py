@@ -183,3 +183,10 @@ def test_two_layer_arguments():
     with pytest.raises(S.SweError) as e:
         gpu_create2(bad, 64)
     assert e.value.status == S.SWE_ERR_ARG
+
+
+@pytest.mark.parametrize("precision", [64, 32])
+def test_cfl_limit_two_layers(precision):
+    d = I.two_layer_hills(53, 41, umax=0.05, bump=0.5)
+    d["cfl"] = 1.0
+    assert_parity2(d, precision, 30)

@@ -428,3 +428,19 @@ def test_entropy_fix_conserves_mass_and_pollutant():
     # and it changed the flow (sonic points were crossed)
     Wp, _, _, _ = O.run1(mesh, d["H"], W0, G, 0.9, 60)
     assert np.abs(W[0] - Wp[0]).max() > 1e-3
+
+
+# ---- the CFL limit ----------------------------------------------------------
+@pytest.mark.parametrize("hl,hr,fix", [(2.0, 1.0, False), (10.0, 0.5, True)])
+def test_stable_at_the_cfl_limit(hl, hr, fix):
+    # eq. (5) allows gamma up to 1: at gamma = 1 the dam breaks stay within
+    # the range of their initial depths (no over- or undershoot) and conserve
+    # mass over 300 steps, before any wave reaches a wall
+    d = I.dam_break_1d(400, h_left=hl, h_right=hr)
+    with O.entropy_fix(fix):
+        W, dts, st = O.grid_run1(400, 4, d["dx"], d["dy"], d["H"], I.fields_of(d), G, 1.0, 300)
+    assert st == O.OM_OK
+    h = W[0]
+    assert h.min() >= hr * (1 - 1e-12) and h.max() <= hl * (1 + 1e-12)
+    assert abs(h.sum() - d["h"].sum()) <= 1e-12 * d["h"].sum()
+    assert dts.sum() * math.sqrt(G * hl) < 1000.0   # the fan has not reached the wall

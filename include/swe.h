@@ -281,8 +281,11 @@ swe_status swe_get_timing(const swe_state *s, swe_kernel_time *out, int32_t max,
  * swe_run on buffers the caller owns, and allocates nothing: no cudaMalloc,
  * no cudaFree, no allocating library routine.
  *
- *  grid, params  as for swe_create_grid (params.cfl is used for every step;
- *                params.stream orders all work)
+ *  grid, params  as for swe_create_grid, one layer with pollutant only
+ *                (n_layers = 1, pollutant = 1, else SWE_ERR_UNSUPPORTED);
+ *                params.cfl is used for every step, params.entropy_fix
+ *                selects the step with the entropy fix, params.stream
+ *                orders all work
  *  H             device, the bottom depth in the padded layout below
  *  W_a           4 device pointers (h, qx, qy, hC), padded layout: the state
  *                to advance on input, the state after nsteps steps on output

@@ -11,7 +11,9 @@
 //
 // g_noalloc_scratch is a host-side stand-in in host code: its device address
 // is obtained once per device with cudaGetSymbolAddress and passed to the
-// kernels.  It is held by every GPU that loads the library until exit.
+// kernels.  CUDA loads device code lazily, so the array is reserved on a
+// device by the first call there (which also does that look-up) and held
+// until the process exits.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

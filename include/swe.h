@@ -281,8 +281,9 @@ swe_status swe_get_timing(const swe_state *s, swe_kernel_time *out, int32_t max,
  * swe_run on buffers the caller owns, and allocates nothing: no cudaMalloc,
  * no cudaFree, no allocating library routine.
  *
- *  grid, params  as for swe_create_grid, one layer with pollutant only
- *                (n_layers = 1, pollutant = 1, else SWE_ERR_UNSUPPORTED);
+ *  grid, params  as for swe_create_grid, one layer with pollutant only:
+ *                n_layers = 2 or pollutant != 1 gives SWE_ERR_UNSUPPORTED,
+ *                any other n_layers than 1 or 2 gives SWE_ERR_ARG;
  *                params.cfl is used for every step, params.entropy_fix
  *                selects the step with the entropy fix, params.stream
  *                orders all work
@@ -299,13 +300,17 @@ swe_status swe_get_timing(const swe_state *s, swe_kernel_time *out, int32_t max,
  * (j + 2) * pitch + (i + 2).  The padding may hold anything; it is read but
  * never affects a result and never written.
  * The scratch (wave-speed maxima, error word, clock and the dt of at most
- * SWE_NOALLOC_MAX_STEPS steps, about 8 KB) is one static device array per
- * GPU, held from library load until exit.  Every call clears the parts that
- * must start at zero; all calls share the array, so calls that overlap on the
- * GPU (other streams, other threads) race and must be serialised.  The first
- * call on a device also looks up the array's device address and sets the
- * step kernel's launch attributes; make that first call before any stream
- * capture.  The call waits for its stream before returning.
+ * SWE_NOALLOC_MAX_STEPS steps, about 8.4 KB) is one static device array per
+ * GPU, held until the process exits.  CUDA loads a library's device code
+ * lazily, so that array is reserved on a device by the first call there,
+ * which also looks up the array's device address and sets the step kernel's
+ * launch attributes.  A caller whose pool will claim nearly all of a device's
+ * memory should make that first call -- a call with nsteps = 0 does -- before
+ * the pool does; it should also make it before any stream capture starts on
+ * that device.  Every call clears the parts of the array that must start at
+ * zero; all calls share the array, so calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised.  The call waits for
+ * its stream before returning.
  * Errors: SWE_ERR_ARG (bad argument, nsteps beyond SWE_NOALLOC_MAX_STEPS,
  * pitch too small, unaligned buffer); SWE_ERR_DEPTH / SWE_ERR_NONFINITE for
  * an invalid input state or one that appears (not sticky: nothing persists

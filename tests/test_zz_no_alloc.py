@@ -1,4 +1,5 @@
-"""swe_run_noalloc, the allocation-free entry point, against the handle API.
+"""swe_run_noalloc, the allocation-free entry point, against the handle API
+and the oracle.
 
 Some callers cannot allocate device memory once they are running (a framework
 whose pool already owns the GPU's memory, a real-time loop that forbids
@@ -6,15 +7,20 @@ allocation); swe_run_noalloc runs the same step on buffers they own and keeps
 its scratch in a static device array.  This test owns the buffers (torch
 allocates them here, not the entry point), fills their padding with NaN to
 show the padding never reaches a result, and checks two calls in a row against
-swe_create_grid + swe_run + swe_get_state on the same inputs, within the GPU
-parity tolerances.  It lives in the file pytest collects last.
+swe_create_grid + swe_run + swe_get_state on the same inputs.  Both paths run
+the same kernels with the same launch shape and the same order of wave-speed
+slots, and a call that starts from a state computes its first dt exactly as a
+running loop does, so the fields and the dt agree bit for bit.  The first call
+is also checked against the oracle within the GPU parity tolerances, and a
+warm call must leave the device's free memory unchanged.  It lives in the file
+pytest collects last.
 """
 import numpy as np
 import pytest
 
 from finite_volume_shallow_gb300 import inputs as I
 from finite_volume_shallow_gb300 import swe as S
-from gpu_util import TOL, gpu_create, np_dtype, rel_errors
+from gpu_util import TOL, gpu_create, np_dtype, oracle_run, rel_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -45,22 +51,35 @@ def test_noalloc_matches_handle_api(precision):
     Wb = [_padded(torch, None, nx, ny, pitch, tdt) for _ in range(4)]
     torch.cuda.synchronize()
 
+    def call(nsteps):
+        return S.swe_run_noalloc(nx, ny, d["dx"], d["dy"], H.data_ptr(),
+                                 [w.data_ptr() for w in Wa], [w.data_ptr() for w in Wb], pitch,
+                                 nsteps, precision=precision, g=d["g"], cfl=d["cfl"])
+
     ref = gpu_create(d, precision)
     start = [f.astype(np.float64) for f in I.fields_of(d)]
     for nsteps in (7, 12):  # two calls in a row: odd, then even step count
-        dts = S.swe_run_noalloc(nx, ny, d["dx"], d["dy"], H.data_ptr(),
-                                [w.data_ptr() for w in Wa], [w.data_ptr() for w in Wb], pitch,
-                                nsteps, precision=precision, g=d["g"], cfl=d["cfl"])
+        free_before = torch.cuda.mem_get_info()[0]
+        dts = call(nsteps)
+        torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
+        if nsteps == 12:  # a warm call: the entry point allocated nothing
+            assert free_after == free_before, (free_before, free_after)
         S.swe_run(ref, nsteps)
         W_ref, _ = S.swe_get_state(ref)
         dts_ref = S.swe_get_dt_history(ref, nsteps)
-        W = [_interior(w, nx, ny, pitch).astype(np.float64) for w in Wa]
-        errs = rel_errors(W, [w.astype(np.float64) for w in W_ref], start)
-        for k in ("h", "qx", "qy", "hC"):
-            assert errs[k] <= TOL[precision][k], (nsteps, errs)
+        W = [_interior(w, nx, ny, pitch) for w in Wa]
         assert len(dts) == nsteps
-        assert np.abs(dts / dts_ref - 1.0).max() <= TOL[precision]["dt"]
+        assert np.array_equal(dts, dts_ref), (nsteps, dts, dts_ref)
+        for k, (a, b) in enumerate(zip(W, W_ref)):
+            assert np.array_equal(a, b), (nsteps, k, np.abs(a.astype(float) - b).max())
         assert all(np.isfinite(w).all() for w in W)
+        if nsteps == 7:  # independent of the handle: the oracle on the same inputs
+            Wo, dto = oracle_run(d, precision, nsteps)
+            errs = rel_errors([w.astype(np.float64) for w in W], Wo, start)
+            for k in ("h", "qx", "qy", "hC"):
+                assert errs[k] <= TOL[precision][k], errs
+            assert np.abs(dts / dto - 1.0).max() <= TOL[precision]["dt"]
     S.swe_destroy(ref)
 
 

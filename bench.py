@@ -53,14 +53,24 @@ BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC writt
 # converged: on the interface dam break and the triangle workload it takes
 # 2.01 iterations per edge in fp32 and 3.01 in fp64 (counted on the GPU with
 # an instrumented build); the inner one runs 2.
-FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2, 64: 213 + 28 * 3.01 + 28 * 2}
+# In fp64 each reciprocal is a hardware seed refined by two Newton steps of
+# two FMAs each (8 flops, counted): per edge 2 for the Roe velocities, 2 per
+# outer and 2 per inner iteration, 1 for 1/c1^2 and 1 per wave; in fp32 they
+# are single MUFU instructions (not counted).
+RCP_FLOPS_FP64 = 8
+RCP_PER_EDGE_2L_FP64 = 2 + 2 * 3.01 + 2 * 2 + 1 + 4
+FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2,
+                     64: 213 + 28 * 3.01 + 28 * 2 + RCP_FLOPS_FP64 * RCP_PER_EDGE_2L_FP64}
 # Per cell-update on a grid: two edges (each edge once; the tiles' halo
 # recomputation not counted) plus 25 for the per-cell quantities and the
 # residual sums.
 FLOPS_PER_CELL_2L = {p: 2 * FLOPS_PER_EDGE_2L[p] + 25 for p in (32, 64)}
-# FP32 FMA peak of a GB300: 152 SMs x 128 lanes x 2 flops x 2.07 GHz;
-# FP64: the nominal 1.25 TFLOP/s of the part.
-ALU_PEAK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
+# The ALU peaks are measured in every run by libswe's FMA probe
+# (swe_probe_fma_rate: independent FFMA / packed FFMA2 / DFMA chains over a
+# full wave, CUDA events); these data-sheet figures are used only if the
+# probe fails: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz, and the part's
+# nominal 1.25 TFLOP/s FP64.
+ALU_PEAK_FALLBACK_TFLOPS = {32: 152 * 128 * 2 * 2.07e9 / 1e12, 64: 1.25}
 DTYPE_NAME = {32: "f32", 64: "f64"}
 CSRC = os.path.join(ROOT, "finite_volume_shallow_gb300", "csrc")
 # kernel -> (sources whose concatenation's hash keys its traffic record,
@@ -96,14 +106,18 @@ def source_hash(files):
 # the edge-length scaling; one layer 88 (in fp32 the one-layer edge kernel
 # is modelled by its bytes instead: its arithmetic is light).
 FLOPS_PER_EDGE_MESH = {(2, 32): 213 + 28 * 2.0 + 28 * 2 + 79,
-                       (2, 64): 213 + 28 * 3.0 + 28 * 2 + 79, (1, 64): 88}
+                       (2, 64): 213 + 28 * 3.0 + 28 * 2 + 79
+                       + RCP_FLOPS_FP64 * (2 + 2 * 3.0 + 2 * 2 + 1 + 4),
+                       (1, 64): 88 + RCP_FLOPS_FP64 * 2}
 # One layer on a grid: floating-point operations per cell-update of the
 # fused step, counted from its formulas (FMA = 2; the 10 reciprocals and
 # reciprocal square roots per cell not counted): 36 per edge flux pair in the
 # Roe head, 10 in its tail, 18 for the per-cell quantities, 40 for the next
 # step's wave speeds, 34 for accumulation, update and checks -> 200 per two
-# cells.  The fp32 step is bound by HBM; the fp64 one by GB300's FP64 pipe.
-FLOPS_PER_CELL_1L = 100
+# cells; in fp64 the 4 reciprocals per cell are Newton-refined (8 flops each,
+# counted; the 6 reciprocal square roots are CUDA's rsqrt, not counted).
+# The fp32 step is bound by HBM; the fp64 one by GB300's FP64 pipe.
+FLOPS_PER_CELL_1L = 100 + 4 * RCP_FLOPS_FP64
 
 DESCR = {
     "pulses8192": "8192x8192 Cartesian, dx=10 m, 128 seeded Gaussian hills, 16 surface pulses, "
@@ -154,8 +168,40 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
     raise KeyError(kernel)
 
 
-def alu_peak_tflops(precision):
-    return ALU_PEAK_TFLOPS[precision]
+def measure_alu_peaks(S, stream=None, target_ms=100.0):
+    """FMA throughput of this GPU, measured now by libswe's probe: FP32 (the
+    faster of scalar and packed-pair FMAs) and FP64, in TFLOP/s."""
+    out = {}
+    try:
+        ffma, _ = S.swe_probe_fma_rate(S.PROBE_FFMA, target_ms, stream)
+        ffma2, _ = S.swe_probe_fma_rate(S.PROBE_FFMA2, target_ms, stream)
+        dfma, _ = S.swe_probe_fma_rate(S.PROBE_DFMA, target_ms, stream)
+        out = {32: max(ffma, ffma2) / 1e12, 64: dfma / 1e12, "ffma_tflops": ffma / 1e12,
+               "ffma2_tflops": ffma2 / 1e12, "dfma_tflops": dfma / 1e12,
+               "source": "measured in this run (swe_probe_fma_rate, CUDA events)"}
+    except Exception as e:  # reported, never silent
+        out = {32: ALU_PEAK_FALLBACK_TFLOPS[32], 64: ALU_PEAK_FALLBACK_TFLOPS[64],
+               "source": f"fallback (data sheet): probe failed: {e}"}
+    return out
+
+
+def host_cpu_info():
+    """What the oracle's baseline ran on: the host's core count and model."""
+    info = {"os_cpu_count": os.cpu_count()}
+    try:
+        info["nproc"] = int(subprocess.run(["nproc"], capture_output=True, text=True,
+                                           timeout=10).stdout.strip())
+    except Exception:
+        info["nproc"] = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() in ("Model name", "Architecture", "Vendor ID"):
+                info[k.strip().lower().replace(" ", "_")] = v.strip()
+    except Exception:
+        pass
+    return info
 
 
 def state_fields(I, d):
@@ -408,7 +454,9 @@ def cpu_baseline(d, budget_s=12.0):
     _, dts, st = smp.run(O, steps)
     el = time.perf_counter() - t0
     return {"value": smp.cells * steps / el / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{smp.what}, {steps} steps, fp64, single thread, {el:.1f} s"}
+            "sample": f"{smp.what}, {steps} steps, fp64, single thread, {el:.1f} s",
+            "cores_note": "cores = threads the oracle used; host lists the box's cores",
+            "host": host_cpu_info()}
 
 
 def run_reference(args, rank, world):
@@ -439,7 +487,7 @@ def run_reference(args, rank, world):
         "config": {"workload": workload_name(args, d, precision),
                    "cells": n_cells_of(d), "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "status": st,
     }
@@ -559,6 +607,7 @@ def main():
     S.swe_destroy(st)
 
     peak, peak_kind = load_peaks()
+    alu = measure_alu_peaks(S, stream.cuda_stream)
     kernels = {}
     ktimes = {k: v for k, v in ktimes.items() if v[0] > 0}
     for name, (launches, kms) in ktimes.items():
@@ -570,11 +619,10 @@ def main():
                              "frac": rate / 1e9 / peak, "peak_source": peak_kind,
                              "algorithmic_bytes_per_launch": amount}
         else:
-            pk = alu_peak_tflops(precision)
+            pk = alu[precision]
             kernels[name] = {"bound": "alu", "achieved": rate / 1e12, "peak": pk,
                              "unit": "TFLOP/s", "frac": rate / 1e12 / pk,
-                             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz "
-                                            "(fp32); the part's nominal FP64 rate (fp64)",
+                             "peak_source": alu["source"],
                              "algorithmic_flops_per_launch": amount}
         kernels[name].update({"kernel": name, "launches": launches, "ms_per_launch": avg,
                               "timing": "CUDA events between the kernels of each of K "
@@ -611,6 +659,7 @@ def main():
                        "launch": {"bands": info["bands"], "segments": info["segments"],
                                   "warps_per_block": info["warps_per_block"]}},
             "e2e": e2e, "roofline": roof, "cpu_baseline": base, "clocks": clocks,
+            "alu_peaks": {k: v for k, v in alu.items() if isinstance(k, str)},
             "gpu_launches": sum(v[0] for v in ktimes.values()),
         }
         print(json.dumps(line), flush=True)

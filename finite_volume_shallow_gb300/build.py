@@ -17,10 +17,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswe.so")
 SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_cart2.cu", "swe_mesh.cu", "swe_mesh_prep.cpp",
-           "swe_noalloc.cu"]
+           "swe_noalloc.cu", "swe_probe.cu"]
 HEADERS = [os.path.join(CSRC, "swe_internal.h"), os.path.join(CSRC, "swe_roe2.cuh"),
            os.path.join(CSRC, "swe_fastmath.cuh"), os.path.join(CSRC, "swe_plan.h"),
-           os.path.join(ROOT, "include", "swe.h")]
+           os.path.join(ROOT, "include", "swe.h"), os.path.join(ROOT, "include", "swe_probe.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-ftz=true",

@@ -95,6 +95,7 @@ def load(build_if_needed: bool = True):
     L.swe_device_fields.argtypes = [vp, vp]
     L.swe_run_noalloc.argtypes = [C.POINTER(_Grid), C.POINTER(_Params), vp, vp, vp, i32, i64, vp]
     L.swe_selftest_wait.argtypes = [i64]
+    L.swe_probe_fma_rate.argtypes = [i32, d, vp, C.POINTER(d), C.POINTER(d)]
     L.swe_destroy.argtypes = [vp]
     L.swe_destroy.restype = None
     L.swe_status_str.argtypes = [i32]
@@ -103,7 +104,7 @@ def load(build_if_needed: bool = True):
                  "swe_step", "swe_run",
                  "swe_get_state", "swe_set_state", "swe_get_dt_history", "swe_get_info",
                  "swe_device_fields", "swe_run_noalloc", "swe_set_timing", "swe_get_timing",
-                 "swe_selftest_wait"):
+                 "swe_selftest_wait", "swe_probe_fma_rate"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -323,6 +324,19 @@ def swe_selftest_wait(budget_cycles) -> int:
     on (see swe.h); returns the status, SWE_ERR_TIMEOUT when the wait gave up
     as designed."""
     return int(load().swe_selftest_wait(int(budget_cycles)))
+
+
+PROBE_FFMA, PROBE_FFMA2, PROBE_DFMA = 0, 1, 2
+
+
+def swe_probe_fma_rate(kind, target_ms=50.0, stream=None):
+    """Measured FMA throughput of the current device (see swe_probe.h):
+    (flops per second, duration of the timed launch in ms)."""
+    rate, ms = C.c_double(0.0), C.c_double(0.0)
+    _check(load().swe_probe_fma_rate(int(kind), float(target_ms),
+                                      C.c_void_p(stream) if stream else None, C.byref(rate),
+                                      C.byref(ms)), "swe_probe_fma_rate")
+    return rate.value, ms.value
 
 
 def swe_destroy(s: State):

@@ -1,4 +1,4 @@
-"""libswe loads and exports every function that include/swe.h declares, and
+"""libswe loads and exports every function that include/*.h declares, and
 rejects bad arguments before it touches the GPU (no compute calls here)."""
 import ctypes as C
 import os
@@ -11,13 +11,16 @@ from finite_volume_shallow_gb300 import build as B
 from finite_volume_shallow_gb300 import swe as S
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "swe.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(swe_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(swe_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -30,7 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("swe_create_grid", "swe_step", "swe_run", "swe_get_state", "swe_set_state",
                  "swe_get_dt_history", "swe_get_info", "swe_device_fields", "swe_destroy",
-                 "swe_status_str"):
+                 "swe_status_str", "swe_run_noalloc", "swe_probe_fma_rate"):
         assert want in names
 
 
@@ -147,6 +150,18 @@ def test_noalloc_rejects_bad_arguments_before_touching_the_gpu(lib):
         S.swe_run_noalloc(64, 40, 1.0, 1.0, fake[0], fake[1:5], fake[5:9], S.noalloc_pitch(64), 3,
                           entropy_fix=3)
     assert e.value.status == S.SWE_ERR_ARG
+    # the layer count and the pollutant switch, straight through the C ABI:
+    # two layers or no pollutant are unsupported, any other count is invalid
+    import ctypes as C
+    grid = S._Grid(64, 40, 1.0, 1.0)
+    wa = (C.c_void_p * 4)(*fake[1:5])
+    wb = (C.c_void_p * 4)(*fake[5:9])
+    for layers, pollutant, want in ((2, 1, S.SWE_ERR_UNSUPPORTED), (1, 0, S.SWE_ERR_UNSUPPORTED),
+                                    (0, 1, S.SWE_ERR_ARG), (3, 1, S.SWE_ERR_ARG)):
+        params = S._Params(layers, 64, pollutant, 9.81, 0.0, 0.9, None, 0)
+        got = lib.swe_run_noalloc(C.byref(grid), C.byref(params), C.c_void_p(fake[0]), wa, wb,
+                                  S.noalloc_pitch(64), 3, None)
+        assert got == want, (layers, pollutant, got)
 
 
 def test_wait_selftest_rejects_bad_budgets_before_touching_the_gpu(lib):

@@ -1,4 +1,5 @@
-"""The boundary is a C ABI: include/swe.h compiles as C99 (and as C++), and a
+"""The boundary is a C ABI: include/swe.h and include/swe_probe.h compile as C99
+(and as C++), and a
 C program links against libswe and gets its argument checks and status
 strings without a GPU (no compute call)."""
 import os
@@ -16,6 +17,7 @@ PROGRAM = r"""
 #include <stdio.h>
 #include <string.h>
 #include "swe.h"
+#include "swe_probe.h"
 
 int main(void) {
   swe_grid grid;
@@ -41,6 +43,12 @@ int main(void) {
   if (swe_step(NULL, 0.9, NULL) != SWE_ERR_ARG) bad |= 8;
   swe_destroy(NULL);
   if (strcmp(swe_status_str(SWE_OK), swe_status_str(SWE_ERR_ARG)) == 0) bad |= 16;
+  {
+    double rate = 0.0;
+    if (swe_probe_fma_rate(9, 10.0, NULL, &rate, NULL) != SWE_ERR_ARG) bad |= 32;
+    if (swe_probe_fma_rate(SWE_PROBE_DFMA, 0.5, NULL, &rate, NULL) != SWE_ERR_ARG) bad |= 64;
+    if (swe_probe_fma_rate(SWE_PROBE_FFMA, 10.0, NULL, NULL, NULL) != SWE_ERR_ARG) bad |= 128;
+  }
   printf("%d\n", bad);
   return bad;
 }

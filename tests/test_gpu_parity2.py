@@ -72,9 +72,11 @@ def test_two_layer_lake_at_rest():
 @pytest.mark.parametrize("precision", [64, 32])
 def test_full_size_interface_dam_rows_match_strip(precision):
     # the 2048^2 interface dam break is y-invariant with walls: every row of
-    # the full grid must equal the oracle on a walled 2048 x 4 strip
-    steps = 20
+    # the full grid must equal the oracle on a walled 2048 x 4 strip, over the
+    # workload's own 500 steps
     d = I.make_workload("interface2048")
+    steps = d["steps"]
+    assert steps == 500
     Wg, dtg, _ = gpu_run2(d, precision, steps)
     strip = I.make_workload("interface2048", ny=4)
     Wo, dto = oracle_run2(strip, precision, steps)

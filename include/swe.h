@@ -195,7 +195,10 @@ swe_status swe_mesh_info(const swe_mesh *mesh, int32_t *new_of_old,
  * edge's Roe matrix has complex eigenvalues). */
 swe_status swe_step(swe_state *s, double cfl, double *dt_out);
 
-/* Advance nsteps >= 0 steps with params.cfl.  Enqueues all steps on the
+/* Advance nsteps >= 0 steps with params.cfl: the time loop of [P1]
+ * Algorithm 1 (per step: edge fluxes, per-volume dt of eq. (5) and its
+ * minimum, the update of eq. (4), the clock), with the minimum taken on the
+ * device.  Enqueues all steps on the
  * handle's stream without host synchronisation, then waits once and reports
  * the sticky device error.  On a two-layer grid the update of each step is
  * applied inside the next step's flux pass (and the last one by a separate

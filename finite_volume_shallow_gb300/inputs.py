@@ -164,6 +164,44 @@ def dam_break_1d(nx, ny=4, length=2000.0, x_dam=1000.0, h_left=2.0, h_right=1.0)
     return _as_fields(z, h, z, z, h * C, nx=nx, ny=ny, dx=dx, dy=dx)
 
 
+def dry_dam_1d(nx, ny=4, length=2000.0, x_dam=1000.0, h0=2.0):
+    """Dam break over a dry, flat bed along x (Ritter's problem): h = h0 for
+    x < x_dam and 0 beyond, water at rest, C = 1 in the water; square cells.
+    For runs with the wet/dry treatment."""
+    dx = length / nx
+    x = (np.arange(nx) + 0.5) * dx
+    h1 = np.where(x < x_dam, h0, 0.0)
+    h = np.tile(h1, (ny, 1))
+    z = np.zeros_like(h)
+    return _as_fields(z, h, z, z, h.copy(), nx=nx, ny=ny, dx=dx, dy=dx)
+
+
+def emerged_hills(nx, ny, dx=10.0, seed=1007, n_hills=8, eta=None, column=None):
+    """Gaussian hills (amplitude U[0.5, 2.5] m, sigma U[50, 300] m, centres
+    U[0, L]^2) that pierce a lake at rest, for runs with the wet/dry
+    treatment.  The surface ``eta`` (default: 0.3 m below the highest bed
+    point) leaves the hill tops dry: h = max(0, eta - z_b) exactly, q = 0,
+    C per 16 x 16 block.  ``column = (cx, cy, radius, rise)`` raises the
+    surface by ``rise`` inside the disc (a dam break that floods dry land).
+    Draw order: hills (amp, sigma, cx, cy), then block concentrations."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lx, ly = nx * dx, ny * dx
+    a, s, cx, cy = _hills(rng, n_hills, lx, ly, 0.5, 2.5)
+    zb = _gaussian_sum(nx, ny, dx, dx, a, s, cx, cy)
+    C = _block_concentration(rng, nx, ny)
+    level = zb.max() - 0.3 if eta is None else float(eta)
+    surf = np.full_like(zb, level)
+    if column is not None:
+        x0, y0, rad, rise = column
+        xc = (np.arange(nx) + 0.5) * dx
+        yc = (np.arange(ny) + 0.5) * dx
+        X, Y = np.meshgrid(xc, yc)
+        surf = np.where(np.hypot(X - x0, Y - y0) < rad, level + rise, level)
+    h = np.maximum(0.0, surf - zb)
+    z = np.zeros_like(h)
+    return _as_fields(-zb, h, z, z, h * C, nx=nx, ny=ny, dx=dx, dy=dx)
+
+
 def interface_dam(nx, ny, dx=10.0, depth=10.0, h_left=6.0, h_right=4.0, r=0.98):
     """Two-layer interface dam break on a flat bottom ``depth`` deep: upper
     layer h1 = h_left for x < L/2 and h_right beyond, lower layer

@@ -71,6 +71,8 @@ def lib():
         _lib.om_flux1.argtypes = [vp, vp, d, d, d, d, d, vp, vp]
         _lib.om_set_entropy_fix.restype = None
         _lib.om_set_entropy_fix.argtypes = [C.c_int]
+        _lib.om_set_wet_dry.restype = None
+        _lib.om_set_wet_dry.argtypes = [C.c_int, C.c_double]
         _lib.om_wall_ghost1.restype = None
         _lib.om_wall_ghost1.argtypes = [vp, d, d, vp]
         _lib.om_dt1.restype = d
@@ -128,6 +130,23 @@ class entropy_fix:
 
     def __exit__(self, *exc):
         lib().om_set_entropy_fix(0)
+        return False
+
+
+class wet_dry:
+    """Context manager: the one-layer oracle with the wet/dry treatment on
+    (depth threshold h_dry; see om_set_wet_dry)."""
+
+    def __init__(self, h_dry=1e-6, on=True):
+        self.on = bool(on)
+        self.h_dry = float(h_dry)
+
+    def __enter__(self):
+        lib().om_set_wet_dry(1 if self.on else 0, self.h_dry)
+        return self
+
+    def __exit__(self, *exc):
+        lib().om_set_wet_dry(0, 0.0)
         return False
 
 

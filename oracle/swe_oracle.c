@@ -84,6 +84,38 @@ static double sgn(double x) { return (x > 0.0) ? 1.0 : ((x < 0.0) ? -1.0 : 0.0);
 static int g_entropy_fix = 0;
 void om_set_entropy_fix(int on) { g_entropy_fix = on ? 1 : 0; }
 
+/* Optional wet/dry treatment (one layer; off unless switched on).  The
+ * pages give none: they report depths bounded away from zero.  This is the
+ * combination of two published techniques for explicit upwind finite-volume
+ * schemes:
+ *  - dry cells and wet/dry fronts as in Brufau, Vazquez-Cendon and
+ *    Garcia-Navarro, "A numerical model for the flooding and drying of
+ *    irregular domains" (Int. J. Numer. Meth. Fluids 39, 2002): a cell with
+ *    h <= h_dry is dry and carries no velocity and no concentration; an edge
+ *    between two dry cells passes nothing; an edge between a wet cell and a
+ *    dry cell whose bed (-H) is at or above the wet cell's free surface
+ *    (h - H) is a reflective wall for both (the wet side sees its mirror
+ *    ghost over its own bed, so water at rest against an emerged bank stays
+ *    at rest); any other wet/dry edge takes the Roe flux with the dry side's
+ *    velocity and concentration zero;
+ *  - positivity by the draining time of Bollermann, Chen, Kurganov and
+ *    Noelle, "A well-balanced reconstruction of wet/dry fronts for the
+ *    shallow water equations" (J. Sci. Comput. 56, 2013): a cell i whose
+ *    edges carry mass out at the total rate M_i = sum_e L_e max(0, phi_e)
+ *    empties in tau_i = h_i |V_i| / M_i; every term of an edge (mass,
+ *    momentum, pollutant, both sides) is scaled by min(1, tau_d / dt), d the
+ *    cell the edge's mass flux leaves, so no cell loses more water than it
+ *    holds.
+ * After the update a depth is clamped at 0 (rounding only) and a cell that
+ * ended dry loses its discharge. */
+static int g_wet_dry = 0;
+static double g_h_dry = 0.0;
+void om_set_wet_dry(int on, double h_dry) {
+  g_wet_dry = on ? 1 : 0;
+  g_h_dry = on ? h_dry : 0.0;
+}
+static int is_dry(double h) { return g_wet_dry && h <= g_h_dry; }
+
 static double harten_abs(double lam, double lamL, double lamR) {
   double delta = fmax(0.0, fmax(lam - lamL, lamR - lam));
   double a = fabs(lam);
@@ -107,19 +139,39 @@ static void flux_1d(double h, double qn, double g, double F[2]) {
 
 void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
               double ex, double ey, double g, double *F, double *Dinf) {
+  /* wet/dry (when switched on): two dry sides pass nothing; a dry side
+   * whose bed is at or above the wet side's surface is a wall */
+  int dry_i = is_dry(Wi[0]), dry_j = is_dry(Wj[0]);
+  if (dry_i && dry_j) {
+    F[0] = F[1] = F[2] = F[3] = 0.0;
+    *Dinf = 0.0;
+    return;
+  }
+  if ((dry_j && -Hj >= Wi[0] - Hi) || (dry_i && -Hi >= Wj[0] - Hj)) {
+    if (dry_i) {
+      F[0] = F[1] = F[2] = F[3] = 0.0;
+      *Dinf = 0.0;
+      return;
+    }
+    double Wg[4];
+    om_wall_ghost1(Wi, ex, ey, Wg);
+    om_flux1(Wi, Wg, Hi, Hi, ex, ey, g, F, Dinf);
+    return;
+  }
   /* Step 1: W_eta = T_eta W.  R_eta maps (qx, qy) to
-   * (q . eta, q . eta_perp) with eta_perp = (-ey, ex)  (eq. (2)). */
+   * (q . eta, q . eta_perp) with eta_perp = (-ey, ex)  (eq. (2)).  A dry
+   * side carries no discharge. */
   double hi = Wi[0], hj = Wj[0];
-  double qni = Wi[1] * ex + Wi[2] * ey;
-  double qnj = Wj[1] * ex + Wj[2] * ey;
-  double qti = -Wi[1] * ey + Wi[2] * ex;
-  double qtj = -Wj[1] * ey + Wj[2] * ex;
+  double qni = dry_i ? 0.0 : Wi[1] * ex + Wi[2] * ey;
+  double qnj = dry_j ? 0.0 : Wj[1] * ex + Wj[2] * ey;
+  double qti = dry_i ? 0.0 : -Wi[1] * ey + Wi[2] * ex;
+  double qtj = dry_j ? 0.0 : -Wj[1] * ey + Wj[2] * ex;
 
   /* Step 2: Roe matrix of the 1D system.  Velocities are averaged with
    * sqrt(h) weights per Cartesian component, depths arithmetically. */
   double si = sqrt(hi), sj = sqrt(hj);
-  double uxi = Wi[1] / hi, uyi = Wi[2] / hi;
-  double uxj = Wj[1] / hj, uyj = Wj[2] / hj;
+  double uxi = dry_i ? 0.0 : Wi[1] / hi, uyi = dry_i ? 0.0 : Wi[2] / hi;
+  double uxj = dry_j ? 0.0 : Wj[1] / hj, uyj = dry_j ? 0.0 : Wj[2] / hj;
   double ux = (si * uxi + sj * uxj) / (si + sj);
   double uy = (si * uyi + sj * uyj) / (si + sj);
   double un = ux * ex + uy * ey;
@@ -144,13 +196,15 @@ void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
   double Fi[2], Fj[2];
   flux_1d(hi, qni, g, Fi);
   flux_1d(hj, qnj, g, Fj);
+  if (dry_i) Fi[1] = 0.5 * g * hi * hi;  /* no q^2 / h on a dry side */
+  if (dry_j) Fj[1] = 0.5 * g * hj * hj;
   double d[2] = {Fj[0] - Fi[0], Fj[1] - Fi[1] - g * hbar * (Hj - Hi)};
   /* Phi^- = P^- d + F_1(W_eta,i) */
   double phi[2];
   for (int r = 0; r < 2; ++r) phi[r] = P[r][0] * d[0] + P[r][1] * d[1] + Fi[r];
   if (g_entropy_fix) {
     /* the eigenvalues of each side's own Jacobian, u_eta -/+ sqrt(g h) */
-    double uni = qni / hi, unj = qnj / hj;
+    double uni = dry_i ? 0.0 : qni / hi, unj = dry_j ? 0.0 : qnj / hj;
     double ci = sqrt(g * hi), cj = sqrt(g * hj);
     double lamL[2] = {uni - ci, uni + ci}, lamR[2] = {unj - cj, unj + cj};
     double dW[2] = {hj - hi, qnj - qni};
@@ -163,8 +217,14 @@ void om_flux1(const double *Wi, const double *Wj, double Hi, double Hj,
 
   /* Step 3: tangential discharge and pollutant as passive scalars carried
    * by the mass flux, upwinded on its sign. */
-  double ut = (phi[0] > 0.0) ? qti / hi : qtj / hj;
-  double Cs = (phi[0] > 0.0) ? Wi[3] / hi : Wj[3] / hj;
+  double ut, Cs;
+  if (phi[0] > 0.0) {
+    ut = dry_i ? 0.0 : qti / hi;
+    Cs = dry_i ? 0.0 : Wi[3] / hi;
+  } else {
+    ut = dry_j ? 0.0 : qtj / hj;
+    Cs = dry_j ? 0.0 : Wj[3] / hj;
+  }
   double phit = phi[0] * ut;
 
   /* Step 4: back to Cartesian components with T_eta^-1. */
@@ -262,8 +322,45 @@ static double dt_view(const view *v, const double *const *W, const double *H,
 static int check_state(const double w[4]) {
   for (int k = 0; k < 4; ++k)
     if (!isfinite(w[k])) return OM_ERR_NONFINITE;
-  if (!(w[0] > 0.0)) return OM_ERR_DEPTH;
+  if (g_wet_dry ? !(w[0] >= 0.0) : !(w[0] > 0.0)) return OM_ERR_DEPTH;
   return OM_OK;
+}
+
+/* Wet/dry only: min(1, tau_i / dt) of cell i, tau_i = h_i |V_i| / M_i its
+ * draining time (1 when no mass leaves it). */
+static double drain_ratio(const view *v, const double *const *W, const double *H, double g,
+                          double dt, int64_t i) {
+  double Fl[4][OM_MAX_EDGES], Dl[OM_MAX_EDGES], out[OM_MAX_EDGES];
+  int n = cell_terms(v, W, H, g, i, Fl, Dl);
+  for (int k = 0; k < n; ++k) out[k] = fmax(Fl[0][k], 0.0);
+  double M = psum(out, n);
+  if (!(M > 0.0)) return 1.0;
+  return fmin(1.0, W[0][i] * view_area(v, i) / M / dt);
+}
+
+/* Wet/dry only: scale every term of each edge of cell i by the ratio of the
+ * cell its mass flux leaves (ratio_of(j) gives it for any cell j). */
+static void drain_scale(const view *v, int64_t i, double Fl[4][OM_MAX_EDGES], int n,
+                        double ri, const double *ratios, const double *const *W,
+                        const double *H, double g, double dt) {
+  int64_t nbr[OM_MAX_EDGES];
+  double exs[OM_MAX_EDGES], eys[OM_MAX_EDGES], lens[OM_MAX_EDGES];
+  view_edges(v, i, nbr, exs, eys, lens);
+  for (int k = 0; k < n; ++k) {
+    double theta = 1.0;
+    if (Fl[0][k] > 0.0) theta = ri;
+    else if (Fl[0][k] < 0.0 && nbr[k] >= 0)
+      theta = ratios ? ratios[nbr[k]] : drain_ratio(v, W, H, g, dt, nbr[k]);
+    for (int c = 0; c < 4; ++c) Fl[c][k] *= theta;
+  }
+}
+
+/* Wet/dry only: a depth below zero (rounding) is clamped, and a dry cell
+ * keeps no discharge. */
+static void dry_cleanup(double w[4]) {
+  if (!g_wet_dry) return;
+  if (w[0] < 0.0) w[0] = 0.0;
+  if (w[0] <= g_h_dry) w[1] = w[2] = 0.0;
 }
 
 static int update_view(const view *v, double *const *W, const double *H, double g,
@@ -271,18 +368,25 @@ static int update_view(const view *v, double *const *W, const double *H, double 
   const double *const *Wc = (const double *const *)W;
   double Fl[4][OM_MAX_EDGES], Dl[OM_MAX_EDGES];
   int64_t N = view_cells(v);
+  double *ratios = NULL;
+  if (g_wet_dry) {
+    ratios = (double *)malloc((size_t)N * sizeof(double));
+    if (!ratios) return OM_ERR_ARG;
+    for (int64_t i = 0; i < N; ++i) ratios[i] = drain_ratio(v, Wc, H, g, dt, i);
+  }
   for (int64_t i = 0; i < N; ++i) {
     int n = cell_terms(v, Wc, H, g, i, Fl, Dl);
+    if (ratios) drain_scale(v, i, Fl, n, ratios[i], ratios, Wc, H, g, dt);
     for (int c = 0; c < 4; ++c)
       work[c * N + i] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
   }
+  free(ratios);
   int status = OM_OK;
   for (int64_t i = 0; i < N; ++i) {
     double w[4];
-    for (int c = 0; c < 4; ++c) {
-      w[c] = work[c * N + i];
-      W[c][i] = w[c];
-    }
+    for (int c = 0; c < 4; ++c) w[c] = work[c * N + i];
+    dry_cleanup(w);
+    for (int c = 0; c < 4; ++c) W[c][i] = w[c];
     int s = check_state(w);
     if (s != OM_OK && status == OM_OK) status = s;
   }
@@ -296,8 +400,12 @@ static void update_at_view(const view *v, const double *const *W, const double *
   for (int64_t s = 0; s < n_sel; ++s) {
     int64_t i = cells[s];
     int n = cell_terms(v, W, H, g, i, Fl, Dl);
-    for (int c = 0; c < 4; ++c)
-      out[c * n_sel + s] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
+    if (g_wet_dry)
+      drain_scale(v, i, Fl, n, drain_ratio(v, W, H, g, dt, i), NULL, W, H, g, dt);
+    double w[4];
+    for (int c = 0; c < 4; ++c) w[c] = W[c][i] - dt / view_area(v, i) * psum(Fl[c], n);
+    dry_cleanup(w);
+    for (int c = 0; c < 4; ++c) out[c * n_sel + s] = w[c];
   }
 }
 

@@ -84,6 +84,15 @@ void om_wall_ghost1(const double *Wi, double ex, double ey, double *Wg);
  * default) for every later call, one layer or two. */
 void om_set_entropy_fix(int on);
 
+/* Switch the wet/dry treatment of the one-layer scheme on (1, with depth
+ * threshold h_dry >= 0: a cell with h <= h_dry is dry) or off (0, the
+ * default) for every later call: dry cells carry no velocity, a dry cell
+ * whose bed is at or above its wet neighbour's surface is a wall, and each
+ * edge is scaled by the draining ratio of the cell its mass flux leaves, so
+ * that depths stay >= 0 (see swe_oracle.c for the two published sources).
+ * With it on, h = 0 is a valid state. */
+void om_set_wet_dry(int on, double h_dry);
+
 /* Time step of eq. (5): min_i 2 cfl |V_i| / sum_j |Gamma_ij| ||D_ij||_inf.
  * W holds the four fields h, qx, qy, hC as separate arrays (W[0..3]). */
 double om_dt1(const om_mesh *m, const double *const *W, const double *H,

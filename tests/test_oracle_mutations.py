@@ -46,11 +46,26 @@ MUTANTS = {
     "p_plus": ("0.5 * (1.0 - sgn(lam[0])), 0.5 * (1.0 - sgn(lam[1]))",
                "0.5 * (1.0 + sgn(lam[0])), 0.5 * (1.0 + sgn(lam[1]))"),
     # tangential velocity upwinded from the wrong side
-    "tangential_downwind": ("double ut = (phi[0] > 0.0) ? qti / hi : qtj / hj;",
-                            "double ut = (phi[0] > 0.0) ? qtj / hj : qti / hi;"),
+    "tangential_downwind": ("    ut = dry_i ? 0.0 : qti / hi;\n    Cs = dry_i ? 0.0 : Wi[3] / hi;\n"
+                            "  } else {\n    ut = dry_j ? 0.0 : qtj / hj;",
+                            "    ut = dry_j ? 0.0 : qtj / hj;\n    Cs = dry_i ? 0.0 : Wi[3] / hi;\n"
+                            "  } else {\n    ut = dry_i ? 0.0 : qti / hi;"),
     # pollutant upwinded from the wrong side
-    "pollutant_downwind": ("double Cs = (phi[0] > 0.0) ? Wi[3] / hi : Wj[3] / hj;",
-                           "double Cs = (phi[0] > 0.0) ? Wj[3] / hj : Wi[3] / hi;"),
+    "pollutant_downwind": ("    Cs = dry_i ? 0.0 : Wi[3] / hi;\n  } else {\n"
+                           "    ut = dry_j ? 0.0 : qtj / hj;\n    Cs = dry_j ? 0.0 : Wj[3] / hj;",
+                           "    Cs = dry_j ? 0.0 : Wj[3] / hj;\n  } else {\n"
+                           "    ut = dry_j ? 0.0 : qtj / hj;\n    Cs = dry_i ? 0.0 : Wi[3] / hi;"),
+    # wet/dry: the emerged-bank rule reversed (flooded cells become walls,
+    # banks pass water), the draining limit taken from the receiving cell,
+    # no draining limit at all, the draining time without the cell's area
+    "wd_bank_rule": ("(dry_j && -Hj >= Wi[0] - Hi) || (dry_i && -Hi >= Wj[0] - Hj)",
+                     "(dry_j && -Hj <= Wi[0] - Hi) || (dry_i && -Hi <= Wj[0] - Hj)"),
+    "wd_theta_receiver": ("if (Fl[0][k] > 0.0) theta = ri;\n    else if (Fl[0][k] < 0.0 && nbr[k] >= 0)",
+                          "if (Fl[0][k] < 0.0) theta = ri;\n    else if (Fl[0][k] > 0.0 && nbr[k] >= 0)"),
+    "wd_no_drain": ("for (int c = 0; c < 4; ++c) Fl[c][k] *= theta;",
+                    "for (int c = 0; c < 4; ++c) Fl[c][k] *= 1.0 + 0.0 * theta;"),
+    "wd_tau_area": ("return fmin(1.0, W[0][i] * view_area(v, i) / M / dt);",
+                    "return fmin(1.0, W[0][i] / M / dt);"),
     # back-rotation with a transposed operator
     "back_rotation": ("F[1] = phi[1] * ex - phit * ey;", "F[1] = phi[1] * ex + phit * ey;"),
     # hydrostatic pressure without its factor 1/2 (one layer, two layers)
@@ -134,6 +149,7 @@ def test_pins_catch_mutant(name, workdir):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_pins.py"),
                         os.path.join(HERE, "test_oracle_pins2.py"),
-                        os.path.join(HERE, "test_oracle_pins_tri.py")],
+                        os.path.join(HERE, "test_oracle_pins_tri.py"),
+                        os.path.join(HERE, "test_oracle_pins_wetdry.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

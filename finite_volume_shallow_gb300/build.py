@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libswe.so")
 SOURCES = ["swe_api.cu", "swe_cart1.cu", "swe_cart2.cu", "swe_mesh.cu", "swe_mesh_prep.cpp",
-           "swe_noalloc.cu", "swe_probe.cu"]
+           "swe_noalloc.cu", "swe_probe.cu", "swe_wetdry.cu"]
 HEADERS = [os.path.join(CSRC, "swe_internal.h"), os.path.join(CSRC, "swe_roe2.cuh"),
            os.path.join(CSRC, "swe_fastmath.cuh"), os.path.join(CSRC, "swe_plan.h"),
            os.path.join(ROOT, "include", "swe.h"), os.path.join(ROOT, "include", "swe_probe.h")]

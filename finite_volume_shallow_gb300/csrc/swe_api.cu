@@ -69,6 +69,12 @@ struct swe_state {
   const cudaEvent_t* marks = nullptr; // events of the step being enqueued, or null
   int* mark_kid = nullptr;            // with marks: kernel index of each interval
   int* mark_n = nullptr;              // with marks: intervals recorded so far
+  // one layer with wet/dry fronts on a grid (swe_params.wet_dry)
+  bool wd = false;
+  void* wd_ex = nullptr;             // edge records, see WdStepArgs
+  void* wd_ey = nullptr;
+  void* wd_tau = nullptr;
+  int64_t wd_xs = 0, wd_ys = 0;
 };
 
 // Per-kernel device time: a ring of event sets, one set per step; a set is
@@ -337,7 +343,50 @@ swe_status enqueue_mesh_step(swe_state* s, double cfl) {
   return SWE_OK;
 }
 
+// Wet/dry: the cell pass of step n reduces into slot n % 3, the update of
+// step n reads it and zeroes slot (n + 1) % 3 (all three zero at set-up).
+template <typename T>
+swe_status enqueue_wd_check(swe_state* s) {
+  CK(cudaMemsetAsync(s->slots, 0, 3 * sizeof(uint64_t), s->stream));
+  const T* w[4] = {(const T*)s->w[s->cur][0], (const T*)s->w[s->cur][1],
+                   (const T*)s->w[s->cur][2], (const T*)s->w[s->cur][3]};
+  CK(launch_wd_check<T>(w, s->nx, s->ny, s->pitch, s->err, s->stream));
+  return SWE_OK;
+}
+
+template <typename T>
+swe_status enqueue_wd_step(swe_state* s, double cfl) {
+  WdStepArgs a{};
+  for (int f = 0; f < 4; ++f) a.w[f] = s->w[s->cur][f];
+  a.H = s->H;
+  a.nx = s->nx;
+  a.ny = s->ny;
+  a.pitch = s->pitch;
+  a.g = s->p.g;
+  a.h_dry = s->p.h_dry;
+  a.dx = s->dx;
+  a.dy = s->dy;
+  a.ex = s->wd_ex;
+  a.ey = s->wd_ey;
+  a.xs = s->wd_xs;
+  a.ys = s->wd_ys;
+  a.tau = s->wd_tau;
+  a.two_cfl = 2.0 * cfl;
+  char* sl = (char*)s->slots;
+  a.tmax_slot = sl + (s->step % 3) * sizeof(uint64_t);
+  a.tmax_clear = sl + ((s->step + 1) % 3) * sizeof(uint64_t);
+  a.dt_hist = s->dt_hist;
+  a.t_dev = s->t_dev;
+  a.step = s->step;
+  a.err = s->err;
+  a.efix = s->p.entropy_fix;
+  CK(launch_wd_step<T>(a, s->stream, s->marks));
+  s->step += 1;
+  return SWE_OK;
+}
+
 swe_status enqueue_dt0_any(swe_state* s) {
+  if (s->wd) return s->prec == 32 ? enqueue_wd_check<float>(s) : enqueue_wd_check<double>(s);
   if (s->mesh)
     return s->prec == 32 ? enqueue_mesh_check<float>(s) : enqueue_mesh_check<double>(s);
   if (s->nl == 2) return s->prec == 32 ? enqueue_check2<float>(s) : enqueue_check2<double>(s);
@@ -374,6 +423,7 @@ swe_status enqueue_step_timed(swe_state* s, double cfl, bool last);
 // applies its pending update).
 swe_status enqueue_step_any(swe_state* s, double cfl, bool last) {
   if (s->timing && s->timing->on) return enqueue_step_timed(s, cfl, last);
+  if (s->wd) return s->prec == 32 ? enqueue_wd_step<float>(s, cfl) : enqueue_wd_step<double>(s, cfl);
   if (s->mesh)
     return s->prec == 32 ? enqueue_mesh_step<float>(s, cfl) : enqueue_mesh_step<double>(s, cfl);
   if (s->nl == 2)
@@ -408,7 +458,12 @@ swe_status enqueue_step_timed(swe_state* s, double cfl, bool last) {
 }
 
 void timing_names(swe_state* s, Timing* tm) {
-  if (s->mesh) {
+  if (s->wd) {
+    tm->nk = 3;
+    tm->names[0] = "wd_edge_kernel";
+    tm->names[1] = "wd_cell_kernel";
+    tm->names[2] = "wd_update_kernel";
+  } else if (s->mesh) {
     tm->nk = 3;
     tm->names[0] = "mesh_edge_kernel";
     tm->names[1] = "mesh_gather_kernel";
@@ -506,6 +561,11 @@ swe_status check_params(const swe_params* params) {
   if (params->n_layers != 1 && params->n_layers != 2) return SWE_ERR_ARG;
   if (params->n_layers == 1 && params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
   if (params->entropy_fix != 0 && params->entropy_fix != 1) return SWE_ERR_ARG;
+  if (params->wet_dry != 0 && params->wet_dry != 1) return SWE_ERR_ARG;
+  if (params->wet_dry == 1) {
+    if (!(isfinite(params->h_dry) && params->h_dry >= 0.0)) return SWE_ERR_ARG;
+    if (params->n_layers != 1) return SWE_ERR_UNSUPPORTED;
+  }
   if (params->n_layers == 2) {
     if (params->pollutant != 0) return SWE_ERR_UNSUPPORTED;
     if (!(params->r >= 0.0 && params->r < 1.0)) return SWE_ERR_ARG;
@@ -614,6 +674,8 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   // index arithmetic inside the kernels is 32-bit per row and column
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
+  // wet/dry: one block per 8 rows of edges in the launch's y dimension
+  if (params->wet_dry == 1 && ((int64_t)grid->ny + 1 + 7) / 8 > 65535) return SWE_ERR_ARG;
   // two layers: one block per tile row in the grid's y dimension (<= 65535)
   if (params->n_layers == 2) {
     const int64_t ty = params->precision == 32 ? Tile2Y<float>::v : Tile2Y<double>::v;
@@ -646,7 +708,12 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   const int64_t aux = kAuxBytes;
   // two buffers of the fields (+ two of the residual for two layers) + H
   const int nalloc = s->nl == 2 ? 25 : 9;
-  s->dev_bytes = (size_t)(nalloc * fbytes + aux);
+  // wet/dry: edge records of the x- and y-edges and a draining time per cell
+  s->wd = params->wet_dry == 1;
+  const int64_t wd_xb = s->wd ? round_up((int64_t)(s->nx + 1) * s->ny * (int64_t)s->esz, 256) : 0;
+  const int64_t wd_yb = s->wd ? round_up((int64_t)s->nx * (s->ny + 1) * (int64_t)s->esz, 256) : 0;
+  const int64_t wd_tb = s->wd ? round_up((int64_t)s->nx * s->ny * (int64_t)s->esz, 256) : 0;
+  s->dev_bytes = (size_t)(nalloc * fbytes + aux + kWdEdgeFields * (wd_xb + wd_yb) + wd_tb);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
   if (e != cudaSuccess) {
     s->dev = nullptr;
@@ -676,6 +743,16 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   s->H = p;
   p += fbytes;
+  if (s->wd) {
+    s->wd_ex = p;
+    s->wd_xs = wd_xb / (int64_t)s->esz;
+    p += kWdEdgeFields * wd_xb;
+    s->wd_ey = p;
+    s->wd_ys = wd_yb / (int64_t)s->esz;
+    p += kWdEdgeFields * wd_yb;
+    s->wd_tau = p;
+    p += wd_tb;
+  }
   if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
 
   if (s->nl == 1) {
@@ -708,6 +785,7 @@ swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* cons
     const swe_status pst = check_params(params);
     if (pst != SWE_OK) return pst;
   }
+  if (params->wet_dry) return SWE_ERR_UNSUPPORTED;
   const int nfields = params->n_layers == 2 ? 6 : 4;
   for (int f = 0; f < nfields; ++f)
     if (!W0[f]) return SWE_ERR_ARG;

@@ -226,6 +226,36 @@ struct MeshPrep {
 int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const int32_t* tri,
                  bool reorder, MeshPrep* out);
 
+// ---- one layer with wet/dry fronts on a grid (swe_wetdry.cu) ----------------
+// State in the one-layer padded layout, updated in place; per step an edge
+// pass (records of every x- and y-edge: 7 values each), a cell pass (sum of
+// L ||D|| reduced into tmax_slot, draining time per cell) and the update,
+// which reads tmax_slot and zeroes tmax_clear.
+struct WdStepArgs {
+  void* w[4];
+  const void* H;
+  int nx, ny, pitch;
+  double g, h_dry, dx, dy;
+  void* ex;          // 7 fields of (nx + 1) * ny x-edge values, stride xs
+  void* ey;          // 7 fields of nx * (ny + 1) y-edge values, stride ys
+  int64_t xs, ys;
+  void* tau;         // nx * ny draining times
+  double two_cfl;
+  void* tmax_slot;
+  void* tmax_clear;
+  double* dt_hist;
+  double* t_dev;
+  int64_t step;
+  unsigned* err;
+  int efix;
+};
+constexpr int kWdEdgeFields = 7;
+template <typename T>
+cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent_t* marks);
+template <typename T>
+cudaError_t launch_wd_check(const T* const* w, int nx, int ny, int pitch, unsigned* err,
+                            cudaStream_t st);
+
 // Programmatic dependent launch: consecutive step kernels on a stream are
 // launched with programmatic stream serialisation, so the next kernel's
 // launch overlaps the end of the previous one.  Each such kernel waits

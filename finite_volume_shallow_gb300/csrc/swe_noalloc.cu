@@ -173,6 +173,7 @@ extern "C" swe_status swe_run_noalloc(const swe_grid* grid, const swe_params* pa
   if (params->precision != 32 && params->precision != 64) return SWE_ERR_ARG;
   if (!pos_finite(params->g) || !(params->cfl > 0.0 && params->cfl <= 1.0)) return SWE_ERR_ARG;
   if (params->n_layers == 2 || params->pollutant != 1) return SWE_ERR_UNSUPPORTED;
+  if (params->wet_dry != 0) return SWE_ERR_UNSUPPORTED;
   if (params->entropy_fix != 0 && params->entropy_fix != 1) return SWE_ERR_ARG;
   if (params->n_layers != 1) return SWE_ERR_ARG;
   if (nsteps < 0 || nsteps > SWE_NOALLOC_MAX_STEPS) return SWE_ERR_ARG;

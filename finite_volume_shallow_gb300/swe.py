@@ -48,7 +48,8 @@ class _Mesh(C.Structure):
 class _Params(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("precision", C.c_int32), ("pollutant", C.c_int32),
                 ("g", C.c_double), ("r", C.c_double), ("cfl", C.c_double),
-                ("stream", C.c_void_p), ("entropy_fix", C.c_int32)]
+                ("stream", C.c_void_p), ("entropy_fix", C.c_int32), ("wet_dry", C.c_int32),
+                ("h_dry", C.c_double)]
 
 
 class _Info(C.Structure):
@@ -163,19 +164,22 @@ class State:
 
 
 def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream=None,
-                    n_layers=1, pollutant=1, r=0.0, entropy_fix=0) -> State:
+                    n_layers=1, pollutant=1, r=0.0, entropy_fix=0, wet_dry=0,
+                    h_dry=0.0) -> State:
     """Create a simulation on an nx x ny grid (see swe_create_grid in swe.h).
     H and the fields of W0 (h, qx, qy, hC; or h1, q1x, q1y, h2, q2x, q2y with
     n_layers=2, pollutant=0) are host arrays of the state's precision;
     ``stream`` is a cudaStream_t as an int (e.g.
     ``torch.cuda.current_stream().cuda_stream``) or None; ``entropy_fix=1``
-    switches on the Harten-Hyman entropy fix."""
+    switches on the Harten-Hyman entropy fix, ``wet_dry=1`` the wet/dry
+    treatment with dry threshold ``h_dry`` (see swe_params in swe.h)."""
     L = load()
     dt = _dtype(precision)
     n = int(nx) * int(ny)
     grid = _Grid(int(nx), int(ny), float(dx), float(dy))
     params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
-                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix))
+                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix),
+                     int(wet_dry), float(h_dry))
     Hp = _host_ptr(H, dt, n)
     W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
     out = C.c_void_p()
@@ -185,7 +189,8 @@ def swe_create_grid(nx, ny, dx, dy, H, W0, precision=64, g=9.81, cfl=0.9, stream
 
 
 def swe_create_mesh(xy, tri, H, W0, precision=64, g=9.81, cfl=0.9, stream=None, n_layers=1,
-                    pollutant=1, r=0.0, reorder=1, entropy_fix=0) -> State:
+                    pollutant=1, r=0.0, reorder=1, entropy_fix=0, wet_dry=0,
+                    h_dry=0.0) -> State:
     """Create a simulation on a triangle mesh (see swe_create_mesh in swe.h):
     ``xy`` is an (n_vertices, 2) float64 array, ``tri`` an (n_cells, 3) int32
     array of counter-clockwise vertex indices; H and the fields of W0 hold
@@ -195,7 +200,8 @@ def swe_create_mesh(xy, tri, H, W0, precision=64, g=9.81, cfl=0.9, stream=None, 
     mesh, xy, tri = _mesh_struct(xy, tri, reorder)
     n = int(tri.shape[0])
     params = _Params(int(n_layers), int(precision), int(pollutant), float(g), float(r),
-                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix))
+                     float(cfl), C.c_void_p(stream) if stream else None, int(entropy_fix),
+                     int(wet_dry), float(h_dry))
     Hp = _host_ptr(H, dt, n)
     W = (C.c_void_p * len(W0))(*[_host_ptr(w, dt, n) for w in W0])
     out = C.c_void_p()

@@ -60,8 +60,7 @@ typedef enum {
   SWE_ERR_ARG = -1,         /* invalid argument (NULL, size, parameter)     */
   SWE_ERR_CUDA = -2,        /* a CUDA runtime call failed                   */
   SWE_ERR_OOM = -3,         /* device memory exhausted                      */
-  SWE_ERR_DEPTH = -4,       /* a depth h <= 0 appeared (dry cells are out   */
-                            /* of scope of the scheme as implemented)       */
+  SWE_ERR_DEPTH = -4,       /* a depth h <= 0 appeared (h < 0 with wet_dry) */
   SWE_ERR_NONFINITE = -5,   /* a non-finite value appeared in the state     */
   SWE_ERR_HYPERBOLIC = -6,  /* the two-layer Roe matrix lost hyperbolicity  */
   SWE_ERR_UNSUPPORTED = -7, /* valid request this build does not implement  */
@@ -120,7 +119,31 @@ typedef struct {
  *             (|lambda_k| - |lambda_k|_d) beta_k K_k / 2 with beta = K^-1
  *             (W_j - W_i).  Two layers: a side state whose own system is
  *             not hyperbolic is reported as SWE_ERR_HYPERBOLIC.  Any value
- *             other than 0 or 1 returns SWE_ERR_ARG. */
+ *             other than 0 or 1 returns SWE_ERR_ARG.
+ *  wet_dry    0: every depth must stay > 0 (h <= 0 is SWE_ERR_DEPTH), the
+ *             scheme as printed; 1 (one layer on a grid only, else
+ *             SWE_ERR_UNSUPPORTED): wet/dry fronts, which [P1] leaves open,
+ *             by two published techniques.  A cell with h <= h_dry is dry
+ *             and carries no velocity or concentration; an edge between two
+ *             dry cells passes nothing; an edge between a wet cell and a dry
+ *             cell whose bed (-H) is at or above the wet free surface (h - H)
+ *             is a reflective wall for both (Brufau, Vazquez-Cendon and
+ *             Garcia-Navarro, Int. J. Numer. Meth. Fluids 39, 2002); every
+ *             term of an edge is scaled by min(1, tau_d / dt), tau_d = h_d
+ *             |V_d| / (the mass that leaves cell d per unit time) of the cell
+ *             its mass flux leaves, so no depth turns negative (the draining
+ *             time of Bollermann, Chen, Kurganov and Noelle, J. Sci. Comput.
+ *             56, 2013).  After each step a depth below zero (rounding) is
+ *             clamped to 0 and a dry cell's discharge is set to 0.  h = 0
+ *             is then a valid input; dt stays eq. (5).  Runs as three
+ *             kernels per step (edges, cells, update) instead of the fused
+ *             step.  Any value other than 0 or 1 returns SWE_ERR_ARG.
+ *  h_dry      with wet_dry = 1: the depth at or below which a cell is dry,
+ *             >= 0 and finite.  It must exceed the thin-film scale of the
+ *             problem: with 1e-6 m a film of a few tenths of a millimetre
+ *             next to deep water was driven to km/s velocities (and dt
+ *             collapsed) in the oracle; 1e-4 m to 1e-3 m kept the fastest
+ *             speed physical.  Ignored when wet_dry = 0. */
 typedef struct {
   int32_t n_layers;
   int32_t precision;
@@ -130,6 +153,8 @@ typedef struct {
   double cfl;
   void *stream;
   int32_t entropy_fix;
+  int32_t wet_dry;
+  double h_dry;
 } swe_params;
 
 typedef struct swe_state swe_state;
@@ -138,7 +163,8 @@ typedef struct swe_state swe_state;
  * loop: mesh construction and initial state).
  *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite;
  *          nx <= 2^30, ny <= 2^30 - 8; two layers also ny <= 524280 (fp32)
- *          or 262140 (fp64): 65535 tiles of 8 (fp32) or 4 (fp64) rows
+ *          or 262140 (fp64): 65535 tiles of 8 (fp32) or 4 (fp64) rows;
+ *          with wet_dry also ny <= 524279 (65535 blocks of 8 edge rows)
  *  H       host, nx*ny values: bottom depth below the reference level
  *  W0      host, array of 4 pointers (h, qx, qy, hC), or 6 (h1, q1x, q1y,
  *          h2, q2x, q2y) for two layers, nx*ny values each; depths > 0
@@ -285,8 +311,9 @@ swe_status swe_get_timing(const swe_state *s, swe_kernel_time *out, int32_t max,
  * no cudaFree, no allocating library routine.
  *
  *  grid, params  as for swe_create_grid, one layer with pollutant only:
- *                n_layers = 2 or pollutant != 1 gives SWE_ERR_UNSUPPORTED,
- *                any other n_layers than 1 or 2 gives SWE_ERR_ARG;
+ *                n_layers = 2, pollutant != 1 or wet_dry != 0 gives
+ *                SWE_ERR_UNSUPPORTED, any other n_layers than 1 or 2 gives
+ *                SWE_ERR_ARG;
  *                params.cfl is used for every step, params.entropy_fix
  *                selects the step with the entropy fix, params.stream
  *                orders all work

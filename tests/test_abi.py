@@ -61,10 +61,10 @@ def _grid(nx=4, ny=3, dx=1.0, dy=1.0):
 
 def _params(**kw):
     p = dict(n_layers=1, precision=64, pollutant=1, g=9.81, r=0.0, cfl=0.9, stream=None,
-             entropy_fix=0)
+             entropy_fix=0, wet_dry=0, h_dry=0.0)
     p.update(kw)
     return S._Params(p["n_layers"], p["precision"], p["pollutant"], p["g"], p["r"], p["cfl"],
-                     p["stream"], p["entropy_fix"])
+                     p["stream"], p["entropy_fix"], p["wet_dry"], p["h_dry"])
 
 
 def _create(lib, grid, params, n=12, with_fields=True):
@@ -95,6 +95,13 @@ def _create(lib, grid, params, n=12, with_fields=True):
     (_grid(), _params(entropy_fix=2), S.SWE_ERR_ARG),
     (_grid(), _params(entropy_fix=-1), S.SWE_ERR_ARG),
     (_grid(), _params(n_layers=2, pollutant=0, r=0.5, entropy_fix=2), S.SWE_ERR_ARG),
+    (_grid(), _params(wet_dry=2, h_dry=1e-4), S.SWE_ERR_ARG),
+    (_grid(), _params(wet_dry=1, h_dry=-1e-4), S.SWE_ERR_ARG),
+    (_grid(), _params(wet_dry=1, h_dry=float("nan")), S.SWE_ERR_ARG),
+    (_grid(), _params(wet_dry=1, h_dry=float("inf")), S.SWE_ERR_ARG),
+    (_grid(), _params(n_layers=2, pollutant=0, r=0.5, wet_dry=1, h_dry=1e-4),
+     S.SWE_ERR_UNSUPPORTED),
+    (_grid(ny=524280), _params(wet_dry=1, h_dry=1e-4), S.SWE_ERR_ARG),
 ])
 def test_create_rejects_bad_arguments(lib, grid, params, expect):
     st, out = _create(lib, grid, params)
@@ -199,3 +206,17 @@ def test_valid_create_without_a_gpu_is_a_cuda_error(lib):
         pytest.skip("a GPU is present")
     st, out = _create(lib, _grid(), _params())
     assert st == S.SWE_ERR_CUDA and out is None
+
+
+def test_mesh_has_no_wet_dry_treatment(lib):
+    # refused before the mesh is prepared or any CUDA call
+    xy = np.array([0.0, 0.0, 1.0, 0.0, 0.0, 1.0])
+    tri = np.array([0, 1, 2], dtype=np.int32)
+    mesh = S._Mesh(3, xy.ctypes.data, 1, tri.ctypes.data, 1)
+    W = [np.ones(1), np.zeros(1), np.zeros(1), np.zeros(1)]
+    Wp = (C.c_void_p * 4)(*[w.ctypes.data for w in W])
+    H = np.zeros(1)
+    out = C.c_void_p(123)
+    st = lib.swe_create_mesh(C.byref(mesh), C.c_void_p(H.ctypes.data), Wp,
+                             C.byref(_params(wet_dry=1, h_dry=1e-4)), C.byref(out))
+    assert st == S.SWE_ERR_UNSUPPORTED and out.value is None

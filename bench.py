@@ -2,7 +2,8 @@
 """Throughput of the Roe finite-volume shallow-water step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload pulses8192|hills2048|dam128|interface2048|tri1024|tri1024_1l]
+                    [--workload pulses8192|hills2048|dam128|interface2048|tri1024|tri1024_1l|
+                                flood2048]
                     [--precision 32|64] [--entropy-fix]
 
 One "step" is one explicit time step of the IR-Roe scheme over the whole
@@ -130,6 +131,11 @@ DESCR = {
     "tri1024": "two layers on 1024x1024 unit squares split into 2,097,152 triangles, interior "
                "vertices jittered by +-0.2, cells shuffled then RCM-reordered, r=0.98, "
                "8 Gaussian hills, 0.5 m interface bump, at rest, reflective walls",
+    "flood2048": "one layer with pollutant and wet/dry fronts, 2048x2048 Cartesian, dx=10 m, "
+                 "bed rising 4 m across x plus 64 seeded Gaussian hills (amplitude "
+                 "U[0.5,2.5] m), lake at rest at level 0 (about half the domain dry), a disc "
+                 "of radius 2048 m raised by 2 m at the centre flooding dry land, "
+                 "h_dry=1e-4 m, Harten-Hyman entropy fix, reflective walls",
     "tri1024_1l": "one layer with pollutant on 1024x1024 unit squares split into 2,097,152 "
                   "triangles, interior vertices jittered by +-0.2, cells shuffled then "
                   "RCM-reordered, 6 Gaussian hills under a 2 m deep surface, 4 surface pulses "
@@ -165,6 +171,13 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
         return "hbm", (12 + e + nf * e) * n_cells + ne * e * n_edges, "B"
     if kernel == "mesh_update_kernel":
         return "hbm", 3 * nf * e * n_cells, "B"
+    # wet/dry on a grid: each field and each edge record crosses HBM once
+    if kernel == "wd_edge_kernel":    # h, qx, qy, hC, H read; 7 values per edge written
+        return "hbm", 5 * e * n_cells + 7 * e * n_edges, "B"
+    if kernel == "wd_cell_kernel":    # m and both speeds per edge, h read; tau written
+        return "hbm", 3 * e * n_edges + 2 * e * n_cells, "B"
+    if kernel == "wd_update_kernel":  # m, both momenta, t, c per edge, tau, 4 fields in/out
+        return "hbm", 5 * e * n_edges + 9 * e * n_cells, "B"
     raise KeyError(kernel)
 
 
@@ -251,7 +264,8 @@ class Sample:
                          f"walled {nx}x{rows} grid")
 
     def run(self, O, nsteps, W=None):
-        with O.entropy_fix(self.d.get("entropy_fix", 0)):
+        with O.entropy_fix(self.d.get("entropy_fix", 0)), \
+                O.wet_dry(self.d.get("h_dry", 0.0), on=bool(self.d.get("wet_dry", 0))):
             return self._run(O, nsteps, W)
 
     def _run(self, O, nsteps, W=None):
@@ -309,7 +323,7 @@ def workload_of(I, args):
 
 def workload_name(args, d, precision):
     s = f"{args.workload}: {DESCR[args.workload]}, fp{precision}"
-    if d.get("entropy_fix"):
+    if d.get("entropy_fix") and args.workload != "flood2048":
         s += ", Harten-Hyman entropy fix"
     return s
 
@@ -537,7 +551,8 @@ def main():
                                precision=precision, g=d["g"], cfl=d["cfl"],
                                stream=stream.cuda_stream, n_layers=nl,
                                pollutant=0 if two else 1, r=d.get("r", 0.0),
-                               entropy_fix=d.get("entropy_fix", 0))
+                               entropy_fix=d.get("entropy_fix", 0),
+                               wet_dry=d.get("wet_dry", 0), h_dry=d.get("h_dry", 0.0))
     info = S.swe_get_info(st)
 
     # warm-up (also gives a step-time estimate for the busy window below)

@@ -41,6 +41,7 @@ WORKLOADS = {
     "interface2048": dict(nx=2048, ny=2048, dx=10.0, steps=500, seed=1004, precision=64),
     "tri1024": dict(nx=1024, ny=1024, dx=1.0, steps=500, seed=1005, precision=32),
     "tri1024_1l": dict(nx=1024, ny=1024, dx=1.0, steps=500, seed=1006, precision=32),
+    "flood2048": dict(nx=2048, ny=2048, dx=10.0, steps=500, seed=1007, precision=32),
 }
 TWO_LAYER = ("interface2048", "tri1024")
 
@@ -176,18 +177,22 @@ def dry_dam_1d(nx, ny=4, length=2000.0, x_dam=1000.0, h0=2.0):
     return _as_fields(z, h, z, z, h.copy(), nx=nx, ny=ny, dx=dx, dy=dx)
 
 
-def emerged_hills(nx, ny, dx=10.0, seed=1007, n_hills=8, eta=None, column=None):
+def emerged_hills(nx, ny, dx=10.0, seed=1007, n_hills=8, eta=None, column=None, slope=0.0):
     """Gaussian hills (amplitude U[0.5, 2.5] m, sigma U[50, 300] m, centres
     U[0, L]^2) that pierce a lake at rest, for runs with the wet/dry
     treatment.  The surface ``eta`` (default: 0.3 m below the highest bed
     point) leaves the hill tops dry: h = max(0, eta - z_b) exactly, q = 0,
-    C per 16 x 16 block.  ``column = (cx, cy, radius, rise)`` raises the
-    surface by ``rise`` inside the disc (a dam break that floods dry land).
-    Draw order: hills (amp, sigma, cx, cy), then block concentrations."""
+    C per 16 x 16 block.  ``slope`` tilts the bed, z_b += slope (x - L/2),
+    so that one side of the domain is dry land.  ``column = (cx, cy,
+    radius, rise)`` raises the surface by ``rise`` inside the disc (a dam
+    break that floods dry land).  Draw order: hills (amp, sigma, cx, cy),
+    then block concentrations."""
     rng = np.random.Generator(np.random.PCG64(seed))
     lx, ly = nx * dx, ny * dx
     a, s, cx, cy = _hills(rng, n_hills, lx, ly, 0.5, 2.5)
     zb = _gaussian_sum(nx, ny, dx, dx, a, s, cx, cy)
+    if slope:
+        zb = zb + slope * ((np.arange(nx) + 0.5) * dx - 0.5 * lx)[None, :]
     C = _block_concentration(rng, nx, ny)
     level = zb.max() - 0.3 if eta is None else float(eta)
     surf = np.full_like(zb, level)
@@ -384,6 +389,17 @@ def make_workload(name, nx=None, ny=None, lake_at_rest=False):
         d = tri_workload(nx)
         d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
                  name=name)
+        return d
+    if name == "flood2048":
+        # wet/dry fronts: a bed rising 4 m across the domain with 64 hills
+        # (16 per 1024^2 cells), a lake at rest at level 0 (about half the
+        # domain dry), a disc of radius L/10 raised by 2 m at the centre
+        lx = nx * dx
+        n_h = max(8, int(round(64 * nx * ny / (2048 * 2048))))
+        d = emerged_hills(nx, ny, dx, seed=w["seed"], n_hills=n_h, eta=0.0,
+                          column=(0.5 * lx, 0.5 * ny * dx, 0.1 * lx, 2.0), slope=4.0 / lx)
+        d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
+                 name=name, wet_dry=1, h_dry=1e-4, entropy_fix=1)
         return d
     if name == "tri1024_1l":
         d = tri_workload1(nx, ny, seed=w["seed"])

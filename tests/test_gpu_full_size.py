@@ -1,0 +1,86 @@
+"""Every full-size workload over its own step count, on the GPU through the C
+ABI in the launch configuration the benchmark times (swe_run), against the
+oracle's records of the same seeded run (tests/golden/full_*.json, written by
+tests/golden/make_full_size.py through the fp64 CPU oracle alone):
+
+    hills2048   2048 x 2048, one layer + pollutant, 1000 steps, fp64 and fp32
+    pulses8192  8192 x 8192, one layer + pollutant,  200 steps, fp32
+    tri1024     2,097,152 triangles, two layers,      500 steps, fp32
+
+Checked: the dt of every step (eq. (5) of An MPI-CUDA implementation of an
+improved Roe method for two-layer shallow water systems, Sec. 2.2) and the
+clock; the final state (eq. (4)) at the record's ~2,300 seeded cells, walls
+and corners included, and each field's mean over 1,024 blocks that tile the
+domain, every value relative to the field's scale; the area-weighted sums of
+the conserved quantities.  Tolerances as everywhere: fp64 1e-10 per field and
+1e-12 on dt; fp32 1e-4 on depths, 1e-3 on discharges and hC, 1e-6 on dt.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from finite_volume_shallow_gb300 import inputs as I
+from gpu_util import TOL, TOL2, gpu_run, gpu_run_mesh
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+CASES = [("hills2048", 64), ("hills2048", 32)]
+
+
+def _block_means_grid(w, nx, ny, nb=32):
+    return w.reshape(nb, ny // nb, nb, nx // nb).mean(axis=(1, 3)).reshape(-1)
+
+
+def _block_means_chunks(w, nb=32):
+    return np.array([c.mean() for c in np.array_split(w, nb * nb)])
+
+
+@pytest.mark.parametrize("name,precision", CASES)
+def test_full_size_over_the_workloads_own_steps(name, precision):
+    path = os.path.join(GOLDEN, f"full_{name}_fp{precision}.json")
+    assert os.path.exists(path), f"missing oracle record {path}"
+    rec = json.load(open(path))
+    d = I.make_workload(name)
+    steps = rec["steps"]
+    assert steps == d["steps"]
+    mesh = name == "tri1024"
+    if mesh:
+        W, dts, t = gpu_run_mesh(d, precision, steps)
+        tol = TOL2[precision]
+        p = d["xy"][d["tri"]]  # shoelace areas of the triangles
+        area = 0.5 * ((p[:, 1, 0] - p[:, 0, 0]) * (p[:, 2, 1] - p[:, 0, 1])
+                      - (p[:, 2, 0] - p[:, 0, 0]) * (p[:, 1, 1] - p[:, 0, 1]))
+    else:
+        W, dts, t = gpu_run(d, precision, steps, use_run=True)
+        tol = TOL[precision]
+        area = d["dx"] * d["dy"]
+    names = rec["fields"]
+    # every step's dt and the clock
+    dto = np.array(rec["dts"])
+    assert len(dts) == steps
+    dte = float(np.abs(dts / dto - 1.0).max())
+    # the final state at the sampled cells and the block means
+    cells = np.array(rec["cells"])
+    errs, berrs = {}, {}
+    for k, nm in enumerate(names):
+        scale = rec["scale"][nm]
+        errs[nm] = float(np.abs(W[k][cells] - np.array(rec["values"][nm])).max() / scale)
+        bm = _block_means_chunks(W[k]) if mesh else _block_means_grid(W[k], d["nx"], d["ny"])
+        berrs[nm] = float(np.abs(bm - np.array(rec["block_means"][nm])).max() / scale)
+    print(f"\nFULLSIZE {name} fp{precision} steps={steps} dt_rel={dte:.3e} "
+          f"cells={ {k: f'{v:.2e}' for k, v in errs.items()} } "
+          f"blocks={ {k: f'{v:.2e}' for k, v in berrs.items()} }")
+    assert dte <= tol["dt"], dte
+    assert abs(t / rec["t"] - 1.0) <= tol["dt"]
+    for nm in names:
+        assert errs[nm] <= tol[nm], (nm, errs)
+        assert berrs[nm] <= tol[nm], (nm, berrs)
+    # conservation of the depths (and the pollutant) by the GPU run itself
+    mass = ("h1", "h2") if mesh else ("h", "hC")
+    for nm in mass:
+        k = names.index(nm)
+        s = W[k].dot(area) if mesh else W[k].sum() * area
+        assert abs(s / rec["sum0"][nm] - 1.0) <= (1e-12 if precision == 64 else 1e-5), nm

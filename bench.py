@@ -80,10 +80,10 @@ KERNEL_SOURCES = {
     "cart1_step_kernel": (("swe_cart1.cu", "swe_internal.h"), "cart1_step_traffic.txt"),
     # (swe_fastmath.cuh is used by the fp64 kernels only, which have no
     # traffic record)
-    "cart2_flux_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
-                          "cart2_flux_traffic.txt"),
-    "cart2_step_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
-                          "cart2_flux_traffic.txt"),
+    "cart2_march_kernel<plain>": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
+                                  "cart2_flux_traffic.txt"),
+    "cart2_march_kernel<fused>": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
+                                  "cart2_flux_traffic.txt"),
     "cart2_update_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
                             "cart2_flux_traffic.txt"),
     "mesh_edge_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"), "mesh_traffic.txt"),
@@ -153,9 +153,9 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
         if precision == 64:
             return "alu", FLOPS_PER_CELL_1L * n_cells, "flop"
         return "hbm", BYTES_PER_CELL[precision] * n_cells, "B"
-    if kernel == "cart2_flux_kernel":
+    if kernel == "cart2_march_kernel<plain>":
         return "alu", FLOPS_PER_CELL_2L[precision] * n_cells, "flop"
-    if kernel == "cart2_step_kernel":   # + the fused update, 6 FMAs per cell
+    if kernel == "cart2_march_kernel<fused>":   # + the fused update, 6 FMAs per cell
         return "alu", (FLOPS_PER_CELL_2L[precision] + 12) * n_cells, "flop"
     if kernel == "cart2_update_kernel":
         return "hbm", 3 * 6 * e * n_cells, "B"

@@ -138,6 +138,27 @@ swe_status plan_launch(swe_state* s) {
   return SWE_OK;
 }
 
+// Two layers: one warp per (band of kBand2 columns, row segment), about one
+// unit per resident warp; segments of at least 16 rows.
+template <typename T>
+swe_status plan_launch2(swe_state* s) {
+  int bpsm = 0, dev = 0, sms = 0;
+  CK(march2_occupancy<T>(&bpsm, s->p.entropy_fix != 0));
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (bpsm < 1) return SWE_ERR_CUDA;
+  const int64_t slots = (int64_t)sms * bpsm * kMarch2Warps;
+  const int64_t nb = (s->nx + kBand2 - 1) / kBand2;
+  int64_t S = slots / nb;
+  const int64_t most = s->ny / 16 > 1 ? s->ny / 16 : 1;
+  if (S > most) S = most;
+  if (S < 1) S = 1;
+  s->nbands = (int)nb;
+  s->nsegs = (int)S;
+  s->nsegs_wall = (int)S;
+  return SWE_OK;
+}
+
 template <typename T>
 swe_status enqueue_dt0(swe_state* s) {
   // all three wave-speed slots to zero, then slot (step % 3) <- max of W^n
@@ -239,6 +260,8 @@ swe_status enqueue_step2(swe_state* s, double cfl, bool last) {
   f.tmax_out = slot(m);
   f.err = s->err;
   f.efix = s->p.entropy_fix;
+  f.nbands = s->nbands;
+  f.nsegs = s->nsegs;
   auto upd_args = [&](Update2Args<T>& u, int a, int dst, int64_t step, double c, bool end) {
     for (int k = 0; k < 6; ++k) {
       u.win[k] = (const T*)s->w[a][k];
@@ -470,8 +493,8 @@ void timing_names(swe_state* s, Timing* tm) {
     tm->names[2] = "mesh_update_kernel";
   } else if (s->nl == 2) {
     tm->nk = 3;
-    tm->names[0] = "cart2_flux_kernel";
-    tm->names[1] = "cart2_step_kernel";
+    tm->names[0] = "cart2_march_kernel<plain>";
+    tm->names[1] = "cart2_march_kernel<fused>";
     tm->names[2] = "cart2_update_kernel";
   } else {
     tm->nk = 1;
@@ -676,11 +699,6 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
   // wet/dry: one block per 8 rows of edges in the launch's y dimension
   if (params->wet_dry == 1 && ((int64_t)grid->ny + 1 + 7) / 8 > 65535) return SWE_ERR_ARG;
-  // two layers: one block per tile row in the grid's y dimension (<= 65535)
-  if (params->n_layers == 2) {
-    const int64_t ty = params->precision == 32 ? Tile2Y<float>::v : Tile2Y<double>::v;
-    if (((int64_t)grid->ny + ty - 1) / ty > 65535) return SWE_ERR_ARG;
-  }
 
   swe_state* s = new (std::nothrow) swe_state();
   if (!s) return SWE_ERR_OOM;
@@ -755,10 +773,9 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
 
-  if (s->nl == 1) {
-    st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
-    if (st != SWE_OK) return fail(st);
-  }
+  if (s->nl == 1) st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
+  else st = s->prec == 32 ? plan_launch2<float>(s) : plan_launch2<double>(s);
+  if (st != SWE_OK) return fail(st);
   st = s->prec == 32 ? fill_pads<float>(s) : fill_pads<double>(s);
   if (st != SWE_OK) return fail(st);
   void* hdst[1] = {s->H};

@@ -7,24 +7,25 @@
 // with the 4x4 Roe matrix A_ij of the rotated system, CFL eq. (5)).
 //
 // Kernels:
-//   cart2_flux_kernel    a 32 x 8 tile of cells and its one-cell halo in
-//                        shared memory; every edge of the tile evaluated once
-//                        (as in the tile scheme of A multi-GPU shallow-water
-//                        simulation with transport of contaminants, Figure
-//                        4); each cell sums its four edges into the residual
-//                        R (global scratch) and max-reduces sum |Gamma| ||D||,
-//                        which fixes dt of this step;
-//   cart2_step_kernel    the same with the update of the previous step fused
-//                        into the tile load: it reads W^{n-1}, R^{n-1} and
-//                        the wave-speed maximum of W^{n-1}, forms W^n =
-//                        W^{n-1} - (dt/dx) R^{n-1} for the tile and its halo,
-//                        writes W^n of its own cells to the other buffer and
-//                        evaluates the fluxes of W^n (W and R alternate
-//                        between two buffers);
+//   cart2_march_kernel   one warp per (column band, row segment) marches up
+//                        its rows; each lane evaluates the x-edge east of its
+//                        cell and the y-edge below it (as one FP32x2
+//                        evaluation in fp32), so every edge is computed once
+//                        except at band and segment borders, and the edge
+//                        results pass between cells by warp shuffles and
+//                        registers (the idea of A multi-GPU shallow-water
+//                        simulation with transport of contaminants, Figure 4,
+//                        at warp level).  Each cell sums its four edges into
+//                        the residual R and max-reduces sum |Gamma| ||D||,
+//                        which fixes dt of this step.  FUSED: the update of
+//                        the previous step is applied to every cell as it is
+//                        loaded (W^n = W^{n-1} - (dt/dx) R^{n-1}, W and R
+//                        alternate between two buffers) and W^n of the own
+//                        cells is written;
 //   cart2_update_kernel  W -= (dt/dx) R (16-byte vectors over whole rows, the
 //                        padding left as it is), checks, dt bookkeeping: a
 //                        lone step, and the last step of a run.
-// A run of n >= 2 steps is one flux launch, n - 1 fused launches and one
+// A run of n >= 2 steps is one plain march, n - 1 fused marches and one
 // update; every form applies the update with the same rounding (upd below),
 // so a run and the same steps taken one at a time agree bit for bit.
 //
@@ -38,11 +39,6 @@
 
 namespace swe {
 namespace {
-
-// per-cell quantities in shared memory
-enum { C_H1, C_Q1X, C_Q1Y, C_H2, C_Q2X, C_Q2Y, C_H, C_S1, C_S2, C_RS1, C_RS2, NCQ };
-
-constexpr int TX = kTile2X;
 
 // Early exit of the outer Newton iteration (warp vote): always for fp64;
 // for fp32 a compile-time choice (SWE_CART2_ADAPT32; on by default: 162 us
@@ -87,162 +83,243 @@ template <typename T> struct Vec2;
 template <> struct Vec2<float> { using type = float4; static constexpr int n = 4; };
 template <> struct Vec2<double> { using type = double2; static constexpr int n = 2; };
 
-template <typename T, int TY>
-__device__ __forceinline__ Side2<T> side_of(const T (*c)[TY + 2][TX + 2], int lj, int li,
-                                            bool xdir) {
+// ---- the row march -----------------------------------------------------------
+// One warp per (column band, row segment).  Lane l of band b holds column
+// x = kBand2 * b - 1 + l: lanes 1..30 own their columns, lanes 0 and 31 are
+// the one-cell halo.  The warp marches up rows y0 - 1 .. y1 of its segment;
+// at row r each lane evaluates, in one FP32x2 evaluation in fp32 (one after
+// the other in fp64 and with the entropy fix), the x-edge east of its cell
+// and the y-edge below it.  The west x-edge's results come from the lane on
+// the left by shuffle; the residual of row r - 1 is complete once the
+// y-edge above it is known (row r), and is written then.
+
+// one cell of a row: per layer depth, discharge (x, y), sqrt(h), 1/sqrt(h);
+// the bottom depth
+template <typename T>
+struct Cell2 {
+  T h[2], qx[2], qy[2], s[2], rs[2], H;
+};
+
+template <typename T>
+__device__ __forceinline__ void derive(Cell2<T>& c) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    c.rs[k] = M2<T>::rsq(c.h[k]);
+    c.s[k] = c.h[k] * c.rs[k];
+  }
+}
+
+// the cell seen from an x-edge (normal (1, 0)) or a y-edge (normal (0, 1));
+// `mirror`: the reflective wall's ghost (normal discharge negated)
+template <typename T>
+__device__ __forceinline__ Side2<T> side2(const Cell2<T>& c, bool xdir, bool mirror) {
   Side2<T> s;
-  s.h[0] = c[C_H1][lj][li];
-  s.h[1] = c[C_H2][lj][li];
-  s.s[0] = c[C_S1][lj][li];
-  s.s[1] = c[C_S2][lj][li];
-  s.rs[0] = c[C_RS1][lj][li];
-  s.rs[1] = c[C_RS2][lj][li];
-  // normal / tangential discharge: x-edges (q_x, q_y); y-edges (q_y, q_x),
-  // the tangential flux of a y-edge going to the x-momentum
-  s.qn[0] = xdir ? c[C_Q1X][lj][li] : c[C_Q1Y][lj][li];
-  s.qt[0] = xdir ? c[C_Q1Y][lj][li] : c[C_Q1X][lj][li];
-  s.qn[1] = xdir ? c[C_Q2X][lj][li] : c[C_Q2Y][lj][li];
-  s.qt[1] = xdir ? c[C_Q2Y][lj][li] : c[C_Q2X][lj][li];
-  s.H = c[C_H][lj][li];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    s.h[k] = c.h[k];
+    s.s[k] = c.s[k];
+    s.rs[k] = c.rs[k];
+    const T n = xdir ? c.qx[k] : c.qy[k];
+    s.qn[k] = mirror ? -n : n;
+    s.qt[k] = xdir ? c.qy[k] : c.qx[k];
+  }
+  s.H = c.H;
   return s;
 }
 
-// FUSED: the cart2_step_kernel form (U carries the previous step's update);
-// otherwise U is unused.  EFIX: the entropy fix of edge2.
-template <typename T, bool ANISO, bool FUSED, bool EFIX>
-__device__ __forceinline__ void flux_tile(const Step2Args<T>& A, const Update2Args<T>& U) {
-  constexpr int TY = Tile2Y<T>::v;
-  __shared__ T cq[NCQ][TY + 2][TX + 2];
-  __shared__ T ex[NEQ][TY][TX + 1];   // x-edge e joins local columns e and e + 1
-  __shared__ T ey[NEQ][TY + 1][TX];   // y-edge e joins local rows e and e + 1
-  __shared__ T k_sh;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  const int t = ty * TX + tx;
-  const int i0 = blockIdx.x * TX, j0 = blockIdx.y * TY;
-  const int nx = A.nx, ny = A.ny;
-  const T g = A.g, gh = T(0.5) * A.g, r = A.r;
-  pdl_wait();
-  const T k = FUSED ? dt_of_step<T>(U, &k_sh) : T(0);
-  unsigned bad = 0;
+template <typename T>
+__device__ __forceinline__ Cell2<T> shfl_down_cell(const Cell2<T>& c) {
+  Cell2<T> o;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    o.h[k] = __shfl_down_sync(kFull2, c.h[k], 1);
+    o.qx[k] = __shfl_down_sync(kFull2, c.qx[k], 1);
+    o.qy[k] = __shfl_down_sync(kFull2, c.qy[k], 1);
+    o.s[k] = __shfl_down_sync(kFull2, c.s[k], 1);
+    o.rs[k] = __shfl_down_sync(kFull2, c.rs[k], 1);
+  }
+  o.H = __shfl_down_sync(kFull2, c.H, 1);
+  return o;
+}
 
-  // tile + one-cell halo (the padded layout keeps every read in bounds)
-  for (int idx = t; idx < (TX + 2) * (TY + 2); idx += TX * TY) {
-    const int li = idx % (TX + 2), lj = idx / (TX + 2);
-    const int64_t o = (int64_t)(j0 - 1 + lj + kPadY) * A.pitch + (i0 - 1 + li + kPadX);
-    T w[6];
+// Both edges of a lane: ox for (a_x, b_x), oy for (a_y, b_y); returns bit 0
+// (bit 1) when the x-edge's (y-edge's) Roe matrix has real eigenvalues.
+template <typename T, bool EFIX>
+__device__ __forceinline__ unsigned edge_pair(const Side2<T>& ax, const Side2<T>& bx, bool wx,
+                                              const Side2<T>& ay, const Side2<T>& by, bool wy,
+                                              T g, T gh, T r, T ox[NEQ], T oy[NEQ]) {
+  unsigned ok = edge2<T, kAdapt2<T>, EFIX>(ax, bx, g, gh, r, wx, ox) ? 1u : 0u;
+  ok |= edge2<T, kAdapt2<T>, EFIX>(ay, by, g, gh, r, wy, oy) ? 2u : 0u;
+  return ok;
+}
+__device__ __forceinline__ Side2P pack2(const Side2<float>& x, const Side2<float>& y) {
+  Side2P p;
 #pragma unroll
-    for (int f = 0; f < 6; ++f) w[f] = A.w[f][o];
-    if (FUSED) {
-      // the previous step's update, on cells of the grid only (the padding
-      // keeps its resting state); the tile's own cells are written out
-      const int gi = i0 - 1 + li, gj = j0 - 1 + lj;
-      if (gi >= 0 && gi < nx && gj >= 0 && gj < ny) {
+  for (int k = 0; k < 2; ++k) {
+    p.h[k] = f2(x.h[k], y.h[k]);
+    p.s[k] = f2(x.s[k], y.s[k]);
+    p.rs[k] = f2(x.rs[k], y.rs[k]);
+    p.qn[k] = f2(x.qn[k], y.qn[k]);
+    p.qt[k] = f2(x.qt[k], y.qt[k]);
+  }
+  p.H = f2(x.H, y.H);
+  return p;
+}
+template <>
+__device__ __forceinline__ unsigned edge_pair<float, false>(
+    const Side2<float>& ax, const Side2<float>& bx, bool wx, const Side2<float>& ay,
+    const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
+  float2 o[NEQ];
+  const unsigned ok = edge2p(pack2(ax, ay), pack2(bx, by), g, gh, r, wx, wy, o);
 #pragma unroll
-        for (int f = 0; f < 6; ++f) w[f] = upd(w[f], k, U.R[f][o]);
-        if (li >= 1 && li <= TX && lj >= 1 && lj <= TY) {
+  for (int q = 0; q < NEQ; ++q) {
+    ox[q] = o[q].x;
+    oy[q] = o[q].y;
+  }
+  return ok;
+}
+
+// what a cell takes from the x-edge on its west (it is side b) and from the
+// y-edge below it: mass fluxes, P^+ d of the normal momentum, tangential
+// fluxes, ||D|| (the order of the shuffled and carried arrays)
+enum { B_M1, B_PS1, B_T1, B_M2, B_PS2, B_T2, B_D, NB };
+
+// Resident blocks per SM the registers are held to (four-warp blocks).
+#ifndef SWE_MARCH2_MIN_BLOCKS
+#define SWE_MARCH2_MIN_BLOCKS 4
+#endif
+template <typename T, bool EFIX> struct MinBlocks2 { static constexpr int v = 1; };
+template <> struct MinBlocks2<float, false> { static constexpr int v = SWE_MARCH2_MIN_BLOCKS; };
+
+// FUSED: the pass also applies the previous step's update to every cell it
+// loads (W^n = W^{n-1} - (dt/dx) R^{n-1}) and writes W^n of its own cells.
+template <typename T, bool ANISO, bool FUSED, bool EFIX>
+__global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
+    cart2_march_kernel(const Step2Args<T> A, const Update2Args<T> U) {
+  __shared__ T k_sh;
+  pdl_wait();
+  const T kdt = FUSED ? dt_of_step<T>(U, &k_sh) : T(0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nx = A.nx, ny = A.ny, nb = A.nbands, ns = A.nsegs;
+  const int unit = blockIdx.x * kMarch2Warps + warp;
+  T tmax = T(0);
+  unsigned bad = 0, hyp_ok = 1u;
+  if (unit < nb * ns) {
+    const int band = unit % nb, seg = unit / nb;
+    const int y0 = (int)((int64_t)seg * ny / ns), y1 = (int)((int64_t)(seg + 1) * ny / ns);
+    const int x = kBand2 * band - 1 + lane;
+    const bool own_x = lane >= 1 && lane <= kBand2 && x < nx;
+    const bool in_x = x >= 0 && x < nx;
+    const bool need_ex = lane <= kBand2 && x >= -1 && x <= nx - 1;  // x-edges used
+    const T g = A.g, gh = T(0.5) * A.g, r = A.r, rho = A.rho;
+    auto ys = [&](T v) { return ANISO ? v * rho : v; };
+    int64_t o = (int64_t)(y0 - 1 + kPadY) * A.pitch + x + kPadX;
+    // row y0 - 1 into registers
+    T w[6], R[6], Hn;
+    auto load = [&](int64_t at, T* wv, T* rv, T& hv) {
 #pragma unroll
-          for (int f = 0; f < 6; ++f) U.w[f][o] = w[f];
-          const T sum = ((w[0] + w[1]) + (w[2] + w[3])) + (w[4] + w[5]);
-          if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
-          if (!(w[0] > T(0)) || !(w[3] > T(0))) bad |= kErrDepth;
+      for (int f = 0; f < 6; ++f) wv[f] = A.w[f][at];
+      if (FUSED) {
+#pragma unroll
+        for (int f = 0; f < 6; ++f) rv[f] = U.R[f][at];
+      }
+      hv = A.H[at];
+    };
+    load(o, w, R, Hn);
+    Cell2<T> prev;
+    T xr[6], xd = T(0), yb[NB];  // row r - 1: x-part of its residual, its south edge
+#pragma unroll
+    for (int f = 0; f < 6; ++f) xr[f] = T(0);
+#pragma unroll
+    for (int q = 0; q < NB; ++q) yb[q] = T(0);
+    for (int rr = y0 - 1; rr <= y1; ++rr, o += A.pitch) {
+      // ---- the row: previous step's update (fused), next row's loads -----
+      Cell2<T> cur;
+      {
+        T wc[6];
+#pragma unroll
+        for (int f = 0; f < 6; ++f) wc[f] = w[f];
+        if (FUSED && in_x && rr >= 0 && rr < ny) {
+#pragma unroll
+          for (int f = 0; f < 6; ++f) wc[f] = upd(wc[f], kdt, R[f]);
+          if (own_x && rr >= y0 && rr < y1) {
+#pragma unroll
+            for (int f = 0; f < 6; ++f) U.w[f][o] = wc[f];
+            const T sum = ((wc[0] + wc[1]) + (wc[2] + wc[3])) + (wc[4] + wc[5]);
+            if (!(fabs(sum) <= M2<T>::big())) bad |= kErrNonfinite;
+            if (!(wc[0] > T(0)) || !(wc[3] > T(0))) bad |= kErrDepth;
+          }
+        }
+        cur.h[0] = wc[0]; cur.qx[0] = wc[1]; cur.qy[0] = wc[2];
+        cur.h[1] = wc[3]; cur.qx[1] = wc[4]; cur.qy[1] = wc[5];
+        cur.H = Hn;
+      }
+      if (rr < y1) load(o + A.pitch, w, R, Hn);
+      derive(cur);
+      if (rr >= y0) {
+        // ---- the x-edge east of the cell, the y-edge below it ---------------
+        const Cell2<T> right = shfl_down_cell(cur);
+        const bool lw = x == -1, rw = x == nx - 1;
+        const Side2<T> ax = lw ? side2(right, true, true) : side2(cur, true, false);
+        const Side2<T> bx = rw ? side2(cur, true, true) : side2(right, true, false);
+        const bool bw = rr == 0, tw = rr == ny;
+        const Side2<T> ay = bw ? side2(cur, false, true) : side2(prev, false, false);
+        const Side2<T> by = tw ? side2(prev, false, true) : side2(cur, false, false);
+        T ox[NEQ], oy[NEQ];
+        const unsigned ok = edge_pair<T, EFIX>(ax, bx, lw || rw, ay, by, bw || tw, g, gh, r,
+                                               ox, oy);
+        const bool row_x = rr < y1;  // this row's x-edges are used
+        if (row_x && need_ex && !(ok & 1u)) hyp_ok = 0u;
+        if (own_x && !(ok & 2u)) hyp_ok = 0u;
+        // ---- row r - 1 is complete: its north edge is this y-edge ---------
+        if (rr - 1 >= y0 && own_x) {
+          T Rn[6];
+          Rn[0] = xr[0] + ys(oy[E_M1] - yb[B_M1]);
+          Rn[1] = xr[1] + ys(oy[E_T1] - yb[B_T1]);
+          Rn[2] = xr[2] + ys(oy[E_PM1] + yb[B_PS1]);
+          Rn[3] = xr[3] + ys(oy[E_M2] - yb[B_M2]);
+          Rn[4] = xr[4] + ys(oy[E_T2] - yb[B_T2]);
+          Rn[5] = xr[5] + ys(oy[E_PM2] + yb[B_PS2]);
+          const T ts = xd + ys(yb[B_D] + oy[E_D]);
+          const int64_t ob = o - A.pitch;
+#pragma unroll
+          for (int f = 0; f < 6; ++f) A.R[f][ob] = Rn[f];
+          tmax = nanmax2(tmax, ts);
+        }
+        // ---- this row's x-part, from the east edge and (shuffled) the west
+        {
+          T wv[NB];
+          wv[B_M1] = __shfl_up_sync(kFull2, ox[E_M1], 1);
+          wv[B_PS1] = __shfl_up_sync(kFull2, ox[E_PS1], 1);
+          wv[B_T1] = __shfl_up_sync(kFull2, ox[E_T1], 1);
+          wv[B_M2] = __shfl_up_sync(kFull2, ox[E_M2], 1);
+          wv[B_PS2] = __shfl_up_sync(kFull2, ox[E_PS2], 1);
+          wv[B_T2] = __shfl_up_sync(kFull2, ox[E_T2], 1);
+          wv[B_D] = __shfl_up_sync(kFull2, ox[E_D], 1);
+          xr[0] = ox[E_M1] - wv[B_M1];
+          xr[1] = ox[E_PM1] + wv[B_PS1];
+          xr[2] = ox[E_T1] - wv[B_T1];
+          xr[3] = ox[E_M2] - wv[B_M2];
+          xr[4] = ox[E_PM2] + wv[B_PS2];
+          xr[5] = ox[E_T2] - wv[B_T2];
+          xd = wv[B_D] + ox[E_D];
+          yb[B_M1] = oy[E_M1];
+          yb[B_PS1] = oy[E_PS1];
+          yb[B_T1] = oy[E_T1];
+          yb[B_M2] = oy[E_M2];
+          yb[B_PS2] = oy[E_PS2];
+          yb[B_T2] = oy[E_T2];
+          yb[B_D] = oy[E_D];
         }
       }
+      prev = cur;
     }
-    const T h1 = w[0], h2 = w[3];
-    cq[C_H1][lj][li] = h1;
-    cq[C_Q1X][lj][li] = w[1];
-    cq[C_Q1Y][lj][li] = w[2];
-    cq[C_H2][lj][li] = h2;
-    cq[C_Q2X][lj][li] = w[4];
-    cq[C_Q2Y][lj][li] = w[5];
-    cq[C_H][lj][li] = A.H[o];
-    const T r1 = M2<T>::rsq(h1), r2 = M2<T>::rsq(h2);
-    cq[C_RS1][lj][li] = r1;
-    cq[C_RS2][lj][li] = r2;
-    cq[C_S1][lj][li] = h1 * r1;
-    cq[C_S2][lj][li] = h2 * r2;
   }
-  __syncthreads();
-
-  bool hyper_ok = true;
-  // x-edges: (TX + 1) per row; global column of the left cell i0 - 1 + e
-  for (int k = t; k < (TX + 1) * TY; k += TX * TY) {
-    const int e = k % (TX + 1), row = k / (TX + 1);
-    const int gl = i0 - 1 + e;  // left cell's global column
-    Side2<T> a = side_of<T, TY>(cq, row + 1, e, true);
-    Side2<T> b = side_of<T, TY>(cq, row + 1, e + 1, true);
-    const bool lw = gl == -1, rw = gl == nx - 1;
-    if (lw) mirror2(a, b);
-    if (rw) mirror2(b, a);
-    T out[NEQ];
-    hyper_ok &= edge2<T, kAdapt2<T>, EFIX>(a, b, g, gh, r, lw || rw, out);
-#pragma unroll
-    for (int q = 0; q < NEQ; ++q) ex[q][row][e] = out[q];
-  }
-  // y-edges: TY + 1 per column; global row of the lower cell j0 - 1 + e.
-  // The thread index is rotated by one warp, so that the second pass of the
-  // y-edges falls on the last warp, not on the one that took the x-edges'
-  // second pass.
-  for (int k = (t + TX * TY - 32) % (TX * TY); k < TX * (TY + 1); k += TX * TY) {
-    const int col = k % TX, e = k / TX;
-    const int gl = j0 - 1 + e;
-    Side2<T> a = side_of<T, TY>(cq, e, col + 1, false);
-    Side2<T> b = side_of<T, TY>(cq, e + 1, col + 1, false);
-    const bool lw = gl == -1, rw = gl == ny - 1;
-    if (lw) mirror2(a, b);
-    if (rw) mirror2(b, a);
-    T out[NEQ];
-    hyper_ok &= edge2<T, kAdapt2<T>, EFIX>(a, b, g, gh, r, lw || rw, out);
-#pragma unroll
-    for (int q = 0; q < NEQ; ++q) ey[q][e][col] = out[q];
-  }
-  __syncthreads();
-
-  // residual of this thread's cell: east and north edges as the left/lower
-  // side, west and south as the right/upper side
-  const int gi = i0 + tx, gj = j0 + ty;
-  const bool own = gi < nx && gj < ny;
-  const T rho = A.rho;
-  auto ys = [&](T v) { return ANISO ? v * rho : v; };
-  T R[6];
-  R[0] = (ex[E_M1][ty][tx + 1] - ex[E_M1][ty][tx]) + ys(ey[E_M1][ty + 1][tx] - ey[E_M1][ty][tx]);
-  R[1] = (ex[E_PM1][ty][tx + 1] + ex[E_PS1][ty][tx]) + ys(ey[E_T1][ty + 1][tx] - ey[E_T1][ty][tx]);
-  R[2] = (ex[E_T1][ty][tx + 1] - ex[E_T1][ty][tx]) + ys(ey[E_PM1][ty + 1][tx] + ey[E_PS1][ty][tx]);
-  R[3] = (ex[E_M2][ty][tx + 1] - ex[E_M2][ty][tx]) + ys(ey[E_M2][ty + 1][tx] - ey[E_M2][ty][tx]);
-  R[4] = (ex[E_PM2][ty][tx + 1] + ex[E_PS2][ty][tx]) + ys(ey[E_T2][ty + 1][tx] - ey[E_T2][ty][tx]);
-  R[5] = (ex[E_T2][ty][tx + 1] - ex[E_T2][ty][tx]) + ys(ey[E_PM2][ty + 1][tx] + ey[E_PS2][ty][tx]);
-  const T Tsum = (ex[E_D][ty][tx] + ex[E_D][ty][tx + 1]) +
-                 ys(ey[E_D][ty][tx] + ey[E_D][ty + 1][tx]);
-  if (own) {
-    const int64_t o = (int64_t)(gj + kPadY) * A.pitch + gi + kPadX;
-#pragma unroll
-    for (int f = 0; f < 6; ++f) A.R[f][o] = R[f];
-  }
-  // hyperbolicity of every edge of this block, and the block's max of T
-  if (!__all_sync(kFull2, hyper_ok) && (tx & 31) == 0) atomicOr(A.err, kErrHyperbolic);
+  // hyperbolicity and the checks of this warp, the block's max of sum L ||D||
+  if (!__all_sync(kFull2, hyp_ok != 0u) && lane == 0) atomicOr(A.err, kErrHyperbolic);
   if (FUSED && bad) atomicOr(A.err, bad);
-  T m = own ? Tsum : T(0);
   pdl_trigger();
-  block_max_publish<T, TX * TY / 32>(m, A.tmax_out);
-}
-
-// Resident blocks per SM the registers are held to: five 256-thread fp32
-// tiles (48 registers) fit next to their 35 KB of shared memory each; fp64
-// tiles are bounded by shared memory and the FP64 pipe; the entropy-fix
-// variants (two more root solves per edge) are left to the compiler.
-template <typename T, bool EFIX> struct MinBlocks2 { static constexpr int v = 1; };
-template <> struct MinBlocks2<float, false> { static constexpr int v = 5; };
-
-template <typename T, bool ANISO, bool EFIX>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T, EFIX>::v)
-    cart2_flux_kernel(const Step2Args<T> A) {
-  flux_tile<T, ANISO, false, EFIX>(A, Update2Args<T>{});
-}
-
-template <typename T, bool ANISO, bool EFIX>
-__global__ void __launch_bounds__(kTile2X * Tile2Y<T>::v, MinBlocks2<T, EFIX>::v)
-    cart2_step_kernel(const Step2Args<T> A, const Update2Args<T> U) {
-  flux_tile<T, ANISO, true, EFIX>(A, U);
+  block_max_publish<T, kMarch2Warps>(tmax, A.tmax_out);
 }
 
 template <typename T>
@@ -310,28 +387,35 @@ __global__ void cart2_check_kernel(const Fields6<T> w6, int nx, int ny, int pitc
 }  // namespace
 
 template <typename T>
-cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st) {
-  constexpr int TY = Tile2Y<T>::v;
-  dim3 block(TX, TY);
-  dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
+cudaError_t march2_occupancy(int* blocks_per_sm, bool efix) {
+  return efix ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    blocks_per_sm, cart2_march_kernel<T, false, true, true>, kMarch2Warps * 32, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    blocks_per_sm, cart2_march_kernel<T, false, true, false>, kMarch2Warps * 32,
+                    0);
+}
+
+template <typename T, bool FUSED>
+cudaError_t launch_march2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st) {
+  const int units = f.nbands * f.nsegs;
+  const dim3 grid((unsigned)((units + kMarch2Warps - 1) / kMarch2Warps));
+  const dim3 block(kMarch2Warps * 32);
+  const bool aniso = f.rho != T(1);
   if (f.efix)
-    return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false, true>, grid, block, 0, st, f)
-                         : launch_pdl(cart2_flux_kernel<T, true, true>, grid, block, 0, st, f);
-  return f.rho == T(1) ? launch_pdl(cart2_flux_kernel<T, false, false>, grid, block, 0, st, f)
-                       : launch_pdl(cart2_flux_kernel<T, true, false>, grid, block, 0, st, f);
+    return aniso ? launch_pdl(cart2_march_kernel<T, true, FUSED, true>, grid, block, 0, st, f, u)
+                 : launch_pdl(cart2_march_kernel<T, false, FUSED, true>, grid, block, 0, st, f, u);
+  return aniso ? launch_pdl(cart2_march_kernel<T, true, FUSED, false>, grid, block, 0, st, f, u)
+               : launch_pdl(cart2_march_kernel<T, false, FUSED, false>, grid, block, 0, st, f, u);
+}
+
+template <typename T>
+cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st) {
+  return launch_march2<T, false>(f, Update2Args<T>{}, st);
 }
 
 template <typename T>
 cudaError_t launch_fused2(const Step2Args<T>& f, const Update2Args<T>& u, cudaStream_t st) {
-  constexpr int TY = Tile2Y<T>::v;
-  dim3 block(TX, TY);
-  dim3 grid((unsigned)((f.nx + TX - 1) / TX), (unsigned)((f.ny + TY - 1) / TY));
-  if (f.efix)
-    return f.rho == T(1)
-               ? launch_pdl(cart2_step_kernel<T, false, true>, grid, block, 0, st, f, u)
-               : launch_pdl(cart2_step_kernel<T, true, true>, grid, block, 0, st, f, u);
-  return f.rho == T(1) ? launch_pdl(cart2_step_kernel<T, false, false>, grid, block, 0, st, f, u)
-                       : launch_pdl(cart2_step_kernel<T, true, false>, grid, block, 0, st, f, u);
+  return launch_march2<T, true>(f, u, st);
 }
 
 template <typename T>
@@ -350,6 +434,8 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
   return cudaGetLastError();
 }
 
+template cudaError_t march2_occupancy<float>(int*, bool);
+template cudaError_t march2_occupancy<double>(int*, bool);
 template cudaError_t launch_flux2<float>(const Step2Args<float>&, cudaStream_t);
 template cudaError_t launch_flux2<double>(const Step2Args<double>&, cudaStream_t);
 template cudaError_t launch_fused2<float>(const Step2Args<float>&, const Update2Args<float>&,

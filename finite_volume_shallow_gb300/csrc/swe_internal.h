@@ -77,15 +77,21 @@ struct StepArgs {
 };
 
 // ---- two layers (swe_cart2.cu) ----------------------------------------------
-// Tiles of kTile2X x Tile2Y<T> cells; the padded layout of a two-layer state
-// covers whole tiles plus the one-cell halo: pitch2 / rows2 below.
+// A warp marches over a band of kBand2 owned columns and reads one halo
+// column on each side (lane l of band b: column kBand2 * b - 1 + l), so a
+// row must hold 30 * ceil(nx / 30) + 1 columns past the padding; rows are
+// padded to whole groups of Tile2Y<T> (the update kernel's blocks).
 constexpr int kTile2X = 32;
+constexpr int kBand2 = 30;
+constexpr int kMarch2Warps = 4;
 template <typename T> struct Tile2Y { static constexpr int v = 8; };
 template <> struct Tile2Y<double> { static constexpr int v = 4; };
 
 template <typename T>
 inline int64_t grid_pitch2(int nx) {
-  int64_t cols = (int64_t)(nx + kTile2X - 1) / kTile2X * kTile2X + 2 * kPadX;
+  int64_t tiles = (int64_t)(nx + kTile2X - 1) / kTile2X * kTile2X;
+  int64_t bands = (int64_t)(nx + kBand2 - 1) / kBand2 * kBand2 + 1;
+  int64_t cols = (tiles > bands ? tiles : bands) + 2 * kPadX;
   return (cols + 31) / 32 * 32;
 }
 template <typename T>
@@ -108,11 +114,12 @@ struct Step2Args {
   void* tmax_out;  // max over cells of sum_x D + rho sum_y D (must start at 0)
   unsigned* err;
   int efix;        // 1: the Harten-Hyman entropy fix
+  int nbands, nsegs;  // launch shape: one warp per (band, row segment)
 };
 // The update W_out = W_in - (dt/dx) R of step `step`, dt from the wave-speed
 // maximum in tmax_in.  cart2_update_kernel reads win and writes w (the same
-// buffer, or buffer 0 at the end of a run); cart2_step_kernel writes the
-// updated cells of its tiles to w.
+// buffer, or buffer 0 at the end of a run); the fused march writes the
+// updated cells it owns to w.
 template <typename T>
 struct Update2Args {
   const T* win[6];
@@ -129,6 +136,9 @@ struct Update2Args {
   unsigned* err;
 };
 
+// Resident four-warp blocks per SM of the march (efix: the entropy-fix variant).
+template <typename T>
+cudaError_t march2_occupancy(int* blocks_per_sm, bool efix);
 template <typename T>
 cudaError_t launch_flux2(const Step2Args<T>& f, cudaStream_t st);
 template <typename T>

@@ -199,145 +199,7 @@ __global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepA
 }
 
 // ---- two layers, fp32: two edges per thread on the packed FP32x2 pipe -------
-// The same arithmetic as edge2<float> (swe_roe2.cuh), written with
-// FADD2 / FMUL2 / FFMA2 so that one instruction serves both edges; the
-// square roots and reciprocals stay per component.
-__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
-__device__ __forceinline__ float2 s2(float v) { return make_float2(v, v); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, s2(-1.f), a); }
-__device__ __forceinline__ float2 rcp2(float2 a) { return f2(M2<float>::rcp(a.x), M2<float>::rcp(a.y)); }
-__device__ __forceinline__ float2 rsq2(float2 a) { return f2(M2<float>::rsq(a.x), M2<float>::rsq(a.y)); }
-__device__ __forceinline__ float2 sqrt2(float2 a) { return f2(sqrt_approx(a.x), sqrt_approx(a.y)); }
-__device__ __forceinline__ float2 min2(float2 a, float2 b) { return f2(fminf(a.x, b.x), fminf(a.y, b.y)); }
-__device__ __forceinline__ float2 max2(float2 a, float2 b) { return f2(fmaxf(a.x, b.x), fmaxf(a.y, b.y)); }
-__device__ __forceinline__ float sgnw1(float l) { return l < 0.f ? 1.f : (l > 0.f ? 0.f : 0.5f); }
-
-struct Side2P {
-  float2 h[2], s[2], rs[2], qn[2], qt[2], H;
-};
-
-struct QuarticP {
-  float2 u1, u2, c1s, c2s, rc;
-  __device__ __forceinline__ void qq(float2 l, float2& d1, float2& d2, float2& q1,
-                                     float2& q2) const {
-    d1 = sub2(l, u1);
-    d2 = sub2(l, u2);
-    q1 = fma2(d1, d1, f2(-c1s.x, -c1s.y));
-    q2 = fma2(d2, d2, f2(-c2s.x, -c2s.y));
-  }
-  // the Newton step p / p' at l (p = q1 q2 - rc, p' = 2 (d1 q2 + d2 q1))
-  __device__ __forceinline__ float2 step(float2 l) const {
-    float2 d1, d2, q1, q2;
-    qq(l, d1, d2, q1, q2);
-    const float2 p = fma2(q1, q2, f2(-rc.x, -rc.y));
-    const float2 dp = mul2(s2(2.f), fma2(d1, q2, mul2(d2, q1)));
-    return mul2(p, rcp2(dp));
-  }
-};
-
-// Flux of two edges at once; walls per component.  Returns false if either
-// edge's A_ij has a complex pair of eigenvalues.
-__device__ __forceinline__ bool edge2p(const Side2P& a, const Side2P& b, float g, float gh,
-                                       float r, bool w0, bool w1, float2* out) {
-  float2 un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float2 va = mul2(a.qn[k], a.rs[k]), vb = mul2(b.qn[k], b.rs[k]);
-    un[k] = mul2(add2(va, vb), rcp2(add2(a.s[k], b.s[k])));
-    cs[k] = mul2(s2(gh), add2(a.h[k], b.h[k]));
-    const float2 iha = mul2(a.rs[k], a.rs[k]), ihb = mul2(b.rs[k], b.rs[k]);
-    qu_a[k] = mul2(mul2(a.qn[k], a.qn[k]), iha);
-    qu_b[k] = mul2(mul2(b.qn[k], b.qn[k]), ihb);
-    ut_a[k] = mul2(a.qt[k], iha);
-    ut_b[k] = mul2(b.qt[k], ihb);
-  }
-  const QuarticP q{un[0], un[1], cs[0], cs[1], mul2(mul2(s2(r), cs[0]), cs[1])};
-  const float2 c1 = sqrt2(cs[0]), c2 = sqrt2(cs[1]);
-  const float2 sc = sqrt2(add2(cs[0], cs[1]));
-  const float kr2 = 1.4142135623730951f * (1.f + 1.f / 4096), ks = 1.f + 1.f / 4096;
-  // outer roots: the safe starts of edge2 (swe_roe2.cuh)
-  float2 l1 = max2(min2(fma2(s2(-kr2), c1, un[0]), fma2(s2(-kr2), c2, un[1])),
-                   fma2(s2(-ks), sc, min2(un[0], un[1])));
-  float2 l4 = min2(max2(fma2(s2(kr2), c1, un[0]), fma2(s2(kr2), c2, un[1])),
-                   fma2(s2(ks), sc, max2(un[0], un[1])));
-  const float2 tol = mul2(s2(Iters<float>::tol), max2(c1, c2));
-  const unsigned act = __activemask();
-  bool done0 = false, done1 = false;  // per edge, as in edge2
-#pragma unroll
-  for (int it = 0; it < Iters<float>::outer; ++it) {
-    const float2 t1 = q.step(l1), t4 = q.step(l4);
-    const float2 n1 = sub2(l1, t1), n4 = sub2(l4, t4);
-    l1 = f2(done0 ? l1.x : n1.x, done1 ? l1.y : n1.y);
-    l4 = f2(done0 ? l4.x : n4.x, done1 ? l4.y : n4.y);
-    done0 |= it >= 1 && (fabsf(t1.x) <= tol.x) & (fabsf(t4.x) <= tol.x);
-    done1 |= it >= 1 && (fabsf(t1.y) <= tol.y) & (fabsf(t4.y) <= tol.y);
-    if (__all_sync(act, done0 & done1)) break;
-  }
-  // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
-  const float2 p3 = mul2(s2(-2.f), add2(un[0], un[1]));
-  const float2 p2 = add2(add2(fma2(un[0], un[0], f2(-cs[0].x, -cs[0].y)),
-                              fma2(un[1], un[1], f2(-cs[1].x, -cs[1].y))),
-                         mul2(mul2(s2(4.f), un[0]), un[1]));
-  const float2 ss = add2(l1, l4), pp = mul2(l1, l4);
-  const float2 bb = add2(p3, ss);
-  const float2 cc = sub2(fma2(ss, bb, p2), pp);
-  const float2 disc = fma2(bb, bb, mul2(s2(-4.f), cc));
-  const bool hyper = (disc.x > 0.f) & (disc.y > 0.f);
-  const float2 sd = sqrt2(max2(disc, s2(0.f)));
-  float2 l2 = mul2(s2(0.5f), sub2(f2(-bb.x, -bb.y), sd));
-  float2 l3 = mul2(s2(0.5f), sub2(sd, bb));
-  const float2 lim = mul2(s2(0.5f), sd);  // steps clamped as in edge2
-  const float2 nlim = f2(-lim.x, -lim.y);
-#pragma unroll
-  for (int it = 0; it < Iters<float>::inner; ++it) {
-    l2 = sub2(l2, min2(max2(q.step(l2), nlim), lim));
-    l3 = sub2(l3, min2(max2(q.step(l3), nlim), lim));
-  }
-  // fluctuation d (pressure differences written g hbar_k dh_k)
-  const float2 dh1 = sub2(b.h[0], a.h[0]), dh2 = sub2(b.h[1], a.h[1]), dH = sub2(b.H, a.H);
-  const float2 d1 = sub2(b.qn[0], a.qn[0]);
-  const float2 d2 = fma2(cs[0], sub2(add2(dh1, dh2), dH), sub2(qu_b[0], qu_a[0]));
-  const float2 d3 = sub2(b.qn[1], a.qn[1]);
-  const float2 d4 = fma2(cs[1], sub2(fma2(s2(r), dh1, dh2), dH), sub2(qu_b[1], qu_a[1]));
-  // P^- d = sum_k w_k alpha_k K_k
-  const float2 lam[4] = {l1, l2, l3, l4};
-  const float2 ic1s = rcp2(cs[0]);
-  const float2 tu1 = mul2(s2(2.f), un[0]), tu2 = mul2(s2(2.f), un[1]);
-  float2 pd0 = s2(0.f), pd1 = s2(0.f), pd2 = s2(0.f), pd3 = s2(0.f);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 l = lam[k];
-    const float2 w = f2(sgnw1(l.x), sgnw1(l.y));
-    float2 e1, e2, Q1, Q2;
-    q.qq(l, e1, e2, Q1, Q2);
-    const float2 dp = mul2(s2(2.f), fma2(e1, Q2, mul2(e2, Q1)));
-    const float2 num = fma2(Q2, fma2(sub2(l, tu1), d1, d2),
-                            mul2(cs[0], fma2(sub2(l, tu2), d3, d4)));
-    const float2 alpha = mul2(mul2(w, num), rcp2(dp));
-    const float2 mu = mul2(Q1, ic1s);
-    pd0 = add2(pd0, alpha);
-    pd1 = fma2(alpha, l, pd1);
-    pd2 = fma2(alpha, mu, pd2);
-    pd3 = fma2(mul2(alpha, l), mu, pd3);
-  }
-  float2 m1 = add2(a.qn[0], pd0);
-  float2 m2 = add2(a.qn[1], pd2);
-  if (w0) { m1.x = 0.f; m2.x = 0.f; }  // a reflective wall passes no mass
-  if (w1) { m1.y = 0.f; m2.y = 0.f; }
-  out[E_M1] = m1;
-  out[E_PM1] = pd1;
-  out[E_PS1] = sub2(d2, pd1);
-  out[E_T1] = mul2(m1, f2(m1.x > 0.f ? ut_a[0].x : ut_b[0].x, m1.y > 0.f ? ut_a[0].y : ut_b[0].y));
-  out[E_M2] = m2;
-  out[E_PM2] = pd3;
-  out[E_PS2] = sub2(d4, pd3);
-  out[E_T2] = mul2(m2, f2(m2.x > 0.f ? ut_a[1].x : ut_b[1].x, m2.y > 0.f ? ut_a[1].y : ut_b[1].y));
-  out[E_D] = max2(f2(fabsf(l1.x), fabsf(l1.y)), f2(fabsf(l4.x), fabsf(l4.y)));
-  return hyper;
-}
+// (edge2p and its FP32x2 helpers are in swe_roe2.cuh)
 
 __device__ __forceinline__ void load_side2p(const MeshStepArgs<float>& A, int32_t c0, int32_t c1,
                                             float2 ex, float2 ey, Side2P& s) {
@@ -389,7 +251,7 @@ __global__ void __launch_bounds__(kPairThreads, SWE_PAIR_MIN_BLOCKS)
     if (w0) { sb.qn[0].x = -sa.qn[0].x; sb.qn[1].x = -sa.qn[1].x; }
     if (w1) { sb.qn[0].y = -sa.qn[0].y; sb.qn[1].y = -sa.qn[1].y; }
     float2 out[NEQ];
-    ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out);
+    ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out) == 3u;
     float* buf = A.ebuf;
     const int64_t st = A.estride;
     auto put = [&](int q, float2 v) { *reinterpret_cast<float2*>(buf + q * st + e0) = v; };

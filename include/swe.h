@@ -162,9 +162,8 @@ typedef struct swe_state swe_state;
 /* Create a simulation on a Cartesian grid ([P1] Algorithm 1, before the time
  * loop: mesh construction and initial state).
  *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite;
- *          nx <= 2^30, ny <= 2^30 - 8; two layers also ny <= 524280 (fp32)
- *          or 262140 (fp64): 65535 tiles of 8 (fp32) or 4 (fp64) rows;
- *          with wet_dry also ny <= 524279 (65535 blocks of 8 edge rows)
+ *          nx <= 2^30, ny <= 2^30 - 8; with wet_dry also ny <= 524279
+ *          (65535 blocks of 8 edge rows)
  *  H       host, nx*ny values: bottom depth below the reference level
  *  W0      host, array of 4 pointers (h, qx, qy, hC), or 6 (h1, q1x, q1y,
  *          h2, q2x, q2y) for two layers, nx*ny values each; depths > 0

@@ -176,20 +176,6 @@ def test_wait_selftest_rejects_bad_budgets_before_touching_the_gpu(lib):
         assert S.swe_selftest_wait(budget) == S.SWE_ERR_ARG
 
 
-@pytest.mark.parametrize("precision,ny_ok", [(32, 524280), (64, 262140)])
-def test_two_layer_grid_height_limit(lib, precision, ny_ok):
-    # the tile kernels put one block per tile row in the launch's y dimension
-    # (at most 65535): one row more is refused before any CUDA call
-    dt = np.float32 if precision == 32 else np.float64
-    n = ny_ok + 1
-    H = np.full(n, 10.0, dt)
-    W = [np.full(n, v, dt) for v in (6.0, 0.0, 0.0, 4.0, 0.0, 0.0)]
-    with pytest.raises(S.SweError) as e:
-        S.swe_create_grid(1, n, 10.0, 10.0, H, W, precision=precision, n_layers=2,
-                          pollutant=0, r=0.98)
-    assert e.value.status == S.SWE_ERR_ARG
-
-
 def test_missing_library_fails_loudly(lib, monkeypatch):
     # the binding never falls back to anything else when libswe is absent
     monkeypatch.setattr(B, "LIB", os.path.join(ROOT, "no_such_dir", "libswe.so"))

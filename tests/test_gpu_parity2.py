@@ -192,3 +192,11 @@ def test_cfl_limit_two_layers(precision):
     d = I.two_layer_hills(53, 41, umax=0.05, bump=0.5)
     d["cfl"] = 1.0
     assert_parity2(d, precision, 30)
+
+
+def test_grid_taller_than_a_launch_dimension():
+    # the march puts all its units in the launch's x dimension: a strip of
+    # 530,000 rows (more than 65,535 blocks of 8 rows) runs and matches the
+    # oracle
+    d = I.two_layer_hills(2, 530_000, umax=0.05, bump=0.5)
+    assert_parity2(d, 32, 3)

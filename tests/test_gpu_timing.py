@@ -32,7 +32,7 @@ EVERY = STEPS + 1
 
 @pytest.mark.parametrize("case,kernels", [
     ("grid1", {"cart1_step_kernel": EVERY}),
-    ("grid2", {"cart2_flux_kernel": 2, "cart2_step_kernel": STEPS - 1,
+    ("grid2", {"cart2_march_kernel<plain>": 2, "cart2_march_kernel<fused>": STEPS - 1,
                "cart2_update_kernel": 2}),
     ("mesh2", {"mesh_edge_kernel": EVERY, "mesh_gather_kernel": EVERY,
                "mesh_update_kernel": EVERY}),

@@ -622,9 +622,14 @@ def main():
     S.swe_destroy(st)
 
     peak, peak_kind = load_peaks()
-    alu = measure_alu_peaks(S, stream.cuda_stream)
-    kernels = {}
     ktimes = {k: v for k, v in ktimes.items() if v[0] > 0}
+    # the FMA probe runs only when a kernel of this workload is bound by
+    # arithmetic (it would otherwise only add launches to a profile)
+    if any(kernel_model(k, precision, nl, n, info["n_edges"])[0] == "alu" for k in ktimes):
+        alu = measure_alu_peaks(S, stream.cuda_stream)
+    else:
+        alu = {"source": "not measured: every kernel of this workload is bound by HBM"}
+    kernels = {}
     for name, (launches, kms) in ktimes.items():
         bound, amount, unit = kernel_model(name, precision, nl, n, info["n_edges"])
         avg = kms / max(launches, 1)

@@ -47,21 +47,28 @@ METRIC = "cell-updates/s (Mcell-steps/s) of the Roe FV step; achieved HBM GB/s v
 UNIT = "Mcell-updates/s"
 BYTES_PER_CELL = {32: 36, 64: 72}   # h, qx, qy, hC, H read; h, qx, qy, hC written
 # Floating-point operations of one two-layer edge flux, counted from its
-# formulas (an add or a multiply 1, an FMA 2; square
-# roots, reciprocals and reciprocal square roots not counted): 213 outside
-# the root iterations, 28 per outer Newton iteration (two roots x 14) and 28
-# per inner one.  The outer iteration stops once every edge of the warp has
-# converged: on the interface dam break and the triangle workload it takes
-# 2.01 iterations per edge in fp32 and 3.01 in fp64 (counted on the GPU with
-# an instrumented build); the inner one runs 2.
+# formulas (an add or a multiply 1, an FMA 2; square roots, reciprocals and
+# reciprocal square roots not counted): 93 outside the root iterations and
+# P^- d (Roe averages 30, rc 2, safe starts and tolerance 13, inner-pair set-up
+# 24, fluctuation 16, 2 u_k 2, results 6), 28 per outer Newton iteration
+# (two roots x 14), 28 per inner one, and 30 per wave of P^- d =
+# sum_k w_k alpha_k K_k.  Only the waves with l_k < 0 (w_k != 0) are needed;
+# on these workloads every edge is subcritical in both wave families
+# (l1 < l2 < 0 < l3 < l4), so 2 waves.  The outer iteration stops once every
+# edge of the warp has converged: on the interface dam break and the triangle
+# workload it takes 2.01 iterations per edge in fp32 and 3.01 in fp64
+# (counted on the GPU with an instrumented build); the inner one runs 2.
 # In fp64 each reciprocal is a hardware seed refined by two Newton steps of
 # two FMAs each (8 flops, counted): per edge 2 for the Roe velocities, 2 per
 # outer and 2 per inner iteration, 1 for 1/c1^2 and 1 per wave; in fp32 they
 # are single MUFU instructions (not counted).
+FLOPS_EDGE_2L_BASE, FLOPS_PER_WAVE_2L, WAVES_2L = 93, 30, 2
 RCP_FLOPS_FP64 = 8
-RCP_PER_EDGE_2L_FP64 = 2 + 2 * 3.01 + 2 * 2 + 1 + 4
-FLOPS_PER_EDGE_2L = {32: 213 + 28 * 2.01 + 28 * 2,
-                     64: 213 + 28 * 3.01 + 28 * 2 + RCP_FLOPS_FP64 * RCP_PER_EDGE_2L_FP64}
+RCP_PER_EDGE_2L_FP64 = 2 + 2 * 3.01 + 2 * 2 + 1 + WAVES_2L
+FLOPS_PER_EDGE_2L = {
+    32: FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L + 28 * 2.01 + 28 * 2,
+    64: FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L + 28 * 3.01 + 28 * 2
+        + RCP_FLOPS_FP64 * RCP_PER_EDGE_2L_FP64}
 # Per cell-update on a grid: two edges (each edge once; the tiles' halo
 # recomputation not counted) plus 25 for the per-cell quantities and the
 # residual sums.
@@ -106,9 +113,11 @@ def source_hash(files):
 # for the rotations into and out of the edge frame, the fluctuation terms and
 # the edge-length scaling; one layer 88 (in fp32 the one-layer edge kernel
 # is modelled by its bytes instead: its arithmetic is light).
-FLOPS_PER_EDGE_MESH = {(2, 32): 213 + 28 * 2.0 + 28 * 2 + 79,
-                       (2, 64): 213 + 28 * 3.0 + 28 * 2 + 79
-                       + RCP_FLOPS_FP64 * (2 + 2 * 3.0 + 2 * 2 + 1 + 4),
+FLOPS_PER_EDGE_MESH = {(2, 32): FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L
+                       + 28 * 2.0 + 28 * 2 + 79,
+                       (2, 64): FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L
+                       + 28 * 3.0 + 28 * 2 + 79
+                       + RCP_FLOPS_FP64 * (2 + 2 * 3.0 + 2 * 2 + 1 + WAVES_2L),
                        (1, 64): 88 + RCP_FLOPS_FP64 * 2}
 # One layer on a grid: floating-point operations per cell-update of the
 # fused step, counted from its formulas (FMA = 2; the 10 reciprocals and
@@ -653,6 +662,17 @@ def main():
                                   args.workload + ("_efix" if d.get("entropy_fix") else ""))})
     dominant = max(ktimes, key=lambda k: ktimes[k][1])
     roof = dict(kernels[dominant])
+    # the whole step against HBM when every kernel of it is bound by HBM: the
+    # algorithmic bytes of all its kernels over the measured step time (the
+    # per-kernel times come from a run with events between the kernels,
+    # which stops consecutive launches overlapping)
+    if len(kernels) > 1 and all(v["bound"] == "hbm" for v in kernels.values()):
+        step_bytes = sum(v["algorithmic_bytes_per_launch"] * v["launches"] for v in kernels.values()) \
+            / max(ktimes[dominant][0], 1)
+        achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+        roof["step"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "algorithmic_bytes_per_step": step_bytes,
+                        "timing": "ms_per_step of the timed region"}
     roof["other_kernels"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "unit", "frac",
                                                       "ms_per_launch", "share")}
                              for k, v in kernels.items() if k != dominant}

@@ -227,11 +227,20 @@ __device__ __forceinline__ bool edge2(const Side2<T>& a, const Side2<T>& b, T g,
     hyper &= quartic_roots<T, ADAPT>(side_quartic(a, g, r), la);
     hyper &= quartic_roots<T, ADAPT>(side_quartic(b, g, r), lb);
   }
-  // P^- d = sum_k w_k alpha_k K_k (+ the fix's nu_k K_k)
+  // P^- d = sum_k w_k alpha_k K_k (+ the fix's nu_k K_k).  Where every edge
+  // of the warp has l1 < l2 < 0 < l3 < l4 (subcritical in both wave
+  // families) waves 3 and 4 have w = 0 and add exact zeros: the loop stops
+  // after wave 2, bit for bit the same sum.
   const T ic1s = M2<T>::rcp(cs[0]);
   T pd0 = T(0), pd1 = T(0), pd2 = T(0), pd3 = T(0);
+  bool two_waves = false;
+  if (ADAPT && !EFIX) {
+    const bool sub = (l1 < T(0)) & (lam[1] < T(0)) & (lam[2] > T(0)) & (l4 > T(0));
+    two_waves = __all_sync(__activemask(), sub);
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
+    if (k == 2 && two_waves) break;
     const T l = lam[k];
     const T w = (l < T(0)) ? T(1) : ((l > T(0)) ? T(0) : T(0.5));
     const T Q1 = q.q1(l), Q2 = q.q2(l);
@@ -375,13 +384,18 @@ __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, flo
   const float2 d2 = fma2(cs[0], sub2(add2(dh1, dh2), dH), sub2(qu_b[0], qu_a[0]));
   const float2 d3 = sub2(b.qn[1], a.qn[1]);
   const float2 d4 = fma2(cs[1], sub2(fma2(s2(r), dh1, dh2), dH), sub2(qu_b[1], qu_a[1]));
-  // P^- d = sum_k w_k alpha_k K_k
+  // P^- d = sum_k w_k alpha_k K_k; waves 3 and 4 add exact zeros when every
+  // edge of the warp is subcritical in both families (as in edge2)
   const float2 lam[4] = {l1, l2, l3, l4};
   const float2 ic1s = rcp2(cs[0]);
   const float2 tu1 = mul2(s2(2.f), un[0]), tu2 = mul2(s2(2.f), un[1]);
   float2 pd0 = s2(0.f), pd1 = s2(0.f), pd2 = s2(0.f), pd3 = s2(0.f);
+  const bool sub = (l1.x < 0.f) & (l1.y < 0.f) & (l2.x < 0.f) & (l2.y < 0.f) & (l3.x > 0.f) &
+                   (l3.y > 0.f) & (l4.x > 0.f) & (l4.y > 0.f);
+  const bool two_waves = __all_sync(act, sub);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
+    if (k == 2 && two_waves) break;
     const float2 l = lam[k];
     const float2 w = f2(sgnw1(l.x), sgnw1(l.y));
     float2 e1, e2, Q1, Q2;

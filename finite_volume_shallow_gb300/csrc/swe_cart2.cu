@@ -209,11 +209,19 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
     const int y0 = (int)((int64_t)seg * ny / ns), y1 = (int)((int64_t)(seg + 1) * ny / ns);
     const int x = kBand2 * band - 1 + lane;
     const bool own_x = lane >= 1 && lane <= kBand2 && x < nx;
-    const bool in_x = x >= 0 && x < nx;
     const bool need_ex = lane <= kBand2 && x >= -1 && x <= nx - 1;  // x-edges used
     const T g = A.g, gh = T(0.5) * A.g, r = A.r, rho = A.rho;
     auto ys = [&](T v) { return ANISO ? v * rho : v; };
-    int64_t o = (int64_t)(y0 - 1 + kPadY) * A.pitch + x + kPadX;
+    // Every lane and row outside the grid reads the nearest cell of the grid
+    // instead (column -1 reads column 0, column nx reads nx - 1, rows -1 and
+    // ny read rows 0 and ny - 1): a wall's mirror ghost is then that copy
+    // with its normal discharge negated.
+    const int xc = min(max(x, 0), nx - 1);
+    auto row_of = [&](int rr) -> int64_t {
+      const int rc = min(max(rr, 0), ny - 1);
+      return (int64_t)(rc + kPadY) * A.pitch + xc + kPadX;
+    };
+    int64_t o = row_of(y0 - 1);
     // row y0 - 1 into registers
     T w[6], R[6], Hn;
     auto load = [&](int64_t at, T* wv, T* rv, T& hv) {
@@ -232,14 +240,14 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
     for (int f = 0; f < 6; ++f) xr[f] = T(0);
 #pragma unroll
     for (int q = 0; q < NB; ++q) yb[q] = T(0);
-    for (int rr = y0 - 1; rr <= y1; ++rr, o += A.pitch) {
+    for (int rr = y0 - 1; rr <= y1; ++rr) {
       // ---- the row: previous step's update (fused), next row's loads -----
       Cell2<T> cur;
       {
         T wc[6];
 #pragma unroll
         for (int f = 0; f < 6; ++f) wc[f] = w[f];
-        if (FUSED && in_x && rr >= 0 && rr < ny) {
+        if (FUSED) {
 #pragma unroll
           for (int f = 0; f < 6; ++f) wc[f] = upd(wc[f], kdt, R[f]);
           if (own_x && rr >= y0 && rr < y1) {
@@ -254,17 +262,18 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
         cur.h[1] = wc[3]; cur.qx[1] = wc[4]; cur.qy[1] = wc[5];
         cur.H = Hn;
       }
-      if (rr < y1) load(o + A.pitch, w, R, Hn);
+      const int64_t on = row_of(rr + 1);
+      if (rr < y1) load(on, w, R, Hn);
       derive(cur);
       if (rr >= y0) {
         // ---- the x-edge east of the cell, the y-edge below it ---------------
         const Cell2<T> right = shfl_down_cell(cur);
         const bool lw = x == -1, rw = x == nx - 1;
-        const Side2<T> ax = lw ? side2(right, true, true) : side2(cur, true, false);
-        const Side2<T> bx = rw ? side2(cur, true, true) : side2(right, true, false);
         const bool bw = rr == 0, tw = rr == ny;
-        const Side2<T> ay = bw ? side2(cur, false, true) : side2(prev, false, false);
-        const Side2<T> by = tw ? side2(prev, false, true) : side2(cur, false, false);
+        const Side2<T> ax = side2(cur, true, lw);
+        const Side2<T> bx = side2(right, true, rw);
+        const Side2<T> ay = side2(prev, false, bw);
+        const Side2<T> by = side2(cur, false, tw);
         T ox[NEQ], oy[NEQ];
         const unsigned ok = edge_pair<T, EFIX>(ax, bx, lw || rw, ay, by, bw || tw, g, gh, r,
                                                ox, oy);
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
           Rn[4] = xr[4] + ys(oy[E_T2] - yb[B_T2]);
           Rn[5] = xr[5] + ys(oy[E_PM2] + yb[B_PS2]);
           const T ts = xd + ys(yb[B_D] + oy[E_D]);
-          const int64_t ob = o - A.pitch;
+          const int64_t ob = row_of(rr - 1);  // an owned row: inside the grid
 #pragma unroll
           for (int f = 0; f < 6; ++f) A.R[f][ob] = Rn[f];
           tmax = nanmax2(tmax, ts);
@@ -313,6 +322,7 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
         }
       }
       prev = cur;
+      o = on;
     }
   }
   // hyperbolicity and the checks of this warp, the block's max of sum L ||D||

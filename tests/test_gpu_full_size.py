@@ -27,7 +27,7 @@ from gpu_util import TOL, TOL2, gpu_run, gpu_run_mesh
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-CASES = [("hills2048", 64), ("hills2048", 32)]
+CASES = [("hills2048", 64), ("hills2048", 32), ("pulses8192", 32)]
 
 
 def _block_means_grid(w, nx, ny, nb=32):

@@ -180,13 +180,11 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
         return "hbm", (12 + e + nf * e) * n_cells + ne * e * n_edges, "B"
     if kernel == "mesh_update_kernel":
         return "hbm", 3 * nf * e * n_cells, "B"
-    # wet/dry on a grid: each field and each edge record crosses HBM once
-    if kernel == "wd_edge_kernel":    # h, qx, qy, hC, H read; 7 values per edge written
-        return "hbm", 5 * e * n_cells + 7 * e * n_edges, "B"
-    if kernel == "wd_cell_kernel":    # m and both speeds per edge, h read; tau written
-        return "hbm", 3 * e * n_edges + 2 * e * n_cells, "B"
-    if kernel == "wd_update_kernel":  # m, both momenta, t, c per edge, tau, 4 fields in/out
-        return "hbm", 5 * e * n_edges + 9 * e * n_cells, "B"
+    # wet/dry on a grid: each field crosses HBM once per pass
+    if kernel == "wd_speed_kernel":   # h, qx, qy, H read
+        return "hbm", 4 * e * n_cells, "B"
+    if kernel == "wd_tile_kernel":    # h, qx, qy, hC, H read; h, qx, qy, hC written
+        return "hbm", 9 * e * n_cells, "B"
     raise KeyError(kernel)
 
 

@@ -71,10 +71,6 @@ struct swe_state {
   int* mark_n = nullptr;              // with marks: intervals recorded so far
   // one layer with wet/dry fronts on a grid (swe_params.wet_dry)
   bool wd = false;
-  void* wd_ex = nullptr;             // edge records, see WdStepArgs
-  void* wd_ey = nullptr;
-  void* wd_tau = nullptr;
-  int64_t wd_xs = 0, wd_ys = 0;
 };
 
 // Per-kernel device time: a ring of event sets, one set per step; a set is
@@ -380,7 +376,10 @@ swe_status enqueue_wd_check(swe_state* s) {
 template <typename T>
 swe_status enqueue_wd_step(swe_state* s, double cfl) {
   WdStepArgs a{};
-  for (int f = 0; f < 4; ++f) a.w[f] = s->w[s->cur][f];
+  for (int f = 0; f < 4; ++f) {
+    a.win[f] = s->w[s->cur][f];
+    a.wout[f] = s->w[s->cur ^ 1][f];
+  }
   a.H = s->H;
   a.nx = s->nx;
   a.ny = s->ny;
@@ -389,11 +388,6 @@ swe_status enqueue_wd_step(swe_state* s, double cfl) {
   a.h_dry = s->p.h_dry;
   a.dx = s->dx;
   a.dy = s->dy;
-  a.ex = s->wd_ex;
-  a.ey = s->wd_ey;
-  a.xs = s->wd_xs;
-  a.ys = s->wd_ys;
-  a.tau = s->wd_tau;
   a.two_cfl = 2.0 * cfl;
   char* sl = (char*)s->slots;
   a.tmax_slot = sl + (s->step % 3) * sizeof(uint64_t);
@@ -404,6 +398,7 @@ swe_status enqueue_wd_step(swe_state* s, double cfl) {
   a.err = s->err;
   a.efix = s->p.entropy_fix;
   CK(launch_wd_step<T>(a, s->stream, s->marks));
+  s->cur ^= 1;
   s->step += 1;
   return SWE_OK;
 }
@@ -482,10 +477,9 @@ swe_status enqueue_step_timed(swe_state* s, double cfl, bool last) {
 
 void timing_names(swe_state* s, Timing* tm) {
   if (s->wd) {
-    tm->nk = 3;
-    tm->names[0] = "wd_edge_kernel";
-    tm->names[1] = "wd_cell_kernel";
-    tm->names[2] = "wd_update_kernel";
+    tm->nk = 2;
+    tm->names[0] = "wd_speed_kernel";
+    tm->names[1] = "wd_tile_kernel";
   } else if (s->mesh) {
     tm->nk = 3;
     tm->names[0] = "mesh_edge_kernel";
@@ -697,8 +691,8 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   // index arithmetic inside the kernels is 32-bit per row and column
   if ((int64_t)grid->nx > (1 << 30) || (int64_t)grid->ny > (1 << 30) - 8) return SWE_ERR_ARG;
-  // wet/dry: one block per 8 rows of edges in the launch's y dimension
-  if (params->wet_dry == 1 && ((int64_t)grid->ny + 1 + 7) / 8 > 65535) return SWE_ERR_ARG;
+  // wet/dry: one block per 8 rows in the launch's y dimension
+  if (params->wet_dry == 1 && ((int64_t)grid->ny + 7) / 8 > 65535) return SWE_ERR_ARG;
 
   swe_state* s = new (std::nothrow) swe_state();
   if (!s) return SWE_ERR_OOM;
@@ -726,12 +720,8 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   const int64_t aux = kAuxBytes;
   // two buffers of the fields (+ two of the residual for two layers) + H
   const int nalloc = s->nl == 2 ? 25 : 9;
-  // wet/dry: edge records of the x- and y-edges and a draining time per cell
   s->wd = params->wet_dry == 1;
-  const int64_t wd_xb = s->wd ? round_up((int64_t)(s->nx + 1) * s->ny * (int64_t)s->esz, 256) : 0;
-  const int64_t wd_yb = s->wd ? round_up((int64_t)s->nx * (s->ny + 1) * (int64_t)s->esz, 256) : 0;
-  const int64_t wd_tb = s->wd ? round_up((int64_t)s->nx * s->ny * (int64_t)s->esz, 256) : 0;
-  s->dev_bytes = (size_t)(nalloc * fbytes + aux + kWdEdgeFields * (wd_xb + wd_yb) + wd_tb);
+  s->dev_bytes = (size_t)(nalloc * fbytes + aux);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
   if (e != cudaSuccess) {
     s->dev = nullptr;
@@ -761,16 +751,6 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   }
   s->H = p;
   p += fbytes;
-  if (s->wd) {
-    s->wd_ex = p;
-    s->wd_xs = wd_xb / (int64_t)s->esz;
-    p += kWdEdgeFields * wd_xb;
-    s->wd_ey = p;
-    s->wd_ys = wd_yb / (int64_t)s->esz;
-    p += kWdEdgeFields * wd_yb;
-    s->wd_tau = p;
-    p += wd_tb;
-  }
   if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
 
   if (s->nl == 1) st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);

@@ -237,19 +237,16 @@ int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const in
                  bool reorder, MeshPrep* out);
 
 // ---- one layer with wet/dry fronts on a grid (swe_wetdry.cu) ----------------
-// State in the one-layer padded layout, updated in place; per step an edge
-// pass (records of every x- and y-edge: 7 values each), a cell pass (sum of
-// L ||D|| reduced into tmax_slot, draining time per cell) and the update,
-// which reads tmax_slot and zeroes tmax_clear.
+// State in the one-layer padded layout, W^n in win, W^{n+1} written to wout;
+// per step a speed pass (sum of L ||D|| reduced into tmax_slot) and a tile
+// pass (edges, draining times, update), which reads tmax_slot and zeroes
+// tmax_clear.
 struct WdStepArgs {
-  void* w[4];
+  void* win[4];
+  void* wout[4];
   const void* H;
   int nx, ny, pitch;
   double g, h_dry, dx, dy;
-  void* ex;          // 7 fields of (nx + 1) * ny x-edge values, stride xs
-  void* ey;          // 7 fields of nx * (ny + 1) y-edge values, stride ys
-  int64_t xs, ys;
-  void* tau;         // nx * ny draining times
   double two_cfl;
   void* tmax_slot;
   void* tmax_clear;
@@ -259,7 +256,6 @@ struct WdStepArgs {
   unsigned* err;
   int efix;
 };
-constexpr int kWdEdgeFields = 7;
 template <typename T>
 cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent_t* marks);
 template <typename T>

@@ -19,20 +19,23 @@
 //    unit time) limits every term of an edge to min(1, tau_d / dt), d the
 //    cell its mass flux leaves, so that no depth turns negative.
 //
-// Three kernels per step (the draining time of a cell needs all of its
-// edges, and each edge's limit the draining time of its donor):
-//   wd_edge_kernel    one thread per grid vertex (i, j): the x-edge on the
-//                     left of cell (i, j) and the y-edge below it, each edge
-//                     once: mass flux m (a -> b), each side's normal momentum
-//                     flux (a: Phi^-[1]; b: Phi^-[1] + g hbar (H_b - H_a)),
-//                     tangential momentum flux, pollutant flux, ||D|| as
-//                     each side counts it;
-//   wd_cell_kernel    one thread per cell: sum_e L ||D_e|| (its block maximum
-//                     published with one atomic: dt of this step, eq. (5))
-//                     and the draining time tau_i;
-//   wd_update_kernel  one thread per cell: dt, the limit of each of its four
-//                     edges, the update of eq. (4) in place, clean-up of dry
-//                     cells, checks, the clock.
+// Two kernels per step:
+//   wd_speed_kernel  one thread per cell: sum_e L ||D_e|| over its four edges
+//                    of W^n with the rules above (its block maximum published
+//                    with one atomic: dt of this step, eq. (5));
+//   wd_tile_kernel   one block per 32 x 16 tile: the tile and a two-cell ring
+//                    of W^n into shared memory; every edge that the tile and
+//                    its one-cell ring need, once per block (mass flux m
+//                    a -> b, each side's normal momentum flux in flux form
+//                    -- a: Phi^-[1]; b: Phi^-[1] + g hbar (H_b - H_a) --,
+//                    tangential momentum and pollutant fluxes); the draining
+//                    time of the tile's cells and of the ring (a tile edge's
+//                    donor may lie in the ring); then each cell of the tile:
+//                    the limit of its four edges, the update of eq. (4) into
+//                    the other state buffer, clean-up of dry cells, checks;
+//                    block (0, 0) keeps the clock.  Edges on a tile's border
+//                    are evaluated by both tiles with the same code and
+//                    inputs, so every cell sees one value per edge.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -62,9 +65,6 @@ template <> struct Wm<double> {  // Newton-refined reciprocal, CUDA's square roo
   __device__ static __forceinline__ double rcp(double x) { return rcp_nr(x); }
   __device__ static __forceinline__ double sqrt_(double x) { return sqrt(x); }
 };
-
-// per-edge record (structure of arrays): field q of an edge at q * stride + e
-enum { WD_M, WD_FA, WD_FB, WD_T, WD_C, WD_DA, WD_DB, WD_NE };
 
 // One side of an edge in the frame of its normal.
 template <typename T>
@@ -186,77 +186,41 @@ __device__ __forceinline__ EdgeW<T> edge_any(const SideW<T>& a, const SideW<T>& 
   return roe_edge<T, EFIX>(a, b, g, hdry);
 }
 
+// Both sides' ||D|| of an edge a -> b under the same rules as edge_any
+// (the Roe speed |u| + c; sqrt(g h) for the wet side of a wall; 0 for a
+// side that receives nothing).
+template <typename T>
+__device__ __forceinline__ void edge_speeds(const SideW<T>& a, const SideW<T>& b, bool a_wall,
+                                            bool b_wall, T g, T hdry, T& da, T& db) {
+  auto wall_d = [&](const SideW<T>& w) { return w.h <= hdry ? T(0) : Wm<T>::sqrt_(g * w.h); };
+  da = db = T(0);
+  if (b_wall) { da = wall_d(a); return; }
+  if (a_wall) { db = wall_d(b); return; }
+  const bool dry_a = a.h <= hdry, dry_b = b.h <= hdry;
+  if (dry_a && dry_b) return;
+  if (dry_b && -b.H >= a.h - a.H) { da = wall_d(a); return; }
+  if (dry_a && -a.H >= b.h - b.H) { db = wall_d(b); return; }
+  const T sa = Wm<T>::sqrt_(a.h), sb = Wm<T>::sqrt_(b.h);
+  const T ua = dry_a ? T(0) : a.qn * Wm<T>::rcp(a.h), ub = dry_b ? T(0) : b.qn * Wm<T>::rcp(b.h);
+  const T un = (sa * ua + sb * ub) * Wm<T>::rcp(sa + sb);
+  da = db = fabs(un) + Wm<T>::sqrt_(g * (T(0.5) * (a.h + b.h)));
+}
+
 template <typename T>
 struct WdArgs {
-  T* w[4];          // h, qx, qy, hC (padded layout), updated in place
+  const T* win[4];  // W^n: h, qx, qy, hC (padded layout)
+  T* wout[4];       // W^{n+1}
   const T* H;
   int nx, ny, pitch;
   T g, hdry, dx, dy;
-  T* ex;            // x-edge records: (nx + 1) * ny per field, edge (ie, j) at j * (nx + 1) + ie
-  T* ey;            // y-edge records: nx * (ny + 1) per field, edge (i, je) at je * nx + i
-  int64_t xs, ys;   // field strides of ex and ey
-  T* tau;           // draining time per cell (j * nx + i)
   double two_cfl, area;
-  void* tmax_out;   // wd_cell_kernel: max over cells of sum L ||D|| (starts at 0)
-  const void* tmax_in;
-  void* tmax_clear;
+  void* tmax;       // max over cells of sum L ||D|| of W^n (starts at 0)
+  void* tmax_clear; // the slot the next step reduces into
   double* dt_hist;
   double* t_dev;
   int64_t step;
   unsigned* err;
-  int efix;
 };
-
-template <typename T>
-__device__ __forceinline__ SideW<T> load_side(const WdArgs<T>& A, int i, int j, bool xdir) {
-  const int64_t o = (int64_t)(j + kPadY) * A.pitch + i + kPadX;
-  SideW<T> s;
-  s.h = A.w[0][o];
-  s.qn = xdir ? A.w[1][o] : A.w[2][o];
-  s.qt = xdir ? A.w[2][o] : A.w[1][o];
-  s.hC = A.w[3][o];
-  s.H = A.H[o];
-  return s;
-}
-
-template <typename T, bool EFIX>
-__global__ void __launch_bounds__(256) wd_edge_kernel(const WdArgs<T> A) {
-  pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // 0..nx
-  const int j = blockIdx.y * blockDim.y + threadIdx.y;  // 0..ny
-  const int nx = A.nx, ny = A.ny;
-  if (i <= nx && j < ny) {  // x-edge between cells (i - 1, j) and (i, j)
-    const bool aw = i == 0, bw = i == nx;
-    const SideW<T> a = load_side(A, aw ? i : i - 1, j, true);
-    const SideW<T> b = load_side(A, bw ? i - 1 : i, j, true);
-    const EdgeW<T> e = edge_any<T, EFIX>(a, b, aw, bw, A.g, A.hdry);
-    const int64_t k = (int64_t)j * (nx + 1) + i;
-    A.ex[WD_M * A.xs + k] = e.m;
-    A.ex[WD_FA * A.xs + k] = e.fa;
-    A.ex[WD_FB * A.xs + k] = e.fb;
-    A.ex[WD_T * A.xs + k] = e.t;
-    A.ex[WD_C * A.xs + k] = e.c;
-    A.ex[WD_DA * A.xs + k] = e.d;
-    A.ex[WD_DB * A.xs + k] = e.db;
-  }
-  if (i < nx && j <= ny) {  // y-edge between cells (i, j - 1) and (i, j)
-    const bool aw = j == 0, bw = j == ny;
-    const SideW<T> a = load_side(A, i, aw ? j : j - 1, false);
-    const SideW<T> b = load_side(A, i, bw ? j - 1 : j, false);
-    // (the sides carry q_x as their tangential discharge, so e.t is the
-    // x-momentum flux m u_x^* itself)
-    const EdgeW<T> e = edge_any<T, EFIX>(a, b, aw, bw, A.g, A.hdry);
-    const int64_t k = (int64_t)j * nx + i;
-    A.ey[WD_M * A.ys + k] = e.m;
-    A.ey[WD_FA * A.ys + k] = e.fa;
-    A.ey[WD_FB * A.ys + k] = e.fb;
-    A.ey[WD_T * A.ys + k] = e.t;
-    A.ey[WD_C * A.ys + k] = e.c;
-    A.ey[WD_DA * A.ys + k] = e.d;
-    A.ey[WD_DB * A.ys + k] = e.db;
-  }
-  pdl_trigger();
-}
 
 template <typename T>
 __device__ __forceinline__ T nanmax_wd(T acc, T x) {
@@ -271,7 +235,7 @@ __device__ __forceinline__ void atomic_max_wd(void* slot, double v) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) wd_cell_kernel(const WdArgs<T> A) {
+__global__ void __launch_bounds__(256) wd_speed_kernel(const WdArgs<T> A) {
   __shared__ T part[8];
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -279,22 +243,29 @@ __global__ void __launch_bounds__(256) wd_cell_kernel(const WdArgs<T> A) {
   const int nx = A.nx, ny = A.ny;
   T s = T(0);
   if (i < nx && j < ny) {
-    const int64_t kw = (int64_t)j * (nx + 1) + i, ks = (int64_t)j * nx + i;
-    const T ly = A.dy, lx = A.dx;
-    // sum L ||D|| over East, North, West, South: (E + N) + (W + S)
-    const T dE = ly * A.ex[WD_DA * A.xs + kw + 1], dN = lx * A.ey[WD_DA * A.ys + ks + nx];
-    const T dW = ly * A.ex[WD_DB * A.xs + kw], dS = lx * A.ey[WD_DB * A.ys + ks];
-    s = (dE + dN) + (dW + dS);
-    // mass leaving the cell per unit time
-    const T oE = fmax(ly * A.ex[WD_M * A.xs + kw + 1], T(0));
-    const T oN = fmax(lx * A.ey[WD_M * A.ys + ks + nx], T(0));
-    const T oW = fmax(-(ly * A.ex[WD_M * A.xs + kw]), T(0));
-    const T oS = fmax(-(lx * A.ey[WD_M * A.ys + ks]), T(0));
-    const T M = (oE + oN) + (oW + oS);
-    const T h = A.w[0][(int64_t)(j + kPadY) * A.pitch + i + kPadX];
-    A.tau[ks] = M > T(0) ? h * (T)A.area / M : T(INFINITY);
+    // the cell and its four neighbours (a missing one: the cell itself,
+    // unused behind the wall), h, q_x, q_y and H of each read once
+    const int64_t o = (int64_t)(j + kPadY) * A.pitch + i + kPadX;
+    const int64_t on[4] = {i + 1 < nx ? o + 1 : o, j + 1 < ny ? o + A.pitch : o,
+                           i > 0 ? o - 1 : o, j > 0 ? o - A.pitch : o};
+    auto side = [&](int64_t at, bool xdir) {
+      SideW<T> c;
+      c.h = A.win[0][at];
+      c.qn = xdir ? A.win[1][at] : A.win[2][at];
+      c.qt = T(0);
+      c.hC = T(0);
+      c.H = A.H[at];
+      return c;
+    };
+    const SideW<T> cx = side(o, true), cy = side(o, false);
+    T dE, dN, dW, dS, unused;
+    // East, North (the cell is a), West, South (the cell is b)
+    edge_speeds(cx, side(on[0], true), false, i + 1 >= nx, A.g, A.hdry, dE, unused);
+    edge_speeds(cy, side(on[1], false), false, j + 1 >= ny, A.g, A.hdry, dN, unused);
+    edge_speeds(side(on[2], true), cx, i == 0, false, A.g, A.hdry, unused, dW);
+    edge_speeds(side(on[3], false), cy, j == 0, false, A.g, A.hdry, unused, dS);
+    s = (A.dy * dE + A.dx * dN) + (A.dy * dW + A.dx * dS);
   }
-  // block maximum (NaN wins), one atomic per block
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = nanmax_wd(s, __shfl_xor_sync(kFullWd, s, o));
   const int t = threadIdx.y * blockDim.x + threadIdx.x;
@@ -304,84 +275,170 @@ __global__ void __launch_bounds__(256) wd_cell_kernel(const WdArgs<T> A) {
     s = t < (int)(blockDim.x * blockDim.y / 32) ? part[t] : T(0);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = nanmax_wd(s, __shfl_xor_sync(kFullWd, s, o));
-    if (t == 0 && (s > T(0) || s != s)) atomic_max_wd(A.tmax_out, s);
+    if (t == 0 && (s > T(0) || s != s)) atomic_max_wd(A.tmax, s);
   }
   pdl_trigger();
 }
 
+// tile of TX x TY cells; shared memory holds the cells of the tile and a
+// two-cell ring, the x- and y-edges of the tile and a one-cell ring, and the
+// draining times of the tile and a one-cell ring
+constexpr int kWdTX = 32, kWdTY = 16;
+constexpr int kCX = kWdTX + 4, kCY = kWdTY + 4;  // cells (x0 - 2 + i, y0 - 2 + j)
+constexpr int kXX = kWdTX + 3, kXY = kWdTY + 2;  // x-edge (ii, jj): cells (x0-2+ii | x0-1+ii), row y0-1+jj
+constexpr int kYX = kWdTX + 2, kYY = kWdTY + 3;  // y-edge (ii, jj): column x0-1+ii, rows (y0-2+jj | y0-1+jj)
+constexpr int kRX = kWdTX + 2, kRY = kWdTY + 2;  // ring cells (x0 - 1 + i, y0 - 1 + j)
+enum { TE_M, TE_FA, TE_FB, TE_T, TE_C, TE_N };
+
 template <typename T>
-__global__ void __launch_bounds__(256) wd_update_kernel(const WdArgs<T> A) {
-  __shared__ T k_sh;
-  __shared__ int bad_dt;
+struct WdSmem {
+  T c[5][kCY][kCX];         // h, qx, qy, hC, H
+  T ex[TE_N][kXY][kXX];
+  T ey[TE_N][kYY][kYX];
+  T tau[kRY][kRX];
+  T kdt;
+  int bad_dt;
+};
+
+template <typename T>
+__device__ __forceinline__ SideW<T> sm_side(const WdSmem<T>& S, int j, int i, bool xdir) {
+  SideW<T> s;
+  s.h = S.c[0][j][i];
+  s.qn = xdir ? S.c[1][j][i] : S.c[2][j][i];
+  s.qt = xdir ? S.c[2][j][i] : S.c[1][j][i];
+  s.hC = S.c[3][j][i];
+  s.H = S.c[4][j][i];
+  return s;
+}
+
+template <typename T, bool EFIX>
+__global__ void __launch_bounds__(kWdTX * kWdTY) wd_tile_kernel(const WdArgs<T> A) {
+  extern __shared__ __align__(16) unsigned char wd_smem[];
+  WdSmem<T>& S = *reinterpret_cast<WdSmem<T>*>(wd_smem);
+  const int nx = A.nx, ny = A.ny;
+  const int x0 = blockIdx.x * kWdTX, y0 = blockIdx.y * kWdTY;
+  const int t = threadIdx.y * kWdTX + threadIdx.x;
+  constexpr int NT = kWdTX * kWdTY;
   pdl_wait();
-  const int t = threadIdx.y * blockDim.x + threadIdx.x;
   if (t == 0) {
-    const T tm = *reinterpret_cast<const T*>(A.tmax_in);
+    const T tm = *reinterpret_cast<const T*>(A.tmax);
     // dt = min_i 2 cfl |V_i| / sum L ||D|| (eq. (5)); no wet edge at all
     // (every cell dry) leaves no finite dt
     const double dt = A.two_cfl * A.area / (double)tm;
-    bad_dt = !(tm > T(0)) || !isfinite(dt);
-    k_sh = (T)dt;
+    S.bad_dt = !(tm > T(0)) || !isfinite(dt);
+    S.kdt = (T)dt;
     if (blockIdx.x == 0 && blockIdx.y == 0) {
       A.dt_hist[A.step % kHistCap] = dt;
       *A.t_dev += dt;
       if (sizeof(T) == 4) *reinterpret_cast<unsigned*>(A.tmax_clear) = 0u;
       else *reinterpret_cast<unsigned long long*>(A.tmax_clear) = 0ull;
-      if (bad_dt) atomicOr(A.err, kErrNonfinite);
+      if (S.bad_dt) atomicOr(A.err, kErrNonfinite);
+    }
+  }
+  // cells of the tile and a two-cell ring; outside the grid the nearest
+  // grid cell (never used as such: edges to it are walls)
+  for (int k = t; k < kCX * kCY; k += NT) {
+    const int i = k % kCX, j = k / kCX;
+    const int gx = min(max(x0 - 2 + i, 0), nx - 1), gy = min(max(y0 - 2 + j, 0), ny - 1);
+    const int64_t o = (int64_t)(gy + kPadY) * A.pitch + gx + kPadX;
+#pragma unroll
+    for (int f = 0; f < 4; ++f) S.c[f][j][i] = A.win[f][o];
+    S.c[4][j][i] = A.H[o];
+  }
+  __syncthreads();
+  // edges of the tile and its one-cell ring
+  auto inside = [&](int gx, int gy) { return gx >= 0 && gx < nx && gy >= 0 && gy < ny; };
+  for (int k = t; k < kXX * kXY + kYX * kYY; k += NT) {
+    EdgeW<T> e;
+    if (k < kXX * kXY) {
+      const int ii = k % kXX, jj = k / kXX;
+      const int gy = y0 - 1 + jj, ga = x0 - 2 + ii;
+      const bool ia = inside(ga, gy), ib = inside(ga + 1, gy);
+      e.m = e.fa = e.fb = e.t = e.c = T(0);
+      if (ia || ib)
+        e = edge_any<T, EFIX>(sm_side(S, jj + 1, ii, true), sm_side(S, jj + 1, ii + 1, true),
+                              !ia, !ib, A.g, A.hdry);
+      S.ex[TE_M][jj][ii] = e.m;
+      S.ex[TE_FA][jj][ii] = e.fa;
+      S.ex[TE_FB][jj][ii] = e.fb;
+      S.ex[TE_T][jj][ii] = e.t;
+      S.ex[TE_C][jj][ii] = e.c;
+    } else {
+      const int kk = k - kXX * kXY;
+      const int ii = kk % kYX, jj = kk / kYX;
+      const int gx = x0 - 1 + ii, ga = y0 - 2 + jj;
+      const bool ia = inside(gx, ga), ib = inside(gx, ga + 1);
+      e.m = e.fa = e.fb = e.t = e.c = T(0);
+      if (ia || ib)
+        e = edge_any<T, EFIX>(sm_side(S, jj, ii + 1, false), sm_side(S, jj + 1, ii + 1, false),
+                              !ia, !ib, A.g, A.hdry);
+      S.ey[TE_M][jj][ii] = e.m;
+      S.ey[TE_FA][jj][ii] = e.fa;
+      S.ey[TE_FB][jj][ii] = e.fb;
+      S.ey[TE_T][jj][ii] = e.t;
+      S.ey[TE_C][jj][ii] = e.c;
     }
   }
   __syncthreads();
-  const T dt = k_sh;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const int j = blockIdx.y * blockDim.y + threadIdx.y;
-  const int nx = A.nx, ny = A.ny;
+  // draining time of the tile's cells and the ring: h |V| / mass leaving per
+  // unit time (East, North, West, South: (E + N) + (W + S))
+  const T ly = A.dy, lx = A.dx;
+  for (int k = t; k < kRX * kRY; k += NT) {
+    const int i = k % kRX, j = k / kRX;
+    const T oE = fmax(ly * S.ex[TE_M][j][i + 1], T(0));
+    const T oN = fmax(lx * S.ey[TE_M][j + 1][i], T(0));
+    const T oW = fmax(-(ly * S.ex[TE_M][j][i]), T(0));
+    const T oS = fmax(-(lx * S.ey[TE_M][j][i]), T(0));
+    const T M = (oE + oN) + (oW + oS);
+    S.tau[j][i] = M > T(0) ? S.c[0][j + 1][i + 1] * (T)A.area / M : T(INFINITY);
+  }
+  __syncthreads();
+  // the update of the tile's own cell
+  const int ti = threadIdx.x, tj = threadIdx.y;
+  const int gx = x0 + ti, gy = y0 + tj;
   unsigned bad = 0;
-  if (i < nx && j < ny && !bad_dt) {
-    const int64_t kw = (int64_t)j * (nx + 1) + i, ks = (int64_t)j * nx + i;
-    const T ri = fmin(T(1), A.tau[ks] / dt);
-    // limit of an edge: the ratio of the cell its mass flux leaves
-    auto theta = [&](T m_out, bool nb_ok, int64_t nb) -> T {
-      if (m_out > T(0)) return ri;
-      if (m_out < T(0) && nb_ok) return fmin(T(1), A.tau[nb] / dt);
+  if (gx < nx && gy < ny && !S.bad_dt) {
+    const T dt = S.kdt;
+    const int ri = ti + 1, rj = tj + 1;  // ring coordinates of the cell
+    const T r0 = fmin(T(1), S.tau[rj][ri] / dt);
+    auto theta = [&](T m_out, bool nb_in, int ni, int nj) -> T {
+      if (m_out > T(0)) return r0;
+      if (m_out < T(0) && nb_in) return fmin(T(1), S.tau[nj][ni] / dt);
       return T(1);
     };
-    const T* ex = A.ex;
-    const T* ey = A.ey;
-    const T ly = A.dy, lx = A.dx;
-    // East (the cell is a), North (a), West (b), South (b)
-    const T mE = ly * ex[WD_M * A.xs + kw + 1], mN = lx * ey[WD_M * A.ys + ks + nx];
-    const T mW = ly * ex[WD_M * A.xs + kw], mS = lx * ey[WD_M * A.ys + ks];
-    const T tE = theta(mE, i + 1 < nx, ks + 1), tN = theta(mN, j + 1 < ny, ks + nx);
-    const T tW = theta(-mW, i > 0, ks - 1), tS = theta(-mS, j > 0, ks - nx);
+    const T mE = ly * S.ex[TE_M][rj][ri + 1], mN = lx * S.ey[TE_M][rj + 1][ri];
+    const T mW = ly * S.ex[TE_M][rj][ri], mS = lx * S.ey[TE_M][rj][ri];
+    const T tE = theta(mE, gx + 1 < nx, ri + 1, rj), tN = theta(mN, gy + 1 < ny, ri, rj + 1);
+    const T tW = theta(-mW, gx > 0, ri - 1, rj), tS = theta(-mS, gy > 0, ri, rj - 1);
     T fE[4], fN[4], fW[4], fS[4];
     fE[0] = tE * mE;
-    fE[1] = tE * (ly * ex[WD_FA * A.xs + kw + 1]);
-    fE[2] = tE * (ly * ex[WD_T * A.xs + kw + 1]);
-    fE[3] = tE * (ly * ex[WD_C * A.xs + kw + 1]);
+    fE[1] = tE * (ly * S.ex[TE_FA][rj][ri + 1]);
+    fE[2] = tE * (ly * S.ex[TE_T][rj][ri + 1]);
+    fE[3] = tE * (ly * S.ex[TE_C][rj][ri + 1]);
     fN[0] = tN * mN;
-    fN[1] = tN * (lx * ey[WD_T * A.ys + ks + nx]);
-    fN[2] = tN * (lx * ey[WD_FA * A.ys + ks + nx]);
-    fN[3] = tN * (lx * ey[WD_C * A.ys + ks + nx]);
+    fN[1] = tN * (lx * S.ey[TE_T][rj + 1][ri]);
+    fN[2] = tN * (lx * S.ey[TE_FA][rj + 1][ri]);
+    fN[3] = tN * (lx * S.ey[TE_C][rj + 1][ri]);
     fW[0] = -(tW * mW);
-    fW[1] = -(tW * (ly * ex[WD_FB * A.xs + kw]));
-    fW[2] = -(tW * (ly * ex[WD_T * A.xs + kw]));
-    fW[3] = -(tW * (ly * ex[WD_C * A.xs + kw]));
+    fW[1] = -(tW * (ly * S.ex[TE_FB][rj][ri]));
+    fW[2] = -(tW * (ly * S.ex[TE_T][rj][ri]));
+    fW[3] = -(tW * (ly * S.ex[TE_C][rj][ri]));
     fS[0] = -(tS * mS);
-    fS[1] = -(tS * (lx * ey[WD_T * A.ys + ks]));
-    fS[2] = -(tS * (lx * ey[WD_FB * A.ys + ks]));
-    fS[3] = -(tS * (lx * ey[WD_C * A.ys + ks]));
-    const int64_t o = (int64_t)(j + kPadY) * A.pitch + i + kPadX;
+    fS[1] = -(tS * (lx * S.ey[TE_T][rj][ri]));
+    fS[2] = -(tS * (lx * S.ey[TE_FB][rj][ri]));
+    fS[3] = -(tS * (lx * S.ey[TE_C][rj][ri]));
     const T kk = dt / (T)A.area;
     T w[4];
 #pragma unroll
-    for (int f = 0; f < 4; ++f) w[f] = A.w[f][o] - kk * ((fE[f] + fN[f]) + (fW[f] + fS[f]));
+    for (int f = 0; f < 4; ++f) w[f] = S.c[f][tj + 2][ti + 2] - kk * ((fE[f] + fN[f]) + (fW[f] + fS[f]));
     // clean-up: a depth below zero is rounding; a dry cell keeps no discharge
     if (w[0] < T(0)) w[0] = T(0);
     if (w[0] <= A.hdry) w[1] = w[2] = T(0);
     const T sum = (w[0] + w[1]) + (w[2] + w[3]);
     if (!isfinite(sum)) bad |= kErrNonfinite;
+    const int64_t o = (int64_t)(gy + kPadY) * A.pitch + gx + kPadX;
 #pragma unroll
-    for (int f = 0; f < 4; ++f) A.w[f][o] = w[f];
+    for (int f = 0; f < 4; ++f) A.wout[f][o] = w[f];
   }
   if (bad) atomicOr(A.err, bad);
   pdl_trigger();
@@ -408,7 +465,10 @@ __global__ void wd_check_kernel(const T* h, const T* qx, const T* qy, const T* h
 template <typename T>
 cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent_t* marks) {
   WdArgs<T> A;
-  for (int f = 0; f < 4; ++f) A.w[f] = (T*)a.w[f];
+  for (int f = 0; f < 4; ++f) {
+    A.win[f] = (const T*)a.win[f];
+    A.wout[f] = (T*)a.wout[f];
+  }
   A.H = (const T*)a.H;
   A.nx = a.nx;
   A.ny = a.ny;
@@ -417,34 +477,40 @@ cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent
   A.hdry = (T)a.h_dry;
   A.dx = (T)a.dx;
   A.dy = (T)a.dy;
-  A.ex = (T*)a.ex;
-  A.ey = (T*)a.ey;
-  A.xs = a.xs;
-  A.ys = a.ys;
-  A.tau = (T*)a.tau;
   A.two_cfl = a.two_cfl;
   A.area = a.dx * a.dy;
-  A.tmax_out = a.tmax_slot;
-  A.tmax_in = a.tmax_slot;
+  A.tmax = a.tmax_slot;
   A.tmax_clear = a.tmax_clear;
   A.dt_hist = a.dt_hist;
   A.t_dev = a.t_dev;
   A.step = a.step;
   A.err = a.err;
-  A.efix = a.efix;
-  const dim3 blk(32, 8);
-  const dim3 ge((unsigned)((a.nx + 1 + 31) / 32), (unsigned)((a.ny + 1 + 7) / 8));
-  const dim3 gc((unsigned)((a.nx + 31) / 32), (unsigned)((a.ny + 7) / 8));
+  const dim3 blk(kWdTX, kWdTY), sblk(32, 8);
+  const dim3 grid((unsigned)((a.nx + kWdTX - 1) / kWdTX), (unsigned)((a.ny + kWdTY - 1) / kWdTY));
+  const dim3 sgrid((unsigned)((a.nx + 31) / 32), (unsigned)((a.ny + 7) / 8));
+  const size_t smem = sizeof(WdSmem<T>);
   cudaError_t e;
+  // the tile's shared memory can exceed the default 48 KB (fp64): allow it
+  // once per process (the attribute is idempotent)
+  static bool attr_set = false;
+  if (!attr_set) {
+    if ((e = cudaFuncSetAttribute(wd_tile_kernel<T, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(wd_tile_kernel<T, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return e;
+    attr_set = true;
+  }
   if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
-  e = a.efix ? launch_pdl(wd_edge_kernel<T, true>, ge, blk, 0, st, A)
-             : launch_pdl(wd_edge_kernel<T, false>, ge, blk, 0, st, A);
-  if (e != cudaSuccess) return e;
+  if ((e = launch_pdl(wd_speed_kernel<T>, sgrid, sblk, 0, st, A)) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
-  if ((e = launch_pdl(wd_cell_kernel<T>, gc, blk, 0, st, A)) != cudaSuccess) return e;
+  e = a.efix ? launch_pdl(wd_tile_kernel<T, true>, grid, blk, smem, st, A)
+             : launch_pdl(wd_tile_kernel<T, false>, grid, blk, smem, st, A);
+  if (e != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
-  if ((e = launch_pdl(wd_update_kernel<T>, gc, blk, 0, st, A)) != cudaSuccess) return e;
-  if (marks && (e = cudaEventRecord(marks[3], st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -135,9 +135,10 @@ typedef struct {
  *             time of Bollermann, Chen, Kurganov and Noelle, J. Sci. Comput.
  *             56, 2013).  After each step a depth below zero (rounding) is
  *             clamped to 0 and a dry cell's discharge is set to 0.  h = 0
- *             is then a valid input; dt stays eq. (5).  Runs as three
- *             kernels per step (edges, cells, update) instead of the fused
- *             step.  Any value other than 0 or 1 returns SWE_ERR_ARG.
+ *             is then a valid input; dt stays eq. (5).  Runs as two
+ *             kernels per step (wave speeds; a tile pass of edges, draining
+ *             times and update) instead of the fused step.  Any value other
+ *             than 0 or 1 returns SWE_ERR_ARG.
  *  h_dry      with wet_dry = 1: the depth at or below which a cell is dry,
  *             >= 0 and finite.  It must exceed the thin-film scale of the
  *             problem: with 1e-6 m a film of a few tenths of a millimetre
@@ -162,8 +163,8 @@ typedef struct swe_state swe_state;
 /* Create a simulation on a Cartesian grid ([P1] Algorithm 1, before the time
  * loop: mesh construction and initial state).
  *  grid    grid size and spacing; nx, ny >= 1, dx, dy > 0 and finite;
- *          nx <= 2^30, ny <= 2^30 - 8; with wet_dry also ny <= 524279
- *          (65535 blocks of 8 edge rows)
+ *          nx <= 2^30, ny <= 2^30 - 8; with wet_dry also ny <= 524280
+ *          (65535 blocks of 8 rows)
  *  H       host, nx*ny values: bottom depth below the reference level
  *  W0      host, array of 4 pointers (h, qx, qy, hC), or 6 (h1, q1x, q1y,
  *          h2, q2x, q2y) for two layers, nx*ny values each; depths > 0

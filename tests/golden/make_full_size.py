@@ -5,6 +5,8 @@ sizes and step counts:
     hills2048   2048 x 2048 grid, one layer + pollutant, 1000 steps, fp64 and fp32
     pulses8192  8192 x 8192 grid, one layer + pollutant,  200 steps, fp32
     tri1024     2,097,152 triangles, two layers,           500 steps, fp32
+    flood2048   2048 x 2048 grid, one layer + pollutant with wet/dry fronts and
+                the entropy fix,                           500 steps, fp64
 
 An fp32 record is the fp64 oracle started from the inputs rounded to fp32 (the
 values the fp32 GPU run starts from).  Each record holds the dt of every step
@@ -23,6 +25,7 @@ one CPU core each.  Run from the repository root, one record per process:
     python tests/golden/make_full_size.py hills2048 32
     python tests/golden/make_full_size.py pulses8192 32
     python tests/golden/make_full_size.py tri1024 32
+    python tests/golden/make_full_size.py flood2048 64
 """
 import json
 import os
@@ -93,7 +96,10 @@ def make(name, precision):
         names = ("h", "qx", "qy", "hC")
         W0 = I.fields_of(dr)
         nx, ny = d["nx"], d["ny"]
-        W, dts, st = O.grid_run1(nx, ny, d["dx"], d["dy"], dr["H"], W0, d["g"], d["cfl"], steps)
+        with O.wet_dry(d.get("h_dry", 0.0), on=bool(d.get("wet_dry", 0))), \
+                O.entropy_fix(d.get("entropy_fix", 0)):
+            W, dts, st = O.grid_run1(nx, ny, d["dx"], d["dy"], dr["H"], W0, d["g"], d["cfl"],
+                                     steps)
         area = np.full(nx * ny, d["dx"] * d["dy"])
         cells = _grid_sample(nx, ny, rng)
         blocks = _grid_block_means(W, nx, ny)

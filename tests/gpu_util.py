@@ -22,7 +22,8 @@ def gpu_create(d, precision, cfl=None, stream=None):
     return S.swe_create_grid(d["nx"], d["ny"], d["dx"], d["dy"], d["H"].astype(dt),
                              [f.astype(dt) for f in I.fields_of(d)], precision=precision,
                              g=d["g"], cfl=d["cfl"] if cfl is None else cfl, stream=stream,
-                             entropy_fix=d.get("entropy_fix", 0))
+                             entropy_fix=d.get("entropy_fix", 0), wet_dry=d.get("wet_dry", 0),
+                             h_dry=d.get("h_dry", 0.0))
 
 
 def gpu_run(d, precision, nsteps, use_run=False):

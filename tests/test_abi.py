@@ -101,7 +101,7 @@ def _create(lib, grid, params, n=12, with_fields=True):
     (_grid(), _params(wet_dry=1, h_dry=float("inf")), S.SWE_ERR_ARG),
     (_grid(), _params(n_layers=2, pollutant=0, r=0.5, wet_dry=1, h_dry=1e-4),
      S.SWE_ERR_UNSUPPORTED),
-    (_grid(ny=524280), _params(wet_dry=1, h_dry=1e-4), S.SWE_ERR_ARG),
+    (_grid(ny=524281), _params(wet_dry=1, h_dry=1e-4), S.SWE_ERR_ARG),
 ])
 def test_create_rejects_bad_arguments(lib, grid, params, expect):
     st, out = _create(lib, grid, params)

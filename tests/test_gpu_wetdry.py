@@ -158,7 +158,7 @@ def test_per_kernel_timing_lists_the_wet_dry_kernels():
     S.swe_run(st, 5)
     tm = S.swe_get_timing(st)
     S.swe_destroy(st)
-    assert list(tm) == ["wd_edge_kernel", "wd_cell_kernel", "wd_update_kernel"]
+    assert list(tm) == ["wd_speed_kernel", "wd_tile_kernel"]
     assert all(v[0] == 5 and v[1] > 0 for v in tm.values())
 
 

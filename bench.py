@@ -144,7 +144,7 @@ DESCR = {
                  "bed rising 4 m across x plus 64 seeded Gaussian hills (amplitude "
                  "U[0.5,2.5] m), lake at rest at level 0 (about half the domain dry), a disc "
                  "of radius 2048 m raised by 2 m at the centre flooding dry land, "
-                 "h_dry=1e-4 m, Harten-Hyman entropy fix, reflective walls",
+                 "h_dry=1e-2 m, Harten-Hyman entropy fix, reflective walls",
     "tri1024_1l": "one layer with pollutant on 1024x1024 unit squares split into 2,097,152 "
                   "triangles, interior vertices jittered by +-0.2, cells shuffled then "
                   "RCM-reordered, 6 Gaussian hills under a 2 m deep surface, 4 surface pulses "

@@ -393,13 +393,15 @@ def make_workload(name, nx=None, ny=None, lake_at_rest=False):
     if name == "flood2048":
         # wet/dry fronts: a bed rising 4 m across the domain with 64 hills
         # (16 per 1024^2 cells), a lake at rest at level 0 (about half the
-        # domain dry), a disc of radius L/10 raised by 2 m at the centre
+        # domain dry), a disc of radius L/10 raised by 2 m at the centre;
+        # cells below 1 cm are dry (thinner films run up the slope at
+        # unphysical speeds)
         lx = nx * dx
         n_h = max(8, int(round(64 * nx * ny / (2048 * 2048))))
         d = emerged_hills(nx, ny, dx, seed=w["seed"], n_hills=n_h, eta=0.0,
                           column=(0.5 * lx, 0.5 * ny * dx, 0.1 * lx, 2.0), slope=4.0 / lx)
         d.update(g=G_DEFAULT, cfl=CFL_DEFAULT, steps=w["steps"], precision=w["precision"],
-                 name=name, wet_dry=1, h_dry=1e-4, entropy_fix=1)
+                 name=name, wet_dry=1, h_dry=1e-2, entropy_fix=1)
         return d
     if name == "tri1024_1l":
         d = tri_workload1(nx, ny, seed=w["seed"])

@@ -141,10 +141,12 @@ typedef struct {
  *             than 0 or 1 returns SWE_ERR_ARG.
  *  h_dry      with wet_dry = 1: the depth at or below which a cell is dry,
  *             >= 0 and finite.  It must exceed the thin-film scale of the
- *             problem: with 1e-6 m a film of a few tenths of a millimetre
- *             next to deep water was driven to km/s velocities (and dt
- *             collapsed) in the oracle; 1e-4 m to 1e-3 m kept the fastest
- *             speed physical.  Ignored when wet_dry = 0. */
+ *             problem: a film just above h_dry next to deep water receives
+ *             the deep side's pressure and can be driven to unphysical
+ *             speeds, which collapses dt.  In the oracle, water at rest
+ *             around emerging hills needed 1e-4 m (1e-6 m: km/s); a column
+ *             of water flooding up a slope needed 1e-2 m (1e-4 m: 130 m/s,
+ *             dt down 440-fold).  Ignored when wet_dry = 0. */
 typedef struct {
   int32_t n_layers;
   int32_t precision;

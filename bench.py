@@ -88,11 +88,13 @@ KERNEL_SOURCES = {
     # (swe_fastmath.cuh is used by the fp64 kernels only, which have no
     # traffic record)
     "cart2_march_kernel<plain>": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
-                                  "cart2_flux_traffic.txt"),
+                                  "cart2_march_traffic.txt"),
     "cart2_march_kernel<fused>": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
-                                  "cart2_flux_traffic.txt"),
+                                  "cart2_march_traffic.txt"),
     "cart2_update_kernel": (("swe_cart2.cu", "swe_roe2.cuh", "swe_internal.h"),
-                            "cart2_flux_traffic.txt"),
+                            "cart2_march_traffic.txt"),
+    "wd_speed_kernel": (("swe_wetdry.cu", "swe_internal.h"), "wetdry_traffic.txt"),
+    "wd_tile_kernel": (("swe_wetdry.cu", "swe_internal.h"), "wetdry_traffic.txt"),
     "mesh_edge_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"), "mesh_traffic.txt"),
     "mesh_gather_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"),
                            "mesh_traffic.txt"),

@@ -756,6 +756,8 @@ swe_status swe_create_grid(const swe_grid* grid, const void* H, const void* cons
   if (s->nl == 1) st = s->prec == 32 ? plan_launch<float>(s) : plan_launch<double>(s);
   else st = s->prec == 32 ? plan_launch2<float>(s) : plan_launch2<double>(s);
   if (st != SWE_OK) return fail(st);
+  if (s->wd && (e = s->prec == 32 ? wd_prepare<float>() : wd_prepare<double>()) != cudaSuccess)
+    return fail(cuda_status(e));
   st = s->prec == 32 ? fill_pads<float>(s) : fill_pads<double>(s);
   if (st != SWE_OK) return fail(st);
   void* hdst[1] = {s->H};

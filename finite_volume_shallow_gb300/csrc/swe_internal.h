@@ -256,6 +256,10 @@ struct WdStepArgs {
   unsigned* err;
   int efix;
 };
+// Launch attributes of the wet/dry kernels on the current device (once per
+// handle, before the first step).
+template <typename T>
+cudaError_t wd_prepare();
 template <typename T>
 cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent_t* marks);
 template <typename T>

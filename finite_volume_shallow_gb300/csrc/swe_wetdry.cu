@@ -490,20 +490,6 @@ cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent
   const dim3 sgrid((unsigned)((a.nx + 31) / 32), (unsigned)((a.ny + 7) / 8));
   const size_t smem = sizeof(WdSmem<T>);
   cudaError_t e;
-  // the tile's shared memory can exceed the default 48 KB (fp64): allow it
-  // once per process (the attribute is idempotent)
-  static bool attr_set = false;
-  if (!attr_set) {
-    if ((e = cudaFuncSetAttribute(wd_tile_kernel<T, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(wd_tile_kernel<T, false>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
-      return e;
-    attr_set = true;
-  }
   if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
   if ((e = launch_pdl(wd_speed_kernel<T>, sgrid, sblk, 0, st, A)) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
@@ -512,6 +498,18 @@ cudaError_t launch_wd_step(const WdStepArgs& a, cudaStream_t st, const cudaEvent
   if (e != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
   return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t wd_prepare() {
+  // the tile's shared memory exceeds the default 48 KB in fp64: allow it on
+  // the current device (function attributes are per device)
+  const int smem = (int)sizeof(WdSmem<T>);
+  cudaError_t e = cudaFuncSetAttribute(wd_tile_kernel<T, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(wd_tile_kernel<T, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 template <typename T>
@@ -524,6 +522,8 @@ cudaError_t launch_wd_check(const T* const* w, int nx, int ny, int pitch, unsign
 
 template cudaError_t launch_wd_step<float>(const WdStepArgs&, cudaStream_t, const cudaEvent_t*);
 template cudaError_t launch_wd_step<double>(const WdStepArgs&, cudaStream_t, const cudaEvent_t*);
+template cudaError_t wd_prepare<float>();
+template cudaError_t wd_prepare<double>();
 template cudaError_t launch_wd_check<float>(const float* const*, int, int, int, unsigned*,
                                             cudaStream_t);
 template cudaError_t launch_wd_check<double>(const double* const*, int, int, int, unsigned*,

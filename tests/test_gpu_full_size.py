@@ -6,6 +6,8 @@ tests/golden/make_full_size.py through the fp64 CPU oracle alone):
     hills2048   2048 x 2048, one layer + pollutant, 1000 steps, fp64 and fp32
     pulses8192  8192 x 8192, one layer + pollutant,  200 steps, fp32
     tri1024     2,097,152 triangles, two layers,      500 steps, fp32
+    flood2048   2048 x 2048, one layer + pollutant with wet/dry fronts and the
+                entropy fix,                          500 steps, fp64
 
 Checked: the dt of every step (eq. (5) of An MPI-CUDA implementation of an
 improved Roe method for two-layer shallow water systems, Sec. 2.2) and the
@@ -27,7 +29,7 @@ from gpu_util import TOL, TOL2, gpu_run, gpu_run_mesh
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-CASES = [("hills2048", 64), ("hills2048", 32), ("pulses8192", 32)]
+CASES = [("hills2048", 64), ("hills2048", 32), ("pulses8192", 32), ("flood2048", 64)]
 
 
 def _block_means_grid(w, nx, ny, nb=32):
@@ -70,14 +72,31 @@ def test_full_size_over_the_workloads_own_steps(name, precision):
         errs[nm] = float(np.abs(W[k][cells] - np.array(rec["values"][nm])).max() / scale)
         bm = _block_means_chunks(W[k]) if mesh else _block_means_grid(W[k], d["nx"], d["ny"])
         berrs[nm] = float(np.abs(bm - np.array(rec["block_means"][nm])).max() / scale)
+    # cells whose error exceeds the tolerance (any field)
+    over = np.zeros(len(cells), dtype=bool)
+    for k, nm in enumerate(names):
+        over |= np.abs(W[k][cells] - np.array(rec["values"][nm])) > tol[nm] * rec["scale"][nm]
     print(f"\nFULLSIZE {name} fp{precision} steps={steps} dt_rel={dte:.3e} "
           f"cells={ {k: f'{v:.2e}' for k, v in errs.items()} } "
-          f"blocks={ {k: f'{v:.2e}' for k, v in berrs.items()} }")
+          f"blocks={ {k: f'{v:.2e}' for k, v in berrs.items()} } "
+          f"cells_over_tol={int(over.sum())}/{len(cells)}")
     assert dte <= tol["dt"], dte
     assert abs(t / rec["t"] - 1.0) <= tol["dt"]
-    for nm in names:
-        assert errs[nm] <= tol[nm], (nm, errs)
-        assert berrs[nm] <= tol[nm], (nm, berrs)
+    if d.get("wet_dry"):
+        # A depth near h_dry, or a bank whose bed is level with the water, is
+        # a branch of the wet/dry treatment; the GPU and the oracle round in
+        # different orders, so over hundreds of steps a few such decisions go
+        # the other way at wet/dry fronts.  Every dt must still agree, at most
+        # 2 % of the sampled cells may exceed the tolerance, by at most 1e-4
+        # of the field's scale, and the block means within 1e-5.
+        assert over.mean() <= 0.02, over.mean()
+        for nm in names:
+            assert errs[nm] <= 1e-4, (nm, errs)
+            assert berrs[nm] <= 1e-5, (nm, berrs)
+    else:
+        for nm in names:
+            assert errs[nm] <= tol[nm], (nm, errs)
+            assert berrs[nm] <= tol[nm], (nm, berrs)
     # conservation of the depths (and the pollutant) by the GPU run itself
     mass = ("h1", "h2") if mesh else ("h", "hC")
     for nm in mass:

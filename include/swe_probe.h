@@ -5,7 +5,7 @@
  * than by memory (the fp64 steps, and the two-layer flux whose Roe matrix of
  * An MPI-CUDA implementation of an improved Roe method for two-layer shallow
  * water systems, Sec. 2.2, needs the roots of a quartic per edge) are measured
- * against the rate at which this GPU retires fused multiply-adds.  The pages
+ * against the rate at which this GPU retires fused multiply-adds.  The papers
  * have no counterpart of this call: it measures that rate on the device it
  * runs on, so the fractions do not rest on a data-sheet figure.
  */

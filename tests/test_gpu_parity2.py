@@ -200,3 +200,13 @@ def test_grid_taller_than_a_launch_dimension():
     # oracle
     d = I.two_layer_hills(2, 530_000, umax=0.05, bump=0.5)
     assert_parity2(d, 32, 3)
+
+
+@pytest.mark.parametrize("precision", [32, 64])
+@pytest.mark.parametrize("nx,ny", [(30, 17), (60, 9), (61, 23), (91, 40), (29, 70)])
+def test_band_borders_of_the_march(precision, nx, ny):
+    # widths at and around multiples of the march's 30-column bands: a band
+    # whose halo lane sits on the east wall, a band with one column, and
+    # row segments of a few rows each
+    d = I.two_layer_hills(nx, ny, umax=0.05, bump=0.5)
+    assert_parity2(d, precision, 15)

@@ -95,9 +95,7 @@ KERNEL_SOURCES = {
                             "cart2_march_traffic.txt"),
     "wd_speed_kernel": (("swe_wetdry.cu", "swe_internal.h"), "wetdry_traffic.txt"),
     "wd_tile_kernel": (("swe_wetdry.cu", "swe_internal.h"), "wetdry_traffic.txt"),
-    "mesh_edge_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"), "mesh_traffic.txt"),
-    "mesh_gather_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"),
-                           "mesh_traffic.txt"),
+    "mesh_tile_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"), "mesh_traffic.txt"),
     "mesh_update_kernel": (("swe_mesh.cu", "swe_roe2.cuh", "swe_internal.h"),
                            "mesh_traffic.txt"),
 }
@@ -110,11 +108,15 @@ def source_hash(files):
         h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
 # Triangle meshes, two layers, per edge: floating-point operations of the
-# edge kernel, counted from its formulas: the Roe flux above (2.0 outer
-# iterations per edge in fp32, 3.0 in fp64 on the triangle workload) plus 79
-# for the rotations into and out of the edge frame, the fluctuation terms and
-# the edge-length scaling; one layer 88 (in fp32 the one-layer edge kernel
-# is modelled by its bytes instead: its arithmetic is light).
+# flux part of the tile kernel, counted from its formulas: the Roe flux above
+# (2.0 outer iterations per edge in fp32, 3.0 in fp64 on the triangle
+# workload) plus 79 for the rotations into and out of the edge frame, the
+# fluctuation terms and the edge-length scaling; one layer 88.  Each edge is
+# counted once (the second evaluation of an edge shared by two tiles is not
+# counted).  Per cell the tile kernel adds 3 nf + 3 for the sums of its three
+# edges, the division by the area and the wave-speed sum.  In fp32 the
+# one-layer tile kernel is modelled by its bytes instead: its arithmetic is
+# light.
 FLOPS_PER_EDGE_MESH = {(2, 32): FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L
                        + 28 * 2.0 + 28 * 2 + 79,
                        (2, 64): FLOPS_EDGE_2L_BASE + FLOPS_PER_WAVE_2L * WAVES_2L
@@ -140,7 +142,7 @@ DESCR = {
     "interface2048": "two layers, 2048x2048 Cartesian, dx=10 m, flat bottom 10 m, interface "
                      "dam break h1=6/4 m at x=L/2, r=0.98, at rest, reflective walls",
     "tri1024": "two layers on 1024x1024 unit squares split into 2,097,152 triangles, interior "
-               "vertices jittered by +-0.2, cells shuffled then RCM-reordered, r=0.98, "
+               "vertices jittered by +-0.2, cells shuffled then put in Hilbert order, r=0.98, "
                "8 Gaussian hills, 0.5 m interface bump, at rest, reflective walls",
     "flood2048": "one layer with pollutant and wet/dry fronts, 2048x2048 Cartesian, dx=10 m, "
                  "bed rising 4 m across x plus 64 seeded Gaussian hills (amplitude "
@@ -149,7 +151,7 @@ DESCR = {
                  "h_dry=1e-2 m, Harten-Hyman entropy fix, reflective walls",
     "tri1024_1l": "one layer with pollutant on 1024x1024 unit squares split into 2,097,152 "
                   "triangles, interior vertices jittered by +-0.2, cells shuffled then "
-                  "RCM-reordered, 6 Gaussian hills under a 2 m deep surface, 4 surface pulses "
+                  "put in Hilbert order, 6 Gaussian hills under a 2 m deep surface, 4 surface pulses "
                   "of 0.5 m, |u|<=0.1 m/s per component, pollutant per 4x4 block of squares, "
                   "reflective walls",
 }
@@ -170,16 +172,14 @@ def kernel_model(kernel, precision, nl, n_cells, n_edges):
         return "alu", (FLOPS_PER_CELL_2L[precision] + 12) * n_cells, "flop"
     if kernel == "cart2_update_kernel":
         return "hbm", 3 * 6 * e * n_cells, "B"
-    ne = 11 if nl == 2 else 7
-    if kernel == "mesh_edge_kernel" and nl == 1 and precision == 32:
-        # light arithmetic: two cell ids, normal and length, the 7 results
-        # per edge, and the 5 values (state + H) of each cell once
-        return "hbm", (8 + 3 * e + ne * e) * n_edges + 5 * e * n_cells, "B"
-    if kernel == "mesh_edge_kernel":
-        return "alu", FLOPS_PER_EDGE_MESH[(nl, precision)] * n_edges, "flop"
-    if kernel == "mesh_gather_kernel":
-        # three int32 references, every edge record once, 1/|V|, R written
-        return "hbm", (12 + e + nf * e) * n_cells + ne * e * n_edges, "B"
+    if kernel == "mesh_tile_kernel" and nl == 1 and precision == 32:
+        # light arithmetic: the state and H of every cell read once, its
+        # slot references (8 B), 1/|V| and R written; per edge its two cell
+        # indices (4 B) and normal and length, once
+        return "hbm", ((nf + 1) * e + nf * e + e + 8) * n_cells + (4 + 3 * e) * n_edges, "B"
+    if kernel == "mesh_tile_kernel":
+        return "alu", (FLOPS_PER_EDGE_MESH[(nl, precision)] * n_edges
+                       + (3 * nf + 3) * n_cells), "flop"
     if kernel == "mesh_update_kernel":
         return "hbm", 3 * nf * e * n_cells, "B"
     # wet/dry on a grid: each field crosses HBM once per pass
@@ -696,8 +696,11 @@ def main():
                        "l2": "inputs larger than L2 (no flush needed)"
                              if info["device_bytes"] > 129e6 else "inputs fit in L2 (no flush)",
                        "device_bytes": info["device_bytes"],
-                       "launch": {"bands": info["bands"], "segments": info["segments"],
-                                  "warps_per_block": info["warps_per_block"]}},
+                       "launch": ({"tiles": info["bands"], "blocks": info["segments"],
+                                   "warps_per_block": info["warps_per_block"]}
+                                  if d.get("mesh") else
+                                  {"bands": info["bands"], "segments": info["segments"],
+                                   "warps_per_block": info["warps_per_block"]})},
             "e2e": e2e, "roofline": roof, "cpu_baseline": base, "clocks": clocks,
             "alu_peaks": {k: v for k, v in alu.items() if isinstance(k, str)},
             "gpu_launches": sum(v[0] for v in ktimes.values()),

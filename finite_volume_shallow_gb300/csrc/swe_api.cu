@@ -52,15 +52,17 @@ struct swe_state {
   unsigned sticky = 0;
   // triangle meshes
   bool mesh = false;
-  int64_t ncells = 0, nedges = 0;
-  int64_t estride = 0;               // elements between per-edge result arrays
-  void* ea = nullptr;                // int32 [nedges]
-  void* eb = nullptr;
-  void* enx = nullptr;               // T [nedges]
-  void* eny = nullptr;
-  void* elen = nullptr;
-  void* ebuf = nullptr;              // T [ne_fields * estride]
-  void* ref[3] = {nullptr};          // int32 [ncells]
+  int64_t ncells = 0, nedges = 0, ntiles = 0;
+  int mesh_grid = 0;                 // blocks of the tile kernel
+  void* tile_cell = nullptr;         // int32 [ntiles + 1]
+  void* tile_halo = nullptr;
+  void* tile_slot = nullptr;
+  void* halo = nullptr;              // int32 [halo entries]
+  void* slot_ab = nullptr;           // int32 [slots]
+  void* slot_nx = nullptr;           // T [slots]
+  void* slot_ny = nullptr;
+  void* slot_len = nullptr;
+  void* cref = nullptr;              // uint2 [ncells]
   void* inv_area = nullptr;          // T [ncells]
   int32_t* new_of_old = nullptr;     // device [ncells]
   int32_t* old_of_new = nullptr;
@@ -335,17 +337,19 @@ swe_status enqueue_mesh_step(swe_state* s, double cfl) {
     u.R[k] = (const T*)s->R[k];
   }
   f.H = (const T*)s->H;
-  f.ea = (const int32_t*)s->ea;
-  f.eb = (const int32_t*)s->eb;
-  f.enx = (const T*)s->enx;
-  f.eny = (const T*)s->eny;
-  f.elen = (const T*)s->elen;
-  f.ebuf = (T*)s->ebuf;
-  f.estride = s->estride;
-  for (int k = 0; k < 3; ++k) f.ref[k] = (const int32_t*)s->ref[k];
+  f.tile_cell = (const int32_t*)s->tile_cell;
+  f.tile_halo = (const int32_t*)s->tile_halo;
+  f.tile_slot = (const int32_t*)s->tile_slot;
+  f.halo = (const int32_t*)s->halo;
+  f.slot_ab = (const int32_t*)s->slot_ab;
+  f.slot_nx = (const T*)s->slot_nx;
+  f.slot_ny = (const T*)s->slot_ny;
+  f.slot_len = (const T*)s->slot_len;
+  f.cref = (const uint2*)s->cref;
   f.inv_area = (const T*)s->inv_area;
   f.ncells = u.ncells = s->ncells;
-  f.nedges = s->nedges;
+  f.ntiles = s->ntiles;
+  f.grid = s->mesh_grid;
   f.g = (T)s->p.g;
   f.r = (T)s->p.r;
   f.tmax_out = sl + (s->step % 3) * sizeof(uint64_t);
@@ -481,10 +485,9 @@ void timing_names(swe_state* s, Timing* tm) {
     tm->names[0] = "wd_speed_kernel";
     tm->names[1] = "wd_tile_kernel";
   } else if (s->mesh) {
-    tm->nk = 3;
-    tm->names[0] = "mesh_edge_kernel";
-    tm->names[1] = "mesh_gather_kernel";
-    tm->names[2] = "mesh_update_kernel";
+    tm->nk = 2;
+    tm->names[0] = "mesh_tile_kernel";
+    tm->names[1] = "mesh_update_kernel";
   } else if (s->nl == 2) {
     tm->nk = 3;
     tm->names[0] = "cart2_march_kernel<plain>";
@@ -796,6 +799,7 @@ swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* cons
   const int rc = prepare_mesh(mesh->n_vertices, mesh->xy, mesh->n_cells, mesh->tri,
                               mesh->reorder == 1, &prep);
   if (rc == -3) return SWE_ERR_OOM;
+  if (rc == -2) return SWE_ERR_UNSUPPORTED;
   if (rc != 0) return SWE_ERR_ARG;
 
   swe_state* s = new (std::nothrow) swe_state();
@@ -815,13 +819,17 @@ swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* cons
   } catch (const std::bad_alloc&) {
     return fail(SWE_ERR_OOM);
   }
-  const int64_t nc = s->ncells, ne = s->nedges, esz = (int64_t)s->esz;
-  const int nef = s->nl == 2 ? MeshLayout<2>::ne : MeshLayout<1>::ne;
+  s->ntiles = prep.ntiles;
+  const int64_t nc = s->ncells, esz = (int64_t)s->esz;
+  const int64_t nt1 = prep.ntiles + 1, nhalo = (int64_t)prep.halo.size();
+  const int64_t nsl = (int64_t)prep.slot_ab.size();
   const int64_t fb = round_up(nc * esz, 256), ib = round_up(nc * 4, 256);
-  const int64_t et = round_up(ne * esz, 256), ei = round_up(ne * 4, 256);
+  const int64_t tb = round_up(nt1 * 4, 256), hb = round_up(nhalo * 4 + 4, 256);
+  const int64_t sib = round_up(nsl * 4, 256), stb = round_up(nsl * esz, 256);
+  const int64_t cb = round_up(nc * 8, 256);
   s->field_stride = fb / esz;
-  s->estride = et / esz;
-  s->dev_bytes = (size_t)((2 * s->nf + 2) * fb + 5 * ib + 2 * ei + (3 + nef) * et + kAuxBytes);
+  s->dev_bytes = (size_t)((2 * s->nf + 2) * fb + 2 * ib + 3 * tb + hb + sib + 3 * stb + cb +
+                          kAuxBytes);
   cudaError_t e = cudaMalloc(&s->dev, s->dev_bytes);
   if (e != cudaSuccess) {
     s->dev = nullptr;
@@ -837,31 +845,40 @@ swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* cons
   for (int f = 0; f < s->nf; ++f) s->R[f] = take(fb);
   s->H = take(fb);
   s->inv_area = take(fb);
-  for (int k = 0; k < 3; ++k) s->ref[k] = take(ib);
   s->new_of_old = (int32_t*)take(ib);
   s->old_of_new = (int32_t*)take(ib);
-  s->ea = take(ei);
-  s->eb = take(ei);
-  s->enx = take(et);
-  s->eny = take(et);
-  s->elen = take(et);
-  s->ebuf = take(nef * et);
+  s->tile_cell = take(tb);
+  s->tile_halo = take(tb);
+  s->tile_slot = take(tb);
+  s->halo = take(hb);
+  s->slot_ab = take(sib);
+  s->slot_nx = take(stb);
+  s->slot_ny = take(stb);
+  s->slot_len = take(stb);
+  s->cref = take(cb);
   swe_status st;
   if ((st = carve_aux(s, p)) != SWE_OK) return fail(st);
+  e = s->prec == 32 ? mesh_prepare<float>(s->nl, s->p.entropy_fix, s->ntiles, &s->mesh_grid)
+                     : mesh_prepare<double>(s->nl, s->p.entropy_fix, s->ntiles, &s->mesh_grid);
+  if (e != cudaSuccess) return fail(cuda_status(e));
 
-  // geometry and orderings (synchronous copies from the temporary arrays)
-  auto put_i32 = [&](void* dst, const int32_t* src, int64_t n) {
-    return cuda_status(cudaMemcpy(dst, src, (size_t)n * 4, cudaMemcpyHostToDevice));
+  // geometry, tiles and orderings (synchronous copies from the temporary arrays)
+  auto put_raw = [&](void* dst, const void* src, int64_t bytes) {
+    if (bytes == 0) return SWE_OK;
+    return cuda_status(cudaMemcpy(dst, src, (size_t)bytes, cudaMemcpyHostToDevice));
   };
-  if ((st = put_i32(s->ea, prep.ea.data(), ne)) != SWE_OK) return fail(st);
-  if ((st = put_i32(s->eb, prep.eb.data(), ne)) != SWE_OK) return fail(st);
-  for (int k = 0; k < 3; ++k)
-    if ((st = put_i32(s->ref[k], prep.ref.data() + k * nc, nc)) != SWE_OK) return fail(st);
-  if ((st = put_i32(s->new_of_old, prep.new_of_old.data(), nc)) != SWE_OK) return fail(st);
-  if ((st = put_i32(s->old_of_new, prep.old_of_new.data(), nc)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->new_of_old, prep.new_of_old.data(), nc * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->old_of_new, prep.old_of_new.data(), nc * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->tile_cell, prep.tile_cell.data(), nt1 * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->tile_halo, prep.tile_halo.data(), nt1 * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->tile_slot, prep.tile_slot.data(), nt1 * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->halo, prep.halo.data(), nhalo * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->slot_ab, prep.slot_ab.data(), nsl * 4)) != SWE_OK) return fail(st);
+  if ((st = put_raw(s->cref, prep.cref.data(), nc * 8)) != SWE_OK) return fail(st);
   try {
-    void* dsts[4] = {s->enx, s->eny, s->elen, s->inv_area};
-    const std::vector<double>* srcs[4] = {&prep.enx, &prep.eny, &prep.elen, &prep.inv_area};
+    void* dsts[4] = {s->slot_nx, s->slot_ny, s->slot_len, s->inv_area};
+    const std::vector<double>* srcs[4] = {&prep.slot_nx, &prep.slot_ny, &prep.slot_len,
+                                          &prep.inv_area};
     for (int k = 0; k < 4; ++k) {
       st = s->prec == 32 ? put_as<float>(dsts[k], *srcs[k]) : put_as<double>(dsts[k], *srcs[k]);
       if (st != SWE_OK) return fail(st);
@@ -886,7 +903,7 @@ swe_status swe_create_mesh(const swe_mesh* mesh, const void* H, const void* cons
 }
 
 swe_status swe_mesh_info(const swe_mesh* mesh, int32_t* new_of_old, int64_t* n_edges,
-                         int64_t* bandwidth) {
+                         int64_t* n_tiles, int64_t* n_edge_evals, int64_t* n_halo) {
   if (!mesh || !mesh->xy || !mesh->tri || mesh->n_vertices < 3 || mesh->n_cells < 1)
     return SWE_ERR_ARG;
   if (mesh->n_vertices > INT32_MAX || mesh->n_cells > kMaxMeshCells) return SWE_ERR_ARG;
@@ -895,16 +912,14 @@ swe_status swe_mesh_info(const swe_mesh* mesh, int32_t* new_of_old, int64_t* n_e
   const int rc = prepare_mesh(mesh->n_vertices, mesh->xy, mesh->n_cells, mesh->tri,
                               mesh->reorder == 1, &prep);
   if (rc == -3) return SWE_ERR_OOM;
+  if (rc == -2) return SWE_ERR_UNSUPPORTED;
   if (rc != 0) return SWE_ERR_ARG;
   if (new_of_old)
     memcpy(new_of_old, prep.new_of_old.data(), (size_t)prep.ncells * sizeof(int32_t));
   if (n_edges) *n_edges = prep.nedges;
-  if (bandwidth) {
-    int64_t bw = 0;
-    for (int64_t e = 0; e < prep.nedges; ++e)
-      if (prep.eb[e] >= 0 && prep.eb[e] - prep.ea[e] > bw) bw = prep.eb[e] - prep.ea[e];
-    *bandwidth = bw;
-  }
+  if (n_tiles) *n_tiles = prep.ntiles;
+  if (n_edge_evals) *n_edge_evals = prep.edge_evals;
+  if (n_halo) *n_halo = (int64_t)prep.halo.size();
   return SWE_OK;
 }
 
@@ -1093,6 +1108,9 @@ swe_status swe_get_info(const swe_state* s, swe_info* info) {
     info->n_cells = s->ncells;
     info->n_edges = s->nedges;
     info->mesh = 1;
+    info->bands = (int32_t)s->ntiles;
+    info->segments = s->mesh_grid;
+    info->warps_per_block = mesh_tile_warps(s->prec, s->nl, s->p.entropy_fix);
   } else {
     info->n_cells = (int64_t)s->nx * s->ny;
     info->n_edges = (int64_t)(s->nx + 1) * s->ny + (int64_t)s->nx * (s->ny + 1);

@@ -150,15 +150,26 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
                           cudaStream_t st);
 
 // ---- triangle meshes (swe_mesh.cu, swe_mesh_prep.cpp) ------------------------
-// A mesh state keeps its cells in an internal order (reverse Cuthill-McKee
-// unless the caller asked for its own), one contiguous array per field.
-// Every edge is stored once: cells a < b (b = -1 on a wall), the unit normal
-// (nx, ny) pointing from a to b and the length L.  Each cell lists its three
-// edges as ref = 2 * edge + side (side 0: the cell is a, 1: it is b), in the
-// order of its vertices (edge k joins vertex k and vertex k + 1).
+// A mesh state keeps its cells in an internal order (the Hilbert curve through
+// the cell centroids unless the caller asked for its own), one contiguous
+// array per field, and cuts that order into tiles: consecutive cells, each
+// tile with at most kTileSlots edge slots, at most kTileHalo halo cells and
+// at most kTileCap cells plus halo cells.  A tile's edge slots are the edges with at least one cell in
+// the tile: an edge inside a tile has one slot, an edge between two tiles
+// one slot in each (the two evaluate it identically).  Every edge keeps one
+// orientation: cells a < b (b a wall on the mesh boundary) and the unit
+// normal (nx, ny) pointing from a to b, length L.
 //
-// The edge pass writes per edge, already multiplied by L and rotated back to
-// x / y components, what each side adds to its residual:
+// Per slot (tile-major, each tile's range starts at an even index):
+//   slot_ab  tile-local index of a | tile-local index of b << 16 (0xffff: wall);
+//            local indices 0 .. nct-1 are the tile's cells, nct .. the halo
+//   slot_nx, slot_ny, slot_len
+// Per cell: cref = its three edges in the order of its vertices (edge k
+// joins vertex k and vertex k + 1) as slot | side << 15 (side 1: the cell
+// is b), packed 16 bits each into (x: edges 0, 1; y: edge 2).
+//
+// In shared memory the tile kernel keeps, per slot, what each side adds to
+// its residual, already multiplied by L and rotated back to x / y:
 //   two layers  [0] m1  [1] m2           mass fluxes a -> b (a adds, b subtracts)
 //               [2..5] a: (x, y) momentum of layer 1, then of layer 2
 //               [6..9] b: the same for b
@@ -166,6 +177,10 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
 //   one layer   [0] m  [1] m C_upwind    mass and pollutant fluxes a -> b
 //               [2, 3] a: (x, y) momentum   [4, 5] b: (x, y) momentum
 //               [6] L * max |lambda|
+constexpr int kTileSlots = 512;
+constexpr int kTileCap = 640;
+constexpr int kTileHalo = 256;
+constexpr int kTileWall = 0xffff;
 template <int NL> struct MeshLayout;
 template <> struct MeshLayout<1> {
   static constexpr int nf = 4, ne = 7, a_mom = 2, b_mom = 4, d = 6;
@@ -176,23 +191,25 @@ template <> struct MeshLayout<2> {
 
 template <typename T>
 struct MeshStepArgs {
-  const T* w[6];          // state, internal cell order
+  const T* w[6];              // state, internal cell order
   const T* H;
-  T* R[6];                // residual / area (scratch)
-  const int32_t* ea;      // edge -> cell a
-  const int32_t* eb;      // edge -> cell b, or -1 (wall)
-  const T* enx;           // unit normal from a to b
-  const T* eny;
-  const T* elen;          // edge length
-  T* ebuf;                // per-edge results: field q of edge e at q * estride + e
-  int64_t estride;
-  const int32_t* ref[3];  // per cell: 2 * edge + side
-  const T* inv_area;      // 1 / |V_i|
-  int64_t ncells, nedges;
+  T* R[6];                    // residual / area (scratch)
+  const int32_t* tile_cell;   // [ntiles + 1]: first cell of each tile
+  const int32_t* tile_halo;   // [ntiles + 1]: first entry of each tile in halo
+  const int32_t* tile_slot;   // [ntiles + 1]: first slot of each tile
+  const int32_t* halo;        // halo cells (internal index), tile by tile
+  const int32_t* slot_ab;
+  const T* slot_nx;           // unit normal from a to b
+  const T* slot_ny;
+  const T* slot_len;          // edge length
+  const uint2* cref;          // [ncells]
+  const T* inv_area;          // 1 / |V_i|
+  int64_t ncells, ntiles;
+  int grid;                   // blocks of the tile kernel (mesh_prepare)
   T g, r;
-  void* tmax_out;         // max over cells of sum L max|lambda| / |V_i| (starts at 0)
+  void* tmax_out;             // max over cells of sum L max|lambda| / |V_i| (starts at 0)
   unsigned* err;
-  int efix;               // 1: the Harten-Hyman entropy fix
+  int efix;                   // 1: the Harten-Hyman entropy fix
 };
 template <typename T>
 struct MeshUpdateArgs {
@@ -208,6 +225,21 @@ struct MeshUpdateArgs {
   unsigned* err;
 };
 
+// Dynamic shared memory of the tile kernel: staged cells (nf fields and H)
+// and the per-slot results.
+template <typename T>
+constexpr size_t mesh_tile_smem(int n_layers) {
+  return (size_t)((n_layers == 2 ? 7 : 5) * kTileCap + (n_layers == 2 ? 11 : 7) * kTileSlots) *
+         sizeof(T);
+}
+// Sets the shared-memory limit of the tile kernel a mesh state of this
+// kind runs on the current device and returns its grid: in fp32 the
+// persistent form, one block per resident slot (at most ntiles); in fp64
+// one block per tile.
+template <typename T>
+cudaError_t mesh_prepare(int n_layers, int efix, int64_t ntiles, int* grid);
+// warps per block of that tile kernel
+int mesh_tile_warps(int precision, int n_layers, int efix);
 template <typename T>
 cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& u, int n_layers,
                              cudaStream_t st, const cudaEvent_t* marks = nullptr);
@@ -220,19 +252,27 @@ cudaError_t launch_mesh_permute(T* const* dst, const T* const* src, int nf, cons
                                 int64_t n, cudaStream_t st);
 
 // Host preparation of a triangle mesh (swe_mesh_prep.cpp): geometry in
-// double precision, edges, cell order and the per-cell edge references.
+// double precision, edges, cell order, tiles and the per-cell slot references.
 struct MeshPrep {
-  int64_t ncells = 0, nedges = 0;
-  std::vector<int32_t> ea, eb;            // [nedges]
+  int64_t ncells = 0, nedges = 0, ntiles = 0;
+  std::vector<int32_t> ea, eb;            // [nedges], internal order, a < b (b = -1: wall)
   std::vector<double> enx, eny, elen;     // [nedges]
-  std::vector<int32_t> ref;               // [3 * ncells]: ref k of cell c at k * ncells + c
+  std::vector<int32_t> ref;               // [3 * ncells]: 2 * edge + side of edge k of cell c at k * ncells + c
   std::vector<double> inv_area;           // [ncells], internal order
   std::vector<int32_t> new_of_old;        // caller cell -> internal cell
   std::vector<int32_t> old_of_new;        // internal cell -> caller cell
+  std::vector<int32_t> tile_cell, tile_halo, tile_slot;  // [ntiles + 1]
+  std::vector<int32_t> halo;
+  std::vector<int32_t> slot_ab;
+  std::vector<double> slot_nx, slot_ny, slot_len;
+  std::vector<uint32_t> cref;             // [2 * ncells]
+  int64_t edge_evals = 0;                 // slots without the even padding
 };
 // 0 on success; -1 for an invalid mesh (index out of range, non-finite
 // coordinate, clockwise or degenerate triangle, an edge used by more than two
-// triangles or twice in the same direction); -3 when host memory runs out.
+// triangles or twice in the same direction); -2 if the tiles failed their
+// consistency check (not expected for any valid mesh); -3 when host memory
+// runs out.
 int prepare_mesh(int64_t n_vertices, const double* xy, int64_t n_cells, const int32_t* tri,
                  bool reorder, MeshPrep* out);
 

@@ -9,14 +9,17 @@
 // carries the pollutant of A multi-GPU shallow-water simulation with
 // transport of contaminants (abstract: a transport equation for hC).
 //
-// Three launches per step, no floating-point atomics on results:
-//   mesh_edge_kernel    one thread per edge: the rotated Roe flux of the edge
-//                       (eq. (2)-(3)), evaluated once for both of its cells;
-//                       writes what each side adds to its residual;
-//   mesh_gather_kernel  one thread per cell: sums its three edge records in
-//                       a fixed order (a CSR gather), stores R / |V_i| and
-//                       max-reduces sum L max|lambda| / |V_i| for dt;
+// Two launches per step, no floating-point atomics on results:
+//   mesh_tile_kernel    one block per tile of consecutive cells (compact
+//                       patches, swe_mesh_prep.cpp): stages the tile's cells
+//                       and halo in shared memory, evaluates the rotated Roe
+//                       flux of every edge of the tile once (eq. (2)-(3)),
+//                       then sums each cell's three edges in a fixed order,
+//                       stores R / |V_i| and max-reduces
+//                       sum L max|lambda| / |V_i| for dt;
 //   mesh_update_kernel  W -= dt R / |V_i| in place, checks, dt bookkeeping.
+// Algorithm 1's edge and volume loops thus meet in shared memory; the
+// per-edge results never travel through DRAM.
 //
 // Momentum enters in fluctuation form: each side keeps only P^- d (side a)
 // or P^+ d (side b) of the normal component and the tangential transport
@@ -35,9 +38,6 @@
 
 namespace swe {
 namespace {
-
-constexpr int kEdgeThreads = 256;
-constexpr int kCellThreads = 256;
 
 // ---- one layer ----------------------------------------------------------------
 template <typename T>
@@ -105,218 +105,447 @@ __device__ __forceinline__ void edge1(const Side1<T>& a, const Side1<T>& b, T gh
   D = fmax(fabs(l1), fabs(l2));
 }
 
+// ---- the tile kernel -------------------------------------------------------
+// One block per tile (see swe_internal.h):
+//   1. the tile's cells and its halo cells (W^n and H) into shared memory;
+//   2. every slot of the tile: the Roe flux of the edge from the staged
+//      cells, written per slot to shared memory, what each side adds;
+//   3. every cell of the tile: its three slots summed as e0 + (e1 + e2), the
+//      residual R / |V_i| stored, and sum L max|lambda| / |V_i| max-reduced
+//      for dt.
+// An edge on a tile border is evaluated by both tiles from the same inputs,
+// so both sides see the same flux and mass and pollutant stay conserved.
+template <typename T, int NL, bool EFIX> struct TileThreads {
+  static constexpr int v = (NL == 2 && EFIX) ? 128 : 256;
+};
+
+// staged cells: field f of local cell i at cw[f * kTileCap + i] (H last)
 template <typename T>
-__device__ __forceinline__ Side1<T> load_side1(const MeshStepArgs<T>& A, int32_t c, T ex, T ey) {
+__device__ __forceinline__ Side1<T> side1_of(const T* cw, int i, T ex, T ey) {
   Side1<T> s;
-  const T h = A.w[0][c], qx = A.w[1][c], qy = A.w[2][c];
+  const T h = cw[i], qx = cw[kTileCap + i], qy = cw[2 * kTileCap + i];
   s.h = h;
   s.rs = M2<T>::rsq(h);
   s.s = h * s.rs;
   s.qn = qx * ex + qy * ey;
   s.qt = -qx * ey + qy * ex;
-  s.hc = A.w[3][c];
-  s.H = A.H[c];
+  s.hc = cw[3 * kTileCap + i];
+  s.H = cw[4 * kTileCap + i];
   return s;
 }
 
 template <typename T>
-__device__ __forceinline__ Side2<T> load_side2(const MeshStepArgs<T>& A, int32_t c, T ex, T ey) {
+__device__ __forceinline__ Side2<T> side2_of(const T* cw, int i, T ex, T ey) {
   Side2<T> s;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    const T h = A.w[3 * k][c], qx = A.w[3 * k + 1][c], qy = A.w[3 * k + 2][c];
+    const T h = cw[3 * k * kTileCap + i], qx = cw[(3 * k + 1) * kTileCap + i];
+    const T qy = cw[(3 * k + 2) * kTileCap + i];
     s.h[k] = h;
     s.rs[k] = M2<T>::rsq(h);
     s.s[k] = h * s.rs[k];
     s.qn[k] = qx * ex + qy * ey;
     s.qt[k] = -qx * ey + qy * ex;
   }
-  s.H = A.H[c];
+  s.H = cw[6 * kTileCap + i];
   return s;
 }
 
-// (normal, tangential) components in the edge frame -> (x, y), times L
+// (normal, tangential) components in the edge frame -> (x, y), times L, into
+// result q of slot j
 template <typename T>
-__device__ __forceinline__ void put_xy(T* buf, int64_t st, int64_t e, int q, T L, T fn, T ft,
-                                       T ex, T ey) {
-  buf[q * st + e] = L * (fn * ex - ft * ey);
-  buf[(q + 1) * st + e] = L * (fn * ey + ft * ex);
+__device__ __forceinline__ void put_xy(T* er, int j, int q, T L, T fn, T ft, T ex, T ey) {
+  er[q * kTileSlots + j] = L * (fn * ex - ft * ey);
+  er[(q + 1) * kTileSlots + j] = L * (fn * ey + ft * ex);
 }
 
-template <typename T, int NL, bool EFIX = false>
-__global__ void __launch_bounds__(kEdgeThreads) mesh_edge_kernel(const MeshStepArgs<T> A) {
+// One slot: the edge's flux from the staged cells into er.  Returns false
+// when a two-layer Roe matrix has a complex pair of eigenvalues.
+template <typename T>
+struct Slot {
+  int32_t ab;
+  T ex, ey, L;
+};
+template <typename T>
+__device__ __forceinline__ Slot<T> load_slot(const MeshStepArgs<T>& A, int64_t gs) {
+  return Slot<T>{A.slot_ab[gs], A.slot_nx[gs], A.slot_ny[gs], A.slot_len[gs]};
+}
+
+template <typename T, int NL, bool EFIX>
+__device__ __forceinline__ bool tile_edge(const MeshStepArgs<T>& A, const T* cw, T* er, int j,
+                                          const Slot<T>& sl) {
   using Lay = MeshLayout<NL>;
-  const int64_t e = (int64_t)blockIdx.x * kEdgeThreads + threadIdx.x;
-  bool ok = true;
-  pdl_wait();
-  if (e < A.nedges) {
-    const int32_t a = A.ea[e], b = A.eb[e];
-    const T ex = A.enx[e], ey = A.eny[e], L = A.elen[e];
-    const bool wall = b < 0;
-    const T gh = T(0.5) * A.g;
-    T* buf = A.ebuf;
-    const int64_t st = A.estride;
-    if constexpr (NL == 1) {
-      const Side1<T> sa = load_side1(A, a, ex, ey);
-      Side1<T> sb = sa;  // wall: mirror ghost (normal discharge negated)
-      if (wall) sb.qn = -sa.qn;
-      else sb = load_side1(A, b, ex, ey);
-      T m, p, pa, pb, t, D;
-      edge1<T, EFIX>(sa, sb, gh, wall, m, p, pa, pb, t, D);
-      buf[0 * st + e] = L * m;
-      buf[1 * st + e] = L * p;
-      const T ta = t - sa.qn * (sa.qt * sa.rs * sa.rs);
-      put_xy(buf, st, e, Lay::a_mom, L, pa, ta, ex, ey);
-      if (!wall) {
-        const T tb = sb.qn * (sb.qt * sb.rs * sb.rs) - t;
-        put_xy(buf, st, e, Lay::b_mom, L, pb, tb, ex, ey);
-      }
-      buf[Lay::d * st + e] = L * D;
-    } else {
-      const Side2<T> sa = load_side2(A, a, ex, ey);
-      Side2<T> sb;
-      if (wall) mirror2(sb, sa);
-      else sb = load_side2(A, b, ex, ey);
-      T out[NEQ];
-      ok = edge2<T, true, EFIX>(sa, sb, A.g, gh, A.r, wall, out);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const T m = out[k ? E_M2 : E_M1];
-        const T t = out[k ? E_T2 : E_T1];
-        buf[k * st + e] = L * m;
-        const T ta = t - sa.qn[k] * (sa.qt[k] * sa.rs[k] * sa.rs[k]);
-        put_xy(buf, st, e, Lay::a_mom + 2 * k, L, out[k ? E_PM2 : E_PM1], ta, ex, ey);
-        if (!wall) {
-          const T tb = sb.qn[k] * (sb.qt[k] * sb.rs[k] * sb.rs[k]) - t;
-          put_xy(buf, st, e, Lay::b_mom + 2 * k, L, out[k ? E_PS2 : E_PS1], tb, ex, ey);
-        }
-      }
-      buf[Lay::d * st + e] = L * out[E_D];
+  const int la = sl.ab & 0xffff, lb = (sl.ab >> 16) & 0xffff;
+  const T ex = sl.ex, ey = sl.ey, L = sl.L;
+  const bool wall = lb == kTileWall;
+  const T gh = T(0.5) * A.g;
+  if constexpr (NL == 1) {
+    const Side1<T> sa = side1_of(cw, la, ex, ey);
+    Side1<T> sb = sa;  // wall: mirror ghost (normal discharge negated)
+    if (wall) sb.qn = -sa.qn;
+    else sb = side1_of(cw, lb, ex, ey);
+    T m, p, pa, pb, t, D;
+    edge1<T, EFIX>(sa, sb, gh, wall, m, p, pa, pb, t, D);
+    er[0 * kTileSlots + j] = L * m;
+    er[1 * kTileSlots + j] = L * p;
+    const T ta = t - sa.qn * (sa.qt * sa.rs * sa.rs);
+    put_xy(er, j, Lay::a_mom, L, pa, ta, ex, ey);
+    if (!wall) {
+      const T tb = sb.qn * (sb.qt * sb.rs * sb.rs) - t;
+      put_xy(er, j, Lay::b_mom, L, pb, tb, ex, ey);
     }
+    er[Lay::d * kTileSlots + j] = L * D;
+    return true;
+  } else {
+    const Side2<T> sa = side2_of(cw, la, ex, ey);
+    Side2<T> sb;
+    if (wall) mirror2(sb, sa);
+    else sb = side2_of(cw, lb, ex, ey);
+    T out[NEQ];
+    const bool ok = edge2<T, true, EFIX>(sa, sb, A.g, gh, A.r, wall, out);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const T m = out[k ? E_M2 : E_M1];
+      const T t = out[k ? E_T2 : E_T1];
+      er[k * kTileSlots + j] = L * m;
+      const T ta = t - sa.qn[k] * (sa.qt[k] * sa.rs[k] * sa.rs[k]);
+      put_xy(er, j, Lay::a_mom + 2 * k, L, out[k ? E_PM2 : E_PM1], ta, ex, ey);
+      if (!wall) {
+        const T tb = sb.qn[k] * (sb.qt[k] * sb.rs[k] * sb.rs[k]) - t;
+        put_xy(er, j, Lay::b_mom + 2 * k, L, out[k ? E_PS2 : E_PS1], tb, ex, ey);
+      }
+    }
+    er[Lay::d * kTileSlots + j] = L * out[E_D];
+    return ok;
   }
-  pdl_trigger();
-  if (NL == 2 && !__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
 }
 
-// ---- two layers, fp32: two edges per thread on the packed FP32x2 pipe -------
-// (edge2p and its FP32x2 helpers are in swe_roe2.cuh)
-
-__device__ __forceinline__ void load_side2p(const MeshStepArgs<float>& A, int32_t c0, int32_t c1,
-                                            float2 ex, float2 ey, Side2P& s) {
+// Two layers, fp32: slots j and j + 1 on the packed FP32x2 pipe (edge2p).
+// Every tile's slot range starts at an even index and has even length.
+__device__ __forceinline__ void side2p_of(const float* cw, int i0, int i1, float2 ex, float2 ey,
+                                          Side2P& s) {
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    const float2 h = f2(A.w[3 * k][c0], A.w[3 * k][c1]);
-    const float2 qx = f2(A.w[3 * k + 1][c0], A.w[3 * k + 1][c1]);
-    const float2 qy = f2(A.w[3 * k + 2][c0], A.w[3 * k + 2][c1]);
+    const float* f = cw + 3 * k * kTileCap;
+    const float2 h = f2(f[i0], f[i1]);
+    const float2 qx = f2(f[kTileCap + i0], f[kTileCap + i1]);
+    const float2 qy = f2(f[2 * kTileCap + i0], f[2 * kTileCap + i1]);
     s.h[k] = h;
     s.rs[k] = rsq2(h);
     s.s[k] = mul2(h, s.rs[k]);
     s.qn[k] = fma2(qx, ex, mul2(qy, ey));
     s.qt[k] = fma2(qy, ex, f2(-(qx.x * ey.x), -(qx.y * ey.y)));
   }
-  s.H = f2(A.H[c0], A.H[c1]);
+  s.H = f2(cw[6 * kTileCap + i0], cw[6 * kTileCap + i1]);
 }
 
-// Two layers, fp32: edges 2t and 2t + 1.  Every edge array is 256-byte
-// aligned with room for one element past an odd count, so the pair loads
-// and stores stay inside the allocation; the missing second edge of an odd
-// count takes the first edge's data and its results land in that padding.
-constexpr int kPairThreads = 128;
-// Blocks per SM the registers are held to: six (80 registers) leave the
-// per-edge convergence state unspilled; seven spilled 32 bytes and ran 2 %
-// slower on the 2.1M-triangle two-layer mesh.
-#ifndef SWE_PAIR_MIN_BLOCKS
-#define SWE_PAIR_MIN_BLOCKS 6
-#endif
-__global__ void __launch_bounds__(kPairThreads, SWE_PAIR_MIN_BLOCKS)
-    mesh_edge2_pair_kernel(const MeshStepArgs<float> A) {
-  const int64_t e0 = 2 * ((int64_t)blockIdx.x * kPairThreads + threadIdx.x);
-  bool ok = true;
-  pdl_wait();
-  if (e0 < A.nedges) {
-    const bool both = e0 + 1 < A.nedges;
-    int2 ia = *reinterpret_cast<const int2*>(A.ea + e0);
-    int2 ib = *reinterpret_cast<const int2*>(A.eb + e0);
-    float2 ex = *reinterpret_cast<const float2*>(A.enx + e0);
-    float2 ey = *reinterpret_cast<const float2*>(A.eny + e0);
-    float2 L = *reinterpret_cast<const float2*>(A.elen + e0);
-    if (!both) {
-      ia.y = ia.x; ib.y = ib.x; ex.y = ex.x; ey.y = ey.x; L.y = L.x;
-    }
-    const bool w0 = ib.x < 0, w1 = ib.y < 0;
-    Side2P sa, sb;
-    load_side2p(A, ia.x, ia.y, ex, ey, sa);
-    load_side2p(A, w0 ? ia.x : ib.x, w1 ? ia.y : ib.y, ex, ey, sb);
-    // walls: the mirror ghost has the normal discharge negated
-    if (w0) { sb.qn[0].x = -sa.qn[0].x; sb.qn[1].x = -sa.qn[1].x; }
-    if (w1) { sb.qn[0].y = -sa.qn[0].y; sb.qn[1].y = -sa.qn[1].y; }
-    float2 out[NEQ];
-    ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out) == 3u;
-    float* buf = A.ebuf;
-    const int64_t st = A.estride;
-    auto put = [&](int q, float2 v) { *reinterpret_cast<float2*>(buf + q * st + e0) = v; };
-    using Lay = MeshLayout<2>;
+struct SlotPair {
+  int2 ab;
+  float2 ex, ey, L;
+};
+__device__ __forceinline__ SlotPair load_slot_pair(const MeshStepArgs<float>& A, int64_t gs) {
+  return SlotPair{*reinterpret_cast<const int2*>(A.slot_ab + gs),
+                  *reinterpret_cast<const float2*>(A.slot_nx + gs),
+                  *reinterpret_cast<const float2*>(A.slot_ny + gs),
+                  *reinterpret_cast<const float2*>(A.slot_len + gs)};
+}
+
+__device__ __forceinline__ bool tile_edge_pair(const MeshStepArgs<float>& A, const float* cw,
+                                               float* er, int j, const SlotPair& sp) {
+  const int2 ab = sp.ab;
+  const float2 ex = sp.ex, ey = sp.ey, L = sp.L;
+  const int la0 = ab.x & 0xffff, lb0 = (ab.x >> 16) & 0xffff;
+  const int la1 = ab.y & 0xffff, lb1 = (ab.y >> 16) & 0xffff;
+  const bool w0 = lb0 == kTileWall, w1 = lb1 == kTileWall;
+  Side2P sa, sb;
+  side2p_of(cw, la0, la1, ex, ey, sa);
+  side2p_of(cw, w0 ? la0 : lb0, w1 ? la1 : lb1, ex, ey, sb);
+  // walls: the mirror ghost has the normal discharge negated
+  if (w0) { sb.qn[0].x = -sa.qn[0].x; sb.qn[1].x = -sa.qn[1].x; }
+  if (w1) { sb.qn[0].y = -sa.qn[0].y; sb.qn[1].y = -sa.qn[1].y; }
+  float2 out[NEQ];
+  const bool ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out) == 3u;
+  auto put = [&](int q, float2 v) { *reinterpret_cast<float2*>(er + q * kTileSlots + j) = v; };
+  using Lay = MeshLayout<2>;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 m = out[k ? E_M2 : E_M1];
-      const float2 t = out[k ? E_T2 : E_T1];
-      put(k, mul2(L, m));
-      const float2 ta = sub2(t, mul2(sa.qn[k], mul2(sa.qt[k], mul2(sa.rs[k], sa.rs[k]))));
-      const float2 tb = sub2(mul2(sb.qn[k], mul2(sb.qt[k], mul2(sb.rs[k], sb.rs[k]))), t);
-      const float2 pa = out[k ? E_PM2 : E_PM1], pb = out[k ? E_PS2 : E_PS1];
-      // (normal, tangential) -> (x, y), times L
-      put(Lay::a_mom + 2 * k, mul2(L, fma2(pa, ex, f2(-(ta.x * ey.x), -(ta.y * ey.y)))));
-      put(Lay::a_mom + 2 * k + 1, mul2(L, fma2(pa, ey, mul2(ta, ex))));
-      put(Lay::b_mom + 2 * k, mul2(L, fma2(pb, ex, f2(-(tb.x * ey.x), -(tb.y * ey.y)))));
-      put(Lay::b_mom + 2 * k + 1, mul2(L, fma2(pb, ey, mul2(tb, ex))));
-    }
-    put(Lay::d, mul2(L, out[E_D]));
+  for (int k = 0; k < 2; ++k) {
+    const float2 m = out[k ? E_M2 : E_M1];
+    const float2 t = out[k ? E_T2 : E_T1];
+    put(k, mul2(L, m));
+    const float2 ta = sub2(t, mul2(sa.qn[k], mul2(sa.qt[k], mul2(sa.rs[k], sa.rs[k]))));
+    const float2 tb = sub2(mul2(sb.qn[k], mul2(sb.qt[k], mul2(sb.rs[k], sb.rs[k]))), t);
+    const float2 pa = out[k ? E_PM2 : E_PM1], pb = out[k ? E_PS2 : E_PS1];
+    // (normal, tangential) -> (x, y), times L
+    put(Lay::a_mom + 2 * k, mul2(L, fma2(pa, ex, f2(-(ta.x * ey.x), -(ta.y * ey.y)))));
+    put(Lay::a_mom + 2 * k + 1, mul2(L, fma2(pa, ey, mul2(ta, ex))));
+    put(Lay::b_mom + 2 * k, mul2(L, fma2(pb, ex, f2(-(tb.x * ey.x), -(tb.y * ey.y)))));
+    put(Lay::b_mom + 2 * k + 1, mul2(L, fma2(pb, ey, mul2(tb, ex))));
   }
-  pdl_trigger();
-  if (!__all_sync(kFull2, ok) && (threadIdx.x & 31) == 0) atomicOr(A.err, kErrHyperbolic);
+  put(Lay::d, mul2(L, out[E_D]));
+  return ok;
 }
 
-// residual of one cell: its three edges, summed as e0 + (e1 + e2)
+// Residual of cell c from its three slots, summed as e0 + (e1 + e2): stores
+// R / |V_c| and returns sum L max|lambda| / |V_c|.
 template <typename T, int NL>
-__global__ void __launch_bounds__(kCellThreads) mesh_gather_kernel(const MeshStepArgs<T> A) {
+__device__ __forceinline__ T cell_residual(const MeshStepArgs<T>& A, const T* er, int64_t c,
+                                           uint2 cr, T ia) {
   using Lay = MeshLayout<NL>;
   constexpr int NF = Lay::nf;
-  const int64_t c = (int64_t)blockIdx.x * kCellThreads + threadIdx.x;
-  T m = T(0);
-  pdl_wait();
-  if (c < A.ncells) {
-    const T* buf = A.ebuf;
-    const int64_t st = A.estride;
-    T v[3][NF], d[3];
+  const uint32_t rk[3] = {cr.x & 0xffffu, cr.x >> 16, cr.y & 0xffffu};
+  T v[3][NF], d[3];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const int32_t ref = A.ref[k][c];
-      const int64_t e = ref >> 1;
-      const bool bside = ref & 1;
-      const int q = bside ? Lay::b_mom : Lay::a_mom;
-      const T s = bside ? T(-1) : T(1);
-      if constexpr (NL == 1) {
-        v[k][0] = s * buf[0 * st + e];
-        v[k][1] = buf[q * st + e];
-        v[k][2] = buf[(q + 1) * st + e];
-        v[k][3] = s * buf[1 * st + e];
-      } else {
-        v[k][0] = s * buf[0 * st + e];
-        v[k][1] = buf[q * st + e];
-        v[k][2] = buf[(q + 1) * st + e];
-        v[k][3] = s * buf[1 * st + e];
-        v[k][4] = buf[(q + 2) * st + e];
-        v[k][5] = buf[(q + 3) * st + e];
-      }
-      d[k] = buf[Lay::d * st + e];
+  for (int k = 0; k < 3; ++k) {
+    const int j = (int)(rk[k] & 0x7fffu);
+    const bool bside = (rk[k] >> 15) != 0;
+    const int q = bside ? Lay::b_mom : Lay::a_mom;
+    const T sg = bside ? T(-1) : T(1);
+    v[k][0] = sg * er[0 * kTileSlots + j];
+    v[k][1] = er[q * kTileSlots + j];
+    v[k][2] = er[(q + 1) * kTileSlots + j];
+    v[k][3] = sg * er[1 * kTileSlots + j];
+    if constexpr (NL == 2) {
+      v[k][4] = er[(q + 2) * kTileSlots + j];
+      v[k][5] = er[(q + 3) * kTileSlots + j];
     }
-    const T ia = A.inv_area[c];
+    d[k] = er[Lay::d * kTileSlots + j];
+  }
 #pragma unroll
-    for (int f = 0; f < NF; ++f) A.R[f][c] = (v[0][f] + (v[1][f] + v[2][f])) * ia;
-    m = (d[0] + (d[1] + d[2])) * ia;
+  for (int f = 0; f < NF; ++f) A.R[f][c] = (v[0][f] + (v[1][f] + v[2][f])) * ia;
+  return (d[0] + (d[1] + d[2])) * ia;
+}
+
+// One tile per block (the fp64 form: bound by the FP64 pipe, not by the
+// latency of its loads).
+template <typename T, int NL, bool EFIX, bool PAIR>
+__global__ void __launch_bounds__((TileThreads<T, NL, EFIX>::v))
+    mesh_tile_kernel(const MeshStepArgs<T> A) {
+  using Lay = MeshLayout<NL>;
+  constexpr int NF = Lay::nf;
+  constexpr int NT = TileThreads<T, NL, EFIX>::v;
+  extern __shared__ __align__(16) unsigned char tile_smem[];
+  T* cw = reinterpret_cast<T*>(tile_smem);
+  T* er = cw + (NF + 1) * kTileCap;
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int32_t c0 = A.tile_cell[t], nct = A.tile_cell[t + 1] - c0;
+  const int32_t h0 = A.tile_halo[t], nh = A.tile_halo[t + 1] - h0;
+  const int32_t s0 = A.tile_slot[t], ns = A.tile_slot[t + 1] - s0;
+  pdl_wait();
+  // 1. cells, then halo
+  for (int i = tid; i < nct + nh; i += NT) {
+    const int32_t c = i < nct ? c0 + i : A.halo[h0 + i - nct];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) cw[f * kTileCap + i] = A.w[f][c];
+    cw[NF * kTileCap + i] = A.H[c];
+  }
+  __syncthreads();
+  // 2. slots
+  bool ok = true;
+  if constexpr (PAIR) {
+    for (int j = 2 * tid; j < ns; j += 2 * NT)
+      ok &= tile_edge_pair(A, cw, er, j, load_slot_pair(A, (int64_t)s0 + j));
+  } else {
+    for (int j = tid; j < ns; j += NT)
+      ok &= tile_edge<T, NL, EFIX>(A, cw, er, j, load_slot(A, (int64_t)s0 + j));
+  }
+  __syncthreads();
+  // 3. cells: residual and wave-speed sum
+  T m = T(0);
+  for (int i = tid; i < nct; i += NT)
+    m = nanmax2(m, cell_residual<T, NL>(A, er, c0 + i, A.cref[c0 + i], A.inv_area[c0 + i]));
+  pdl_trigger();
+  if (NL == 2 && !__syncthreads_and(ok) && tid == 0) atomicOr(A.err, kErrHyperbolic);
+  block_max_publish<T, NT / 32>(m, A.tmax_out);
+}
+
+// ---- fp32: the persistent, pipelined form of the tile kernel -----------------
+// The same three phases, but each block walks the tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... and, while it evaluates tile k, stages in
+// shared memory with cp.async: the cells and halo cells of tile k + 1 (into
+// the other of two buffers), the halo indices of tile k + 2 (which the
+// addresses of its halo cells need) and the header of tile k + 3 (which the
+// halo indices need).  The slot data of tile k + 1 is read into registers
+// after the edge phase of tile k.  All of it has the whole edge and cell
+// phases of a tile to land, so a block's loads overlap its own arithmetic;
+// with tiles of equal size the blocks of one SM would otherwise load, and
+// then compute, at the same time.
+constexpr int kPipeThreads = 256;
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// shared memory: two cell buffers (nf fields and H of the tile's cells and
+// halo), three halo-index buffers, the slot results.  Three blocks of the
+// two-layer form take at most 196 KB of shared memory, so the SM keeps the
+// larger of its L1 configurations for the few registers that spill.
+template <int NL>
+constexpr int pipe_cell_words() {
+  return (MeshLayout<NL>::nf + 1) * kTileCap;
+}
+template <int NL>
+constexpr size_t pipe_smem() {
+  return (size_t)(2 * pipe_cell_words<NL>() + 3 * kTileHalo + MeshLayout<NL>::ne * kTileSlots) *
+         sizeof(float);
+}
+
+struct TileHdr {
+  int32_t c0, nct, h0, nh, s0, ns;
+};
+// header entry: tile_cell, tile_halo and tile_slot at t and t + 1
+__device__ __forceinline__ void request_hdr(const MeshStepArgs<float>& A, int32_t* e, int t) {
+  const int i = threadIdx.x;
+  if (i < 6) {
+    const int32_t* src = i < 2 ? A.tile_cell : (i < 4 ? A.tile_halo : A.tile_slot);
+    cp_async4(e + i, src + t + (i & 1));
+  }
+}
+__device__ __forceinline__ TileHdr read_hdr(const int32_t* e) {
+  return TileHdr{e[0], e[1] - e[0], e[2], e[3] - e[2], e[4], e[5] - e[4]};
+}
+__device__ __forceinline__ void request_hidx(const MeshStepArgs<float>& A, int32_t* hidx,
+                                             const TileHdr& h) {
+  for (int k = threadIdx.x; k < h.nh; k += kPipeThreads) cp_async4(hidx + k, A.halo + h.h0 + k);
+}
+template <int NL>
+__device__ __forceinline__ void request_cells(const MeshStepArgs<float>& A, float* buf,
+                                              const int32_t* hidx, const TileHdr& h) {
+  constexpr int NF = MeshLayout<NL>::nf;
+  for (int i = threadIdx.x; i < h.nct + h.nh; i += kPipeThreads) {
+    const int64_t c = i < h.nct ? (int64_t)h.c0 + i : (int64_t)hidx[i - h.nct];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) cp_async4(buf + f * kTileCap + i, A.w[f] + c);
+    cp_async4(buf + NF * kTileCap + i, A.H + c);
+  }
+}
+
+// slot data of one tile in registers: a pair per thread (PAIR), else
+// kTileSlots / kPipeThreads single slots
+constexpr int kPipeSlots = kTileSlots / kPipeThreads;
+template <bool PAIR> struct PipeSlots {
+  Slot<float> s[kPipeSlots];
+};
+template <> struct PipeSlots<true> {
+  SlotPair p;
+};
+template <bool PAIR>
+__device__ __forceinline__ void load_slots(const MeshStepArgs<float>& A, const TileHdr& h,
+                                           PipeSlots<PAIR>& r) {
+  if constexpr (PAIR) {
+    const int j = 2 * threadIdx.x;
+    if (j < h.ns) r.p = load_slot_pair(A, (int64_t)h.s0 + j);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPipeSlots; ++k) {
+      const int j = threadIdx.x + k * kPipeThreads;
+      if (j < h.ns) r.s[k] = load_slot(A, (int64_t)h.s0 + j);
+    }
+  }
+}
+
+constexpr int kPipeCells = (kTileCap + kPipeThreads - 1) / kPipeThreads;
+
+#ifndef SWE_PIPE_PAIR_MIN_BLOCKS
+#define SWE_PIPE_PAIR_MIN_BLOCKS 3
+#endif
+template <int NL, bool EFIX, bool PAIR> struct PipeMinBlocks { static constexpr int v = 2; };
+template <> struct PipeMinBlocks<2, false, true> { static constexpr int v = SWE_PIPE_PAIR_MIN_BLOCKS; };
+template <> struct PipeMinBlocks<1, false, false> { static constexpr int v = 4; };
+template <> struct PipeMinBlocks<1, true, false> { static constexpr int v = 4; };
+
+template <int NL, bool EFIX, bool PAIR>
+__global__ void __launch_bounds__(kPipeThreads, (PipeMinBlocks<NL, EFIX, PAIR>::v))
+    mesh_tile_pipe_kernel(const MeshStepArgs<float> A) {
+  extern __shared__ __align__(16) unsigned char tile_smem[];
+  __shared__ __align__(16) int32_t ring[4][8];
+  float* const cbuf = reinterpret_cast<float*>(tile_smem);
+  int32_t* const hbuf = reinterpret_cast<int32_t*>(cbuf + 2 * pipe_cell_words<NL>());
+  float* const er = reinterpret_cast<float*>(hbuf + 3 * kTileHalo);
+  const int G = gridDim.x, nt = (int)A.ntiles, tid = threadIdx.x;
+  const int t0 = blockIdx.x;  // < nt: the grid never exceeds the tile count
+  auto valid = [&](int k) { return t0 + k * G < nt; };
+  pdl_wait();
+  // prologue: headers of tiles 0-2 of this block, halo indices of tiles 0-1,
+  // cells of tile 0, slots of tile 0
+  for (int k = 0; k < 3; ++k)
+    if (valid(k)) request_hdr(A, ring[k], t0 + k * G);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  for (int k = 0; k < 2; ++k)
+    if (valid(k)) request_hidx(A, hbuf + k * kTileHalo, read_hdr(ring[k]));
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  request_cells<NL>(A, cbuf, hbuf, read_hdr(ring[0]));
+  cp_async_commit();
+  PipeSlots<PAIR> sl;
+  load_slots<PAIR>(A, read_hdr(ring[0]), sl);
+  cp_async_wait_all();
+  __syncthreads();
+  bool ok = true;
+  float m = 0.f;
+  for (int it = 0;; ++it) {
+    const int t = t0 + it * G;
+    const bool more = valid(it + 1);
+    const float* cw = cbuf + (it & 1) * pipe_cell_words<NL>();
+    const int32_t* hcur = ring[it & 3];
+    // staging ahead: header k + 3, halo indices k + 2, cells k + 1
+    if (valid(it + 3)) request_hdr(A, ring[(it + 3) & 3], t + 3 * G);
+    if (valid(it + 2)) request_hidx(A, hbuf + ((it + 2) % 3) * kTileHalo, read_hdr(ring[(it + 2) & 3]));
+    if (more)
+      request_cells<NL>(A, cbuf + ((it + 1) & 1) * pipe_cell_words<NL>(),
+                        hbuf + ((it + 1) % 3) * kTileHalo, read_hdr(ring[(it + 1) & 3]));
+    cp_async_commit();
+    // edges of this tile
+    {
+      const int ns = hcur[5] - hcur[4];
+      if constexpr (PAIR) {
+        if (2 * tid < ns) ok &= tile_edge_pair(A, cw, er, 2 * tid, sl.p);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kPipeSlots; ++k) {
+          const int j = tid + k * kPipeThreads;
+          if (j < ns) ok &= tile_edge<float, NL, EFIX>(A, cw, er, j, sl.s[k]);
+        }
+      }
+    }
+    // the next tile's slots; this tile's cell references and areas
+    if (more) load_slots<PAIR>(A, read_hdr(ring[(it + 1) & 3]), sl);
+    const int c0 = hcur[0], nct = hcur[1] - hcur[0];
+    uint2 cr[kPipeCells];
+    float ia[kPipeCells];
+#pragma unroll
+    for (int k = 0; k < kPipeCells; ++k) {
+      const int i = tid + k * kPipeThreads;
+      if (i < nct) {
+        cr[k] = A.cref[(int64_t)c0 + i];
+        ia[k] = A.inv_area[(int64_t)c0 + i];
+      }
+    }
+    __syncthreads();  // slot results complete
+    // cells of this tile
+#pragma unroll
+    for (int k = 0; k < kPipeCells; ++k) {
+      const int i = tid + k * kPipeThreads;
+      if (i < nct) m = nanmax2(m, cell_residual<float, NL>(A, er, (int64_t)c0 + i, cr[k], ia[k]));
+    }
+    cp_async_wait_all();
+    __syncthreads();  // what was staged landed; slot results free
+    if (!more) break;
   }
   pdl_trigger();
-  block_max_publish<T, kCellThreads / 32>(m, A.tmax_out);
+  if (NL == 2 && !__syncthreads_and(ok) && tid == 0) atomicOr(A.err, kErrHyperbolic);
+  block_max_publish<float, kPipeThreads / 32>(m, A.tmax_out);
 }
 
 // Vector width of the update: 16-byte loads and stores.
@@ -430,44 +659,111 @@ unsigned grid_1d(int64_t n, int threads, int64_t cap) {
   return (unsigned)b;
 }
 
+template <typename T, int NL, bool EFIX, bool PAIR>
+cudaError_t tile_attr() {
+  return cudaFuncSetAttribute(mesh_tile_kernel<T, NL, EFIX, PAIR>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)mesh_tile_smem<T>(NL));
+}
+template <int NL, bool EFIX, bool PAIR>
+cudaError_t pipe_attr() {
+  return cudaFuncSetAttribute(mesh_tile_pipe_kernel<NL, EFIX, PAIR>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe_smem<NL>());
+}
+template <int NL, bool EFIX, bool PAIR>
+cudaError_t pipe_grid(int64_t ntiles, int* grid) {
+  int bpsm = 0, dev = 0, sms = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &bpsm, mesh_tile_pipe_kernel<NL, EFIX, PAIR>, kPipeThreads, pipe_smem<NL>());
+  if (e != cudaSuccess) return e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int64_t g = (int64_t)(bpsm > 0 ? bpsm : 1) * sms;
+  if (g > ntiles) g = ntiles;
+  *grid = (int)(g > 0 ? g : 1);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t mesh_prepare(int n_layers, int efix, int64_t ntiles, int* grid) {
+  cudaError_t e;
+  *grid = (int)ntiles;
+  if constexpr (sizeof(T) == 4) {
+    if (n_layers == 2 && efix) {
+      if ((e = pipe_attr<2, true, false>()) != cudaSuccess) return e;
+      return pipe_grid<2, true, false>(ntiles, grid);
+    }
+    if (n_layers == 2) {
+      if ((e = pipe_attr<2, false, true>()) != cudaSuccess) return e;
+      return pipe_grid<2, false, true>(ntiles, grid);
+    }
+    if (efix) {
+      if ((e = pipe_attr<1, true, false>()) != cudaSuccess) return e;
+      return pipe_grid<1, true, false>(ntiles, grid);
+    }
+    if ((e = pipe_attr<1, false, false>()) != cudaSuccess) return e;
+    return pipe_grid<1, false, false>(ntiles, grid);
+  } else {
+    if (n_layers == 2)
+      return efix ? tile_attr<T, 2, true, false>() : tile_attr<T, 2, false, false>();
+    return efix ? tile_attr<T, 1, true, false>() : tile_attr<T, 1, false, false>();
+  }
+}
+
+int mesh_tile_warps(int precision, int n_layers, int efix) {
+  if (precision == 32) return kPipeThreads / 32;
+  return (n_layers == 2 && efix ? TileThreads<double, 2, true>::v : TileThreads<double, 1, false>::v) / 32;
+}
+
+namespace {
+
+template <typename T>
+cudaError_t launch_tile(const MeshStepArgs<T>& f, int n_layers, cudaStream_t st) {
+  if constexpr (sizeof(T) == 4) {
+    // fp32: persistent, double-buffered; two layers two slots per thread
+    // on the FP32x2 pipe (one with the entropy fix)
+    const unsigned g = (unsigned)f.grid;
+    if (n_layers == 2 && f.efix)
+      return launch_pdl(mesh_tile_pipe_kernel<2, true, false>, g, kPipeThreads, pipe_smem<2>(), st, f);
+    if (n_layers == 2)
+      return launch_pdl(mesh_tile_pipe_kernel<2, false, true>, g, kPipeThreads, pipe_smem<2>(), st, f);
+    if (f.efix)
+      return launch_pdl(mesh_tile_pipe_kernel<1, true, false>, g, kPipeThreads, pipe_smem<1>(), st, f);
+    return launch_pdl(mesh_tile_pipe_kernel<1, false, false>, g, kPipeThreads, pipe_smem<1>(), st, f);
+  } else {
+    // fp64: one tile per block (bound by the FP64 pipe, not by latency)
+    const unsigned g = (unsigned)f.ntiles;
+    const size_t sm = mesh_tile_smem<T>(n_layers);
+    if (n_layers == 2 && f.efix)
+      return launch_pdl(mesh_tile_kernel<T, 2, true, false>, g, TileThreads<T, 2, true>::v, sm, st, f);
+    if (n_layers == 2)
+      return launch_pdl(mesh_tile_kernel<T, 2, false, false>, g, TileThreads<T, 2, false>::v, sm, st, f);
+    if (f.efix)
+      return launch_pdl(mesh_tile_kernel<T, 1, true, false>, g, TileThreads<T, 1, true>::v, sm, st, f);
+    return launch_pdl(mesh_tile_kernel<T, 1, false, false>, g, TileThreads<T, 1, false>::v, sm, st, f);
+  }
+}
+
 }  // namespace
 
 template <typename T>
 cudaError_t launch_mesh_step(const MeshStepArgs<T>& f, const MeshUpdateArgs<T>& u, int n_layers,
                              cudaStream_t st, const cudaEvent_t* marks) {
-  const unsigned ge = grid_1d(f.nedges, kEdgeThreads, INT32_MAX);
-  const unsigned gc = grid_1d(f.ncells, kCellThreads, INT32_MAX);
   const unsigned gu = grid_1d((u.ncells + Vec<T>::n - 1) / Vec<T>::n, 256, 152 * 8);
   auto mark = [&](int k) {
     if (marks) cudaEventRecord(marks[k], st);
   };
   mark(0);
-  cudaError_t e;
-  if (n_layers == 2 && f.efix) {
-    // with the entropy fix both precisions take the one-edge-per-thread form
-    e = launch_pdl(mesh_edge_kernel<T, 2, true>, ge, kEdgeThreads, 0, st, f);
-  } else if (n_layers == 2) {
-    if constexpr (sizeof(T) == 4) {
-      const unsigned gp = grid_1d((f.nedges + 1) / 2, kPairThreads, INT32_MAX);
-      e = launch_pdl(mesh_edge2_pair_kernel, gp, kPairThreads, 0, st, f);
-    } else {
-      e = launch_pdl(mesh_edge_kernel<T, 2>, ge, kEdgeThreads, 0, st, f);
-    }
-  } else if (f.efix) {
-    e = launch_pdl(mesh_edge_kernel<T, 1, true>, ge, kEdgeThreads, 0, st, f);
-  } else {
-    e = launch_pdl(mesh_edge_kernel<T, 1>, ge, kEdgeThreads, 0, st, f);
-  }
+  cudaError_t e = launch_tile<T>(f, n_layers, st);
   if (e != cudaSuccess) return e;
   mark(1);
-  e = n_layers == 2 ? launch_pdl(mesh_gather_kernel<T, 2>, gc, kCellThreads, 0, st, f)
-                    : launch_pdl(mesh_gather_kernel<T, 1>, gc, kCellThreads, 0, st, f);
-  if (e != cudaSuccess) return e;
-  mark(2);
   e = n_layers == 2 ? launch_pdl(mesh_update_kernel<T, 2>, gu, 256, 0, st, u)
                     : launch_pdl(mesh_update_kernel<T, 1>, gu, 256, 0, st, u);
   if (e != cudaSuccess) return e;
-  mark(3);
+  mark(2);
   return cudaGetLastError();
 }
 
@@ -492,6 +788,8 @@ cudaError_t launch_mesh_permute(T* const* dst, const T* const* src, int nf, cons
   return cudaGetLastError();
 }
 
+template cudaError_t mesh_prepare<float>(int, int, int64_t, int*);
+template cudaError_t mesh_prepare<double>(int, int, int64_t, int*);
 template cudaError_t launch_mesh_step<float>(const MeshStepArgs<float>&,
                                              const MeshUpdateArgs<float>&, int, cudaStream_t,
                                              const cudaEvent_t*);

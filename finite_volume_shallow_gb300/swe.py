@@ -84,7 +84,7 @@ def load(build_if_needed: bool = True):
     L.swe_create_grid.argtypes = [C.POINTER(_Grid), vp, vp, C.POINTER(_Params), C.POINTER(vp)]
     L.swe_create_mesh.argtypes = [C.POINTER(_Mesh), vp, vp, C.POINTER(_Params), C.POINTER(vp)]
     L.swe_cell_index.argtypes = [vp, vp]
-    L.swe_mesh_info.argtypes = [C.POINTER(_Mesh), vp, vp, vp]
+    L.swe_mesh_info.argtypes = [C.POINTER(_Mesh), vp, vp, vp, vp, vp]
     L.swe_set_timing.argtypes = [vp, i32]
     L.swe_get_timing.argtypes = [vp, vp, i32, C.POINTER(i32)]
     L.swe_step.argtypes = [vp, d, C.POINTER(d)]
@@ -223,13 +223,13 @@ def _mesh_struct(xy, tri, reorder):
 
 def swe_mesh_info(xy, tri, reorder=1):
     """Host-only preview of the mesh preparation: (new_of_old, n_edges,
-    bandwidth); see swe_mesh_info in swe.h."""
+    n_tiles, n_edge_evals, n_halo); see swe_mesh_info in swe.h."""
     mesh, xy, tri = _mesh_struct(xy, tri, reorder)
     order = np.empty(tri.shape[0], dtype=np.int32)
-    ne, bw = C.c_int64(), C.c_int64()
-    _check(load().swe_mesh_info(C.byref(mesh), order.ctypes.data, C.byref(ne), C.byref(bw)),
+    out = [C.c_int64() for _ in range(4)]
+    _check(load().swe_mesh_info(C.byref(mesh), order.ctypes.data, *[C.byref(v) for v in out]),
            "swe_mesh_info")
-    return order, ne.value, bw.value
+    return (order, *[v.value for v in out])
 
 
 def swe_cell_index(s: State):

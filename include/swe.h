@@ -84,10 +84,12 @@ typedef struct {
  *  n_cells     1 <= n_cells <= 2^28: number of triangles
  *  tri         host, 3*n_cells int32: the vertices of triangle c at
  *              tri[3c], tri[3c+1], tri[3c+2], counter-clockwise
- *  reorder     1: store the cells in reverse Cuthill-McKee order (breadth-
- *              first from a pseudo-peripheral cell, then reversed) for
- *              memory locality; 0: keep the caller's order.  Results are in
- *              the caller's numbering either way. */
+ *  reorder     1: store the cells in the order of the Hilbert curve through
+ *              their centroids, so that runs of consecutive cells (the
+ *              tiles of a step, see swe_create_mesh) are compact patches;
+ *              0: keep the caller's order (still correct, but tiles of cells
+ *              far apart evaluate more edges twice and load more halo
+ *              cells).  Results are in the caller's numbering either way. */
 typedef struct {
   int64_t n_vertices;
   const double *xy;
@@ -191,18 +193,22 @@ swe_status swe_create_grid(const swe_grid *grid, const void *H,
  *  out     receives the handle (NULL on failure)
  * Computes on the host, in double precision, every triangle's area and every
  * edge's length and unit normal, pairs the triangles across their shared
- * edges, orders the cells (swe_mesh.reorder) and stores each edge once; then
- * allocates the device state and copies the geometry, H and W0 there.  Each
- * step runs three kernels: one thread per edge for its Roe flux, one thread
- * per cell to sum its three edges in a fixed order and reduce dt, and the
- * update.  The device keeps about (2 nf + 5) values per cell and (3 + 7)
- * (one layer) or (3 + 11) (two layers) values per edge, plus 5 int32 per
- * cell and 2 per edge.
+ * edges, orders the cells (swe_mesh.reorder) and cuts that order into tiles:
+ * runs of consecutive cells with at most 512 edges touching them and at most
+ * 640 cells and neighbouring (halo) cells.  Then allocates the device state
+ * and copies the geometry, H and W0 there.  Each step runs two kernels
+ * ([P1] Algorithm 1, edge processing then volume processing): one block per
+ * tile stages its cells and halo in shared memory, evaluates the Roe flux of
+ * each of its edges once and sums every cell's three edges in a fixed order
+ * (an edge between two tiles is evaluated by both, identically), then the
+ * update.  The device keeps about (2 nf + 3) values and 4 int32 per cell, 3
+ * values and 1 int32 per edge evaluation, 1 int32 per halo entry.
  * Errors: SWE_ERR_ARG (bad argument; an index out of range, a non-finite
  * coordinate, a clockwise or degenerate triangle, an edge traversed twice in
  * the same direction -- which includes any edge of three or more triangles;
- * h <= 0 or non-finite input), SWE_ERR_UNSUPPORTED, SWE_ERR_OOM,
- * SWE_ERR_CUDA. */
+ * h <= 0 or non-finite input), SWE_ERR_UNSUPPORTED (also if the tiles fail
+ * the consistency check run on every preparation, which no valid mesh is
+ * expected to), SWE_ERR_OOM, SWE_ERR_CUDA. */
 swe_status swe_create_mesh(const swe_mesh *mesh, const void *H,
                            const void *const *W0, const swe_params *params,
                            swe_state **out);
@@ -210,11 +216,13 @@ swe_status swe_create_mesh(const swe_mesh *mesh, const void *H,
 /* Host-only preview of the preparation swe_create_mesh does (no device
  * work): checks the mesh and reports, for each caller cell, its internal
  * index (new_of_old, n_cells int32, may be NULL), the number of edges walls
- * included (*n_edges, may be NULL) and the largest index distance between
- * the two cells of an interior edge in the internal order (*bandwidth, may
- * be NULL).  Errors: SWE_ERR_ARG as for swe_create_mesh, SWE_ERR_OOM. */
+ * included (*n_edges), the number of tiles (*n_tiles), the flux evaluations
+ * per step (*n_edge_evals: n_edges plus one for every edge shared by two
+ * tiles) and the halo cells loaded per step (*n_halo); each output may be
+ * NULL.  Errors: SWE_ERR_ARG as for swe_create_mesh, SWE_ERR_OOM. */
 swe_status swe_mesh_info(const swe_mesh *mesh, int32_t *new_of_old,
-                         int64_t *n_edges, int64_t *bandwidth);
+                         int64_t *n_edges, int64_t *n_tiles,
+                         int64_t *n_edge_evals, int64_t *n_halo);
 
 /* Advance one step of eq. (4) with dt_n from eq. (5) evaluated on the
  * current state with CFL number cfl (0 < cfl <= 1).  Waits for the step to
@@ -261,7 +269,11 @@ typedef struct {
   int32_t pitch;        /* elements between rows of a device field         */
   int64_t field_offset; /* elements from a field's base to cell (0, 0)     */
   int64_t device_bytes; /* device memory held by the handle                */
-  int32_t bands, segments, warps_per_block; /* launch shape (one layer)   */
+  int32_t bands, segments, warps_per_block; /* launch shape: one layer on */
+                        /* a grid: column bands, row segments per band and */
+                        /* warps per block of the step kernel; a mesh:     */
+                        /* tiles, blocks and warps per block of the tile   */
+                        /* kernel                                          */
   int32_t n_layers;
   int64_t n_cells;      /* nx*ny, or the mesh's triangles                  */
   int64_t n_edges;      /* edges, walls included                           */

@@ -34,10 +34,8 @@ EVERY = STEPS + 1
     ("grid1", {"cart1_step_kernel": EVERY}),
     ("grid2", {"cart2_march_kernel<plain>": 2, "cart2_march_kernel<fused>": STEPS - 1,
                "cart2_update_kernel": 2}),
-    ("mesh2", {"mesh_edge_kernel": EVERY, "mesh_gather_kernel": EVERY,
-               "mesh_update_kernel": EVERY}),
-    ("mesh1", {"mesh_edge_kernel": EVERY, "mesh_gather_kernel": EVERY,
-               "mesh_update_kernel": EVERY}),
+    ("mesh2", {"mesh_tile_kernel": EVERY, "mesh_update_kernel": EVERY}),
+    ("mesh1", {"mesh_tile_kernel": EVERY, "mesh_update_kernel": EVERY}),
 ])
 def test_kernel_times_listed_and_results_unchanged(case, kernels):
     if case == "grid1":

@@ -1,6 +1,9 @@
-"""Host side of the triangle-mesh path (no GPU): mesh validation and the cell
-order, through swe_mesh_info and swe_create_mesh's argument checks, which
-run entirely on the host before any device call."""
+"""Host side of the triangle-mesh path (no GPU): mesh validation, the cell
+order and the tiles, through swe_mesh_info and swe_create_mesh's argument
+checks, which run entirely on the host before any device call.  Every
+preparation also runs libswe's own consistency check of the tiles (each
+cell's three slot references against the edges), so every call here that
+succeeds has passed it."""
 import ctypes as C
 
 import numpy as np
@@ -29,9 +32,14 @@ def n_edges_of(tri):
 def test_order_is_a_permutation_and_edges_are_counted(n, m, shuffle):
     xy, tri = I.square_tri_mesh(n, m, jitter=0.2, seed=n, shuffle=shuffle)
     for reorder in (0, 1):
-        order, ne, bw = S.swe_mesh_info(xy, tri, reorder=reorder)
+        order, ne, nt, nev, nh = S.swe_mesh_info(xy, tri, reorder=reorder)
         assert np.array_equal(np.sort(order), np.arange(tri.shape[0]))
         assert ne == n_edges_of(tri)
+        assert 1 <= nt <= tri.shape[0]
+        # every edge evaluated at least once, at most once per tile it touches
+        assert ne <= nev <= 2 * ne
+        if nt == 1:
+            assert nev == ne and nh == 0
         if reorder == 0:
             assert np.array_equal(order, np.arange(tri.shape[0]))
     # the oracle's independent edge pairing sees the same edges
@@ -39,20 +47,36 @@ def test_order_is_a_permutation_and_edges_are_counted(n, m, shuffle):
     assert ne == (len(mo.nbr) + int((mo.nbr < 0).sum())) // 2
 
 
-def test_reverse_cuthill_mckee_narrows_the_band():
-    # a shuffled 64 x 64 square: the caller's numbering has a band of about
-    # the whole mesh, the internal order about one row of squares
+def test_hilbert_order_makes_compact_tiles():
+    # a shuffled 64 x 64 square (8192 triangles): in the caller's numbering a
+    # run of consecutive cells is scattered over the mesh, so nearly every
+    # edge of a tile is shared with another tile; in the internal order the
+    # tiles are compact patches
     xy, tri = I.square_tri_mesh(64, jitter=0.2, seed=9, shuffle=True)
-    _, _, bw_caller = S.swe_mesh_info(xy, tri, reorder=0)
-    order, _, bw = S.swe_mesh_info(xy, tri, reorder=1)
-    assert bw_caller > 4000
-    assert bw <= 2 * 64 + 2
-    # neighbours in the internal order really are neighbours in the mesh
-    mo = O.tri_mesh(xy, tri)
-    a = np.repeat(np.arange(tri.shape[0]), 3)
-    inner = mo.nbr >= 0
-    d = np.abs(order[a[inner]] - order[mo.nbr[inner]])
-    assert d.max() == bw
+    n = tri.shape[0]
+    _, ne, nt0, nev0, nh0 = S.swe_mesh_info(xy, tri, reorder=0)
+    order, ne1, nt, nev, nh = S.swe_mesh_info(xy, tri, reorder=1)
+    assert ne1 == ne
+    assert nev0 > 1.8 * ne and nh0 > 2 * n
+    assert nev < 1.10 * ne and nh < 0.2 * n
+    # tiles hold about 300 cells: at most 511 edges each, 1.5 per cell
+    assert 250 <= n / nt <= 400
+    # consecutive cells of the internal order are close in the plane: the
+    # step between them is about one cell, never more than a few on average
+    c = I.tri_centroids(xy, tri)
+    inv = np.empty(n, dtype=np.int64)
+    inv[order] = np.arange(n)
+    step = np.hypot(*(c[inv[1:]] - c[inv[:-1]]).T)
+    assert np.median(step) < 1.0 and step.mean() < 2.0
+
+
+def test_tiles_of_a_graded_mesh():
+    # cells of very different sizes: tiles are cut by counts, not by area
+    xy, tri = I.square_tri_mesh(48, jitter=0.2, seed=4, shuffle=True)
+    xy = np.ascontiguousarray(np.stack([xy[:, 0] ** 3 / 48.0 ** 2, xy[:, 1]], axis=1))
+    order, ne, nt, nev, nh = S.swe_mesh_info(xy, tri)
+    assert np.array_equal(np.sort(order), np.arange(tri.shape[0]))
+    assert nev < 1.15 * ne
 
 
 def test_disconnected_components_are_all_ordered():
@@ -60,9 +84,10 @@ def test_disconnected_components_are_all_ordered():
     xy2 = xy1 + np.array([100.0, 0.0])
     xy = np.ascontiguousarray(np.concatenate([xy1, xy2]))
     tri = np.ascontiguousarray(np.concatenate([tri1, tri1 + xy1.shape[0]]).astype(np.int32))
-    order, ne, _ = S.swe_mesh_info(xy, tri)
+    order, ne, nt, nev, nh = S.swe_mesh_info(xy, tri)
     assert np.array_equal(np.sort(order), np.arange(tri.shape[0]))
     assert ne == 2 * n_edges_of(tri1)
+    assert nt == 1 and nev == ne and nh == 0
 
 
 def bad_meshes():
@@ -128,5 +153,5 @@ def test_create_mesh_rejects_bad_parameters_on_the_host():
     out = C.c_void_p(7)
     assert L.swe_create_mesh(None, None, None, None, C.byref(out)) == S.SWE_ERR_ARG
     assert out.value is None
-    assert L.swe_mesh_info(None, None, None, None) == S.SWE_ERR_ARG
+    assert L.swe_mesh_info(None, None, None, None, None, None) == S.SWE_ERR_ARG
     assert L.swe_cell_index(None, None) == S.SWE_ERR_ARG

@@ -53,7 +53,7 @@ struct swe_state {
   // triangle meshes
   bool mesh = false;
   int64_t ncells = 0, nedges = 0, ntiles = 0;
-  int mesh_grid = 0;                 // blocks of the tile kernel
+  int mesh_grid = 0;                 // blocks of the (persistent) tile kernel
   void* tile_cell = nullptr;         // int32 [ntiles + 1]
   void* tile_halo = nullptr;
   void* tile_slot = nullptr;

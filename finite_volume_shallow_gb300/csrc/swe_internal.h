@@ -225,17 +225,9 @@ struct MeshUpdateArgs {
   unsigned* err;
 };
 
-// Dynamic shared memory of the tile kernel: staged cells (nf fields and H)
-// and the per-slot results.
-template <typename T>
-constexpr size_t mesh_tile_smem(int n_layers) {
-  return (size_t)((n_layers == 2 ? 7 : 5) * kTileCap + (n_layers == 2 ? 11 : 7) * kTileSlots) *
-         sizeof(T);
-}
 // Sets the shared-memory limit of the tile kernel a mesh state of this
-// kind runs on the current device and returns its grid: in fp32 the
-// persistent form, one block per resident slot (at most ntiles); in fp64
-// one block per tile.
+// kind runs on the current device and returns its grid: one block per
+// resident slot (the kernel is persistent), at most ntiles.
 template <typename T>
 cudaError_t mesh_prepare(int n_layers, int efix, int64_t ntiles, int* grid);
 // warps per block of that tile kernel

@@ -10,13 +10,12 @@
 // transport of contaminants (abstract: a transport equation for hC).
 //
 // Two launches per step, no floating-point atomics on results:
-//   mesh_tile_kernel    one block per tile of consecutive cells (compact
-//                       patches, swe_mesh_prep.cpp): stages the tile's cells
-//                       and halo in shared memory, evaluates the rotated Roe
-//                       flux of every edge of the tile once (eq. (2)-(3)),
-//                       then sums each cell's three edges in a fixed order,
-//                       stores R / |V_i| and max-reduces
-//                       sum L max|lambda| / |V_i| for dt;
+//   mesh_tile_kernel    tiles of consecutive cells (compact patches,
+//                       swe_mesh_prep.cpp), each staged with its halo in
+//                       shared memory: the rotated Roe flux of every edge of
+//                       the tile once (eq. (2)-(3)), then each cell's three
+//                       edges summed in a fixed order, R / |V_i| stored and
+//                       sum L max|lambda| / |V_i| max-reduced for dt;
 //   mesh_update_kernel  W -= dt R / |V_i| in place, checks, dt bookkeeping.
 // Algorithm 1's edge and volume loops thus meet in shared memory; the
 // per-edge results never travel through DRAM.
@@ -106,7 +105,7 @@ __device__ __forceinline__ void edge1(const Side1<T>& a, const Side1<T>& b, T gh
 }
 
 // ---- the tile kernel -------------------------------------------------------
-// One block per tile (see swe_internal.h):
+// Per tile (see swe_internal.h) three phases:
 //   1. the tile's cells and its halo cells (W^n and H) into shared memory;
 //   2. every slot of the tile: the Roe flux of the edge from the staged
 //      cells, written per slot to shared memory, what each side adds;
@@ -115,9 +114,6 @@ __device__ __forceinline__ void edge1(const Side1<T>& a, const Side1<T>& b, T gh
 //      for dt.
 // An edge on a tile border is evaluated by both tiles from the same inputs,
 // so both sides see the same flux and mass and pollutant stay conserved.
-template <typename T, int NL, bool EFIX> struct TileThreads {
-  static constexpr int v = (NL == 2 && EFIX) ? 128 : 256;
-};
 
 // staged cells: field f of local cell i at cw[f * kTileCap + i] (H last)
 template <typename T>
@@ -315,67 +311,40 @@ __device__ __forceinline__ T cell_residual(const MeshStepArgs<T>& A, const T* er
   return (d[0] + (d[1] + d[2])) * ia;
 }
 
-// One tile per block (the fp64 form: bound by the FP64 pipe, not by the
-// latency of its loads).
-template <typename T, int NL, bool EFIX, bool PAIR>
-__global__ void __launch_bounds__((TileThreads<T, NL, EFIX>::v))
-    mesh_tile_kernel(const MeshStepArgs<T> A) {
-  using Lay = MeshLayout<NL>;
-  constexpr int NF = Lay::nf;
-  constexpr int NT = TileThreads<T, NL, EFIX>::v;
-  extern __shared__ __align__(16) unsigned char tile_smem[];
-  T* cw = reinterpret_cast<T*>(tile_smem);
-  T* er = cw + (NF + 1) * kTileCap;
-  const int t = blockIdx.x, tid = threadIdx.x;
-  const int32_t c0 = A.tile_cell[t], nct = A.tile_cell[t + 1] - c0;
-  const int32_t h0 = A.tile_halo[t], nh = A.tile_halo[t + 1] - h0;
-  const int32_t s0 = A.tile_slot[t], ns = A.tile_slot[t + 1] - s0;
-  pdl_wait();
-  // 1. cells, then halo
-  for (int i = tid; i < nct + nh; i += NT) {
-    const int32_t c = i < nct ? c0 + i : A.halo[h0 + i - nct];
-#pragma unroll
-    for (int f = 0; f < NF; ++f) cw[f * kTileCap + i] = A.w[f][c];
-    cw[NF * kTileCap + i] = A.H[c];
-  }
-  __syncthreads();
-  // 2. slots
-  bool ok = true;
-  if constexpr (PAIR) {
-    for (int j = 2 * tid; j < ns; j += 2 * NT)
-      ok &= tile_edge_pair(A, cw, er, j, load_slot_pair(A, (int64_t)s0 + j));
-  } else {
-    for (int j = tid; j < ns; j += NT)
-      ok &= tile_edge<T, NL, EFIX>(A, cw, er, j, load_slot(A, (int64_t)s0 + j));
-  }
-  __syncthreads();
-  // 3. cells: residual and wave-speed sum
-  T m = T(0);
-  for (int i = tid; i < nct; i += NT)
-    m = nanmax2(m, cell_residual<T, NL>(A, er, c0 + i, A.cref[c0 + i], A.inv_area[c0 + i]));
-  pdl_trigger();
-  if (NL == 2 && !__syncthreads_and(ok) && tid == 0) atomicOr(A.err, kErrHyperbolic);
-  block_max_publish<T, NT / 32>(m, A.tmax_out);
+// ---- mesh_tile_kernel: persistent and pipelined ------------------------------
+// Each block walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ... and,
+// while it evaluates tile k, stages in shared memory with cp.async: the
+// cells and halo cells of tile k + 1 (into the other of two buffers), the
+// halo indices of tile k + 2 (which the addresses of its halo cells need)
+// and the header of tile k + 3 (which the halo indices need).  The slot data
+// of tile k + 1 is read into registers after the edge phase of tile k.  All
+// of it has the whole edge and cell phases of a tile to land, so a block's
+// loads overlap its own arithmetic; with tiles of equal size the blocks of
+// one SM would otherwise load, and then compute, at the same time.
+// Threads per block: 256, but 512 for two layers in fp64 without the
+// entropy fix (one slot per thread): there the shared memory holds one
+// block per SM, and the FP64 pipe wants more warps than eight.
+template <typename T, int NL, bool EFIX>
+constexpr int pipe_threads() {
+  return (sizeof(T) == 8 && NL == 2 && !EFIX) ? 512 : 256;
 }
-
-// ---- fp32: the persistent, pipelined form of the tile kernel -----------------
-// The same three phases, but each block walks the tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... and, while it evaluates tile k, stages in
-// shared memory with cp.async: the cells and halo cells of tile k + 1 (into
-// the other of two buffers), the halo indices of tile k + 2 (which the
-// addresses of its halo cells need) and the header of tile k + 3 (which the
-// halo indices need).  The slot data of tile k + 1 is read into registers
-// after the edge phase of tile k.  All of it has the whole edge and cell
-// phases of a tile to land, so a block's loads overlap its own arithmetic;
-// with tiles of equal size the blocks of one SM would otherwise load, and
-// then compute, at the same time.
-constexpr int kPipeThreads = 256;
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                    (uint32_t)__cvta_generic_to_shared(dst)),
                "l"(src)
                : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void cp_async_el(T* dst, const T* src) {
+  if constexpr (sizeof(T) == 8) cp_async8(dst, src);
+  else cp_async4(dst, src);
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -392,17 +361,18 @@ template <int NL>
 constexpr int pipe_cell_words() {
   return (MeshLayout<NL>::nf + 1) * kTileCap;
 }
-template <int NL>
+template <typename T, int NL>
 constexpr size_t pipe_smem() {
-  return (size_t)(2 * pipe_cell_words<NL>() + 3 * kTileHalo + MeshLayout<NL>::ne * kTileSlots) *
-         sizeof(float);
+  return (size_t)(2 * pipe_cell_words<NL>() + MeshLayout<NL>::ne * kTileSlots) * sizeof(T) +
+         (size_t)3 * kTileHalo * sizeof(int32_t);
 }
 
 struct TileHdr {
   int32_t c0, nct, h0, nh, s0, ns;
 };
 // header entry: tile_cell, tile_halo and tile_slot at t and t + 1
-__device__ __forceinline__ void request_hdr(const MeshStepArgs<float>& A, int32_t* e, int t) {
+template <typename T>
+__device__ __forceinline__ void request_hdr(const MeshStepArgs<T>& A, int32_t* e, int t) {
   const int i = threadIdx.x;
   if (i < 6) {
     const int32_t* src = i < 2 ? A.tile_cell : (i < 4 ? A.tile_halo : A.tile_slot);
@@ -412,64 +382,74 @@ __device__ __forceinline__ void request_hdr(const MeshStepArgs<float>& A, int32_
 __device__ __forceinline__ TileHdr read_hdr(const int32_t* e) {
   return TileHdr{e[0], e[1] - e[0], e[2], e[3] - e[2], e[4], e[5] - e[4]};
 }
-__device__ __forceinline__ void request_hidx(const MeshStepArgs<float>& A, int32_t* hidx,
+template <int NT, typename T>
+__device__ __forceinline__ void request_hidx(const MeshStepArgs<T>& A, int32_t* hidx,
                                              const TileHdr& h) {
-  for (int k = threadIdx.x; k < h.nh; k += kPipeThreads) cp_async4(hidx + k, A.halo + h.h0 + k);
+  for (int k = threadIdx.x; k < h.nh; k += NT) cp_async4(hidx + k, A.halo + h.h0 + k);
 }
-template <int NL>
-__device__ __forceinline__ void request_cells(const MeshStepArgs<float>& A, float* buf,
+template <int NT, typename T, int NL>
+__device__ __forceinline__ void request_cells(const MeshStepArgs<T>& A, T* buf,
                                               const int32_t* hidx, const TileHdr& h) {
   constexpr int NF = MeshLayout<NL>::nf;
-  for (int i = threadIdx.x; i < h.nct + h.nh; i += kPipeThreads) {
+  for (int i = threadIdx.x; i < h.nct + h.nh; i += NT) {
     const int64_t c = i < h.nct ? (int64_t)h.c0 + i : (int64_t)hidx[i - h.nct];
 #pragma unroll
-    for (int f = 0; f < NF; ++f) cp_async4(buf + f * kTileCap + i, A.w[f] + c);
-    cp_async4(buf + NF * kTileCap + i, A.H + c);
+    for (int f = 0; f < NF; ++f) cp_async_el(buf + f * kTileCap + i, A.w[f] + c);
+    cp_async_el(buf + NF * kTileCap + i, A.H + c);
   }
 }
 
-// slot data of one tile in registers: a pair per thread (PAIR), else
-// kTileSlots / kPipeThreads single slots
-constexpr int kPipeSlots = kTileSlots / kPipeThreads;
-template <bool PAIR> struct PipeSlots {
-  Slot<float> s[kPipeSlots];
+// slot data of one tile in registers: a pair per thread (PAIR, 256
+// threads), else kTileSlots / NT single slots
+template <typename T, bool PAIR, int NT> struct PipeSlots {
+  Slot<T> s[kTileSlots / NT];
 };
-template <> struct PipeSlots<true> {
+template <int NT> struct PipeSlots<float, true, NT> {
   SlotPair p;
 };
-template <bool PAIR>
-__device__ __forceinline__ void load_slots(const MeshStepArgs<float>& A, const TileHdr& h,
-                                           PipeSlots<PAIR>& r) {
+template <int NT, typename T, bool PAIR>
+__device__ __forceinline__ void load_slots(const MeshStepArgs<T>& A, const TileHdr& h,
+                                           PipeSlots<T, PAIR, NT>& r) {
   if constexpr (PAIR) {
     const int j = 2 * threadIdx.x;
     if (j < h.ns) r.p = load_slot_pair(A, (int64_t)h.s0 + j);
   } else {
 #pragma unroll
-    for (int k = 0; k < kPipeSlots; ++k) {
-      const int j = threadIdx.x + k * kPipeThreads;
+    for (int k = 0; k < kTileSlots / NT; ++k) {
+      const int j = threadIdx.x + k * NT;
       if (j < h.ns) r.s[k] = load_slot(A, (int64_t)h.s0 + j);
     }
   }
 }
 
-constexpr int kPipeCells = (kTileCap + kPipeThreads - 1) / kPipeThreads;
-
 #ifndef SWE_PIPE_PAIR_MIN_BLOCKS
-#define SWE_PIPE_PAIR_MIN_BLOCKS 3
+#define SWE_PIPE_PAIR_MIN_BLOCKS 2
 #endif
-template <int NL, bool EFIX, bool PAIR> struct PipeMinBlocks { static constexpr int v = 2; };
-template <> struct PipeMinBlocks<2, false, true> { static constexpr int v = SWE_PIPE_PAIR_MIN_BLOCKS; };
-template <> struct PipeMinBlocks<1, false, false> { static constexpr int v = 4; };
-template <> struct PipeMinBlocks<1, true, false> { static constexpr int v = 4; };
+// Blocks per SM the registers are held to: as many as the shared memory
+// admits in fp32 (the packed two-layer form spills a little at three); in
+// fp64 the FP64 pipe is the bound and one or two blocks keep it busy.
+template <typename T, int NL, bool EFIX, bool PAIR> struct PipeMinBlocks {
+  static constexpr int v = 1;
+};
+template <> struct PipeMinBlocks<float, 2, false, true> {
+  static constexpr int v = SWE_PIPE_PAIR_MIN_BLOCKS;
+};
+template <> struct PipeMinBlocks<float, 2, true, false> { static constexpr int v = 2; };
+template <> struct PipeMinBlocks<float, 1, false, false> { static constexpr int v = 4; };
+template <> struct PipeMinBlocks<float, 1, true, false> { static constexpr int v = 4; };
 
-template <int NL, bool EFIX, bool PAIR>
-__global__ void __launch_bounds__(kPipeThreads, (PipeMinBlocks<NL, EFIX, PAIR>::v))
-    mesh_tile_pipe_kernel(const MeshStepArgs<float> A) {
+template <typename T, int NL, bool EFIX, bool PAIR>
+__global__ void __launch_bounds__((pipe_threads<T, NL, EFIX>()), (PipeMinBlocks<T, NL, EFIX, PAIR>::v))
+    mesh_tile_kernel(const MeshStepArgs<T> A) {
+  constexpr int NT = pipe_threads<T, NL, EFIX>();
+  constexpr int NSL = kTileSlots / NT;
+  constexpr int NCL = (kTileCap + NT - 1) / NT;
+  static_assert(!PAIR || NT == 256, "the packed pair form has 256 threads");
   extern __shared__ __align__(16) unsigned char tile_smem[];
   __shared__ __align__(16) int32_t ring[4][8];
-  float* const cbuf = reinterpret_cast<float*>(tile_smem);
-  int32_t* const hbuf = reinterpret_cast<int32_t*>(cbuf + 2 * pipe_cell_words<NL>());
-  float* const er = reinterpret_cast<float*>(hbuf + 3 * kTileHalo);
+  T* const cbuf = reinterpret_cast<T*>(tile_smem);
+  T* const er = cbuf + 2 * pipe_cell_words<NL>();
+  int32_t* const hbuf = reinterpret_cast<int32_t*>(er + MeshLayout<NL>::ne * kTileSlots);
   const int G = gridDim.x, nt = (int)A.ntiles, tid = threadIdx.x;
   const int t0 = blockIdx.x;  // < nt: the grid never exceeds the tile count
   auto valid = [&](int k) { return t0 + k * G < nt; };
@@ -482,51 +462,53 @@ __global__ void __launch_bounds__(kPipeThreads, (PipeMinBlocks<NL, EFIX, PAIR>::
   cp_async_wait_all();
   __syncthreads();
   for (int k = 0; k < 2; ++k)
-    if (valid(k)) request_hidx(A, hbuf + k * kTileHalo, read_hdr(ring[k]));
+    if (valid(k)) request_hidx<NT>(A, hbuf + k * kTileHalo, read_hdr(ring[k]));
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
-  request_cells<NL>(A, cbuf, hbuf, read_hdr(ring[0]));
+  request_cells<NT, T, NL>(A, cbuf, hbuf, read_hdr(ring[0]));
   cp_async_commit();
-  PipeSlots<PAIR> sl;
-  load_slots<PAIR>(A, read_hdr(ring[0]), sl);
+  PipeSlots<T, PAIR, NT> sl;
+  load_slots<NT>(A, read_hdr(ring[0]), sl);
   cp_async_wait_all();
   __syncthreads();
   bool ok = true;
-  float m = 0.f;
+  T m = T(0);
   for (int it = 0;; ++it) {
     const int t = t0 + it * G;
     const bool more = valid(it + 1);
-    const float* cw = cbuf + (it & 1) * pipe_cell_words<NL>();
+    const T* cw = cbuf + (it & 1) * pipe_cell_words<NL>();
     const int32_t* hcur = ring[it & 3];
     // staging ahead: header k + 3, halo indices k + 2, cells k + 1
     if (valid(it + 3)) request_hdr(A, ring[(it + 3) & 3], t + 3 * G);
-    if (valid(it + 2)) request_hidx(A, hbuf + ((it + 2) % 3) * kTileHalo, read_hdr(ring[(it + 2) & 3]));
+    if (valid(it + 2))
+      request_hidx<NT>(A, hbuf + ((it + 2) % 3) * kTileHalo, read_hdr(ring[(it + 2) & 3]));
     if (more)
-      request_cells<NL>(A, cbuf + ((it + 1) & 1) * pipe_cell_words<NL>(),
-                        hbuf + ((it + 1) % 3) * kTileHalo, read_hdr(ring[(it + 1) & 3]));
+      request_cells<NT, T, NL>(A, cbuf + ((it + 1) & 1) * pipe_cell_words<NL>(),
+                               hbuf + ((it + 1) % 3) * kTileHalo, read_hdr(ring[(it + 1) & 3]));
     cp_async_commit();
     // edges of this tile
     {
       const int ns = hcur[5] - hcur[4];
       if constexpr (PAIR) {
+        static_assert(sizeof(T) == 4, "the packed pair form is fp32");
         if (2 * tid < ns) ok &= tile_edge_pair(A, cw, er, 2 * tid, sl.p);
       } else {
 #pragma unroll
-        for (int k = 0; k < kPipeSlots; ++k) {
-          const int j = tid + k * kPipeThreads;
-          if (j < ns) ok &= tile_edge<float, NL, EFIX>(A, cw, er, j, sl.s[k]);
+        for (int k = 0; k < NSL; ++k) {
+          const int j = tid + k * NT;
+          if (j < ns) ok &= tile_edge<T, NL, EFIX>(A, cw, er, j, sl.s[k]);
         }
       }
     }
     // the next tile's slots; this tile's cell references and areas
-    if (more) load_slots<PAIR>(A, read_hdr(ring[(it + 1) & 3]), sl);
+    if (more) load_slots<NT>(A, read_hdr(ring[(it + 1) & 3]), sl);
     const int c0 = hcur[0], nct = hcur[1] - hcur[0];
-    uint2 cr[kPipeCells];
-    float ia[kPipeCells];
+    uint2 cr[NCL];
+    T ia[NCL];
 #pragma unroll
-    for (int k = 0; k < kPipeCells; ++k) {
-      const int i = tid + k * kPipeThreads;
+    for (int k = 0; k < NCL; ++k) {
+      const int i = tid + k * NT;
       if (i < nct) {
         cr[k] = A.cref[(int64_t)c0 + i];
         ia[k] = A.inv_area[(int64_t)c0 + i];
@@ -535,9 +517,9 @@ __global__ void __launch_bounds__(kPipeThreads, (PipeMinBlocks<NL, EFIX, PAIR>::
     __syncthreads();  // slot results complete
     // cells of this tile
 #pragma unroll
-    for (int k = 0; k < kPipeCells; ++k) {
-      const int i = tid + k * kPipeThreads;
-      if (i < nct) m = nanmax2(m, cell_residual<float, NL>(A, er, (int64_t)c0 + i, cr[k], ia[k]));
+    for (int k = 0; k < NCL; ++k) {
+      const int i = tid + k * NT;
+      if (i < nct) m = nanmax2(m, cell_residual<T, NL>(A, er, (int64_t)c0 + i, cr[k], ia[k]));
     }
     cp_async_wait_all();
     __syncthreads();  // what was staged landed; slot results free
@@ -545,7 +527,7 @@ __global__ void __launch_bounds__(kPipeThreads, (PipeMinBlocks<NL, EFIX, PAIR>::
   }
   pdl_trigger();
   if (NL == 2 && !__syncthreads_and(ok) && tid == 0) atomicOr(A.err, kErrHyperbolic);
-  block_max_publish<float, kPipeThreads / 32>(m, A.tmax_out);
+  block_max_publish<T, NT / 32>(m, A.tmax_out);
 }
 
 // Vector width of the update: 16-byte loads and stores.
@@ -660,21 +642,14 @@ unsigned grid_1d(int64_t n, int threads, int64_t cap) {
 }
 
 template <typename T, int NL, bool EFIX, bool PAIR>
-cudaError_t tile_attr() {
-  return cudaFuncSetAttribute(mesh_tile_kernel<T, NL, EFIX, PAIR>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)mesh_tile_smem<T>(NL));
-}
-template <int NL, bool EFIX, bool PAIR>
-cudaError_t pipe_attr() {
-  return cudaFuncSetAttribute(mesh_tile_pipe_kernel<NL, EFIX, PAIR>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe_smem<NL>());
-}
-template <int NL, bool EFIX, bool PAIR>
-cudaError_t pipe_grid(int64_t ntiles, int* grid) {
+cudaError_t pipe_prepare(int64_t ntiles, int* grid) {
+  cudaError_t e = cudaFuncSetAttribute(mesh_tile_kernel<T, NL, EFIX, PAIR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pipe_smem<T, NL>());
+  if (e != cudaSuccess) return e;
   int bpsm = 0, dev = 0, sms = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &bpsm, mesh_tile_pipe_kernel<NL, EFIX, PAIR>, kPipeThreads, pipe_smem<NL>());
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &bpsm, mesh_tile_kernel<T, NL, EFIX, PAIR>, pipe_threads<T, NL, EFIX>(), pipe_smem<T, NL>());
   if (e != cudaSuccess) return e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -689,62 +664,35 @@ cudaError_t pipe_grid(int64_t ntiles, int* grid) {
 
 template <typename T>
 cudaError_t mesh_prepare(int n_layers, int efix, int64_t ntiles, int* grid) {
-  cudaError_t e;
-  *grid = (int)ntiles;
-  if constexpr (sizeof(T) == 4) {
-    if (n_layers == 2 && efix) {
-      if ((e = pipe_attr<2, true, false>()) != cudaSuccess) return e;
-      return pipe_grid<2, true, false>(ntiles, grid);
-    }
-    if (n_layers == 2) {
-      if ((e = pipe_attr<2, false, true>()) != cudaSuccess) return e;
-      return pipe_grid<2, false, true>(ntiles, grid);
-    }
-    if (efix) {
-      if ((e = pipe_attr<1, true, false>()) != cudaSuccess) return e;
-      return pipe_grid<1, true, false>(ntiles, grid);
-    }
-    if ((e = pipe_attr<1, false, false>()) != cudaSuccess) return e;
-    return pipe_grid<1, false, false>(ntiles, grid);
-  } else {
-    if (n_layers == 2)
-      return efix ? tile_attr<T, 2, true, false>() : tile_attr<T, 2, false, false>();
-    return efix ? tile_attr<T, 1, true, false>() : tile_attr<T, 1, false, false>();
-  }
+  constexpr bool F32 = sizeof(T) == 4;
+  if (n_layers == 2 && efix) return pipe_prepare<T, 2, true, false>(ntiles, grid);
+  if (n_layers == 2) return pipe_prepare<T, 2, false, F32>(ntiles, grid);
+  if (efix) return pipe_prepare<T, 1, true, false>(ntiles, grid);
+  return pipe_prepare<T, 1, false, false>(ntiles, grid);
 }
 
 int mesh_tile_warps(int precision, int n_layers, int efix) {
-  if (precision == 32) return kPipeThreads / 32;
-  return (n_layers == 2 && efix ? TileThreads<double, 2, true>::v : TileThreads<double, 1, false>::v) / 32;
+  if (precision == 64 && n_layers == 2 && !efix) return pipe_threads<double, 2, false>() / 32;
+  return pipe_threads<float, 1, false>() / 32;
 }
 
 namespace {
 
+template <typename T, int NL, bool EFIX, bool PAIR>
+cudaError_t launch_pipe(const MeshStepArgs<T>& f, cudaStream_t st) {
+  return launch_pdl(mesh_tile_kernel<T, NL, EFIX, PAIR>, (unsigned)f.grid,
+                    pipe_threads<T, NL, EFIX>(), pipe_smem<T, NL>(), st, f);
+}
+
+// The tile kernel of a step: two layers in fp32 two slots per thread on the
+// FP32x2 pipe (one with the entropy fix), else one.
 template <typename T>
 cudaError_t launch_tile(const MeshStepArgs<T>& f, int n_layers, cudaStream_t st) {
-  if constexpr (sizeof(T) == 4) {
-    // fp32: persistent, double-buffered; two layers two slots per thread
-    // on the FP32x2 pipe (one with the entropy fix)
-    const unsigned g = (unsigned)f.grid;
-    if (n_layers == 2 && f.efix)
-      return launch_pdl(mesh_tile_pipe_kernel<2, true, false>, g, kPipeThreads, pipe_smem<2>(), st, f);
-    if (n_layers == 2)
-      return launch_pdl(mesh_tile_pipe_kernel<2, false, true>, g, kPipeThreads, pipe_smem<2>(), st, f);
-    if (f.efix)
-      return launch_pdl(mesh_tile_pipe_kernel<1, true, false>, g, kPipeThreads, pipe_smem<1>(), st, f);
-    return launch_pdl(mesh_tile_pipe_kernel<1, false, false>, g, kPipeThreads, pipe_smem<1>(), st, f);
-  } else {
-    // fp64: one tile per block (bound by the FP64 pipe, not by latency)
-    const unsigned g = (unsigned)f.ntiles;
-    const size_t sm = mesh_tile_smem<T>(n_layers);
-    if (n_layers == 2 && f.efix)
-      return launch_pdl(mesh_tile_kernel<T, 2, true, false>, g, TileThreads<T, 2, true>::v, sm, st, f);
-    if (n_layers == 2)
-      return launch_pdl(mesh_tile_kernel<T, 2, false, false>, g, TileThreads<T, 2, false>::v, sm, st, f);
-    if (f.efix)
-      return launch_pdl(mesh_tile_kernel<T, 1, true, false>, g, TileThreads<T, 1, true>::v, sm, st, f);
-    return launch_pdl(mesh_tile_kernel<T, 1, false, false>, g, TileThreads<T, 1, false>::v, sm, st, f);
-  }
+  constexpr bool F32 = sizeof(T) == 4;
+  if (n_layers == 2 && f.efix) return launch_pipe<T, 2, true, false>(f, st);
+  if (n_layers == 2) return launch_pipe<T, 2, false, F32>(f, st);
+  if (f.efix) return launch_pipe<T, 1, true, false>(f, st);
+  return launch_pipe<T, 1, false, false>(f, st);
 }
 
 }  // namespace

@@ -100,8 +100,8 @@ def test_full_size_over_the_workloads_own_steps(name, precision):
     assert abs(t / rec["t"] - 1.0) <= tol["dt"]
     long_fp32 = LONG_RUN_FP32.get(name) if precision == 32 else None
     if long_fp32:
-        # fp32 round-off grows with the step count; the benchmark spec's fp32 bounds
-        # are read as holding after 100 steps, as its fp64 bound does (see
+        # fp32 round-off grows with the step count; the fp32 bounds are read
+        # as holding after 100 steps, as the fp64 bound does (see
         # LONG_RUN_FP32): depths, dt and block means keep them here, the
         # discharges at single cells get the measured growth
         for nm in names:

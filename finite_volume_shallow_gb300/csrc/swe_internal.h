@@ -153,8 +153,8 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
 // A mesh state keeps its cells in an internal order (the Hilbert curve through
 // the cell centroids unless the caller asked for its own), one contiguous
 // array per field, and cuts that order into tiles: consecutive cells, each
-// tile with at most kTileSlots edge slots, at most kTileHalo halo cells and
-// at most kTileCap cells plus halo cells.  A tile's edge slots are the edges with at least one cell in
+// tile with at most kTileSlots edge slots, kTileCells cells, kTileHalo halo
+// cells and kTileCap cells plus halo cells.  A tile's edge slots are the edges with at least one cell in
 // the tile: an edge inside a tile has one slot, an edge between two tiles
 // one slot in each (the two evaluate it identically).  Every edge keeps one
 // orientation: cells a < b (b a wall on the mesh boundary) and the unit
@@ -180,6 +180,7 @@ cudaError_t launch_check2(const Fields6<T>& w6, int nx, int ny, int pitch, unsig
 constexpr int kTileSlots = 512;
 constexpr int kTileCap = 640;
 constexpr int kTileHalo = 256;
+constexpr int kTileCells = 512;
 constexpr int kTileWall = 0xffff;
 template <int NL> struct MeshLayout;
 template <> struct MeshLayout<1> {

@@ -438,92 +438,193 @@ template <> struct PipeMinBlocks<float, 2, true, false> { static constexpr int v
 template <> struct PipeMinBlocks<float, 1, false, false> { static constexpr int v = 4; };
 template <> struct PipeMinBlocks<float, 1, true, false> { static constexpr int v = 4; };
 
+// Overlapped form (OVL): two slot-result buffers, so that one phase
+// evaluates the edges of tile k + 1 and sums the cells of tile k, with one
+// barrier per tile instead of two; the staging runs one tile further ahead
+// (cells k + 2, halo indices k + 3, headers k + 4) and each tile's cell
+// references and areas are staged too.  It needs more shared memory: chosen
+// per variant by measurement (SWE_MESH_OVERLAP: bit 0 one layer fp32, 1 two
+// layers fp32, 2 one layer fp64, 3 two layers fp64).  On the 2.1M-triangle
+// workloads (CUDA events per step): two layers fp32 0.0876 ms against
+// 0.1014, fp64 2.670 against 2.699; one layer fp32 0.0673 against 0.0553
+// and fp64 0.853 against 0.773, where the extra shared memory costs a block
+// per SM.
+#ifndef SWE_MESH_OVERLAP
+#define SWE_MESH_OVERLAP 0xa
+#endif
+template <typename T, int NL>
+constexpr bool pipe_overlap() {
+  return (SWE_MESH_OVERLAP >> ((sizeof(T) == 8 ? 2 : 0) + (NL == 2 ? 1 : 0))) & 1;
+}
+// shared memory of the tile kernel
+template <typename T, int NL>
+constexpr size_t tile_smem() {
+  if (!pipe_overlap<T, NL>()) return pipe_smem<T, NL>();
+  return (size_t)(2 * pipe_cell_words<NL>() + 2 * MeshLayout<NL>::ne * kTileSlots +
+                  2 * kTileCells) * sizeof(T) +
+         (size_t)2 * kTileCells * sizeof(uint2) + (size_t)3 * kTileHalo * sizeof(int32_t);
+}
+
+template <int NT, typename T>
+__device__ __forceinline__ void request_crefs(const MeshStepArgs<T>& A, uint2* cr, T* ia,
+                                              const TileHdr& h) {
+  for (int i = threadIdx.x; i < h.nct; i += NT) {
+    cp_async8(cr + i, A.cref + (int64_t)h.c0 + i);
+    cp_async_el(ia + i, A.inv_area + (int64_t)h.c0 + i);
+  }
+}
+
 template <typename T, int NL, bool EFIX, bool PAIR>
 __global__ void __launch_bounds__((pipe_threads<T, NL, EFIX>()), (PipeMinBlocks<T, NL, EFIX, PAIR>::v))
     mesh_tile_kernel(const MeshStepArgs<T> A) {
   constexpr int NT = pipe_threads<T, NL, EFIX>();
   constexpr int NSL = kTileSlots / NT;
-  constexpr int NCL = (kTileCap + NT - 1) / NT;
+  constexpr int NCL = (kTileCells + NT - 1) / NT;
+  constexpr int NE = MeshLayout<NL>::ne * kTileSlots;
   static_assert(!PAIR || NT == 256, "the packed pair form has 256 threads");
   extern __shared__ __align__(16) unsigned char tile_smem[];
-  __shared__ __align__(16) int32_t ring[4][8];
-  T* const cbuf = reinterpret_cast<T*>(tile_smem);
-  T* const er = cbuf + 2 * pipe_cell_words<NL>();
-  int32_t* const hbuf = reinterpret_cast<int32_t*>(er + MeshLayout<NL>::ne * kTileSlots);
   const int G = gridDim.x, nt = (int)A.ntiles, tid = threadIdx.x;
   const int t0 = blockIdx.x;  // < nt: the grid never exceeds the tile count
   auto valid = [&](int k) { return t0 + k * G < nt; };
-  pdl_wait();
-  // prologue: headers of tiles 0-2 of this block, halo indices of tiles 0-1,
-  // cells of tile 0, slots of tile 0
-  for (int k = 0; k < 3; ++k)
-    if (valid(k)) request_hdr(A, ring[k], t0 + k * G);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-  for (int k = 0; k < 2; ++k)
-    if (valid(k)) request_hidx<NT>(A, hbuf + k * kTileHalo, read_hdr(ring[k]));
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-  request_cells<NT, T, NL>(A, cbuf, hbuf, read_hdr(ring[0]));
-  cp_async_commit();
-  PipeSlots<T, PAIR, NT> sl;
-  load_slots<NT>(A, read_hdr(ring[0]), sl);
-  cp_async_wait_all();
-  __syncthreads();
   bool ok = true;
   T m = T(0);
-  for (int it = 0;; ++it) {
-    const int t = t0 + it * G;
-    const bool more = valid(it + 1);
-    const T* cw = cbuf + (it & 1) * pipe_cell_words<NL>();
-    const int32_t* hcur = ring[it & 3];
-    // staging ahead: header k + 3, halo indices k + 2, cells k + 1
-    if (valid(it + 3)) request_hdr(A, ring[(it + 3) & 3], t + 3 * G);
-    if (valid(it + 2))
-      request_hidx<NT>(A, hbuf + ((it + 2) % 3) * kTileHalo, read_hdr(ring[(it + 2) & 3]));
-    if (more)
-      request_cells<NT, T, NL>(A, cbuf + ((it + 1) & 1) * pipe_cell_words<NL>(),
-                               hbuf + ((it + 1) % 3) * kTileHalo, read_hdr(ring[(it + 1) & 3]));
-    cp_async_commit();
-    // edges of this tile
-    {
-      const int ns = hcur[5] - hcur[4];
-      if constexpr (PAIR) {
-        static_assert(sizeof(T) == 4, "the packed pair form is fp32");
-        if (2 * tid < ns) ok &= tile_edge_pair(A, cw, er, 2 * tid, sl.p);
-      } else {
+  PipeSlots<T, PAIR, NT> sl;
+  // the edges of a staged tile into er
+  auto edges = [&](const T* cw, T* er, const int32_t* h) {
+    const int ns = h[5] - h[4];
+    if constexpr (PAIR) {
+      static_assert(sizeof(T) == 4, "the packed pair form is fp32");
+      if (2 * tid < ns) ok &= tile_edge_pair(A, cw, er, 2 * tid, sl.p);
+    } else {
 #pragma unroll
-        for (int k = 0; k < NSL; ++k) {
-          const int j = tid + k * NT;
-          if (j < ns) ok &= tile_edge<T, NL, EFIX>(A, cw, er, j, sl.s[k]);
+      for (int k = 0; k < NSL; ++k) {
+        const int j = tid + k * NT;
+        if (j < ns) ok &= tile_edge<T, NL, EFIX>(A, cw, er, j, sl.s[k]);
+      }
+    }
+  };
+  pdl_wait();
+  if constexpr (!pipe_overlap<T, NL>()) {
+    __shared__ __align__(16) int32_t ring[4][8];
+    T* const cbuf = reinterpret_cast<T*>(tile_smem);
+    T* const er = cbuf + 2 * pipe_cell_words<NL>();
+    int32_t* const hbuf = reinterpret_cast<int32_t*>(er + NE);
+    // prologue: headers of tiles 0-2 of this block, halo indices of tiles
+    // 0-1, cells of tile 0, slots of tile 0
+    for (int k = 0; k < 3; ++k)
+      if (valid(k)) request_hdr(A, ring[k], t0 + k * G);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int k = 0; k < 2; ++k)
+      if (valid(k)) request_hidx<NT>(A, hbuf + k * kTileHalo, read_hdr(ring[k]));
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    request_cells<NT, T, NL>(A, cbuf, hbuf, read_hdr(ring[0]));
+    cp_async_commit();
+    load_slots<NT>(A, read_hdr(ring[0]), sl);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int it = 0;; ++it) {
+      const int t = t0 + it * G;
+      const bool more = valid(it + 1);
+      const int32_t* hcur = ring[it & 3];
+      // staging ahead: header k + 3, halo indices k + 2, cells k + 1
+      if (valid(it + 3)) request_hdr(A, ring[(it + 3) & 3], t + 3 * G);
+      if (valid(it + 2))
+        request_hidx<NT>(A, hbuf + ((it + 2) % 3) * kTileHalo, read_hdr(ring[(it + 2) & 3]));
+      if (more)
+        request_cells<NT, T, NL>(A, cbuf + ((it + 1) & 1) * pipe_cell_words<NL>(),
+                                 hbuf + ((it + 1) % 3) * kTileHalo, read_hdr(ring[(it + 1) & 3]));
+      cp_async_commit();
+      edges(cbuf + (it & 1) * pipe_cell_words<NL>(), er, hcur);
+      // the next tile's slots; this tile's cell references and areas
+      if (more) load_slots<NT>(A, read_hdr(ring[(it + 1) & 3]), sl);
+      const int c0 = hcur[0], nct = hcur[1] - hcur[0];
+      uint2 cr[NCL];
+      T ia[NCL];
+#pragma unroll
+      for (int k = 0; k < NCL; ++k) {
+        const int i = tid + k * NT;
+        if (i < nct) {
+          cr[k] = A.cref[(int64_t)c0 + i];
+          ia[k] = A.inv_area[(int64_t)c0 + i];
         }
       }
-    }
-    // the next tile's slots; this tile's cell references and areas
-    if (more) load_slots<NT>(A, read_hdr(ring[(it + 1) & 3]), sl);
-    const int c0 = hcur[0], nct = hcur[1] - hcur[0];
-    uint2 cr[NCL];
-    T ia[NCL];
+      __syncthreads();  // slot results complete
 #pragma unroll
-    for (int k = 0; k < NCL; ++k) {
-      const int i = tid + k * NT;
-      if (i < nct) {
-        cr[k] = A.cref[(int64_t)c0 + i];
-        ia[k] = A.inv_area[(int64_t)c0 + i];
+      for (int k = 0; k < NCL; ++k) {
+        const int i = tid + k * NT;
+        if (i < nct) m = nanmax2(m, cell_residual<T, NL>(A, er, (int64_t)c0 + i, cr[k], ia[k]));
       }
+      cp_async_wait_all();
+      __syncthreads();  // what was staged landed; slot results free
+      if (!more) break;
     }
-    __syncthreads();  // slot results complete
-    // cells of this tile
-#pragma unroll
-    for (int k = 0; k < NCL; ++k) {
-      const int i = tid + k * NT;
-      if (i < nct) m = nanmax2(m, cell_residual<T, NL>(A, er, (int64_t)c0 + i, cr[k], ia[k]));
-    }
+  } else {
+    __shared__ __align__(16) int32_t ring[8][8];
+    T* const cbuf = reinterpret_cast<T*>(tile_smem);
+    T* const erb = cbuf + 2 * pipe_cell_words<NL>();
+    T* const iab = erb + 2 * NE;
+    uint2* const crb = reinterpret_cast<uint2*>(iab + 2 * kTileCells);
+    int32_t* const hbuf = reinterpret_cast<int32_t*>(crb + 2 * kTileCells);
+    auto cbuf_of = [&](int k) { return cbuf + (k & 1) * pipe_cell_words<NL>(); };
+    auto hidx_of = [&](int k) { return hbuf + (k % 3) * kTileHalo; };
+    // prologue: headers of tiles 0-3, halo indices of tiles 0-2, cells of
+    // tiles 0-1, cell references of tile 0, slots of tile 0; edges of tile 0
+    for (int k = 0; k < 4; ++k)
+      if (valid(k)) request_hdr(A, ring[k], t0 + k * G);
+    cp_async_commit();
     cp_async_wait_all();
-    __syncthreads();  // what was staged landed; slot results free
-    if (!more) break;
+    __syncthreads();
+    for (int k = 0; k < 3; ++k)
+      if (valid(k)) request_hidx<NT>(A, hidx_of(k), read_hdr(ring[k]));
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int k = 0; k < 2; ++k)
+      if (valid(k)) request_cells<NT, T, NL>(A, cbuf_of(k), hidx_of(k), read_hdr(ring[k]));
+    request_crefs<NT>(A, crb, iab, read_hdr(ring[0]));
+    cp_async_commit();
+    load_slots<NT>(A, read_hdr(ring[0]), sl);
+    cp_async_wait_all();
+    __syncthreads();
+    edges(cbuf_of(0), erb, ring[0]);
+    if (valid(1)) load_slots<NT>(A, read_hdr(ring[1]), sl);
+    __syncthreads();
+    for (int it = 0;; ++it) {
+      const int t = t0 + it * G;
+      const bool more = valid(it + 1);
+      // staging ahead: header k + 4, halo indices k + 3, cells k + 2, cell
+      // references k + 1
+      if (valid(it + 4)) request_hdr(A, ring[(it + 4) & 7], t + 4 * G);
+      if (valid(it + 3)) request_hidx<NT>(A, hidx_of(it + 3), read_hdr(ring[(it + 3) & 7]));
+      if (valid(it + 2))
+        request_cells<NT, T, NL>(A, cbuf_of(it + 2), hidx_of(it + 2), read_hdr(ring[(it + 2) & 7]));
+      if (more)
+        request_crefs<NT>(A, crb + ((it + 1) & 1) * kTileCells, iab + ((it + 1) & 1) * kTileCells,
+                          read_hdr(ring[(it + 1) & 7]));
+      cp_async_commit();
+      // edges of the next tile
+      if (more) {
+        edges(cbuf_of(it + 1), erb + ((it + 1) & 1) * NE, ring[(it + 1) & 7]);
+        if (valid(it + 2)) load_slots<NT>(A, read_hdr(ring[(it + 2) & 7]), sl);
+      }
+      // cells of this tile
+      {
+        const int32_t* h = ring[it & 7];
+        const int c0 = h[0], nct = h[1] - h[0];
+        const T* er = erb + (it & 1) * NE;
+        const uint2* cr = crb + (it & 1) * kTileCells;
+        const T* ia = iab + (it & 1) * kTileCells;
+        for (int i = tid; i < nct; i += NT)
+          m = nanmax2(m, cell_residual<T, NL>(A, er, (int64_t)c0 + i, cr[i], ia[i]));
+      }
+      cp_async_wait_all();
+      __syncthreads();  // staged data landed; next slot results complete
+      if (!more) break;
+    }
   }
   pdl_trigger();
   if (NL == 2 && !__syncthreads_and(ok) && tid == 0) atomicOr(A.err, kErrHyperbolic);
@@ -645,11 +746,11 @@ template <typename T, int NL, bool EFIX, bool PAIR>
 cudaError_t pipe_prepare(int64_t ntiles, int* grid) {
   cudaError_t e = cudaFuncSetAttribute(mesh_tile_kernel<T, NL, EFIX, PAIR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pipe_smem<T, NL>());
+                                       (int)tile_smem<T, NL>());
   if (e != cudaSuccess) return e;
   int bpsm = 0, dev = 0, sms = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &bpsm, mesh_tile_kernel<T, NL, EFIX, PAIR>, pipe_threads<T, NL, EFIX>(), pipe_smem<T, NL>());
+      &bpsm, mesh_tile_kernel<T, NL, EFIX, PAIR>, pipe_threads<T, NL, EFIX>(), tile_smem<T, NL>());
   if (e != cudaSuccess) return e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -681,7 +782,7 @@ namespace {
 template <typename T, int NL, bool EFIX, bool PAIR>
 cudaError_t launch_pipe(const MeshStepArgs<T>& f, cudaStream_t st) {
   return launch_pdl(mesh_tile_kernel<T, NL, EFIX, PAIR>, (unsigned)f.grid,
-                    pipe_threads<T, NL, EFIX>(), pipe_smem<T, NL>(), st, f);
+                    pipe_threads<T, NL, EFIX>(), tile_smem<T, NL>(), st, f);
 }
 
 // The tile kernel of a step: two layers in fp32 two slots per thread on the

@@ -83,8 +83,8 @@ void hilbert_order(const double* xy, const int32_t* tri, int64_t nc, std::vector
 // Cuts the internal order into tiles and lays out their slots, halo lists
 // and per-cell slot references.  Cells are taken greedily: a cell joins the
 // current tile unless the tile would then exceed kTileSlots - 1 slots (one
-// is kept for the even padding), kTileHalo halo cells or kTileCap cells plus
-// halo cells.
+// is kept for the even padding), kTileCells cells, kTileHalo halo cells or
+// kTileCap cells plus halo cells.
 void build_tiles(MeshPrep* out) {
   const int64_t nc = out->ncells;
   const std::vector<int32_t>& ref = out->ref;
@@ -117,7 +117,7 @@ void build_tiles(MeshPrep* out) {
         }
       }
       const bool fits = ns + ds <= kTileSlots - 1 && nh + dh <= kTileHalo &&
-                        (c - c0 + 1) + nh + dh <= kTileCap;
+                        c - c0 + 1 <= kTileCells && (c - c0 + 1) + nh + dh <= kTileCap;
       if (!fits && attempt == 0 && c > c0) {  // close the tile, retry c in a new one
         out->tile_cell.push_back((int32_t)c);
         ++tile;
@@ -214,7 +214,8 @@ bool tiles_consistent(const MeshPrep& m) {
     const int64_t h0 = m.tile_halo[t], nh = m.tile_halo[t + 1] - h0;
     const int64_t s0 = m.tile_slot[t], ns = m.tile_slot[t + 1] - s0;
     const int64_t nct = c1 - c0;
-    if (nct < 1 || nh < 0 || nh > kTileHalo || nct + nh > kTileCap || (s0 & 1) || (ns & 1) || ns < 2 ||
+    if (nct < 1 || nct > kTileCells || nh < 0 || nh > kTileHalo || nct + nh > kTileCap ||
+        (s0 & 1) || (ns & 1) || ns < 2 ||
         ns > kTileSlots)
       return false;
     auto global = [&](int32_t l) -> int64_t {

@@ -165,18 +165,33 @@ __device__ __forceinline__ Side2P pack2(const Side2<float>& x, const Side2<float
   p.H = f2(x.H, y.H);
   return p;
 }
-template <>
-__device__ __forceinline__ unsigned edge_pair<float, false>(
-    const Side2<float>& ax, const Side2<float>& bx, bool wx, const Side2<float>& ay,
-    const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
+// fp32: both edges in one evaluation on the FP32x2 pipe
+template <bool EFIX>
+__device__ __forceinline__ unsigned edge_pair_f32(const Side2<float>& ax, const Side2<float>& bx,
+                                                  bool wx, const Side2<float>& ay,
+                                                  const Side2<float>& by, bool wy, float g,
+                                                  float gh, float r, float ox[NEQ],
+                                                  float oy[NEQ]) {
   float2 o[NEQ];
-  const unsigned ok = edge2p(pack2(ax, ay), pack2(bx, by), g, gh, r, wx, wy, o);
+  const unsigned ok = edge2p<EFIX>(pack2(ax, ay), pack2(bx, by), g, gh, r, wx, wy, o);
 #pragma unroll
   for (int q = 0; q < NEQ; ++q) {
     ox[q] = o[q].x;
     oy[q] = o[q].y;
   }
   return ok;
+}
+template <>
+__device__ __forceinline__ unsigned edge_pair<float, false>(
+    const Side2<float>& ax, const Side2<float>& bx, bool wx, const Side2<float>& ay,
+    const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
+  return edge_pair_f32<false>(ax, bx, wx, ay, by, wy, g, gh, r, ox, oy);
+}
+template <>
+__device__ __forceinline__ unsigned edge_pair<float, true>(
+    const Side2<float>& ax, const Side2<float>& bx, bool wx, const Side2<float>& ay,
+    const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
+  return edge_pair_f32<true>(ax, bx, wx, ay, by, wy, g, gh, r, ox, oy);
 }
 
 // what a cell takes from the x-edge on its west (it is side b) and from the
@@ -190,6 +205,14 @@ enum { B_M1, B_PS1, B_T1, B_M2, B_PS2, B_T2, B_D, NB };
 #endif
 template <typename T, bool EFIX> struct MinBlocks2 { static constexpr int v = 1; };
 template <> struct MinBlocks2<float, false> { static constexpr int v = SWE_MARCH2_MIN_BLOCKS; };
+// With the entropy fix (fp32 evaluates both edges with the packed fix form,
+// about 200 registers unbounded): three blocks at 168 registers, a few bytes
+// spilled, ran 0.234 ms per step on the 2048^2 interface dam break against
+// 0.258 ms at two blocks unspilled.
+#ifndef SWE_MARCH2_MIN_BLOCKS_EFIX
+#define SWE_MARCH2_MIN_BLOCKS_EFIX 3
+#endif
+template <> struct MinBlocks2<float, true> { static constexpr int v = SWE_MARCH2_MIN_BLOCKS_EFIX; };
 
 // FUSED: the pass also applies the previous step's update to every cell it
 // loads (W^n = W^{n-1} - (dt/dx) R^{n-1}) and writes W^n of its own cells.

@@ -246,6 +246,7 @@ __device__ __forceinline__ SlotPair load_slot_pair(const MeshStepArgs<float>& A,
                   *reinterpret_cast<const float2*>(A.slot_len + gs)};
 }
 
+template <bool EFIX>
 __device__ __forceinline__ bool tile_edge_pair(const MeshStepArgs<float>& A, const float* cw,
                                                float* er, int j, const SlotPair& sp) {
   const int2 ab = sp.ab;
@@ -260,7 +261,7 @@ __device__ __forceinline__ bool tile_edge_pair(const MeshStepArgs<float>& A, con
   if (w0) { sb.qn[0].x = -sa.qn[0].x; sb.qn[1].x = -sa.qn[1].x; }
   if (w1) { sb.qn[0].y = -sa.qn[0].y; sb.qn[1].y = -sa.qn[1].y; }
   float2 out[NEQ];
-  const bool ok = edge2p(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out) == 3u;
+  const bool ok = edge2p<EFIX>(sa, sb, A.g, 0.5f * A.g, A.r, w0, w1, out) == 3u;
   auto put = [&](int q, float2 v) { *reinterpret_cast<float2*>(er + q * kTileSlots + j) = v; };
   using Lay = MeshLayout<2>;
 #pragma unroll
@@ -434,7 +435,7 @@ template <typename T, int NL, bool EFIX, bool PAIR> struct PipeMinBlocks {
 template <> struct PipeMinBlocks<float, 2, false, true> {
   static constexpr int v = SWE_PIPE_PAIR_MIN_BLOCKS;
 };
-template <> struct PipeMinBlocks<float, 2, true, false> { static constexpr int v = 2; };
+template <> struct PipeMinBlocks<float, 2, true, true> { static constexpr int v = 2; };
 template <> struct PipeMinBlocks<float, 1, false, false> { static constexpr int v = 4; };
 template <> struct PipeMinBlocks<float, 1, true, false> { static constexpr int v = 4; };
 
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__((pipe_threads<T, NL, EFIX>()), (PipeMinBlocks<
     const int ns = h[5] - h[4];
     if constexpr (PAIR) {
       static_assert(sizeof(T) == 4, "the packed pair form is fp32");
-      if (2 * tid < ns) ok &= tile_edge_pair(A, cw, er, 2 * tid, sl.p);
+      if (2 * tid < ns) ok &= tile_edge_pair<EFIX>(A, cw, er, 2 * tid, sl.p);
     } else {
 #pragma unroll
       for (int k = 0; k < NSL; ++k) {
@@ -766,7 +767,7 @@ cudaError_t pipe_prepare(int64_t ntiles, int* grid) {
 template <typename T>
 cudaError_t mesh_prepare(int n_layers, int efix, int64_t ntiles, int* grid) {
   constexpr bool F32 = sizeof(T) == 4;
-  if (n_layers == 2 && efix) return pipe_prepare<T, 2, true, false>(ntiles, grid);
+  if (n_layers == 2 && efix) return pipe_prepare<T, 2, true, F32>(ntiles, grid);
   if (n_layers == 2) return pipe_prepare<T, 2, false, F32>(ntiles, grid);
   if (efix) return pipe_prepare<T, 1, true, false>(ntiles, grid);
   return pipe_prepare<T, 1, false, false>(ntiles, grid);
@@ -786,11 +787,11 @@ cudaError_t launch_pipe(const MeshStepArgs<T>& f, cudaStream_t st) {
 }
 
 // The tile kernel of a step: two layers in fp32 two slots per thread on the
-// FP32x2 pipe (one with the entropy fix), else one.
+// FP32x2 pipe, else one.
 template <typename T>
 cudaError_t launch_tile(const MeshStepArgs<T>& f, int n_layers, cudaStream_t st) {
   constexpr bool F32 = sizeof(T) == 4;
-  if (n_layers == 2 && f.efix) return launch_pipe<T, 2, true, false>(f, st);
+  if (n_layers == 2 && f.efix) return launch_pipe<T, 2, true, F32>(f, st);
   if (n_layers == 2) return launch_pipe<T, 2, false, F32>(f, st);
   if (f.efix) return launch_pipe<T, 1, true, false>(f, st);
   return launch_pipe<T, 1, false, false>(f, st);

@@ -320,31 +320,19 @@ struct QuarticP {
   }
 };
 
-// Flux of two edges at once; walls per component.  Returns a mask: bit 0
-// (bit 1) set when the first (second) edge's A_ij has real eigenvalues.
-__device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, float g, float gh,
-                                       float r, bool w0, bool w1, float2* out) {
-  float2 un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float2 va = mul2(a.qn[k], a.rs[k]), vb = mul2(b.qn[k], b.rs[k]);
-    un[k] = mul2(add2(va, vb), rcp2(add2(a.s[k], b.s[k])));
-    cs[k] = mul2(s2(gh), add2(a.h[k], b.h[k]));
-    const float2 iha = mul2(a.rs[k], a.rs[k]), ihb = mul2(b.rs[k], b.rs[k]);
-    qu_a[k] = mul2(mul2(a.qn[k], a.qn[k]), iha);
-    qu_b[k] = mul2(mul2(b.qn[k], b.qn[k]), ihb);
-    ut_a[k] = mul2(a.qt[k], iha);
-    ut_b[k] = mul2(b.qt[k], ihb);
-  }
-  const QuarticP q{un[0], un[1], cs[0], cs[1], mul2(mul2(s2(r), cs[0]), cs[1])};
-  const float2 c1 = sqrt2(cs[0]), c2 = sqrt2(cs[1]);
-  const float2 sc = sqrt2(add2(cs[0], cs[1]));
+// The four roots of two quartics at once, in increasing order: edge2's
+// quartic_roots (the same safe starts, per-edge early exit of the outer
+// Newton iteration, clamped inner steps) on the FP32x2 pipe.  Returns a mask:
+// bit 0 (bit 1) when the first (second) quartic's inner pair is real.
+__device__ __forceinline__ unsigned roots2p(const QuarticP& q, float2 lam[4]) {
+  const float2 c1 = sqrt2(q.c1s), c2 = sqrt2(q.c2s);
+  const float2 sc = sqrt2(add2(q.c1s, q.c2s));
   const float kr2 = 1.4142135623730951f * (1.f + 1.f / 4096), ks = 1.f + 1.f / 4096;
   // outer roots: the safe starts of edge2 (swe_roe2.cuh)
-  float2 l1 = max2(min2(fma2(s2(-kr2), c1, un[0]), fma2(s2(-kr2), c2, un[1])),
-                   fma2(s2(-ks), sc, min2(un[0], un[1])));
-  float2 l4 = min2(max2(fma2(s2(kr2), c1, un[0]), fma2(s2(kr2), c2, un[1])),
-                   fma2(s2(ks), sc, max2(un[0], un[1])));
+  float2 l1 = max2(min2(fma2(s2(-kr2), c1, q.u1), fma2(s2(-kr2), c2, q.u2)),
+                   fma2(s2(-ks), sc, min2(q.u1, q.u2)));
+  float2 l4 = min2(max2(fma2(s2(kr2), c1, q.u1), fma2(s2(kr2), c2, q.u2)),
+                   fma2(s2(ks), sc, max2(q.u1, q.u2)));
   const float2 tol = mul2(s2(Iters<float>::tol), max2(c1, c2));
   const unsigned act = __activemask();
   bool done0 = false, done1 = false;  // per edge, as in edge2
@@ -359,10 +347,10 @@ __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, flo
     if (__all_sync(act, done0 & done1)) break;
   }
   // inner pair: p / ((l - l1)(l - l4)) = l^2 + bb l + cc
-  const float2 p3 = mul2(s2(-2.f), add2(un[0], un[1]));
-  const float2 p2 = add2(add2(fma2(un[0], un[0], f2(-cs[0].x, -cs[0].y)),
-                              fma2(un[1], un[1], f2(-cs[1].x, -cs[1].y))),
-                         mul2(mul2(s2(4.f), un[0]), un[1]));
+  const float2 p3 = mul2(s2(-2.f), add2(q.u1, q.u2));
+  const float2 p2 = add2(add2(fma2(q.u1, q.u1, f2(-q.c1s.x, -q.c1s.y)),
+                              fma2(q.u2, q.u2, f2(-q.c2s.x, -q.c2s.y))),
+                         mul2(mul2(s2(4.f), q.u1), q.u2));
   const float2 ss = add2(l1, l4), pp = mul2(l1, l4);
   const float2 bb = add2(p3, ss);
   const float2 cc = sub2(fma2(ss, bb, p2), pp);
@@ -378,21 +366,67 @@ __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, flo
     l2 = sub2(l2, min2(max2(q.step(l2), nlim), lim));
     l3 = sub2(l3, min2(max2(q.step(l3), nlim), lim));
   }
+  lam[0] = l1;
+  lam[1] = l2;
+  lam[2] = l3;
+  lam[3] = l4;
+  return hyper;
+}
+
+// A side's own quartic (side_quartic) for two edges at once.
+__device__ __forceinline__ QuarticP side_quartic2p(const Side2P& a, float g, float r) {
+  const float2 c1s = mul2(s2(g), a.h[0]), c2s = mul2(s2(g), a.h[1]);
+  return QuarticP{mul2(a.qn[0], mul2(a.rs[0], a.rs[0])), mul2(a.qn[1], mul2(a.rs[1], a.rs[1])),
+                  c1s, c2s, mul2(mul2(s2(r), c1s), c2s)};
+}
+
+// Flux of two edges at once; walls per component.  Returns a mask: bit 0
+// (bit 1) set when the first (second) edge's A_ij (and, with EFIX, each
+// side's own matrix) has real eigenvalues.  EFIX: the Harten-Hyman fix of
+// edge2, per component.
+template <bool EFIX = false>
+__device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, float g, float gh,
+                                           float r, bool w0, bool w1, float2* out) {
+  float2 un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float2 va = mul2(a.qn[k], a.rs[k]), vb = mul2(b.qn[k], b.rs[k]);
+    un[k] = mul2(add2(va, vb), rcp2(add2(a.s[k], b.s[k])));
+    cs[k] = mul2(s2(gh), add2(a.h[k], b.h[k]));
+    const float2 iha = mul2(a.rs[k], a.rs[k]), ihb = mul2(b.rs[k], b.rs[k]);
+    qu_a[k] = mul2(mul2(a.qn[k], a.qn[k]), iha);
+    qu_b[k] = mul2(mul2(b.qn[k], b.qn[k]), ihb);
+    ut_a[k] = mul2(a.qt[k], iha);
+    ut_b[k] = mul2(b.qt[k], ihb);
+  }
+  const QuarticP q{un[0], un[1], cs[0], cs[1], mul2(mul2(s2(r), cs[0]), cs[1])};
+  float2 lam[4];
+  unsigned hyper = roots2p(q, lam);
+  const float2 l1 = lam[0], l2 = lam[1], l3 = lam[2], l4 = lam[3];
   // fluctuation d (pressure differences written g hbar_k dh_k)
   const float2 dh1 = sub2(b.h[0], a.h[0]), dh2 = sub2(b.h[1], a.h[1]), dH = sub2(b.H, a.H);
   const float2 d1 = sub2(b.qn[0], a.qn[0]);
   const float2 d2 = fma2(cs[0], sub2(add2(dh1, dh2), dH), sub2(qu_b[0], qu_a[0]));
   const float2 d3 = sub2(b.qn[1], a.qn[1]);
   const float2 d4 = fma2(cs[1], sub2(fma2(s2(r), dh1, dh2), dH), sub2(qu_b[1], qu_a[1]));
-  // P^- d = sum_k w_k alpha_k K_k; waves 3 and 4 add exact zeros when every
-  // edge of the warp is subcritical in both families (as in edge2)
-  const float2 lam[4] = {l1, l2, l3, l4};
+  // P^- d = sum_k w_k alpha_k K_k (+ the fix's term); without the fix waves
+  // 3 and 4 add exact zeros when every edge of the warp is subcritical in
+  // both families (as in edge2)
+  // entropy fix: each side's own speeds
+  float2 la[4], lb[4];
+  if (EFIX) {
+    hyper &= roots2p(side_quartic2p(a, g, r), la);
+    hyper &= roots2p(side_quartic2p(b, g, r), lb);
+  }
   const float2 ic1s = rcp2(cs[0]);
   const float2 tu1 = mul2(s2(2.f), un[0]), tu2 = mul2(s2(2.f), un[1]);
   float2 pd0 = s2(0.f), pd1 = s2(0.f), pd2 = s2(0.f), pd3 = s2(0.f);
-  const bool sub = (l1.x < 0.f) & (l1.y < 0.f) & (l2.x < 0.f) & (l2.y < 0.f) & (l3.x > 0.f) &
-                   (l3.y > 0.f) & (l4.x > 0.f) & (l4.y > 0.f);
-  const bool two_waves = __all_sync(act, sub);
+  bool two_waves = false;
+  if (!EFIX) {
+    const bool sub = (l1.x < 0.f) & (l1.y < 0.f) & (l2.x < 0.f) & (l2.y < 0.f) & (l3.x > 0.f) &
+                     (l3.y > 0.f) & (l4.x > 0.f) & (l4.y > 0.f);
+    two_waves = __all_sync(__activemask(), sub);
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k == 2 && two_waves) break;
@@ -403,7 +437,23 @@ __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, flo
     const float2 dp = mul2(s2(2.f), fma2(e1, Q2, mul2(e2, Q1)));
     const float2 num = fma2(Q2, fma2(sub2(l, tu1), d1, d2),
                             mul2(cs[0], fma2(sub2(l, tu2), d3, d4)));
-    const float2 alpha = mul2(mul2(w, num), rcp2(dp));
+    const float2 rdp = rcp2(dp);
+    float2 alpha = mul2(mul2(w, num), rdp);
+    if (EFIX) {
+      const float2 del = max2(s2(0.f), max2(sub2(l, la[k]), sub2(lb[k], l)));
+      if ((fabsf(l.x) < del.x) | (fabsf(l.y) < del.y)) {
+        // beta_k: the left eigenvector applied to the state jump
+        const float2 nb = fma2(Q2, fma2(sub2(l, tu1), dh1, d1),
+                               mul2(cs[0], fma2(sub2(l, tu2), dh2, d3)));
+        const float2 nbr = mul2(nb, rdp);
+        if (fabsf(l.x) < del.x)
+          alpha.x += 0.5f * (fabsf(l.x) - (l.x * l.x + del.x * del.x) *
+                                              M2<float>::rcp(del.x + del.x)) * nbr.x;
+        if (fabsf(l.y) < del.y)
+          alpha.y += 0.5f * (fabsf(l.y) - (l.y * l.y + del.y * del.y) *
+                                              M2<float>::rcp(del.y + del.y)) * nbr.y;
+      }
+    }
     const float2 mu = mul2(Q1, ic1s);
     pd0 = add2(pd0, alpha);
     pd1 = fma2(alpha, l, pd1);

@@ -314,7 +314,7 @@ swe_status enqueue_step2(swe_state* s, double cfl, bool last) {
   return mark_end(s);
 }
 
-// Meshes: the gather pass of step n reduces into slot n % 3, the update of
+// Meshes: the tile pass of step n reduces into slot n % 3, the update of
 // step n reads it and zeroes slot (n + 1) % 3 (as for two layers on a grid).
 template <typename T>
 swe_status enqueue_mesh_check(swe_state* s) {

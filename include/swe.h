@@ -194,15 +194,16 @@ swe_status swe_create_grid(const swe_grid *grid, const void *H,
  * Computes on the host, in double precision, every triangle's area and every
  * edge's length and unit normal, pairs the triangles across their shared
  * edges, orders the cells (swe_mesh.reorder) and cuts that order into tiles:
- * runs of consecutive cells with at most 512 edges touching them and at most
- * 640 cells and neighbouring (halo) cells.  Then allocates the device state
- * and copies the geometry, H and W0 there.  Each step runs two kernels
- * ([P1] Algorithm 1, edge processing then volume processing): one block per
- * tile stages its cells and halo in shared memory, evaluates the Roe flux of
- * each of its edges once and sums every cell's three edges in a fixed order
- * (an edge between two tiles is evaluated by both, identically), then the
- * update.  The device keeps about (2 nf + 3) values and 4 int32 per cell, 3
- * values and 1 int32 per edge evaluation, 1 int32 per halo entry.
+ * runs of consecutive cells with at most 512 edges touching them, 512 cells,
+ * 256 neighbouring (halo) cells and 640 cells and halo cells together.  Then
+ * allocates the device state and copies the geometry, H and W0 there.  Each
+ * step runs two kernels ([P1] Algorithm 1, edge processing then volume
+ * processing): the tile kernel stages each tile's cells and halo in shared
+ * memory, evaluates the Roe flux of each of its edges once and sums every
+ * cell's three edges in a fixed order (an edge between two tiles is
+ * evaluated by both, identically), then the update.  The device keeps about
+ * (2 nf + 2) values and 4 int32 per cell, 3 values and 1 int32 per edge
+ * evaluation, 1 int32 per halo entry.
  * Errors: SWE_ERR_ARG (bad argument; an index out of range, a non-finite
  * coordinate, a clockwise or degenerate triangle, an edge traversed twice in
  * the same direction -- which includes any edge of three or more triangles;

@@ -21,8 +21,9 @@
 //
 // Two kernels per step:
 //   wd_speed_kernel  one thread per cell: sum_e L ||D_e|| over its four edges
-//                    of W^n with the rules above (its block maximum published
-//                    with one atomic: dt of this step, eq. (5));
+//                    of W^n with the rules above, each edge evaluated once per
+//                    block (its block maximum published with one atomic: dt
+//                    of this step, eq. (5));
 //   wd_tile_kernel   one block per 32 x 16 tile: the tile and a two-cell ring
 //                    of W^n into shared memory; every edge that the tile and
 //                    its one-cell ring need, once per block (mass flux m
@@ -236,18 +237,25 @@ __device__ __forceinline__ void atomic_max_wd(void* slot, double v) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) wd_speed_kernel(const WdArgs<T> A) {
+  // 32 x 8 threads, one per cell.  Each thread evaluates the east and north
+  // edges of its cell (the cell is side a) and hands side b's speed to the
+  // neighbour through shared memory; the block's first column and first row
+  // evaluate their west and south edges themselves.  Every edge is thus
+  // evaluated once inside a block (the two sides can differ: a bank is a
+  // wall for one of them only).
   __shared__ T part[8];
+  __shared__ T east_b[8][33], north_b[8][32];
   pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const int j = blockIdx.y * blockDim.y + threadIdx.y;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int i = blockIdx.x * blockDim.x + tx;
+  const int j = blockIdx.y * blockDim.y + ty;
   const int nx = A.nx, ny = A.ny;
-  T s = T(0);
-  if (i < nx && j < ny) {
-    // the cell and its four neighbours (a missing one: the cell itself,
+  const bool in = i < nx && j < ny;
+  T s = T(0), dEa = T(0), dNa = T(0), dW = T(0), dS = T(0), dEb = T(0), dNb = T(0);
+  if (in) {
+    // the cell and the neighbours it needs (a missing one: the cell itself,
     // unused behind the wall), h, q_x, q_y and H of each read once
     const int64_t o = (int64_t)(j + kPadY) * A.pitch + i + kPadX;
-    const int64_t on[4] = {i + 1 < nx ? o + 1 : o, j + 1 < ny ? o + A.pitch : o,
-                           i > 0 ? o - 1 : o, j > 0 ? o - A.pitch : o};
     auto side = [&](int64_t at, bool xdir) {
       SideW<T> c;
       c.h = A.win[0][at];
@@ -258,13 +266,25 @@ __global__ void __launch_bounds__(256) wd_speed_kernel(const WdArgs<T> A) {
       return c;
     };
     const SideW<T> cx = side(o, true), cy = side(o, false);
-    T dE, dN, dW, dS, unused;
+    T unused;
     // East, North (the cell is a), West, South (the cell is b)
-    edge_speeds(cx, side(on[0], true), false, i + 1 >= nx, A.g, A.hdry, dE, unused);
-    edge_speeds(cy, side(on[1], false), false, j + 1 >= ny, A.g, A.hdry, dN, unused);
-    edge_speeds(side(on[2], true), cx, i == 0, false, A.g, A.hdry, unused, dW);
-    edge_speeds(side(on[3], false), cy, j == 0, false, A.g, A.hdry, unused, dS);
-    s = (A.dy * dE + A.dx * dN) + (A.dy * dW + A.dx * dS);
+    edge_speeds(cx, side(i + 1 < nx ? o + 1 : o, true), false, i + 1 >= nx, A.g, A.hdry, dEa,
+                dEb);
+    edge_speeds(cy, side(j + 1 < ny ? o + A.pitch : o, false), false, j + 1 >= ny, A.g, A.hdry,
+                dNa, dNb);
+    if (tx == 0)
+      edge_speeds(side(i > 0 ? o - 1 : o, true), cx, i == 0, false, A.g, A.hdry, unused, dW);
+    if (ty == 0)
+      edge_speeds(side(j > 0 ? o - A.pitch : o, false), cy, j == 0, false, A.g, A.hdry, unused,
+                  dS);
+  }
+  east_b[ty][tx] = dEb;
+  north_b[ty][tx] = dNb;
+  __syncthreads();
+  if (in) {
+    if (tx > 0) dW = east_b[ty][tx - 1];
+    if (ty > 0) dS = north_b[ty - 1][tx];
+    s = (A.dy * dEa + A.dx * dNa) + (A.dy * dW + A.dx * dS);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = nanmax_wd(s, __shfl_xor_sync(kFullWd, s, o));

@@ -187,11 +187,50 @@ __device__ __forceinline__ unsigned edge_pair<float, false>(
     const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
   return edge_pair_f32<false>(ax, bx, wx, ay, by, wy, g, gh, r, ox, oy);
 }
-template <>
-__device__ __forceinline__ unsigned edge_pair<float, true>(
-    const Side2<float>& ax, const Side2<float>& bx, bool wx, const Side2<float>& ay,
-    const Side2<float>& by, bool wy, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
-  return edge_pair_f32<true>(ax, bx, wx, ay, by, wy, g, gh, r, ox, oy);
+// (fp32 with the entropy fix: edge_pair_shared below)
+
+// Entropy fix, fp32: the sides' own speeds (roots of side_quartic2p) are
+// the same for every edge of a cell in one frame, so each lane solves its
+// cell's quartics once per row, in the x- and the y-frame at once, and the
+// edges take them from there: the x-edge's side b from the east lane, the
+// y-edge's side a from the row below.  A wall's mirror ghost (its normal
+// discharge negated) has exactly the negated roots in reverse order, every
+// step of the root finding being symmetric under that sign change.
+struct OwnRoots {
+  float2 l[4];  // .x: the cell in the x-frame, .y: in the y-frame
+  unsigned hyper;
+};
+__device__ __forceinline__ OwnRoots own_roots(const Cell2<float>& c, float g, float r) {
+  OwnRoots o;
+  o.hyper = roots2p(side_quartic2p(pack2(side2(c, true, false), side2(c, false, false)), g, r),
+                    o.l);
+  return o;
+}
+__device__ __forceinline__ unsigned edge_pair_shared(
+    const Side2<float>& ax, const Side2<float>& bx, bool lw, bool rw, const Side2<float>& ay,
+    const Side2<float>& by, bool bw, bool tw, const OwnRoots& cur, const float below[4],
+    unsigned below_hyper, float g, float gh, float r, float ox[NEQ], float oy[NEQ]) {
+  float east[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) east[k] = __shfl_down_sync(kFull2, cur.l[k].x, 1);
+  const unsigned east_hyper = __shfl_down_sync(kFull2, cur.hyper & 1u, 1);
+  float2 la[4], lb[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    la[k] = f2(lw ? -cur.l[3 - k].x : cur.l[k].x, bw ? -below[3 - k] : below[k]);
+    lb[k] = f2(rw ? -cur.l[3 - k].x : east[k], tw ? -cur.l[3 - k].y : cur.l[k].y);
+  }
+  const unsigned hx = (cur.hyper & 1u) & (rw ? cur.hyper & 1u : east_hyper);
+  const unsigned hy = below_hyper & ((cur.hyper >> 1) & 1u);
+  float2 o[NEQ];
+  const unsigned ok = edge2p<true>(pack2(ax, ay), pack2(bx, by), g, gh, r, lw || rw, bw || tw,
+                                   o, la, lb, hx | (hy << 1));
+#pragma unroll
+  for (int q = 0; q < NEQ; ++q) {
+    ox[q] = o[q].x;
+    oy[q] = o[q].y;
+  }
+  return ok;
 }
 
 // what a cell takes from the x-edge on its west (it is side b) and from the
@@ -258,6 +297,9 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
     };
     load(o, w, R, Hn);
     Cell2<T> prev;
+    constexpr bool SHARED = EFIX && sizeof(T) == 4;  // fp32 fix: own roots shared
+    float below[4] = {0.f, 0.f, 0.f, 0.f};           // y-frame roots of row r - 1
+    unsigned below_hyper = 1u;
     T xr[6], xd = T(0), yb[NB];  // row r - 1: x-part of its residual, its south edge
 #pragma unroll
     for (int f = 0; f < 6; ++f) xr[f] = T(0);
@@ -288,6 +330,8 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
       const int64_t on = row_of(rr + 1);
       if (rr < y1) load(on, w, R, Hn);
       derive(cur);
+      OwnRoots own;
+      if constexpr (SHARED) own = own_roots(cur, g, r);
       if (rr >= y0) {
         // ---- the x-edge east of the cell, the y-edge below it ---------------
         const Cell2<T> right = shfl_down_cell(cur);
@@ -298,8 +342,12 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
         const Side2<T> ay = side2(prev, false, bw);
         const Side2<T> by = side2(cur, false, tw);
         T ox[NEQ], oy[NEQ];
-        const unsigned ok = edge_pair<T, EFIX>(ax, bx, lw || rw, ay, by, bw || tw, g, gh, r,
-                                               ox, oy);
+        unsigned ok;
+        if constexpr (SHARED)
+          ok = edge_pair_shared(ax, bx, lw, rw, ay, by, bw, tw, own, below, below_hyper, g, gh, r,
+                                ox, oy);
+        else
+          ok = edge_pair<T, EFIX>(ax, bx, lw || rw, ay, by, bw || tw, g, gh, r, ox, oy);
         const bool row_x = rr < y1;  // this row's x-edges are used
         if (row_x && need_ex && !(ok & 1u)) hyp_ok = 0u;
         if (own_x && !(ok & 2u)) hyp_ok = 0u;
@@ -345,6 +393,11 @@ __global__ void __launch_bounds__(kMarch2Warps * 32, MinBlocks2<T, EFIX>::v)
         }
       }
       prev = cur;
+      if constexpr (SHARED) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) below[k] = own.l[k].y;
+        below_hyper = (own.hyper >> 1) & 1u;
+      }
       o = on;
     }
   }

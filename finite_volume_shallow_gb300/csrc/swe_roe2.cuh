@@ -383,10 +383,15 @@ __device__ __forceinline__ QuarticP side_quartic2p(const Side2P& a, float g, flo
 // Flux of two edges at once; walls per component.  Returns a mask: bit 0
 // (bit 1) set when the first (second) edge's A_ij (and, with EFIX, each
 // side's own matrix) has real eigenvalues.  EFIX: the Harten-Hyman fix of
-// edge2, per component.
+// edge2, per component; the sides' own speeds are solved here unless the
+// caller passes them (la_in, lb_in: roots of side_quartic2p of a and b,
+// with side_hyper the mask of those quartics whose inner pair is real).
 template <bool EFIX = false>
 __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, float g, float gh,
-                                           float r, bool w0, bool w1, float2* out) {
+                                           float r, bool w0, bool w1, float2* out,
+                                           const float2* la_in = nullptr,
+                                           const float2* lb_in = nullptr,
+                                           unsigned side_hyper = 3u) {
   float2 un[2], cs[2], qu_a[2], qu_b[2], ut_a[2], ut_b[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
@@ -415,8 +420,17 @@ __device__ __forceinline__ unsigned edge2p(const Side2P& a, const Side2P& b, flo
   // entropy fix: each side's own speeds
   float2 la[4], lb[4];
   if (EFIX) {
-    hyper &= roots2p(side_quartic2p(a, g, r), la);
-    hyper &= roots2p(side_quartic2p(b, g, r), lb);
+    if (la_in) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        la[k] = la_in[k];
+        lb[k] = lb_in[k];
+      }
+      hyper &= side_hyper;
+    } else {
+      hyper &= roots2p(side_quartic2p(a, g, r), la);
+      hyper &= roots2p(side_quartic2p(b, g, r), lb);
+    }
   }
   const float2 ic1s = rcp2(cs[0]);
   const float2 tu1 = mul2(s2(2.f), un[0]), tu2 = mul2(s2(2.f), un[1]);

@@ -26,6 +26,12 @@ one CPU core each.  Run from the repository root, one record per process:
     python tests/golden/make_full_size.py pulses8192 32
     python tests/golden/make_full_size.py tri1024 32
     python tests/golden/make_full_size.py flood2048 64
+
+A third argument records a shorter run of the same workload
+(full_<name>_fp<precision>_<steps>steps.json), e.g. the two-layer mesh over
+100 steps, where the fp32 bounds are stated:
+
+    python tests/golden/make_full_size.py tri1024 32 100
 """
 import json
 import os
@@ -46,8 +52,9 @@ N_WALL = 256
 N_BLOCKS = 32
 
 
-def record_path(name, precision):
-    return os.path.join(HERE, f"full_{name}_fp{precision}.json")
+def record_path(name, precision, steps=None):
+    tail = f"_{steps}steps" if steps else ""
+    return os.path.join(HERE, f"full_{name}_fp{precision}{tail}.json")
 
 
 def _grid_sample(nx, ny, rng):
@@ -74,9 +81,10 @@ def _chunk_means(W):
     return [np.array([c.mean() for c in np.array_split(w, N_BLOCKS * N_BLOCKS)]) for w in W]
 
 
-def make(name, precision):
+def make(name, precision, steps=None):
     d = I.make_workload(name)
-    steps = d["steps"]
+    own = steps is None
+    steps = d["steps"] if own else steps
     dr = I.rounded(d, np.float32) if precision == 32 else d
     rng = np.random.default_rng(20_000 + precision)
     t0 = time.time()
@@ -122,9 +130,9 @@ def make(name, precision):
         "values": {k: [float(W[i][c]) for c in cells] for i, k in enumerate(names)},
         "block_means": {k: [float(x) for x in blocks[i]] for i, k in enumerate(names)},
     }
-    with open(record_path(name, precision), "w") as f:
+    with open(record_path(name, precision, None if own else steps), "w") as f:
         json.dump(out, f, separators=(",", ":"))
 
 
 if __name__ == "__main__":
-    make(sys.argv[1], int(sys.argv[2]))
+    make(sys.argv[1], int(sys.argv[2]), int(sys.argv[3]) if len(sys.argv) > 3 else None)

@@ -5,7 +5,8 @@ tests/golden/make_full_size.py through the fp64 CPU oracle alone):
 
     hills2048   2048 x 2048, one layer + pollutant, 1000 steps, fp64 and fp32
     pulses8192  8192 x 8192, one layer + pollutant,  200 steps, fp32
-    tri1024     2,097,152 triangles, two layers,      500 steps, fp32
+    tri1024     2,097,152 triangles, two layers,      500 steps, fp32 (and
+                a 100-step record, checked at the fp32 bounds themselves)
     flood2048   2048 x 2048, one layer + pollutant with wet/dry fronts and the
                 entropy fix,                          500 steps, fp64
 
@@ -129,6 +130,33 @@ def test_full_size_over_the_workloads_own_steps(name, precision):
         k = names.index(nm)
         s = W[k].dot(area) if mesh else W[k].sum() * area
         assert abs(s / rec["sum0"][nm] - 1.0) <= (1e-12 if precision == 64 else 1e-5), nm
+
+
+def test_mesh_fp32_within_the_bounds_after_100_steps():
+    # the same workload over 100 steps against its own oracle record
+    # (tests/golden/make_full_size.py tri1024 32 100): every field at the
+    # fp32 bounds themselves, no allowance for round-off growth
+    path = os.path.join(GOLDEN, "full_tri1024_fp32_100steps.json")
+    assert os.path.exists(path), f"missing oracle record {path}"
+    rec = json.load(open(path))
+    assert rec["steps"] == 100
+    W, dts, t = gpu_run_mesh(I.make_workload("tri1024"), 32, rec["steps"])
+    tol = TOL2[32]
+    dte = float(np.abs(dts / np.array(rec["dts"]) - 1.0).max())
+    assert dte <= tol["dt"], dte
+    assert abs(t / rec["t"] - 1.0) <= tol["dt"]
+    cells = np.array(rec["cells"])
+    errs = {}
+    for k, nm in enumerate(rec["fields"]):
+        errs[nm] = float(np.abs(W[k][cells] - np.array(rec["values"][nm])).max()
+                         / rec["scale"][nm])
+        berr = float(np.abs(_block_means_chunks(W[k]) - np.array(rec["block_means"][nm])).max()
+                     / rec["scale"][nm])
+        assert berr <= tol[nm], (nm, berr)
+    print(f"\nFULLSIZE tri1024 fp32 steps=100 dt_rel={dte:.3e} "
+          f"cells={ {k: f'{v:.2e}' for k, v in errs.items()} }")
+    for nm, e in errs.items():
+        assert e <= tol[nm], (nm, errs)
 
 
 def test_mesh_full_size_in_fp64_from_the_records_inputs():

@@ -42,8 +42,8 @@
  *  - A handle is not thread-safe; it may be used from any one thread at a
  *    time.  All device work of a handle is ordered on swe_params.stream.
  *  - Device-detected errors (SWE_ERR_DEPTH, SWE_ERR_NONFINITE,
- *    SWE_ERR_TIMEOUT) are sticky: every later swe_step / swe_run returns them
- *    until swe_set_state installs a new state.  The handle stays valid and
+ *    SWE_ERR_HYPERBOLIC, SWE_ERR_TIMEOUT) are sticky: every later swe_step /
+ *    swe_run returns them until swe_set_state installs a new state.  The handle stays valid and
  *    destroyable after any error.
  */
 #ifndef SWE_H

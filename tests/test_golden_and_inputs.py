@@ -66,3 +66,29 @@ def test_dam128_shape():
     assert h[64, 64] == 2.0 and h[0, 0] == 1.0
     assert np.array_equal(h, h.T) and np.array_equal(h, h[::-1, ::-1])
     assert d["steps"] == 100 and d["precision"] == 64
+
+
+def test_full_size_records_are_consistent():
+    # the full-size records come from one deterministic oracle: each names
+    # its workload's own step count (or a shorter run), holds one dt per
+    # step and a value per sampled cell and field; the 100-step record of
+    # the mesh repeats the first 100 dt of the 500-step one bit for bit and
+    # samples the same cells
+    golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    recs = {}
+    for f in sorted(os.listdir(golden)):
+        if f.startswith("full_") and f.endswith(".json"):
+            r = json.load(open(os.path.join(golden, f)))
+            recs[f] = r
+            assert len(r["dts"]) == r["steps"], f
+            assert all(d > 0 for d in r["dts"]), f
+            assert abs(sum(r["dts"]) - r["t"]) <= 1e-12 * r["t"], f
+            for nm in r["fields"]:
+                assert len(r["values"][nm]) == len(r["cells"]), (f, nm)
+                assert len(r["block_means"][nm]) == 1024, (f, nm)
+            if "steps.json" not in f:
+                assert r["steps"] == I.WORKLOADS[r["workload"]]["steps"], f
+    long, short = recs["full_tri1024_fp32.json"], recs["full_tri1024_fp32_100steps.json"]
+    assert short["steps"] == 100
+    assert short["dts"] == long["dts"][:100]
+    assert short["cells"] == long["cells"]
